@@ -1,0 +1,357 @@
+"""Benchmark of the chunkwise Gated DeltaNet forward on one GB300 (or N replicas).
+
+One step = one gdn_chunk_fwd over the whole workload (every step of the hot
+path: gate cumsum, decayed Gram, triangular solve, WY factors, the serial state
+pass and the outputs), inputs resident in HBM.  L2 is flushed (a 512 MiB write)
+between timed steps; each step is timed with CUDA events on the launching
+stream.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this path) on the host cores, each step a bounded sample of the workload.
+Under torchrun (N > 1) every rank runs its own replica of the workload (no
+collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "gated-DeltaNet chunkwise fwd tokens/s and % of roofline, 1×GB300"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+def algorithmic(inp: dict) -> dict:
+    """Algorithmic bytes and FLOPs of one forward.
+
+    Bytes: q, k, v read and out written once in the qkv dtype, log_alpha and
+    beta read once (fp32), S0 read and S_final written once (fp32 dv x dk per
+    (sequence, head)).  FLOPs: the dense chunk tiles per token and head,
+    2C(3dk + 2dv) + 6 dk dv (Gram K K^T and Q K^T, W~ and U, delta, Q S^T,
+    P delta and the state update)."""
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    th = inp["B"] * inp["T"] * inp["H"]
+    dk, dv, C = inp["dk"], inp["dv"], inp["C"]
+    units = inp["N"] * inp["H"]
+    by = th * ((2 * dk + dv) * esz + dv * esz + 8)
+    if inp["S0"] is not None:
+        by += units * dv * dk * 4
+    by += units * dv * dk * 4  # S_final
+    fl = th * (2 * C * (3 * dk + 2 * dv) + 6 * dk * dv)
+    return dict(bytes=by, flops=fl, tok_heads=th)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_time(inp: dict, budget_s: float = 20.0):
+    """Time the fp64 oracle on the host cores over a bounded sample of
+    (sequence, head) units of the workload.  Returns (tokens/s, cores, sample)."""
+    from oracle import native
+    spans = native.spans(inp["B"], inp["T"], inp["cu_seqlens"])
+    H = inp["H"]
+    units_all = [(s, h) for s in range(len(spans)) for h in range(H)]
+    cores = native.max_threads()
+    # probe one unit to size the sample
+    probe = [units_all[0]]
+    t0 = time.perf_counter()
+    native.gdn_units_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], inp["S0"],
+                       inp["cu_seqlens"], probe, n_threads=1)
+    per_tok_thread = (time.perf_counter() - t0) / max(1, spans[0][1])
+    total_tok_heads = sum(l for _, l in spans) * H
+    est = per_tok_thread * total_tok_heads / max(1, cores)
+    if est <= budget_s:
+        units = units_all
+    else:
+        frac = budget_s / est
+        step = max(1, int(round(1 / frac)))
+        units = units_all[::step]
+    t0 = time.perf_counter()
+    native.gdn_units_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], inp["S0"],
+                       inp["cu_seqlens"], units, n_threads=cores)
+    dt = time.perf_counter() - t0
+    tok_heads = sum(spans[s][1] for s, _ in units)
+    tokens_per_s = tok_heads / H / dt  # tokens of all heads, per second
+    sample = (f"{len(units)} of {len(units_all)} (sequence, head) units of the workload "
+              f"({tok_heads} token-heads), fp64 per-token recurrence, OpenMP over units")
+    return tokens_per_s, cores, sample, dt
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(w)
+    for _ in range(args.warmup if args.warmup > 0 else 0):
+        pass  # the oracle has no state to warm; warm-up steps are not timed
+    vals, times = [], []
+    cores = sample = None
+    for _ in range(args.steps):
+        v, cores, sample, dt = cpu_oracle_time(inp, budget_s=args.ref_budget)
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * n_tokens_of(inp) / value, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "B": inp["B"], "H": inp["H"], "T": inp["T"],
+                       "dk": w.dk, "dv": w.dv, "C": w.C},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def n_tokens_of(inp):
+    return inp["B"] * inp["T"]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--ref-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import chunkwise_gated_deltanet_gb300 as gdn
+    gdn.load_library()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workloads.make_inputs(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    B, T, H, dk, dv, C, N = inp["B"], inp["T"], inp["H"], w.dk, w.dv, w.C, inp["N"]
+    out = torch.empty((B, T, H, dv), dtype=d["v"].dtype, device=dev)
+    Sf = torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], out, Sf,
+                          C, d["cu_seqlens"], stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    gdn.gdn_check_status(stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    gdn.gdn_check_status(stream)
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(per) / len(per)
+    ms = max_over_ranks(ms, world, dev)
+    alg = algorithmic(dict(inp, C=C))
+    tokens = B * T * world
+    value = tokens / (ms * 1e-3)
+    peaks = load_peaks()
+    sec = ms * 1e-3
+    achieved_gbs = alg["bytes"] / sec / 1e9
+    achieved_tf = alg["flops"] / sec / 1e12
+    path = gdn.gdn_select_path(dk, dv, C, d["v"].dtype)
+    launches = gdn.gdn_launches_per_call(dk, dv, C, d["v"].dtype)
+
+    # ---- end to end through the public call with pinned host buffers ----
+    host_in = {k: (inp[k].pin_memory() if inp[k] is not None else None)
+               for k in ("q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens")}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values() if t is not None)
+    d2h = out_h.numel() * out_h.element_size() + Sf_h.numel() * Sf_h.element_size()
+
+    def e2e_step():
+        for key, t in host_in.items():
+            if t is not None:
+                d[key].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        Sf_h.copy_(Sf, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    gdn.gdn_check_status(stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = cpu_oracle_time(inp)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if path == gdn.GDN_PATH_TCGEN05 else "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "T": T, "dk": dk, "dv": dv, "C": C,
+                       "seqs": N, "qkv_dtype": w.dtype,
+                       "path": {1: "simt", 2: "tcgen05"}.get(path, "none"),
+                       "l2": "flushed between timed steps (512 MiB write)",
+                       "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": peaks["source"],
+                         "algorithmic_bytes": alg["bytes"],
+                         "tensor_tflops": achieved_tf,
+                         "tensor_frac": achieved_tf / peaks["bf16_tflops"]},
+            "clocks": clk.summary(),
+            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches * args.steps,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,119 @@
+// C ABI of libgdn: argument checks, kernel selection, error reporting.
+// The operation and the meaning of every argument are documented in include/gdn.h.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+bool head_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool chunk_ok(int c) { return c == 16 || c == 32 || c == 64; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* gdn_last_error(void) { return g_err; }
+
+int gdn_select_path(int dk, int dv, int C, int qkv_dtype) {
+  if (!head_ok(dk) || !head_ok(dv) || !chunk_ok(C)) return GDN_PATH_NONE;
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16) return GDN_PATH_NONE;
+  if (gdn::tc_supported(dk, dv, C, qkv_dtype == GDN_BF16)) return GDN_PATH_TCGEN05;
+  return GDN_PATH_SIMT;
+}
+
+int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype) {
+  gdn::FwdArgs a{};
+  a.dk = dk; a.dv = dv; a.C = C; a.bf16 = qkv_dtype == GDN_BF16;
+  switch (gdn_select_path(dk, dv, C, qkv_dtype)) {
+    case GDN_PATH_TCGEN05: return gdn::tc_launches(a);
+    case GDN_PATH_SIMT: return gdn::simt_launches(a);
+    default: return 0;
+  }
+}
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha,
+                  const float* beta, const float* S0, void* out, float* S_final, int B, int H,
+                  int T, int dk, int dv, int C, const int32_t* cu_seqlens, int N_seqs,
+                  int qkv_dtype, void* stream) {
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
+    return fail(GDN_EDTYPE, "gdn_chunk_fwd: qkv_dtype %d is neither GDN_F32 nor GDN_BF16",
+                qkv_dtype);
+  if (T > 0 && (!q || !k || !v || !log_alpha || !beta || !out))
+    return fail(GDN_EINVAL, "gdn_chunk_fwd: q, k, v, log_alpha, beta and out must be non-NULL");
+  if (B <= 0 || H <= 0 || T < 0)
+    return fail(GDN_EINVAL, "gdn_chunk_fwd: need B > 0, H > 0, T >= 0 (got B=%d H=%d T=%d)", B,
+                H, T);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(GDN_EINVAL, "gdn_chunk_fwd: dk and dv must be 16, 32, 64 or 128 (got %d, %d)",
+                dk, dv);
+  if (!chunk_ok(C))
+    return fail(GDN_EINVAL, "gdn_chunk_fwd: C must be 16, 32 or 64 (got %d)", C);
+  int N = B;
+  if (cu_seqlens) {
+    if (B != 1) return fail(GDN_EINVAL, "gdn_chunk_fwd: packed sequences need B == 1 (got %d)", B);
+    if (N_seqs <= 0)
+      return fail(GDN_EINVAL, "gdn_chunk_fwd: N_seqs must be > 0 with cu_seqlens (got %d)",
+                  N_seqs);
+    N = N_seqs;
+  }
+  const void* ptrs[] = {q, k, v, log_alpha, beta, S0, out, S_final, cu_seqlens};
+  const char* names[] = {"q", "k", "v", "log_alpha", "beta", "S0", "out", "S_final",
+                         "cu_seqlens"};
+  for (int i = 0; i < 9; ++i)
+    if (ptrs[i] && !aligned16(ptrs[i]))
+      return fail(GDN_EINVAL, "gdn_chunk_fwd: %s is not 16-byte aligned", names[i]);
+  const long long rows = (long long)B * T;
+  if (rows * H * (dk > dv ? dk : dv) > (1LL << 40))
+    return fail(GDN_EINVAL, "gdn_chunk_fwd: problem too large");
+
+  gdn::FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
+  a.out = out; a.S_final = S_final; a.cu_seqlens = cu_seqlens;
+  a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.C = C; a.N = N;
+  a.bf16 = qkv_dtype == GDN_BF16;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  const int path = gdn_select_path(dk, dv, C, qkv_dtype);
+  if (path == GDN_PATH_TCGEN05)
+    e = gdn::launch_tc(a, s);
+  else
+    e = gdn::launch_simt(a, s);
+  if (e != cudaSuccess)
+    return fail(GDN_ELAUNCH, "gdn_chunk_fwd: launch failed: %s", cudaGetErrorString(e));
+  return GDN_OK;
+}
+
+int gdn_check_status(void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess)
+    return fail(GDN_ECUDA, "gdn_check_status: stream failed: %s", cudaGetErrorString(e));
+  int code = gdn::tc_read_and_clear_status(s, &e);
+  if (e != cudaSuccess)
+    return fail(GDN_ECUDA, "gdn_check_status: reading the status word failed: %s",
+                cudaGetErrorString(e));
+  if (code != 0)
+    return fail(GDN_ETIMEOUT,
+                "gdn_check_status: a tcgen05 kernel gave up a bounded wait (code 0x%x)", code);
+  return GDN_OK;
+}
+
+}  // extern "C"

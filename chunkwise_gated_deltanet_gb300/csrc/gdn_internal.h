@@ -1,0 +1,38 @@
+// Internal declarations shared by the host-side translation units of libgdn.
+// Not part of the public ABI (that is include/gdn.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Everything a forward launch needs, already validated by the API layer.
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_alpha;
+  const float* beta;
+  const float* S0;        // may be null (zeros)
+  void* out;
+  float* S_final;         // may be null (not written)
+  const int32_t* cu_seqlens;  // may be null (fixed-length sequences)
+  int B, H, T, dk, dv, C;
+  int N;                  // number of sequences (B, or N_seqs when packed)
+  int bf16;               // 1: q/k/v/out are bf16, 0: fp32
+};
+
+// CUDA-core kernel: any supported shape, fp32 arithmetic.  Returns a cudaError_t.
+cudaError_t launch_simt(const FwdArgs& a, cudaStream_t stream);
+int simt_launches(const FwdArgs& a);
+
+// tcgen05 kernel: bf16, dk = dv = 128, C = 64.
+bool tc_supported(int dk, int dv, int C, int bf16);
+cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream);
+int tc_launches(const FwdArgs& a);
+// Reads and clears the tcgen05 kernel's device status word (synchronous copy).
+// Returns 0 if clear, else the code a bounded wait recorded.
+int tc_read_and_clear_status(cudaStream_t stream, cudaError_t* err);
+
+}  // namespace gdn

@@ -1,0 +1,278 @@
+// CUDA-core (SIMT) chunkwise Gated DeltaNet forward, fp32 arithmetic.
+//
+// Serves every supported shape and both input dtypes; it is the path for fp32
+// inputs, where tensor-core rounding would miss a 1e-4 relative bound.
+//
+// One CTA owns one (sequence, head, dv-tile) and walks the sequence's chunks in
+// order (Nyysyyan, "Chunk Computation": chunks are serial, tokens inside a chunk
+// parallel).  Per chunk of C tokens (rows are tokens, S is dv x dk):
+//
+//   g     = inclusive cumsum of log alpha inside the chunk
+//   A     = strictly-lower( beta_i (k_i . k_j) e^{g_i - g_j} )
+//   [W~|U] = (I + A)^{-1} [diag(beta e^g) K | diag(beta) V]      forward substitution
+//   delta = U - W~ S^T                                   prediction error vs chunk-start S
+//   o     = e^{g_i} (S q_i) + sum_{j<=i} e^{g_i-g_j} (q_i . k_j) delta_j
+//   S     = e^{g_last} S + sum_j e^{g_last-g_j} delta_j k_j^T
+//
+// The solve is the WY representation with the decay folded in (myhz0606,
+// "DeltaNet的Chunkwise Form推导", section 4.5: W and U depend only on the
+// chunk's own k, v, beta; Nyysyyan, "Gated-DeltaNet": the U recursion with
+// gamma_i / gamma_s factors; W~ is gamma_i w_i).  Only in-chunk differences
+// g_i - g_j with i >= j are exponentiated, so no factor exceeds 1 when
+// log alpha <= 0.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+struct SimtLayout {
+  int dk, dvt, C;
+  int ldk, ldv, ldc;  // padded leading dimensions (odd => conflict-free column walks)
+  int oK, oQ, oW, oV, oD, oA, oP, oS, oG, oB, oEG, oED;
+  int floats;
+  __host__ __device__ SimtLayout(int dk_, int dvt_, int C_) : dk(dk_), dvt(dvt_), C(C_) {
+    ldk = dk + 1;
+    ldv = dvt + 1;
+    ldc = C + 1;
+    int o = 0;
+    oK = o; o += C * ldk;
+    oQ = o; o += C * ldk;
+    oW = o; o += C * ldk;
+    oV = o; o += C * ldv;
+    oD = o; o += C * ldv;
+    oA = o; o += C * ldc;
+    oP = o; o += C * ldc;
+    oS = o; o += dvt * ldk;
+    oG = o; o += C;
+    oB = o; o += C;
+    oEG = o; o += C;   // e^{g_i}
+    oED = o; o += C;   // e^{g_last - g_i}
+    floats = o;
+  }
+};
+
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads)
+gdn_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
+                const float* __restrict__ log_alpha, const float* __restrict__ beta,
+                const float* __restrict__ S0, TIn* __restrict__ out, float* __restrict__ S_final,
+                const int32_t* __restrict__ cu_seqlens, int H, int T, int dk, int dv, int dvt,
+                int C) {
+  extern __shared__ float smem[];
+  const SimtLayout L(dk, dvt, C);
+  float* Ks = smem + L.oK;
+  float* Qs = smem + L.oQ;
+  float* Ws = smem + L.oW;
+  float* Vs = smem + L.oV;   // beta V, then U in place
+  float* Ds = smem + L.oD;   // delta
+  float* As = smem + L.oA;
+  float* Ps = smem + L.oP;
+  float* Ss = smem + L.oS;
+  float* gs = smem + L.oG;
+  float* bs = smem + L.oB;
+  float* egs = smem + L.oEG;
+  float* eds = smem + L.oED;
+
+  const int n_dvt = dv / dvt;
+  const int tile = blockIdx.x % n_dvt;
+  const int h = (blockIdx.x / n_dvt) % H;
+  const int n = blockIdx.x / (n_dvt * H);
+  const int tid = threadIdx.x;
+
+  long long row0, len;
+  if (cu_seqlens) {
+    int a = cu_seqlens[n], b = cu_seqlens[n + 1];
+    a = min(max(a, 0), T);
+    b = min(max(b, a), T);
+    row0 = a;
+    len = b - a;
+  } else {
+    row0 = (long long)n * T;
+    len = T;
+  }
+  const int j0 = tile * dvt;  // first value column of this tile
+
+  // S tile: rows j0..j0+dvt of the dv x dk state.
+  const size_t sbase = ((size_t)n * H + h) * dv * dk + (size_t)j0 * dk;
+  for (int idx = tid; idx < dvt * dk; idx += kThreads) {
+    const int j = idx / dk, d = idx % dk;
+    Ss[j * L.ldk + d] = S0 ? S0[sbase + (size_t)j * dk + d] : 0.f;
+  }
+
+  for (long long c0 = 0; c0 < len; c0 += C) {
+    const int lc = (int)min((long long)C, len - c0);
+    __syncthreads();  // previous chunk is done with every buffer
+    // ---- stage the chunk; rows past the sequence end are zero with beta = 0 ----
+    for (int idx = tid; idx < C * dk; idx += kThreads) {
+      const int r = idx / dk, d = idx % dk;
+      float kv = 0.f, qv = 0.f;
+      if (r < lc) {
+        const size_t off = ((size_t)(row0 + c0 + r) * H + h) * dk + d;
+        kv = to_f32(k[off]);
+        qv = to_f32(q[off]);
+      }
+      Ks[r * L.ldk + d] = kv;
+      Qs[r * L.ldk + d] = qv;
+    }
+    for (int idx = tid; idx < C * dvt; idx += kThreads) {
+      const int r = idx / dvt, j = idx % dvt;
+      float vv = 0.f;
+      if (r < lc) vv = to_f32(v[((size_t)(row0 + c0 + r) * H + h) * dv + j0 + j]);
+      Vs[r * L.ldv + j] = vv;
+    }
+    if (tid < C) {
+      const bool ok = tid < lc;
+      const size_t gi = (size_t)(row0 + c0 + tid) * H + h;
+      gs[tid] = ok ? log_alpha[gi] : 0.f;
+      bs[tid] = ok ? beta[gi] : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {  // inclusive cumsum of log alpha inside the chunk
+      float acc = 0.f;
+      for (int r = 0; r < C; ++r) { acc += gs[r]; gs[r] = acc; }
+    }
+    __syncthreads();
+    if (tid < C) {
+      egs[tid] = __expf(gs[tid]);
+      eds[tid] = __expf(gs[C - 1] - gs[tid]);
+    }
+    // ---- A (strictly lower) and P (lower incl. diagonal) ----
+    for (int idx = tid; idx < C * C; idx += kThreads) {
+      const int i = idx / C, j = idx % C;
+      float a = 0.f, p = 0.f;
+      if (j <= i) {
+        float kk = 0.f, qk = 0.f;
+        for (int d = 0; d < dk; ++d) {
+          const float kj = Ks[j * L.ldk + d];
+          kk = fmaf(Ks[i * L.ldk + d], kj, kk);
+          qk = fmaf(Qs[i * L.ldk + d], kj, qk);
+        }
+        const float dec = __expf(gs[i] - gs[j]);
+        if (j < i) a = bs[i] * kk * dec;
+        p = qk * dec;
+      }
+      As[i * L.ldc + j] = a;
+      Ps[i * L.ldc + j] = p;
+    }
+    __syncthreads();
+    // ---- right-hand sides: diag(beta e^g) K and diag(beta) V ----
+    for (int idx = tid; idx < C * dk; idx += kThreads) {
+      const int r = idx / dk, d = idx % dk;
+      Ws[r * L.ldk + d] = bs[r] * egs[r] * Ks[r * L.ldk + d];
+    }
+    for (int idx = tid; idx < C * dvt; idx += kThreads) {
+      const int r = idx / dvt, j = idx % dvt;
+      Vs[r * L.ldv + j] *= bs[r];
+    }
+    __syncthreads();
+    // ---- (I + A) X = RHS by forward substitution, one column per thread ----
+    for (int col = tid; col < dk + dvt; col += kThreads) {
+      float* X = col < dk ? (Ws + col) : (Vs + (col - dk));
+      const int ld = col < dk ? L.ldk : L.ldv;
+      for (int i = 1; i < lc; ++i) {
+        float acc = X[i * ld];
+        for (int j = 0; j < i; ++j) acc = fmaf(-As[i * L.ldc + j], X[j * ld], acc);
+        X[i * ld] = acc;
+      }
+    }
+    __syncthreads();
+    // ---- delta = U - W~ S^T and the state part of the output, e^{g} Q S^T ----
+    float o_state[(64 * 32 + kThreads - 1) / kThreads];
+    {
+      int slot = 0;
+      for (int idx = tid; idx < C * dvt; idx += kThreads, ++slot) {
+        const int i = idx / dvt, j = idx % dvt;
+        float ws = 0.f, qs = 0.f;
+        for (int d = 0; d < dk; ++d) {
+          const float s = Ss[j * L.ldk + d];
+          ws = fmaf(Ws[i * L.ldk + d], s, ws);
+          qs = fmaf(Qs[i * L.ldk + d], s, qs);
+        }
+        Ds[i * L.ldv + j] = Vs[i * L.ldv + j] - ws;
+        o_state[slot] = egs[i] * qs;
+      }
+    }
+    __syncthreads();
+    // ---- outputs: add the in-chunk part P delta, write valid rows ----
+    {
+      int slot = 0;
+      for (int idx = tid; idx < C * dvt; idx += kThreads, ++slot) {
+        const int i = idx / dvt, j = idx % dvt;
+        float acc = o_state[slot];
+        for (int m = 0; m <= i; ++m) acc = fmaf(Ps[i * L.ldc + m], Ds[m * L.ldv + j], acc);
+        if (i < lc) out[((size_t)(row0 + c0 + i) * H + h) * dv + j0 + j] = from_f32<TIn>(acc);
+      }
+    }
+    // ---- state: S = e^{g_last} S + delta^T diag(e^{g_last - g}) K ----
+    {
+      const float gl = __expf(gs[C - 1]);
+      for (int idx = tid; idx < dvt * dk; idx += kThreads) {
+        const int j = idx / dk, d = idx % dk;
+        float acc = 0.f;
+        for (int i = 0; i < lc; ++i) acc = fmaf(Ds[i * L.ldv + j] * eds[i], Ks[i * L.ldk + d], acc);
+        Ss[j * L.ldk + d] = fmaf(gl, Ss[j * L.ldk + d], acc);
+      }
+    }
+  }
+  __syncthreads();
+  if (S_final) {
+    for (int idx = tid; idx < dvt * dk; idx += kThreads) {
+      const int j = idx / dk, d = idx % dk;
+      S_final[sbase + (size_t)j * dk + d] = Ss[j * L.ldk + d];
+    }
+  }
+}
+
+int pick_dvt(int dv) { return dv < 32 ? dv : 32; }
+
+}  // namespace
+
+int simt_launches(const FwdArgs&) { return 1; }
+
+cudaError_t launch_simt(const FwdArgs& a, cudaStream_t stream) {
+  const int dvt = pick_dvt(a.dv);
+  const SimtLayout L(a.dk, dvt, a.C);
+  const size_t smem = (size_t)L.floats * sizeof(float);
+  const long long blocks = (long long)a.N * a.H * (a.dv / dvt);
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaError_t e;
+  if (a.bf16) {
+    e = cudaFuncSetAttribute(gdn_simt_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gdn_simt_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, smem, stream>>>(
+        (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
+        a.log_alpha, a.beta, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.cu_seqlens, a.H, a.T,
+        a.dk, a.dv, dvt, a.C);
+  } else {
+    e = cudaFuncSetAttribute(gdn_simt_kernel<float>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gdn_simt_kernel<float><<<(unsigned)blocks, kThreads, smem, stream>>>(
+        (const float*)a.q, (const float*)a.k, (const float*)a.v, a.log_alpha, a.beta, a.S0,
+        (float*)a.out, a.S_final, a.cu_seqlens, a.H, a.T, a.dk, a.dv, dvt, a.C);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,154 @@
+"""Thin ctypes binding of ``libgdn.so`` (see include/gdn.h).
+
+Argument marshalling only: every step of the forward runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current CUDA stream.  There is
+no CPU fallback; if the library is missing or the tensors are not on a CUDA
+device the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
+GDN_F32, GDN_BF16 = 0, 1
+GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
+EXPORTS = ("gdn_chunk_fwd", "gdn_select_path", "gdn_launches_per_call", "gdn_check_status",
+           "gdn_last_error", "gdn_version")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"[gdn status {status}] {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libgdn.so (built by ``chunkwise_gated_deltanet_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libgdn.so is not built at {path}; run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, I, I, P]
+    lib.gdn_chunk_fwd.restype = I
+    for name in ("gdn_select_path", "gdn_launches_per_call"):
+        getattr(lib, name).argtypes = [I, I, I, I]
+        getattr(lib, name).restype = I
+    lib.gdn_check_status.argtypes = [P]
+    lib.gdn_check_status.restype = I
+    lib.gdn_last_error.argtypes = []
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    lib.gdn_version.restype = I
+    _lib = lib
+    return lib
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return GDN_F32
+    if dt == torch.bfloat16:
+        return GDN_BF16
+    raise TypeError(f"q/k/v must be float32 or bfloat16, got {dt}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int):
+    if status != GDN_OK:
+        raise GdnError(status, load_library().gdn_last_error().decode(errors="replace"))
+
+
+def gdn_version() -> int:
+    return load_library().gdn_version()
+
+
+def gdn_select_path(dk: int, dv: int, C: int, dtype: torch.dtype) -> int:
+    return load_library().gdn_select_path(dk, dv, C, _dtype_code(dtype))
+
+
+def gdn_launches_per_call(dk: int, dv: int, C: int, dtype: torch.dtype) -> int:
+    return load_library().gdn_launches_per_call(dk, dv, C, _dtype_code(dtype))
+
+
+def gdn_check_status(stream: Optional[torch.cuda.Stream] = None) -> None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(load_library().gdn_check_status(ctypes.c_void_p(s.cuda_stream)))
+
+
+def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, S_final, C: int,
+                  cu_seqlens: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name.
+
+    Shapes: q, k [B, T, H, dk]; v, out [B, T, H, dv]; log_alpha, beta [B, T, H]
+    fp32; S0, S_final [N, H, dv, dk] fp32 or None; cu_seqlens int32 [N+1] or None.
+    All tensors contiguous on one CUDA device.  Launches on ``stream`` (default:
+    the current torch stream) and returns without synchronising.
+    """
+    lib = load_library()
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    tensors = [q, k, v, log_alpha, beta, S0, out, S_final, cu_seqlens]
+    for t in tensors:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("gdn_chunk_fwd: every tensor must be a contiguous CUDA tensor")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    code = _dtype_code(v.dtype)
+    if q.dtype != v.dtype or k.dtype != v.dtype or out.dtype != v.dtype:
+        raise TypeError("q, k, v and out must share one dtype")
+    for name, t in (("log_alpha", log_alpha), ("beta", beta), ("S0", S0), ("S_final", S_final)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    n_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    s = stream if stream is not None else torch.cuda.current_stream(v.device)
+    _check(lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                             _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
+                             _ptr(cu_seqlens), n_seqs, code, ctypes.c_void_p(s.cuda_stream)))
+
+
+def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, C: int = 64,
+              output_final_state: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Allocate the outputs and run the forward.  Returns (out, S_final or None).
+
+    Device tensors: runs on the current stream and returns device tensors.
+    Host tensors (pinned for asynchronous copies): copies the inputs to the
+    current CUDA device, runs there, copies the results back to pinned host
+    tensors, and synchronises before returning.
+    """
+    host = not v.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
+        q, k, v, log_alpha, beta, S0, cu_seqlens = map(mv, (q, k, v, log_alpha, beta, S0, cu_seqlens))
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    out = torch.empty((B, T, H, dv), dtype=v.dtype, device=v.device)
+    Sf = torch.empty((N, H, dv, dk), dtype=torch.float32, device=v.device) if output_final_state else None
+    gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, Sf, C, cu_seqlens)
+    if host:
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        out_h.copy_(out, non_blocking=True)
+        Sf_h = None
+        if Sf is not None:
+            Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
+            Sf_h.copy_(Sf, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return out_h, Sf_h
+    return out, Sf

@@ -1,0 +1,109 @@
+/*
+ * gdn.h -- C ABI of the GB300 chunkwise Gated DeltaNet forward.
+ *
+ * The operation (qiita Nyysyyan, "Gated-DeltaNet" section, first equation block;
+ * the same layer as kkkzoz "linear-attention", "Gated DeltaNet" section):
+ *
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t                          (read after token t is written)
+ *
+ * for every (sequence, head) pair independently, with S a dv x dk fp32 matrix
+ * that starts at S0 and ends at S_final.  It is computed chunk by chunk
+ * (Nyysyyan, "Chunk Computation"): inside a chunk of C tokens every token is
+ * handled at once through the WY representation (myhz0606, "DeltaNet的Chunkwise
+ * Form推导", section 4.5; Nyysyyan, "Gated-DeltaNet", W and U matrix forms);
+ * chunks of one sequence run in order, each handing its final state to the next.
+ *
+ * All pointers except `cu_seqlens`'s host copy are DEVICE pointers owned by the
+ * caller, contiguous, 16-byte aligned.  No call allocates, frees or
+ * synchronises unless stated.  Every function returns a gdn_status; on a non-OK
+ * status `gdn_last_error()` gives a message for the calling host thread.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_EINVAL = 1,    /* bad size, NULL required pointer, misalignment: nothing launched */
+  GDN_EDTYPE = 2,    /* unknown qkv dtype code: nothing launched */
+  GDN_ELAUNCH = 3,   /* a kernel launch failed (message from the CUDA runtime) */
+  GDN_ETIMEOUT = 4,  /* a kernel gave up a bounded wait (see gdn_check_status) */
+  GDN_ECUDA = 5      /* another CUDA runtime error */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Which kernel family a call with these sizes runs (for callers and tests). */
+typedef enum {
+  GDN_PATH_NONE = 0,      /* sizes not supported */
+  GDN_PATH_SIMT = 1,      /* fp32 CUDA-core kernel: fp32 inputs, or other shapes */
+  GDN_PATH_TCGEN05 = 2    /* bf16 tcgen05 tensor-core kernel: dk = dv = 128, C = 64 */
+} gdn_path;
+
+/*
+ * gdn_chunk_fwd -- chunkwise forward of the Gated DeltaNet recurrence.
+ *
+ * q, k       [B, T, H, dk]   qkv_dtype (fp32 or bf16), token-major, heads inner
+ * v          [B, T, H, dv]   qkv_dtype
+ * log_alpha  [B, T, H]       fp32, natural log of the gate alpha_t in (0, 1], so <= 0
+ * beta       [B, T, H]       fp32, writing strength beta_t (normally in (0, 1))
+ * S0         [N, H, dv, dk]  fp32 initial state per (sequence, head), or NULL = zeros
+ * out        [B, T, H, dv]   qkv_dtype, written for every token (bf16 rounded to
+ *                            nearest even from fp32)
+ * S_final    [N, H, dv, dk]  fp32 final state per (sequence, head), or NULL = not written
+ * B, H, T    batch, heads, tokens per sequence; with cu_seqlens, B must be 1 and T is
+ *            the total packed token count
+ * dk, dv     head sizes, each one of 16, 32, 64, 128
+ * C          chunk length, one of 16, 32, 64; a sequence's last chunk may be shorter
+ * cu_seqlens int32 [N_seqs + 1] DEVICE array of packed sequence offsets
+ *            (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N_seqs] = T), or NULL for
+ *            N = B fixed-length sequences.  The state restarts at every offset.
+ * N_seqs     number of packed sequences (ignored when cu_seqlens is NULL)
+ * qkv_dtype  a gdn_dtype code
+ * stream     cudaStream_t to launch on (NULL = legacy default stream)
+ *
+ * With T == 0 the token arrays may be NULL; S_final then receives S0 (or zeros).
+ *
+ * Asynchronous: GDN_OK means every launch was queued.  Values of log_alpha > 0
+ * are not checked (exp of in-chunk gate sums could overflow).  The contents of
+ * cu_seqlens are not read on the host: offsets out of [0, T] are clamped on the
+ * device, so bad offsets give wrong results, never out-of-bounds accesses.
+ * `out` and `S_final` must not overlap the inputs.
+ */
+int gdn_chunk_fwd(const void* q, const void* k, const void* v,
+                  const float* log_alpha, const float* beta, const float* S0,
+                  void* out, float* S_final,
+                  int B, int H, int T, int dk, int dv, int C,
+                  const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
+                  void* stream);
+
+/* The path gdn_chunk_fwd takes for these sizes, GDN_PATH_NONE if unsupported. */
+int gdn_select_path(int dk, int dv, int C, int qkv_dtype);
+
+/* Kernels gdn_chunk_fwd launches per call for these sizes (0 if unsupported). */
+int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word that kernels
+ * set when a bounded wait (mbarrier, async copy) gives up.  Returns GDN_OK or
+ * GDN_ETIMEOUT (message names the wait), or GDN_ECUDA if the stream failed.
+ */
+int gdn_check_status(void* stream);
+
+/* Message for the last non-OK status returned on this host thread. */
+const char* gdn_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

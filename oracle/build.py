@@ -6,12 +6,13 @@ aarch64 hosts.  The shared object goes to ``oracle/_build/`` (not committed).
 from __future__ import annotations
 
 import os
+import platform
 import subprocess
 import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "gdn_oracle.c")
-OUT_DIR = os.path.join(HERE, "_build")
+OUT_DIR = os.path.join(HERE, "_build", platform.machine())
 LIB = os.path.join(OUT_DIR, "liboracle.so")
 
 

@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI (CPU only: no kernel is launched).
+
+The library must load, export every function include/gdn.h declares, pick the
+kernel path the header documents, and reject every invalid argument before any
+launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import chunkwise_gated_deltanet_gb300 as gdn
+from chunkwise_gated_deltanet_gb300 import build as gdn_build
+from chunkwise_gated_deltanet_gb300 import gdn as binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def lib():
+    gdn_build.build()
+    return gdn.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gdn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    assert "gdn_chunk_fwd" in names and "gdn_last_error" in names
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libgdn.so does not export {name}"
+
+
+def test_version(lib):
+    assert gdn.gdn_version() >= 10000
+
+
+@pytest.mark.parametrize("dk,dv,C,dt,path", [
+    (128, 128, 64, torch.bfloat16, None),     # tensor-core path once available
+    (128, 128, 64, torch.float32, gdn.GDN_PATH_SIMT),
+    (16, 16, 16, torch.float32, gdn.GDN_PATH_SIMT),
+    (64, 64, 64, torch.float32, gdn.GDN_PATH_SIMT),
+    (64, 128, 32, torch.bfloat16, gdn.GDN_PATH_SIMT),
+    (48, 64, 64, torch.float32, gdn.GDN_PATH_NONE),
+    (64, 64, 128, torch.float32, gdn.GDN_PATH_NONE),
+    (64, 256, 64, torch.bfloat16, gdn.GDN_PATH_NONE),
+])
+def test_select_path(lib, dk, dv, C, dt, path):
+    got = gdn.gdn_select_path(dk, dv, C, dt)
+    if path is None:
+        assert got in (gdn.GDN_PATH_SIMT, gdn.GDN_PATH_TCGEN05)
+    else:
+        assert got == path
+    assert (gdn.gdn_launches_per_call(dk, dv, C, dt) > 0) == (got != gdn.GDN_PATH_NONE)
+
+
+def _call(lib, **over):
+    """Call gdn_chunk_fwd with fake (never dereferenced) aligned pointers."""
+    a = dict(q=4096, k=8192, v=12288, la=16384, be=20480, S0=None, out=24576, Sf=None,
+             B=2, H=4, T=128, dk=64, dv=64, C=64, cu=None, N=0, dt=gdn.GDN_F32, stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_chunk_fwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["la"]), P(a["be"]), P(a["S0"]),
+                             P(a["out"]), P(a["Sf"]), a["B"], a["H"], a["T"], a["dk"], a["dv"],
+                             a["C"], P(a["cu"]), a["N"], a["dt"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("over,code,word", [
+    (dict(dt=7), binding.GDN_EDTYPE, "dtype"),
+    (dict(q=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(out=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(la=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(B=0), binding.GDN_EINVAL, "B > 0"),
+    (dict(H=-1), binding.GDN_EINVAL, "H > 0"),
+    (dict(T=-5), binding.GDN_EINVAL, "T >= 0"),
+    (dict(dk=48), binding.GDN_EINVAL, "dk and dv"),
+    (dict(dv=256), binding.GDN_EINVAL, "dk and dv"),
+    (dict(C=8), binding.GDN_EINVAL, "C must be"),
+    (dict(C=128), binding.GDN_EINVAL, "C must be"),
+    (dict(cu=28672, N=3, B=2), binding.GDN_EINVAL, "B == 1"),
+    (dict(cu=28672, N=0, B=1), binding.GDN_EINVAL, "N_seqs"),
+    (dict(k=8200), binding.GDN_EINVAL, "k is not 16-byte aligned"),
+    (dict(S0=36), binding.GDN_EINVAL, "S0 is not 16-byte aligned"),
+    (dict(cu=28676, N=2, B=1), binding.GDN_EINVAL, "cu_seqlens is not 16-byte aligned"),
+])
+def test_invalid_arguments_rejected_before_launch(lib, over, code, word):
+    assert _call(lib, **over) == code
+    msg = lib.gdn_last_error().decode()
+    assert word in msg, msg
+
+
+def test_binding_rejects_host_tensors(lib):
+    x = torch.zeros(1, 4, 1, 16)
+    g = torch.zeros(1, 4, 1)
+    with pytest.raises(ValueError):
+        gdn.gdn_chunk_fwd(x, x, x, g, g, None, x.clone(), None, C=16)
+
+
+def test_binding_has_no_cpu_path():
+    """The product code never imports the oracle and has no CPU compute."""
+    pkg = os.path.join(ROOT, "chunkwise_gated_deltanet_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert "oracle" not in src, fn
+            assert "einsum" not in src and "matmul" not in src, fn
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(ImportError):
+            binding.load_library(str(tmp_path / "nope.so"))
+    finally:
+        binding._lib = saved
