@@ -1,31 +1,46 @@
 // tcgen05 tensor-core chunkwise Gated DeltaNet forward: bf16 q/k/v/out, fp32
 // gates and state, dk = dv = 128, chunk C = 64.
 //
-// One CTA owns one (sequence, head) and its whole 128 x 128 fp32 state, and walks
-// the sequence's chunks in order (Nyysyyan, "Chunk Computation").  Every
-// contraction runs on the tensor cores with M = 128 (dk or dv as M):
+// One cluster of two CTAs owns one (sequence, head) and walks its chunks in
+// order (Nyysyyan, "Chunk Computation": chunks serial, tokens of a chunk
+// parallel).  The work of a chunk splits into the part that does not depend on
+// the running state and the part that does (myhz0606, "DeltaNet的Chunkwise
+// Form推导", section 4.5: W and U depend only on the chunk's own k, v, beta):
 //
-//   [K;Q] K^T         -> K K^T (rows 0..63) and Q K^T (rows 64..127)      MMA-A
-//   A = strictly-lower(beta_i e^{g_i-g_j} k_i.k_j), P = lower(e^{g_t-g_j} q_t.k_j)
-//   T = (I + A)^{-1}  (blocked forward substitution, fp32, shared memory)
-//   W~^T = K^T (T diag(beta e^g))^T,  U^T = V^T (T diag(beta))^T,  S Q^T    MMA-B
-//   delta^T = U^T - S W~^T           (accumulated onto U^T in TMEM)     MMA-C
-//   delta^T P^T,  dS = (delta diag(e^{g_last-g}))^T K                    MMA-D
-//   o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t,  S <- e^{g_last} S + dS
+// CTA 0, "WY" (two warpgroups on alternating chunks, one TMA producer warp):
+//   K K^T                    tcgen05, M=128 (rows 64..127 unused)
+//   A = strictly-lower(beta_i e^{g_i-g_j} k_i.k_j)          fp32 epilogue
+//   T = (I + A)^{-1}         16x16 diagonal blocks, then block rows, fp32
+//   W~^T = K^T (T diag(beta e^g))^T, U^T = V^T (T diag(beta))^T   tcgen05
+//   -W~^T (bf16) and U^T (fp32) go to CTA 1 by DSMEM bulk copies.
+// CTA 1, "state" (chain warpgroup, aux warpgroup, one TMA producer warp):
+//   chain: SW = S (-W~^T); delta^T = U^T + SW; S <- e^{g_last} S + delta~^T K
+//          (S accumulates in TMEM; delta feeds the MMAs from TMEM)
+//   aux:   Q K^T -> P = lower(e^{g_t-g_j} q_t.k_j); S Q^T; delta^T P^T;
+//          o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t -> out
 //
-// The WY factors use the decayed triangular factor (myhz0606, "DeltaNet的
-// Chunkwise Form推导", section 4.5; Nyysyyan, "Gated-DeltaNet": the U
-// recursion with gamma_i / gamma_s, and W~ = gamma_i w_i).
+// W~ uses the decayed triangular factor (W~_i = gamma_i w_i with the WY
+// recursion of Nyysyyan's "Gated-DeltaNet" section); then
+// delta = U - W~ S^T and the chunk's states and outputs follow from the unrolled
+// recurrence.
 //
-// Precision: operands are bf16 in 128-byte-swizzled shared memory and
-// accumulators fp32 in tensor memory.  T, delta, the decayed delta and P are
-// carried as two bf16 terms (hi = bf16(x), lo = bf16(x - hi)) and multiplied as
-// hi*hi + hi*lo + lo*hi (or hi + lo against an exact bf16 operand), which keeps
-// their rounding near 2^-16; the state S and W~ are single bf16 operands.  The
-// running state stays fp32 in registers.
+// Precision: operands are bf16, accumulators fp32.  T, delta, the decayed delta
+// (delta~ = delta diag(e^{g_last-g})) and P are carried as two bf16 terms
+// (hi = bf16(x), lo = bf16(x - hi)) and multiplied as hi*hi + hi*lo + lo*hi, or
+// hi + lo against an exact bf16 operand (K, V).  S and W~ are single bf16
+// operands; the running state itself stays fp32 (in TMEM).
 //
+// Synchronisation (mbarriers; "phase j" completes once per chunk j):
+//   WY:    kv_full[s]  (TMA bytes + producer arrive)   kv_empty[s] (WG after its MMAs)
+//          wg_mma[w]   (MMA commits of warpgroup w)
+//          hand_empty_w/_u (arrived by CTA 1 when it no longer needs chunk j's W~ / U)
+//   state: qk_full[s], qk_empty[s] (chain + aux), hand_full_w/_u (bulk-copy bytes),
+//          bar_c, bar_ds (chain MMA commits), bar_qk, bar_sq, bar_dp (aux MMA commits),
+//          sb_ready (bf16 S of chunk j written), delta_ready (delta of chunk j in TMEM)
+// "Empty" barriers are waited with parity ^ 1 so that their first wait passes.
 // Every wait is bounded; a wait that gives up records a code in a device status
-// word and the CTA leaves the chunk loop after its copies in flight have landed.
+// word, every role of both CTAs leaves its loop, and both CTAs still meet at the
+// final cluster barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,54 +59,77 @@ using namespace ptx;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;  // 2 warpgroups + 1 producer warp, in both CTAs
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
-// Shared memory map (bytes from a 1024-aligned base).
-constexpr int OFF_KQ = 0;          // 2 stages x 32 KB; per dk panel p: K rows (8 KB), Q rows (8 KB)
-constexpr int KQ_STAGE = 32768;
-constexpr int OFF_V = 65536;       // 16 KB: 2 dv panels of 64 token rows
-constexpr int OFF_SB = 81920;      // S bf16 [128 dv][128 dk], 2 K panels of 16 KB
-constexpr int OFF_WT = 114688;     // -W~^T bf16 [128 dk][64 tok] (MN-major B); later output staging
-constexpr int OFF_PH = 131072;     // P hi bf16 [64 t][64 j] (K-major B)
-constexpr int OFF_PL = 139264;     // P lo
-constexpr int OFF_AR = 147456;     // 64 KB arena
-//   prep phase:  A/T fp32 [64][68] | X fp32 [3][16][16] | Tw hi, Tw lo, Tu hi, Tu lo bf16 [64][64]
+// ---- CTA 0 ("WY") shared memory ----
+constexpr int WY_KV = 0;                 // 3 stages x 32 KB: K p0 | K p1 | V p0 | V p1 (8 KB each)
+constexpr int WY_STAGE = 32768;
+constexpr int WY_NST = 3;
+constexpr int WY_SCR = 98304;            // per-warpgroup scratch
+constexpr int WY_SCR_BYTES = 53248;
+//   A/T fp32 [64][68] @0 | X fp32 [3][256] @17408 | Tw hi @20480 | Tw lo @28672
+//   | Tu hi @36864 | Tu lo @45056;   epilogue B reuses it: -W~^T bf16 [128][64] @0,
+//   U^T fp32 [128][68] @16384
 constexpr int LDA = 68;
-constexpr int AR_A = 0;
-constexpr int AR_X = 64 * LDA * 4;           // 17408
-constexpr int AR_TWH = 20480;
-constexpr int AR_TWL = AR_TWH + 8192;
-constexpr int AR_TUH = AR_TWL + 8192;
-constexpr int AR_TUL = AR_TUH + 8192;        // ends at 53248
-//   state phase: delta hi, delta lo, decayed delta hi, lo, bf16 [128 dv][64 tok] (K-major A)
-constexpr int AR_DH = 0;
-constexpr int AR_DL = 16384;
-constexpr int AR_DSH = 32768;
-constexpr int AR_DSL = 49152;
-constexpr int OFF_RAW = OFF_AR + 65536;      // raw gates [2 stages][la 64 | beta 64]
-constexpr int OFF_DER = OFF_RAW + 1024;      // G, EG, ED, BG, BE, SCAN [6][64] fp32
-constexpr int OFF_BAR = OFF_DER + 1536;
-constexpr int OFF_MISC = OFF_BAR + 64;
-constexpr int SMEM_USED = OFF_MISC + 64;
+constexpr int SC_X = 17408, SC_TWH = 20480, SC_TWL = 28672, SC_TUH = 36864, SC_TUL = 45056;
+constexpr int SC_HW = 0, SC_HU = 16384;
+constexpr int WY_DER = WY_SCR + 2 * WY_SCR_BYTES;  // [3 stages][G, EG, BG, BE][64] fp32
+constexpr int WY_BAR = WY_DER + WY_NST * 4 * 256;
+constexpr int WY_MISC = WY_BAR + 128;
+constexpr int WY_USED = WY_MISC + 64;
+
+// ---- CTA 1 ("state") shared memory ----
+constexpr int ST_QK = 0;                 // 2 stages x 32 KB; per dk panel p: Q rows (8 KB), K rows (8 KB)
+constexpr int ST_STAGE = 32768;
+constexpr int ST_NST = 2;
+constexpr int ST_HW = 65536;             // -W~^T bf16 [128 dk][64 tok], MN-major B operand
+constexpr int ST_HU = 81920;             // U^T fp32 [128 dv][68]
+constexpr int ST_PH = 117760;            // P hi bf16 [64 t][64 j], K-major B operand
+constexpr int ST_PL = 125952;            // P lo
+constexpr int ST_SB = 134144;            // S bf16 [128 dv][128 dk], 2 K panels
+constexpr int ST_OST = 166912;           // output staging bf16 [64 t][128]
+constexpr int ST_DER = 183296;           // [2 stages][G, EG, ED][64] fp32
+constexpr int ST_BAR = ST_DER + ST_NST * 3 * 256;
+constexpr int ST_MISC = ST_BAR + 128;
+constexpr int ST_USED = ST_MISC + 64;
+
+constexpr int SMEM_USED = WY_USED > ST_USED ? WY_USED : ST_USED;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
-static_assert(AR_TUL + 8192 <= 65536, "arena");
+static_assert(SC_TUL + 8192 <= WY_SCR_BYTES, "WY scratch");
+static_assert(SC_HU + 128 * LDA * 4 <= WY_SCR_BYTES, "WY staging");
+static_assert(ST_HU + 128 * LDA * 4 <= ST_PH, "state handoff");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// TMEM columns (fp32 accumulators, 128 lanes each).
-constexpr uint32_t TM_KQ = 0;      // [K K^T ; Q K^T]   64 cols
-constexpr uint32_t TM_W = 64;      // W~^T               64
-constexpr uint32_t TM_U = 128;     // U^T, then delta^T  64
-constexpr uint32_t TM_SQ = 192;    // S Q^T              64
-constexpr uint32_t TM_DP = 256;    // delta^T P^T        64
-constexpr uint32_t TM_DS = 320;    // dS                 128
+// barrier slots (8 bytes each)
+enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE_W = 8, WB_HE_U = 9 };
+enum StBar {
+  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF_W = 4, SB_HF_U = 5, SB_C = 6, SB_DS = 7, SB_QKM = 8,
+  SB_SQ = 9, SB_DP = 10, SB_SBR = 11, SB_DR = 12
+};
+
+// TMEM columns.  WY: per warpgroup w at 192*w: K K^T 0, W~^T 64, U^T 128.
+constexpr uint32_t WT_KK = 0, WT_W = 64, WT_U = 128, WT_WG = 192;
+// state: S 0..127, SW 128, SQ 192, DP 256, QK 320, delta hi 384, delta lo 416,
+// delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
+constexpr uint32_t TT_S = 0, TT_SW = 128, TT_SQ = 192, TT_DP = 256, TT_QK = 320, TT_DH = 384,
+                   TT_DL = 416, TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
 
-constexpr int ST_WAIT_KQ = 1, ST_WAIT_V = 2, ST_WAIT_MMA = 4;
+constexpr int ST_WAIT = 1;
 
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float x) {  // 2^x by the PTX ex2.approx instruction
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -99,25 +137,23 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                "r"(d)
                : "memory");
 }
-// Store 8 consecutive columns (col % 8 == 0) of `row` into a 128B-swizzled bf16 tile.
+// 8 consecutive columns (col % 8 == 0) of `row` into a 128B-swizzled bf16 tile.
 __device__ __forceinline__ void st_sw128_8(uint8_t* tile, int row, int col, int rows,
                                            const float* v) {
   st_shared_v4(smem_u32(tile + sw128_offset(row, col, rows)), pack_bf16(v[0], v[1]),
                pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
 }
-// Same, as two bf16 terms: hi = bf16(v), lo = bf16(v - hi).
 __device__ __forceinline__ void st_sw128_8_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
                                                  int col, int rows, const float* v) {
   float hi[8], lo[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    hi[u] = __bfloat162float(__float2bfloat16_rn(v[u]));
+    hi[u] = bf16_round(v[u]);
     lo[u] = v[u] - hi[u];
   }
   st_sw128_8(hi_tile, row, col, rows, hi);
   st_sw128_8(lo_tile, row, col, rows, lo);
 }
-
 // K-major operand, 128B swizzle, K advanced by 16 elements per step.
 __device__ __forceinline__ uint64_t desc_k(const uint8_t* tile, int kstep, int panel_bytes) {
   return smem_desc(smem_u32(tile) + (kstep >> 2) * panel_bytes + (kstep & 3) * 32, 16, 1024);
@@ -126,262 +162,189 @@ __device__ __forceinline__ uint64_t desc_k(const uint8_t* tile, int kstep, int p
 __device__ __forceinline__ uint64_t desc_mn(const uint8_t* tile, int kstep, int panel_bytes) {
   return smem_desc(smem_u32(tile) + kstep * 2048, panel_bytes, 1024);
 }
-
-constexpr float kLog2e = 1.4426950408889634f;
-// 2^x by the PTX ex2.approx instruction (flushes subnormal results to zero).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float a, float b, float c, float d) {
   *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ log_alpha,
-              const float* __restrict__ beta, const float* __restrict__ S0,
-              __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
-              const int32_t* __restrict__ cu_seqlens, int H, int T) {
-  extern __shared__ uint8_t smem_raw[];
-  // Align to 1024 bytes by pointer arithmetic on the shared array itself, so that
-  // every access below stays a shared-memory (not generic) access.
-  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* AR = sm + OFF_AR;
-  float* Am = reinterpret_cast<float*>(AR + AR_A);   // A, then T in place
-  float* Xs = reinterpret_cast<float*>(AR + AR_X);
-  float* raw = reinterpret_cast<float*>(sm + OFF_RAW);
-  float* G = reinterpret_cast<float*>(sm + OFF_DER);
-  float* EG = G + 64;
-  float* ED = G + 128;
-  float* BG = G + 192;
-  float* BE = G + 256;
-  float* SCAN = G + 320;
-  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // [2]
-  uint64_t* bar_v = bar_kq + 2;
-  uint64_t* bar_mma = bar_kq + 3;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
-  __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_WT);  // output staging [64][128]
+// Bounded parity wait that also gives up when another role of this CTA already
+// gave up.  Returns false on timeout (recording `code`) or on abort.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         bool cluster_scope) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    if (ok) return true;
+    if (*abort_flag) return false;
+    if (it == 0) {
+      t0 = globaltimer_ns();
+    } else if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr((int*)abort_flag, ST_WAIT);
+      return false;
+    }
+  }
+}
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3;          // TMEM lane quarter this warp may access
-  const int half = warp >> 2;         // column half this warp handles
-  const int row = quad * 32 + lane;   // TMEM lane = accumulator row
-  const int h = blockIdx.x % H;
-  const int n = blockIdx.x / H;
-
+struct Unit {
   long long row0, len;
-  if (cu_seqlens) {
-    int a = cu_seqlens[n], b = cu_seqlens[n + 1];
-    a = min(max(a, 0), T);
-    b = min(max(b, a), T);
-    row0 = a;
-    len = b - a;
-  } else {
-    row0 = (long long)n * T;
-    len = T;
-  }
-  const int nc = (int)((len + kC - 1) / kC);
+  int nc, h;
+  size_t sidx;  // offset of S[n][h] in S0 / S_final
+};
 
-  if (warp == 0) tmem_alloc(tslot, TM_COLS);
-  if (tid == 0) {
-    mbar_init(&bar_kq[0], 1);
-    mbar_init(&bar_kq[1], 1);
-    mbar_init(bar_v, 1);
-    mbar_init(bar_mma, 1);
-    *s_abort = 0;
-    fence_mbarrier_init();
-    prefetch_tensormap(&tm_q);
-    prefetch_tensormap(&tm_k);
-    prefetch_tensormap(&tm_v);
+// Chunk gate values of one stage, computed by a whole warp: thread `lane` owns
+// tokens lane and lane + 32.  Returns the in-chunk cumulative gate sums in log2
+// units (g0 for token lane, g1 for token lane + 32) and their total.
+__device__ __forceinline__ void warp_gate_scan(const float* __restrict__ log_alpha,
+                                               const float* __restrict__ beta, const Unit& u,
+                                               int H, int chunk, int lane, float& g0, float& g1,
+                                               float& tot, float& b0, float& b1) {
+  const long long c0 = (long long)chunk * kC;
+  float x0 = 0.f, x1 = 0.f;
+  b0 = 0.f;
+  b1 = 0.f;
+  if (c0 + lane < u.len) {
+    const size_t gi = (size_t)(u.row0 + c0 + lane) * H + u.h;
+    x0 = __ldg(log_alpha + gi);
+    b0 = __ldg(beta + gi);
   }
-
-  // Running state: this thread holds S[row][64*half .. 64*half + 63] in fp32.
-  float S[64];
-  const size_t sidx = (((size_t)n * H + h) * kD + row) * kD + 64 * half;
-  if (S0) {
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float4 t4 = *reinterpret_cast<const float4*>(S0 + sidx + 4 * q);
-      S[4 * q] = t4.x; S[4 * q + 1] = t4.y; S[4 * q + 2] = t4.z; S[4 * q + 3] = t4.w;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 64; ++q) S[q] = 0.f;
+  if (c0 + lane + 32 < u.len) {
+    const size_t gi = (size_t)(u.row0 + c0 + lane + 32) * H + u.h;
+    x1 = __ldg(log_alpha + gi);
+    b1 = __ldg(beta + gi);
   }
 #pragma unroll
-  for (int q = 0; q < 8; ++q) st_sw128_8(sm + OFF_SB, row, 64 * half + 8 * q, 128, S + 8 * q);
-
-  // Gate values of one chunk: thread t in [0, 64) of a 64-thread group loads token t.
-  auto fetch_gates = [&](int chunk, float& la, float& be) {
-    const int t = tid & 63;
-    const long long c0 = (long long)chunk * kC;
-    la = 0.f;
-    be = 0.f;
-    if (c0 + t < len) {
-      const size_t gi = (size_t)(row0 + c0 + t) * H + h;
-      la = __ldg(log_alpha + gi);
-      be = __ldg(beta + gi);
-    }
-  };
-  auto issue_kq = [&](int chunk, int stage) {
-    const int r = (int)(row0 + (long long)chunk * kC);
-    uint8_t* base = sm + OFF_KQ + stage * KQ_STAGE;
-    mbar_arrive_expect_tx(&bar_kq[stage], 4 * 8192);
-    tma_load_3d(base, &tm_k, &bar_kq[stage], 0, h, r);
-    tma_load_3d(base + 8192, &tm_q, &bar_kq[stage], 0, h, r);
-    tma_load_3d(base + 16384, &tm_k, &bar_kq[stage], 64, h, r);
-    tma_load_3d(base + 16384 + 8192, &tm_q, &bar_kq[stage], 64, h, r);
-  };
-  auto issue_v = [&](int chunk) {
-    const int r = (int)(row0 + (long long)chunk * kC);
-    mbar_arrive_expect_tx(bar_v, 2 * 8192);
-    tma_load_3d(sm + OFF_V, &tm_v, bar_v, 0, h, r);
-    tma_load_3d(sm + OFF_V + 8192, &tm_v, bar_v, 64, h, r);
-  };
-
-  fence_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16);  // this warp's lane quarter
-
-  // Copies in flight and the mbarrier parity each will complete (for a clean abort).
-  int kq_pending[2] = {0, 0}, kq_par[2] = {0, 0};
-  int v_pending = 0, v_par = 0;
-  if (nc > 0) {
-    if (tid == 0) { issue_kq(0, 0); issue_v(0); }
-    kq_pending[0] = 1;
-    v_pending = 1;
-    if (tid < 64) {
-      float la, be;
-      fetch_gates(0, la, be);
-      raw[tid] = la;
-      raw[64 + tid] = be;
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+    const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    if (lane >= o) {
+      x0 += y0;
+      x1 += y1;
     }
   }
-  uint32_t mma_phase = 0;
-  bool aborted = false;
+  const float t0 = __shfl_sync(0xffffffffu, x0, 31);
+  const float t1 = __shfl_sync(0xffffffffu, x1, 31);
+  g0 = x0 * kLog2e;
+  g1 = (x1 + t0) * kLog2e;
+  tot = (t0 + t1) * kLog2e;
+}
 
-  // Wait for the MMA batch just committed; every thread leaves together.
-  auto wait_mma = [&]() -> bool {
-    const bool ok = mbar_wait(bar_mma, mma_phase, kWaitNs);
-    mma_phase ^= 1;
-    if (!ok) atomicOr((int*)s_abort, ST_WAIT_MMA);
-    tc_fence_after();
-    __syncthreads();
-    return *s_abort == 0;
-  };
+// ============================================================ CTA 0: WY ======
+__device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                       const float* __restrict__ log_alpha, const float* __restrict__ beta,
+                       const Unit& u, int H, volatile int* abort_flag) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + WY_BAR);
+  float* der_all = reinterpret_cast<float*>(sm + WY_DER);
 
-  for (int j = 0; j < nc; ++j) {
-    const int s = j & 1;
-    const long long c0 = (long long)j * kC;
-    const int lc = (int)min((long long)kC, len - c0);
-    uint8_t* KQ = sm + OFF_KQ + s * KQ_STAGE;
-
-    // ---- prefetch chunk j+1: K, Q by TMA; gates into registers (stored at chunk end) ----
-    float nla = 0.f, nbe = 0.f;
-    if (j + 1 < nc) {
-      if (tid == 0) issue_kq(j + 1, s ^ 1);
-      kq_pending[s ^ 1] = 1;
-      kq_par[s ^ 1] = ((j + 1) >> 1) & 1;
-      if (tid >= 64 && tid < 128) fetch_gates(j + 1, nla, nbe);
-    }
-
-    // ---- gates: in-chunk cumsum of log alpha and the derived factors ----
-    {
-      const bool ok = mbar_wait(&bar_kq[s], (j >> 1) & 1, kWaitNs);
-      if (ok) kq_pending[s] = 0;
-      if (!ok) atomicOr((int*)s_abort, ST_WAIT_KQ);
-      if (tid < 64) {
-        float x = raw[s * 128 + tid];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        SCAN[tid] = x;
+  if (warp == 8) {
+    // ---------------- producer: K and V tiles by TMA, gate factors ----------------
+    int issued = 0;
+    for (int j = 0; j < u.nc; ++j) {
+      const int s = j % WY_NST;
+      const uint32_t use = j / WY_NST;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[WB_KV_EMPTY + s], (use & 1) ^ 1, abort_flag, false)))
+        break;
+      uint8_t* st = sm + WY_KV + s * WY_STAGE;
+      const int r = (int)(u.row0 + (long long)j * kC);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[WB_KV_FULL + s], 4 * 8192);
+        tma_load_3d(st, tm_k, &bars[WB_KV_FULL + s], 0, u.h, r);
+        tma_load_3d(st + 8192, tm_k, &bars[WB_KV_FULL + s], 64, u.h, r);
+        tma_load_3d(st + 16384, tm_v, &bars[WB_KV_FULL + s], 0, u.h, r);
+        tma_load_3d(st + 24576, tm_v, &bars[WB_KV_FULL + s], 64, u.h, r);
       }
-      __syncthreads();
-      if (*s_abort) { aborted = true; break; }
-      if (tid < 64) {
-        // gate sums in log2 units, so every decay factor is one ex2
-        const float total = (SCAN[31] + SCAN[63]) * kLog2e;
-        const float g = (SCAN[tid] + (tid >= 32 ? SCAN[31] : 0.f)) * kLog2e;
-        const float b = raw[s * 128 + 64 + tid];
-        const float eg = ex2(g);
-        G[tid] = g;
-        EG[tid] = eg;
-        ED[tid] = ex2(total - g);
-        BG[tid] = b * eg;
-        BE[tid] = b;
-      }
-      __syncthreads();
+      issued = j + 1;
+      float g0, g1, tot, b0, b1;
+      warp_gate_scan(log_alpha, beta, u, H, j, lane, g0, g1, tot, b0, b1);
+      float* der = der_all + s * 256;  // G, EG, BG, BE
+      const float e0 = ex2(g0), e1 = ex2(g1);
+      der[lane] = g0;        der[lane + 32] = g1;
+      der[64 + lane] = e0;   der[64 + lane + 32] = e1;
+      der[128 + lane] = b0 * e0;  der[128 + lane + 32] = b1 * e1;
+      der[192 + lane] = b0;  der[192 + lane + 32] = b1;
+      (void)tot;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[WB_KV_FULL + s]);
     }
+    // copies still in flight must land before the CTA can leave
+    for (int j = issued - WY_NST; j < issued; ++j)
+      if (j >= 0) (void)mbar_wait(&bars[WB_KV_FULL + j % WY_NST], (j / WY_NST) & 1, 100000000ull);
+    return;
+  }
 
-    // ---- MMA-A: [K;Q] K^T ----
-    if (tid == 0) {
+  // ---------------- warpgroups: w = 0 takes even chunks, w = 1 odd chunks ----------------
+  const int w = warp >> 2;
+  const int wtid = tid & 127;
+  const int q4 = warp & 3;
+  const int row = q4 * 32 + lane;
+  const uint32_t nb = 1 + w;  // named barrier of this warpgroup
+  uint8_t* scr = sm + WY_SCR + w * WY_SCR_BYTES;
+  float* Am = reinterpret_cast<float*>(scr);
+  float* Xs = reinterpret_cast<float*>(scr + SC_X);
+  const uint32_t tw = tmem + w * WT_WG;
+  const uint32_t tq = tw + ((uint32_t)(q4 * 32) << 16);
+  uint32_t mph = 0;
+  const uint32_t rb_hf_w = map_shared(smem_u32(sm + ST_BAR + 8 * SB_HF_W), 1);
+  const uint32_t rb_hf_u = map_shared(smem_u32(sm + ST_BAR + 8 * SB_HF_U), 1);
+  const uint32_t rdst_w = map_shared(smem_u32(sm + ST_HW), 1);
+  const uint32_t rdst_u = map_shared(smem_u32(sm + ST_HU), 1);
+
+#define WY_WAIT(bar, par, cl)                                                  \
+  {                                                                            \
+    const bool ok_ = wait_bar((bar), (par), abort_flag, (cl));                 \
+    if (named_sync_or(nb, 128, !ok_ || *abort_flag != 0)) break;               \
+  }
+
+  for (int j = w; j < u.nc; j += 2) {
+    const int s = j % WY_NST;
+    uint8_t* st = sm + WY_KV + s * WY_STAGE;
+    const float* G = der_all + s * 256;
+    const float* BG = G + 128;
+    const float* BE = G + 192;
+    if (wtid == 0) bulk_wait_read_all();  // the previous staging of this warpgroup was read
+    WY_WAIT(&bars[WB_KV_FULL + s], (j / WY_NST) & 1, false);
+
+    // ---- K K^T (rows 0..63 of the M=128 accumulator) ----
+    if (wtid == 0) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TM_KQ, desc_k(KQ, kk, 16384), desc_k(KQ, kk, 16384), idesc, kk > 0);
-      mma_commit(bar_mma);
+        mma_bf16(tw + WT_KK, desc_k(st, kk, 8192), desc_k(st, kk, 8192), id, kk > 0);
+      mma_commit(&bars[WB_MMA + w]);
     }
-    if (!wait_mma()) { aborted = true; break; }
+    WY_WAIT(&bars[WB_MMA + w], mph, false);
+    mph ^= 1;
+    tc_fence_after();
 
-    // ---- epilogue A: decayed, beta-scaled, masked A (fp32) and P (bf16 hi/lo) ----
-    {
-      uint32_t r[32];
-      tmem_ld32(tq + TM_KQ + 32 * half, r);
-      float gc[32];
+    // ---- A = strictly-lower(beta_i e^{g_i - g_j} k_i.k_j), fp32 ----
+    if (q4 < 2) {
+      const int i = row;
+      const float gi = G[i], bi = BE[i];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 g4 = ld4(G + 32 * half + 4 * q);
-        gc[4 * q] = g4.x; gc[4 * q + 1] = g4.y; gc[4 * q + 2] = g4.z; gc[4 * q + 3] = g4.w;
-      }
-      tmem_wait_ld();
-      if (quad < 2) {
-        const int i = row;
-        const float gi = G[i], bi = BE[i];
-        float* arow = Am + i * LDA + 32 * half;
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[32];
+        tmem_ld32(tq + WT_KK + 32 * hh, r);
+        tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
+          const float4 g4 = ld4(G + 32 * hh + 4 * q);
+          const float gc[4] = {g4.x, g4.y, g4.z, g4.w};
           float v[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int jc = 32 * half + 4 * q + u;
-            v[u] = (jc < i) ? bi * ex2(gi - gc[4 * q + u]) * __uint_as_float(r[4 * q + u]) : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int jc = 32 * hh + 4 * q + e;
+            v[e] = (jc < i) ? bi * ex2(gi - gc[e]) * __uint_as_float(r[4 * q + e]) : 0.f;
           }
-          st4(arow + 4 * q, v[0], v[1], v[2], v[3]);
-        }
-      } else {
-        const int t = row - 64;
-        const float gt = G[t];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int jc = 32 * half + 8 * q + u;
-            v[u] = (jc <= t) ? ex2(gt - gc[8 * q + u]) * __uint_as_float(r[8 * q + u]) : 0.f;
-          }
-          st_sw128_8_split(sm + OFF_PH, sm + OFF_PL, t, 32 * half + 8 * q, 64, v);
+          st4(Am + i * LDA + 32 * hh + 4 * q, v[0], v[1], v[2], v[3]);
         }
       }
     }
-    __syncthreads();
+    named_sync(nb, 128);
 
-    // ---- T = (I + A)^{-1}, in place over A ----
-    // 16 x 16 diagonal blocks: one thread per column, then written back together.
-    if (tid < 64) {
-      const int b = tid >> 4, c = tid & 15;
+    // ---- T = (I + A)^{-1} in place: diagonal 16x16 blocks ----
+    if (wtid < 64) {
+      const int b = wtid >> 4, c = wtid & 15;
       const float* Ab = Am + (16 * b) * LDA + 16 * b;
       float x[16];
 #pragma unroll
@@ -391,19 +354,17 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int m = 0; m < r; ++m) acc = fmaf(-Ab[r * LDA + m], x[m], acc);
         x[r] = acc;
       }
-      asm volatile("bar.sync 1, 64;" ::: "memory");
+      named_sync(3 + w, 64);
       float* Tb = Am + (16 * b) * LDA + 16 * b + c;
 #pragma unroll
       for (int r = 0; r < 16; ++r) Tb[r * LDA] = x[r];
     }
-    __syncthreads();
-    // Block rows ib = 1..3: X_{ib,jb} = sum_{kb=jb}^{ib-1} A_{ib,kb} T_{kb,jb}, then
-    // T_{ib,jb} = -T_{ib,ib} X_{ib,jb}; each thread owns a 1 x 4 strip.
+    named_sync(nb, 128);
+    // ---- block rows: X = sum_k A_{ib,k} T_{k,jb}; T_{ib,jb} = -T_{ib,ib} X ----
 #pragma unroll 1
     for (int ib = 1; ib < 4; ++ib) {
-      const bool active = tid < ib * 64;
-      const int jb = tid >> 6, r = (tid >> 2) & 15, cq = tid & 3;
-      if (active) {
+      for (int e = wtid; e < ib * 64; e += 128) {
+        const int jb = e >> 6, r = (e >> 2) & 15, cq = e & 3;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         const float* arow = Am + (16 * ib + r) * LDA;
 #pragma unroll 1
@@ -422,8 +383,9 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         st4(Xs + jb * 256 + r * 16 + 4 * cq, a0, a1, a2, a3);
       }
-      __syncthreads();
-      if (active) {
+      named_sync(nb, 128);
+      for (int e = wtid; e < ib * 64; e += 128) {
+        const int jb = e >> 6, r = (e >> 2) & 15, cq = e & 3;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         const float* trow = Am + (16 * ib + r) * LDA + 16 * ib;
 #pragma unroll
@@ -438,13 +400,13 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         st4(Am + (16 * ib + r) * LDA + 16 * jb + 4 * cq, -a0, -a1, -a2, -a3);
       }
-      __syncthreads();
+      named_sync(nb, 128);
     }
 
-    // ---- T diag(beta e^g) and T diag(beta) as bf16 hi/lo B operands ----
+    // ---- T diag(beta e^g), T diag(beta) as bf16 hi/lo B operands ----
 #pragma unroll
-    for (int it0 = 0; it0 < 512; it0 += kThreads) {
-      const int it = it0 + tid;
+    for (int it0 = 0; it0 < 512; it0 += 128) {
+      const int it = it0 + wtid;
       const int i = it >> 3, jc = (it & 7) * 8;
       const float4 ta = ld4(Am + i * LDA + jc), tb = ld4(Am + i * LDA + jc + 4);
       const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
@@ -452,176 +414,396 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       const float4 be0 = ld4(BE + jc), be1 = ld4(BE + jc + 4);
       const float bgv[8] = {bg0.x, bg0.y, bg0.z, bg0.w, bg1.x, bg1.y, bg1.z, bg1.w};
       const float bev[8] = {be0.x, be0.y, be0.z, be0.w, be1.x, be1.y, be1.z, be1.w};
-      float tw[8], tu[8];
+      float twv[8], tuv[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float t = (jc + u <= i) ? tv[u] : 0.f;
-        tw[u] = t * bgv[u];
-        tu[u] = t * bev[u];
+      for (int e = 0; e < 8; ++e) {
+        const float t = (jc + e <= i) ? tv[e] : 0.f;
+        twv[e] = t * bgv[e];
+        tuv[e] = t * bev[e];
       }
-      st_sw128_8_split(AR + AR_TWH, AR + AR_TWL, i, jc, 64, tw);
-      st_sw128_8_split(AR + AR_TUH, AR + AR_TUL, i, jc, 64, tu);
+      st_sw128_8_split(scr + SC_TWH, scr + SC_TWL, i, jc, 64, twv);
+      st_sw128_8_split(scr + SC_TUH, scr + SC_TUL, i, jc, 64, tuv);
     }
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
+    named_sync(nb, 128);
 
-    // ---- MMA-B: W~^T = K^T Tw^T, U^T = V^T Tu^T (hi + lo), S Q^T ----
-    {
-      const bool ok = mbar_wait(bar_v, j & 1, kWaitNs);
-      if (ok) v_pending = 0;
-      if (!ok) atomicOr((int*)s_abort, ST_WAIT_V);
-      __syncthreads();
-      if (*s_abort) { aborted = true; break; }
-    }
-    if (tid == 0) {
+    // ---- W~^T = K^T Tw^T and U^T = V^T Tu^T (hi + lo) ----
+    if (wtid == 0) {
       tc_fence_after();
-      const uint32_t id_t = idesc_bf16(128, 64, 1, 0);
+      const uint32_t id = idesc_bf16(128, 64, 1, 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ak = desc_mn(KQ, kk, 16384);
-        const uint64_t av = desc_mn(sm + OFF_V, kk, 8192);
-        mma_bf16(tmem + TM_W, ak, desc_k(AR + AR_TWH, kk, 8192), id_t, kk > 0);
-        mma_bf16(tmem + TM_W, ak, desc_k(AR + AR_TWL, kk, 8192), id_t, 1);
-        mma_bf16(tmem + TM_U, av, desc_k(AR + AR_TUH, kk, 8192), id_t, kk > 0);
-        mma_bf16(tmem + TM_U, av, desc_k(AR + AR_TUL, kk, 8192), id_t, 1);
+        const uint64_t ak = desc_mn(st, kk, 8192);
+        const uint64_t av = desc_mn(st + 16384, kk, 8192);
+        mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWH, kk, 8192), id, kk > 0);
+        mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWL, kk, 8192), id, 1);
+        mma_bf16(tw + WT_U, av, desc_k(scr + SC_TUH, kk, 8192), id, kk > 0);
+        mma_bf16(tw + WT_U, av, desc_k(scr + SC_TUL, kk, 8192), id, 1);
       }
-      const uint32_t id_sq = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TM_SQ, desc_k(sm + OFF_SB, kk, 16384), desc_k(KQ + 8192, kk, 16384), id_sq,
-                 kk > 0);
-      mma_commit(bar_mma);
+      mma_commit(&bars[WB_MMA + w]);
     }
-    if (!wait_mma()) { aborted = true; break; }
-    if (j + 1 < nc) {
-      if (tid == 0) issue_v(j + 1);  // the V buffer is free: MMA-B has completed
-      v_pending = 1;
-      v_par = (j + 1) & 1;
-    }
+    WY_WAIT(&bars[WB_MMA + w], mph, false);
+    mph ^= 1;
+    tc_fence_after();
+    if (wtid == 0) mbar_arrive(&bars[WB_KV_EMPTY + s]);  // K, V of this stage are consumed
 
-    // ---- epilogue B: -W~^T as the bf16 MN-major B operand [dk][tok] ----
+    // ---- hand chunk j to the state CTA once its slot is free ----
+    WY_WAIT(&bars[WB_HE_W], (j & 1) ^ 1, true);
+    WY_WAIT(&bars[WB_HE_U], (j & 1) ^ 1, true);
     {
-      uint32_t r[32];
-      tmem_ld32(tq + TM_W + 32 * half, r);
-      tmem_wait_ld();
+      float* Us = reinterpret_cast<float*>(scr + SC_HU);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = -__uint_as_float(r[8 * q + u]);
-        st_sw128_8(sm + OFF_WT, row, 32 * half + 8 * q, 128, v);
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- MMA-C: delta^T = U^T + S (-W~^T) ----
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TM_U, desc_k(sm + OFF_SB, kk, 16384), desc_mn(sm + OFF_WT, kk, 16384),
-                 idesc, 1);
-      mma_commit(bar_mma);
-    }
-    if (!wait_mma()) { aborted = true; break; }
-
-    // ---- epilogue C: delta^T and its decayed copy as bf16 hi/lo A operands ----
-    {
-      uint32_t r[32];
-      tmem_ld32(tq + TM_U + 32 * half, r);
-      float ed[32];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 e4 = ld4(ED + 32 * half + 4 * q);
-        ed[4 * q] = e4.x; ed[4 * q + 1] = e4.y; ed[4 * q + 2] = e4.z; ed[4 * q + 3] = e4.w;
-      }
-      tmem_wait_ld();
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v[8], w[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          v[u] = __uint_as_float(r[8 * q + u]);
-          w[u] = v[u] * ed[8 * q + u];
-        }
-        st_sw128_8_split(AR + AR_DH, AR + AR_DL, row, 32 * half + 8 * q, 128, v);
-        st_sw128_8_split(AR + AR_DSH, AR + AR_DSL, row, 32 * half + 8 * q, 128, w);
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- MMA-D: delta^T P^T and dS = delta~^T K (hi/lo terms) ----
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id_dp = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t dh = desc_k(AR + AR_DH, kk, 16384), dl = desc_k(AR + AR_DL, kk, 16384);
-        const uint64_t ph = desc_k(sm + OFF_PH, kk, 8192), pl = desc_k(sm + OFF_PL, kk, 8192);
-        mma_bf16(tmem + TM_DP, dh, ph, id_dp, kk > 0);
-        mma_bf16(tmem + TM_DP, dh, pl, id_dp, 1);
-        mma_bf16(tmem + TM_DP, dl, ph, id_dp, 1);
-      }
-      const uint32_t id_ds = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t kb = desc_mn(KQ, kk, 16384);
-        mma_bf16(tmem + TM_DS, desc_k(AR + AR_DSH, kk, 16384), kb, id_ds, kk > 0);
-        mma_bf16(tmem + TM_DS, desc_k(AR + AR_DSL, kk, 16384), kb, id_ds, 1);
-      }
-      mma_commit(bar_mma);
-    }
-    if (!wait_mma()) { aborted = true; break; }
-
-    // ---- epilogue D: outputs (staged in shared memory) and the state update ----
-    {
-      uint32_t a[32], b[32];
-      tmem_ld32(tq + TM_SQ + 32 * half, a);
-      tmem_ld32(tq + TM_DP + 32 * half, b);
-      float eg[32];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 e4 = ld4(EG + 32 * half + 4 * q);
-        eg[4 * q] = e4.x; eg[4 * q + 1] = e4.y; eg[4 * q + 2] = e4.z; eg[4 * q + 3] = e4.w;
-      }
-      tmem_wait_ld();
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int t = 32 * half + jj;
-        ost[t * kD + row] =
-            __float2bfloat16_rn(fmaf(eg[jj], __uint_as_float(a[jj]), __uint_as_float(b[jj])));
-      }
-      const float gam = EG[63];
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        uint32_t d[32];
-        tmem_ld32(tq + TM_DS + 64 * half + 32 * p, d);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t rw[32], ru[32];
+        tmem_ld32(tq + WT_W + 32 * hh, rw);
+        tmem_ld32(tq + WT_U + 32 * hh, ru);
         tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) S[32 * p + u] = fmaf(gam, S[32 * p + u], __uint_as_float(d[u]));
-      }
+        for (int q = 0; q < 4; ++q) {
+          float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) st_sw128_8(sm + OFF_SB, row, 64 * half + 8 * q, 128, S + 8 * q);
-      if (j + 1 < nc && tid >= 64 && tid < 128) {
-        raw[(s ^ 1) * 128 + (tid - 64)] = nla;
-        raw[(s ^ 1) * 128 + 64 + (tid - 64)] = nbe;
+          for (int e = 0; e < 8; ++e) v[e] = -__uint_as_float(rw[8 * q + e]);
+          st_sw128_8(scr + SC_HW, row, 32 * hh + 8 * q, 128, v);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st4(Us + row * LDA + 32 * hh + 4 * q, __uint_as_float(ru[4 * q]),
+              __uint_as_float(ru[4 * q + 1]), __uint_as_float(ru[4 * q + 2]),
+              __uint_as_float(ru[4 * q + 3]));
       }
     }
     fence_async_smem();
     tc_fence_before();
-    __syncthreads();
-    // coalesced copy of the valid output rows: 16 bytes per thread per step
-    {
-      const size_t obase = (size_t)(row0 + c0) * H + h;
+    named_sync(nb, 128);
+    if (wtid == 0) {
+      mbar_arrive_expect_tx_remote(rb_hf_w, 16384);
+      bulk_copy_to_cluster(rdst_w, scr + SC_HW, 16384, rb_hf_w);
+      mbar_arrive_expect_tx_remote(rb_hf_u, 128 * LDA * 4);
+      bulk_copy_to_cluster(rdst_u, scr + SC_HU, 128 * LDA * 4, rb_hf_u);
+      bulk_commit();
+    }
+  }
+#undef WY_WAIT
+  if (wtid == 0) bulk_wait_all();
+}
+
+// ========================================================= CTA 1: state ======
+__device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
+                          const CUtensorMap* tm_k, const float* __restrict__ log_alpha,
+                          const float* __restrict__ beta, const float* __restrict__ S0,
+                          __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
+                          const Unit& u, int H, volatile int* abort_flag) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + ST_BAR);
+  float* der_all = reinterpret_cast<float*>(sm + ST_DER);
+
+  if (warp == 8) {
+    // ---------------- producer: Q and K tiles by TMA, gate factors ----------------
+    int issued = 0;
+    for (int j = 0; j < u.nc; ++j) {
+      const int s = j % ST_NST;
+      const uint32_t use = j / ST_NST;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[SB_QK_EMPTY + s], (use & 1) ^ 1, abort_flag, false)))
+        break;
+      uint8_t* st = sm + ST_QK + s * ST_STAGE;
+      const int r = (int)(u.row0 + (long long)j * kC);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[SB_QK_FULL + s], 4 * 8192);
+        tma_load_3d(st, tm_q, &bars[SB_QK_FULL + s], 0, u.h, r);
+        tma_load_3d(st + 8192, tm_k, &bars[SB_QK_FULL + s], 0, u.h, r);
+        tma_load_3d(st + 16384, tm_q, &bars[SB_QK_FULL + s], 64, u.h, r);
+        tma_load_3d(st + 24576, tm_k, &bars[SB_QK_FULL + s], 64, u.h, r);
+      }
+      issued = j + 1;
+      float g0, g1, tot, b0, b1;
+      warp_gate_scan(log_alpha, beta, u, H, j, lane, g0, g1, tot, b0, b1);
+      float* der = der_all + s * 192;  // G, EG, ED
+      der[lane] = g0;              der[lane + 32] = g1;
+      der[64 + lane] = ex2(g0);    der[64 + lane + 32] = ex2(g1);
+      der[128 + lane] = ex2(tot - g0);  der[128 + lane + 32] = ex2(tot - g1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[SB_QK_FULL + s]);
+    }
+    for (int j = issued - ST_NST; j < issued; ++j)
+      if (j >= 0) (void)mbar_wait(&bars[SB_QK_FULL + j % ST_NST], (j / ST_NST) & 1, 100000000ull);
+    return;
+  }
+
+  const int q4 = warp & 3;
+  const int row = q4 * 32 + lane;
+  const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16);
+
+  if (warp < 4) {
+    // ======================= chain: the serial state pass =======================
+    const uint32_t rb_he_w = map_shared(smem_u32(sm + WY_BAR + 8 * WB_HE_W), 0);
+    const uint32_t rb_he_u = map_shared(smem_u32(sm + WY_BAR + 8 * WB_HE_U), 0);
+    const float* Uh = reinterpret_cast<const float*>(sm + ST_HU);
+    bool alive = true;
+#define CH_WAIT(bar, par, cl)                                                  \
+  {                                                                            \
+    const bool ok_ = wait_bar((bar), (par), abort_flag, (cl));                 \
+    if (named_sync_or(1, 128, !ok_ || *abort_flag != 0)) { alive = false; break; } \
+  }
+    // initial state: bf16 copy for the first MMAs, gamma_0 * S0 into TMEM
+    do {
+      float gam = 1.f;
+      if (u.nc > 0) {
+        CH_WAIT(&bars[SB_QK_FULL + 0], 0, false);
+        gam = der_all[64 + 63];  // e^{g_last} of chunk 0
+      }
+#pragma unroll 1
+      for (int p = 0; p < 4; ++p) {
+        float v[32];
 #pragma unroll
-      for (int it0 = 0; it0 < 1024; it0 += kThreads) {
-        const int it = it0 + tid;
+        for (int q = 0; q < 8; ++q) {
+          float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (S0) t4 = *reinterpret_cast<const float4*>(S0 + u.sidx + (size_t)row * kD + 32 * p + 4 * q);
+          v[4 * q] = t4.x; v[4 * q + 1] = t4.y; v[4 * q + 2] = t4.z; v[4 * q + 3] = t4.w;
+        }
+        if (u.nc == 0) {
+          if (S_final)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st4(S_final + u.sidx + (size_t)row * kD + 32 * p + 4 * q, v[4 * q], v[4 * q + 1],
+                  v[4 * q + 2], v[4 * q + 3]);
+          continue;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_sw128_8(sm + ST_SB, row, 32 * p + 8 * q, 128, v + 8 * q);
+        uint32_t sv[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(gam * v[e]);
+        tmem_st32(tq + TT_S + 32 * p, sv);
+      }
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      named_sync(1, 128);
+      if (tid == 0 && u.nc > 0) mbar_arrive(&bars[SB_SBR]);  // phase 0: S of chunk 0 ready
+    } while (0);
+
+    for (int j = 0; alive && j < u.nc; ++j) {
+      const int s = j % ST_NST;
+      const float* ED = der_all + s * 192 + 128;
+      uint8_t* stg = sm + ST_QK + s * ST_STAGE;
+
+      // ---- SW = S (-W~^T) ----
+      CH_WAIT(&bars[SB_HF_W], j & 1, true);
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(sm + ST_HW, kk, 16384), id,
+                   kk > 0);
+        mma_commit(&bars[SB_C]);
+      }
+      CH_WAIT(&bars[SB_C], j & 1, false);
+      tc_fence_after();
+      if (tid == 0) mbar_arrive_remote(rb_he_w);  // W~ slot may be refilled
+      CH_WAIT(&bars[SB_HF_U], j & 1, true);
+      if (j > 0) CH_WAIT(&bars[SB_DP], (j - 1) & 1, false);  // delta of j-1 no longer read
+
+      // ---- delta^T = U^T + SW, and the decayed copy; hi/lo into TMEM ----
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[32];
+        tmem_ld32(tq + TT_SW + 32 * hh, r);
+        tmem_wait_ld();
+        uint32_t dh[16], dl[16], sh[16], sl[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 u4 = ld4(Uh + row * LDA + 32 * hh + 4 * q);
+          const float4 e4 = ld4(ED + 32 * hh + 4 * q);
+          const float d0 = __uint_as_float(r[4 * q]) + u4.x;
+          const float d1 = __uint_as_float(r[4 * q + 1]) + u4.y;
+          const float d2 = __uint_as_float(r[4 * q + 2]) + u4.z;
+          const float d3 = __uint_as_float(r[4 * q + 3]) + u4.w;
+          const float s0 = d0 * e4.x, s1 = d1 * e4.y, s2 = d2 * e4.z, s3 = d3 * e4.w;
+          const float h0 = bf16_round(d0), h1 = bf16_round(d1), h2 = bf16_round(d2),
+                      h3 = bf16_round(d3);
+          const float k0 = bf16_round(s0), k1 = bf16_round(s1), k2 = bf16_round(s2),
+                      k3 = bf16_round(s3);
+          dh[2 * q] = pack_bf16(h0, h1);             dh[2 * q + 1] = pack_bf16(h2, h3);
+          dl[2 * q] = pack_bf16(d0 - h0, d1 - h1);   dl[2 * q + 1] = pack_bf16(d2 - h2, d3 - h3);
+          sh[2 * q] = pack_bf16(k0, k1);             sh[2 * q + 1] = pack_bf16(k2, k3);
+          sl[2 * q] = pack_bf16(s0 - k0, s1 - k1);   sl[2 * q + 1] = pack_bf16(s2 - k2, s3 - k3);
+        }
+        tmem_st16(tq + TT_DH + 16 * hh, dh);
+        tmem_st16(tq + TT_DL + 16 * hh, dl);
+        tmem_st16(tq + TT_DSH + 16 * hh, sh);
+        tmem_st16(tq + TT_DSL + 16 * hh, sl);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      named_sync(1, 128);
+
+      // ---- S <- e^{g_last} S + delta~^T K (accumulated onto the pre-scaled S) ----
+      if (tid == 0) {
+        mbar_arrive_remote(rb_he_u);    // U slot may be refilled
+        mbar_arrive(&bars[SB_DR]);      // delta of chunk j is in TMEM
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t kb = desc_mn(stg + 8192, kk, 16384);
+          mma_bf16_ta(tmem + TT_S, tmem + TT_DSH + 8 * kk, kb, id, 1);
+          mma_bf16_ta(tmem + TT_S, tmem + TT_DSL + 8 * kk, kb, id, 1);
+        }
+        mma_commit(&bars[SB_DS]);
+      }
+      CH_WAIT(&bars[SB_DS], j & 1, false);
+      tc_fence_after();
+      if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // chain is done with K of this stage
+      CH_WAIT(&bars[SB_SQ], j & 1, false);                 // S Q^T of chunk j has read S
+      const bool last = (j + 1 == u.nc);
+      float gam = 1.f;
+      if (!last) {
+        CH_WAIT(&bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1, false);
+        gam = der_all[((j + 1) % ST_NST) * 192 + 64 + 63];
+      }
+      // ---- new state: bf16 copy for the next chunk, pre-scaled fp32 back to TMEM ----
+#pragma unroll 1
+      for (int p = 0; p < 4; ++p) {
+        uint32_t r[32];
+        tmem_ld32(tq + TT_S + 32 * p, r);
+        tmem_wait_ld();
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+        if (last) {
+          if (S_final)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st4(S_final + u.sidx + (size_t)row * kD + 32 * p + 4 * q, v[4 * q], v[4 * q + 1],
+                  v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) st_sw128_8(sm + ST_SB, row, 32 * p + 8 * q, 128, v + 8 * q);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(gam * v[e]);
+          tmem_st32(tq + TT_S + 32 * p, r);
+        }
+      }
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      named_sync(1, 128);
+      if (tid == 0 && !last) mbar_arrive(&bars[SB_SBR]);  // phase j + 1
+    }
+#undef CH_WAIT
+    return;
+  }
+
+  // ========================= aux: P, S Q^T, delta^T P^T, outputs =========================
+  const int atid = tid - 128;
+  __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + ST_OST);
+#define AX_WAIT(bar, par)                                                      \
+  {                                                                            \
+    const bool ok_ = wait_bar((bar), (par), abort_flag, false);                \
+    if (named_sync_or(2, 128, !ok_ || *abort_flag != 0)) break;                \
+  }
+  for (int j = 0; j < u.nc; ++j) {
+    const int s = j % ST_NST;
+    uint8_t* stg = sm + ST_QK + s * ST_STAGE;
+    const float* G = der_all + s * 192;
+    const float* EG = G + 64;
+    const long long c0 = (long long)j * kC;
+    const int lc = (int)min((long long)kC, u.len - c0);
+    AX_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
+
+    // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T) ----
+    if (atid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(tmem + TT_QK, desc_k(stg, kk, 16384), desc_k(stg + 8192, kk, 16384), id, kk > 0);
+      mma_commit(&bars[SB_QKM]);
+    }
+    AX_WAIT(&bars[SB_QKM], j & 1);
+    tc_fence_after();
+    if (q4 < 2) {
+      const int t = row;
+      const float gt = G[t];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[32];
+        tmem_ld32(tq + TT_QK + 32 * hh, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 ga = ld4(G + 32 * hh + 8 * q), gb = ld4(G + 32 * hh + 8 * q + 4);
+          const float gc[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int jc = 32 * hh + 8 * q + e;
+            v[e] = (jc <= t) ? ex2(gt - gc[e]) * __uint_as_float(r[8 * q + e]) : 0.f;
+          }
+          st_sw128_8_split(sm + ST_PH, sm + ST_PL, t, 32 * hh + 8 * q, 64, v);
+        }
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    named_sync(2, 128);
+
+    // ---- S Q^T once the chain has written S of chunk j ----
+    AX_WAIT(&bars[SB_SBR], j & 1);
+    if (atid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16(tmem + TT_SQ, desc_k(sm + ST_SB, kk, 16384), desc_k(stg, kk, 16384), id, kk > 0);
+      mma_commit(&bars[SB_SQ]);
+    }
+    // ---- delta^T P^T once the chain has delta of chunk j ----
+    AX_WAIT(&bars[SB_DR], j & 1);
+    if (atid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ph = desc_k(sm + ST_PH, kk, 8192), pl = desc_k(sm + ST_PL, kk, 8192);
+        mma_bf16_ta(tmem + TT_DP, tmem + TT_DH + 8 * kk, ph, id, kk > 0);
+        mma_bf16_ta(tmem + TT_DP, tmem + TT_DH + 8 * kk, pl, id, 1);
+        mma_bf16_ta(tmem + TT_DP, tmem + TT_DL + 8 * kk, ph, id, 1);
+      }
+      mma_commit(&bars[SB_DP]);
+    }
+    AX_WAIT(&bars[SB_SQ], j & 1);
+    AX_WAIT(&bars[SB_DP], j & 1);
+    tc_fence_after();
+
+    // ---- o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t, staged, then coalesced rows ----
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t a[32], b[32];
+      tmem_ld32(tq + TT_SQ + 32 * hh, a);
+      tmem_ld32(tq + TT_DP + 32 * hh, b);
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 e4 = ld4(EG + 32 * hh + 4 * q);
+        const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 32 * hh + 4 * q + e;
+          ost[t * kD + row] = __float2bfloat16_rn(
+              fmaf(ev[e], __uint_as_float(a[4 * q + e]), __uint_as_float(b[4 * q + e])));
+        }
+      }
+    }
+    tc_fence_before();
+    named_sync(2, 128);
+    {
+      const size_t obase = (size_t)(u.row0 + c0) * H + u.h;
+#pragma unroll
+      for (int it0 = 0; it0 < 1024; it0 += 128) {
+        const int it = it0 + atid;
         const int t = it >> 4, ch = it & 15;
         if (t < lc) {
           const uint4 v = *reinterpret_cast<const uint4*>(ost + t * kD + 8 * ch);
@@ -629,25 +811,91 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       }
     }
+    named_sync(2, 128);
+    // Q, K and the gate factors of this stage are no longer read by aux
+    if (atid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);
   }
+#undef AX_WAIT
+}
 
-  if (aborted) {
-    // Let copies still in flight land before the CTA's shared memory goes away.
-    if (tid == 0) {
-      for (int st = 0; st < 2; ++st)
-        if (kq_pending[st]) (void)mbar_wait(&bar_kq[st], kq_par[st], 100000000ull);
-      if (v_pending) (void)mbar_wait(bar_v, v_par, 100000000ull);
-      atomicOr(&g_tc_status, *s_abort);
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ log_alpha,
+              const float* __restrict__ beta, const float* __restrict__ S0,
+              __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
+              const int32_t* __restrict__ cu_seqlens, int H, int T) {
+  extern __shared__ uint8_t smem_raw[];
+  // Align to 1024 bytes by pointer arithmetic on the shared array itself (accesses
+  // stay shared-memory accesses); the offset is the same in both CTAs.
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int unit = blockIdx.x >> 1;
+  Unit u;
+  u.h = unit % H;
+  const int n = unit / H;
+  if (cu_seqlens) {
+    int a = cu_seqlens[n], b = cu_seqlens[n + 1];
+    a = min(max(a, 0), T);
+    b = min(max(b, a), T);
+    u.row0 = a;
+    u.len = b - a;
+  } else {
+    u.row0 = (long long)n * T;
+    u.len = T;
+  }
+  u.nc = (int)((u.len + kC - 1) / kC);
+  u.sidx = ((size_t)n * H + u.h) * kD * kD;
+
+  uint8_t* misc = sm + (rank == 0 ? WY_MISC : ST_MISC);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  if (warp == 0) tmem_alloc(tslot, TM_COLS);
+  if (tid == 32) {
+    *abort_flag = 0;
+    if (rank == 0) {
+      uint64_t* b = reinterpret_cast<uint64_t*>(sm + WY_BAR);
+      for (int s = 0; s < WY_NST; ++s) {
+        mbar_init(&b[WB_KV_FULL + s], 2);
+        mbar_init(&b[WB_KV_EMPTY + s], 1);
+      }
+      mbar_init(&b[WB_MMA + 0], 1);
+      mbar_init(&b[WB_MMA + 1], 1);
+      mbar_init(&b[WB_HE_W], 1);
+      mbar_init(&b[WB_HE_U], 1);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+    } else {
+      uint64_t* b = reinterpret_cast<uint64_t*>(sm + ST_BAR);
+      for (int s = 0; s < ST_NST; ++s) {
+        mbar_init(&b[SB_QK_FULL + s], 2);
+        mbar_init(&b[SB_QK_EMPTY + s], 2);
+      }
+      for (int k = SB_HF_W; k <= SB_DR; ++k) mbar_init(&b[k], 1);
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
     }
-  } else if (S_final) {
-#pragma unroll
-    for (int q = 0; q < 16; ++q)
-      *reinterpret_cast<float4*>(S_final + sidx + 4 * q) =
-          make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+    fence_mbarrier_init();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy
+
+  if (rank == 0)
+    run_wy(sm, tmem, &tm_k, &tm_v, log_alpha, beta, u, H, abort_flag);
+  else
+    run_state(sm, tmem, &tm_q, &tm_k, log_alpha, beta, S0, out, S_final, u, H, abort_flag);
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) atomicOr(&g_tc_status, *abort_flag);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+  cluster_sync();  // neither CTA leaves while the other may still touch its memory
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -693,7 +941,7 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
   if (!make_map(&mq, a.q, rows, a.H) || !make_map(&mk, a.k, rows, a.H) ||
       !make_map(&mv, a.v, rows, a.H))
     return cudaErrorInvalidValue;
-  const long long blocks = (long long)a.N * a.H;
+  const long long blocks = 2LL * a.N * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
