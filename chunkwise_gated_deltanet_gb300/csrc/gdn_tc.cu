@@ -69,13 +69,13 @@ constexpr int WY_NST = 3;
 constexpr int WY_SCR = 98304;            // per-warpgroup scratch
 constexpr int WY_SCR_BYTES = 53248;
 //   A/T fp32 [64][68] @0 | X fp32 [3][256] @17408 | Tw hi @20480 | Tw lo @28672
-//   | Tu hi @36864 | Tu lo @45056;   epilogue B reuses it: -W~^T bf16 [128][64] @0,
-//   U^T fp32 [128][68] @16384
+//   | Tu hi @36864 | Tu lo @45056
 constexpr int LDA = 68;
 constexpr int SC_X = 17408, SC_TWH = 20480, SC_TWL = 28672, SC_TUH = 36864, SC_TUL = 45056;
-constexpr int SC_HW = 0, SC_HU = 16384;
-constexpr int WY_DER = WY_SCR + 2 * WY_SCR_BYTES;  // [3 stages][G, EG, BG, BE][64] fp32
-constexpr int WY_BAR = WY_DER + WY_NST * 4 * 256;
+constexpr int WY_DER = WY_SCR + 2 * WY_SCR_BYTES;  // [3 stages][G, EG, BG, BE, EN][64] fp32
+constexpr int WY_DER_STAGE = 5 * 64;                // floats per stage
+constexpr int WY_FLAG = WY_DER + WY_NST * WY_DER_STAGE * 4;  // [3] int: factored decay allowed
+constexpr int WY_BAR = WY_FLAG + 64;
 constexpr int WY_MISC = WY_BAR + 128;
 constexpr int WY_USED = WY_MISC + 64;
 
@@ -83,29 +83,36 @@ constexpr int WY_USED = WY_MISC + 64;
 constexpr int ST_QK = 0;                 // 2 stages x 32 KB; per dk panel p: Q rows (8 KB), K rows (8 KB)
 constexpr int ST_STAGE = 32768;
 constexpr int ST_NST = 2;
-constexpr int ST_HW = 65536;             // -W~^T bf16 [128 dk][64 tok], MN-major B operand
-constexpr int ST_HU = 81920;             // U^T fp32 [128 dv][68]
-constexpr int ST_PH = 117760;            // P hi bf16 [64 t][64 j], K-major B operand
-constexpr int ST_PL = 125952;            // P lo
-constexpr int ST_SB = 134144;            // S bf16 [128 dv][128 dk], 2 K panels
-constexpr int ST_OST = 166912;           // output staging bf16 [64 t][128]
-constexpr int ST_DER = 183296;           // [2 stages][G, EG, ED][64] fp32
-constexpr int ST_BAR = ST_DER + ST_NST * 3 * 256;
-constexpr int ST_MISC = ST_BAR + 128;
+constexpr int ST_HS = 65536;             // 2 handoff slots of 48 KB each:
+constexpr int HS_BYTES = 49152;          //   -W~^T bf16 [128 dk][64 tok] (MN-major B) @0,
+constexpr int HS_UH = 16384, HS_UL = 32768;  // U^T hi, lo bf16 [128 dv][64 tok] (swizzled rows)
+constexpr int ST_PH = ST_HS + 2 * HS_BYTES;  // 163840: P hi bf16 [64 t][64 j], K-major B operand
+constexpr int ST_PL = ST_PH + 8192;      // P lo
+constexpr int ST_SB = ST_PL + 8192;      // 180224: S bf16 [128 dv][128 dk], 2 K panels
+constexpr int ST_DER = ST_SB + 32768;    // [2 stages][G, EG, ED, EN][64] fp32
+constexpr int ST_DER_STAGE = 4 * 64;
+constexpr int ST_FLAG = ST_DER + ST_NST * ST_DER_STAGE * 4;  // [2] int
+constexpr int ST_BAR = ST_FLAG + 64;
+constexpr int ST_MISC = ST_BAR + 160;
 constexpr int ST_USED = ST_MISC + 64;
+// The output tile of a chunk is staged in the Q rows of its own stage once Q is no
+// longer read (rows 0..31 in panel 0, rows 32..63 in panel 1, 256 bytes a row).
 
 constexpr int SMEM_USED = WY_USED > ST_USED ? WY_USED : ST_USED;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SC_TUL + 8192 <= WY_SCR_BYTES, "WY scratch");
-static_assert(SC_HU + 128 * LDA * 4 <= WY_SCR_BYTES, "WY staging");
-static_assert(ST_HU + 128 * LDA * 4 <= ST_PH, "state handoff");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
+// The factored decay e^{g_i} e^{-g_j} replaces e^{g_i - g_j} when the chunk's
+// total decay (in log2 units) is below this bound, so that neither factor
+// overflows or underflows fp32.
+constexpr float kMaxFactoredDecayLog2 = 80.f;
+
 // barrier slots (8 bytes each)
-enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE_W = 8, WB_HE_U = 9 };
+enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE_W = 8, WB_HE_U = 10 };
 enum StBar {
-  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF_W = 4, SB_HF_U = 5, SB_C = 6, SB_DS = 7, SB_QKM = 8,
-  SB_SQ = 9, SB_DP = 10, SB_SBR = 11, SB_DR = 12
+  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF_W = 4, SB_HF_U = 6, SB_C = 8, SB_DS = 9, SB_QKM = 10,
+  SB_SQ = 11, SB_DP = 12, SB_SBR = 13, SB_DR = 14
 };
 
 // TMEM columns.  WY: per warpgroup w at 192*w: K K^T 0, W~^T 64, U^T 128.
@@ -128,9 +135,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ float bf16_round(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
-}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -143,16 +147,22 @@ __device__ __forceinline__ void st_sw128_8(uint8_t* tile, int row, int col, int 
   st_shared_v4(smem_u32(tile + sw128_offset(row, col, rows)), pack_bf16(v[0], v[1]),
                pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
 }
+// Two floats as a pair of packed bf16 terms: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+  lo = pack_bf16(x0 - h0, x1 - h1);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ void st_sw128_8_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
                                                  int col, int rows, const float* v) {
-  float hi[8], lo[8];
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    hi[u] = bf16_round(v[u]);
-    lo[u] = v[u] - hi[u];
-  }
-  st_sw128_8(hi_tile, row, col, rows, hi);
-  st_sw128_8(lo_tile, row, col, rows, lo);
+  for (int u = 0; u < 4; ++u) split2(v[2 * u], v[2 * u + 1], h[u], l[u]);
+  const uint32_t off = sw128_offset(row, col, rows);
+  st_shared_v4(smem_u32(hi_tile + off), h[0], h[1], h[2], h[3]);
+  st_shared_v4(smem_u32(lo_tile + off), l[0], l[1], l[2], l[3]);
 }
 // K-major operand, 128B swizzle, K advanced by 16 elements per step.
 __device__ __forceinline__ uint64_t desc_k(const uint8_t* tile, int kstep, int panel_bytes) {
@@ -191,27 +201,34 @@ struct Unit {
   size_t sidx;  // offset of S[n][h] in S0 / S_final
 };
 
-// Chunk gate values of one stage, computed by a whole warp: thread `lane` owns
-// tokens lane and lane + 32.  Returns the in-chunk cumulative gate sums in log2
-// units (g0 for token lane, g1 for token lane + 32) and their total.
-__device__ __forceinline__ void warp_gate_scan(const float* __restrict__ log_alpha,
-                                               const float* __restrict__ beta, const Unit& u,
-                                               int H, int chunk, int lane, float& g0, float& g1,
-                                               float& tot, float& b0, float& b1) {
+// Gate inputs of one chunk for a whole warp: thread `lane` owns tokens lane and
+// lane + 32 (zeros past the sequence end).  Split from the scan so the loads of
+// the next chunk can be in flight while the current one is processed.
+struct GateLoad {
+  float la0, la1, b0, b1;
+};
+__device__ __forceinline__ GateLoad load_gates(const float* __restrict__ log_alpha,
+                                               const float* __restrict__ beta, const Unit& u, int H,
+                                               int chunk, int lane) {
+  GateLoad g{0.f, 0.f, 0.f, 0.f};
   const long long c0 = (long long)chunk * kC;
-  float x0 = 0.f, x1 = 0.f;
-  b0 = 0.f;
-  b1 = 0.f;
-  if (c0 + lane < u.len) {
+  if (chunk < u.nc && c0 + lane < u.len) {
     const size_t gi = (size_t)(u.row0 + c0 + lane) * H + u.h;
-    x0 = __ldg(log_alpha + gi);
-    b0 = __ldg(beta + gi);
+    g.la0 = __ldg(log_alpha + gi);
+    g.b0 = __ldg(beta + gi);
   }
-  if (c0 + lane + 32 < u.len) {
+  if (chunk < u.nc && c0 + lane + 32 < u.len) {
     const size_t gi = (size_t)(u.row0 + c0 + lane + 32) * H + u.h;
-    x1 = __ldg(log_alpha + gi);
-    b1 = __ldg(beta + gi);
+    g.la1 = __ldg(log_alpha + gi);
+    g.b1 = __ldg(beta + gi);
   }
+  return g;
+}
+// In-chunk cumulative gate sums in log2 units (g0 for token lane, g1 for token
+// lane + 32) and their total.
+__device__ __forceinline__ void scan_gates(const GateLoad& in, int lane, float& g0, float& g1,
+                                           float& tot) {
+  float x0 = in.la0, x1 = in.la1;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
@@ -229,19 +246,23 @@ __device__ __forceinline__ void warp_gate_scan(const float* __restrict__ log_alp
 }
 
 // ============================================================ CTA 0: WY ======
-__device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+__device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                        const float* __restrict__ log_alpha, const float* __restrict__ beta,
                        const Unit& u, int H, volatile int* abort_flag) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + WY_BAR);
   float* der_all = reinterpret_cast<float*>(sm + WY_DER);
+  int* flags = reinterpret_cast<int*>(sm + WY_FLAG);
 
   if (warp == 8) {
     // ---------------- producer: K and V tiles by TMA, gate factors ----------------
     int issued = 0;
+    GateLoad next = load_gates(log_alpha, beta, u, H, 0, lane);
     for (int j = 0; j < u.nc; ++j) {
       const int s = j % WY_NST;
       const uint32_t use = j / WY_NST;
+      const GateLoad cur = next;
+      next = load_gates(log_alpha, beta, u, H, j + 1, lane);  // in flight during the wait
       if (!__all_sync(0xffffffffu, wait_bar(&bars[WB_KV_EMPTY + s], (use & 1) ^ 1, abort_flag, false)))
         break;
       uint8_t* st = sm + WY_KV + s * WY_STAGE;
@@ -254,15 +275,17 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
         tma_load_3d(st + 24576, tm_v, &bars[WB_KV_FULL + s], 64, u.h, r);
       }
       issued = j + 1;
-      float g0, g1, tot, b0, b1;
-      warp_gate_scan(log_alpha, beta, u, H, j, lane, g0, g1, tot, b0, b1);
-      float* der = der_all + s * 256;  // G, EG, BG, BE
+      float g0, g1, tot;
+      scan_gates(cur, lane, g0, g1, tot);
+      const float b0 = cur.b0, b1 = cur.b1;
+      float* der = der_all + s * WY_DER_STAGE;  // G, EG, BG, BE, EN
       const float e0 = ex2(g0), e1 = ex2(g1);
-      der[lane] = g0;        der[lane + 32] = g1;
-      der[64 + lane] = e0;   der[64 + lane + 32] = e1;
-      der[128 + lane] = b0 * e0;  der[128 + lane + 32] = b1 * e1;
-      der[192 + lane] = b0;  der[192 + lane + 32] = b1;
-      (void)tot;
+      der[lane] = g0;                 der[lane + 32] = g1;
+      der[64 + lane] = e0;            der[64 + lane + 32] = e1;
+      der[128 + lane] = b0 * e0;      der[128 + lane + 32] = b1 * e1;
+      der[192 + lane] = b0;           der[192 + lane + 32] = b1;
+      der[256 + lane] = ex2(-g0);     der[256 + lane + 32] = ex2(-g1);
+      if (lane == 0) flags[s] = (-tot < kMaxFactoredDecayLog2) ? 1 : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[WB_KV_FULL + s]);
     }
@@ -284,10 +307,6 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
   const uint32_t tw = tmem + w * WT_WG;
   const uint32_t tq = tw + ((uint32_t)(q4 * 32) << 16);
   uint32_t mph = 0;
-  const uint32_t rb_hf_w = map_shared(smem_u32(sm + ST_BAR + 8 * SB_HF_W), 1);
-  const uint32_t rb_hf_u = map_shared(smem_u32(sm + ST_BAR + 8 * SB_HF_U), 1);
-  const uint32_t rdst_w = map_shared(smem_u32(sm + ST_HW), 1);
-  const uint32_t rdst_u = map_shared(smem_u32(sm + ST_HU), 1);
 
 #define WY_WAIT(bar, par, cl)                                                  \
   {                                                                            \
@@ -298,11 +317,12 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
   for (int j = w; j < u.nc; j += 2) {
     const int s = j % WY_NST;
     uint8_t* st = sm + WY_KV + s * WY_STAGE;
-    const float* G = der_all + s * 256;
+    const float* G = der_all + s * WY_DER_STAGE;
     const float* BG = G + 128;
     const float* BE = G + 192;
-    if (wtid == 0) bulk_wait_read_all();  // the previous staging of this warpgroup was read
+    const float* EN = G + 256;
     WY_WAIT(&bars[WB_KV_FULL + s], (j / WY_NST) & 1, false);
+    const bool factored = flags[s] != 0;
 
     // ---- K K^T (rows 0..63 of the M=128 accumulator) ----
     if (wtid == 0) {
@@ -313,6 +333,9 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
         mma_bf16(tw + WT_KK, desc_k(st, kk, 8192), desc_k(st, kk, 8192), id, kk > 0);
       mma_commit(&bars[WB_MMA + w]);
     }
+    // the bulk copy of this warpgroup's previous chunk reads the scratch that A is
+    // about to overwrite; it has had the K K^T round trip to finish
+    if (wtid == 0) bulk_wait_read_all();
     WY_WAIT(&bars[WB_MMA + w], mph, false);
     mph ^= 1;
     tc_fence_after();
@@ -320,7 +343,7 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
     // ---- A = strictly-lower(beta_i e^{g_i - g_j} k_i.k_j), fp32 ----
     if (q4 < 2) {
       const int i = row;
-      const float gi = G[i], bi = BE[i];
+      const float gi = G[i], bi = BE[i], bgi = BG[i];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
@@ -328,15 +351,22 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const float4 g4 = ld4(G + 32 * hh + 4 * q);
-          const float gc[4] = {g4.x, g4.y, g4.z, g4.w};
+          const int jc0 = 32 * hh + 4 * q;
           float v[4];
+          if (factored) {
+            const float4 n4 = ld4(EN + jc0);
+            const float en[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int jc = 32 * hh + 4 * q + e;
-            v[e] = (jc < i) ? bi * ex2(gi - gc[e]) * __uint_as_float(r[4 * q + e]) : 0.f;
+            for (int e = 0; e < 4; ++e)
+              v[e] = (jc0 + e < i) ? bgi * __uint_as_float(r[4 * q + e]) * en[e] : 0.f;
+          } else {
+            const float4 g4 = ld4(G + jc0);
+            const float gc[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              v[e] = (jc0 + e < i) ? bi * ex2(gi - gc[e]) * __uint_as_float(r[4 * q + e]) : 0.f;
           }
-          st4(Am + i * LDA + 32 * hh + 4 * q, v[0], v[1], v[2], v[3]);
+          st4(Am + i * LDA + jc0, v[0], v[1], v[2], v[3]);
         }
       }
     }
@@ -361,9 +391,13 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
     }
     named_sync(nb, 128);
     // ---- block rows: X = sum_k A_{ib,k} T_{k,jb}; T_{ib,jb} = -T_{ib,ib} X ----
+    // each thread owns 1 x 4 strips of the 16 x 16 blocks
 #pragma unroll 1
     for (int ib = 1; ib < 4; ++ib) {
-      for (int e = wtid; e < ib * 64; e += 128) {
+      // strip e covers block jb = e / 64 (1 x 4 of its 16 x 16).  Thread t takes strip
+      // t, and in block row 3 threads t >= 64 also take strip t + 64, so every thread
+      // of row 3 does three block products (jb 0: 3; jb 1 + jb 2: 2 + 1).
+      for (int e = wtid; e < ib * 64; e += (ib == 3) ? (wtid >= 64 ? 64 : 192) : 128) {
         const int jb = e >> 6, r = (e >> 2) & 15, cq = e & 3;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         const float* arow = Am + (16 * ib + r) * LDA;
@@ -384,7 +418,7 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
         st4(Xs + jb * 256 + r * 16 + 4 * cq, a0, a1, a2, a3);
       }
       named_sync(nb, 128);
-      for (int e = wtid; e < ib * 64; e += 128) {
+      for (int e = wtid; e < ib * 64; e += (ib == 3) ? (wtid >= 64 ? 64 : 192) : 128) {
         const int jb = e >> 6, r = (e >> 2) & 15, cq = e & 3;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
         const float* trow = Am + (16 * ib + r) * LDA + 16 * ib;
@@ -448,11 +482,12 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
     tc_fence_after();
     if (wtid == 0) mbar_arrive(&bars[WB_KV_EMPTY + s]);  // K, V of this stage are consumed
 
-    // ---- hand chunk j to the state CTA once its slot is free ----
-    WY_WAIT(&bars[WB_HE_W], (j & 1) ^ 1, true);
-    WY_WAIT(&bars[WB_HE_U], (j & 1) ^ 1, true);
+    // ---- hand chunk j to the state CTA: stage in scratch, bulk-copy into slot j % 2 ----
+    const int slot = j & 1;
+    const uint32_t huse = (uint32_t)(j >> 1);
     {
-      float* Us = reinterpret_cast<float*>(scr + SC_HU);
+      // -W~^T bf16 [128 dk][64 tok] at scratch 0, U^T hi / lo bf16 [128 dv][64 tok] at
+      // 16 KB / 32 KB: the slot's layout, so one bulk copy moves each part.
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t rw[32], ru[32];
@@ -461,35 +496,74 @@ __device__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, cons
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float v[8];
+          const uint32_t off = sw128_offset(row, 32 * hh + 8 * q, 128);
+          uint32_t wv[4], uh[4], ul[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = -__uint_as_float(rw[8 * q + e]);
-          st_sw128_8(scr + SC_HW, row, 32 * hh + 8 * q, 128, v);
+          for (int e = 0; e < 4; ++e) {
+            wv[e] = pack_bf16(-__uint_as_float(rw[8 * q + 2 * e]),
+                              -__uint_as_float(rw[8 * q + 2 * e + 1]));
+            split2(__uint_as_float(ru[8 * q + 2 * e]), __uint_as_float(ru[8 * q + 2 * e + 1]),
+                   uh[e], ul[e]);
+          }
+          st_shared_v4(smem_u32(scr + off), wv[0], wv[1], wv[2], wv[3]);
+          st_shared_v4(smem_u32(scr + HS_UH + off), uh[0], uh[1], uh[2], uh[3]);
+          st_shared_v4(smem_u32(scr + HS_UL + off), ul[0], ul[1], ul[2], ul[3]);
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st4(Us + row * LDA + 32 * hh + 4 * q, __uint_as_float(ru[4 * q]),
-              __uint_as_float(ru[4 * q + 1]), __uint_as_float(ru[4 * q + 2]),
-              __uint_as_float(ru[4 * q + 3]));
       }
     }
     fence_async_smem();
     tc_fence_before();
-    named_sync(nb, 128);
+    WY_WAIT(&bars[WB_HE_W + slot], (huse & 1) ^ 1, true);
+    WY_WAIT(&bars[WB_HE_U + slot], (huse & 1) ^ 1, true);
     if (wtid == 0) {
-      mbar_arrive_expect_tx_remote(rb_hf_w, 16384);
-      bulk_copy_to_cluster(rdst_w, scr + SC_HW, 16384, rb_hf_w);
-      mbar_arrive_expect_tx_remote(rb_hf_u, 128 * LDA * 4);
-      bulk_copy_to_cluster(rdst_u, scr + SC_HU, 128 * LDA * 4, rb_hf_u);
+      const uint32_t rb_w = map_shared(smem_u32(sm + ST_BAR + 8 * (SB_HF_W + slot)), 1);
+      const uint32_t rb_u = map_shared(smem_u32(sm + ST_BAR + 8 * (SB_HF_U + slot)), 1);
+      const uint32_t rs = map_shared(smem_u32(sm + ST_HS + slot * HS_BYTES), 1);
+      mbar_arrive_expect_tx_remote(rb_w, 16384);
+      bulk_copy_to_cluster(rs, scr, 16384, rb_w);
+      mbar_arrive_expect_tx_remote(rb_u, 32768);
+      bulk_copy_to_cluster(rs + HS_UH, scr + HS_UH, 32768, rb_u);
       bulk_commit();
     }
   }
 #undef WY_WAIT
-  if (wtid == 0) bulk_wait_all();
+  if (wtid == 0) bulk_wait_all();  // every copy this warpgroup issued has landed
+}
+
+// One half (tokens 32*hh .. 32*hh + 31) of the delta epilogue of the state CTA:
+// delta^T = SW + U^T (U^T arrives as hi + lo bf16), delta~ = delta e^{g_last - g};
+// both written to TMEM as hi / lo bf16 pairs (the A operands of the next MMAs).
+__device__ __forceinline__ void delta_half(uint32_t tq, const uint8_t* hs, const float* ED, int row,
+                                           int hh) {
+  uint32_t r[32];
+  tmem_ld32(tq + TT_SW + 32 * hh, r);
+  tmem_wait_ld();
+  uint32_t dh[16], dl[16], sh[16], sl[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t off = sw128_offset(row, 32 * hh + 8 * q, 128);
+    const uint4 uh = *reinterpret_cast<const uint4*>(hs + HS_UH + off);
+    const uint4 ul = *reinterpret_cast<const uint4*>(hs + HS_UL + off);
+    const uint32_t uhw[4] = {uh.x, uh.y, uh.z, uh.w}, ulw[4] = {ul.x, ul.y, ul.z, ul.w};
+    const float4 ea = ld4(ED + 32 * hh + 8 * q), eb = ld4(ED + 32 * hh + 8 * q + 4);
+    const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float d0 = __uint_as_float(r[8 * q + 2 * e]) + bf16_lo(uhw[e]) + bf16_lo(ulw[e]);
+      const float d1 = __uint_as_float(r[8 * q + 2 * e + 1]) + bf16_hi(uhw[e]) + bf16_hi(ulw[e]);
+      split2(d0, d1, dh[4 * q + e], dl[4 * q + e]);
+      split2(d0 * ev[2 * e], d1 * ev[2 * e + 1], sh[4 * q + e], sl[4 * q + e]);
+    }
+  }
+  tmem_st16(tq + TT_DH + 16 * hh, dh);
+  tmem_st16(tq + TT_DL + 16 * hh, dl);
+  tmem_st16(tq + TT_DSH + 16 * hh, sh);
+  tmem_st16(tq + TT_DSL + 16 * hh, sl);
+  tmem_wait_st();
 }
 
 // ========================================================= CTA 1: state ======
-__device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
+__device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
                           const CUtensorMap* tm_k, const float* __restrict__ log_alpha,
                           const float* __restrict__ beta, const float* __restrict__ S0,
                           __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
@@ -497,13 +571,17 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + ST_BAR);
   float* der_all = reinterpret_cast<float*>(sm + ST_DER);
+  int* flags = reinterpret_cast<int*>(sm + ST_FLAG);
 
   if (warp == 8) {
     // ---------------- producer: Q and K tiles by TMA, gate factors ----------------
     int issued = 0;
+    GateLoad next = load_gates(log_alpha, beta, u, H, 0, lane);
     for (int j = 0; j < u.nc; ++j) {
       const int s = j % ST_NST;
       const uint32_t use = j / ST_NST;
+      const GateLoad cur = next;
+      next = load_gates(log_alpha, beta, u, H, j + 1, lane);  // in flight during the wait
       if (!__all_sync(0xffffffffu, wait_bar(&bars[SB_QK_EMPTY + s], (use & 1) ^ 1, abort_flag, false)))
         break;
       uint8_t* st = sm + ST_QK + s * ST_STAGE;
@@ -516,12 +594,14 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
         tma_load_3d(st + 24576, tm_k, &bars[SB_QK_FULL + s], 64, u.h, r);
       }
       issued = j + 1;
-      float g0, g1, tot, b0, b1;
-      warp_gate_scan(log_alpha, beta, u, H, j, lane, g0, g1, tot, b0, b1);
-      float* der = der_all + s * 192;  // G, EG, ED
-      der[lane] = g0;              der[lane + 32] = g1;
-      der[64 + lane] = ex2(g0);    der[64 + lane + 32] = ex2(g1);
+      float g0, g1, tot;
+      scan_gates(cur, lane, g0, g1, tot);
+      float* der = der_all + s * ST_DER_STAGE;  // G, EG, ED, EN
+      der[lane] = g0;                   der[lane + 32] = g1;
+      der[64 + lane] = ex2(g0);         der[64 + lane + 32] = ex2(g1);
       der[128 + lane] = ex2(tot - g0);  der[128 + lane + 32] = ex2(tot - g1);
+      der[192 + lane] = ex2(-g0);       der[192 + lane + 32] = ex2(-g1);
+      if (lane == 0) flags[s] = (-tot < kMaxFactoredDecayLog2) ? 1 : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[SB_QK_FULL + s]);
     }
@@ -536,9 +616,6 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
 
   if (warp < 4) {
     // ======================= chain: the serial state pass =======================
-    const uint32_t rb_he_w = map_shared(smem_u32(sm + WY_BAR + 8 * WB_HE_W), 0);
-    const uint32_t rb_he_u = map_shared(smem_u32(sm + WY_BAR + 8 * WB_HE_U), 0);
-    const float* Uh = reinterpret_cast<const float*>(sm + ST_HU);
     bool alive = true;
 #define CH_WAIT(bar, par, cl)                                                  \
   {                                                                            \
@@ -585,64 +662,37 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
 
     for (int j = 0; alive && j < u.nc; ++j) {
       const int s = j % ST_NST;
-      const float* ED = der_all + s * 192 + 128;
+      const float* ED = der_all + s * ST_DER_STAGE + 128;
       uint8_t* stg = sm + ST_QK + s * ST_STAGE;
+      const int slot = j & 1;
+      const uint32_t huse = (uint32_t)(j >> 1);
+      uint8_t* hs = sm + ST_HS + slot * HS_BYTES;
 
       // ---- SW = S (-W~^T) ----
-      CH_WAIT(&bars[SB_HF_W], j & 1, true);
+      CH_WAIT(&bars[SB_HF_W + slot], huse & 1, true);
       if (tid == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(sm + ST_HW, kk, 16384), id,
-                   kk > 0);
+          mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(hs, kk, 16384), id, kk > 0);
         mma_commit(&bars[SB_C]);
       }
       CH_WAIT(&bars[SB_C], j & 1, false);
       tc_fence_after();
-      if (tid == 0) mbar_arrive_remote(rb_he_w);  // W~ slot may be refilled
-      CH_WAIT(&bars[SB_HF_U], j & 1, true);
+      if (tid == 0) mbar_arrive_remote(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE_W + slot)), 0));
+      CH_WAIT(&bars[SB_HF_U + slot], huse & 1, true);
       if (j > 0) CH_WAIT(&bars[SB_DP], (j - 1) & 1, false);  // delta of j-1 no longer read
 
       // ---- delta^T = U^T + SW, and the decayed copy; hi/lo into TMEM ----
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r[32];
-        tmem_ld32(tq + TT_SW + 32 * hh, r);
-        tmem_wait_ld();
-        uint32_t dh[16], dl[16], sh[16], sl[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 u4 = ld4(Uh + row * LDA + 32 * hh + 4 * q);
-          const float4 e4 = ld4(ED + 32 * hh + 4 * q);
-          const float d0 = __uint_as_float(r[4 * q]) + u4.x;
-          const float d1 = __uint_as_float(r[4 * q + 1]) + u4.y;
-          const float d2 = __uint_as_float(r[4 * q + 2]) + u4.z;
-          const float d3 = __uint_as_float(r[4 * q + 3]) + u4.w;
-          const float s0 = d0 * e4.x, s1 = d1 * e4.y, s2 = d2 * e4.z, s3 = d3 * e4.w;
-          const float h0 = bf16_round(d0), h1 = bf16_round(d1), h2 = bf16_round(d2),
-                      h3 = bf16_round(d3);
-          const float k0 = bf16_round(s0), k1 = bf16_round(s1), k2 = bf16_round(s2),
-                      k3 = bf16_round(s3);
-          dh[2 * q] = pack_bf16(h0, h1);             dh[2 * q + 1] = pack_bf16(h2, h3);
-          dl[2 * q] = pack_bf16(d0 - h0, d1 - h1);   dl[2 * q + 1] = pack_bf16(d2 - h2, d3 - h3);
-          sh[2 * q] = pack_bf16(k0, k1);             sh[2 * q + 1] = pack_bf16(k2, k3);
-          sl[2 * q] = pack_bf16(s0 - k0, s1 - k1);   sl[2 * q + 1] = pack_bf16(s2 - k2, s3 - k3);
-        }
-        tmem_st16(tq + TT_DH + 16 * hh, dh);
-        tmem_st16(tq + TT_DL + 16 * hh, dl);
-        tmem_st16(tq + TT_DSH + 16 * hh, sh);
-        tmem_st16(tq + TT_DSL + 16 * hh, sl);
-      }
-      tmem_wait_st();
+      delta_half(tq, hs, ED, row, 0);
+      delta_half(tq, hs, ED, row, 1);
       tc_fence_before();
       named_sync(1, 128);
 
       // ---- S <- e^{g_last} S + delta~^T K (accumulated onto the pre-scaled S) ----
       if (tid == 0) {
-        mbar_arrive_remote(rb_he_u);    // U slot may be refilled
-        mbar_arrive(&bars[SB_DR]);      // delta of chunk j is in TMEM
+        mbar_arrive_remote(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE_U + slot)), 0));
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
@@ -652,6 +702,7 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
           mma_bf16_ta(tmem + TT_S, tmem + TT_DSL + 8 * kk, kb, id, 1);
         }
         mma_commit(&bars[SB_DS]);
+        mbar_arrive(&bars[SB_DR]);  // after the state update is queued on the tensor pipe
       }
       CH_WAIT(&bars[SB_DS], j & 1, false);
       tc_fence_after();
@@ -661,7 +712,7 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
       float gam = 1.f;
       if (!last) {
         CH_WAIT(&bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1, false);
-        gam = der_all[((j + 1) % ST_NST) * 192 + 64 + 63];
+        gam = der_all[((j + 1) % ST_NST) * ST_DER_STAGE + 64 + 63];
       }
       // ---- new state: bf16 copy for the next chunk, pre-scaled fp32 back to TMEM ----
 #pragma unroll 1
@@ -698,7 +749,6 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
 
   // ========================= aux: P, S Q^T, delta^T P^T, outputs =========================
   const int atid = tid - 128;
-  __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + ST_OST);
 #define AX_WAIT(bar, par)                                                      \
   {                                                                            \
     const bool ok_ = wait_bar((bar), (par), abort_flag, false);                \
@@ -707,11 +757,13 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
   for (int j = 0; j < u.nc; ++j) {
     const int s = j % ST_NST;
     uint8_t* stg = sm + ST_QK + s * ST_STAGE;
-    const float* G = der_all + s * 192;
+    const float* G = der_all + s * ST_DER_STAGE;
     const float* EG = G + 64;
+    const float* EN = G + 192;
     const long long c0 = (long long)j * kC;
     const int lc = (int)min((long long)kC, u.len - c0);
     AX_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
+    const bool factored = flags[s] != 0;
 
     // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T) ----
     if (atid == 0) {
@@ -726,7 +778,7 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
     tc_fence_after();
     if (q4 < 2) {
       const int t = row;
-      const float gt = G[t];
+      const float gt = G[t], egt = EG[t];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
@@ -734,15 +786,22 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float4 ga = ld4(G + 32 * hh + 8 * q), gb = ld4(G + 32 * hh + 8 * q + 4);
-          const float gc[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+          const int jc0 = 32 * hh + 8 * q;
           float v[8];
+          if (factored) {
+            const float4 na = ld4(EN + jc0), nb4 = ld4(EN + jc0 + 4);
+            const float en[8] = {na.x, na.y, na.z, na.w, nb4.x, nb4.y, nb4.z, nb4.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int jc = 32 * hh + 8 * q + e;
-            v[e] = (jc <= t) ? ex2(gt - gc[e]) * __uint_as_float(r[8 * q + e]) : 0.f;
+            for (int e = 0; e < 8; ++e)
+              v[e] = (jc0 + e <= t) ? egt * __uint_as_float(r[8 * q + e]) * en[e] : 0.f;
+          } else {
+            const float4 ga = ld4(G + jc0), gb = ld4(G + jc0 + 4);
+            const float gc[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              v[e] = (jc0 + e <= t) ? ex2(gt - gc[e]) * __uint_as_float(r[8 * q + e]) : 0.f;
           }
-          st_sw128_8_split(sm + ST_PH, sm + ST_PL, t, 32 * hh + 8 * q, 64, v);
+          st_sw128_8_split(sm + ST_PH, sm + ST_PL, t, jc0, 64, v);
         }
       }
     }
@@ -750,8 +809,9 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
     tc_fence_before();
     named_sync(2, 128);
 
-    // ---- S Q^T once the chain has written S of chunk j ----
+    // ---- S Q^T once the chain has written S of chunk j and its S W~^T is done ----
     AX_WAIT(&bars[SB_SBR], j & 1);
+    AX_WAIT(&bars[SB_C], j & 1);
     if (atid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 64, 0, 0);
@@ -760,7 +820,7 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
         mma_bf16(tmem + TT_SQ, desc_k(sm + ST_SB, kk, 16384), desc_k(stg, kk, 16384), id, kk > 0);
       mma_commit(&bars[SB_SQ]);
     }
-    // ---- delta^T P^T once the chain has delta of chunk j ----
+    // ---- delta^T P^T once the chain has delta of chunk j (and queued its update) ----
     AX_WAIT(&bars[SB_DR], j & 1);
     if (atid == 0) {
       tc_fence_after();
@@ -778,9 +838,12 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
     AX_WAIT(&bars[SB_DP], j & 1);
     tc_fence_after();
 
-    // ---- o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t, staged, then coalesced rows ----
+    // ---- o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t, staged in the dead Q rows ----
+    __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(stg);          // rows 0..31
+    __nv_bfloat16* ost1 = reinterpret_cast<__nv_bfloat16*>(stg + 16384);  // rows 32..63
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
+      __nv_bfloat16* ost = hh ? ost1 : ost0;
       uint32_t a[32], b[32];
       tmem_ld32(tq + TT_SQ + 32 * hh, a);
       tmem_ld32(tq + TT_DP + 32 * hh, b);
@@ -791,9 +854,9 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
         const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int t = 32 * hh + 4 * q + e;
-          ost[t * kD + row] = __float2bfloat16_rn(
-              fmaf(ev[e], __uint_as_float(a[4 * q + e]), __uint_as_float(b[4 * q + e])));
+          const int tl = 4 * q + e;  // row within this half
+          ost[tl * kD + row] = __float2bfloat16_rn(
+              fmaf(ev[e], __uint_as_float(a[tl]), __uint_as_float(b[tl])));
         }
       }
     }
@@ -806,13 +869,14 @@ __device__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
         const int it = it0 + atid;
         const int t = it >> 4, ch = it & 15;
         if (t < lc) {
-          const uint4 v = *reinterpret_cast<const uint4*>(ost + t * kD + 8 * ch);
+          const __nv_bfloat16* src = (t < 32 ? ost0 + t * kD : ost1 + (t - 32) * kD) + 8 * ch;
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
           *reinterpret_cast<uint4*>(out + (obase + (size_t)t * H) * kD + 8 * ch) = v;
         }
       }
     }
     named_sync(2, 128);
-    // Q, K and the gate factors of this stage are no longer read by aux
+    // Q, K, the staged outputs and the gate factors of this stage are no longer read
     if (atid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);
   }
 #undef AX_WAIT
@@ -861,8 +925,10 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       mbar_init(&b[WB_MMA + 0], 1);
       mbar_init(&b[WB_MMA + 1], 1);
-      mbar_init(&b[WB_HE_W], 1);
-      mbar_init(&b[WB_HE_U], 1);
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(&b[WB_HE_W + k], 1);
+        mbar_init(&b[WB_HE_U + k], 1);
+      }
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
     } else {
@@ -890,7 +956,14 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && tid == 0) atomicOr(&g_tc_status, *abort_flag);
+  if (*abort_flag) {
+    // after a wait gave up, let any remote stores or copies still in flight land
+    // before either CTA can pass the final cluster barrier
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) {
+    }
+    if (tid == 0) atomicOr(&g_tc_status, *abort_flag);
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);

@@ -315,3 +315,18 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t nthreads, bo
 }
 }  // namespace ptx
 }  // namespace gdn
+
+namespace gdn {
+namespace ptx {
+// Asynchronous 16-byte store into another CTA's shared memory; completes 16 bytes
+// of transaction count on the remote mbarrier `bar_cluster`.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint32_t a, uint32_t b,
+                                            uint32_t c, uint32_t d, uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(dst_cluster),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
+      : "memory");
+}
+}  // namespace ptx
+}  // namespace gdn
