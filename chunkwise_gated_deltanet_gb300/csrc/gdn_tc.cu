@@ -63,10 +63,10 @@ constexpr int kThreads = 288;  // 2 warpgroups + 1 producer warp, in both CTAs
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 // ---- CTA 0 ("WY") shared memory ----
-constexpr int WY_KV = 0;                 // 3 stages x 32 KB: K p0 | K p1 | V p0 | V p1 (8 KB each)
-constexpr int WY_STAGE = 32768;
+constexpr int WY_KV = 0;                 // 3 stages x 16 KB: K p0 | K p1 (8 KB each)
+constexpr int WY_STAGE = 16384;
 constexpr int WY_NST = 3;
-constexpr int WY_SCR = 98304;            // per-warpgroup scratch
+constexpr int WY_SCR = WY_NST * WY_STAGE;  // 49152: per-warpgroup scratch
 constexpr int WY_SCR_BYTES = 53248;
 //   A/T fp32 [64][68] @0 | X fp32 [3][256] @17408 | Tw hi @20480 | Tw lo @28672
 //   | Tu hi @36864 | Tu lo @45056
@@ -80,12 +80,13 @@ constexpr int WY_MISC = WY_BAR + 128;
 constexpr int WY_USED = WY_MISC + 64;
 
 // ---- CTA 1 ("state") shared memory ----
-constexpr int ST_QK = 0;                 // 2 stages x 32 KB; per dk panel p: Q rows (8 KB), K rows (8 KB)
-constexpr int ST_STAGE = 32768;
+constexpr int ST_QK = 0;                 // 2 stages x 48 KB: per dk panel p (16 KB): Q rows, K rows
+constexpr int ST_STAGE = 49152;          //   (8 KB each); then V p0 @32 KB, V p1 @40 KB
+constexpr int ST_V = 32768;
 constexpr int ST_NST = 2;
-constexpr int ST_HS = 65536;             // 2 handoff slots of 48 KB each:
-constexpr int HS_BYTES = 49152;          //   -W~^T bf16 [128 dk][64 tok] (MN-major B) @0,
-constexpr int HS_UH = 16384, HS_UL = 32768;  // U^T hi, lo bf16 [128 dv][64 tok] (swizzled rows)
+constexpr int ST_HS = ST_NST * ST_STAGE;  // 98304: 2 handoff slots of 32 KB each:
+constexpr int HS_BYTES = 32768;          //   -W~^T bf16 [128 dk][64 tok] (MN-major B) @0,
+constexpr int HS_TUH = 16384, HS_TUL = 24576;  // T diag(beta) hi, lo bf16 [64][64] (K-major B)
 constexpr int ST_PH = ST_HS + 2 * HS_BYTES;  // 163840: P hi bf16 [64 t][64 j], K-major B operand
 constexpr int ST_PL = ST_PH + 8192;      // P lo
 constexpr int ST_SB = ST_PL + 8192;      // 180224: S bf16 [128 dv][128 dk], 2 K panels
@@ -109,15 +110,15 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr float kMaxFactoredDecayLog2 = 80.f;
 
 // barrier slots (8 bytes each)
-enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE_W = 8, WB_HE_U = 10 };
+enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE = 8 };
 enum StBar {
-  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF_W = 4, SB_HF_U = 6, SB_C = 8, SB_DS = 9, SB_QKM = 10,
-  SB_SQ = 11, SB_DP = 12, SB_SBR = 13, SB_DR = 14
+  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF = 4, SB_C = 6, SB_DS = 7, SB_QKM = 8, SB_SQ = 9,
+  SB_DP = 10, SB_SBR = 11, SB_DR = 12
 };
 
-// TMEM columns.  WY: per warpgroup w at 192*w: K K^T 0, W~^T 64, U^T 128.
-constexpr uint32_t WT_KK = 0, WT_W = 64, WT_U = 128, WT_WG = 192;
-// state: S 0..127, SW 128, SQ 192, DP 256, QK 320, delta hi 384, delta lo 416,
+// TMEM columns.  WY: per warpgroup w at 128*w: K K^T 0, W~^T 64.
+constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
+// state: S 0..127, U^T + S(-W~^T) 128, SQ 192, DP 256, QK 320, delta hi 384, delta lo 416,
 // delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
 constexpr uint32_t TT_S = 0, TT_SW = 128, TT_SQ = 192, TT_DP = 256, TT_QK = 320, TT_DH = 384,
                    TT_DL = 416, TT_DSH = 448, TT_DSL = 480;
@@ -153,8 +154,6 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
   lo = pack_bf16(x0 - h0, x1 - h1);
 }
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ void st_sw128_8_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
                                                  int col, int rows, const float* v) {
   uint32_t h[4], l[4];
@@ -246,7 +245,7 @@ __device__ __forceinline__ void scan_gates(const GateLoad& in, int lane, float& 
 }
 
 // ============================================================ CTA 0: WY ======
-__device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+__device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k,
                        const float* __restrict__ log_alpha, const float* __restrict__ beta,
                        const Unit& u, int H, volatile int* abort_flag) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -268,11 +267,9 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       uint8_t* st = sm + WY_KV + s * WY_STAGE;
       const int r = (int)(u.row0 + (long long)j * kC);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[WB_KV_FULL + s], 4 * 8192);
+        mbar_arrive_expect_tx(&bars[WB_KV_FULL + s], 2 * 8192);
         tma_load_3d(st, tm_k, &bars[WB_KV_FULL + s], 0, u.h, r);
         tma_load_3d(st + 8192, tm_k, &bars[WB_KV_FULL + s], 64, u.h, r);
-        tma_load_3d(st + 16384, tm_v, &bars[WB_KV_FULL + s], 0, u.h, r);
-        tma_load_3d(st + 24576, tm_v, &bars[WB_KV_FULL + s], 64, u.h, r);
       }
       issued = j + 1;
       float g0, g1, tot;
@@ -462,67 +459,52 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     tc_fence_before();
     named_sync(nb, 128);
 
-    // ---- W~^T = K^T Tw^T and U^T = V^T Tu^T (hi + lo) ----
+    // ---- W~^T = K^T Tw^T (hi + lo); U is formed by the state CTA from Tu ----
     if (wtid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 64, 1, 0);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t ak = desc_mn(st, kk, 8192);
-        const uint64_t av = desc_mn(st + 16384, kk, 8192);
         mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWH, kk, 8192), id, kk > 0);
         mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWL, kk, 8192), id, 1);
-        mma_bf16(tw + WT_U, av, desc_k(scr + SC_TUH, kk, 8192), id, kk > 0);
-        mma_bf16(tw + WT_U, av, desc_k(scr + SC_TUL, kk, 8192), id, 1);
       }
       mma_commit(&bars[WB_MMA + w]);
     }
     WY_WAIT(&bars[WB_MMA + w], mph, false);
     mph ^= 1;
     tc_fence_after();
-    if (wtid == 0) mbar_arrive(&bars[WB_KV_EMPTY + s]);  // K, V of this stage are consumed
+    if (wtid == 0) mbar_arrive(&bars[WB_KV_EMPTY + s]);  // K of this stage is consumed
 
-    // ---- hand chunk j to the state CTA: stage in scratch, bulk-copy into slot j % 2 ----
+    // ---- hand chunk j to the state CTA (slot j % 2): -W~^T staged at scratch 0, and
+    //      Tu hi / lo straight from scratch (they already have the slot's layout) ----
     const int slot = j & 1;
     const uint32_t huse = (uint32_t)(j >> 1);
-    {
-      // -W~^T bf16 [128 dk][64 tok] at scratch 0, U^T hi / lo bf16 [128 dv][64 tok] at
-      // 16 KB / 32 KB: the slot's layout, so one bulk copy moves each part.
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t rw[32], ru[32];
-        tmem_ld32(tq + WT_W + 32 * hh, rw);
-        tmem_ld32(tq + WT_U + 32 * hh, ru);
-        tmem_wait_ld();
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t rw[32];
+      tmem_ld32(tq + WT_W + 32 * hh, rw);
+      tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t off = sw128_offset(row, 32 * hh + 8 * q, 128);
-          uint32_t wv[4], uh[4], ul[4];
+      for (int q = 0; q < 4; ++q) {
+        uint32_t wv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            wv[e] = pack_bf16(-__uint_as_float(rw[8 * q + 2 * e]),
-                              -__uint_as_float(rw[8 * q + 2 * e + 1]));
-            split2(__uint_as_float(ru[8 * q + 2 * e]), __uint_as_float(ru[8 * q + 2 * e + 1]),
-                   uh[e], ul[e]);
-          }
-          st_shared_v4(smem_u32(scr + off), wv[0], wv[1], wv[2], wv[3]);
-          st_shared_v4(smem_u32(scr + HS_UH + off), uh[0], uh[1], uh[2], uh[3]);
-          st_shared_v4(smem_u32(scr + HS_UL + off), ul[0], ul[1], ul[2], ul[3]);
-        }
+        for (int e = 0; e < 4; ++e)
+          wv[e] = pack_bf16(-__uint_as_float(rw[8 * q + 2 * e]),
+                            -__uint_as_float(rw[8 * q + 2 * e + 1]));
+        st_shared_v4(smem_u32(scr + sw128_offset(row, 32 * hh + 8 * q, 128)), wv[0], wv[1], wv[2],
+                     wv[3]);
       }
     }
     fence_async_smem();
     tc_fence_before();
-    WY_WAIT(&bars[WB_HE_W + slot], (huse & 1) ^ 1, true);
-    WY_WAIT(&bars[WB_HE_U + slot], (huse & 1) ^ 1, true);
+    WY_WAIT(&bars[WB_HE + slot], (huse & 1) ^ 1, true);
     if (wtid == 0) {
-      const uint32_t rb_w = map_shared(smem_u32(sm + ST_BAR + 8 * (SB_HF_W + slot)), 1);
-      const uint32_t rb_u = map_shared(smem_u32(sm + ST_BAR + 8 * (SB_HF_U + slot)), 1);
+      const uint32_t rb = map_shared(smem_u32(sm + ST_BAR + 8 * (SB_HF + slot)), 1);
       const uint32_t rs = map_shared(smem_u32(sm + ST_HS + slot * HS_BYTES), 1);
-      mbar_arrive_expect_tx_remote(rb_w, 16384);
-      bulk_copy_to_cluster(rs, scr, 16384, rb_w);
-      mbar_arrive_expect_tx_remote(rb_u, 32768);
-      bulk_copy_to_cluster(rs + HS_UH, scr + HS_UH, 32768, rb_u);
+      mbar_arrive_expect_tx_remote(rb, HS_BYTES);
+      bulk_copy_to_cluster(rs, scr, 16384, rb);
+      bulk_copy_to_cluster(rs + HS_TUH, scr + SC_TUH, 16384, rb);
       bulk_commit();
     }
   }
@@ -531,26 +513,22 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
 }
 
 // One half (tokens 32*hh .. 32*hh + 31) of the delta epilogue of the state CTA:
-// delta^T = SW + U^T (U^T arrives as hi + lo bf16), delta~ = delta e^{g_last - g};
-// both written to TMEM as hi / lo bf16 pairs (the A operands of the next MMAs).
-__device__ __forceinline__ void delta_half(uint32_t tq, const uint8_t* hs, const float* ED, int row,
-                                           int hh) {
+// the accumulator already holds delta^T = U^T + S(-W~^T); write delta and
+// delta~ = delta e^{g_last - g} to TMEM as hi / lo bf16 pairs (the A operands of
+// the next MMAs).
+__device__ __forceinline__ void delta_half(uint32_t tq, const float* ED, int hh) {
   uint32_t r[32];
   tmem_ld32(tq + TT_SW + 32 * hh, r);
   tmem_wait_ld();
   uint32_t dh[16], dl[16], sh[16], sl[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint32_t off = sw128_offset(row, 32 * hh + 8 * q, 128);
-    const uint4 uh = *reinterpret_cast<const uint4*>(hs + HS_UH + off);
-    const uint4 ul = *reinterpret_cast<const uint4*>(hs + HS_UL + off);
-    const uint32_t uhw[4] = {uh.x, uh.y, uh.z, uh.w}, ulw[4] = {ul.x, ul.y, ul.z, ul.w};
     const float4 ea = ld4(ED + 32 * hh + 8 * q), eb = ld4(ED + 32 * hh + 8 * q + 4);
     const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float d0 = __uint_as_float(r[8 * q + 2 * e]) + bf16_lo(uhw[e]) + bf16_lo(ulw[e]);
-      const float d1 = __uint_as_float(r[8 * q + 2 * e + 1]) + bf16_hi(uhw[e]) + bf16_hi(ulw[e]);
+      const float d0 = __uint_as_float(r[8 * q + 2 * e]);
+      const float d1 = __uint_as_float(r[8 * q + 2 * e + 1]);
       split2(d0, d1, dh[4 * q + e], dl[4 * q + e]);
       split2(d0 * ev[2 * e], d1 * ev[2 * e + 1], sh[4 * q + e], sl[4 * q + e]);
     }
@@ -564,7 +542,8 @@ __device__ __forceinline__ void delta_half(uint32_t tq, const uint8_t* hs, const
 
 // ========================================================= CTA 1: state ======
 __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
-                          const CUtensorMap* tm_k, const float* __restrict__ log_alpha,
+                          const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                          const float* __restrict__ log_alpha,
                           const float* __restrict__ beta, const float* __restrict__ S0,
                           __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
                           const Unit& u, int H, volatile int* abort_flag) {
@@ -587,11 +566,13 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       uint8_t* st = sm + ST_QK + s * ST_STAGE;
       const int r = (int)(u.row0 + (long long)j * kC);
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[SB_QK_FULL + s], 4 * 8192);
+        mbar_arrive_expect_tx(&bars[SB_QK_FULL + s], 6 * 8192);
         tma_load_3d(st, tm_q, &bars[SB_QK_FULL + s], 0, u.h, r);
         tma_load_3d(st + 8192, tm_k, &bars[SB_QK_FULL + s], 0, u.h, r);
         tma_load_3d(st + 16384, tm_q, &bars[SB_QK_FULL + s], 64, u.h, r);
         tma_load_3d(st + 24576, tm_k, &bars[SB_QK_FULL + s], 64, u.h, r);
+        tma_load_3d(st + ST_V, tm_v, &bars[SB_QK_FULL + s], 0, u.h, r);
+        tma_load_3d(st + ST_V + 8192, tm_v, &bars[SB_QK_FULL + s], 64, u.h, r);
       }
       issued = j + 1;
       float g0, g1, tot;
@@ -668,31 +649,36 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       const uint32_t huse = (uint32_t)(j >> 1);
       uint8_t* hs = sm + ST_HS + slot * HS_BYTES;
 
-      // ---- SW = S (-W~^T) ----
-      CH_WAIT(&bars[SB_HF_W + slot], huse & 1, true);
+      // ---- delta^T = U^T + S (-W~^T): U^T = V^T Tu^T (hi + lo), then S W~^T onto it ----
+      CH_WAIT(&bars[SB_HF + slot], huse & 1, true);
       if (tid == 0) {
         tc_fence_after();
+        const uint32_t id_u = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t av = desc_mn(stg + ST_V, kk, 8192);
+          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUH, kk, 8192), id_u, kk > 0);
+          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUL, kk, 8192), id_u, 1);
+        }
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(hs, kk, 16384), id, kk > 0);
+          mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(hs, kk, 16384), id, 1);
         mma_commit(&bars[SB_C]);
       }
       CH_WAIT(&bars[SB_C], j & 1, false);
       tc_fence_after();
-      if (tid == 0) mbar_arrive_remote(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE_W + slot)), 0));
-      CH_WAIT(&bars[SB_HF_U + slot], huse & 1, true);
+      if (tid == 0) mbar_arrive_remote(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + slot)), 0));
       if (j > 0) CH_WAIT(&bars[SB_DP], (j - 1) & 1, false);  // delta of j-1 no longer read
 
-      // ---- delta^T = U^T + SW, and the decayed copy; hi/lo into TMEM ----
-      delta_half(tq, hs, ED, row, 0);
-      delta_half(tq, hs, ED, row, 1);
+      // ---- delta and its decayed copy as hi/lo bf16 A operands in TMEM ----
+      delta_half(tq, ED, 0);
+      delta_half(tq, ED, 1);
       tc_fence_before();
       named_sync(1, 128);
 
       // ---- S <- e^{g_last} S + delta~^T K (accumulated onto the pre-scaled S) ----
       if (tid == 0) {
-        mbar_arrive_remote(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE_U + slot)), 0));
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
@@ -706,7 +692,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       }
       CH_WAIT(&bars[SB_DS], j & 1, false);
       tc_fence_after();
-      if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // chain is done with K of this stage
+      if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // chain is done with K, V of this stage
       CH_WAIT(&bars[SB_SQ], j & 1, false);                 // S Q^T of chunk j has read S
       const bool last = (j + 1 == u.nc);
       float gam = 1.f;
@@ -925,21 +911,18 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       mbar_init(&b[WB_MMA + 0], 1);
       mbar_init(&b[WB_MMA + 1], 1);
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(&b[WB_HE_W + k], 1);
-        mbar_init(&b[WB_HE_U + k], 1);
-      }
+      for (int k = 0; k < 2; ++k) mbar_init(&b[WB_HE + k], 1);
       prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
     } else {
       uint64_t* b = reinterpret_cast<uint64_t*>(sm + ST_BAR);
       for (int s = 0; s < ST_NST; ++s) {
         mbar_init(&b[SB_QK_FULL + s], 2);
         mbar_init(&b[SB_QK_EMPTY + s], 2);
       }
-      for (int k = SB_HF_W; k <= SB_DR; ++k) mbar_init(&b[k], 1);
+      for (int k = SB_HF; k <= SB_DR; ++k) mbar_init(&b[k], 1);
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
     }
     fence_mbarrier_init();
   }
@@ -950,9 +933,9 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy
 
   if (rank == 0)
-    run_wy(sm, tmem, &tm_k, &tm_v, log_alpha, beta, u, H, abort_flag);
+    run_wy(sm, tmem, &tm_k, log_alpha, beta, u, H, abort_flag);
   else
-    run_state(sm, tmem, &tm_q, &tm_k, log_alpha, beta, S0, out, S_final, u, H, abort_flag);
+    run_state(sm, tmem, &tm_q, &tm_k, &tm_v, log_alpha, beta, S0, out, S_final, u, H, abort_flag);
 
   tc_fence_before();
   __syncthreads();
