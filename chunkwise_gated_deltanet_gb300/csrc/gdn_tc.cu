@@ -7,17 +7,26 @@
 // the running state and the part that does (myhz0606, "DeltaNet的Chunkwise
 // Form推导", section 4.5: W and U depend only on the chunk's own k, v, beta):
 //
-// CTA 0, "WY" (two warpgroups on alternating chunks, one TMA producer warp):
+// CTA 0, "WY" (three warpgroups on chunks j = w mod 3, one TMA producer warp):
 //   K K^T                    tcgen05, M=128 (rows 64..127 unused)
 //   A = strictly-lower(beta_i e^{g_i-g_j} k_i.k_j)          fp32 epilogue
 //   T = (I + A)^{-1}         16x16 diagonal blocks, then block rows, fp32
-//   W~^T = K^T (T diag(beta e^g))^T, U^T = V^T (T diag(beta))^T   tcgen05
-//   -W~^T (bf16) and U^T (fp32) go to CTA 1 by DSMEM bulk copies.
-// CTA 1, "state" (chain warpgroup, aux warpgroup, one TMA producer warp):
-//   chain: SW = S (-W~^T); delta^T = U^T + SW; S <- e^{g_last} S + delta~^T K
-//          (S accumulates in TMEM; delta feeds the MMAs from TMEM)
-//   aux:   Q K^T -> P = lower(e^{g_t-g_j} q_t.k_j); S Q^T; delta^T P^T;
-//          o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t -> out
+//   W~^T = K^T (T diag(beta e^g))^T                        tcgen05
+//   -W~^T (bf16) and T diag(beta) (hi/lo bf16) go to CTA 1 by DSMEM bulk copies,
+//   in chunk order, into two hand-off slots.
+// CTA 1, "state" (three warpgroups, a TMA producer warp and an MMA warp):
+//   chain (serial):  SW = U^T + S (-W~^T) = delta^T;  S <- e^{g_last} S + delta~^T K
+//                    (S accumulates in TMEM; delta feeds the MMAs from TMEM)
+//   MMA warp:        U^T = V^T (T diag(beta))^T into SW ahead of the chain;
+//                    O = S Q^T, then O += delta^T P^T (one accumulator per chunk
+//                    parity, so the outputs of chunk j drain while j+1 runs)
+//   aux P (ahead):   Q K^T -> P' = lower(q_t.k_j e^{-g_j}) (factored decay), or
+//                    P = lower(q_t.k_j e^{g_t-g_j}) and Q <- diag(e^g) Q in place
+//   aux O (behind):  o_t = e^{g_t} O_t (factored) or O_t -> out
+// The factored form keeps the output accumulator in the frame of e^{-g_t}: the
+// state part S q_t and every in-chunk term e^{-g_j} (q_t.k_j) delta_j share that
+// factor, which aux O multiplies back.  It is used when the chunk's total decay
+// e^{g_last} is above 2^-80, so that e^{-g_j} stays inside the fp32 range.
 //
 // W~ uses the decayed triangular factor (W~_i = gamma_i w_i with the WY
 // recursion of Nyysyyan's "Gated-DeltaNet" section); then
@@ -28,19 +37,26 @@
 // (delta~ = delta diag(e^{g_last-g})) and P are carried as two bf16 terms
 // (hi = bf16(x), lo = bf16(x - hi)) and multiplied as hi*hi + hi*lo + lo*hi, or
 // hi + lo against an exact bf16 operand (K, V).  S and W~ are single bf16
-// operands; the running state itself stays fp32 (in TMEM).
+// operands (and Q scaled by e^{g} in the strong-decay form); the running state
+// itself stays fp32 (in TMEM).
 //
 // Synchronisation (mbarriers; "phase j" completes once per chunk j):
 //   WY:    kv_full[s]  (TMA bytes + producer arrive)   kv_empty[s] (WG after its MMAs)
 //          wg_mma[w]   (MMA commits of warpgroup w)
-//          hand_empty_w/_u (arrived by CTA 1 when it no longer needs chunk j's W~ / U)
-//   state: qk_full[s], qk_empty[s] (chain + aux), hand_full_w/_u (bulk-copy bytes),
-//          bar_c, bar_ds (chain MMA commits), bar_qk, bar_sq, bar_dp (aux MMA commits),
-//          sb_ready (bf16 S of chunk j written), delta_ready (delta of chunk j in TMEM)
+//          hand_empty[b] (arrived by CTA 1 once chunk j's slot has been read)
+//   state: qk_full[s]; qk_empty[s] (chain after its state update + aux O after its
+//          copy-out); hand_full[b] (bulk-copy bytes); bar_u, bar_sq, bar_dp[b] (MMA warp
+//          commits); bar_c, bar_ds (chain commits); sw_issued, delta_ready (chain
+//          arrives); p_full[b] (aux P); o_empty[b] (aux O); bar_qk (aux P's commit)
 // "Empty" barriers are waited with parity ^ 1 so that their first wait passes.
 // Every wait is bounded; a wait that gives up records a code in a device status
 // word, every role of both CTAs leaves its loop, and both CTAs still meet at the
 // final cluster barrier.
+//
+// Instruction footprint matters here: with every SM of a GPC running this
+// kernel, instruction-cache misses queue at the GPC level, so the per-chunk
+// loops favour rolled loops and one out-of-line polling routine over unrolled
+// code.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -59,7 +75,9 @@ using namespace ptx;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kThreads = 288;  // 2 warpgroups + 1 producer warp, in both CTAs
+constexpr int kThreads = 448;  // 3 warpgroups, a TMA producer warp and (state CTA) an MMA warp
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 // ---- CTA 0 ("WY") shared memory ----
@@ -68,11 +86,12 @@ constexpr int WY_STAGE = 16384;
 constexpr int WY_NST = 3;
 constexpr int WY_SCR = WY_NST * WY_STAGE;  // 49152: per-warpgroup scratch
 constexpr int WY_SCR_BYTES = 53248;
+constexpr int WY_NWG = 3;                  // warpgroup w takes chunks j = w (mod 3), stage w
 //   A/T fp32 [64][68] @0 | X fp32 [3][256] @17408 | Tw hi @20480 | Tw lo @28672
 //   | Tu hi @36864 | Tu lo @45056
 constexpr int LDA = 68;
 constexpr int SC_X = 17408, SC_TWH = 20480, SC_TWL = 28672, SC_TUH = 36864, SC_TUL = 45056;
-constexpr int WY_DER = WY_SCR + 2 * WY_SCR_BYTES;  // [3 stages][G, EG, BG, BE, EN][64] fp32
+constexpr int WY_DER = WY_SCR + WY_NWG * WY_SCR_BYTES;  // [3 stages][G, EG, BG, BE, EN][64] fp32
 constexpr int WY_DER_STAGE = 5 * 64;                // floats per stage
 constexpr int WY_FLAG = WY_DER + WY_NST * WY_DER_STAGE * 4;  // [3] int: factored decay allowed
 constexpr int WY_BAR = WY_FLAG + 64;
@@ -87,11 +106,11 @@ constexpr int ST_NST = 2;
 constexpr int ST_HS = ST_NST * ST_STAGE;  // 98304: 2 handoff slots of 32 KB each:
 constexpr int HS_BYTES = 32768;          //   -W~^T bf16 [128 dk][64 tok] (MN-major B) @0,
 constexpr int HS_TUH = 16384, HS_TUL = 24576;  // T diag(beta) hi, lo bf16 [64][64] (K-major B)
-constexpr int ST_PH = ST_HS + 2 * HS_BYTES;  // 163840: P hi bf16 [64 t][64 j], K-major B operand
-constexpr int ST_PL = ST_PH + 8192;      // P lo
-constexpr int ST_SB = ST_PL + 8192;      // 180224: S bf16 [128 dv][128 dk], 2 K panels
-constexpr int ST_DER = ST_SB + 32768;    // [2 stages][G, EG, ED, EN][64] fp32
-constexpr int ST_DER_STAGE = 4 * 64;
+constexpr int ST_PS = ST_HS + 2 * HS_BYTES;  // 163840: 2 P slots of 16 KB: hi @0, lo @8 KB,
+constexpr int PS_BYTES = 16384;          //   bf16 [64 t][64 j], K-major B operand
+constexpr int ST_SB = ST_PS + 2 * PS_BYTES;  // 196608: S bf16 [128 dv][128 dk], 2 K panels
+constexpr int ST_DER = ST_SB + 32768;    // [2 stages][GN, EG, ED][64] fp32 (GN: e^{-g}, or g)
+constexpr int ST_DER_STAGE = 3 * 64;
 constexpr int ST_FLAG = ST_DER + ST_NST * ST_DER_STAGE * 4;  // [2] int
 constexpr int ST_BAR = ST_FLAG + 64;
 constexpr int ST_MISC = ST_BAR + 160;
@@ -102,6 +121,7 @@ constexpr int ST_USED = ST_MISC + 64;
 constexpr int SMEM_USED = WY_USED > ST_USED ? WY_USED : ST_USED;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SC_TUL + 8192 <= WY_SCR_BYTES, "WY scratch");
+static_assert(WY_NWG == WY_NST, "one K stage per WY warpgroup");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // The factored decay e^{g_i} e^{-g_j} replaces e^{g_i - g_j} when the chunk's
@@ -110,18 +130,20 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr float kMaxFactoredDecayLog2 = 80.f;
 
 // barrier slots (8 bytes each)
-enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE = 8 };
+enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE = 9, WB_COUNT = 11 };
+static_assert(WB_COUNT * 8 <= WY_MISC - WY_BAR, "WY barriers");
 enum StBar {
-  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF = 4, SB_C = 6, SB_DS = 7, SB_QKM = 8, SB_SQ = 9,
-  SB_DP = 10, SB_SBR = 11, SB_DR = 12
+  SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF = 4, SB_C = 6, SB_DS = 7, SB_QKM = 8, SB_DP = 9,
+  SB_PF = 11, SB_OE = 13, SB_U = 15, SB_DR = 16, SB_SWI = 17, SB_SQ = 18, SB_COUNT = 19
 };
+static_assert(SB_COUNT * 8 <= ST_MISC - ST_BAR, "state barriers");
 
 // TMEM columns.  WY: per warpgroup w at 128*w: K K^T 0, W~^T 64.
 constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
-// state: S 0..127, U^T + S(-W~^T) 128, SQ 192, DP 256, QK 320, delta hi 384, delta lo 416,
-// delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
-constexpr uint32_t TT_S = 0, TT_SW = 128, TT_SQ = 192, TT_DP = 256, TT_QK = 320, TT_DH = 384,
-                   TT_DL = 416, TT_DSH = 448, TT_DSL = 480;
+// state: S 0..127, U^T + S(-W~^T) 128, outputs of chunk j at 192 + 64 (j % 2), QK 320,
+// delta hi 384, delta lo 416, delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
+constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_QK = 320, TT_DH = 384, TT_DL = 416,
+                   TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
 
 constexpr int ST_WAIT = 1;
@@ -177,13 +199,34 @@ __device__ __forceinline__ void st4(float* p, float a, float b, float c, float d
 }
 
 // Bounded parity wait that also gives up when another role of this CTA already
-// gave up.  Returns false on timeout (recording `code`) or on abort.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         bool cluster_scope) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
+// gave up.  Returns false on timeout (recording `code`) or on abort.  The polling
+// loop is one shared out-of-line function; only the first test is inlined at
+// each call site, which keeps the hot code of every role small.
+__device__ __noinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
+                                           volatile int* abort_flag, bool cluster_scope) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
     const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     if (ok) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      atomicOr((int*)abort_flag, ST_WAIT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         bool cluster_scope) {
+  const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  return ok || wait_bar_poll(bar, parity, abort_flag, cluster_scope);
+}
+
+// Bounded wait until the hand-off ticket reaches `want`; false on timeout or abort.
+__device__ __forceinline__ bool wait_ticket(volatile int* ticket, int want,
+                                            volatile int* abort_flag) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (*ticket == want) return true;
     if (*abort_flag) return false;
     if (it == 0) {
       t0 = globaltimer_ns();
@@ -253,8 +296,8 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
   float* der_all = reinterpret_cast<float*>(sm + WY_DER);
   int* flags = reinterpret_cast<int*>(sm + WY_FLAG);
 
-  if (warp == 8) {
-    // ---------------- producer: K and V tiles by TMA, gate factors ----------------
+  if (warp == kProducerWarp) {
+    // ---------------- producer: K tiles by TMA, gate factors ----------------
     int issued = 0;
     GateLoad next = load_gates(log_alpha, beta, u, H, 0, lane);
     for (int j = 0; j < u.nc; ++j) {
@@ -291,13 +334,15 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       if (j >= 0) (void)mbar_wait(&bars[WB_KV_FULL + j % WY_NST], (j / WY_NST) & 1, 100000000ull);
     return;
   }
+  if (warp >= 4 * WY_NWG) return;
 
-  // ---------------- warpgroups: w = 0 takes even chunks, w = 1 odd chunks ----------------
+  // ---------------- warpgroups: w takes chunks j = w (mod 3) ----------------
   const int w = warp >> 2;
   const int wtid = tid & 127;
   const int q4 = warp & 3;
   const int row = q4 * 32 + lane;
-  const uint32_t nb = 1 + w;  // named barrier of this warpgroup
+  const uint32_t nb = 1 + w;  // named barrier of this warpgroup (1..3); 4 + w: half of it
+  volatile int* ticket = reinterpret_cast<volatile int*>(sm + WY_MISC + 8);
   uint8_t* scr = sm + WY_SCR + w * WY_SCR_BYTES;
   float* Am = reinterpret_cast<float*>(scr);
   float* Xs = reinterpret_cast<float*>(scr + SC_X);
@@ -311,7 +356,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     if (named_sync_or(nb, 128, !ok_ || *abort_flag != 0)) break;               \
   }
 
-  for (int j = w; j < u.nc; j += 2) {
+  for (int j = w; j < u.nc; j += WY_NWG) {
     const int s = j % WY_NST;
     uint8_t* st = sm + WY_KV + s * WY_STAGE;
     const float* G = der_all + s * WY_DER_STAGE;
@@ -325,7 +370,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     if (wtid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
+#pragma unroll 1
       for (int kk = 0; kk < 8; ++kk)
         mma_bf16(tw + WT_KK, desc_k(st, kk, 8192), desc_k(st, kk, 8192), id, kk > 0);
       mma_commit(&bars[WB_MMA + w]);
@@ -341,7 +386,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     if (q4 < 2) {
       const int i = row;
       const float gi = G[i], bi = BE[i], bgi = BG[i];
-#pragma unroll
+#pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[32];
         tmem_ld32(tq + WT_KK + 32 * hh, r);
@@ -381,7 +426,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
         for (int m = 0; m < r; ++m) acc = fmaf(-Ab[r * LDA + m], x[m], acc);
         x[r] = acc;
       }
-      named_sync(3 + w, 64);
+      named_sync(4 + w, 64);
       float* Tb = Am + (16 * b) * LDA + 16 * b + c;
 #pragma unroll
       for (int r = 0; r < 16; ++r) Tb[r * LDA] = x[r];
@@ -435,7 +480,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     }
 
     // ---- T diag(beta e^g), T diag(beta) as bf16 hi/lo B operands ----
-#pragma unroll
+#pragma unroll 1
     for (int it0 = 0; it0 < 512; it0 += 128) {
       const int it = it0 + wtid;
       const int i = it >> 3, jc = (it & 7) * 8;
@@ -463,7 +508,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     if (wtid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 64, 1, 0);
-#pragma unroll
+#pragma unroll 1
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t ak = desc_mn(st, kk, 8192);
         mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWH, kk, 8192), id, kk > 0);
@@ -480,7 +525,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     //      Tu hi / lo straight from scratch (they already have the slot's layout) ----
     const int slot = j & 1;
     const uint32_t huse = (uint32_t)(j >> 1);
-#pragma unroll
+#pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       uint32_t rw[32];
       tmem_ld32(tq + WT_W + 32 * hh, rw);
@@ -498,6 +543,13 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     }
     fence_async_smem();
     tc_fence_before();
+    // Hand-offs leave in chunk order: when chunk j waits for its slot, chunk j - 4 has
+    // been consumed, so the slot's barrier is at most one phase behind and its parity
+    // is unambiguous.
+    {
+      const bool ok_ = (wtid != 0) || wait_ticket(ticket, j, abort_flag);
+      if (named_sync_or(nb, 128, !ok_ || *abort_flag != 0)) break;
+    }
     WY_WAIT(&bars[WB_HE + slot], (huse & 1) ^ 1, true);
     if (wtid == 0) {
       const uint32_t rb = map_shared(smem_u32(sm + ST_BAR + 8 * (SB_HF + slot)), 1);
@@ -506,6 +558,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       bulk_copy_to_cluster(rs, scr, 16384, rb);
       bulk_copy_to_cluster(rs + HS_TUH, scr + SC_TUH, 16384, rb);
       bulk_commit();
+      *ticket = j + 1;
     }
   }
 #undef WY_WAIT
@@ -552,8 +605,8 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   float* der_all = reinterpret_cast<float*>(sm + ST_DER);
   int* flags = reinterpret_cast<int*>(sm + ST_FLAG);
 
-  if (warp == 8) {
-    // ---------------- producer: Q and K tiles by TMA, gate factors ----------------
+  if (warp == kProducerWarp) {
+    // ---------------- producer: Q, K, V tiles by TMA, gate factors ----------------
     int issued = 0;
     GateLoad next = load_gates(log_alpha, beta, u, H, 0, lane);
     for (int j = 0; j < u.nc; ++j) {
@@ -577,12 +630,13 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       issued = j + 1;
       float g0, g1, tot;
       scan_gates(cur, lane, g0, g1, tot);
-      float* der = der_all + s * ST_DER_STAGE;  // G, EG, ED, EN
-      der[lane] = g0;                   der[lane + 32] = g1;
+      const bool factored = -tot < kMaxFactoredDecayLog2;
+      float* der = der_all + s * ST_DER_STAGE;  // GN (e^{-g} or g), EG, ED
+      der[lane] = factored ? ex2(-g0) : g0;
+      der[lane + 32] = factored ? ex2(-g1) : g1;
       der[64 + lane] = ex2(g0);         der[64 + lane + 32] = ex2(g1);
       der[128 + lane] = ex2(tot - g0);  der[128 + lane + 32] = ex2(tot - g1);
-      der[192 + lane] = ex2(-g0);       der[192 + lane + 32] = ex2(-g1);
-      if (lane == 0) flags[s] = (-tot < kMaxFactoredDecayLog2) ? 1 : 0;
+      if (lane == 0) flags[s] = factored ? 1 : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[SB_QK_FULL + s]);
     }
@@ -590,6 +644,69 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       if (j >= 0) (void)mbar_wait(&bars[SB_QK_FULL + j % ST_NST], (j / ST_NST) & 1, 100000000ull);
     return;
   }
+  if (warp == kMmaWarp) {
+    // ------------- MMA warp: the tensor-core work that is not on the chain's path -------------
+    //   U^T = V^T Tu^T into the chain's accumulator once delta of chunk j-1 has left it,
+    //   S Q^T (state part of the outputs) behind the chain's S W~^T,
+    //   delta^T P^T (in-chunk part of the outputs) behind the chain's state update.
+#define MW_WAIT(bar, par, cl) \
+  if (!__all_sync(0xffffffffu, wait_bar((bar), (par), abort_flag, (cl)))) break;
+    for (int j = 0; j < u.nc; ++j) {
+      const int s = j % ST_NST;
+      const int b = j & 1;
+      const uint32_t buse = (uint32_t)(j >> 1);
+      uint8_t* stg = sm + ST_QK + s * ST_STAGE;
+      uint8_t* hs = sm + ST_HS + b * HS_BYTES;
+      const uint8_t* ps = sm + ST_PS + b * PS_BYTES;
+      const uint32_t t_o = tmem + TT_O + 64 * b;
+      MW_WAIT(&bars[SB_HF + b], buse & 1, true);
+      MW_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1, false);
+      if (j > 0) MW_WAIT(&bars[SB_DR], (j - 1) & 1, false);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t id_u = idesc_bf16(128, 64, 1, 0);
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t av = desc_mn(stg + ST_V, kk, 8192);
+          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUH, kk, 8192), id_u, kk > 0);
+          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUL, kk, 8192), id_u, 1);
+        }
+        mma_commit(&bars[SB_U]);
+      }
+      // S Q^T, or S (diag(e^g) Q)^T once aux P has scaled Q when the chunk's decay is
+      // too strong for the factored form
+      const bool factored = flags[s] != 0;
+      MW_WAIT(&bars[SB_SWI], j & 1, false);
+      MW_WAIT(&bars[SB_OE + b], (buse & 1) ^ 1, false);  // outputs of chunk j - 2 read
+      if (!factored) MW_WAIT(&bars[SB_PF + b], buse & 1, false);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t id_q = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(t_o, desc_k(sm + ST_SB, kk, 16384), desc_k(stg, kk, 16384), id_q, kk > 0);
+        mma_commit(&bars[SB_SQ]);
+      }
+      MW_WAIT(&bars[SB_DR], j & 1, false);
+      MW_WAIT(&bars[SB_PF + b], buse & 1, false);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ph = desc_k(ps, kk, 8192), pl = desc_k(ps + 8192, kk, 8192);
+          mma_bf16_ta(t_o, tmem + TT_DH + 8 * kk, ph, id, 1);
+          mma_bf16_ta(t_o, tmem + TT_DH + 8 * kk, pl, id, 1);
+          mma_bf16_ta(t_o, tmem + TT_DL + 8 * kk, ph, id, 1);
+        }
+        mma_commit(&bars[SB_DP + b]);
+      }
+      __syncwarp();
+    }
+#undef MW_WAIT
+    return;
+  }
+  if (warp > kMmaWarp) return;
 
   const int q4 = warp & 3;
   const int row = q4 * 32 + lane;
@@ -638,42 +755,38 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       fence_async_smem();
       tc_fence_before();
       named_sync(1, 128);
-      if (tid == 0 && u.nc > 0) mbar_arrive(&bars[SB_SBR]);  // phase 0: S of chunk 0 ready
     } while (0);
 
     for (int j = 0; alive && j < u.nc; ++j) {
       const int s = j % ST_NST;
       const float* ED = der_all + s * ST_DER_STAGE + 128;
       uint8_t* stg = sm + ST_QK + s * ST_STAGE;
-      const int slot = j & 1;
-      const uint32_t huse = (uint32_t)(j >> 1);
-      uint8_t* hs = sm + ST_HS + slot * HS_BYTES;
+      const int b = j & 1;  // handoff slot, P slot and output accumulator of chunk j
+      const uint32_t buse = (uint32_t)(j >> 1);
+      uint8_t* hs = sm + ST_HS + b * HS_BYTES;
 
-      // ---- delta^T = U^T + S (-W~^T): U^T = V^T Tu^T (hi + lo), then S W~^T onto it ----
-      CH_WAIT(&bars[SB_HF + slot], huse & 1, true);
+      // ---- delta^T = U^T + S (-W~^T): U^T = V^T Tu^T is already in the accumulator
+      //      (issued by the MMA warp) ----
+      CH_WAIT(&bars[SB_U], j & 1, false);
+      CH_WAIT(&bars[SB_HF + b], buse & 1, true);
       if (tid == 0) {
         tc_fence_after();
-        const uint32_t id_u = idesc_bf16(128, 64, 1, 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t av = desc_mn(stg + ST_V, kk, 8192);
-          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUH, kk, 8192), id_u, kk > 0);
-          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUL, kk, 8192), id_u, 1);
-        }
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)
           mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(hs, kk, 16384), id, 1);
         mma_commit(&bars[SB_C]);
+        mbar_arrive(&bars[SB_SWI]);  // S Q^T may now be queued behind S W~^T
       }
       CH_WAIT(&bars[SB_C], j & 1, false);
       tc_fence_after();
-      if (tid == 0) mbar_arrive_remote(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + slot)), 0));
-      if (j > 0) CH_WAIT(&bars[SB_DP], (j - 1) & 1, false);  // delta of j-1 no longer read
+      // the slot's only readers were the MMAs whose completion was just observed
+      if (tid == 0) mbar_arrive_remote_relaxed(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + b)), 0));
+      if (j > 0) CH_WAIT(&bars[SB_DP + (b ^ 1)], ((j - 1) >> 1) & 1, false);  // delta of j-1 read
 
       // ---- delta and its decayed copy as hi/lo bf16 A operands in TMEM ----
-      delta_half(tq, ED, 0);
-      delta_half(tq, ED, 1);
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) delta_half(tq, ED, hh);
       tc_fence_before();
       named_sync(1, 128);
 
@@ -681,18 +794,19 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       if (tid == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < 4; ++kk) {
           const uint64_t kb = desc_mn(stg + 8192, kk, 16384);
           mma_bf16_ta(tmem + TT_S, tmem + TT_DSH + 8 * kk, kb, id, 1);
           mma_bf16_ta(tmem + TT_S, tmem + TT_DSL + 8 * kk, kb, id, 1);
         }
         mma_commit(&bars[SB_DS]);
-        mbar_arrive(&bars[SB_DR]);  // after the state update is queued on the tensor pipe
+        // delta of chunk j is in TMEM and the accumulator of U^T + S(-W~^T) is free
+        mbar_arrive(&bars[SB_DR]);
       }
       CH_WAIT(&bars[SB_DS], j & 1, false);
       tc_fence_after();
-      if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // chain is done with K, V of this stage
+      if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // the chain's last read of stage s
       CH_WAIT(&bars[SB_SQ], j & 1, false);                 // S Q^T of chunk j has read S
       const bool last = (j + 1 == u.nc);
       float gam = 1.f;
@@ -727,130 +841,147 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       fence_async_smem();
       tc_fence_before();
       named_sync(1, 128);
-      if (tid == 0 && !last) mbar_arrive(&bars[SB_SBR]);  // phase j + 1
     }
 #undef CH_WAIT
     return;
   }
 
-  // ========================= aux: P, S Q^T, delta^T P^T, outputs =========================
-  const int atid = tid - 128;
-#define AX_WAIT(bar, par)                                                      \
+  if (warp < 8) {
+    // ============ aux P: Q K^T -> P (or P' = P e^{-g_t}), ahead of the chain ============
+    const int atid = tid - 128;
+#define AP_WAIT(bar, par)                                                      \
   {                                                                            \
     const bool ok_ = wait_bar((bar), (par), abort_flag, false);                \
     if (named_sync_or(2, 128, !ok_ || *abort_flag != 0)) break;                \
   }
-  for (int j = 0; j < u.nc; ++j) {
-    const int s = j % ST_NST;
-    uint8_t* stg = sm + ST_QK + s * ST_STAGE;
-    const float* G = der_all + s * ST_DER_STAGE;
-    const float* EG = G + 64;
-    const float* EN = G + 192;
-    const long long c0 = (long long)j * kC;
-    const int lc = (int)min((long long)kC, u.len - c0);
-    AX_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
-    const bool factored = flags[s] != 0;
+    for (int j = 0; j < u.nc; ++j) {
+      const int s = j % ST_NST;
+      const int b = j & 1;
+      uint8_t* stg = sm + ST_QK + s * ST_STAGE;
+      uint8_t* ps = sm + ST_PS + b * PS_BYTES;
+      const float* GN = der_all + s * ST_DER_STAGE;
+      const float* EG = GN + 64;
+      // Stage s holds chunk j only after chunk j - 2 has released it, which happens
+      // after the chain's delta^T P^T of chunk j - 2: P slot b is free as well.
+      AP_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
+      const bool factored = flags[s] != 0;
 
-    // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T) ----
-    if (atid == 0) {
+      // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T) ----
+      if (atid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16(tmem + TT_QK, desc_k(stg, kk, 16384), desc_k(stg + 8192, kk, 16384), id, kk > 0);
+        mma_commit(&bars[SB_QKM]);
+      }
+      AP_WAIT(&bars[SB_QKM], j & 1);
       tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+      // factored:  P'_{t,j} = q_t.k_j e^{-g_j}      (the e^{g_t} is applied to the outputs)
+      // otherwise: P_{t,j}  = q_t.k_j e^{g_t - g_j} (and Q is scaled by e^{g_t} below)
+      if (q4 < 2) {
+        const int t = row;
+        const float gt = GN[t];
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          tmem_ld32(tq + TT_QK + 32 * hh, r);
+          tmem_wait_ld();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TT_QK, desc_k(stg, kk, 16384), desc_k(stg + 8192, kk, 16384), id, kk > 0);
-      mma_commit(&bars[SB_QKM]);
-    }
-    AX_WAIT(&bars[SB_QKM], j & 1);
-    tc_fence_after();
-    if (q4 < 2) {
-      const int t = row;
-      const float gt = G[t], egt = EG[t];
+          for (int q = 0; q < 4; ++q) {
+            const int jc0 = 32 * hh + 8 * q;
+            const float4 na = ld4(GN + jc0), nb4 = ld4(GN + jc0 + 4);
+            const float gn[8] = {na.x, na.y, na.z, na.w, nb4.x, nb4.y, nb4.z, nb4.w};
+            float v[8];
+            if (factored) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r[32];
-        tmem_ld32(tq + TT_QK + 32 * hh, r);
-        tmem_wait_ld();
+              for (int e = 0; e < 8; ++e)
+                v[e] = (jc0 + e <= t) ? __uint_as_float(r[8 * q + e]) * gn[e] : 0.f;
+            } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int jc0 = 32 * hh + 8 * q;
-          float v[8];
-          if (factored) {
-            const float4 na = ld4(EN + jc0), nb4 = ld4(EN + jc0 + 4);
-            const float en[8] = {na.x, na.y, na.z, na.w, nb4.x, nb4.y, nb4.z, nb4.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              v[e] = (jc0 + e <= t) ? egt * __uint_as_float(r[8 * q + e]) * en[e] : 0.f;
-          } else {
-            const float4 ga = ld4(G + jc0), gb = ld4(G + jc0 + 4);
-            const float gc[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              v[e] = (jc0 + e <= t) ? ex2(gt - gc[e]) * __uint_as_float(r[8 * q + e]) : 0.f;
+              for (int e = 0; e < 8; ++e)
+                v[e] = (jc0 + e <= t) ? ex2(gt - gn[e]) * __uint_as_float(r[8 * q + e]) : 0.f;
+            }
+            st_sw128_8_split(ps, ps + 8192, t, jc0, 64, v);
           }
-          st_sw128_8_split(sm + ST_PH, sm + ST_PL, t, jc0, 64, v);
         }
       }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    named_sync(2, 128);
-
-    // ---- S Q^T once the chain has written S of chunk j and its S W~^T is done ----
-    AX_WAIT(&bars[SB_SBR], j & 1);
-    AX_WAIT(&bars[SB_C], j & 1);
-    if (atid == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+      if (!factored) {
+        // Q <- diag(e^{g}) Q in place (bf16), after Q K^T has read it: 16-byte pieces,
+        // each inside one row (row = offset / 128 in either 64-column panel)
+#pragma unroll 1
+        for (int it0 = 0; it0 < 1024; it0 += 128) {
+          const int it = it0 + atid;
+          const int pnl = it >> 9, off = (it & 511) * 16;
+          uint4* pq = reinterpret_cast<uint4*>(stg + pnl * 16384 + off);
+          const float e = EG[off >> 7];
+          uint4 x = *pq;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&x);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tmem + TT_SQ, desc_k(sm + ST_SB, kk, 16384), desc_k(stg, kk, 16384), id, kk > 0);
-      mma_commit(&bars[SB_SQ]);
-    }
-    // ---- delta^T P^T once the chain has delta of chunk j (and queued its update) ----
-    AX_WAIT(&bars[SB_DR], j & 1);
-    if (atid == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ph = desc_k(sm + ST_PH, kk, 8192), pl = desc_k(sm + ST_PL, kk, 8192);
-        mma_bf16_ta(tmem + TT_DP, tmem + TT_DH + 8 * kk, ph, id, kk > 0);
-        mma_bf16_ta(tmem + TT_DP, tmem + TT_DH + 8 * kk, pl, id, 1);
-        mma_bf16_ta(tmem + TT_DP, tmem + TT_DL + 8 * kk, ph, id, 1);
+          for (int c = 0; c < 4; ++c) {
+            const float lo = __uint_as_float(w[c] << 16), hi = __uint_as_float(w[c] & 0xffff0000u);
+            w[c] = pack_bf16(lo * e, hi * e);
+          }
+          *pq = x;
+        }
       }
-      mma_commit(&bars[SB_DP]);
+      fence_async_smem();
+      tc_fence_before();
+      named_sync(2, 128);
+      if (atid == 0) mbar_arrive(&bars[SB_PF + b]);
     }
-    AX_WAIT(&bars[SB_SQ], j & 1);
-    AX_WAIT(&bars[SB_DP], j & 1);
-    tc_fence_after();
+#undef AP_WAIT
+    return;
+  }
 
-    // ---- o_t = e^{g_t} (S Q^T)_t + (delta^T P^T)_t, staged in the dead Q rows ----
-    __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(stg);          // rows 0..31
-    __nv_bfloat16* ost1 = reinterpret_cast<__nv_bfloat16*>(stg + 16384);  // rows 32..63
-#pragma unroll
+  // ============ aux O: o_t = e^{g_t} O'_t (or O_t) -> out, stage release ============
+  const int atid = tid - 256;
+#define AO_WAIT(bar, par)                                                      \
+  {                                                                            \
+    const bool ok_ = wait_bar((bar), (par), abort_flag, false);                \
+    if (named_sync_or(3, 128, !ok_ || *abort_flag != 0)) break;                \
+  }
+  for (int j = 0; j < u.nc; ++j) {
+    const int s = j % ST_NST;
+    const int b = j & 1;
+    uint8_t* stg = sm + ST_QK + s * ST_STAGE;
+    const float* EG = der_all + s * ST_DER_STAGE + 64;
+    const long long c0 = (long long)j * kC;
+    const int lc = (int)min((long long)kC, u.len - c0);
+    // every MMA of chunk j (the chain commits delta^T P^T last) has completed
+    AO_WAIT(&bars[SB_DP + b], (j >> 1) & 1);
+    tc_fence_after();
+    const bool factored = flags[s] != 0;
+
+    // ---- staged in the dead Q rows (rows 0..31 in panel 0, rows 32..63 in panel 1) ----
+    __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(stg);
+    __nv_bfloat16* ost1 = reinterpret_cast<__nv_bfloat16*>(stg + 16384);
+#pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
       __nv_bfloat16* ost = hh ? ost1 : ost0;
-      uint32_t a[32], b[32];
-      tmem_ld32(tq + TT_SQ + 32 * hh, a);
-      tmem_ld32(tq + TT_DP + 32 * hh, b);
+      uint32_t a[32];
+      tmem_ld32(tq + TT_O + 64 * b + 32 * hh, a);
       tmem_wait_ld();
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 e4 = ld4(EG + 32 * hh + 4 * q);
-        const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+        float ev[4] = {1.f, 1.f, 1.f, 1.f};
+        if (factored) {
+          const float4 e4 = ld4(EG + 32 * hh + 4 * q);
+          ev[0] = e4.x; ev[1] = e4.y; ev[2] = e4.z; ev[3] = e4.w;
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int tl = 4 * q + e;  // row within this half
-          ost[tl * kD + row] = __float2bfloat16_rn(
-              fmaf(ev[e], __uint_as_float(a[tl]), __uint_as_float(b[tl])));
+          ost[tl * kD + row] = __float2bfloat16_rn(ev[e] * __uint_as_float(a[tl]));
         }
       }
     }
     tc_fence_before();
-    named_sync(2, 128);
+    named_sync(3, 128);
+    if (atid == 0) mbar_arrive(&bars[SB_OE + b]);  // accumulator b may be overwritten
     {
       const size_t obase = (size_t)(u.row0 + c0) * H + u.h;
-#pragma unroll
+#pragma unroll 1
       for (int it0 = 0; it0 < 1024; it0 += 128) {
         const int it = it0 + atid;
         const int t = it >> 4, ch = it & 15;
@@ -861,11 +992,11 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         }
       }
     }
-    named_sync(2, 128);
-    // Q, K, the staged outputs and the gate factors of this stage are no longer read
+    named_sync(3, 128);
+    // Q, V, the staged outputs and the gate factors of stage s are no longer read
     if (atid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);
   }
-#undef AX_WAIT
+#undef AO_WAIT
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -909,17 +1040,17 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(&b[WB_KV_FULL + s], 2);
         mbar_init(&b[WB_KV_EMPTY + s], 1);
       }
-      mbar_init(&b[WB_MMA + 0], 1);
-      mbar_init(&b[WB_MMA + 1], 1);
+      for (int k = 0; k < WY_NWG; ++k) mbar_init(&b[WB_MMA + k], 1);
       for (int k = 0; k < 2; ++k) mbar_init(&b[WB_HE + k], 1);
+      *reinterpret_cast<volatile int*>(sm + WY_MISC + 8) = 0;  // hand-off ticket
       prefetch_tensormap(&tm_k);
     } else {
       uint64_t* b = reinterpret_cast<uint64_t*>(sm + ST_BAR);
       for (int s = 0; s < ST_NST; ++s) {
         mbar_init(&b[SB_QK_FULL + s], 2);
-        mbar_init(&b[SB_QK_EMPTY + s], 2);
+        mbar_init(&b[SB_QK_EMPTY + s], 2);  // the chain (after its state update) and aux O
       }
-      for (int k = SB_HF; k <= SB_DR; ++k) mbar_init(&b[k], 1);
+      for (int k = SB_HF; k < SB_COUNT; ++k) mbar_init(&b[k], 1);
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);

@@ -207,6 +207,13 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Arrive once on an mbarrier of another CTA of the cluster without ordering this
+// thread's earlier memory accesses: for a signal that covers only asynchronous
+// reads (tensor-core operands) whose completion has already been observed.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr,
                                                              uint32_t bytes) {
   asm volatile(
