@@ -113,7 +113,7 @@ constexpr int ST_DER = ST_SB + 32768;    // [2 stages][GN, EG, ED][64] fp32 (GN:
 constexpr int ST_DER_STAGE = 3 * 64;
 constexpr int ST_FLAG = ST_DER + ST_NST * ST_DER_STAGE * 4;  // [2] int
 constexpr int ST_BAR = ST_FLAG + 64;
-constexpr int ST_MISC = ST_BAR + 160;
+constexpr int ST_MISC = ST_BAR + 192;
 constexpr int ST_USED = ST_MISC + 64;
 // The output tile of a chunk is staged in the Q rows of its own stage once Q is no
 // longer read (rows 0..31 in panel 0, rows 32..63 in panel 1, 256 bytes a row).
@@ -134,15 +134,16 @@ enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE = 9, WB_COUNT = 
 static_assert(WB_COUNT * 8 <= WY_MISC - WY_BAR, "WY barriers");
 enum StBar {
   SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF = 4, SB_C = 6, SB_DS = 7, SB_QKM = 8, SB_DP = 9,
-  SB_PF = 11, SB_OE = 13, SB_U = 15, SB_DR = 16, SB_SWI = 17, SB_SQ = 18, SB_COUNT = 19
+  SB_PF = 10, SB_U = 13, SB_DR = 15, SB_SWI = 17, SB_SQ = 18, SB_PE = 19,
+  SB_COUNT = 21
 };
 static_assert(SB_COUNT * 8 <= ST_MISC - ST_BAR, "state barriers");
 
 // TMEM columns.  WY: per warpgroup w at 128*w: K K^T 0, W~^T 64.
 constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
-// state: S 0..127, U^T + S(-W~^T) 128, outputs of chunk j at 192 + 64 (j % 2), QK 320,
+// state: S 0..127, U^T + S(-W~^T) of chunk j at 128 + 64 (j % 2), outputs 256, QK 320,
 // delta hi 384, delta lo 416, delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
-constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_QK = 320, TT_DH = 384, TT_DL = 416,
+constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 256, TT_QK = 320, TT_DH = 384, TT_DL = 416,
                    TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
 
@@ -221,6 +222,82 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return ok || wait_bar_poll(bar, parity, abort_flag, cluster_scope);
 }
 
+// A bounded wait taken by every thread of a named-barrier group (`nb`, `nthreads`),
+// followed by one vote: true when the group must leave its loop because its own wait
+// gave up or another role already did.  Out of line, shared by all call sites.
+__device__ __noinline__ bool group_wait_fails(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag, bool cluster_scope,
+                                              uint32_t nb, uint32_t nthreads) {
+  const bool ok = wait_bar(bar, parity, abort_flag, cluster_scope);
+  return named_sync_or(nb, nthreads, !ok || *abort_flag != 0);
+}
+// Inline form for the latency-critical roles, over up to three barriers (a null
+// barrier is skipped) with a single vote: every wait point that is not already
+// satisfied costs a full round of the named barrier, so the chain merges the
+// barriers it needs at the same point.
+__device__ __forceinline__ bool group_waits_fail(volatile int* abort_flag, uint32_t nb,
+                                                 uint32_t nthreads, uint64_t* b1, uint32_t p1,
+                                                 bool c1, uint64_t* b2 = nullptr, uint32_t p2 = 0,
+                                                 uint64_t* b3 = nullptr, uint32_t p3 = 0) {
+  bool ok = wait_bar(b1, p1, abort_flag, c1);
+  if (ok && b2) ok = wait_bar(b2, p2, abort_flag, false);
+  if (ok && b3) ok = wait_bar(b3, p3, abort_flag, false);
+  return named_sync_or(nb, nthreads, !ok || *abort_flag != 0);
+}
+// The same for a single warp.
+__device__ __noinline__ bool warp_wait_fails(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, bool cluster_scope) {
+  return !__all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, cluster_scope));
+}
+
+// MMA issue from one thread.  Descriptors are built once per operand and advanced
+// by constants (16-byte units: 2 per k-step for a K-major operand, 128 for an
+// MN-major one, whose k-step is 16 rows of 128 bytes); a tcgen05.mma then costs the
+// issuing thread little beyond the tensor core's own rate.
+constexpr uint32_t kStepK = 2;
+constexpr uint32_t kStepMN = 128;
+// K = 128 (8 k-steps): A K-major in two 64-column panels pa16 apart; B K-major in
+// panels pb16 apart, or MN-major.  Rolled over the panels, 4 constant steps inside.
+template <bool B_MN>
+__device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a, uint32_t pa16, uint64_t b,
+                                         uint32_t pb16, uint32_t id, uint32_t acc_first) {
+#pragma unroll 1
+  for (int p = 0; p < 2; ++p) {
+    const uint64_t ap = a + (uint64_t)(p * pa16);
+    const uint64_t bp = b + (uint64_t)(B_MN ? p * 4 * kStepMN : p * pb16);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mma_bf16(d, ap + kStepK * k, bp + (B_MN ? kStepMN : kStepK) * k, id, (p | k) ? 1u : acc_first);
+  }
+}
+// K = 64 (4 k-steps): A from TMEM (8 columns per step) or MN-major smem; B K-major
+// or MN-major.  UNROLL for the chain's own MMAs, rolled elsewhere.
+template <bool A_TMEM, bool B_MN, bool UNROLL>
+__device__ __forceinline__ void mma_k64(uint32_t d, uint64_t a, uint32_t a_tmem, uint64_t b,
+                                        uint32_t id, uint32_t acc_first) {
+  if (UNROLL) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint64_t bk = b + (B_MN ? kStepMN : kStepK) * k;
+      if (A_TMEM)
+        mma_bf16_ta(d, a_tmem + 8 * k, bk, id, k ? 1u : acc_first);
+      else
+        mma_bf16(d, a + kStepMN * k, bk, id, k ? 1u : acc_first);
+    }
+  } else {
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      if (A_TMEM)
+        mma_bf16_ta(d, a_tmem, b, id, k ? 1u : acc_first);
+      else
+        mma_bf16(d, a, b, id, k ? 1u : acc_first);
+      a += kStepMN;
+      a_tmem += 8;
+      b += B_MN ? kStepMN : kStepK;
+    }
+  }
+}
+
 // Bounded wait until the hand-off ticket reaches `want`; false on timeout or abort.
 __device__ __forceinline__ bool wait_ticket(volatile int* ticket, int want,
                                             volatile int* abort_flag) {
@@ -287,6 +364,59 @@ __device__ __forceinline__ void scan_gates(const GateLoad& in, int lane, float& 
   tot = (t0 + t1) * kLog2e;
 }
 
+// Row i of A = strictly-lower(beta_i e^{g_i - g_j} k_i.k_j) from the K K^T
+// accumulator (two halves of 32 columns) into fp32 scratch.  FACTORED: ci =
+// beta_i e^{g_i} and colv = e^{-g_j}; otherwise ci = beta_i, gi = g_i, colv = g_j.
+// One instantiation per form keeps the hot form's code contiguous.
+template <bool FACTORED>
+__device__ __forceinline__ void wy_epi_a(uint32_t t_kk, float* arow, int i, float ci, float gi,
+                                         const float* colv) {
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t r[32];
+    tmem_ld32(t_kk + 32 * hh, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int jc0 = 32 * hh + 4 * q;
+      const float4 c4 = ld4(colv + jc0);
+      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x = __uint_as_float(r[4 * q + e]);
+        const float f = FACTORED ? ci * c[e] : ci * ex2(gi - c[e]);
+        v[e] = (jc0 + e < i) ? f * x : 0.f;
+      }
+      st4(arow + jc0, v[0], v[1], v[2], v[3]);
+    }
+  }
+}
+
+// Row t of P (or P') from the Q K^T accumulator as hi/lo bf16 into a P slot.
+// FACTORED: P'_{t,j} = q_t.k_j e^{-g_j} with colv = e^{-g_j}; otherwise
+// P_{t,j} = q_t.k_j e^{g_t - g_j} with gt = g_t and colv = g_j.
+template <bool FACTORED>
+__device__ __forceinline__ void aux_epi_p(uint32_t t_qk, uint8_t* ps, int t, float gt,
+                                          const float* colv) {
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {  // columns 8c .. 8c + 7
+    uint32_t r[8];
+    tmem_ld8(t_qk + 8 * c, r);
+    tmem_wait_ld();
+    const int jc0 = 8 * c;
+    const float4 ca = ld4(colv + jc0), cb = ld4(colv + jc0 + 4);
+    const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float x = __uint_as_float(r[e]);
+      v[e] = (jc0 + e <= t) ? (FACTORED ? x * cv[e] : ex2(gt - cv[e]) * x) : 0.f;
+    }
+    st_sw128_8_split(ps, ps + 8192, t, jc0, 64, v);
+  }
+}
+
 // ============================================================ CTA 0: WY ======
 __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_k,
                        const float* __restrict__ log_alpha, const float* __restrict__ beta,
@@ -305,7 +435,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       const uint32_t use = j / WY_NST;
       const GateLoad cur = next;
       next = load_gates(log_alpha, beta, u, H, j + 1, lane);  // in flight during the wait
-      if (!__all_sync(0xffffffffu, wait_bar(&bars[WB_KV_EMPTY + s], (use & 1) ^ 1, abort_flag, false)))
+      if (warp_wait_fails(&bars[WB_KV_EMPTY + s], (use & 1) ^ 1, abort_flag, false))
         break;
       uint8_t* st = sm + WY_KV + s * WY_STAGE;
       const int r = (int)(u.row0 + (long long)j * kC);
@@ -350,11 +480,8 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
   const uint32_t tq = tw + ((uint32_t)(q4 * 32) << 16);
   uint32_t mph = 0;
 
-#define WY_WAIT(bar, par, cl)                                                  \
-  {                                                                            \
-    const bool ok_ = wait_bar((bar), (par), abort_flag, (cl));                 \
-    if (named_sync_or(nb, 128, !ok_ || *abort_flag != 0)) break;               \
-  }
+#define WY_WAIT(bar, par, cl) \
+  if (group_waits_fail(abort_flag, nb, 128, (bar), (par), (cl))) break;
 
   for (int j = w; j < u.nc; j += WY_NWG) {
     const int s = j % WY_NST;
@@ -370,9 +497,8 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     if (wtid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-      for (int kk = 0; kk < 8; ++kk)
-        mma_bf16(tw + WT_KK, desc_k(st, kk, 8192), desc_k(st, kk, 8192), id, kk > 0);
+      const uint64_t dkk = desc_k(st, 0, 8192);
+      mma_k128<false>(tw + WT_KK, dkk, 8192 >> 4, dkk, 8192 >> 4, id, 0);
       mma_commit(&bars[WB_MMA + w]);
     }
     // the bulk copy of this warpgroup's previous chunk reads the scratch that A is
@@ -384,33 +510,10 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
 
     // ---- A = strictly-lower(beta_i e^{g_i - g_j} k_i.k_j), fp32 ----
     if (q4 < 2) {
-      const int i = row;
-      const float gi = G[i], bi = BE[i], bgi = BG[i];
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r[32];
-        tmem_ld32(tq + WT_KK + 32 * hh, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int jc0 = 32 * hh + 4 * q;
-          float v[4];
-          if (factored) {
-            const float4 n4 = ld4(EN + jc0);
-            const float en[4] = {n4.x, n4.y, n4.z, n4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              v[e] = (jc0 + e < i) ? bgi * __uint_as_float(r[4 * q + e]) * en[e] : 0.f;
-          } else {
-            const float4 g4 = ld4(G + jc0);
-            const float gc[4] = {g4.x, g4.y, g4.z, g4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              v[e] = (jc0 + e < i) ? bi * ex2(gi - gc[e]) * __uint_as_float(r[4 * q + e]) : 0.f;
-          }
-          st4(Am + i * LDA + jc0, v[0], v[1], v[2], v[3]);
-        }
-      }
+      if (factored)
+        wy_epi_a<true>(tq + WT_KK, Am + row * LDA, row, BG[row], 0.f, EN);
+      else
+        wy_epi_a<false>(tq + WT_KK, Am + row * LDA, row, BE[row], G[row], G);
     }
     named_sync(nb, 128);
 
@@ -508,12 +611,10 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     if (wtid == 0) {
       tc_fence_after();
       const uint32_t id = idesc_bf16(128, 64, 1, 0);
-#pragma unroll 1
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ak = desc_mn(st, kk, 8192);
-        mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWH, kk, 8192), id, kk > 0);
-        mma_bf16(tw + WT_W, ak, desc_k(scr + SC_TWL, kk, 8192), id, 1);
-      }
+      const uint64_t da = desc_mn(st, 0, 8192);
+      const uint64_t dh = desc_k(scr + SC_TWH, 0, 8192), dl = desc_k(scr + SC_TWL, 0, 8192);
+      mma_k64<false, false, false>(tw + WT_W, da, 0, dh, id, 0);
+      mma_k64<false, false, false>(tw + WT_W, da, 0, dl, id, 1);
       mma_commit(&bars[WB_MMA + w]);
     }
     WY_WAIT(&bars[WB_MMA + w], mph, false);
@@ -565,18 +666,18 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
   if (wtid == 0) bulk_wait_all();  // every copy this warpgroup issued has landed
 }
 
-// One half (tokens 32*hh .. 32*hh + 31) of the delta epilogue of the state CTA:
-// the accumulator already holds delta^T = U^T + S(-W~^T); write delta and
+// One quarter (tokens 16*qq .. 16*qq + 15) of the delta epilogue of the state CTA:
+// the accumulator t_sw already holds delta^T = U^T + S(-W~^T); write delta and
 // delta~ = delta e^{g_last - g} to TMEM as hi / lo bf16 pairs (the A operands of
 // the next MMAs).
-__device__ __forceinline__ void delta_half(uint32_t tq, const float* ED, int hh) {
-  uint32_t r[32];
-  tmem_ld32(tq + TT_SW + 32 * hh, r);
+__device__ __forceinline__ void delta_quarter(uint32_t tq, uint32_t t_sw, const float* ED, int qq) {
+  uint32_t r[16];
+  tmem_ld16(tq + t_sw + 16 * qq, r);
   tmem_wait_ld();
-  uint32_t dh[16], dl[16], sh[16], sl[16];
+  uint32_t dh[8], dl[8], sh[8], sl[8];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 ea = ld4(ED + 32 * hh + 8 * q), eb = ld4(ED + 32 * hh + 8 * q + 4);
+  for (int q = 0; q < 2; ++q) {
+    const float4 ea = ld4(ED + 16 * qq + 8 * q), eb = ld4(ED + 16 * qq + 8 * q + 4);
     const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -586,11 +687,10 @@ __device__ __forceinline__ void delta_half(uint32_t tq, const float* ED, int hh)
       split2(d0 * ev[2 * e], d1 * ev[2 * e + 1], sh[4 * q + e], sl[4 * q + e]);
     }
   }
-  tmem_st16(tq + TT_DH + 16 * hh, dh);
-  tmem_st16(tq + TT_DL + 16 * hh, dl);
-  tmem_st16(tq + TT_DSH + 16 * hh, sh);
-  tmem_st16(tq + TT_DSL + 16 * hh, sl);
-  tmem_wait_st();
+  tmem_st8(tq + TT_DH + 8 * qq, dh);
+  tmem_st8(tq + TT_DL + 8 * qq, dl);
+  tmem_st8(tq + TT_DSH + 8 * qq, sh);
+  tmem_st8(tq + TT_DSL + 8 * qq, sl);
 }
 
 // ========================================================= CTA 1: state ======
@@ -614,7 +714,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       const uint32_t use = j / ST_NST;
       const GateLoad cur = next;
       next = load_gates(log_alpha, beta, u, H, j + 1, lane);  // in flight during the wait
-      if (!__all_sync(0xffffffffu, wait_bar(&bars[SB_QK_EMPTY + s], (use & 1) ^ 1, abort_flag, false)))
+      if (warp_wait_fails(&bars[SB_QK_EMPTY + s], (use & 1) ^ 1, abort_flag, false))
         break;
       uint8_t* st = sm + ST_QK + s * ST_STAGE;
       const int r = (int)(u.row0 + (long long)j * kC);
@@ -646,64 +746,69 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   }
   if (warp == kMmaWarp) {
     // ------------- MMA warp: the tensor-core work that is not on the chain's path -------------
-    //   U^T = V^T Tu^T into the chain's accumulator once delta of chunk j-1 has left it,
-    //   S Q^T (state part of the outputs) behind the chain's S W~^T,
-    //   delta^T P^T (in-chunk part of the outputs) behind the chain's state update.
-#define MW_WAIT(bar, par, cl) \
-  if (!__all_sync(0xffffffffu, wait_bar((bar), (par), abort_flag, (cl)))) break;
-    for (int j = 0; j < u.nc; ++j) {
-      const int s = j % ST_NST;
-      const int b = j & 1;
-      const uint32_t buse = (uint32_t)(j >> 1);
-      uint8_t* stg = sm + ST_QK + s * ST_STAGE;
-      uint8_t* hs = sm + ST_HS + b * HS_BYTES;
-      const uint8_t* ps = sm + ST_PS + b * PS_BYTES;
-      const uint32_t t_o = tmem + TT_O + 64 * b;
-      MW_WAIT(&bars[SB_HF + b], buse & 1, true);
-      MW_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1, false);
-      if (j > 0) MW_WAIT(&bars[SB_DR], (j - 1) & 1, false);
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t id_u = idesc_bf16(128, 64, 1, 0);
-#pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t av = desc_mn(stg + ST_V, kk, 8192);
-          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUH, kk, 8192), id_u, kk > 0);
-          mma_bf16(tmem + TT_SW, av, desc_k(hs + HS_TUL, kk, 8192), id_u, 1);
+    // U^T = V^T Tu^T (j + 1) goes in behind the chain's state update (j), into the other
+    // U/SW accumulator, ahead of delta^T P^T (j); S Q^T is issued by aux O and Q K^T by
+    // aux P, so that the issue work is spread over three warp schedulers.  Each kind is
+    // issued in chunk order; the warp polls (non-blocking tests), U first.
+    int nu = 0, nd = 0;  // next U, delta^T P^T
+    uint64_t t_idle = globaltimer_ns();
+    while (nd < u.nc) {
+      int kind = -1;
+      if (nu < u.nc) {  // U(i) goes in behind the state update of i - 1
+        const int i = nu;
+        if ((i == 0 || mbar_test(&bars[SB_DR + ((i - 1) & 1)], ((i - 1) >> 1) & 1, false)) &&
+            mbar_test(&bars[SB_QK_FULL + i % ST_NST], (i / ST_NST) & 1, false) &&
+            mbar_test(&bars[SB_HF + (i & 1)], (i >> 1) & 1, true))
+          kind = 0;
+      }
+      if (kind < 0 && nd < nu) {
+        // delta of chunk j in TMEM, P(j) published, and S Q^T (j), which starts the
+        // output accumulator, completed (it comes from another thread)
+        const int j = nd;
+        if (mbar_test(&bars[SB_DR + (j & 1)], (j >> 1) & 1, false) &&
+            mbar_test(&bars[SB_PF + (j & 1)], (j >> 1) & 1, false) &&
+            mbar_test(&bars[SB_SQ], j & 1, false))
+          kind = 2;
+      }
+      const bool did = kind >= 0;
+      if (did) {
+        if (kind == 0) {
+          const int i = nu++;
+          if (lane == 0) {  // U^T(i) = V^T Tu^T (hi + lo) into U/SW accumulator i % 2
+            tc_fence_after();
+            uint8_t* stg = sm + ST_QK + (i % ST_NST) * ST_STAGE;
+            uint8_t* hs = sm + ST_HS + (i & 1) * HS_BYTES;
+            const uint32_t id_u = idesc_bf16(128, 64, 1, 0);
+            const uint32_t d = tmem + TT_SW + 64 * (i & 1);
+            const uint64_t dv = desc_mn(stg + ST_V, 0, 8192);
+            mma_k64<false, false, false>(d, dv, 0, desc_k(hs + HS_TUH, 0, 8192), id_u, 0);
+            mma_k64<false, false, false>(d, dv, 0, desc_k(hs + HS_TUL, 0, 8192), id_u, 1);
+            mma_commit(&bars[SB_U + (i & 1)]);
+          }
+        } else {
+          const int j = nd++;
+          if (lane == 0) {  // += delta^T P^T (j): hi*hi + hi*lo + lo*hi
+            tc_fence_after();
+            const uint8_t* ps = sm + ST_PS + (j & 1) * PS_BYTES;
+            const uint32_t id = idesc_bf16(128, 64, 0, 0);
+            const uint64_t ph = desc_k(ps, 0, 8192), pl = desc_k(ps + 8192, 0, 8192);
+            mma_k64<true, false, false>(tmem + TT_O, 0, tmem + TT_DH, ph, id, 1);
+            mma_k64<true, false, false>(tmem + TT_O, 0, tmem + TT_DH, pl, id, 1);
+            mma_k64<true, false, false>(tmem + TT_O, 0, tmem + TT_DL, ph, id, 1);
+            mma_commit(&bars[SB_DP]);
+          }
         }
-        mma_commit(&bars[SB_U]);
+        __syncwarp();
       }
-      // S Q^T, or S (diag(e^g) Q)^T once aux P has scaled Q when the chunk's decay is
-      // too strong for the factored form
-      const bool factored = flags[s] != 0;
-      MW_WAIT(&bars[SB_SWI], j & 1, false);
-      MW_WAIT(&bars[SB_OE + b], (buse & 1) ^ 1, false);  // outputs of chunk j - 2 read
-      if (!factored) MW_WAIT(&bars[SB_PF + b], buse & 1, false);
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t id_q = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(t_o, desc_k(sm + ST_SB, kk, 16384), desc_k(stg, kk, 16384), id_q, kk > 0);
-        mma_commit(&bars[SB_SQ]);
+      if (did) {
+        t_idle = globaltimer_ns();
+      } else if (*abort_flag != 0) {
+        break;
+      } else if (globaltimer_ns() - t_idle > kWaitNs) {
+        atomicOr((int*)abort_flag, ST_WAIT);
+        break;
       }
-      MW_WAIT(&bars[SB_DR], j & 1, false);
-      MW_WAIT(&bars[SB_PF + b], buse & 1, false);
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ph = desc_k(ps, kk, 8192), pl = desc_k(ps + 8192, kk, 8192);
-          mma_bf16_ta(t_o, tmem + TT_DH + 8 * kk, ph, id, 1);
-          mma_bf16_ta(t_o, tmem + TT_DH + 8 * kk, pl, id, 1);
-          mma_bf16_ta(t_o, tmem + TT_DL + 8 * kk, ph, id, 1);
-        }
-        mma_commit(&bars[SB_DP + b]);
-      }
-      __syncwarp();
     }
-#undef MW_WAIT
     return;
   }
   if (warp > kMmaWarp) return;
@@ -715,10 +820,15 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   if (warp < 4) {
     // ======================= chain: the serial state pass =======================
     bool alive = true;
-#define CH_WAIT(bar, par, cl)                                                  \
-  {                                                                            \
-    const bool ok_ = wait_bar((bar), (par), abort_flag, (cl));                 \
-    if (named_sync_or(1, 128, !ok_ || *abort_flag != 0)) { alive = false; break; } \
+#define CH_WAIT(bar, par, cl)                                   \
+  if (group_waits_fail(abort_flag, 1, 128, (bar), (par), (cl))) { \
+    alive = false;                                              \
+    break;                                                      \
+  }
+#define CH_WAIT3(b1, p1, c1, b2, p2, b3, p3)                                   \
+  if (group_waits_fail(abort_flag, 1, 128, (b1), (p1), (c1), (b2), (p2), (b3), (p3))) { \
+    alive = false;                                                             \
+    break;                                                                     \
   }
     // initial state: bf16 copy for the first MMAs, gamma_0 * S0 into TMEM
     do {
@@ -767,26 +877,25 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
 
       // ---- delta^T = U^T + S (-W~^T): U^T = V^T Tu^T is already in the accumulator
       //      (issued by the MMA warp) ----
-      CH_WAIT(&bars[SB_U], j & 1, false);
-      CH_WAIT(&bars[SB_HF + b], buse & 1, true);
+      CH_WAIT3(&bars[SB_HF + b], buse & 1, true, &bars[SB_U + b], buse & 1, nullptr, 0);
       if (tid == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + TT_SW, desc_k(sm + ST_SB, kk, 16384), desc_mn(hs, kk, 16384), id, 1);
+        const uint64_t ds = desc_k(sm + ST_SB, 0, 16384), dw = desc_mn(hs, 0, 16384);
+        mma_k128<true>(tmem + TT_SW + 64 * b, ds, 16384 >> 4, dw, 0, id, 1);
         mma_commit(&bars[SB_C]);
         mbar_arrive(&bars[SB_SWI]);  // S Q^T may now be queued behind S W~^T
       }
-      CH_WAIT(&bars[SB_C], j & 1, false);
+      // S W~^T done; delta of chunk j - 1 read by its delta^T P^T
+      CH_WAIT3(&bars[SB_C], j & 1, false, j > 0 ? &bars[SB_DP] : nullptr, (j - 1) & 1, nullptr, 0);
       tc_fence_after();
       // the slot's only readers were the MMAs whose completion was just observed
       if (tid == 0) mbar_arrive_remote_relaxed(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + b)), 0));
-      if (j > 0) CH_WAIT(&bars[SB_DP + (b ^ 1)], ((j - 1) >> 1) & 1, false);  // delta of j-1 read
 
       // ---- delta and its decayed copy as hi/lo bf16 A operands in TMEM ----
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) delta_half(tq, ED, hh);
+      for (int qq = 0; qq < 4; ++qq) delta_quarter(tq, TT_SW + 64 * b, ED, qq);
+      tmem_wait_st();
       tc_fence_before();
       named_sync(1, 128);
 
@@ -794,26 +903,20 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       if (tid == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
-#pragma unroll 1
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t kb = desc_mn(stg + 8192, kk, 16384);
-          mma_bf16_ta(tmem + TT_S, tmem + TT_DSH + 8 * kk, kb, id, 1);
-          mma_bf16_ta(tmem + TT_S, tmem + TT_DSL + 8 * kk, kb, id, 1);
-        }
+        const uint64_t dkb = desc_mn(stg + 8192, 0, 16384);
+        mma_k64<true, true, true>(tmem + TT_S, 0, tmem + TT_DSH, dkb, id, 1);
+        mma_k64<true, true, true>(tmem + TT_S, 0, tmem + TT_DSL, dkb, id, 1);
         mma_commit(&bars[SB_DS]);
         // delta of chunk j is in TMEM and the accumulator of U^T + S(-W~^T) is free
-        mbar_arrive(&bars[SB_DR]);
+        mbar_arrive(&bars[SB_DR + b]);
       }
-      CH_WAIT(&bars[SB_DS], j & 1, false);
+      // the state update is done, S Q^T of chunk j has read S, chunk j + 1 is loaded
+      const bool last = (j + 1 == u.nc);
+      CH_WAIT3(&bars[SB_DS], j & 1, false, &bars[SB_SQ], j & 1,
+               last ? nullptr : &bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1);
       tc_fence_after();
       if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // the chain's last read of stage s
-      CH_WAIT(&bars[SB_SQ], j & 1, false);                 // S Q^T of chunk j has read S
-      const bool last = (j + 1 == u.nc);
-      float gam = 1.f;
-      if (!last) {
-        CH_WAIT(&bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1, false);
-        gam = der_all[((j + 1) % ST_NST) * ST_DER_STAGE + 64 + 63];
-      }
+      const float gam = last ? 1.f : der_all[((j + 1) % ST_NST) * ST_DER_STAGE + 64 + 63];
       // ---- new state: bf16 copy for the next chunk, pre-scaled fp32 back to TMEM ----
 #pragma unroll 1
       for (int p = 0; p < 4; ++p) {
@@ -849,11 +952,8 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   if (warp < 8) {
     // ============ aux P: Q K^T -> P (or P' = P e^{-g_t}), ahead of the chain ============
     const int atid = tid - 128;
-#define AP_WAIT(bar, par)                                                      \
-  {                                                                            \
-    const bool ok_ = wait_bar((bar), (par), abort_flag, false);                \
-    if (named_sync_or(2, 128, !ok_ || *abort_flag != 0)) break;                \
-  }
+#define AP_WAIT(bar, par) \
+  if (group_wait_fails((bar), (par), abort_flag, false, 2, 128)) break;
     for (int j = 0; j < u.nc; ++j) {
       const int s = j % ST_NST;
       const int b = j & 1;
@@ -861,50 +961,26 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       uint8_t* ps = sm + ST_PS + b * PS_BYTES;
       const float* GN = der_all + s * ST_DER_STAGE;
       const float* EG = GN + 64;
-      // Stage s holds chunk j only after chunk j - 2 has released it, which happens
-      // after the chain's delta^T P^T of chunk j - 2: P slot b is free as well.
       AP_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
       const bool factored = flags[s] != 0;
 
-      // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T) ----
-      if (atid == 0) {
+      // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T), issued from warp 6 ----
+      if (atid == 64) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16(tmem + TT_QK, desc_k(stg, kk, 16384), desc_k(stg + 8192, kk, 16384), id, kk > 0);
+        mma_k128<false>(tmem + TT_QK, desc_k(stg, 0, 16384), 16384 >> 4, desc_k(stg + 8192, 0, 16384),
+                        16384 >> 4, idesc_bf16(128, 64, 0, 0), 0);
         mma_commit(&bars[SB_QKM]);
       }
       AP_WAIT(&bars[SB_QKM], j & 1);
+      AP_WAIT(&bars[SB_PE + b], ((j >> 1) & 1) ^ 1);  // outputs of chunk j - 2 left slot b
       tc_fence_after();
       // factored:  P'_{t,j} = q_t.k_j e^{-g_j}      (the e^{g_t} is applied to the outputs)
       // otherwise: P_{t,j}  = q_t.k_j e^{g_t - g_j} (and Q is scaled by e^{g_t} below)
       if (q4 < 2) {
-        const int t = row;
-        const float gt = GN[t];
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[32];
-          tmem_ld32(tq + TT_QK + 32 * hh, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int jc0 = 32 * hh + 8 * q;
-            const float4 na = ld4(GN + jc0), nb4 = ld4(GN + jc0 + 4);
-            const float gn[8] = {na.x, na.y, na.z, na.w, nb4.x, nb4.y, nb4.z, nb4.w};
-            float v[8];
-            if (factored) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                v[e] = (jc0 + e <= t) ? __uint_as_float(r[8 * q + e]) * gn[e] : 0.f;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                v[e] = (jc0 + e <= t) ? ex2(gt - gn[e]) * __uint_as_float(r[8 * q + e]) : 0.f;
-            }
-            st_sw128_8_split(ps, ps + 8192, t, jc0, 64, v);
-          }
-        }
+        if (factored)
+          aux_epi_p<true>(tq + TT_QK, ps, row, 0.f, GN);
+        else
+          aux_epi_p<false>(tq + TT_QK, ps, row, GN[row], GN);
       }
       if (!factored) {
         // Q <- diag(e^{g}) Q in place (bf16), after Q K^T has read it: 16-byte pieces,
@@ -928,73 +1004,87 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       fence_async_smem();
       tc_fence_before();
       named_sync(2, 128);
-      if (atid == 0) mbar_arrive(&bars[SB_PF + b]);
+      if (atid == 0) {
+        mbar_arrive(&bars[SB_PF + b]);
+        mbar_arrive(&bars[SB_QK_EMPTY + s]);  // aux P reads nothing more of stage s
+      }
     }
 #undef AP_WAIT
     return;
   }
 
-  // ============ aux O: o_t = e^{g_t} O'_t (or O_t) -> out, stage release ============
+  // ============ aux O: o_t = e^{g_t} O'_t (or O_t) -> out ============
+  // aux O holds no stage: each of its warps recomputes the chunk's gate factors from
+  // the gates in global memory (the same scan as the producer, so the same values and
+  // the same choice of form), and the bf16 outputs are staged in the chunk's P slot,
+  // which delta^T P^T no longer reads.  It also issues S Q^T, which must wait for the
+  // previous chunk's outputs to leave the accumulator.
   const int atid = tid - 256;
-#define AO_WAIT(bar, par)                                                      \
-  {                                                                            \
-    const bool ok_ = wait_bar((bar), (par), abort_flag, false);                \
-    if (named_sync_or(3, 128, !ok_ || *abort_flag != 0)) break;                \
-  }
-  for (int j = 0; j < u.nc; ++j) {
-    const int s = j % ST_NST;
-    const int b = j & 1;
-    uint8_t* stg = sm + ST_QK + s * ST_STAGE;
-    const float* EG = der_all + s * ST_DER_STAGE + 64;
-    const long long c0 = (long long)j * kC;
-    const int lc = (int)min((long long)kC, u.len - c0);
-    // every MMA of chunk j (the chain commits delta^T P^T last) has completed
-    AO_WAIT(&bars[SB_DP + b], (j >> 1) & 1);
-    tc_fence_after();
-    const bool factored = flags[s] != 0;
-
-    // ---- staged in the dead Q rows (rows 0..31 in panel 0, rows 32..63 in panel 1) ----
-    __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(stg);
-    __nv_bfloat16* ost1 = reinterpret_cast<__nv_bfloat16*>(stg + 16384);
+#define AO_WAIT(bar, par) \
+  if (group_wait_fails((bar), (par), abort_flag, false, 3, 128)) break;
+  // Iteration i drains the outputs of chunk i - 1 out of TMEM, issues S Q^T (i), then
+  // copies chunk i - 1 out: one issue site.
+  GateLoad gnext = load_gates(log_alpha, beta, u, H, 0, lane);
+  for (int i = 0; i <= u.nc; ++i) {
+    const int j = i - 1, b = j & 1;
+    __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(sm + ST_PS + b * PS_BYTES);
+    if (i > 0) {
+      const GateLoad gcur = gnext;
+      gnext = load_gates(log_alpha, beta, u, H, i, lane);  // in flight during the wait
+      float g0, g1, tot;
+      scan_gates(gcur, lane, g0, g1, tot);
+      const bool factored = -tot < kMaxFactoredDecayLog2;
+      const float e0 = factored ? ex2(g0) : 1.f, e1 = factored ? ex2(g1) : 1.f;
+      // S Q^T and delta^T P^T of chunk j (the MMA warp commits delta^T P^T last)
+      AO_WAIT(&bars[SB_DP], j & 1);
+      tc_fence_after();
+      // ---- bf16 outputs staged in P slot b (row t at t * 256 bytes), 8 tokens a step ----
 #pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {
-      __nv_bfloat16* ost = hh ? ost1 : ost0;
-      uint32_t a[32];
-      tmem_ld32(tq + TT_O + 64 * b + 32 * hh, a);
-      tmem_wait_ld();
-#pragma unroll
       for (int q = 0; q < 8; ++q) {
-        float ev[4] = {1.f, 1.f, 1.f, 1.f};
-        if (factored) {
-          const float4 e4 = ld4(EG + 32 * hh + 4 * q);
-          ev[0] = e4.x; ev[1] = e4.y; ev[2] = e4.z; ev[3] = e4.w;
-        }
+        uint32_t a[8];
+        tmem_ld8(tq + TT_O + 8 * q, a);
+        tmem_wait_ld();
+        const float ev = q < 4 ? e0 : e1;  // e^{g_t} of tokens 8q .. 8q + 7 (lanes t % 32)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tl = 4 * q + e;  // row within this half
-          ost[tl * kD + row] = __float2bfloat16_rn(ev[e] * __uint_as_float(a[tl]));
-        }
+        for (int e = 0; e < 8; ++e)
+          ost0[(8 * q + e) * kD + row] = __float2bfloat16_rn(
+              __shfl_sync(0xffffffffu, ev, (8 * q + e) & 31) * __uint_as_float(a[e]));
+      }
+      tc_fence_before();
+      named_sync(3, 128);  // O of chunk j is out of TMEM: S Q^T (j + 1) may overwrite it
+    }
+    if (i < u.nc) {
+      // S Q^T (i) starts the output accumulator of chunk i: issued (from warp 11) once
+      // the chain has queued S W~^T (i), which reads the same bf16 S; in the
+      // strong-decay form also once aux P has scaled Q.  The chunk's form is read from
+      // its stage, which the chain waited for before signalling.
+      AO_WAIT(&bars[SB_SWI], i & 1);
+      const int si = i % ST_NST;
+      if (flags[si] == 0) AO_WAIT(&bars[SB_PF + (i & 1)], (i >> 1) & 1);
+      if (atid == 96) {
+        tc_fence_after();
+        mma_k128<false>(tmem + TT_O, desc_k(sm + ST_SB, 0, 16384), 16384 >> 4,
+                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), 16384 >> 4,
+                        idesc_bf16(128, 64, 0, 0), 0);
+        mma_commit(&bars[SB_SQ]);
       }
     }
-    tc_fence_before();
-    named_sync(3, 128);
-    if (atid == 0) mbar_arrive(&bars[SB_OE + b]);  // accumulator b may be overwritten
-    {
+    if (i > 0) {
+      const long long c0 = (long long)j * kC;
+      const int lc = (int)min((long long)kC, u.len - c0);
       const size_t obase = (size_t)(u.row0 + c0) * H + u.h;
 #pragma unroll 1
       for (int it0 = 0; it0 < 1024; it0 += 128) {
         const int it = it0 + atid;
         const int t = it >> 4, ch = it & 15;
         if (t < lc) {
-          const __nv_bfloat16* src = (t < 32 ? ost0 + t * kD : ost1 + (t - 32) * kD) + 8 * ch;
-          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          const uint4 v = *reinterpret_cast<const uint4*>(ost0 + t * kD + 8 * ch);
           *reinterpret_cast<uint4*>(out + (obase + (size_t)t * H) * kD + 8 * ch) = v;
         }
       }
+      named_sync(3, 128);
+      if (atid == 0) mbar_arrive(&bars[SB_PE + b]);  // P slot b may be refilled
     }
-    named_sync(3, 128);
-    // Q, V, the staged outputs and the gate factors of stage s are no longer read
-    if (atid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);
   }
 #undef AO_WAIT
 }
@@ -1048,7 +1138,7 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       uint64_t* b = reinterpret_cast<uint64_t*>(sm + ST_BAR);
       for (int s = 0; s < ST_NST; ++s) {
         mbar_init(&b[SB_QK_FULL + s], 2);
-        mbar_init(&b[SB_QK_EMPTY + s], 2);  // the chain (after its state update) and aux O
+        mbar_init(&b[SB_QK_EMPTY + s], 2);  // the chain (after its state update) and aux P
       }
       for (int k = SB_HF; k < SB_COUNT; ++k) mbar_init(&b[k], 1);
       prefetch_tensormap(&tm_q);
