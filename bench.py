@@ -33,6 +33,7 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "gated-DeltaNet chunkwise fwd tokens/s and % of roofline, 1×GB300"
+DECODE_METRIC = "gated-DeltaNet decode step tokens/s and % of roofline, 1×GB300"
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -211,6 +212,154 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def decode_algorithmic(inp: dict) -> dict:
+    """Algorithmic bytes and FLOPs of one decode step over the batch: the state read
+    and written once (fp32 dv x dk per (sequence, head)), q, k, v read and out
+    written once in the qkv dtype, log_alpha and beta read once.  FLOPs: S k and
+    S q (4 dk dv), the rank-one update (3 dk dv), per (sequence, head)."""
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    units = inp["N"] * inp["H"]
+    dk, dv = inp["dk"], inp["dv"]
+    by = units * (2 * dk * dv * 4 + (2 * dk + dv) * esz + dv * esz + 8)
+    return dict(bytes=by, flops=units * 7 * dk * dv)
+
+
+def decode_oracle_time(inp: dict):
+    """Time the fp64 oracle for one decode step of every (sequence, head) on the host
+    cores.  Returns (tokens/s, cores, sample, seconds)."""
+    from oracle import native
+    cores = native.max_threads()
+    q, k, v = (inp[n].unsqueeze(1) for n in ("q", "k", "v"))
+    la, be = inp["log_alpha"].unsqueeze(1), inp["beta"].unsqueeze(1)
+    units = [(s, h) for s in range(inp["N"]) for h in range(inp["H"])]
+    t0 = time.perf_counter()
+    native.gdn_units_c(q, k, v, la, be, inp["S"], None, units, n_threads=cores)
+    dt = time.perf_counter() - t0
+    sample = (f"all {len(units)} (sequence, head) units, one token each, fp64 recurrence step, "
+              f"OpenMP over units")
+    return inp["N"] / dt, cores, sample, dt
+
+
+def run_decode(args, w, world, rank, local):
+    """The decode workloads: one step = one gdn_decode_step over the whole batch."""
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = workloads.make_decode_inputs(w)
+        vals, cores, sample = [], None, None
+        for _ in range(args.steps):
+            v, cores, sample, _ = decode_oracle_time(inp)
+            vals.append(v)
+        value = statistics.median(vals)
+        print(json.dumps({
+            "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * inp["N"] / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "N": inp["N"], "H": inp["H"], "dk": w.dk, "dv": w.dv},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}), flush=True)
+        return
+    import chunkwise_gated_deltanet_gb300 as gdn
+    gdn.load_library()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workloads.make_decode_inputs(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    N, H = inp["N"], inp["H"]
+    out = torch.empty(d["v"].shape, dtype=d["v"].dtype, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():  # the state evolves in place from step to step, as in decoding
+        gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S"], out,
+                            stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    gdn.gdn_check_status(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    gdn.gdn_check_status(stream)
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps,
+                        world, dev)
+    alg = decode_algorithmic(inp)
+    peaks = load_peaks()
+    sec = ms * 1e-3
+    achieved_gbs = alg["bytes"] / sec / 1e9
+    tokens = N * world
+
+    # end to end through the public call: the token's inputs and the state go in from
+    # pinned host memory, the outputs and the state come back
+    host_in = {k: inp[k].pin_memory() for k in ("q", "k", "v", "log_alpha", "beta", "S")}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    S_h = torch.empty(inp["S"].shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = out_h.numel() * out_h.element_size() + S_h.numel() * S_h.element_size()
+
+    def e2e_step():
+        for key, t in host_in.items():
+            d[key].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        S_h.copy_(d["S"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    gdn.gdn_check_status(stream)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = decode_oracle_time(inp)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps({
+            "metric": DECODE_METRIC, "value": tokens / sec, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "N": N, "H": H, "dk": w.dk, "dv": w.dv,
+                       "qkv_dtype": w.dtype, "state": "fp32, updated in place",
+                       "l2": "flushed between timed steps (512 MiB write)",
+                       "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": None, "peak_source": peaks["source"],
+                         "algorithmic_bytes": alg["bytes"]},
+            "clocks": clk.summary(),
+            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": t_wall}), flush=True)
+
+
 def n_tokens_of(inp):
     return inp["B"] * inp["T"]
 
@@ -220,13 +369,20 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=workloads.HEADLINE,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.DECODE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-budget", type=float, default=20.0)
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.workload in workloads.DECODE_WORKLOADS:
+        run_decode(args, workloads.DECODE_WORKLOADS[args.workload], world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     w = workloads.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w, world, rank)

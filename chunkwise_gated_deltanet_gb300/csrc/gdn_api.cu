@@ -101,6 +101,36 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
   return GDN_OK;
 }
 
+int gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha,
+                    const float* beta, float* S, void* out, int N, int H, int dk, int dv,
+                    int qkv_dtype, void* stream) {
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
+    return fail(GDN_EDTYPE, "gdn_decode_step: qkv_dtype %d is neither GDN_F32 nor GDN_BF16",
+                qkv_dtype);
+  if (N < 0 || H < 0)
+    return fail(GDN_EINVAL, "gdn_decode_step: need N >= 0, H >= 0 (got N=%d H=%d)", N, H);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(GDN_EINVAL, "gdn_decode_step: dk and dv must be 16, 32, 64 or 128 (got %d, %d)",
+                dk, dv);
+  if ((long long)N * H == 0) return GDN_OK;
+  if (!q || !k || !v || !log_alpha || !beta || !S || !out)
+    return fail(GDN_EINVAL, "gdn_decode_step: q, k, v, log_alpha, beta, S and out must be non-NULL");
+  const void* ptrs[] = {q, k, v, log_alpha, beta, S, out};
+  const char* names[] = {"q", "k", "v", "log_alpha", "beta", "S", "out"};
+  for (int i = 0; i < 7; ++i)
+    if (!aligned16(ptrs[i]))
+      return fail(GDN_EINVAL, "gdn_decode_step: %s is not 16-byte aligned", names[i]);
+  if ((long long)N * H > 0x7fffffffLL)
+    return fail(GDN_EINVAL, "gdn_decode_step: problem too large");
+  gdn::DecodeArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S = S; a.out = out;
+  a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.bf16 = qkv_dtype == GDN_BF16;
+  const cudaError_t e = gdn::launch_decode(a, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(GDN_ELAUNCH, "gdn_decode_step: launch failed: %s", cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_check_status(void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaStreamSynchronize(s);

@@ -31,6 +31,20 @@ int simt_launches(const FwdArgs& a);
 bool tc_supported(int dk, int dv, int C, int bf16);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream);
 int tc_launches(const FwdArgs& a);
+// Single-token decode step (recurrent form), already validated by the API layer.
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_alpha;
+  const float* beta;
+  float* S;               // updated in place
+  void* out;
+  int N, H, dk, dv;
+  int bf16;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
 // Reads and clears the tcgen05 kernel's device status word (synchronous copy).
 // Returns 0 if clear, else the code a bounded wait recorded.
 int tc_read_and_clear_status(cudaStream_t stream, cudaError_t* err);

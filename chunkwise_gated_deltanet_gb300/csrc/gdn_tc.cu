@@ -270,6 +270,14 @@ __device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a, uint32_t pa16, 
       mma_bf16(d, ap + kStepK * k, bp + (B_MN ? kStepMN : kStepK) * k, id, (p | k) ? 1u : acc_first);
   }
 }
+// Out-of-line form of mma_k128<false> followed by a commit, shared by the roles that
+// are not on the serial path (one copy of the issue code in the instruction cache).
+__device__ __noinline__ void mma_k128_commit(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                             uint64_t* bar) {
+  tc_fence_after();
+  mma_k128<false>(d, a, 16384 >> 4, b, 16384 >> 4, id, 0);
+  mma_commit(bar);
+}
 // K = 64 (4 k-steps): A from TMEM (8 columns per step) or MN-major smem; B K-major
 // or MN-major.  UNROLL for the chain's own MMAs, rolled elsewhere.
 template <bool A_TMEM, bool B_MN, bool UNROLL>
@@ -430,6 +438,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
     // ---------------- producer: K tiles by TMA, gate factors ----------------
     int issued = 0;
     GateLoad next = load_gates(log_alpha, beta, u, H, 0, lane);
+    #pragma unroll 1
     for (int j = 0; j < u.nc; ++j) {
       const int s = j % WY_NST;
       const uint32_t use = j / WY_NST;
@@ -460,6 +469,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       if (lane == 0) mbar_arrive(&bars[WB_KV_FULL + s]);
     }
     // copies still in flight must land before the CTA can leave
+    #pragma unroll 1
     for (int j = issued - WY_NST; j < issued; ++j)
       if (j >= 0) (void)mbar_wait(&bars[WB_KV_FULL + j % WY_NST], (j / WY_NST) & 1, 100000000ull);
     return;
@@ -483,6 +493,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
 #define WY_WAIT(bar, par, cl) \
   if (group_waits_fail(abort_flag, nb, 128, (bar), (par), (cl))) break;
 
+  #pragma unroll 1
   for (int j = w; j < u.nc; j += WY_NWG) {
     const int s = j % WY_NST;
     uint8_t* st = sm + WY_KV + s * WY_STAGE;
@@ -709,6 +720,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
     // ---------------- producer: Q, K, V tiles by TMA, gate factors ----------------
     int issued = 0;
     GateLoad next = load_gates(log_alpha, beta, u, H, 0, lane);
+    #pragma unroll 1
     for (int j = 0; j < u.nc; ++j) {
       const int s = j % ST_NST;
       const uint32_t use = j / ST_NST;
@@ -740,6 +752,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[SB_QK_FULL + s]);
     }
+    #pragma unroll 1
     for (int j = issued - ST_NST; j < issued; ++j)
       if (j >= 0) (void)mbar_wait(&bars[SB_QK_FULL + j % ST_NST], (j / ST_NST) & 1, 100000000ull);
     return;
@@ -752,6 +765,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
     // issued in chunk order; the warp polls (non-blocking tests), U first.
     int nu = 0, nd = 0;  // next U, delta^T P^T
     uint64_t t_idle = globaltimer_ns();
+    #pragma unroll 1
     while (nd < u.nc) {
       int kind = -1;
       if (nu < u.nc) {  // U(i) goes in behind the state update of i - 1
@@ -867,6 +881,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       named_sync(1, 128);
     } while (0);
 
+    #pragma unroll 1
     for (int j = 0; alive && j < u.nc; ++j) {
       const int s = j % ST_NST;
       const float* ED = der_all + s * ST_DER_STAGE + 128;
@@ -954,6 +969,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
     const int atid = tid - 128;
 #define AP_WAIT(bar, par) \
   if (group_wait_fails((bar), (par), abort_flag, false, 2, 128)) break;
+    #pragma unroll 1
     for (int j = 0; j < u.nc; ++j) {
       const int s = j % ST_NST;
       const int b = j & 1;
@@ -965,12 +981,9 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       const bool factored = flags[s] != 0;
 
       // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T), issued from warp 6 ----
-      if (atid == 64) {
-        tc_fence_after();
-        mma_k128<false>(tmem + TT_QK, desc_k(stg, 0, 16384), 16384 >> 4, desc_k(stg + 8192, 0, 16384),
-                        16384 >> 4, idesc_bf16(128, 64, 0, 0), 0);
-        mma_commit(&bars[SB_QKM]);
-      }
+      if (atid == 64)
+        mma_k128_commit(tmem + TT_QK, desc_k(stg, 0, 16384), desc_k(stg + 8192, 0, 16384),
+                        idesc_bf16(128, 64, 0, 0), &bars[SB_QKM]);
       AP_WAIT(&bars[SB_QKM], j & 1);
       AP_WAIT(&bars[SB_PE + b], ((j >> 1) & 1) ^ 1);  // outputs of chunk j - 2 left slot b
       tc_fence_after();
@@ -1025,6 +1038,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   // Iteration i drains the outputs of chunk i - 1 out of TMEM, issues S Q^T (i), then
   // copies chunk i - 1 out: one issue site.
   GateLoad gnext = load_gates(log_alpha, beta, u, H, 0, lane);
+  #pragma unroll 1
   for (int i = 0; i <= u.nc; ++i) {
     const int j = i - 1, b = j & 1;
     __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(sm + ST_PS + b * PS_BYTES);
@@ -1061,13 +1075,10 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       AO_WAIT(&bars[SB_SWI], i & 1);
       const int si = i % ST_NST;
       if (flags[si] == 0) AO_WAIT(&bars[SB_PF + (i & 1)], (i >> 1) & 1);
-      if (atid == 96) {
-        tc_fence_after();
-        mma_k128<false>(tmem + TT_O, desc_k(sm + ST_SB, 0, 16384), 16384 >> 4,
-                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), 16384 >> 4,
-                        idesc_bf16(128, 64, 0, 0), 0);
-        mma_commit(&bars[SB_SQ]);
-      }
+      if (atid == 96)
+        mma_k128_commit(tmem + TT_O, desc_k(sm + ST_SB, 0, 16384),
+                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),
+                        &bars[SB_SQ]);
     }
     if (i > 0) {
       const long long c0 = (long long)j * kC;

@@ -19,8 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
-EXPORTS = ("gdn_chunk_fwd", "gdn_select_path", "gdn_launches_per_call", "gdn_check_status",
-           "gdn_last_error", "gdn_version")
+EXPORTS = ("gdn_chunk_fwd", "gdn_decode_step", "gdn_select_path", "gdn_launches_per_call",
+           "gdn_check_status", "gdn_last_error", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -44,6 +44,8 @@ def load_library(path: str = LIB_PATH):
     P, I = ctypes.c_void_p, ctypes.c_int
     lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, I, I, P]
     lib.gdn_chunk_fwd.restype = I
+    lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
+    lib.gdn_decode_step.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
         getattr(lib, name).argtypes = [I, I, I, I]
         getattr(lib, name).restype = I
@@ -152,3 +154,37 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, C: int = 64,
         torch.cuda.current_stream().synchronize()
         return out_h, Sf_h
     return out, Sf
+
+
+def gdn_decode_step(q, k, v, log_alpha, beta, S, out,
+                    stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name (one token per
+    (sequence, head), state updated in place).
+
+    Shapes: q, k [N, H, dk]; v, out [N, H, dv]; log_alpha, beta [N, H] fp32;
+    S [N, H, dv, dk] fp32.  All tensors contiguous on one CUDA device.  Launches on
+    ``stream`` (default: the current torch stream) and returns without synchronising.
+    """
+    lib = load_library()
+    N, H, dk = k.shape
+    dv = v.shape[-1]
+    for t in (q, k, v, log_alpha, beta, S, out):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("gdn_decode_step: every tensor must be a contiguous CUDA tensor")
+    code = _dtype_code(v.dtype)
+    if q.dtype != v.dtype or k.dtype != v.dtype or out.dtype != v.dtype:
+        raise TypeError("q, k, v and out must share one dtype")
+    for name, t in (("log_alpha", log_alpha), ("beta", beta), ("S", S)):
+        if t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    s = stream if stream is not None else torch.cuda.current_stream(v.device)
+    _check(lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
+                               _ptr(out), N, H, dk, dv, code, ctypes.c_void_p(s.cuda_stream)))
+
+
+def decode_step(q, k, v, log_alpha, beta, S) -> torch.Tensor:
+    """One decode token for every (sequence, head): updates S in place on the current
+    stream and returns the output tensor [N, H, dv] (same dtype as v)."""
+    out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    gdn_decode_step(q, k, v, log_alpha, beta, S, out)
+    return out

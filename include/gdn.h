@@ -83,6 +83,33 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v,
                   const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
                   void* stream);
 
+/*
+ * gdn_decode_step -- one token of the same recurrence for a batch of sequences,
+ * the recurrent form (Nyysyyan, "Gated-DeltaNet" section, first equation block;
+ * kkkzoz, "Gated DeltaNet" section: gate, predict, delta, write, then read):
+ *
+ *     S <- alpha S (I - beta k k^T) + beta v k^T,   o = S q
+ *
+ * computed as p = S k, u = beta (v - alpha p), S <- alpha S + u k^T and
+ * o = alpha (S q) + u (k . q), with the state read once and written once.
+ *
+ * q, k       [N, H, dk]      qkv_dtype, the token of each (sequence, head)
+ * v          [N, H, dv]      qkv_dtype
+ * log_alpha  [N, H]          fp32, natural log of alpha in (0, 1], so <= 0
+ * beta       [N, H]          fp32 writing strength
+ * S          [N, H, dv, dk]  fp32 state per (sequence, head), updated IN PLACE (required)
+ * out        [N, H, dv]      qkv_dtype, o for every (sequence, head)
+ * N, H       sequences and heads (N * H >= 0; 0 launches nothing)
+ * dk, dv     head sizes, each one of 16, 32, 64, 128
+ * qkv_dtype  a gdn_dtype code
+ * stream     cudaStream_t (NULL = legacy default stream)
+ *
+ * Asynchronous.  Arithmetic is fp32 (bf16 inputs are widened exactly); `out` is
+ * rounded to nearest even for bf16.  `out` must not overlap the inputs or S.
+ */
+int gdn_decode_step(const void* q, const void* k, const void* v,
+                    const float* log_alpha, const float* beta, float* S, void* out,
+                    int N, int H, int dk, int dv, int qkv_dtype, void* stream);
 /* The path gdn_chunk_fwd takes for these sizes, GDN_PATH_NONE if unsupported. */
 int gdn_select_path(int dk, int dv, int C, int qkv_dtype);
 

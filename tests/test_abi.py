@@ -129,3 +129,31 @@ def test_missing_library_fails_loudly(tmp_path):
             binding.load_library(str(tmp_path / "nope.so"))
     finally:
         binding._lib = saved
+
+
+def _call_decode(lib, **over):
+    """Call gdn_decode_step with fake (never dereferenced) aligned pointers."""
+    a = dict(q=4096, k=8192, v=12288, la=16384, be=20480, S=24576, out=28672,
+             N=8, H=4, dk=64, dv=64, dt=gdn.GDN_F32, stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_decode_step(P(a["q"]), P(a["k"]), P(a["v"]), P(a["la"]), P(a["be"]), P(a["S"]),
+                               P(a["out"]), a["N"], a["H"], a["dk"], a["dv"], a["dt"],
+                               P(a["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dt=7), gdn.GDN_EDTYPE if hasattr(gdn, "GDN_EDTYPE") else 2),
+    (dict(dk=48), 1), (dict(dv=256), 1), (dict(N=-1), 1), (dict(H=-2), 1),
+    (dict(q=None), 1), (dict(S=None), 1), (dict(out=None), 1), (dict(la=None), 1),
+    (dict(k=8200), 1), (dict(S=24580), 1),
+])
+def test_decode_rejects_invalid_arguments(lib, over, code):
+    assert _call_decode(lib, **over) == code
+    assert lib.gdn_last_error()
+
+
+def test_decode_empty_batch_launches_nothing(lib):
+    # N * H == 0 returns OK before looking at the pointers (nothing to launch)
+    assert _call_decode(lib, N=0, q=None, S=None, out=None) == binding.GDN_OK
+    assert _call_decode(lib, H=0) == binding.GDN_OK

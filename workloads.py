@@ -134,3 +134,54 @@ def make_inputs(w: Workload, *, B: Optional[int] = None, H: Optional[int] = None
 
 def n_tokens(inp: dict) -> int:
     return inp["B"] * inp["T"]
+
+
+# ---- single-token decode step (one token for each (sequence, head)) ----
+# Recipe: q, k, v, beta, log_alpha as above with T = 1, plus the state
+# S ~ N(0, s_std^2) per (sequence, head); draw order q, k, v, beta-logits,
+# alpha-logits, S.  The batch is sized so that the state (N * H * dv * dk * 4
+# bytes = 256 MiB at N = 256, H = 16, d = 128) is larger than the L2 cache.
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    dtype: str
+    N: int                # sequences
+    H: int
+    dk: int
+    dv: int
+    alpha_mu: float
+    s_std: float
+    seed: int = 0
+
+
+DECODE_WORKLOADS = {
+    "decode_bf16_n256h16d128": DecodeWorkload(
+        "decode_bf16_n256h16d128", "bf16", N=256, H=16, dk=128, dv=128, alpha_mu=2.0, s_std=0.5),
+    "decode_f32_n64h8d64": DecodeWorkload(
+        "decode_f32_n64h8d64", "f32", N=64, H=8, dk=64, dv=64, alpha_mu=2.0, s_std=0.5),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, *, N: Optional[int] = None, H: Optional[int] = None,
+                       dk: Optional[int] = None, dv: Optional[int] = None,
+                       seed: Optional[int] = None) -> dict:
+    """Draw the seeded inputs of decode workload ``w`` on the CPU: q, k [N, H, dk];
+    v [N, H, dv] in the workload dtype; log_alpha, beta [N, H] fp32; S [N, H, dv, dk]
+    fp32; plus the integer sizes."""
+    N = w.N if N is None else N
+    H = w.H if H is None else H
+    dk = w.dk if dk is None else dk
+    dv = w.dv if dv is None else dv
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    dt = torch_dtype(w.dtype)
+    q = _unit_rows(torch.randn(N, H, dk, generator=g)).to(dt)
+    k = _unit_rows(torch.randn(N, H, dk, generator=g)).to(dt)
+    v = torch.randn(N, H, dv, generator=g).to(dt)
+    beta = torch.sigmoid(torch.randn(N, H, generator=g))
+    x = torch.randn(N, H, generator=g) + w.alpha_mu
+    log_alpha = -torch.nn.functional.softplus(-x)
+    S = torch.randn(N, H, dv, dk, generator=g) * w.s_std
+    return dict(q=q.contiguous(), k=k.contiguous(), v=v.contiguous(),
+                log_alpha=log_alpha.contiguous(), beta=beta.contiguous(), S=S.contiguous(),
+                N=N, H=H, dk=dk, dv=dv, dtype=w.dtype)
