@@ -120,7 +120,7 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* lo
   for (int i = 0; i < 7; ++i)
     if (!aligned16(ptrs[i]))
       return fail(GDN_EINVAL, "gdn_decode_step: %s is not 16-byte aligned", names[i]);
-  if ((long long)N * H > 0x7fffffffLL)
+  if (gdn::decode_ctas(N, H, dk, dv) > 0x7fffffffLL)
     return fail(GDN_EINVAL, "gdn_decode_step: problem too large");
   gdn::DecodeArgs a;
   a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S = S; a.out = out;

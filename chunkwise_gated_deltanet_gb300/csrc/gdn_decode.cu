@@ -9,13 +9,17 @@
 //     p = S k,  u = beta (v - alpha p),  S <- alpha S + u k^T,
 //     o = S_new q = alpha (S q) + u (k . q).
 //
-// One CTA of 8 warps per (sequence, head).  S is dv x dk fp32 (row-major, dk
-// inner).  A row is covered by LPR = dk / 4 lanes holding 4 consecutive columns
-// each, so one warp-wide float4 access covers 32 / LPR whole rows (one 512-byte
-// contiguous run for dk = 128).  Warp w takes rows w * RPW, (w + 8) * RPW, ...
-// Each lane keeps its part of S in registers between the read and the write; no
-// CTA-wide synchronisation is needed.  The step is bound by HBM: 2 dk dv 4 bytes of
-// state per (sequence, head) against a few hundred FLOPs per byte-pair.
+// The step is bound by HBM: 2 dk dv 4 bytes of state move per (sequence, head),
+// against about 7 dk dv FLOPs.  Rows of S are independent once k, q, alpha and
+// beta are known, so the work is cut by rows: one warp per CTA takes kDecRows4
+// float4 accesses per lane over a block of rows.  A row is covered by
+// LPR = dk / 4 lanes holding 4 consecutive columns each, so one warp access covers
+// RPW = 32 / LPR whole rows (one 512-byte contiguous run for dk = 128); a CTA
+// covers RPW * kDecRows4 rows (8 for dk = 128), and a (sequence, head) takes
+// ceil(dv / that) CTAs.  Small single-warp CTAs keep 32 of them resident per SM,
+// each with all of its loads in flight before its first use, which keeps HBM
+// busy through the read-then-write shape of the step; each lane holds its part of
+// S in registers between the read and the write, with no synchronisation.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -24,7 +28,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kDecThreads = 256;  // 8 warps
+constexpr int kDecThreads = 32;  // one warp
+constexpr int kDecRows4 = 8;     // float4 accesses of S per lane
 
 __device__ __forceinline__ float4 load4(const void* p, size_t idx, bool bf16) {
   if (bf16) {
@@ -40,19 +45,22 @@ __device__ __forceinline__ float load1(const void* p, size_t idx, bool bf16) {
 }
 
 template <int DK>
+__device__ __forceinline__ constexpr int rows_per_cta() { return (32 / (DK / 4)) * kDecRows4; }
+
+template <int DK, bool BF16>
 __global__ void __launch_bounds__(kDecThreads)
 gdn_decode_kernel(const void* __restrict__ q, const void* __restrict__ k,
                   const void* __restrict__ v, const float* __restrict__ log_alpha,
                   const float* __restrict__ beta, float* __restrict__ S, void* __restrict__ out,
-                  int dv, int bf16) {
+                  int dv, int splits) {
   constexpr int LPR = DK / 4;        // lanes per row
   constexpr int RPW = 32 / LPR;      // rows per warp access
-  constexpr int MAXIT = 128 / (8 * RPW);  // accesses per lane for dv = 128
-  const int nh = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nh = blockIdx.x / splits;
+  const int row0 = (blockIdx.x - nh * splits) * rows_per_cta<DK>();
+  const int lane = threadIdx.x;
   const int c4 = lane % LPR;         // this lane's columns 4 c4 .. 4 c4 + 3
   const int rsub = lane / LPR;       // row within the warp access
-  const bool isbf = bf16 != 0;
+  constexpr bool isbf = BF16;
 
   const float alpha = expf(log_alpha[nh]);
   const float b = beta[nh];
@@ -64,16 +72,16 @@ gdn_decode_kernel(const void* __restrict__ q, const void* __restrict__ k,
   for (int o = LPR / 2; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
 
   float4* Sv = reinterpret_cast<float4*>(S + (size_t)nh * dv * DK);
-  float4 s[MAXIT];
+  float4 s[kDecRows4];
   // issue every load of this lane's part of S before using any
 #pragma unroll
-  for (int it = 0; it < MAXIT; ++it) {
-    const int r = (it * 8 + warp) * RPW + rsub;
+  for (int it = 0; it < kDecRows4; ++it) {
+    const int r = row0 + it * RPW + rsub;
     if (r < dv) s[it] = Sv[(size_t)r * LPR + c4];
   }
 #pragma unroll
-  for (int it = 0; it < MAXIT; ++it) {
-    const int r = (it * 8 + warp) * RPW + rsub;
+  for (int it = 0; it < kDecRows4; ++it) {
+    const int r = row0 + it * RPW + rsub;
     float p = 0.f, sq = 0.f;
     if (r < dv) {
       p = s[it].x * kk.x + s[it].y * kk.y + s[it].z * kk.z + s[it].w * kk.w;
@@ -101,34 +109,36 @@ gdn_decode_kernel(const void* __restrict__ q, const void* __restrict__ k,
   }
 }
 
+template <int DK>
+cudaError_t launch_decode_dk(const DecodeArgs& a, cudaStream_t stream) {
+  const int splits = (a.dv + rows_per_cta<DK>() - 1) / rows_per_cta<DK>();
+  const long long ctas = (long long)a.N * a.H * splits;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (a.bf16)
+    gdn_decode_kernel<DK, true><<<(unsigned)ctas, kDecThreads, 0, stream>>>(
+        a.q, a.k, a.v, a.log_alpha, a.beta, a.S, a.out, a.dv, splits);
+  else
+    gdn_decode_kernel<DK, false><<<(unsigned)ctas, kDecThreads, 0, stream>>>(
+        a.q, a.k, a.v, a.log_alpha, a.beta, a.S, a.out, a.dv, splits);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
+long long decode_ctas(long long N, long long H, int dk, int dv) {
+  const int rows = (32 / (dk / 4)) * kDecRows4;  // rows_per_cta<dk>()
+  return N * H * ((dv + rows - 1) / rows);
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  const long long ctas = (long long)a.N * a.H;
-  if (ctas == 0) return cudaSuccess;
-  if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-  const dim3 grid((unsigned)ctas);
+  if ((long long)a.N * a.H == 0) return cudaSuccess;
   switch (a.dk) {
-    case 16:
-      gdn_decode_kernel<16><<<grid, kDecThreads, 0, stream>>>(a.q, a.k, a.v, a.log_alpha, a.beta,
-                                                              a.S, a.out, a.dv, a.bf16);
-      break;
-    case 32:
-      gdn_decode_kernel<32><<<grid, kDecThreads, 0, stream>>>(a.q, a.k, a.v, a.log_alpha, a.beta,
-                                                              a.S, a.out, a.dv, a.bf16);
-      break;
-    case 64:
-      gdn_decode_kernel<64><<<grid, kDecThreads, 0, stream>>>(a.q, a.k, a.v, a.log_alpha, a.beta,
-                                                              a.S, a.out, a.dv, a.bf16);
-      break;
-    case 128:
-      gdn_decode_kernel<128><<<grid, kDecThreads, 0, stream>>>(a.q, a.k, a.v, a.log_alpha, a.beta,
-                                                               a.S, a.out, a.dv, a.bf16);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+    case 16: return launch_decode_dk<16>(a, stream);
+    case 32: return launch_decode_dk<32>(a, stream);
+    case 64: return launch_decode_dk<64>(a, stream);
+    case 128: return launch_decode_dk<128>(a, stream);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace gdn

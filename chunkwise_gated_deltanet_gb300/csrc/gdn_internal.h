@@ -43,6 +43,8 @@ struct DecodeArgs {
   int N, H, dk, dv;
   int bf16;
 };
+// CTAs the decode step launches for these sizes (dk one of 16, 32, 64, 128).
+long long decode_ctas(long long N, long long H, int dk, int dv);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Reads and clears the tcgen05 kernel's device status word (synchronous copy).
