@@ -33,6 +33,7 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 METRIC = "gated-DeltaNet chunkwise fwd tokens/s and % of roofline, 1×GB300"
+LINEAR_METRIC = "linear-attention (Mamba2 gate) chunkwise fwd tokens/s and % of roofline, 1×GB300"
 DECODE_METRIC = "gated-DeltaNet decode step tokens/s and % of roofline, 1×GB300"
 L2_FLUSH_BYTES = 512 << 20
 
@@ -58,7 +59,8 @@ def algorithmic(inp: dict) -> dict:
     th = inp["B"] * inp["T"] * inp["H"]
     dk, dv, C = inp["dk"], inp["dv"], inp["C"]
     units = inp["N"] * inp["H"]
-    by = th * ((2 * dk + dv) * esz + dv * esz + 8)
+    gates = 4 if inp.get("linear") else 8  # the linear mode reads no beta
+    by = th * ((2 * dk + dv) * esz + dv * esz + gates)
     if inp["S0"] is not None:
         by += units * dv * dk * 4
     by += units * dv * dk * 4  # S_final
@@ -153,8 +155,14 @@ def max_over_ranks(x: float, world: int, dev) -> float:
 
 def cpu_oracle_time(inp: dict, budget_s: float = 20.0):
     """Time the fp64 oracle on the host cores over a bounded sample of
-    (sequence, head) units of the workload.  Returns (tokens/s, cores, sample)."""
+    (sequence, head) units of the workload.  Returns (tokens/s, cores, sample).
+    The linear mode runs the oracle with erase strength 0 and write strength 1."""
     from oracle import native
+    ew = {}
+    beta = inp["beta"]
+    if inp.get("linear"):
+        beta = torch.zeros_like(inp["log_alpha"])  # unused once erase and write are given
+        ew = dict(erase=beta, write=torch.ones_like(inp["log_alpha"]))
     spans = native.spans(inp["B"], inp["T"], inp["cu_seqlens"])
     H = inp["H"]
     units_all = [(s, h) for s in range(len(spans)) for h in range(H)]
@@ -162,8 +170,8 @@ def cpu_oracle_time(inp: dict, budget_s: float = 20.0):
     # probe one unit to size the sample
     probe = [units_all[0]]
     t0 = time.perf_counter()
-    native.gdn_units_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], inp["S0"],
-                       inp["cu_seqlens"], probe, n_threads=1)
+    native.gdn_units_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], beta, inp["S0"],
+                       inp["cu_seqlens"], probe, n_threads=1, **ew)
     per_tok_thread = (time.perf_counter() - t0) / max(1, spans[0][1])
     total_tok_heads = sum(l for _, l in spans) * H
     est = per_tok_thread * total_tok_heads / max(1, cores)
@@ -174,8 +182,8 @@ def cpu_oracle_time(inp: dict, budget_s: float = 20.0):
         step = max(1, int(round(1 / frac)))
         units = units_all[::step]
     t0 = time.perf_counter()
-    native.gdn_units_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], inp["S0"],
-                       inp["cu_seqlens"], units, n_threads=cores)
+    native.gdn_units_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], beta, inp["S0"],
+                       inp["cu_seqlens"], units, n_threads=cores, **ew)
     dt = time.perf_counter() - t0
     tok_heads = sum(spans[s][1] for s, _ in units)
     tokens_per_s = tok_heads / H / dt  # tokens of all heads, per second
@@ -187,7 +195,7 @@ def cpu_oracle_time(inp: dict, budget_s: float = 20.0):
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
-    inp = workloads.make_inputs(w)
+    inp = dict(workloads.make_inputs(w), linear=w.linear)
     for _ in range(args.warmup if args.warmup > 0 else 0):
         pass  # the oracle has no state to warm; warm-up steps are not timed
     vals, times = [], []
@@ -197,7 +205,8 @@ def run_reference(args, w, world, rank):
         vals.append(v)
         times.append(dt)
     value = statistics.median(vals)
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    line = {"metric": LINEAR_METRIC if w.linear else METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * n_tokens_of(inp) / value, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -396,7 +405,9 @@ def main():
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    inp = workloads.make_inputs(w)
+    inp = dict(workloads.make_inputs(w), linear=w.linear)
+    if w.linear:
+        inp["beta"] = None  # the linear mode takes no beta (nor copies it end to end)
     d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
     B, T, H, dk, dv, C, N = inp["B"], inp["T"], inp["H"], w.dk, w.dv, w.C, inp["N"]
     out = torch.empty((B, T, H, dv), dtype=d["v"].dtype, device=dev)
@@ -405,8 +416,12 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], out, Sf,
-                          C, d["cu_seqlens"], stream=stream)
+        if w.linear:
+            gdn.gdn_linear_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["S0"], out, Sf,
+                                     C, d["cu_seqlens"], stream=stream)
+        else:
+            gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], out,
+                              Sf, C, d["cu_seqlens"], stream=stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -479,7 +494,8 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "metric": LINEAR_METRIC if w.linear else METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if path == gdn.GDN_PATH_TCGEN05 else "f32",

@@ -49,29 +49,32 @@ int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype) {
   }
 }
 
-int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha,
-                  const float* beta, const float* S0, void* out, float* S_final, int B, int H,
-                  int T, int dk, int dv, int C, const int32_t* cu_seqlens, int N_seqs,
-                  int qkv_dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The checks and launch shared by gdn_chunk_fwd and gdn_linear_chunk_fwd.  With
+// linear set, beta is NULL (erase 0, write 1) and log_alpha may be NULL (alpha = 1).
+int chunk_fwd_impl(const char* fn, bool linear, const void* q, const void* k, const void* v,
+                   const float* log_alpha, const float* beta, const float* S0, void* out,
+                   float* S_final, int B, int H, int T, int dk, int dv, int C,
+                   const int32_t* cu_seqlens, int N_seqs, int qkv_dtype, void* stream) {
   if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
-    return fail(GDN_EDTYPE, "gdn_chunk_fwd: qkv_dtype %d is neither GDN_F32 nor GDN_BF16",
-                qkv_dtype);
-  if (T > 0 && (!q || !k || !v || !log_alpha || !beta || !out))
-    return fail(GDN_EINVAL, "gdn_chunk_fwd: q, k, v, log_alpha, beta and out must be non-NULL");
+    return fail(GDN_EDTYPE, "%s: qkv_dtype %d is neither GDN_F32 nor GDN_BF16", fn, qkv_dtype);
+  if (T > 0 && (!q || !k || !v || !out))
+    return fail(GDN_EINVAL, "%s: q, k, v and out must be non-NULL", fn);
+  if (T > 0 && !linear && (!log_alpha || !beta))
+    return fail(GDN_EINVAL, "%s: log_alpha and beta must be non-NULL", fn);
   if (B <= 0 || H <= 0 || T < 0)
-    return fail(GDN_EINVAL, "gdn_chunk_fwd: need B > 0, H > 0, T >= 0 (got B=%d H=%d T=%d)", B,
-                H, T);
+    return fail(GDN_EINVAL, "%s: need B > 0, H > 0, T >= 0 (got B=%d H=%d T=%d)", fn, B, H, T);
   if (!head_ok(dk) || !head_ok(dv))
-    return fail(GDN_EINVAL, "gdn_chunk_fwd: dk and dv must be 16, 32, 64 or 128 (got %d, %d)",
-                dk, dv);
-  if (!chunk_ok(C))
-    return fail(GDN_EINVAL, "gdn_chunk_fwd: C must be 16, 32 or 64 (got %d)", C);
+    return fail(GDN_EINVAL, "%s: dk and dv must be 16, 32, 64 or 128 (got %d, %d)", fn, dk, dv);
+  if (!chunk_ok(C)) return fail(GDN_EINVAL, "%s: C must be 16, 32 or 64 (got %d)", fn, C);
   int N = B;
   if (cu_seqlens) {
-    if (B != 1) return fail(GDN_EINVAL, "gdn_chunk_fwd: packed sequences need B == 1 (got %d)", B);
+    if (B != 1) return fail(GDN_EINVAL, "%s: packed sequences need B == 1 (got %d)", fn, B);
     if (N_seqs <= 0)
-      return fail(GDN_EINVAL, "gdn_chunk_fwd: N_seqs must be > 0 with cu_seqlens (got %d)",
-                  N_seqs);
+      return fail(GDN_EINVAL, "%s: N_seqs must be > 0 with cu_seqlens (got %d)", fn, N_seqs);
     N = N_seqs;
   }
   const void* ptrs[] = {q, k, v, log_alpha, beta, S0, out, S_final, cu_seqlens};
@@ -79,14 +82,14 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
                          "cu_seqlens"};
   for (int i = 0; i < 9; ++i)
     if (ptrs[i] && !aligned16(ptrs[i]))
-      return fail(GDN_EINVAL, "gdn_chunk_fwd: %s is not 16-byte aligned", names[i]);
+      return fail(GDN_EINVAL, "%s: %s is not 16-byte aligned", fn, names[i]);
   const long long rows = (long long)B * T;
   if (rows * H * (dk > dv ? dk : dv) > (1LL << 40))
-    return fail(GDN_EINVAL, "gdn_chunk_fwd: problem too large");
+    return fail(GDN_EINVAL, "%s: problem too large", fn);
 
   gdn::FwdArgs a;
-  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
-  a.out = out; a.S_final = S_final; a.cu_seqlens = cu_seqlens;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = linear ? nullptr : beta;
+  a.S0 = S0; a.out = out; a.S_final = S_final; a.cu_seqlens = cu_seqlens;
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.C = C; a.N = N;
   a.bf16 = qkv_dtype == GDN_BF16;
   cudaStream_t s = (cudaStream_t)stream;
@@ -97,8 +100,28 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
   else
     e = gdn::launch_simt(a, s);
   if (e != cudaSuccess)
-    return fail(GDN_ELAUNCH, "gdn_chunk_fwd: launch failed: %s", cudaGetErrorString(e));
+    return fail(GDN_ELAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha,
+                  const float* beta, const float* S0, void* out, float* S_final, int B, int H,
+                  int T, int dk, int dv, int C, const int32_t* cu_seqlens, int N_seqs,
+                  int qkv_dtype, void* stream) {
+  return chunk_fwd_impl("gdn_chunk_fwd", false, q, k, v, log_alpha, beta, S0, out, S_final, B,
+                        H, T, dk, dv, C, cu_seqlens, N_seqs, qkv_dtype, stream);
+}
+
+int gdn_linear_chunk_fwd(const void* q, const void* k, const void* v, const float* log_alpha,
+                         const float* S0, void* out, float* S_final, int B, int H, int T, int dk,
+                         int dv, int C, const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
+                         void* stream) {
+  return chunk_fwd_impl("gdn_linear_chunk_fwd", true, q, k, v, log_alpha, nullptr, S0, out,
+                        S_final, B, H, T, dk, dv, C, cu_seqlens, N_seqs, qkv_dtype, stream);
 }
 
 int gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha,

@@ -20,6 +20,10 @@
 // gamma_i / gamma_s factors; W~ is gamma_i w_i).  Only in-chunk differences
 // g_i - g_j with i >= j are exponentiated, so no factor exceeds 1 when
 // log alpha <= 0.
+//
+// Linear mode (beta == NULL; Nyysyyan, "Mamba2" and "Linear attention"): erase
+// strength 0 and write strength 1, so A = 0, W~ = 0, U = V and delta = V: the
+// same loop computes S_t = alpha_t S_{t-1} + v_t k_t^T.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -118,6 +122,7 @@ gdn_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn*
     Ss[j * L.ldk + d] = S0 ? S0[sbase + (size_t)j * dk + d] : 0.f;
   }
 
+  const float erase = beta ? 1.f : 0.f;  // erase strength factor (0 in the linear mode)
   for (long long c0 = 0; c0 < len; c0 += C) {
     const int lc = (int)min((long long)C, len - c0);
     __syncthreads();  // previous chunk is done with every buffer
@@ -142,8 +147,9 @@ gdn_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn*
     if (tid < C) {
       const bool ok = tid < lc;
       const size_t gi = (size_t)(row0 + c0 + tid) * H + h;
-      gs[tid] = ok ? log_alpha[gi] : 0.f;
-      bs[tid] = ok ? beta[gi] : 0.f;
+      // NULL log_alpha: alpha = 1; NULL beta (linear mode): write strength 1
+      gs[tid] = ok && log_alpha ? log_alpha[gi] : 0.f;
+      bs[tid] = ok ? (beta ? beta[gi] : 1.f) : 0.f;
     }
     __syncthreads();
     if (tid == 0) {  // inclusive cumsum of log alpha inside the chunk
@@ -167,7 +173,7 @@ gdn_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn*
           qk = fmaf(Qs[i * L.ldk + d], kj, qk);
         }
         const float dec = __expf(gs[i] - gs[j]);
-        if (j < i) a = bs[i] * kk * dec;
+        if (j < i) a = erase * bs[i] * kk * dec;
         p = qk * dec;
       }
       As[i * L.ldc + j] = a;
@@ -177,7 +183,7 @@ gdn_simt_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn*
     // ---- right-hand sides: diag(beta e^g) K and diag(beta) V ----
     for (int idx = tid; idx < C * dk; idx += kThreads) {
       const int r = idx / dk, d = idx % dk;
-      Ws[r * L.ldk + d] = bs[r] * egs[r] * Ks[r * L.ldk + d];
+      Ws[r * L.ldk + d] = erase * bs[r] * egs[r] * Ks[r * L.ldk + d];
     }
     for (int idx = tid; idx < C * dvt; idx += kThreads) {
       const int r = idx / dvt, j = idx % dvt;

@@ -28,6 +28,10 @@
 // factor, which aux O multiplies back.  It is used when the chunk's total decay
 // e^{g_last} is above 2^-80, so that e^{-g_j} stays inside the fp32 range.
 //
+// Linear mode (beta == NULL; Nyysyyan, "Mamba2" and "Linear attention"): the
+// erase strength is 0 and the write strength 1, so A = 0, T = I, W~ = 0 and
+// U = V exactly; the same pipeline then computes S_t = alpha_t S_{t-1} + v_t k_t^T.
+//
 // W~ uses the decayed triangular factor (W~_i = gamma_i w_i with the WY
 // recursion of Nyysyyan's "Gated-DeltaNet" section); then
 // delta = U - W~ S^T and the chunk's states and outputs follow from the unrolled
@@ -330,7 +334,9 @@ struct Unit {
 
 // Gate inputs of one chunk for a whole warp: thread `lane` owns tokens lane and
 // lane + 32 (zeros past the sequence end).  Split from the scan so the loads of
-// the next chunk can be in flight while the current one is processed.
+// the next chunk can be in flight while the current one is processed.  A NULL
+// log_alpha reads as alpha = 1; a NULL beta (the linear mode, erase 0) as a write
+// strength of 1.
 struct GateLoad {
   float la0, la1, b0, b1;
 };
@@ -341,13 +347,13 @@ __device__ __forceinline__ GateLoad load_gates(const float* __restrict__ log_alp
   const long long c0 = (long long)chunk * kC;
   if (chunk < u.nc && c0 + lane < u.len) {
     const size_t gi = (size_t)(u.row0 + c0 + lane) * H + u.h;
-    g.la0 = __ldg(log_alpha + gi);
-    g.b0 = __ldg(beta + gi);
+    g.la0 = log_alpha ? __ldg(log_alpha + gi) : 0.f;
+    g.b0 = beta ? __ldg(beta + gi) : 1.f;
   }
   if (chunk < u.nc && c0 + lane + 32 < u.len) {
     const size_t gi = (size_t)(u.row0 + c0 + lane + 32) * H + u.h;
-    g.la1 = __ldg(log_alpha + gi);
-    g.b1 = __ldg(beta + gi);
+    g.la1 = log_alpha ? __ldg(log_alpha + gi) : 0.f;
+    g.b1 = beta ? __ldg(beta + gi) : 1.f;
   }
   return g;
 }
@@ -456,12 +462,15 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       issued = j + 1;
       float g0, g1, tot;
       scan_gates(cur, lane, g0, g1, tot);
+      // write strengths b (beta, or 1 in the linear mode) and erase strengths
+      // (beta, or 0 in the linear mode, which makes A = 0, T = I and W~ = 0)
       const float b0 = cur.b0, b1 = cur.b1;
+      const float er0 = beta ? b0 : 0.f, er1 = beta ? b1 : 0.f;
       float* der = der_all + s * WY_DER_STAGE;  // G, EG, BG, BE, EN
       const float e0 = ex2(g0), e1 = ex2(g1);
       der[lane] = g0;                 der[lane + 32] = g1;
       der[64 + lane] = e0;            der[64 + lane + 32] = e1;
-      der[128 + lane] = b0 * e0;      der[128 + lane + 32] = b1 * e1;
+      der[128 + lane] = er0 * e0;     der[128 + lane + 32] = er1 * e1;
       der[192 + lane] = b0;           der[192 + lane + 32] = b1;
       der[256 + lane] = ex2(-g0);     der[256 + lane + 32] = ex2(-g1);
       if (lane == 0) flags[s] = (-tot < kMaxFactoredDecayLog2) ? 1 : 0;
@@ -524,7 +533,7 @@ __device__ __forceinline__ void run_wy(uint8_t* sm, uint32_t tmem, const CUtenso
       if (factored)
         wy_epi_a<true>(tq + WT_KK, Am + row * LDA, row, BG[row], 0.f, EN);
       else
-        wy_epi_a<false>(tq + WT_KK, Am + row * LDA, row, BE[row], G[row], G);
+        wy_epi_a<false>(tq + WT_KK, Am + row * LDA, row, beta ? BE[row] : 0.f, G[row], G);
     }
     named_sync(nb, 128);
 

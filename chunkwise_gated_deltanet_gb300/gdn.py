@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
-EXPORTS = ("gdn_chunk_fwd", "gdn_decode_step", "gdn_select_path", "gdn_launches_per_call",
+EXPORTS = ("gdn_chunk_fwd", "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_select_path", "gdn_launches_per_call",
            "gdn_check_status", "gdn_last_error", "gdn_version")
 
 
@@ -44,6 +44,8 @@ def load_library(path: str = LIB_PATH):
     P, I = ctypes.c_void_p, ctypes.c_int
     lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, I, I, P]
     lib.gdn_chunk_fwd.restype = I
+    lib.gdn_linear_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, I, I, P]
+    lib.gdn_linear_chunk_fwd.restype = I
     lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
     lib.gdn_decode_step.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
@@ -92,6 +94,37 @@ def gdn_check_status(stream: Optional[torch.cuda.Stream] = None) -> None:
     _check(load_library().gdn_check_status(ctypes.c_void_p(s.cuda_stream)))
 
 
+def _chunk_call(entry: str, q, k, v, log_alpha, beta, S0, out, S_final, C: int,
+                cu_seqlens, stream) -> None:
+    lib = load_library()
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    tensors = [q, k, v, log_alpha, beta, S0, out, S_final, cu_seqlens]
+    for t in tensors:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{entry}: every tensor must be a contiguous CUDA tensor")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    code = _dtype_code(v.dtype)
+    if q.dtype != v.dtype or k.dtype != v.dtype or out.dtype != v.dtype:
+        raise TypeError("q, k, v and out must share one dtype")
+    for name, t in (("log_alpha", log_alpha), ("beta", beta), ("S0", S0), ("S_final", S_final)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    n_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    s = ctypes.c_void_p((stream if stream is not None
+                         else torch.cuda.current_stream(v.device)).cuda_stream)
+    if entry == "gdn_chunk_fwd":
+        st = lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                               _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
+                               _ptr(cu_seqlens), n_seqs, code, s)
+    else:
+        st = lib.gdn_linear_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(S0),
+                                      _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
+                                      _ptr(cu_seqlens), n_seqs, code, s)
+    _check(st)
+
+
 def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, S_final, C: int,
                   cu_seqlens: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None) -> None:
@@ -102,26 +135,18 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, S_final, C: int,
     All tensors contiguous on one CUDA device.  Launches on ``stream`` (default:
     the current torch stream) and returns without synchronising.
     """
-    lib = load_library()
-    B, T, H, dk = k.shape
-    dv = v.shape[-1]
-    tensors = [q, k, v, log_alpha, beta, S0, out, S_final, cu_seqlens]
-    for t in tensors:
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError("gdn_chunk_fwd: every tensor must be a contiguous CUDA tensor")
-    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
-        raise TypeError("cu_seqlens must be int32")
-    code = _dtype_code(v.dtype)
-    if q.dtype != v.dtype or k.dtype != v.dtype or out.dtype != v.dtype:
-        raise TypeError("q, k, v and out must share one dtype")
-    for name, t in (("log_alpha", log_alpha), ("beta", beta), ("S0", S0), ("S_final", S_final)):
-        if t is not None and t.dtype != torch.float32:
-            raise TypeError(f"{name} must be float32")
-    n_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
-    s = stream if stream is not None else torch.cuda.current_stream(v.device)
-    _check(lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                             _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
-                             _ptr(cu_seqlens), n_seqs, code, ctypes.c_void_p(s.cuda_stream)))
+    _chunk_call("gdn_chunk_fwd", q, k, v, log_alpha, beta, S0, out, S_final, C, cu_seqlens,
+                stream)
+
+
+def gdn_linear_chunk_fwd(q, k, v, log_alpha, S0, out, S_final, C: int,
+                         cu_seqlens: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name: the linear mode
+    S_t = alpha_t S_{t-1} + v_t k_t^T (no beta; log_alpha None means alpha = 1).
+    Shapes and stream behaviour as in ``gdn_chunk_fwd``."""
+    _chunk_call("gdn_linear_chunk_fwd", q, k, v, log_alpha, None, S0, out, S_final, C,
+                cu_seqlens, stream)
 
 
 def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, C: int = 64,
@@ -153,6 +178,19 @@ def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, C: int = 64,
             Sf_h.copy_(Sf, non_blocking=True)
         torch.cuda.current_stream().synchronize()
         return out_h, Sf_h
+    return out, Sf
+
+
+def linear_chunk_fwd(q, k, v, log_alpha=None, S0=None, cu_seqlens=None, C: int = 64,
+                     output_final_state: bool = True):
+    """Allocate the outputs and run the linear-mode forward on the current stream
+    (device tensors).  Returns (out, S_final or None)."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    out = torch.empty((B, T, H, dv), dtype=v.dtype, device=v.device)
+    Sf = torch.empty((N, H, dv, dk), dtype=torch.float32, device=v.device) if output_final_state else None
+    gdn_linear_chunk_fwd(q, k, v, log_alpha, S0, out, Sf, C, cu_seqlens)
     return out, Sf
 
 

@@ -84,6 +84,25 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v,
                   void* stream);
 
 /*
+ * gdn_linear_chunk_fwd -- the same chunkwise forward in the linear mode: no delta-rule
+ * erase, a plain write (Nyysyyan, "Mamba2" section, its recurrence and chunk form;
+ * "Linear attention" section when alpha = 1):
+ *
+ *     S_t = alpha_t S_{t-1} + v_t k_t^T,   o_t = S_t q_t
+ *
+ * which is gdn_chunk_fwd's recurrence with the erase strength set to 0 and the
+ * write strength to 1.  Arguments, layouts, ownership, paths and errors are those of
+ * gdn_chunk_fwd, without beta; log_alpha may be NULL, meaning alpha_t = 1 (plain
+ * linear attention).
+ */
+int gdn_linear_chunk_fwd(const void* q, const void* k, const void* v,
+                         const float* log_alpha, const float* S0,
+                         void* out, float* S_final,
+                         int B, int H, int T, int dk, int dv, int C,
+                         const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
+                         void* stream);
+
+/*
  * gdn_decode_step -- one token of the same recurrence for a batch of sequences,
  * the recurrent form (Nyysyyan, "Gated-DeltaNet" section, first equation block;
  * kkkzoz, "Gated DeltaNet" section: gate, predict, delta, write, then read):

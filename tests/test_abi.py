@@ -157,3 +157,35 @@ def test_decode_empty_batch_launches_nothing(lib):
     # N * H == 0 returns OK before looking at the pointers (nothing to launch)
     assert _call_decode(lib, N=0, q=None, S=None, out=None) == binding.GDN_OK
     assert _call_decode(lib, H=0) == binding.GDN_OK
+
+
+def _call_linear(lib, **over):
+    """Call gdn_linear_chunk_fwd with fake (never dereferenced) aligned pointers."""
+    a = dict(q=4096, k=8192, v=12288, la=16384, S0=None, out=24576, Sf=None,
+             B=2, H=4, T=128, dk=64, dv=64, C=64, cu=None, N=0, dt=gdn.GDN_F32, stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_linear_chunk_fwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["la"]), P(a["S0"]),
+                                    P(a["out"]), P(a["Sf"]), a["B"], a["H"], a["T"], a["dk"],
+                                    a["dv"], a["C"], P(a["cu"]), a["N"], a["dt"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("over,code,word", [
+    (dict(dt=3), binding.GDN_EDTYPE, "dtype"),
+    (dict(v=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(B=0), binding.GDN_EINVAL, "B > 0"),
+    (dict(dk=24), binding.GDN_EINVAL, "dk and dv"),
+    (dict(C=48), binding.GDN_EINVAL, "C must be"),
+    (dict(cu=28672, N=3, B=2), binding.GDN_EINVAL, "B == 1"),
+    (dict(la=16388), binding.GDN_EINVAL, "log_alpha is not 16-byte aligned"),
+])
+def test_linear_invalid_arguments_rejected_before_launch(lib, over, code, word):
+    assert _call_linear(lib, **over) == code
+    msg = lib.gdn_last_error().decode()
+    assert msg.startswith("gdn_linear_chunk_fwd") and word in msg, msg
+
+
+def test_chunk_fwd_still_requires_beta(lib):
+    """Only the linear entry point may omit beta."""
+    assert _call(lib, be=None) == binding.GDN_EINVAL
+    assert "beta" in lib.gdn_last_error().decode()

@@ -1,0 +1,132 @@
+"""GPU parity of the linear mode (gdn_linear_chunk_fwd) against the oracle.
+
+The linear mode is the Mamba2 recurrence S_t = alpha_t S_{t-1} + v_t k_t^T,
+o_t = S_t q_t (Nyysyyan, "Mamba2"; with alpha = 1 the "Linear attention" section).
+The oracle is the per-token fp64 recurrence run with erase strength 0 and write
+strength 1; the oracle pins tie that setting to both pages' closed forms.
+Tolerances are those of the chunk forward (tests/parity.py).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import chunkwise_gated_deltanet_gb300 as gdn
+import workloads
+from oracle import native
+from tests.parity import assert_close, sample_units, to_device
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _gates(inp, alpha_one: bool):
+    la = torch.zeros_like(inp["log_alpha"]) if alpha_one else inp["log_alpha"]
+    zeros = torch.zeros_like(la)
+    return la, zeros, torch.ones_like(la)
+
+
+def _oracle(inp, alpha_one: bool, units=None):
+    la, zeros, ones = _gates(inp, alpha_one)
+    if units is None:
+        return native.gdn_forward_c(inp["q"], inp["k"], inp["v"], la, zeros, inp["S0"],
+                                    inp["cu_seqlens"], erase=zeros, write=ones)
+    return native.gdn_units_c(inp["q"], inp["k"], inp["v"], la, zeros, inp["S0"],
+                              inp["cu_seqlens"], units, erase=zeros, write=ones)
+
+
+def _gpu(inp, C: int, alpha_one: bool):
+    d = to_device(inp)
+    la = None if alpha_one else d["log_alpha"]
+    out, Sf = gdn.linear_chunk_fwd(d["q"], d["k"], d["v"], la, d["S0"], d["cu_seqlens"], C=C)
+    gdn.gdn_check_status()
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64), Sf.cpu().numpy().astype(np.float64)
+
+
+def _full(inp, C, alpha_one=False):
+    fp32 = inp["dtype"] == "f32"
+    o, s = _gpu(inp, C, alpha_one)
+    ro, rs = _oracle(inp, alpha_one)
+    assert_close(o, ro, fp32, "out", stored_bf16=not fp32)
+    assert_close(s, rs, fp32, "S_final")
+
+
+@pytest.mark.parametrize("alpha_one", [False, True], ids=["mamba2", "linear_attention"])
+@pytest.mark.parametrize("C", [16, 32, 64])
+def test_linear_f32(C, alpha_one):
+    inp = workloads.make_inputs(W["gdn_f32_b2h4t1024d64c64"], B=2, H=3, T=203, seed=C)
+    _full(inp, C, alpha_one)
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 128), (128, 64)])
+def test_linear_f32_head_sizes(dk, dv):
+    w = dataclasses.replace(W["gdn_f32_b2h4t1024d64c64"], dk=dk, dv=dv)
+    inp = workloads.make_inputs(w, B=1, H=2, T=77, seed=dk + dv)
+    _full(inp, 32)
+
+
+@pytest.mark.parametrize("alpha_one", [False, True], ids=["mamba2", "linear_attention"])
+def test_linear_bf16_tcgen05(alpha_one):
+    """bf16 at dk = dv = 128, C = 64 runs the tcgen05 kernel; several chunks and a
+    ragged tail on every (sequence, head), S0 given."""
+    w = W["gdn_bf16_b4h16t4096d128c64"]
+    assert gdn.gdn_select_path(128, 128, 64, torch.bfloat16) == gdn.GDN_PATH_TCGEN05
+    inp = workloads.make_inputs(w, B=2, H=3, T=333, seed=5)
+    inp["S0"] = torch.randn((2, 3, 128, 128), generator=torch.Generator().manual_seed(9)) * 0.1
+    _full(inp, 64, alpha_one)
+
+
+def test_linear_bf16_varlen():
+    w = W["gdn_bf16_varlen256_h16d128c64"]
+    inp = workloads.make_inputs(w, n_seqs=6, H=2, seed=3)
+    _full(inp, 64)
+
+
+def test_linear_bf16_headline_size_sampled():
+    """The headline shape in the linear mode, compared on sampled (sequence, head)
+    pairs that the oracle computes one by one."""
+    w = W["gdn_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(w)
+    o, s = _gpu(inp, 64, False)
+    units = sample_units(inp["N"], inp["H"], 6)
+    res = _oracle(inp, False, units)
+    got_o = np.concatenate([o[n, :, h] for n, h in units])
+    ref_o = np.concatenate([r[0] for r in res])
+    assert_close(got_o, ref_o, False, "out (sampled)", stored_bf16=True)
+    assert_close(np.stack([s[n, h] for n, h in units]), np.stack([r[1] for r in res]), False,
+                 "S_final (sampled)")
+
+
+def test_zero_write_reduces_to_pure_decay():
+    """With beta = 0 the delta rule writes nothing, so gdn_chunk_fwd is a pure
+    decay of S0; the linear mode with v = 0 is the same pure decay."""
+    w = W["gdn_f32_b2h4t1024d64c64"]
+    inp = workloads.make_inputs(w, B=1, H=2, T=130, seed=4)
+    d = to_device(inp)
+    _, s_gdn = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"],
+                             torch.zeros_like(d["beta"]), d["S0"], None, C=64)
+    _, s_lin = gdn.linear_chunk_fwd(d["q"], d["k"], torch.zeros_like(d["v"]), d["log_alpha"],
+                                    d["S0"], None, C=64)
+    torch.cuda.synchronize()
+    ref = inp["S0"].double() * torch.exp(inp["log_alpha"].double().sum(1))[0][:, None, None]
+    assert torch.allclose(s_gdn.cpu().double(), ref, rtol=1e-5, atol=1e-7)
+    assert torch.allclose(s_lin.cpu().double(), ref, rtol=1e-5, atol=1e-7)
+
+
+def test_linear_empty_sequence_returns_S0():
+    w = W["gdn_f32_b2h4t1024d64c64"]
+    inp = workloads.make_inputs(w, B=2, H=2, T=0)
+    o, s = _gpu(inp, 64, False)
+    assert o.size == 0
+    ref = np.zeros_like(s) if inp["S0"] is None else inp["S0"].numpy()
+    assert np.array_equal(s, ref)

@@ -46,6 +46,7 @@ class Workload:
     n_seqs: int = 0             # >0 => packed variable-length batch (B must be 1)
     len_lo: int = 0
     len_hi: int = 0
+    linear: bool = False        # True => the linear (Mamba2) mode: no beta, erase 0, write 1
 
     @property
     def varlen(self) -> bool:
@@ -69,6 +70,10 @@ WORKLOADS = {
     "gdn_bf16_varlen256_h16d128c64": Workload(
         "gdn_bf16_varlen256_h16d128c64", "bf16", B=1, H=16, T=0, dk=128, dv=128, C=64,
         alpha_mu=2.0, s0_std=0.0, n_seqs=256, len_lo=64, len_hi=2048),
+    # the headline sizes in the linear (Mamba2) mode: same draws, beta unused
+    "linear_bf16_b4h16t4096d128c64": Workload(
+        "linear_bf16_b4h16t4096d128c64", "bf16", B=4, H=16, T=4096, dk=128, dv=128, C=64,
+        alpha_mu=2.0, s0_std=0.0, linear=True),
 }
 
 # The headline workload that bench.py times by default.
