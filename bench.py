@@ -369,6 +369,80 @@ def run_decode(args, w, world, rank, local):
             "wall_s_timed_region": t_wall}), flush=True)
 
 
+def run_seqpar(args, w, world, rank, local):
+    """The sequence-parallel split of one workload over R = --seqpar ranks, with every
+    rank's work timed alone on this one GPU: phase 1 (rank 0's segment from S0; a
+    middle rank's (M, L) passes on two streams), then phase 2 (the fold and the
+    segment from the folded start state).  The critical path max(phase 1) +
+    max(phase 2) is what R GPUs would take, less the exchange of two state-sized
+    tensors per rank, which is not timed here."""
+    import chunkwise_gated_deltanet_gb300 as gdn
+    from chunkwise_gated_deltanet_gb300 import seqpar
+    if world != 1 or w.varlen:
+        raise SystemExit("--seqpar times R ranks on one GPU, for fixed-length workloads")
+    gdn.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workloads.make_inputs(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    Rk, C, T = args.seqpar, w.C, inp["T"]
+    ops = seqpar.cuda_ops()
+    bounds = seqpar.segment_bounds(T, Rk, C)
+    names = ("q", "k", "v", "log_alpha", "beta")
+    segs = [[seqpar.segment(d[n], b) for n in names] for b in bounds]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        res = fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), res
+
+    un, p1, p2 = [], [[] for _ in range(Rk)], [[] for _ in range(Rk)]
+    for it in range(max(3, args.warmup) + args.steps):
+        keep = it >= max(3, args.warmup)
+        t, _ = timed(lambda: ops.forward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                         d["S0"], C, w.linear))
+        if keep:
+            un.append(t)
+        first = []
+        for r in range(Rk):
+            t, res = timed(lambda r=r: seqpar.phase1(r, Rk, *segs[r], d["S0"], C, w.linear, ops))
+            first.append(res)
+            if keep:
+                p1[r].append(t)
+        Ms = torch.stack([m for m, _, _ in first])
+        Ls = torch.stack([l for _, l, _ in first])
+        for r in range(Rk):
+            t, _ = timed(lambda r=r: seqpar.phase2(r, *segs[r], C, w.linear, ops, Ms, Ls,
+                                                   first[r][2]))
+            if keep:
+                p2[r].append(t)
+    gdn.gdn_check_status()
+    med = statistics.median
+    ph1 = [med(x) for x in p1]
+    ph2 = [med(x) for x in p2]
+    crit = max(ph1) + max(ph2)
+    tokens = inp["B"] * T
+    print(json.dumps({
+        "metric": f"gated-DeltaNet sequence-parallel fwd tokens/s over {Rk} ranks "
+                  "(per-rank work timed on one GPU)",
+        "value": tokens / (crit * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": crit, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "ranks": Rk, "segments": bounds,
+                   "l2": "flushed before every timed phase",
+                   "timing": "each rank's phase timed alone with CUDA events (host launch "
+                             "overhead included); exchange not timed"},
+        "unsplit_ms": med(un), "speedup_vs_unsplit": med(un) / crit,
+        "phase1_ms": ph1, "phase2_ms": ph2}), flush=True)
+
+
 def n_tokens_of(inp):
     return inp["B"] * inp["T"]
 
@@ -384,8 +458,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--seqpar", type=int, default=0,
+                    help="time the sequence-parallel split over this many ranks on one GPU")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.seqpar > 0 and args.impl != "reference":
+        run_seqpar(args, workloads.WORKLOADS[args.workload], world, rank, local)
+        return
     if args.workload in workloads.DECODE_WORKLOADS:
         run_decode(args, workloads.DECODE_WORKLOADS[args.workload], world, rank, local)
         if world > 1:

@@ -154,6 +154,43 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* lo
   return GDN_OK;
 }
 
+int gdn_state_fold(const float* S_in, const float* M, const float* L, int count, float* S_out,
+                   int units, int dv, int dk, void* stream) {
+  if (units < 0 || count < 1)
+    return fail(GDN_EINVAL, "gdn_state_fold: need units >= 0 and count >= 1 (got %d, %d)", units,
+                count);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(GDN_EINVAL, "gdn_state_fold: dk and dv must be 16, 32, 64 or 128 (got %d, %d)",
+                dk, dv);
+  if (units == 0) return GDN_OK;
+  const bool needs_m = S_in || count > 1;
+  if ((needs_m && !M) || !L || !S_out)
+    return fail(GDN_EINVAL, "gdn_state_fold: L and S_out (and M when it is read) must be "
+                "non-NULL");
+  const void* ptrs[] = {S_in, M, L, S_out};
+  const char* names[] = {"S_in", "M", "L", "S_out"};
+  for (int i = 0; i < 4; ++i)
+    if (ptrs[i] && !aligned16(ptrs[i]))
+      return fail(GDN_EINVAL, "gdn_state_fold: %s is not 16-byte aligned", names[i]);
+  const size_t sbytes = (size_t)units * dv * dk * sizeof(float);
+  const size_t mbytes = (size_t)count * units * dk * dk * sizeof(float);
+  const size_t lbytes = (size_t)count * sbytes;
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return a && b && x < y + nb && y < x + na;
+  };
+  if (needs_m && overlap(S_out, sbytes, M, mbytes))
+    return fail(GDN_EINVAL, "gdn_state_fold: S_out overlaps M");
+  if ((S_out != S_in && overlap(S_out, sbytes, S_in, sbytes)) ||
+      (S_out != L && overlap(S_out, sbytes, L, lbytes)))
+    return fail(GDN_EINVAL, "gdn_state_fold: S_out overlaps S_in or L without being either");
+  const cudaError_t e = gdn::launch_state_fold(S_in, M, L, count, S_out, units, dv, dk,
+                                               (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(GDN_ELAUNCH, "gdn_state_fold: launch failed: %s", cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_check_status(void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaStreamSynchronize(s);

@@ -5,7 +5,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gdn {
+
+// Raise a kernel's dynamic shared-memory cap to `bytes`, once per device.  The
+// attribute belongs to the function in the current context; it is not set per
+// launch, because changing a kernel's attributes while launches of it are in
+// flight on other streams can serialise them.  `done` holds one bit per device.
+template <typename Kernel>
+cudaError_t ensure_smem_cap(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Everything a forward launch needs, already validated by the API layer.
 struct FwdArgs {
@@ -43,6 +61,9 @@ struct DecodeArgs {
   int N, H, dk, dv;
   int bf16;
 };
+// S <- S M_i + L_i for i < count per state (S_in NULL: zeros), already validated.
+cudaError_t launch_state_fold(const float* S_in, const float* M, const float* L, int count,
+                              float* S_out, int units, int dv, int dk, cudaStream_t stream);
 // CTAs the decode step launches for these sizes (dk one of 16, 32, 64, 128).
 long long decode_ctas(long long N, long long H, int dk, int dv);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

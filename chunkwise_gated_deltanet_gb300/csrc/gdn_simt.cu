@@ -261,18 +261,23 @@ cudaError_t launch_simt(const FwdArgs& a, cudaStream_t stream) {
   const long long blocks = (long long)a.N * a.H * (a.dv / dvt);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaError_t e;
+  // the cap is raised once to the device's opt-in maximum, which covers every shape
+  int cap = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&cap, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (smem > (size_t)cap) return cudaErrorInvalidConfiguration;
+  static std::atomic<unsigned long long> set_bf16{0}, set_f32{0};
   if (a.bf16) {
-    e = cudaFuncSetAttribute(gdn_simt_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_smem_cap(gdn_simt_kernel<__nv_bfloat16>, cap, set_bf16);
     if (e != cudaSuccess) return e;
     gdn_simt_kernel<__nv_bfloat16><<<(unsigned)blocks, kThreads, smem, stream>>>(
         (const __nv_bfloat16*)a.q, (const __nv_bfloat16*)a.k, (const __nv_bfloat16*)a.v,
         a.log_alpha, a.beta, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.cu_seqlens, a.H, a.T,
         a.dk, a.dv, dvt, a.C);
   } else {
-    e = cudaFuncSetAttribute(gdn_simt_kernel<float>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_smem_cap(gdn_simt_kernel<float>, cap, set_f32);
     if (e != cudaSuccess) return e;
     gdn_simt_kernel<float><<<(unsigned)blocks, kThreads, smem, stream>>>(
         (const float*)a.q, (const float*)a.k, (const float*)a.v, a.log_alpha, a.beta, a.S0,

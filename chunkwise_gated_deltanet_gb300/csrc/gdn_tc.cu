@@ -1240,8 +1240,8 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const long long blocks = 2LL * a.N * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES);
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = ensure_smem_cap(gdn_tc_kernel, SMEM_BYTES, smem_set);
   if (e != cudaSuccess) return e;
   gdn_tc_kernel<<<(unsigned)blocks, kThreads, SMEM_BYTES, stream>>>(
       mq, mk, mv, a.log_alpha, a.beta, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.cu_seqlens, a.H,

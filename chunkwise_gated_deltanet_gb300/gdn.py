@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
-EXPORTS = ("gdn_chunk_fwd", "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_select_path", "gdn_launches_per_call",
+EXPORTS = ("gdn_chunk_fwd", "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
            "gdn_check_status", "gdn_last_error", "gdn_version")
 
 
@@ -48,6 +48,8 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_linear_chunk_fwd.restype = I
     lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
     lib.gdn_decode_step.restype = I
+    lib.gdn_state_fold.argtypes = [P, P, P, I, P, I, I, I, P]
+    lib.gdn_state_fold.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
         getattr(lib, name).argtypes = [I, I, I, I]
         getattr(lib, name).restype = I
@@ -226,3 +228,27 @@ def decode_step(q, k, v, log_alpha, beta, S) -> torch.Tensor:
     out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     gdn_decode_step(q, k, v, log_alpha, beta, S, out)
     return out
+
+
+def gdn_state_fold(S_in, M, L, S_out, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name: S <- S M_i + L_i for
+    every step i, from S_in (None: zeros) into S_out.  M [count, ..., dk, dk] and
+    L [count, ..., dv, dk] stack the steps; S_in, S_out [..., dv, dk].  fp32
+    contiguous CUDA tensors; returns without synchronising."""
+    lib = load_library()
+    count = L.shape[0]
+    dv, dk = L.shape[-2], L.shape[-1]
+    units = L[0].numel() // (dv * dk)
+    for name, t in (("S_in", S_in), ("M", M), ("L", L), ("S_out", S_out)):
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32:
+            raise ValueError(f"gdn_state_fold: {name} must be a contiguous fp32 CUDA tensor")
+    if M is not None and (M.shape[0] != count or M.numel() != count * units * dk * dk):
+        raise ValueError("gdn_state_fold: M and L do not describe the same steps and states")
+    for name, t in (("S_in", S_in), ("S_out", S_out)):
+        if t is not None and t.numel() != units * dv * dk:
+            raise ValueError(f"gdn_state_fold: {name} does not hold one state per unit")
+    s = stream if stream is not None else torch.cuda.current_stream(L.device)
+    _check(lib.gdn_state_fold(_ptr(S_in), _ptr(M), _ptr(L), count, _ptr(S_out), units, dv, dk,
+                              ctypes.c_void_p(s.cuda_stream)))

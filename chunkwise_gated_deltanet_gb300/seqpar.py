@@ -1,0 +1,211 @@
+"""Sequence-parallel (context-parallel) forward: the ranks of a process group each
+own one contiguous, chunk-aligned segment of every sequence.
+
+Over a segment of tokens the recurrence is an affine map of the state (Nyysyyan,
+"Gated-DeltaNet": the WY identity for the product of the per-token factors
+A_t = I - beta_t k_t k_t^T and the unrolled state S_i = gamma_i S_0 A_1..A_i + G_i):
+
+    S_end = S_start M + L,
+    M = ordered product of alpha_t (I - beta_t k_t k_t^T)   (dk x dk)
+    L = the segment's final state from a zero start          (dv x dk)
+
+Both come out of the chunk forward itself: L with S0 = 0, M with v = 0 and S0 = I
+(the rows of I are carried through the same recurrence).  The forward then runs in
+two phases around one exchange:
+
+1. rank 0 runs its segment from the true S0 and publishes (-, S_end); every middle
+   rank computes (M, L) of its segment; the last rank has nothing to publish.
+2. all_gather of the (M, L) pairs (the exchange step: two state-sized tensors per
+   rank and (sequence, head)).
+3. rank r > 0 folds S_start = (((L_0) M_1 + L_1) M_2 + ...) over the ranks before it
+   in one gdn_state_fold call and runs its segment from S_start.
+
+Rank 0 runs one segment pass, a middle rank three (two of them independent), the
+last rank one after the exchange.  The linear mode works the same way (there
+M = (product of alpha_t) I).  Only fixed-length batches are split (every sequence
+has the same T); packed batches run whole on one rank.
+
+The compute is the CUDA library (``SegmentOps`` defaults to it); the functions take
+an ``ops`` object so that the host logic can be exercised on CPU ranks.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Callable, List, Optional, Tuple
+
+import torch
+
+
+def segment_bounds(T: int, world: int, C: int) -> List[Tuple[int, int]]:
+    """Contiguous token ranges [a, b) of the `world` segments of a length-T sequence.
+    Every boundary is a multiple of the chunk length C (so each segment's chunks are
+    the sequence's own chunks); trailing segments may be empty."""
+    if world <= 0 or C <= 0 or T < 0:
+        raise ValueError("segment_bounds: need world > 0, C > 0, T >= 0")
+    n_chunks = -(-T // C)
+    per = -(-n_chunks // world) if n_chunks else 0
+    return [(min(r * per * C, T), min((r + 1) * per * C, T)) for r in range(world)]
+
+
+def segment(t: Optional[torch.Tensor], bounds: Tuple[int, int]) -> Optional[torch.Tensor]:
+    """Tokens [a, b) of a [B, T, ...] tensor, contiguous."""
+    return None if t is None else t[:, bounds[0]:bounds[1]].contiguous()
+
+
+@dataclasses.dataclass
+class SegmentOps:
+    """The compute a rank runs.  forward(q, k, v, log_alpha, beta, S0, C, linear)
+    -> (out, S_final); fold(Ms, Ls) -> S after S = L_0, S <- S M_i + L_i for i >= 1
+    (Ms [count, B, H, dk, dk] and Ls [count, B, H, dv, dk] stacked; M_0 not read);
+    states are state_dtype tensors.  summary(q, k, v, log_alpha, beta, C, linear)
+    -> (M, L), if given, replaces the two forward calls of ``segment_summary``."""
+    forward: Callable
+    fold: Callable
+    state_dtype: torch.dtype = torch.float32
+    summary: Optional[Callable] = None
+
+
+_side_streams = {}
+
+
+def _summary_streams(device: torch.device):
+    """Two side streams per device, made once (streams taken afresh per call would
+    each start an empty allocator pool)."""
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    if key not in _side_streams:
+        _side_streams[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _side_streams[key]
+
+
+def cuda_ops() -> SegmentOps:
+    """The CUDA library's entry points (device tensors, current stream)."""
+    from . import gdn
+
+    def forward(q, k, v, log_alpha, beta, S0, C, linear):
+        if linear:
+            return gdn.linear_chunk_fwd(q, k, v, log_alpha, S0, None, C=C)
+        return gdn.chunk_fwd(q, k, v, log_alpha, beta, S0, None, C=C)
+
+    def fold(Ms, Ls):
+        out = torch.empty_like(Ls[0])
+        gdn.gdn_state_fold(None, Ms, Ls, out)
+        return out
+
+    def summary(q, k, v, log_alpha, beta, C, linear):
+        # the M pass (v = 0, S0 = I) and the L pass (S0 = 0) are independent: each
+        # runs on a side stream of its own and takes the SMs the other leaves free.
+        # Every buffer is allocated on the caller's stream, which waits for both
+        # side streams before it goes on, so no buffer is reused under them.
+        B, T, H, dk = k.shape
+        dv = v.shape[-1]
+        dev = k.device
+        main = torch.cuda.current_stream(dev)
+        I = torch.eye(dk, dtype=torch.float32, device=dev).expand(B, H, dk, dk).contiguous()
+        vz = torch.zeros((B, T, H, dk), dtype=v.dtype, device=dev)
+        out_m = torch.empty((B, T, H, dk), dtype=v.dtype, device=dev)
+        out_l = torch.empty((B, T, H, dv), dtype=v.dtype, device=dev)
+        M = torch.empty((B, H, dk, dk), dtype=torch.float32, device=dev)
+        L = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+        sm, sl = _summary_streams(dev)
+        sm.wait_stream(main)
+        sl.wait_stream(main)
+        for st, vv, s0, o, sf in ((sm, vz, I, out_m, M), (sl, v, None, out_l, L)):
+            if linear:
+                gdn.gdn_linear_chunk_fwd(q, k, vv, log_alpha, s0, o, sf, C, stream=st)
+            else:
+                gdn.gdn_chunk_fwd(q, k, vv, log_alpha, beta, s0, o, sf, C, stream=st)
+        main.wait_stream(sm)
+        main.wait_stream(sl)
+        return M, L
+
+    return SegmentOps(forward, fold, torch.float32, summary)
+
+
+def segment_summary(q, k, v, log_alpha, beta, C: int, linear: bool,
+                    ops: SegmentOps) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(M, L) of one segment: L = final state from zero, M = final state of the same
+    recurrence with v = 0 and S0 = I (dv taken as dk)."""
+    if ops.summary is not None:
+        return ops.summary(q, k, v, log_alpha, beta, C, linear)
+    B, T, H, dk = k.shape
+    I = torch.eye(dk, dtype=ops.state_dtype, device=k.device).expand(B, H, dk, dk).contiguous()
+    vz = torch.zeros((B, T, H, dk), dtype=v.dtype, device=v.device)
+    _, L = ops.forward(q, k, v, log_alpha, beta, None, C, linear)
+    _, M = ops.forward(q, k, vz, log_alpha, beta, I, C, linear)
+    return M, L
+
+
+def fold(Ms: torch.Tensor, Ls: torch.Tensor, r: int, ops: SegmentOps):
+    """S = (((L_0) M_1 + L_1) M_2 + ...) over segments 0 .. r-1 of the stacked
+    summaries: the state at the start of segment r, from rank 0's published final
+    state L_0 (its M_0 is not read)."""
+    return ops.fold(Ms[:r], Ls[:r])
+
+
+def phase1(rank: int, world: int, q, k, v, log_alpha, beta, S0, C: int, linear: bool,
+           ops: SegmentOps):
+    """What a rank computes before the exchange.  Returns (M, L, result) where
+    (M, L) is its contribution and result = (out, S_final) for rank 0, else None."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    if rank == 0:
+        out, Sf = ops.forward(q, k, v, log_alpha, beta, S0, C, linear)
+        M = torch.zeros((B, H, dk, dk), dtype=ops.state_dtype, device=dev)  # not read
+        return M, Sf, (out, Sf)
+    if rank == world - 1:  # nobody needs the last segment's map
+        zM = torch.zeros((B, H, dk, dk), dtype=ops.state_dtype, device=dev)
+        zL = torch.zeros((B, H, dv, dk), dtype=ops.state_dtype, device=dev)
+        return zM, zL, None
+    M, L = segment_summary(q, k, v, log_alpha, beta, C, linear, ops)
+    return M, L, None
+
+
+def phase2(rank: int, q, k, v, log_alpha, beta, C: int, linear: bool, ops: SegmentOps,
+           Ms: torch.Tensor, Ls: torch.Tensor, result):
+    """What a rank computes after the exchange: its segment from the folded start
+    state (rank 0 already has its result).  Ms, Ls stack every rank's summary."""
+    if rank == 0:
+        return result
+    S_start = fold(Ms, Ls, rank, ops)
+    return ops.forward(q, k, v, log_alpha, beta, S_start, C, linear)
+
+
+def seqpar_chunk_fwd(q, k, v, log_alpha, beta, S0, C: int, group=None, linear: bool = False,
+                     ops: Optional[SegmentOps] = None):
+    """This rank's part of a sequence-parallel forward.
+
+    q, k, v, log_alpha, beta: this rank's segment of every sequence ([B, T_r, ...],
+    the r-th range of ``segment_bounds``); S0: the sequences' initial state (read
+    on rank 0 only) or None.  Returns (out of this segment, state at the end of this
+    segment): on the last rank that is the sequences' final state.
+    """
+    import torch.distributed as dist
+    ops = ops or cuda_ops()
+    rank, world = dist.get_rank(group), dist.get_world_size(group)
+    M, L, res = phase1(rank, world, q, k, v, log_alpha, beta, S0, C, linear, ops)
+    Ms = [torch.empty_like(M) for _ in range(world)]
+    Ls = [torch.empty_like(L) for _ in range(world)]
+    dist.all_gather(Ms, M.contiguous(), group=group)
+    dist.all_gather(Ls, L.contiguous(), group=group)
+    return phase2(rank, q, k, v, log_alpha, beta, C, linear, ops, torch.stack(Ms),
+                  torch.stack(Ls), res)
+
+
+def emulate(q, k, v, log_alpha, beta, S0, C: int, world: int, linear: bool = False,
+            ops: Optional[SegmentOps] = None):
+    """Run every rank of a `world`-rank sequence-parallel forward in this process,
+    one after another (the exchange is a list).  Returns (out of the whole
+    sequences, final state); for checking the split on one device."""
+    ops = ops or cuda_ops()
+    T = k.shape[1]
+    bounds = segment_bounds(T, world, C)
+    segs = [[segment(t, b) for t in (q, k, v, log_alpha, beta)] for b in bounds]
+    first = [phase1(r, world, *segs[r], S0, C, linear, ops) for r in range(world)]
+    Ms = torch.stack([M for M, _, _ in first])
+    Ls = torch.stack([L for _, L, _ in first])
+    outs, Sf = [], None
+    for r in range(world):
+        out, Sf = phase2(r, *segs[r], C, linear, ops, Ms, Ls, first[r][2])
+        outs.append(out)
+    return torch.cat(outs, dim=1), Sf

@@ -129,6 +129,33 @@ int gdn_linear_chunk_fwd(const void* q, const void* k, const void* v,
 int gdn_decode_step(const void* q, const void* k, const void* v,
                     const float* log_alpha, const float* beta, float* S, void* out,
                     int N, int H, int dk, int dv, int qkv_dtype, void* stream);
+/*
+ * gdn_state_fold -- fold affine state maps: S <- S M_i + L_i for i = 0 .. count-1,
+ * starting from S_in, for each of `units` (sequence, head) states.
+ *
+ * Over a segment of tokens the recurrence maps each row s of a state as s <- s M + l
+ * (Nyysyyan, "Gated-DeltaNet": the WY identity for the product of the per-token
+ * factors and the unrolled state S_i = gamma_i S_0 A_1..A_i + G_i), where
+ *   M = the ordered product of alpha_t (I - beta_t k_t k_t^T) over the segment: the
+ *       S_final of gdn_chunk_fwd run on the segment with v = 0 (dv = dk) and S0 = I;
+ *   L = the S_final of gdn_chunk_fwd run on the segment from a zero state.
+ * (In the linear mode M = (product of alpha_t) I, obtained the same way.)  Folding
+ * the maps of segments 0 .. r-1 gives the state at the start of segment r: this is
+ * the step between the segments of a sequence-parallel forward.
+ *
+ * S_in   [units, dv, dk] fp32, or NULL = zeros (then M_0 is not read)
+ * M      [count, units, dk, dk] fp32 (may be NULL when count == 1 and S_in is NULL)
+ * L      [count, units, dv, dk] fp32
+ * S_out  [units, dv, dk] fp32; may be S_in itself or L itself (the same pointer),
+ *        must not otherwise overlap S_in, M or L
+ * count >= 1; dv, dk one of 16, 32, 64, 128; units >= 0 (0 launches nothing)
+ *
+ * Device pointers, 16-byte aligned, caller-owned; fp32 arithmetic; asynchronous on
+ * `stream`.  Errors: GDN_EINVAL before any launch, GDN_ELAUNCH.
+ */
+int gdn_state_fold(const float* S_in, const float* M, const float* L, int count,
+                   float* S_out, int units, int dv, int dk, void* stream);
+
 /* The path gdn_chunk_fwd takes for these sizes, GDN_PATH_NONE if unsupported. */
 int gdn_select_path(int dk, int dv, int C, int qkv_dtype);
 

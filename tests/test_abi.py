@@ -189,3 +189,34 @@ def test_chunk_fwd_still_requires_beta(lib):
     """Only the linear entry point may omit beta."""
     assert _call(lib, be=None) == binding.GDN_EINVAL
     assert "beta" in lib.gdn_last_error().decode()
+
+
+def _call_fold(lib, **over):
+    """Call gdn_state_fold with fake (never dereferenced) aligned pointers."""
+    a = dict(S=4096, M=1 << 20, L=2 << 20, count=2, out=3 << 20, units=4, dv=64, dk=64,
+             stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_state_fold(P(a["S"]), P(a["M"]), P(a["L"]), a["count"], P(a["out"]),
+                              a["units"], a["dv"], a["dk"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("over,word", [
+    (dict(units=-1), "units >= 0"),
+    (dict(count=0), "count >= 1"),
+    (dict(S=None, M=None), "non-NULL"),
+    (dict(out=(2 << 20) + 4096), "overlaps S_in or L"),
+    (dict(dk=48), "dk and dv"),
+    (dict(L=None), "non-NULL"),
+    (dict(M=None), "non-NULL"),
+    (dict(out=3 << 20 | 8), "S_out is not 16-byte aligned"),
+    (dict(out=4096 + 1024), "overlaps"),
+    (dict(out=(1 << 20) + 4096), "overlaps"),
+])
+def test_state_fold_invalid_arguments(lib, over, word):
+    assert _call_fold(lib, **over) == binding.GDN_EINVAL
+    assert word in lib.gdn_last_error().decode()
+
+
+def test_state_fold_empty_and_no_input_ok(lib):
+    assert _call_fold(lib, units=0) == binding.GDN_OK

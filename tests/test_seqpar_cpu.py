@@ -1,0 +1,161 @@
+"""Sequence-parallel forward on CPU ranks (gloo): the host logic of
+chunkwise_gated_deltanet_gb300.seqpar with the fp64 oracle as each rank's compute.
+
+The split rests on the state map of a segment being affine, S_end = S_start M + L
+(Nyysyyan, "Gated-DeltaNet": unrolled state and WY identity); the first tests pin
+that property on the oracle itself, the rest check that segment bounds, the
+exchange and the fold reproduce the unsplit oracle run.
+"""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+from chunkwise_gated_deltanet_gb300 import seqpar
+from oracle import recurrence as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _inputs(B=2, T=150, H=2, dk=16, dv=16, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, T, H, dk, generator=g)
+    k = torch.randn(B, T, H, dk, generator=g)
+    q, k = q / q.norm(dim=-1, keepdim=True), k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(B, T, H, dv, generator=g)
+    beta = torch.sigmoid(torch.randn(B, T, H, generator=g))
+    la = -torch.nn.functional.softplus(-(torch.randn(B, T, H, generator=g) + 2.0))
+    S0 = 0.1 * torch.randn(B, H, dv, dk, generator=g)
+    return q, k, v, la, beta, S0
+
+
+def _oracle_forward(q, k, v, la, beta, S0, C, linear):
+    """Each (sequence, head) through the fp64 per-token recurrence (C is irrelevant
+    to the definition).  Linear mode: erase 0, write 1."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    out = np.zeros((B, T, H, dv))
+    Sf = np.zeros((B, H, dv, dk))
+    for b in range(B):
+        for h in range(H):
+            s0 = None if S0 is None else S0[b, h].double().numpy()
+            kw = {}
+            if linear:
+                kw = dict(erase=np.zeros(T), write=np.ones(T))
+            o, S = R.gdn_sequence(q[b, :, h].double().numpy(), k[b, :, h].double().numpy(),
+                                  v[b, :, h].double().numpy(), la[b, :, h].double().numpy(),
+                                  beta[b, :, h].double().numpy(), s0, **kw)
+            out[b, :, h], Sf[b, h] = o, S
+    return torch.from_numpy(out), torch.from_numpy(Sf)
+
+
+def _oracle_fold(Ms, Ls):
+    S = Ls[0].clone()
+    for M, L in zip(Ms[1:], Ls[1:]):
+        S = S @ M + L
+    return S
+
+
+ORACLE_OPS = seqpar.SegmentOps(_oracle_forward, _oracle_fold, torch.float64)
+
+
+# ------------------------------------------------------ the affine property --
+
+@pytest.mark.parametrize("linear", [False, True])
+def test_segment_state_map_is_affine(linear):
+    """S_end(X) = X M + L for any start X, with M from v = 0 and S0 = I and L from
+    S0 = 0: the property the split rests on."""
+    q, k, v, la, beta, _ = _inputs(B=1, T=40, H=1, dk=8, dv=5, seed=1)
+    M, L = seqpar.segment_summary(q, k, v, la, beta, 16, linear, ORACLE_OPS)
+    X = torch.randn(1, 1, 5, 8, generator=torch.Generator().manual_seed(2), dtype=torch.float64)
+    _, S_end = _oracle_forward(q, k, v, la, beta, X, 16, linear)
+    assert torch.allclose(S_end, X @ M + L, rtol=1e-12, atol=1e-12)
+    if linear:  # the Mamba2 map is a scalar decay
+        gamma = torch.exp(la.double().sum(1))[0, 0]
+        assert torch.allclose(M[0, 0], gamma * torch.eye(8, dtype=torch.float64), atol=1e-14)
+
+
+def test_transition_product_by_brute_force():
+    """M equals the explicit ordered product of alpha_t (I - beta_t k_t k_t^T)."""
+    q, k, v, la, beta, _ = _inputs(B=1, T=9, H=1, dk=6, dv=3, seed=3)
+    M, _ = seqpar.segment_summary(q, k, v, la, beta, 16, False, ORACLE_OPS)
+    P = np.eye(6)
+    for t in range(9):
+        kt = k[0, t, 0].double().numpy()
+        P = P @ (np.exp(float(la[0, t, 0])) * (np.eye(6) - float(beta[0, t, 0]) * np.outer(kt, kt)))
+    assert np.abs(M[0, 0].numpy() - P).max() < 1e-13
+
+
+# ------------------------------------------------------------- segmentation --
+
+@pytest.mark.parametrize("T,world,C", [(0, 3, 16), (1, 4, 16), (150, 2, 16), (150, 3, 64),
+                                       (4096, 8, 64), (65, 5, 32), (64, 1, 64)])
+def test_segment_bounds(T, world, C):
+    b = seqpar.segment_bounds(T, world, C)
+    assert len(b) == world and b[0][0] == 0 and b[-1][1] == T
+    for (a0, a1), (b0, _) in zip(b, b[1:]):
+        assert a1 == b0
+    for a, e in b:
+        assert 0 <= a <= e <= T and (a % C == 0 or a == T)
+
+
+# --------------------------------------------------- one process, all ranks --
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5])
+@pytest.mark.parametrize("linear", [False, True])
+def test_emulated_split_matches_unsplit(world, linear):
+    q, k, v, la, beta, S0 = _inputs(seed=world)
+    out, Sf = seqpar.emulate(q, k, v, la, beta, S0, 16, world, linear, ORACLE_OPS)
+    ref_o, ref_S = _oracle_forward(q, k, v, la, beta, S0, 16, linear)
+    assert torch.allclose(out, ref_o, rtol=1e-10, atol=1e-12)
+    assert torch.allclose(Sf, ref_S, rtol=1e-10, atol=1e-12)
+
+
+# -------------------------------------------------------- gloo, real ranks --
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, linear, queue):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from chunkwise_gated_deltanet_gb300 import seqpar as sp
+    from tests import test_seqpar_cpu as me
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q, k, v, la, beta, S0 = me._inputs(seed=7)
+    bnd = sp.segment_bounds(q.shape[1], world, 16)[rank]
+    seg = [sp.segment(t, bnd) for t in (q, k, v, la, beta)]
+    out, Sf = sp.seqpar_chunk_fwd(*seg, S0 if rank == 0 else None, 16, linear=linear,
+                                  ops=me.ORACLE_OPS)
+    queue.put((rank, bnd, out.numpy(), Sf.numpy()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,linear", [(2, False), (3, False), (3, True)])
+def test_gloo_ranks_match_unsplit(world, linear):
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, linear, queue))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted((queue.get(timeout=300) for _ in range(world)), key=lambda x: x[0])
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    q, k, v, la, beta, S0 = _inputs(seed=7)
+    ref_o, ref_S = _oracle_forward(q, k, v, la, beta, S0, 16, linear)
+    got_o = np.concatenate([r[2] for r in res], axis=1)
+    assert np.allclose(got_o, ref_o.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(res[-1][3], ref_S.numpy(), rtol=1e-10, atol=1e-12)
+    assert [r[1] for r in res] == seqpar.segment_bounds(q.shape[1], world, 16)
