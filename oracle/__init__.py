@@ -17,6 +17,10 @@ Contents (fp64 throughout):
   recurrence: linear attention and Mamba2 matrix forms, the WY identity, the U/G
   identity, the unrolled state, the full-sequence matrix form and the chunk
   computation.
+* ``backward``    -- the reverse-mode derivative of the per-token recurrence
+  (gradients of q, k, v, log alpha, beta and S0 for given output and final-state
+  gradients); the pages derive none, so it is pinned to finite differences and to
+  autograd of a separately written forward.
 * ``native``      -- the same recurrence in plain C with OpenMP over
   (sequence, head), for sizes numpy is too slow for; built by ``oracle/build.py``.
 
