@@ -154,6 +154,62 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* lo
   return GDN_OK;
 }
 
+size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int N_seqs) {
+  if (B <= 0 || H <= 0 || T <= 0 || N_seqs <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
+  return gdn::bwd_workspace_bytes((long long)B * T, H, dk, dv, N_seqs);
+}
+
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
+                  const float* beta, const float* S0, const void* d_out, const float* dS_final,
+                  void* d_q, void* d_k, void* d_v, float* d_log_alpha, float* d_beta,
+                  float* d_S0, void* workspace, size_t workspace_bytes, int B, int H, int T,
+                  int dk, int dv, const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
+                  void* stream) {
+  const char* fn = "gdn_chunk_bwd";
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
+    return fail(GDN_EDTYPE, "%s: qkv_dtype %d is neither GDN_F32 nor GDN_BF16", fn, qkv_dtype);
+  if (T > 0 && (!q || !k || !v || !log_alpha || !beta || !d_out || !d_q || !d_k || !d_v ||
+                !d_log_alpha || !d_beta))
+    return fail(GDN_EINVAL, "%s: the inputs, d_out and the gradient outputs must be non-NULL",
+                fn);
+  if (B <= 0 || H <= 0 || T < 0)
+    return fail(GDN_EINVAL, "%s: need B > 0, H > 0, T >= 0 (got B=%d H=%d T=%d)", fn, B, H, T);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(GDN_EINVAL, "%s: dk and dv must be 16, 32, 64 or 128 (got %d, %d)", fn, dk, dv);
+  int N = B;
+  if (cu_seqlens) {
+    if (B != 1) return fail(GDN_EINVAL, "%s: packed sequences need B == 1 (got %d)", fn, B);
+    if (N_seqs <= 0)
+      return fail(GDN_EINVAL, "%s: N_seqs must be > 0 with cu_seqlens (got %d)", fn, N_seqs);
+    N = N_seqs;
+  }
+  const void* ptrs[] = {q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v,
+                        d_log_alpha, d_beta, d_S0, workspace, cu_seqlens};
+  const char* names[] = {"q", "k", "v", "log_alpha", "beta", "S0", "d_out", "dS_final", "d_q",
+                         "d_k", "d_v", "d_log_alpha", "d_beta", "d_S0", "workspace",
+                         "cu_seqlens"};
+  for (int i = 0; i < 16; ++i)
+    if (ptrs[i] && !aligned16(ptrs[i]))
+      return fail(GDN_EINVAL, "%s: %s is not 16-byte aligned", fn, names[i]);
+  const long long rows = (long long)B * T;
+  if (rows * H * (dk > dv ? dk : dv) > (1LL << 40))
+    return fail(GDN_EINVAL, "%s: problem too large", fn);
+  const size_t need = gdn::bwd_workspace_bytes(rows, H, dk, dv, N);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(GDN_EINVAL, "%s: workspace of %zu bytes needed (got %zu%s)", fn, need,
+                workspace_bytes, workspace ? "" : ", NULL");
+  gdn::BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
+  a.dout = d_out; a.dS_final = dS_final;
+  a.dq = d_q; a.dk_out = d_k; a.dv_out = d_v; a.dlog_alpha = d_log_alpha; a.dbeta = d_beta;
+  a.dS0 = d_S0; a.workspace = workspace; a.cu_seqlens = cu_seqlens;
+  a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.N = N; a.bf16 = qkv_dtype == GDN_BF16;
+  const cudaError_t e = gdn::launch_bwd(a, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(GDN_ELAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_state_fold(const float* S_in, const float* M, const float* L, int count, float* S_out,
                    int units, int dv, int dk, void* stream) {
   if (units < 0 || count < 1)

@@ -61,6 +61,29 @@ struct DecodeArgs {
   int N, H, dk, dv;
   int bf16;
 };
+// Backward (gradients of q, k, v, log alpha, beta, S0), already validated.
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* log_alpha;
+  const float* beta;
+  const float* S0;        // may be null (zeros)
+  const void* dout;
+  const float* dS_final;  // may be null (zeros)
+  void* dq;
+  void* dk_out;
+  void* dv_out;
+  float* dlog_alpha;
+  float* dbeta;
+  float* dS0;             // may be null (not written)
+  void* workspace;        // bwd_workspace_bytes(...) bytes, 256-byte aligned
+  const int32_t* cu_seqlens;
+  int B, H, T, dk, dv, N;
+  int bf16;
+};
+size_t bwd_workspace_bytes(long long rows, int H, int dk, int dv, int N);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // S <- S M_i + L_i for i < count per state (S_in NULL: zeros), already validated.
 cudaError_t launch_state_fold(const float* S_in, const float* M, const float* L, int count,
                               float* S_out, int units, int dv, int dk, cudaStream_t stream);

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
-EXPORTS = ("gdn_chunk_fwd", "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
+EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_bytes",
+           "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
            "gdn_check_status", "gdn_last_error", "gdn_version")
 
 
@@ -48,6 +49,12 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_linear_chunk_fwd.restype = I
     lib.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
     lib.gdn_decode_step.restype = I
+    Z = ctypes.c_size_t
+    lib.gdn_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
+                                  I, I, I, I, I, P, I, I, P]
+    lib.gdn_chunk_bwd.restype = I
+    lib.gdn_chunk_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.gdn_chunk_bwd_workspace_bytes.restype = Z
     lib.gdn_state_fold.argtypes = [P, P, P, I, P, I, I, I, P]
     lib.gdn_state_fold.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
@@ -252,3 +259,62 @@ def gdn_state_fold(S_in, M, L, S_out, stream: Optional[torch.cuda.Stream] = None
     s = stream if stream is not None else torch.cuda.current_stream(L.device)
     _check(lib.gdn_state_fold(_ptr(S_in), _ptr(M), _ptr(L), count, _ptr(S_out), units, dv, dk,
                               ctypes.c_void_p(s.cuda_stream)))
+
+
+def gdn_chunk_bwd_workspace_bytes(B: int, H: int, T: int, dk: int, dv: int, n_seqs: int) -> int:
+    """Device workspace the backward needs (n_seqs: B, or the packed sequence count)."""
+    return int(load_library().gdn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, n_seqs))
+
+
+def gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_log_alpha,
+                  d_beta, d_S0, workspace, cu_seqlens: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name.  Inputs as for
+    ``gdn_chunk_fwd``; d_out like out; dS_final like S_final (or None); the gradient
+    outputs d_q, d_k, d_v (input dtype), d_log_alpha, d_beta (fp32) and d_S0 (fp32 or
+    None); workspace a CUDA uint8 tensor of at least ``gdn_chunk_bwd_workspace_bytes``
+    bytes.  Launches on ``stream`` (default: current) without synchronising."""
+    lib = load_library()
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    tensors = [q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_log_alpha,
+               d_beta, d_S0, workspace, cu_seqlens]
+    for t in tensors:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("gdn_chunk_bwd: every tensor must be a contiguous CUDA tensor")
+    code = _dtype_code(v.dtype)
+    for t in (q, k, d_out, d_q, d_k, d_v):
+        if t.dtype != v.dtype:
+            raise TypeError("q, k, v, d_out, d_q, d_k and d_v must share one dtype")
+    for name, t in (("log_alpha", log_alpha), ("beta", beta), ("S0", S0), ("dS_final", dS_final),
+                    ("d_log_alpha", d_log_alpha), ("d_beta", d_beta), ("d_S0", d_S0)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    n_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    s = stream if stream is not None else torch.cuda.current_stream(v.device)
+    _check(lib.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                             _ptr(d_out), _ptr(dS_final), _ptr(d_q), _ptr(d_k), _ptr(d_v),
+                             _ptr(d_log_alpha), _ptr(d_beta), _ptr(d_S0), _ptr(workspace),
+                             ws_bytes, B, H, T, dk, dv, _ptr(cu_seqlens),
+                             0 if cu_seqlens is None else n_seqs, code,
+                             ctypes.c_void_p(s.cuda_stream)))
+
+
+def chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final=None, cu_seqlens=None,
+              want_dS0: bool = True):
+    """Allocate the gradients and the workspace and run the backward on the current
+    stream (device tensors).  Returns (d_q, d_k, d_v, d_log_alpha, d_beta, d_S0 or None)."""
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    dev = v.device
+    d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    d_la = torch.empty_like(log_alpha)
+    d_b = torch.empty_like(beta)
+    d_S0 = torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev) if want_dS0 else None
+    nbytes = gdn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, N)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_la, d_b, d_S0,
+                  ws, cu_seqlens)
+    return d_q, d_k, d_v, d_la, d_b, d_S0

@@ -22,6 +22,7 @@
 #ifndef GDN_H_
 #define GDN_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -82,6 +83,51 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v,
                   int B, int H, int T, int dk, int dv, int C,
                   const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
                   void* stream);
+
+/*
+ * gdn_chunk_bwd -- gradients of gdn_chunk_fwd's recurrence: for a loss whose gradients
+ * with respect to `out` and `S_final` are d_out and dS_final, compute the gradients of
+ * q, k, v, log_alpha, beta and S0.
+ *
+ * The pages derive no backward pass; this is the reverse-mode derivative of the
+ * recurrence (Nyysyyan, "Gated-DeltaNet", first equation block), walked backwards in
+ * time with the state gradient G = dL/dS_t:
+ *   G += dO_t q_t^T;  dq_t = S_t^T dO_t;  du = G k_t;  dv_t = beta_t du;
+ *   dbeta_t = du . (v_t - a_t S_{t-1} k_t);
+ *   dlog_alpha_t = a_t (<G, S_{t-1}> - beta_t du . S_{t-1} k_t);
+ *   dk_t = G^T u_t - beta_t a_t S_{t-1}^T du   (u_t = beta_t (v_t - a_t S_{t-1} k_t));
+ *   G <- a_t G (I - beta_t k_t k_t^T);   dS0 = G at the start
+ * (a_t = exp(log_alpha_t)).  States are recomputed from checkpoints every 8 tokens
+ * kept in `workspace`; fp32 arithmetic on CUDA cores; deterministic.
+ *
+ * q, k, v, log_alpha, beta, S0, B, H, T, dk, dv, cu_seqlens, N_seqs, qkv_dtype: as
+ *            passed to gdn_chunk_fwd (S0 NULL = zeros)
+ * d_out      [B, T, H, dv]   qkv_dtype, gradient of `out`
+ * dS_final   [N, H, dv, dk]  fp32 gradient of S_final, or NULL = zeros
+ * d_q, d_k   [B, T, H, dk]   qkv_dtype outputs (rounded to nearest even for bf16)
+ * d_v        [B, T, H, dv]   qkv_dtype output
+ * d_log_alpha, d_beta [B, T, H] fp32 outputs
+ * d_S0       [N, H, dv, dk]  fp32 output, or NULL = not written
+ * workspace  device scratch of at least gdn_chunk_bwd_workspace_bytes(...) bytes
+ *            (may be NULL when that is 0); its contents need no initialisation
+ *
+ * Device pointers, caller-owned, 16-byte aligned; outputs must not overlap inputs.
+ * Asynchronous; 2 kernel launches.  Errors: GDN_EINVAL / GDN_EDTYPE before any launch
+ * (including a missing or short workspace, with the size needed in the message),
+ * GDN_ELAUNCH.  With packed sequences, token rows outside every sequence get
+ * unspecified gradients.
+ */
+int gdn_chunk_bwd(const void* q, const void* k, const void* v,
+                  const float* log_alpha, const float* beta, const float* S0,
+                  const void* d_out, const float* dS_final,
+                  void* d_q, void* d_k, void* d_v, float* d_log_alpha, float* d_beta,
+                  float* d_S0, void* workspace, size_t workspace_bytes,
+                  int B, int H, int T, int dk, int dv,
+                  const int32_t* cu_seqlens, int N_seqs, int qkv_dtype, void* stream);
+
+/* Workspace bytes gdn_chunk_bwd needs (N_seqs = number of sequences: B, or the packed
+ * count); 0 for T == 0 or unsupported sizes. */
+size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int N_seqs);
 
 /*
  * gdn_linear_chunk_fwd -- the same chunkwise forward in the linear mode: no delta-rule

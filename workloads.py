@@ -190,3 +190,16 @@ def make_decode_inputs(w: DecodeWorkload, *, N: Optional[int] = None, H: Optiona
     return dict(q=q.contiguous(), k=k.contiguous(), v=v.contiguous(),
                 log_alpha=log_alpha.contiguous(), beta=beta.contiguous(), S=S.contiguous(),
                 N=N, H=H, dk=dk, dv=dv, dtype=w.dtype)
+
+
+def make_grad_inputs(inp: dict, seed: int = 1, ds_std: float = 0.1) -> dict:
+    """Seeded upstream gradients for a backward test or benchmark of the inputs
+    ``inp`` (from ``make_inputs``): d_out ~ N(0, 1) in the qkv dtype, shaped like out,
+    and dS_final ~ N(0, ds_std^2) fp32, shaped like S_final."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    B, T, H, dk = inp["k"].shape
+    dv = inp["v"].shape[-1]
+    d_out = torch.randn(B, T, H, dv, generator=g).to(inp["v"].dtype)
+    dS_final = ds_std * torch.randn(inp["N"], H, dv, dk, generator=g)
+    return {"d_out": d_out, "dS_final": dS_final}
