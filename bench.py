@@ -34,6 +34,7 @@ import workloads  # noqa: E402
 
 METRIC = "gated-DeltaNet chunkwise fwd tokens/s and % of roofline, 1×GB300"
 LINEAR_METRIC = "linear-attention (Mamba2 gate) chunkwise fwd tokens/s and % of roofline, 1×GB300"
+BWD_METRIC = "gated-DeltaNet backward tokens/s and % of roofline, 1×GB300"
 DECODE_METRIC = "gated-DeltaNet decode step tokens/s and % of roofline, 1×GB300"
 L2_FLUSH_BYTES = 512 << 20
 
@@ -443,6 +444,186 @@ def run_seqpar(args, w, world, rank, local):
         "phase1_ms": ph1, "phase2_ms": ph2}), flush=True)
 
 
+def bwd_algorithmic(inp: dict) -> dict:
+    """Algorithmic bytes and FLOPs of one backward.  Bytes: q, k, v, d_out read and
+    d_q, d_k, d_v written once in the qkv dtype; log_alpha, beta read and their
+    gradients written once (fp32); S0 / dS_final read and d_S0 written once when
+    present.  FLOPs per token and head: the forward state step p = S k and
+    S <- a S + u k^T (5 dk dv) and the reverse step G += dO q^T, dq, du = G k,
+    <G, S>, dk and G <- a G + dp k^T (17 dk dv)."""
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    th = inp["B"] * inp["T"] * inp["H"]
+    dk, dv = inp["dk"], inp["dv"]
+    units = inp["N"] * inp["H"]
+    by = th * (2 * (2 * dk + dv) * esz + 16)
+    state = units * dv * dk * 4
+    by += state * ((inp["S0"] is not None) + 2)  # S0, dS_final, d_S0
+    return dict(bytes=by, flops=th * 22 * dk * dv)
+
+
+def run_bwd(args, w, world, rank, local):
+    """One step = one gdn_chunk_bwd over the workload (its two launches)."""
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = workloads.make_inputs(w)
+        grads = workloads.make_grad_inputs(inp)
+        vals, cores, sample = [], None, None
+        for _ in range(args.steps):
+            v, cores, sample, _ = bwd_oracle_time(inp, grads, args.ref_budget)
+            vals.append(v)
+        value = statistics.median(vals)
+        print(json.dumps({
+            "metric": BWD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * inp["B"] * inp["T"] / value, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": {"workload": w.name, "pass": "backward"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}), flush=True)
+        return
+    import chunkwise_gated_deltanet_gb300 as gdn
+    gdn.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = workloads.make_inputs(w)
+    grads = workloads.make_grad_inputs(inp)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    gd = {k: v.to(dev) for k, v in grads.items()}
+    B, T, H, dk, dv, N = inp["B"], inp["T"], inp["H"], w.dk, w.dv, inp["N"]
+    outs = [torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+            torch.empty_like(d["log_alpha"]), torch.empty_like(d["beta"]),
+            torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev)]
+    nbytes = gdn.gdn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, N)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],
+                          gd["d_out"], gd["dS_final"], *outs, ws, d["cu_seqlens"], stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    gdn.gdn_check_status(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    gdn.gdn_check_status(stream)
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps,
+                        world, dev)
+    alg = bwd_algorithmic(dict(inp, dk=dk, dv=dv))
+    peaks = load_peaks()
+    sec = ms * 1e-3
+    tokens = B * T * world
+    # fp32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 FLOP x the maximum SM clock
+    alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+    achieved_tf = alg["flops"] / sec / 1e12
+
+    host_in = {k: (inp[k].pin_memory() if inp[k] is not None else None)
+               for k in ("q", "k", "v", "log_alpha", "beta", "S0", "cu_seqlens")}
+    host_g = {k: v.pin_memory() for k, v in grads.items()}
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in list(host_in.values()) + list(host_g.values())
+              if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for key, t in host_in.items():
+            if t is not None:
+                d[key].copy_(t, non_blocking=True)
+        for key, t in host_g.items():
+            gd[key].copy_(t, non_blocking=True)
+        step()
+        for ho, o in zip(host_out, outs):
+            ho.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _ = bwd_oracle_time(inp, grads, args.ref_budget)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps({
+            "metric": BWD_METRIC, "value": tokens / sec, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "pass": "backward", "B": B, "H": H, "T": T,
+                       "dk": dk, "dv": dv, "qkv_dtype": w.dtype, "workspace_bytes": nbytes,
+                       "l2": "flushed between timed steps (512 MiB write)",
+                       "parallelism": f"replicas{world}"},
+            "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": alu_peak,
+                         "unit": "TFLOP/s", "frac": achieved_tf / alu_peak, "traffic": None,
+                         "peak_source": "derived: fp32 FMA lanes x 2 x max SM clock",
+                         "algorithmic_flops": alg["flops"],
+                         "hbm_gbs": alg["bytes"] / sec / 1e9,
+                         "hbm_frac": alg["bytes"] / sec / 1e9 / peaks["hbm_gbs"]},
+            "clocks": clk.summary(),
+            "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "cpu_baseline": cpu,
+            "wall_s_timed_region": t_wall}), flush=True)
+
+
+def bwd_oracle_time(inp: dict, grads: dict, budget_s: float = 20.0):
+    """Time the fp64 backward oracle (numpy, one process) over a bounded sample of
+    (sequence, head) units.  Returns (tokens/s, cores, sample, seconds)."""
+    from oracle import backward as BW
+    from oracle import native
+    spans = native.spans(inp["B"], inp["T"], inp["cu_seqlens"])
+    H = inp["H"]
+    units = [(s, h) for s in range(len(spans)) for h in range(H)]
+    arr = {k: inp[k].double().numpy() for k in ("q", "k", "v", "log_alpha", "beta")}
+    dO = grads["d_out"].double().numpy()
+    dSf = grads["dS_final"].double().numpy()
+    S0 = None if inp["S0"] is None else inp["S0"].double().numpy()
+    done, toks = 0, 0
+    t0 = time.perf_counter()
+    for s, h in units:
+        r0, ln = spans[s]
+        b, t_ = (0, r0) if inp["cu_seqlens"] is not None else (s, 0)
+        sl = slice(t_, t_ + ln)
+        BW.gdn_sequence_bwd(arr["q"][b, sl, h], arr["k"][b, sl, h], arr["v"][b, sl, h],
+                            arr["log_alpha"][b, sl, h], arr["beta"][b, sl, h],
+                            None if S0 is None else S0[s, h], dO[b, sl, h], dSf[s, h])
+        done += 1
+        toks += ln
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = (f"{done} of {len(units)} (sequence, head) units ({toks} token-heads), fp64 "
+              "per-token reverse recurrence, numpy, one process")
+    return toks / H / dt, 1, sample, dt
+
+
 def n_tokens_of(inp):
     return inp["B"] * inp["T"]
 
@@ -458,12 +639,27 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--T", type=int, default=0,
+                    help="override the tokens per sequence of a fixed-length workload "
+                         "(for small profiling captures; the default is the workload's)")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward (gdn_chunk_bwd) of the workload instead")
     ap.add_argument("--seqpar", type=int, default=0,
                     help="time the sequence-parallel split over this many ranks on one GPU")
     args = ap.parse_args()
+    if args.T > 0:  # a smaller case of the same workload (profiling captures)
+        import dataclasses
+        base = workloads.WORKLOADS[args.workload]
+        workloads.WORKLOADS[args.workload] = dataclasses.replace(base, T=args.T)
     world, rank, local = dist_setup()
     if args.seqpar > 0 and args.impl != "reference":
         run_seqpar(args, workloads.WORKLOADS[args.workload], world, rank, local)
+        return
+    if args.bwd:
+        run_bwd(args, workloads.WORKLOADS[args.workload], world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
         return
     if args.workload in workloads.DECODE_WORKLOADS:
         run_decode(args, workloads.DECODE_WORKLOADS[args.workload], world, rank, local)
