@@ -318,3 +318,36 @@ def chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final=None, cu_seqlens=Non
     gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_la, d_b, d_S0,
                   ws, cu_seqlens)
     return d_q, d_k, d_v, d_la, d_b, d_S0
+
+
+class GatedDeltaNetFunction(torch.autograd.Function):
+    """(out, S_final) = the chunkwise forward of (q, k, v, log_alpha, beta, S0), with
+    gradients from gdn_chunk_bwd.  Both directions run in the library's kernels on the
+    current stream; device tensors only."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, log_alpha, beta, S0, C, cu_seqlens):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        log_alpha, beta = log_alpha.contiguous(), beta.contiguous()
+        S0 = None if S0 is None else S0.contiguous()
+        out, Sf = chunk_fwd(q, k, v, log_alpha, beta, S0, cu_seqlens, C=C)
+        ctx.save_for_backward(q, k, v, log_alpha, beta, S0, cu_seqlens)
+        return out, Sf
+
+    @staticmethod
+    def backward(ctx, d_out, dS_final):
+        q, k, v, log_alpha, beta, S0, cu_seqlens = ctx.saved_tensors
+        if d_out is None:
+            d_out = torch.zeros(v.shape, dtype=v.dtype, device=v.device)
+        d_out = d_out.to(v.dtype).contiguous()
+        dS_final = None if dS_final is None else dS_final.float().contiguous()
+        want_dS0 = S0 is not None and ctx.needs_input_grad[5]
+        d_q, d_k, d_v, d_la, d_b, d_S0 = chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final,
+                                                   cu_seqlens, want_dS0=want_dS0)
+        return d_q, d_k, d_v, d_la, d_b, d_S0, None, None
+
+
+def gated_delta_rule(q, k, v, log_alpha, beta, S0=None, C: int = 64, cu_seqlens=None):
+    """Differentiable chunkwise Gated DeltaNet: returns (out, S_final); backward by
+    gdn_chunk_bwd."""
+    return GatedDeltaNetFunction.apply(q, k, v, log_alpha, beta, S0, C, cu_seqlens)

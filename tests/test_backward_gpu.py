@@ -154,3 +154,21 @@ def test_backward_headline_size_sampled():
         for i, name in enumerate(NAMES):
             g = got[i][n, :, h] if i < 5 else got[5][n, h]
             _check(g, ref[i], i < 3, f"{name} unit ({n}, {h})")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_autograd_function_matches_oracle(dtype):
+    """loss.backward() through gated_delta_rule gives the oracle's gradients."""
+    w = dataclasses.replace(W["gdn_f32_b2h4t1024d64c64"], dtype=dtype)
+    inp = workloads.make_inputs(w, B=2, H=2, T=37, seed=21)
+    grads = workloads.make_grad_inputs(inp, seed=22)
+    d = to_device(inp)
+    leaves = [d[n].clone().requires_grad_(True) for n in ("q", "k", "v", "log_alpha", "beta", "S0")]
+    out, Sf = gdn.gated_delta_rule(*leaves, C=64)
+    loss = (out.float() * grads["d_out"].cuda().float()).sum() + (Sf * grads["dS_final"].cuda()).sum()
+    loss.backward()
+    torch.cuda.synchronize()
+    got = [x.grad.float().cpu().numpy().astype(np.float64) for x in leaves]
+    ref = _oracle(inp, grads)
+    # the autograd loss multiplies by the bf16 d_out widened to fp32: the same values
+    _compare(got, ref, dtype == "bf16")
