@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) gdn_bwd_rows_kernel(const BwdA
   if (nsb > 0) stage_load(nsb - 1, true);
   for (int sb = nsb - 1; sb >= 0; --sb) {
     float4 st0[kSub], st1[kSub];  // the rows' state before each token of the block
+    float pv0[kSub], pv1[kSub];   // the rows' predictions S_{t-1} k_t
     {
       const float* ck = A.ckpt + ((size_t)(slot0 + sb) * H + h) * dv * DK;
       st0[0] = ok0 ? *reinterpret_cast<const float4*>(ck + (size_t)r0 * DK + 4 * c4)
@@ -294,37 +295,40 @@ __global__ void __launch_bounds__(kBwdThreads, 2) gdn_bwd_rows_kernel(const BwdA
     const int b = sb & 1;
     const int nt = (int)min((long long)kSub, len - (long long)sb * kSub);
 #pragma unroll
-    for (int i = 0; i + 1 < kSub; ++i) {
-      if (i + 1 < nt) {
+    for (int i = 0; i < kSub; ++i) {
+      if (i < nt) {
         const Tok x = token(b, i, false);
-        const float p0 = row_sum<LPR>(dot4(st0[i], x.k)), p1 = row_sum<LPR>(dot4(st1[i], x.k));
-        const float u0 = x.b * (x.v0 - x.a * p0), u1 = x.b * (x.v1 - x.a * p1);
-        st0[i + 1] = axpy4(u0, x.k, scale4(x.a, st0[i]));
-        st1[i + 1] = axpy4(u1, x.k, scale4(x.a, st1[i]));
+        pv0[i] = row_sum<LPR>(dot4(st0[i], x.k));
+        pv1[i] = row_sum<LPR>(dot4(st1[i], x.k));
+        if (i + 1 < kSub) {
+          const float u0 = x.b * (x.v0 - x.a * pv0[i]), u1 = x.b * (x.v1 - x.a * pv1[i]);
+          st0[i + 1] = axpy4(u0, x.k, scale4(x.a, st0[i]));
+          st1[i + 1] = axpy4(u1, x.k, scale4(x.a, st1[i]));
+        }
       }
     }
 #pragma unroll
     for (int i = kSub - 1; i >= 0; --i) {
       if (i < nt) {
         const Tok x = token(b, i, true);
-        const float p0 = row_sum<LPR>(dot4(st0[i], x.k)), p1 = row_sum<LPR>(dot4(st1[i], x.k));
+        const float p0 = pv0[i], p1 = pv1[i];
         const float e0 = x.v0 - x.a * p0, e1 = x.v1 - x.a * p1;  // prediction errors
         const float u0 = x.b * e0, u1 = x.b * e1;
         g0 = axpy4(x.o0, x.q, g0);  // G += dO q^T
         g1 = axpy4(x.o1, x.q, g1);
         const float du0 = row_sum<LPR>(dot4(g0, x.k)), du1 = row_sum<LPR>(dot4(g1, x.k));
-        const float gs0 = row_sum<LPR>(dot4(g0, st0[i])), gs1 = row_sum<LPR>(dot4(g1, st1[i]));
         const long long t = (long long)sb * kSub + i;
         const size_t grow = (size_t)(row0 + t) * H + h;
         if (c4 == 0) {
           if (ok0) reinterpret_cast<TIn*>(A.dv)[grow * dv + r0] = from_f<TIn>(x.b * du0);
           if (ok1) reinterpret_cast<TIn*>(A.dv)[grow * dv + r1] = from_f<TIn>(x.b * du1);
         }
-        // per-row scalars counted once per row (lane c4 == 0 of the row group)
-        float db = 0.f, da = 0.f;
+        // <G, S_{t-1}> enters dalpha as this lane's partial sum (the warp and block
+        // sums below finish it); per-row scalars count once per row (lane c4 == 0)
+        float db = 0.f, da = dot4(g0, st0[i]) + dot4(g1, st1[i]);
         if (c4 == 0) {
           db = du0 * e0 + du1 * e1;
-          da = gs0 - x.b * du0 * p0 + gs1 - x.b * du1 * p1;
+          da -= x.b * (du0 * p0 + du1 * p1);
         }
         const float dp0 = -x.b * x.a * du0, dp1 = -x.b * x.a * du1;
         // dq = a S_{t-1}^T dO + k (u . dO);  dk = G^T u + S_{t-1}^T dp (this warp's rows)
