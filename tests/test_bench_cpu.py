@@ -1,0 +1,35 @@
+"""bench.py's reference arm (the fp64 oracle on the host cores) for every bench mode,
+on CPU: one JSON line with the contract's keys, the oracle named as the baseline."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+        "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "impl",
+        "cpu_baseline", "e2e"}
+
+
+@pytest.mark.parametrize("args", [
+    ["--workload", "deltanet_f32_b1h1t64d16c16"],
+    ["--workload", "linear_bf16_b4h16t4096d128c64", "--ref-budget", "1"],
+    ["--workload", "decode_f32_n64h8d64"],
+    ["--bwd", "--workload", "gdn_f32_b2h4t1024d64c64", "--ref-budget", "1"],
+], ids=["forward", "linear", "decode", "backward"])
+def test_reference_arm_prints_one_contract_line(args):
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+           "--steps", "1", "--warmup", "0"] + args
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT,
+                       env=dict(os.environ, OMP_NUM_THREADS="2"))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert KEYS <= set(d), KEYS - set(d)
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["config"]["workload"] == args[args.index("--workload") + 1]
