@@ -247,6 +247,13 @@ int gdn_state_fold(const float* S_in, const float* M, const float* L, int count,
   return GDN_OK;
 }
 
+int gdn_selftest_wait_timeout(void* stream) {
+  const cudaError_t e = gdn::launch_wait_selftest((cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(GDN_ELAUNCH, "gdn_selftest_wait_timeout: launch failed: %s", cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_check_status(void* stream) {
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaStreamSynchronize(s);

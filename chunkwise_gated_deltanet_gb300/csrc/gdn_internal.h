@@ -61,6 +61,9 @@ struct DecodeArgs {
   int N, H, dk, dv;
   int bf16;
 };
+// One CTA whose bounded wait can never be satisfied (failure-detection self-test).
+cudaError_t launch_wait_selftest(cudaStream_t stream);
+
 // Backward (gradients of q, k, v, log alpha, beta, S0), already validated.
 struct BwdArgs {
   const void* q;

@@ -1249,6 +1249,28 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Self-test of the failure-detection path: one thread waits, through the same
+// bounded wait the kernels use, on an mbarrier that nothing arrives on.  The wait
+// gives up after its limit (kWaitNs), records ST_WAIT, and the kernel publishes it in
+// the status word as the forward kernel does on a failed wait, then returns.
+__global__ void gdn_wait_selftest_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int flag;
+  volatile int* abort_flag = &flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    *abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !wait_bar(&bar, 0, abort_flag, false))
+    atomicOr(&g_tc_status, *abort_flag);
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t stream) {
+  gdn_wait_selftest_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
 int tc_read_and_clear_status(cudaStream_t stream, cudaError_t* err) {
   int v = 0;
   *err = cudaMemcpyFromSymbolAsync(&v, g_tc_status, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);

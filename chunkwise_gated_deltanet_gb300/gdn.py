@@ -21,7 +21,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_bytes",
            "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
-           "gdn_check_status", "gdn_last_error", "gdn_version")
+           "gdn_check_status", "gdn_selftest_wait_timeout", "gdn_last_error", "gdn_version")
 
 
 class GdnError(RuntimeError):
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH):
         getattr(lib, name).restype = I
     lib.gdn_check_status.argtypes = [P]
     lib.gdn_check_status.restype = I
+    lib.gdn_selftest_wait_timeout.argtypes = [P]
+    lib.gdn_selftest_wait_timeout.restype = I
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ctypes.c_char_p
     lib.gdn_version.restype = I
@@ -132,6 +134,13 @@ def _chunk_call(entry: str, q, k, v, log_alpha, beta, S0, out, S_final, C: int,
                                       _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
                                       _ptr(cu_seqlens), n_seqs, code, s)
     _check(st)
+
+
+def gdn_selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch the failure-detection self-test (a bounded wait that nothing satisfies);
+    the next gdn_check_status on the stream raises GdnError(GDN_ETIMEOUT)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(load_library().gdn_selftest_wait_timeout(ctypes.c_void_p(s.cuda_stream)))
 
 
 def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, S_final, C: int,

@@ -215,6 +215,15 @@ int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype);
  */
 int gdn_check_status(void* stream);
 
+/*
+ * Self-test of the failure detection: launch one CTA whose bounded wait (the same
+ * wait routine and limit, 2 s, that the kernels use) waits on an mbarrier that
+ * nothing arrives on.  The wait gives up, the kernel records it in the status word
+ * and returns, so the next gdn_check_status(stream) returns GDN_ETIMEOUT; the context
+ * stays usable.  Returns GDN_OK once launched, GDN_ELAUNCH otherwise.
+ */
+int gdn_selftest_wait_timeout(void* stream);
+
 /* Message for the last non-OK status returned on this host thread. */
 const char* gdn_last_error(void);
 
