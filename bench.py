@@ -741,25 +741,24 @@ def main():
     d2h = out_h.numel() * out_h.element_size() + Sf_h.numel() * Sf_h.element_size()
 
     def e2e_step():
-        for key, t in host_in.items():
-            if t is not None:
-                d[key].copy_(t, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        Sf_h.copy_(Sf, non_blocking=True)
+        # the public call on pinned host tensors: copies in, computes, copies back,
+        # pipelined over token ranges, and synchronises before it returns
+        if w.linear:
+            return gdn.linear_chunk_fwd(host_in["q"], host_in["k"], host_in["v"],
+                                        host_in["log_alpha"], host_in["S0"],
+                                        host_in["cu_seqlens"], C=C)
+        return gdn.chunk_fwd(host_in["q"], host_in["k"], host_in["v"], host_in["log_alpha"],
+                             host_in["beta"], host_in["S0"], host_in["cu_seqlens"], C=C)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    t_e2e = time.perf_counter()
     for _ in range(args.e2e_steps):
         e2e_step()
-    e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e_ms = max_over_ranks((time.perf_counter() - t_e2e) * 1e3 / args.e2e_steps, world, dev)
     gdn.gdn_check_status(stream)
 
     cpu = None
@@ -789,7 +788,8 @@ def main():
             "clocks": clk.summary(),
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms,
+                    "timing": "host clock around the synchronous public call chunk_fwd on pinned host tensors (copies pipelined over 4 token ranges)"},
             "gpu_launches": launches * args.steps,
             "cpu_baseline": cpu,
             "wall_s_timed_region": t_wall,

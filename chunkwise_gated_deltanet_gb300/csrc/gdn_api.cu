@@ -247,6 +247,52 @@ int gdn_state_fold(const float* S_in, const float* M, const float* L, int count,
   return GDN_OK;
 }
 
+size_t gdn_chunk_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
+                                          int qkv_dtype, int pieces, int linear) {
+  if (B <= 0 || H <= 0 || T < 0 || !head_ok(dk) || !head_ok(dv) || !chunk_ok(C) ||
+      pieces < 1 || pieces > 64 || (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16))
+    return 0;
+  return gdn::host_fwd_workspace_bytes(B, H, T, dk, dv, C, qkv_dtype == GDN_BF16 ? 2 : 4,
+                                       pieces, !linear);
+}
+
+int gdn_chunk_fwd_host(const void* q, const void* k, const void* v, const float* log_alpha,
+                       const float* beta, const float* S0, void* out, float* S_final, int B,
+                       int H, int T, int dk, int dv, int C, int qkv_dtype, int pieces,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "gdn_chunk_fwd_host";
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
+    return fail(GDN_EDTYPE, "%s: qkv_dtype %d is neither GDN_F32 nor GDN_BF16", fn, qkv_dtype);
+  if (B <= 0 || H <= 0 || T < 0)
+    return fail(GDN_EINVAL, "%s: need B > 0, H > 0, T >= 0 (got B=%d H=%d T=%d)", fn, B, H, T);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(GDN_EINVAL, "%s: dk and dv must be 16, 32, 64 or 128 (got %d, %d)", fn, dk, dv);
+  if (!chunk_ok(C)) return fail(GDN_EINVAL, "%s: C must be 16, 32 or 64 (got %d)", fn, C);
+  if (pieces < 1 || pieces > 64)
+    return fail(GDN_EINVAL, "%s: pieces must be in [1, 64] (got %d)", fn, pieces);
+  const bool linear = beta == nullptr;
+  if (T > 0 && (!q || !k || !v || !out || (!linear && !log_alpha)))
+    return fail(GDN_EINVAL, "%s: q, k, v, out (and log_alpha with beta) must be non-NULL", fn);
+  if ((long long)B * T * H * (dk > dv ? dk : dv) > (1LL << 40))
+    return fail(GDN_EINVAL, "%s: problem too large", fn);
+  const size_t need = gdn::host_fwd_workspace_bytes(B, H, T, dk, dv, C,
+                                                    qkv_dtype == GDN_BF16 ? 2 : 4, pieces,
+                                                    !linear);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
+    return fail(GDN_EINVAL, "%s: a 256-byte aligned device workspace of %zu bytes is needed "
+                "(got %zu)", fn, need, workspace_bytes);
+  gdn::HostFwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
+  a.out = out; a.S_final = S_final; a.workspace = workspace;
+  a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.C = C; a.pieces = pieces;
+  a.bf16 = qkv_dtype == GDN_BF16;
+  a.tc = gdn_select_path(dk, dv, C, qkv_dtype) == GDN_PATH_TCGEN05;
+  const cudaError_t e = gdn::launch_host_fwd(a, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(GDN_ECUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_selftest_wait_timeout(void* stream) {
   const cudaError_t e = gdn::launch_wait_selftest((cudaStream_t)stream);
   if (e != cudaSuccess)

@@ -1,0 +1,184 @@
+// The forward on host buffers: copies in, the chunkwise forward, copies out, pipelined
+// over consecutive token ranges.
+//
+// A fixed-length batch [B, T, H, d] is cut into `pieces` ranges of whole chunks.  Range
+// r of every tensor is one strided block (B rows of L*H*d elements, pitch T*H*d), so it
+// moves with a single cudaMemcpy2DAsync.  Inputs go in on one copy stream, ranges are
+// computed in order on the caller's stream (range r starts from range r-1's fp32 final
+// state, so the result is the unsplit forward's), outputs come back on a second copy
+// stream; events order the three.  The copy of range r+1 and the write-back of range
+// r-1 then overlap the computation of range r, and the two copy directions overlap
+// each other.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct HostLayout {
+  int pieces;
+  long long per;      // tokens per range (a multiple of C)
+  size_t q, k, v, la, be, out, s0, st, total;  // byte offsets of the device buffers
+};
+
+HostLayout host_layout(int B, int H, int T, int dk, int dv, int C, int esz, int pieces,
+                       bool has_beta) {
+  HostLayout L;
+  const long long n_chunks = (T + C - 1) / C;
+  long long want = n_chunks < pieces ? n_chunks : pieces;
+  if (want < 1) want = 1;
+  const long long per_chunks = n_chunks > 0 ? (n_chunks + want - 1) / want : 1;
+  L.per = per_chunks * C;
+  L.pieces = n_chunks > 0 ? (int)((n_chunks + per_chunks - 1) / per_chunks) : 1;
+  const size_t rows = (size_t)B * T * H;
+  L.q = 0;
+  L.k = L.q + al256(rows * dk * esz);
+  L.v = L.k + al256(rows * dk * esz);
+  L.la = L.v + al256(rows * dv * esz);
+  L.be = L.la + al256(rows * 4);
+  L.out = L.be + (has_beta ? al256(rows * 4) : 0);
+  L.s0 = L.out + al256(rows * dv * esz);
+  const size_t state = al256((size_t)B * H * dv * dk * 4);
+  L.st = L.s0 + state;
+  L.total = L.st + 2 * state;  // two final-state buffers, used in turn by the ranges
+  return L;
+}
+
+// Two copy streams per device, made once.
+struct CopyStreams {
+  cudaStream_t in = nullptr, out = nullptr;
+};
+CopyStreams g_streams[64];
+std::mutex g_streams_mu;
+
+cudaError_t copy_streams(CopyStreams* cs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_streams_mu);
+  CopyStreams& s = g_streams[dev & 63];
+  if (!s.in) {
+    e = cudaStreamCreateWithFlags(&s.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s.out, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  *cs = s;
+  return cudaSuccess;
+}
+
+// block of tokens [a, a + len) of a [B, T, H, width] host tensor <-> the contiguous
+// [B, len, H, width] device block
+cudaError_t copy_range(void* dst, const void* src, bool to_device, int B, int T, int H,
+                       long long a, long long len, int width, int esz, cudaStream_t s) {
+  const size_t row = (size_t)len * H * width * esz;       // one sequence's part
+  const size_t pitch = (size_t)T * H * width * esz;        // one sequence on the host
+  const size_t off = (size_t)a * H * width * esz;
+  if (row == 0) return cudaSuccess;
+  if (to_device)
+    return cudaMemcpy2DAsync(dst, row, static_cast<const char*>(src) + off, pitch, row, B,
+                             cudaMemcpyHostToDevice, s);
+  return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, src, row, row, B,
+                           cudaMemcpyDeviceToHost, s);
+}
+
+}  // namespace
+
+size_t host_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int esz, int pieces,
+                                bool has_beta) {
+  return host_layout(B, H, T, dk, dv, C, esz, pieces, has_beta).total;
+}
+
+cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream) {
+  const int esz = a.bf16 ? 2 : 4;
+  const bool linear = a.beta == nullptr;
+  const HostLayout L = host_layout(a.B, a.H, a.T, a.dk, a.dv, a.C, esz, a.pieces, !linear);
+  char* ws = static_cast<char*>(a.workspace);
+  CopyStreams cs;
+  cudaError_t e = copy_streams(&cs);
+  if (e != cudaSuccess) return e;
+  const size_t state_bytes = (size_t)a.B * a.H * a.dv * a.dk * 4;
+  const int n = L.pieces;
+  cudaEvent_t ev[3 * 64];
+  const int n_ev = 2 * n + 1;
+  if (n > 64) return cudaErrorInvalidValue;
+  for (int i = 0; i < n_ev; ++i) {
+    e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      return e;
+    }
+  }
+  cudaEvent_t* loaded = ev;          // range r is on the device
+  cudaEvent_t* computed = ev + n;    // range r's outputs are ready
+  cudaEvent_t start = ev[2 * n];     // the caller's earlier work is ordered first
+  e = cudaEventRecord(start, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, start, 0);
+  float* s0_dev = a.S0 ? reinterpret_cast<float*>(ws + L.s0) : nullptr;
+  if (e == cudaSuccess && a.S0)
+    e = cudaMemcpyAsync(s0_dev, a.S0, state_bytes, cudaMemcpyHostToDevice, cs.in);
+  // every input range goes in first, in order, so the copy engine never waits
+  for (int r = 0; r < n && e == cudaSuccess; ++r) {
+    const long long t0 = r * L.per, len = (t0 + L.per < a.T ? L.per : a.T - t0);
+    const size_t tok = (size_t)a.B * t0 * a.H;  // token-heads before this range
+    e = copy_range(ws + L.q + tok * a.dk * esz, a.q, true, a.B, a.T, a.H, t0, len, a.dk, esz, cs.in);
+    if (e == cudaSuccess)
+      e = copy_range(ws + L.k + tok * a.dk * esz, a.k, true, a.B, a.T, a.H, t0, len, a.dk, esz, cs.in);
+    if (e == cudaSuccess)
+      e = copy_range(ws + L.v + tok * a.dv * esz, a.v, true, a.B, a.T, a.H, t0, len, a.dv, esz, cs.in);
+    if (e == cudaSuccess && a.log_alpha)
+      e = copy_range(ws + L.la + tok * 4, a.log_alpha, true, a.B, a.T, a.H, t0, len, 1, 4, cs.in);
+    if (e == cudaSuccess && !linear)
+      e = copy_range(ws + L.be + tok * 4, a.beta, true, a.B, a.T, a.H, t0, len, 1, 4, cs.in);
+    if (e == cudaSuccess) e = cudaEventRecord(loaded[r], cs.in);
+  }
+  // ranges in order on the caller's stream, each from the previous final state
+  const float* prev = s0_dev;
+  for (int r = 0; r < n && e == cudaSuccess; ++r) {
+    const long long t0 = r * L.per, len = (t0 + L.per < a.T ? L.per : a.T - t0);
+    const size_t tok = (size_t)a.B * t0 * a.H;
+    float* st = reinterpret_cast<float*>(ws + L.st + (size_t)(r & 1) * al256(state_bytes));
+    e = cudaStreamWaitEvent(stream, loaded[r], 0);
+    if (e != cudaSuccess) break;
+    FwdArgs f{};
+    f.q = ws + L.q + tok * a.dk * esz;
+    f.k = ws + L.k + tok * a.dk * esz;
+    f.v = ws + L.v + tok * a.dv * esz;
+    f.log_alpha = a.log_alpha ? reinterpret_cast<const float*>(ws + L.la + tok * 4) : nullptr;
+    f.beta = linear ? nullptr : reinterpret_cast<const float*>(ws + L.be + tok * 4);
+    f.S0 = prev;
+    f.out = ws + L.out + tok * a.dv * esz;
+    f.S_final = st;
+    f.cu_seqlens = nullptr;
+    f.B = a.B; f.H = a.H; f.T = (int)len; f.dk = a.dk; f.dv = a.dv; f.C = a.C; f.N = a.B;
+    f.bf16 = a.bf16;
+    e = a.tc ? launch_tc(f, stream) : launch_simt(f, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(computed[r], stream);
+    prev = st;
+    if (e != cudaSuccess) break;
+    // range r's outputs come back while range r + 1 is computed
+    e = cudaStreamWaitEvent(cs.out, computed[r], 0);
+    if (e == cudaSuccess)
+      e = copy_range(a.out, ws + L.out + tok * a.dv * esz, false, a.B, a.T, a.H, t0, len, a.dv,
+                     esz, cs.out);
+  }
+  if (e == cudaSuccess && a.S_final)
+    e = cudaMemcpyAsync(a.S_final, prev ? prev : s0_dev, state_bytes, cudaMemcpyDeviceToHost,
+                        cs.out);
+  // the call returns with the outputs in host memory
+  cudaError_t e2 = cudaStreamSynchronize(cs.out);
+  if (e == cudaSuccess) e = e2;
+  e2 = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = e2;
+  e2 = cudaStreamSynchronize(cs.in);
+  if (e == cudaSuccess) e = e2;
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
+  return e;
+}
+
+}  // namespace gdn

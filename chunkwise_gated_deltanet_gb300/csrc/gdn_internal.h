@@ -61,6 +61,25 @@ struct DecodeArgs {
   int N, H, dk, dv;
   int bf16;
 };
+// The forward on host buffers, pipelined over token ranges (fixed-length batches).
+struct HostFwdArgs {
+  const void* q;          // host [B, T, H, dk]
+  const void* k;
+  const void* v;          // host [B, T, H, dv]
+  const float* log_alpha; // host [B, T, H] or null (alpha = 1, linear mode only)
+  const float* beta;      // host [B, T, H] or null (the linear mode)
+  const float* S0;        // host [B, H, dv, dk] or null
+  void* out;              // host [B, T, H, dv]
+  float* S_final;         // host [B, H, dv, dk] or null
+  void* workspace;        // device, host_fwd_workspace_bytes(...)
+  int B, H, T, dk, dv, C, pieces;
+  int bf16;
+  int tc;                 // 1: the tcgen05 kernel, 0: the SIMT kernel
+};
+size_t host_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int esz, int pieces,
+                                bool has_beta);
+cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream);
+
 // One CTA whose bounded wait can never be satisfied (failure-detection self-test).
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 

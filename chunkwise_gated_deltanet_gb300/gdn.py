@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional, Tuple
 
 import torch
@@ -19,7 +20,8 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
-EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_bytes",
+EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_host_workspace_bytes",
+           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_bytes",
            "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
            "gdn_check_status", "gdn_selftest_wait_timeout", "gdn_last_error", "gdn_version")
 
@@ -55,6 +57,10 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_chunk_bwd.restype = I
     lib.gdn_chunk_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.gdn_chunk_bwd_workspace_bytes.restype = Z
+    lib.gdn_chunk_fwd_host.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P]
+    lib.gdn_chunk_fwd_host.restype = I
+    lib.gdn_chunk_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
+    lib.gdn_chunk_fwd_host_workspace_bytes.restype = Z
     lib.gdn_state_fold.argtypes = [P, P, P, I, P, I, I, I, P]
     lib.gdn_state_fold.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
@@ -168,41 +174,96 @@ def gdn_linear_chunk_fwd(q, k, v, log_alpha, S0, out, S_final, C: int,
 
 
 def chunk_fwd(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, C: int = 64,
-              output_final_state: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+              output_final_state: bool = True,
+              pieces: Optional[int] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Allocate the outputs and run the forward.  Returns (out, S_final or None).
 
     Device tensors: runs on the current stream and returns device tensors.
-    Host tensors (pinned for asynchronous copies): copies the inputs to the
-    current CUDA device, runs there, copies the results back to pinned host
-    tensors, and synchronises before returning.
+    Host tensors (pinned, so that the copies are asynchronous): runs on the current
+    CUDA device and returns pinned host tensors, synchronising before it returns.  A
+    fixed-length batch goes through the native gdn_chunk_fwd_host: `pieces`
+    consecutive token ranges (default: up to 4 of whole chunks), each starting from
+    the previous one's final state, so that the copies of one range overlap the
+    computation of the next.
     """
-    host = not v.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
-        q, k, v, log_alpha, beta, S0, cu_seqlens = map(mv, (q, k, v, log_alpha, beta, S0, cu_seqlens))
+    if v.is_cuda:
+        B, T, H, dk = k.shape
+        dv = v.shape[-1]
+        N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+        out = torch.empty((B, T, H, dv), dtype=v.dtype, device=v.device)
+        Sf = (torch.empty((N, H, dv, dk), dtype=torch.float32, device=v.device)
+              if output_final_state else None)
+        gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, Sf, C, cu_seqlens)
+        return out, Sf
+    return _chunk_fwd_host(q, k, v, log_alpha, beta, S0, cu_seqlens, C, output_final_state,
+                           pieces, linear=False)
+
+
+_host_ws = threading.local()
+
+
+def _host_workspace(dev: torch.device, nbytes: int) -> torch.Tensor:
+    """A device scratch buffer for the host path, kept per thread and device."""
+    cache = getattr(_host_ws, "bufs", None)
+    if cache is None:
+        cache = _host_ws.bufs = {}
+    t = cache.get(dev.index)
+    if t is None or t.numel() < nbytes:
+        t = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+        cache[dev.index] = t
+    return t
+
+
+def _chunk_fwd_host(q, k, v, log_alpha, beta, S0, cu_seqlens, C, output_final_state, pieces,
+                    linear: bool):
+    dev = torch.device("cuda", torch.cuda.current_device())
     B, T, H, dk = k.shape
     dv = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    out = torch.empty((B, T, H, dv), dtype=v.dtype, device=v.device)
-    Sf = torch.empty((N, H, dv, dk), dtype=torch.float32, device=v.device) if output_final_state else None
-    gdn_chunk_fwd(q, k, v, log_alpha, beta, S0, out, Sf, C, cu_seqlens)
-    if host:
-        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        out_h.copy_(out, non_blocking=True)
-        Sf_h = None
-        if Sf is not None:
-            Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
-            Sf_h.copy_(Sf, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    out_h = torch.empty((B, T, H, dv), dtype=v.dtype, pin_memory=True)
+    Sf_h = (torch.empty((N, H, dv, dk), dtype=torch.float32, pin_memory=True)
+            if output_final_state else None)
+    stream = torch.cuda.current_stream(dev)
+    if cu_seqlens is None:
+        # the native pipelined path: copies overlap the computation, range by range
+        lib = load_library()
+        code = _dtype_code(v.dtype)
+        for t in (q, k, v, log_alpha, beta, S0):
+            if t is not None and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError("chunk_fwd: host inputs must be contiguous CPU tensors")
+        npieces = pieces or 4
+        nbytes = lib.gdn_chunk_fwd_host_workspace_bytes(B, H, T, dk, dv, C, code, npieces,
+                                                        int(linear))
+        ws = _host_workspace(dev, nbytes)
+        _check(lib.gdn_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                      None if linear else _ptr(beta), _ptr(S0), _ptr(out_h),
+                                      _ptr(Sf_h), B, H, T, dk, dv, C, code, npieces, _ptr(ws),
+                                      ws.numel(), ctypes.c_void_p(stream.cuda_stream)))
         return out_h, Sf_h
-    return out, Sf
+    # packed batches: copy in, run, copy back
+    mv = lambda t: None if t is None else t.to(dev, non_blocking=True)
+    qd, kd, vd, lad, bed, S0d, cud = map(mv, (q, k, v, log_alpha, beta, S0, cu_seqlens))
+    out = torch.empty((B, T, H, dv), dtype=v.dtype, device=dev)
+    Sf = torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev) if output_final_state else None
+    if linear:
+        gdn_linear_chunk_fwd(qd, kd, vd, lad, S0d, out, Sf, C, cud)
+    else:
+        gdn_chunk_fwd(qd, kd, vd, lad, bed, S0d, out, Sf, C, cud)
+    out_h.copy_(out, non_blocking=True)
+    if Sf_h is not None:
+        Sf_h.copy_(Sf, non_blocking=True)
+    stream.synchronize()
+    return out_h, Sf_h
 
 
 def linear_chunk_fwd(q, k, v, log_alpha=None, S0=None, cu_seqlens=None, C: int = 64,
-                     output_final_state: bool = True):
-    """Allocate the outputs and run the linear-mode forward on the current stream
-    (device tensors).  Returns (out, S_final or None)."""
+                     output_final_state: bool = True, pieces: Optional[int] = None):
+    """Allocate the outputs and run the linear-mode forward.  Returns (out, S_final or
+    None).  Device tensors run on the current stream; pinned host tensors take the
+    pipelined host path of ``chunk_fwd``."""
+    if not v.is_cuda:
+        return _chunk_fwd_host(q, k, v, log_alpha, None, S0, cu_seqlens, C, output_final_state,
+                               pieces, linear=True)
     B, T, H, dk = k.shape
     dv = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1

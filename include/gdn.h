@@ -130,6 +130,42 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v,
 size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int N_seqs);
 
 /*
+ * gdn_chunk_fwd_host -- gdn_chunk_fwd (or, with beta == NULL, gdn_linear_chunk_fwd) on
+ * HOST buffers, end to end: copies the inputs in, runs the forward, copies the outputs
+ * back, and returns once they are in host memory.  Fixed-length batches only.
+ *
+ * The batch is cut into at most `pieces` consecutive ranges of whole chunks (1..64).
+ * Inputs go in on one internal copy stream, range r is computed on `stream` from range
+ * r-1's fp32 final state (so the results equal the unsplit forward's bit for bit), and
+ * outputs come back on a second internal copy stream; the copies of one range overlap
+ * the computation of the next, and the two copy directions overlap each other.  Each
+ * range of a [B, T, H, d] tensor moves as one strided 2-D copy.
+ *
+ * q, k, v, log_alpha, beta, S0, out, S_final: as for gdn_chunk_fwd, but HOST pointers
+ *            (page-locked memory is needed for the copies to overlap); beta NULL selects
+ *            the linear mode, where log_alpha may also be NULL (alpha = 1)
+ * workspace  DEVICE scratch, 256-byte aligned, of at least
+ *            gdn_chunk_fwd_host_workspace_bytes(B, H, T, dk, dv, C, qkv_dtype, pieces,
+ *            beta == NULL) bytes (device copies of the inputs and outputs and three
+ *            states); contents need no initialisation
+ * stream     cudaStream_t the forward runs on (NULL = legacy default stream)
+ *
+ * Synchronous (returns with the outputs in host memory).  Errors: GDN_EINVAL /
+ * GDN_EDTYPE before any copy or launch; GDN_ECUDA for a failed copy, launch or
+ * synchronisation (message from the CUDA runtime).
+ */
+int gdn_chunk_fwd_host(const void* q, const void* k, const void* v,
+                       const float* log_alpha, const float* beta, const float* S0,
+                       void* out, float* S_final,
+                       int B, int H, int T, int dk, int dv, int C, int qkv_dtype, int pieces,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes gdn_chunk_fwd_host needs (linear: 1 when beta is NULL); 0 for
+ * invalid sizes. */
+size_t gdn_chunk_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, int C,
+                                          int qkv_dtype, int pieces, int linear);
+
+/*
  * gdn_linear_chunk_fwd -- the same chunkwise forward in the linear mode: no delta-rule
  * erase, a plain write (Nyysyyan, "Mamba2" section, its recurrence and chunk form;
  * "Linear attention" section when alpha = 1):

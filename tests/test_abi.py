@@ -220,3 +220,42 @@ def test_state_fold_invalid_arguments(lib, over, word):
 
 def test_state_fold_empty_and_no_input_ok(lib):
     assert _call_fold(lib, units=0) == binding.GDN_OK
+
+
+def _call_host(lib, **over):
+    """Call gdn_chunk_fwd_host with fake (never dereferenced) pointers."""
+    a = dict(q=4096, k=8192, v=12288, la=16384, be=20480, S0=None, out=24576, Sf=None,
+             B=2, H=4, T=128, dk=64, dv=64, C=64, dt=gdn.GDN_F32, pieces=4, ws=1 << 20,
+             ws_bytes=1 << 40, stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_chunk_fwd_host(P(a["q"]), P(a["k"]), P(a["v"]), P(a["la"]), P(a["be"]),
+                                  P(a["S0"]), P(a["out"]), P(a["Sf"]), a["B"], a["H"], a["T"],
+                                  a["dk"], a["dv"], a["C"], a["dt"], a["pieces"], P(a["ws"]),
+                                  a["ws_bytes"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("over,code,word", [
+    (dict(dt=9), binding.GDN_EDTYPE, "dtype"),
+    (dict(B=0), binding.GDN_EINVAL, "B > 0"),
+    (dict(pieces=0), binding.GDN_EINVAL, "pieces"),
+    (dict(pieces=65), binding.GDN_EINVAL, "pieces"),
+    (dict(q=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(la=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(ws_bytes=1024), binding.GDN_EINVAL, "workspace"),
+    (dict(ws=(1 << 20) + 16), binding.GDN_EINVAL, "workspace"),
+    (dict(ws=None), binding.GDN_EINVAL, "workspace"),
+    (dict(C=8), binding.GDN_EINVAL, "C must be"),
+])
+def test_host_forward_invalid_arguments(lib, over, code, word):
+    assert _call_host(lib, **over) == code
+    assert word in lib.gdn_last_error().decode()
+
+
+def test_host_forward_workspace_query(lib):
+    f = lib.gdn_chunk_fwd_host_workspace_bytes
+    full = f(4, 16, 4096, 128, 128, 64, gdn.GDN_BF16, 4, 0)
+    lin = f(4, 16, 4096, 128, 128, 64, gdn.GDN_BF16, 4, 1)
+    inputs = 4 * 4096 * 16 * (3 * 128 * 2 + 128 * 2 + 8)
+    assert full >= inputs and lin < full
+    assert f(4, 16, 4096, 128, 128, 64, gdn.GDN_BF16, 0, 0) == 0
