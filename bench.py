@@ -326,23 +326,20 @@ def run_decode(args, w, world, rank, local):
     d2h = out_h.numel() * out_h.element_size() + S_h.numel() * S_h.element_size()
 
     def e2e_step():
-        for key, t in host_in.items():
-            d[key].copy_(t, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-        S_h.copy_(d["S"], non_blocking=True)
+        # the public call on pinned host tensors: the token's inputs and the state go in,
+        # the output and the new state come back (copies pipelined over slices of
+        # sequences); it returns with both written
+        return gdn.decode_step(host_in["q"], host_in["k"], host_in["v"], host_in["log_alpha"],
+                               host_in["beta"], host_in["S"])
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    t_e2e = time.perf_counter()
     for _ in range(args.e2e_steps):
         e2e_step()
-    e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e_ms = max_over_ranks((time.perf_counter() - t_e2e) * 1e3 / args.e2e_steps, world, dev)
     gdn.gdn_check_status(stream)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -364,7 +361,9 @@ def run_decode(args, w, world, rank, local):
                          "algorithmic_bytes": alg["bytes"]},
             "clocks": clk.summary(),
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "timing": "host clock around the synchronous public call decode_step on "
+                              "pinned host tensors (copies pipelined over 4 slices)"},
             "gpu_launches": args.steps,
             "cpu_baseline": cpu,
             "wall_s_timed_region": t_wall}), flush=True)

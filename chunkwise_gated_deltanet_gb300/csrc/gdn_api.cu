@@ -293,6 +293,44 @@ int gdn_chunk_fwd_host(const void* q, const void* k, const void* v, const float*
   return GDN_OK;
 }
 
+size_t gdn_decode_step_host_workspace_bytes(int N, int H, int dk, int dv, int qkv_dtype) {
+  if (N < 0 || H < 0 || !head_ok(dk) || !head_ok(dv) ||
+      (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16))
+    return 0;
+  return gdn::host_decode_workspace_bytes(N, H, dk, dv, qkv_dtype == GDN_BF16 ? 2 : 4);
+}
+
+int gdn_decode_step_host(const void* q, const void* k, const void* v, const float* log_alpha,
+                         const float* beta, float* S, void* out, int N, int H, int dk, int dv,
+                         int qkv_dtype, int pieces, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  const char* fn = "gdn_decode_step_host";
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
+    return fail(GDN_EDTYPE, "%s: qkv_dtype %d is neither GDN_F32 nor GDN_BF16", fn, qkv_dtype);
+  if (N < 0 || H < 0)
+    return fail(GDN_EINVAL, "%s: need N >= 0, H >= 0 (got N=%d H=%d)", fn, N, H);
+  if (!head_ok(dk) || !head_ok(dv))
+    return fail(GDN_EINVAL, "%s: dk and dv must be 16, 32, 64 or 128 (got %d, %d)", fn, dk, dv);
+  if (pieces < 1 || pieces > 64)
+    return fail(GDN_EINVAL, "%s: pieces must be in [1, 64] (got %d)", fn, pieces);
+  if ((long long)N * H == 0) return GDN_OK;
+  if (!q || !k || !v || !log_alpha || !beta || !S || !out)
+    return fail(GDN_EINVAL, "%s: q, k, v, log_alpha, beta, S and out must be non-NULL", fn);
+  if (gdn::decode_ctas(N, H, dk, dv) > 0x7fffffffLL)
+    return fail(GDN_EINVAL, "%s: problem too large", fn);
+  const size_t need = gdn::host_decode_workspace_bytes(N, H, dk, dv, qkv_dtype == GDN_BF16 ? 2 : 4);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
+    return fail(GDN_EINVAL, "%s: a 256-byte aligned device workspace of %zu bytes is needed "
+                "(got %zu)", fn, need, workspace_bytes);
+  gdn::HostDecodeArgs a;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S = S; a.out = out;
+  a.workspace = workspace; a.N = N; a.H = H; a.dk = dk; a.dv = dv; a.pieces = pieces;
+  a.bf16 = qkv_dtype == GDN_BF16;
+  const cudaError_t e = gdn::launch_host_decode(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(GDN_ECUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_selftest_wait_timeout(void* stream) {
   const cudaError_t e = gdn::launch_wait_selftest((cudaStream_t)stream);
   if (e != cudaSuccess)

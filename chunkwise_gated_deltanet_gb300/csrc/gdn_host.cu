@@ -181,4 +181,129 @@ cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream) {
   return e;
 }
 
+
+// ---- the decode step on host buffers: slices of sequences, pipelined ----
+// Sequences are independent, so a slice of n sequences of every tensor (q, k, v,
+// gates, the state, the output) is one contiguous block: slice r goes in on one copy
+// stream, its step runs on the caller's stream, its state and output come back on the
+// other copy stream while later slices are still coming in.
+
+namespace {
+
+struct DecodeLayout {
+  size_t q, k, v, la, be, s, out, total;
+};
+
+DecodeLayout decode_layout(int N, int H, int dk, int dv, int esz) {
+  const size_t nh = (size_t)N * H;
+  DecodeLayout L;
+  L.q = 0;
+  L.k = L.q + al256(nh * dk * esz);
+  L.v = L.k + al256(nh * dk * esz);
+  L.la = L.v + al256(nh * dv * esz);
+  L.be = L.la + al256(nh * 4);
+  L.s = L.be + al256(nh * 4);
+  L.out = L.s + al256(nh * dv * dk * 4);
+  L.total = L.out + al256(nh * dv * esz);
+  return L;
+}
+
+}  // namespace
+
+size_t host_decode_workspace_bytes(int N, int H, int dk, int dv, int esz) {
+  return decode_layout(N, H, dk, dv, esz).total;
+}
+
+cudaError_t launch_host_decode(const HostDecodeArgs& a, cudaStream_t stream) {
+  const int esz = a.bf16 ? 2 : 4;
+  const DecodeLayout L = decode_layout(a.N, a.H, a.dk, a.dv, esz);
+  char* ws = static_cast<char*>(a.workspace);
+  if (a.pieces < 1 || a.pieces > 64) return cudaErrorInvalidValue;
+  const int per = (a.N + a.pieces - 1) / a.pieces;
+  const int n = per > 0 ? (a.N + per - 1) / per : 0;
+  if (n == 0) return cudaSuccess;
+  CopyStreams cs;
+  cudaError_t e = copy_streams(&cs);
+  if (e != cudaSuccess) return e;
+  cudaEvent_t ev[2 * 64 + 1];
+  const int n_ev = 2 * n + 1;
+  for (int i = 0; i < n_ev; ++i) {
+    e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      return e;
+    }
+  }
+  cudaEvent_t* loaded = ev;
+  cudaEvent_t* computed = ev + n;
+  e = cudaEventRecord(ev[2 * n], stream);  // the caller's earlier work comes first
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.in, ev[2 * n], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, ev[2 * n], 0);
+  const size_t H = (size_t)a.H;
+  // byte offset of sequence n0 in a [N, H, width] array of `bytes`-sized elements
+  auto at = [&](int n0, size_t width, size_t bytes) { return (size_t)n0 * H * width * bytes; };
+  const char* src_q = static_cast<const char*>(a.q);
+  const char* src_k = static_cast<const char*>(a.k);
+  const char* src_v = static_cast<const char*>(a.v);
+  const char* src_la = reinterpret_cast<const char*>(a.log_alpha);
+  const char* src_be = reinterpret_cast<const char*>(a.beta);
+  char* host_s = reinterpret_cast<char*>(a.S);
+  char* host_o = static_cast<char*>(a.out);
+  const size_t sw = (size_t)a.dv * a.dk;  // state elements per (sequence, head)
+  for (int r = 0; r < n && e == cudaSuccess; ++r) {
+    const int n0 = r * per, nn = (n0 + per < a.N ? per : a.N - n0);
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+    e = cudaMemcpyAsync(ws + L.q + at(n0, a.dk, esz), src_q + at(n0, a.dk, esz),
+                        at(nn, a.dk, esz), h2d, cs.in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ws + L.k + at(n0, a.dk, esz), src_k + at(n0, a.dk, esz),
+                          at(nn, a.dk, esz), h2d, cs.in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ws + L.v + at(n0, a.dv, esz), src_v + at(n0, a.dv, esz),
+                          at(nn, a.dv, esz), h2d, cs.in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ws + L.la + at(n0, 1, 4), src_la + at(n0, 1, 4), at(nn, 1, 4), h2d,
+                          cs.in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ws + L.be + at(n0, 1, 4), src_be + at(n0, 1, 4), at(nn, 1, 4), h2d,
+                          cs.in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ws + L.s + at(n0, sw, 4), host_s + at(n0, sw, 4), at(nn, sw, 4), h2d,
+                          cs.in);
+    if (e == cudaSuccess) e = cudaEventRecord(loaded[r], cs.in);
+  }
+  for (int r = 0; r < n && e == cudaSuccess; ++r) {
+    const int n0 = r * per, nn = (n0 + per < a.N ? per : a.N - n0);
+    e = cudaStreamWaitEvent(stream, loaded[r], 0);
+    if (e != cudaSuccess) break;
+    DecodeArgs d;
+    d.q = ws + L.q + at(n0, a.dk, esz);
+    d.k = ws + L.k + at(n0, a.dk, esz);
+    d.v = ws + L.v + at(n0, a.dv, esz);
+    d.log_alpha = reinterpret_cast<const float*>(ws + L.la + at(n0, 1, 4));
+    d.beta = reinterpret_cast<const float*>(ws + L.be + at(n0, 1, 4));
+    d.S = reinterpret_cast<float*>(ws + L.s + at(n0, sw, 4));
+    d.out = ws + L.out + at(n0, a.dv, esz);
+    d.N = nn; d.H = a.H; d.dk = a.dk; d.dv = a.dv; d.bf16 = a.bf16;
+    e = launch_decode(d, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(computed[r], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs.out, computed[r], 0);
+    const cudaMemcpyKind d2h = cudaMemcpyDeviceToHost;
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(host_o + at(n0, a.dv, esz), ws + L.out + at(n0, a.dv, esz),
+                          at(nn, a.dv, esz), d2h, cs.out);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(host_s + at(n0, sw, 4), ws + L.s + at(n0, sw, 4), at(nn, sw, 4), d2h,
+                          cs.out);
+  }
+  cudaError_t e2 = cudaStreamSynchronize(cs.out);
+  if (e == cudaSuccess) e = e2;
+  e2 = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = e2;
+  e2 = cudaStreamSynchronize(cs.in);
+  if (e == cudaSuccess) e = e2;
+  for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
+  return e;
+}
+
 }  // namespace gdn

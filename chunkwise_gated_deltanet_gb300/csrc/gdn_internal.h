@@ -80,6 +80,22 @@ size_t host_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int 
                                 bool has_beta);
 cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream);
 
+// The decode step on host buffers, pipelined over slices of sequences.
+struct HostDecodeArgs {
+  const void* q;          // host [N, H, dk]
+  const void* k;
+  const void* v;          // host [N, H, dv]
+  const float* log_alpha; // host [N, H]
+  const float* beta;      // host [N, H]
+  float* S;               // host [N, H, dv, dk], updated in place
+  void* out;              // host [N, H, dv]
+  void* workspace;        // device, host_decode_workspace_bytes(...)
+  int N, H, dk, dv, pieces;
+  int bf16;
+};
+size_t host_decode_workspace_bytes(int N, int H, int dk, int dv, int esz);
+cudaError_t launch_host_decode(const HostDecodeArgs& a, cudaStream_t stream);
+
 // One CTA whose bounded wait can never be satisfied (failure-detection self-test).
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 

@@ -21,6 +21,7 @@ GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_host_workspace_bytes",
+           "gdn_decode_step_host", "gdn_decode_step_host_workspace_bytes",
            "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_bytes",
            "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
            "gdn_check_status", "gdn_selftest_wait_timeout", "gdn_last_error", "gdn_version")
@@ -61,6 +62,10 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_chunk_fwd_host.restype = I
     lib.gdn_chunk_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
     lib.gdn_chunk_fwd_host_workspace_bytes.restype = Z
+    lib.gdn_decode_step_host.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+    lib.gdn_decode_step_host.restype = I
+    lib.gdn_decode_step_host_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.gdn_decode_step_host_workspace_bytes.restype = Z
     lib.gdn_state_fold.argtypes = [P, P, P, I, P, I, I, I, P]
     lib.gdn_state_fold.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
@@ -299,9 +304,27 @@ def gdn_decode_step(q, k, v, log_alpha, beta, S, out,
                                _ptr(out), N, H, dk, dv, code, ctypes.c_void_p(s.cuda_stream)))
 
 
-def decode_step(q, k, v, log_alpha, beta, S) -> torch.Tensor:
-    """One decode token for every (sequence, head): updates S in place on the current
-    stream and returns the output tensor [N, H, dv] (same dtype as v)."""
+def decode_step(q, k, v, log_alpha, beta, S, pieces: int = 4) -> torch.Tensor:
+    """One decode token for every (sequence, head): updates S in place and returns the
+    output [N, H, dv] (same dtype as v).  Device tensors run on the current stream;
+    pinned host tensors go through gdn_decode_step_host (copies pipelined over
+    `pieces` slices of sequences) and the call returns with S and the output written."""
+    if not v.is_cuda:
+        lib = load_library()
+        N, H, dk = k.shape
+        dv = v.shape[-1]
+        code = _dtype_code(v.dtype)
+        for t in (q, k, v, log_alpha, beta, S):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("decode_step: host inputs must be contiguous CPU tensors")
+        out = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        ws = _host_workspace(dev, lib.gdn_decode_step_host_workspace_bytes(N, H, dk, dv, code))
+        s = torch.cuda.current_stream(dev)
+        _check(lib.gdn_decode_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                        _ptr(S), _ptr(out), N, H, dk, dv, code, pieces, _ptr(ws),
+                                        ws.numel(), ctypes.c_void_p(s.cuda_stream)))
+        return out
     out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     gdn_decode_step(q, k, v, log_alpha, beta, S, out)
     return out

@@ -238,6 +238,29 @@ int gdn_decode_step(const void* q, const void* k, const void* v,
 int gdn_state_fold(const float* S_in, const float* M, const float* L, int count,
                    float* S_out, int units, int dv, int dk, void* stream);
 
+/*
+ * gdn_decode_step_host -- gdn_decode_step on HOST buffers, end to end and synchronous:
+ * the batch is cut into at most `pieces` (1..64) slices of whole sequences; a slice's
+ * inputs and state go in on one internal copy stream, its step runs on `stream`, and
+ * its output and new state come back on a second copy stream while later slices still
+ * come in (page-locked host memory is needed for the copies to overlap).
+ *
+ * q, k, v, log_alpha, beta, S, out: as for gdn_decode_step, but HOST pointers; S is
+ *            updated in place
+ * workspace  DEVICE scratch, 256-byte aligned, of at least
+ *            gdn_decode_step_host_workspace_bytes(N, H, dk, dv, qkv_dtype) bytes
+ *
+ * Returns with out and S written.  Errors: GDN_EINVAL / GDN_EDTYPE before any copy or
+ * launch; GDN_ECUDA for a failed copy, launch or synchronisation.
+ */
+int gdn_decode_step_host(const void* q, const void* k, const void* v,
+                         const float* log_alpha, const float* beta, float* S, void* out,
+                         int N, int H, int dk, int dv, int qkv_dtype, int pieces,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes gdn_decode_step_host needs; 0 for invalid sizes. */
+size_t gdn_decode_step_host_workspace_bytes(int N, int H, int dk, int dv, int qkv_dtype);
+
 /* The path gdn_chunk_fwd takes for these sizes, GDN_PATH_NONE if unsupported. */
 int gdn_select_path(int dk, int dv, int C, int qkv_dtype);
 

@@ -133,3 +133,21 @@ def test_decode_deterministic():
     a = _gpu_step(inp)
     b = _gpu_step(inp)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("pieces", [1, 3, 4, 64])
+def test_decode_host_path_equals_device_path(pieces):
+    """decode_step on pinned host tensors (gdn_decode_step_host, copies pipelined over
+    slices of sequences) gives bit for bit the device path's output and new state."""
+    inp = workloads.make_decode_inputs(W_BF16, N=37, H=3, seed=13)
+    d = to_device(inp)
+    S_dev = d["S"].clone()
+    out_dev = gdn.decode_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S_dev)
+    h = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    S_host = h["S"].clone().pin_memory()
+    out_host = gdn.decode_step(h["q"], h["k"], h["v"], h["log_alpha"], h["beta"], S_host,
+                               pieces=pieces)
+    torch.cuda.synchronize()
+    assert not out_host.is_cuda
+    assert torch.equal(out_dev.cpu(), out_host)
+    assert torch.equal(S_dev.cpu(), S_host)
