@@ -86,6 +86,13 @@ def test_linear_bf16_tcgen05(alpha_one):
     _full(inp, 64, alpha_one)
 
 
+def test_linear_bf16_strong_decay():
+    """Every chunk in the tcgen05 kernel's strong-decay form, in the linear mode."""
+    w = workloads.Workload("decay_bf16", "bf16", B=1, H=2, T=200, dk=128, dv=128, C=64,
+                           alpha_mu=-2.0, s0_std=0.1)
+    _full(workloads.make_inputs(w), 64)
+
+
 def test_linear_bf16_varlen():
     w = W["gdn_bf16_varlen256_h16d128c64"]
     inp = workloads.make_inputs(w, n_seqs=6, H=2, seed=3)

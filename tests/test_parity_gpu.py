@@ -105,6 +105,23 @@ def test_strong_decay_and_plain_deltanet():
     _full_check(workloads.make_inputs(w), 64)
 
 
+@pytest.mark.parametrize("alpha_mu", [-2.0, -0.3], ids=["all_strong", "mixed_forms"])
+def test_tcgen05_strong_decay_forms(alpha_mu):
+    """The tcgen05 kernel keeps a chunk in the factored frame only while its total decay
+    is above 2^-80; alpha ~ sigmoid(N(-2, 1)) puts every chunk in the strong-decay form,
+    sigmoid(N(-0.3, 1)) puts chunks on both sides of the threshold."""
+    w = workloads.Workload("decay_bf16", "bf16", B=1, H=3, T=333, dk=128, dv=128, C=64,
+                           alpha_mu=alpha_mu, s0_std=0.1)
+    assert gdn.gdn_select_path(128, 128, 64, torch.bfloat16) == gdn.GDN_PATH_TCGEN05
+    inp = workloads.make_inputs(w)
+    per_chunk_bits = -inp["log_alpha"][0, :320].reshape(5, 64, 3).sum(1) * 1.4426950408889634
+    if alpha_mu < -1:
+        assert (per_chunk_bits > 80).all()
+    else:
+        assert (per_chunk_bits > 80).any() and (per_chunk_bits < 80).any()
+    _full_check(inp, 64)
+
+
 def test_without_S0_and_without_S_final():
     inp = workloads.make_inputs(W["gdn_f32_b2h4t1024d64c64"], B=1, H=2, T=100)
     inp["S0"] = None
