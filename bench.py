@@ -222,6 +222,22 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def measured_traffic(workload: str):
+    """DRAM bytes per launch of the workload's dominant kernel from its recorded ncu
+    capture (profiles/dram_traffic.json), or None when there is none or the kernel's
+    source has changed since the capture (its SHA-256 differs)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        rec = json.load(open(path))["workloads"][workload]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha256(src).hexdigest() != rec["source_sha256"]:
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def decode_algorithmic(inp: dict) -> dict:
     """Algorithmic bytes and FLOPs of one decode step over the batch: the state read
     and written once (fp32 dv x dk per (sequence, head)), q, k, v read and out
@@ -357,7 +373,7 @@ def run_decode(args, w, world, rank, local):
                        "parallelism": f"replicas{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": None, "peak_source": peaks["source"],
+                         "traffic": measured_traffic(w.name), "peak_source": peaks["source"],
                          "algorithmic_bytes": alg["bytes"]},
             "clocks": clk.summary(),
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
@@ -780,7 +796,8 @@ def main():
                        "parallelism": f"replicas{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": None, "peak_source": peaks["source"],
+                         "traffic": measured_traffic(w.name) if args.T == 0 else None,
+                         "peak_source": peaks["source"],
                          "algorithmic_bytes": alg["bytes"],
                          "tensor_tflops": achieved_tf,
                          "tensor_frac": achieved_tf / peaks["bf16_tflops"]},

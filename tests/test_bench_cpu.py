@@ -33,3 +33,24 @@ def test_reference_arm_prints_one_contract_line(args):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"] == args[args.index("--workload") + 1]
+
+
+def test_recorded_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypatch):
+    """bench.py reports an ncu capture's DRAM bytes only while the captured kernel's
+    source file still has the recorded hash."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
+    name, entry = next(iter(rec["workloads"].items()))
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / entry["source"]
+    src.parent.mkdir(parents=True)
+    src.write_bytes(open(os.path.join(ROOT, entry["source"]), "rb").read())
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    import hashlib
+    if hashlib.sha256(src.read_bytes()).hexdigest() == entry["source_sha256"]:
+        assert bench.measured_traffic(name) == entry["dram_read_bytes"] + entry["dram_write_bytes"]
+    src.write_bytes(src.read_bytes() + b"\n// changed\n")
+    assert bench.measured_traffic(name) is None
+    assert bench.measured_traffic("no_such_workload") is None
