@@ -44,7 +44,7 @@ int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype) {
   a.dk = dk; a.dv = dv; a.C = C; a.bf16 = qkv_dtype == GDN_BF16;
   switch (gdn_select_path(dk, dv, C, qkv_dtype)) {
     case GDN_PATH_TCGEN05: return gdn::tc_launches(a);
-    case GDN_PATH_SIMT: return gdn::simt_launches(a);
+    case GDN_PATH_SIMT: return 1;  // the recurrence kernel
     default: return 0;
   }
 }
@@ -98,7 +98,7 @@ int chunk_fwd_impl(const char* fn, bool linear, const void* q, const void* k, co
   if (path == GDN_PATH_TCGEN05)
     e = gdn::launch_tc(a, s);
   else
-    e = gdn::launch_simt(a, s);
+    e = gdn::launch_rec(a, s);
   if (e != cudaSuccess)
     return fail(GDN_ELAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return GDN_OK;

@@ -157,7 +157,7 @@ cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream) {
     f.cu_seqlens = nullptr;
     f.B = a.B; f.H = a.H; f.T = (int)len; f.dk = a.dk; f.dv = a.dv; f.C = a.C; f.N = a.B;
     f.bf16 = a.bf16;
-    e = a.tc ? launch_tc(f, stream) : launch_simt(f, stream);
+    e = a.tc ? launch_tc(f, stream) : launch_rec(f, stream);
     if (e == cudaSuccess) e = cudaEventRecord(computed[r], stream);
     prev = st;
     if (e != cudaSuccess) break;

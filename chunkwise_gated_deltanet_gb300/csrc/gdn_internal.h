@@ -41,9 +41,8 @@ struct FwdArgs {
   int bf16;               // 1: q/k/v/out are bf16, 0: fp32
 };
 
-// CUDA-core kernel: any supported shape, fp32 arithmetic.  Returns a cudaError_t.
-cudaError_t launch_simt(const FwdArgs& a, cudaStream_t stream);
-int simt_launches(const FwdArgs& a);
+// Per-token recurrence on CUDA cores, fp32 arithmetic, any supported shape (C unused).
+cudaError_t launch_rec(const FwdArgs& a, cudaStream_t stream);
 
 // tcgen05 kernel: bf16, dk = dv = 128, C = 64.
 bool tc_supported(int dk, int dv, int C, int bf16);

@@ -1232,7 +1232,7 @@ int tc_launches(const FwdArgs&) { return 1; }
 
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.B * a.T;
-  if (rows == 0) return launch_simt(a, stream);  // nothing to load: state copy only
+  if (rows == 0) return launch_rec(a, stream);  // nothing to load: state copy only
   if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, rows, a.H) || !make_map(&mk, a.k, rows, a.H) ||

@@ -43,7 +43,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 /* Which kernel family a call with these sizes runs (for callers and tests). */
 typedef enum {
   GDN_PATH_NONE = 0,      /* sizes not supported */
-  GDN_PATH_SIMT = 1,      /* fp32 CUDA-core kernel: fp32 inputs, or other shapes */
+  GDN_PATH_SIMT = 1,      /* CUDA-core kernel, fp32 arithmetic, the per-token recurrence
+                             (exact; C is not used): fp32 inputs, or other shapes */
   GDN_PATH_TCGEN05 = 2    /* bf16 tcgen05 tensor-core kernel: dk = dv = 128, C = 64 */
 } gdn_path;
 
@@ -61,7 +62,9 @@ typedef enum {
  * B, H, T    batch, heads, tokens per sequence; with cu_seqlens, B must be 1 and T is
  *            the total packed token count
  * dk, dv     head sizes, each one of 16, 32, 64, 128
- * C          chunk length, one of 16, 32, 64; a sequence's last chunk may be shorter
+ * C          chunk length, one of 16, 32, 64; a sequence's last chunk may be shorter (the
+ *            CUDA-core path computes the recurrence token by token, which the chunk form
+ *            equals, and does not use it)
  * cu_seqlens int32 [N_seqs + 1] DEVICE array of packed sequence offsets
  *            (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N_seqs] = T), or NULL for
  *            N = B fixed-length sequences.  The state restarts at every offset.
