@@ -259,3 +259,22 @@ def test_host_forward_workspace_query(lib):
     inputs = 4 * 4096 * 16 * (3 * 128 * 2 + 128 * 2 + 8)
     assert full >= inputs and lin < full
     assert f(4, 16, 4096, 128, 128, 64, gdn.GDN_BF16, 0, 0) == 0
+
+
+@pytest.mark.parametrize("lang,std", [("c", "c99"), ("c++", "c++11")])
+def test_header_compiles_standalone(lang, std, tmp_path):
+    """include/gdn.h is a plain C ABI: it compiles on its own as C99 and as C++11, with
+    warnings as errors, and a C program can take the address of every entry point."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("use.c" if lang == "c" else "use.cpp")
+    names = _declared_functions()
+    src.write_text('#include "gdn.h"\n' + "void* entry_points[] = {\n" +
+                   ",\n".join("  (void*)&%s" % n for n in names) + "\n};\n")
+    r = subprocess.run([cc, "-std=" + std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
