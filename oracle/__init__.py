@@ -16,7 +16,7 @@ Contents (fp64 throughout):
 * ``derivations`` -- the page's own closed forms and identities used to pin the
   recurrence: linear attention and Mamba2 matrix forms, the WY identity, the U/G
   identity, the unrolled state, the full-sequence matrix form and the chunk
-  computation.
+  computation, and the chunk form's backward (pinned to ``backward``).
 * ``backward``    -- the reverse-mode derivative of the per-token recurrence
   (gradients of q, k, v, log alpha, beta and S0 for given output and final-state
   gradients); the pages derive none, so it is pinned to finite differences and to

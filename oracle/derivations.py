@@ -223,3 +223,92 @@ def chunked_wy_delta(q, k, v, log_alpha, beta, S0, C):
         O[t0:t1] = np.exp(g)[:, None] * (Qc @ S.T) + ((Qc @ Kc.T) * D) @ delta
         S = np.exp(g[-1]) * S + delta.T @ (np.exp(g[-1] - g)[:, None] * Kc)
     return O, S
+
+
+def chunked_wy_delta_bwd(q, k, v, log_alpha, beta, S0, dO, dS_final, C):
+    """The backward of ``chunked_wy_delta``, chunk by chunk in reverse (the pages
+    derive none; this is the reverse-mode derivative of the chunk form above,
+    written with matrices so that each line is a dense product a tensor-core kernel
+    can take).  Per chunk, with S the chunk-start state, dS' the gradient of the
+    chunk-end state, E = diag(e^{g_last - g}), P = lower-incl(Q K^T o D):
+
+        d delta = P^T dO + E K dS'^T
+        dS      = dO^T diag(e^g) Q + e^{g_last} dS' - d delta^T W~      (to the previous chunk)
+        dP      = lower-incl(dO delta^T)
+        dQ      = diag(e^g) dO S + (dP o D) K
+        dK      = (dP o D)^T Q + E delta dS'  + diag(beta e^g) T^T dW + X K + X^T K
+        dU      = d delta,  dW = -d delta S,  dV = diag(beta) T^T dU
+        dT      = dU (diag(beta) V)^T + dW (diag(beta e^g) K)^T,  dA = -T^T dT T^T
+        X       = strictly-lower(dA) o D o beta_i
+        dbeta_i = (T^T dU)_i . v_i + e^{g_i} (T^T dW)_i . k_i + sum_j dA_ij (k_i . k_j) D_ij
+
+    and the gate: every use of g (D, e^g, e^{g_last}) gives dg, and d log alpha is
+    the reverse cumulative sum of dg inside the chunk.  Returns (dq, dk, dv,
+    dlog_alpha, dbeta, dS0) like ``backward.gdn_sequence_bwd``.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    la = np.asarray(log_alpha, np.float64)
+    b = np.asarray(beta, np.float64)
+    dO = np.asarray(dO, np.float64)
+    L, dk = k.shape
+    dv = v.shape[1]
+    # forward: chunk-start states
+    S = np.zeros((dv, dk)) if S0 is None else np.array(S0, np.float64)
+    starts = []
+    bounds = [(t0, min(L, t0 + C)) for t0 in range(0, L, C)]
+    for t0, t1 in bounds:
+        starts.append(S.copy())
+        _, S = chunked_wy_delta(q[t0:t1], k[t0:t1], v[t0:t1], la[t0:t1], b[t0:t1], S, C)
+    dS = np.zeros((dv, dk)) if dS_final is None else np.array(dS_final, np.float64)
+    gq, gk, gv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    gla, gb = np.zeros(L), np.zeros(L)
+    for (t0, t1), S in zip(reversed(bounds), reversed(starts)):
+        n = t1 - t0
+        Kc, Qc, Vc, bc, dOc = k[t0:t1], q[t0:t1], v[t0:t1], b[t0:t1], dO[t0:t1]
+        g = np.cumsum(la[t0:t1])
+        eg, Gm = np.exp(g), np.exp(g[-1])
+        E = np.exp(g[-1] - g)
+        Mi = np.tril(np.ones((n, n)))
+        D = np.exp(g[:, None] - g[None, :]) * Mi
+        KK = Kc @ Kc.T
+        A = np.tril(bc[:, None] * KK * D, -1)
+        T = np.linalg.solve(np.eye(n) + A, np.eye(n))
+        Wt = T @ ((bc * eg)[:, None] * Kc)
+        U = T @ (bc[:, None] * Vc)
+        delta = U - Wt @ S.T
+        QK = Qc @ Kc.T
+        P = QK * D
+        dSn = dS  # gradient of this chunk's end state
+        # output and state-update terms
+        ddelta = P.T @ dOc + (E[:, None] * Kc) @ dSn.T
+        dS_prev = dOc.T @ (eg[:, None] * Qc) + Gm * dSn - ddelta.T @ Wt
+        dP = (dOc @ delta.T) * Mi
+        dQ = eg[:, None] * (dOc @ S) + (dP * D) @ Kc
+        dK = (dP * D).T @ Qc + E[:, None] * (delta @ dSn)
+        # delta = U - W~ S^T
+        dU = ddelta
+        dW = -ddelta @ S
+        TdU, TdW = T.T @ dU, T.T @ dW
+        dV = bc[:, None] * TdU
+        dK += (bc * eg)[:, None] * TdW
+        db = np.sum(TdU * Vc, axis=1) + eg * np.sum(TdW * Kc, axis=1)
+        # T = (I + A)^{-1}
+        dT = dU @ (bc[:, None] * Vc).T + dW @ ((bc * eg)[:, None] * Kc).T
+        dA = np.tril(-T.T @ dT @ T.T, -1)
+        X = dA * D * bc[:, None]
+        dK += X @ Kc + X.T @ Kc
+        db += np.sum(dA * KK * D, axis=1)
+        # gates: dD from A and P, d e^g from W~ and O, d e^{g_last} and E from S'
+        dD = dA * bc[:, None] * KK + dP * QK
+        dg = np.sum(dD * D, axis=1) - np.sum(dD * D, axis=0)
+        deg = bc * np.sum(TdW * Kc, axis=1) + np.sum(dOc * (Qc @ S.T), axis=1)
+        dg += deg * eg
+        dE = np.sum((delta @ dSn) * Kc, axis=1)  # d(e^{g_last - g_s})
+        dg -= dE * E
+        dg[-1] += np.sum(dE * E) + np.sum(dSn * S) * Gm
+        gq[t0:t1], gk[t0:t1], gv[t0:t1], gb[t0:t1] = dQ, dK, dV, db
+        gla[t0:t1] = np.cumsum(dg[::-1])[::-1]
+        dS = dS_prev
+    return gq, gk, gv, gla, gb, dS

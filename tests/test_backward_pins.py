@@ -149,3 +149,40 @@ def test_finite_difference_pin_catches_planted_mistake(kind):
     ns = {"np": np}
     exec(src.replace(old, new), ns)
     assert not _fd_agrees(ns["gdn_sequence_bwd"])
+
+
+@pytest.mark.parametrize("C,L", [(1, 7), (2, 9), (4, 13), (16, 40), (64, 64), (16, 37)])
+def test_chunk_form_backward_equals_per_token_backward(C, L):
+    """The chunk-form backward (matrix products per chunk, chunks in reverse) gives the
+    per-token backward's gradients, for chunk lengths from 1 to 64 and ragged tails."""
+    from oracle import derivations as D
+    args, dO, dSf = _rand(L, 6, 5, C + L)
+    ref = BW.gdn_sequence_bwd(*args, dO, dSf)
+    got = D.chunked_wy_delta_bwd(*args, dO, dSf, C)
+    for name, g, r in zip(("dq", "dk", "dv", "dla", "dbeta", "dS0"), got, ref):
+        assert np.allclose(g, r, rtol=1e-9, atol=1e-11), (name, np.abs(g - r).max())
+
+
+CHUNK_PLANTS = {
+    "dK_misses_symmetric_gram_term": ("dK += X @ Kc + X.T @ Kc", "dK += X @ Kc"),
+    "dA_sign": ("dA = np.tril(-T.T @ dT @ T.T, -1)", "dA = np.tril(T.T @ dT @ T.T, -1)"),
+    "state_gradient_not_decayed": ("+ Gm * dSn -", "+ dSn -"),
+    "gate_gradient_not_reverse_summed": ("gla[t0:t1] = np.cumsum(dg[::-1])[::-1]",
+                                         "gla[t0:t1] = dg"),
+    "delta_gradient_misses_state_write": ("ddelta = P.T @ dOc + (E[:, None] * Kc) @ dSn.T",
+                                          "ddelta = P.T @ dOc"),
+}
+
+
+@pytest.mark.parametrize("kind", sorted(CHUNK_PLANTS))
+def test_chunk_form_pin_catches_planted_mistake(kind):
+    from oracle import derivations as D
+    old, new = CHUNK_PLANTS[kind]
+    src = inspect.getsource(D.chunked_wy_delta_bwd)
+    assert old in src
+    ns = {"np": np, "chunked_wy_delta": D.chunked_wy_delta}
+    exec(src.replace(old, new), ns)
+    args, dO, dSf = _rand(37, 6, 5, 3)
+    ref = BW.gdn_sequence_bwd(*args, dO, dSf)
+    got = ns["chunked_wy_delta_bwd"](*args, dO, dSf, 16)
+    assert not all(np.allclose(g, r, rtol=1e-9, atol=1e-11) for g, r in zip(got, ref))
