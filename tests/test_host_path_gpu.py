@@ -73,3 +73,14 @@ def test_host_path_empty_sequence():
     h = _pin(inp)
     out, Sf = gdn.chunk_fwd(h["q"], h["k"], h["v"], h["log_alpha"], h["beta"], h["S0"], C=64)
     assert out.numel() == 0 and torch.equal(Sf, inp["S0"])
+
+
+def test_host_path_linear_attention_without_gates():
+    """The linear mode with log_alpha = None (alpha = 1) through the native host path."""
+    w = W["gdn_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(w, B=2, H=2, T=257, seed=8)
+    d, h = to_device(inp), _pin(inp)
+    dev = gdn.linear_chunk_fwd(d["q"], d["k"], d["v"], None, None, C=64)
+    host = gdn.linear_chunk_fwd(h["q"], h["k"], h["v"], None, None, C=64, pieces=3)
+    torch.cuda.synchronize()
+    _same(dev, host)
