@@ -119,8 +119,8 @@ constexpr int ST_FLAG = ST_DER + ST_NST * ST_DER_STAGE * 4;  // [2] int
 constexpr int ST_BAR = ST_FLAG + 64;
 constexpr int ST_MISC = ST_BAR + 192;
 constexpr int ST_USED = ST_MISC + 64;
-// The output tile of a chunk is staged in the Q rows of its own stage once Q is no
-// longer read (rows 0..31 in panel 0, rows 32..63 in panel 1, 256 bytes a row).
+// The output tile of a chunk is staged in the chunk's P slot once delta^T P^T has
+// read it (token t at t * 256 bytes), then copied out with 16-byte stores.
 
 constexpr int SMEM_USED = WY_USED > ST_USED ? WY_USED : ST_USED;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
