@@ -412,7 +412,7 @@ __device__ __forceinline__ void wy_epi_a(uint32_t t_kk, float* arow, int i, floa
 // P_{t,j} = q_t.k_j e^{g_t - g_j} with gt = g_t and colv = g_j.
 template <bool FACTORED>
 __device__ __forceinline__ void aux_epi_p(uint32_t t_qk, uint8_t* ps, int t, float gt,
-                                          const float* colv) {
+                                          const float* colv, bool store) {
 #pragma unroll 1
   for (int c = 0; c < 8; ++c) {  // columns 8c .. 8c + 7
     uint32_t r[8];
@@ -427,7 +427,7 @@ __device__ __forceinline__ void aux_epi_p(uint32_t t_qk, uint8_t* ps, int t, flo
       const float x = __uint_as_float(r[e]);
       v[e] = (jc0 + e <= t) ? (FACTORED ? x * cv[e] : ex2(gt - cv[e]) * x) : 0.f;
     }
-    st_sw128_8_split(ps, ps + 8192, t, jc0, 64, v);
+    if (store) st_sw128_8_split(ps, ps + 8192, t, jc0, 64, v);
   }
 }
 
@@ -989,20 +989,23 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       AP_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
       const bool factored = flags[s] != 0;
 
-      // ---- Q K^T (rows 0..63 of the M=128 accumulator [Q;K] K^T), issued from warp 6 ----
+      // ---- Q K^T as an M=64 accumulator (row m in TMEM lane 32 (m / 16) + m % 16, so
+      //      every warp of this group holds 16 rows), issued from warp 6 ----
       if (atid == 64)
         mma_k128_commit(tmem + TT_QK, desc_k(stg, 0, 16384), desc_k(stg + 8192, 0, 16384),
-                        idesc_bf16(128, 64, 0, 0), &bars[SB_QKM]);
+                        idesc_bf16(64, 64, 0, 0), &bars[SB_QKM]);
       AP_WAIT(&bars[SB_QKM], j & 1);
       AP_WAIT(&bars[SB_PE + b], ((j >> 1) & 1) ^ 1);  // outputs of chunk j - 2 left slot b
       tc_fence_after();
       // factored:  P'_{t,j} = q_t.k_j e^{-g_j}      (the e^{g_t} is applied to the outputs)
       // otherwise: P_{t,j}  = q_t.k_j e^{g_t - g_j} (and Q is scaled by e^{g_t} below)
-      if (q4 < 2) {
+      {
+        // the TMEM loads are warp-wide; lanes 16..31 of each warp hold no row
+        const int prow = 16 * q4 + (lane & 15);
         if (factored)
-          aux_epi_p<true>(tq + TT_QK, ps, row, 0.f, GN);
+          aux_epi_p<true>(tq + TT_QK, ps, prow, 0.f, GN, lane < 16);
         else
-          aux_epi_p<false>(tq + TT_QK, ps, row, GN[row], GN);
+          aux_epi_p<false>(tq + TT_QK, ps, prow, GN[prow], GN, lane < 16);
       }
       if (!factored) {
         // Q <- diag(e^{g}) Q in place (bf16), after Q K^T has read it: 16-byte pieces,
