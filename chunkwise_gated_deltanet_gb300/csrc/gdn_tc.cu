@@ -138,16 +138,18 @@ enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE = 9, WB_COUNT = 
 static_assert(WB_COUNT * 8 <= WY_MISC - WY_BAR, "WY barriers");
 enum StBar {
   SB_QK_FULL = 0, SB_QK_EMPTY = 2, SB_HF = 4, SB_C = 6, SB_DS = 7, SB_QKM = 8, SB_DP = 9,
-  SB_PF = 10, SB_U = 13, SB_DR = 15, SB_SWI = 17, SB_SQ = 18, SB_PE = 19,
-  SB_COUNT = 21
+  SB_PF = 11, SB_U = 13, SB_DR = 15, SB_SWI = 17, SB_SQ = 18, SB_PE = 20,
+  SB_COUNT = 22
 };
 static_assert(SB_COUNT * 8 <= ST_MISC - ST_BAR, "state barriers");
 
 // TMEM columns.  WY: per warpgroup w at 128*w: K K^T 0, W~^T 64.
 constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
-// state: S 0..127, U^T + S(-W~^T) of chunk j at 128 + 64 (j % 2), outputs 256, QK 320,
-// delta hi 384, delta lo 416, delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
-constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 256, TT_QK = 320, TT_DH = 384, TT_DL = 416,
+// state: S 0..127, U^T + S(-W~^T) 128 (one accumulator: U^T(j + 1) is issued only after
+// the delta epilogue of chunk j has read it), outputs of chunk j at 192 + 64 (j % 2),
+// QK 320, delta hi 384, delta lo 416, delta~ hi 448, delta~ lo 480 (packed bf16 pairs,
+// A operands).
+constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_QK = 320, TT_DH = 384, TT_DL = 416,
                    TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
 
@@ -790,7 +792,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         const int j = nd;
         if (mbar_test(&bars[SB_DR + (j & 1)], (j >> 1) & 1, false) &&
             mbar_test(&bars[SB_PF + (j & 1)], (j >> 1) & 1, false) &&
-            mbar_test(&bars[SB_SQ], j & 1, false))
+            mbar_test(&bars[SB_SQ + (j & 1)], (j >> 1) & 1, false))
           kind = 2;
       }
       const bool did = kind >= 0;
@@ -802,7 +804,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             uint8_t* stg = sm + ST_QK + (i % ST_NST) * ST_STAGE;
             uint8_t* hs = sm + ST_HS + (i & 1) * HS_BYTES;
             const uint32_t id_u = idesc_bf16(128, 64, 1, 0);
-            const uint32_t d = tmem + TT_SW + 64 * (i & 1);
+            const uint32_t d = tmem + TT_SW;
             const uint64_t dv = desc_mn(stg + ST_V, 0, 8192);
             mma_k64<false, false, false>(d, dv, 0, desc_k(hs + HS_TUH, 0, 8192), id_u, 0);
             mma_k64<false, false, false>(d, dv, 0, desc_k(hs + HS_TUL, 0, 8192), id_u, 1);
@@ -815,10 +817,11 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             const uint8_t* ps = sm + ST_PS + (j & 1) * PS_BYTES;
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
             const uint64_t ph = desc_k(ps, 0, 8192), pl = desc_k(ps + 8192, 0, 8192);
-            mma_k64<true, false, false>(tmem + TT_O, 0, tmem + TT_DH, ph, id, 1);
-            mma_k64<true, false, false>(tmem + TT_O, 0, tmem + TT_DH, pl, id, 1);
-            mma_k64<true, false, false>(tmem + TT_O, 0, tmem + TT_DL, ph, id, 1);
-            mma_commit(&bars[SB_DP]);
+            const uint32_t d = tmem + TT_O + 64 * (j & 1);
+            mma_k64<true, false, false>(d, 0, tmem + TT_DH, ph, id, 1);
+            mma_k64<true, false, false>(d, 0, tmem + TT_DH, pl, id, 1);
+            mma_k64<true, false, false>(d, 0, tmem + TT_DL, ph, id, 1);
+            mma_commit(&bars[SB_DP + (j & 1)]);
           }
         }
         __syncwarp();
@@ -906,19 +909,20 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
         const uint64_t ds = desc_k(sm + ST_SB, 0, 16384), dw = desc_mn(hs, 0, 16384);
-        mma_k128<true>(tmem + TT_SW + 64 * b, ds, 16384 >> 4, dw, 0, id, 1);
+        mma_k128<true>(tmem + TT_SW, ds, 16384 >> 4, dw, 0, id, 1);
         mma_commit(&bars[SB_C]);
         mbar_arrive(&bars[SB_SWI]);  // S Q^T may now be queued behind S W~^T
       }
       // S W~^T done; delta of chunk j - 1 read by its delta^T P^T
-      CH_WAIT3(&bars[SB_C], j & 1, false, j > 0 ? &bars[SB_DP] : nullptr, (j - 1) & 1, nullptr, 0);
+      CH_WAIT3(&bars[SB_C], j & 1, false, j > 0 ? &bars[SB_DP + ((j - 1) & 1)] : nullptr,
+               ((j - 1) >> 1) & 1, nullptr, 0);
       tc_fence_after();
       // the slot's only readers were the MMAs whose completion was just observed
       if (tid == 0) mbar_arrive_remote_relaxed(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + b)), 0));
 
       // ---- delta and its decayed copy as hi/lo bf16 A operands in TMEM ----
 #pragma unroll 1
-      for (int qq = 0; qq < 4; ++qq) delta_quarter(tq, TT_SW + 64 * b, ED, qq);
+      for (int qq = 0; qq < 4; ++qq) delta_quarter(tq, TT_SW, ED, qq);
       tmem_wait_st();
       tc_fence_before();
       named_sync(1, 128);
@@ -936,7 +940,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       }
       // the state update is done, S Q^T of chunk j has read S, chunk j + 1 is loaded
       const bool last = (j + 1 == u.nc);
-      CH_WAIT3(&bars[SB_DS], j & 1, false, &bars[SB_SQ], j & 1,
+      CH_WAIT3(&bars[SB_DS], j & 1, false, &bars[SB_SQ + b], (j >> 1) & 1,
                last ? nullptr : &bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1);
       tc_fence_after();
       if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // the chain's last read of stage s
@@ -1042,19 +1046,34 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   // aux O holds no stage: each of its warps recomputes the chunk's gate factors from
   // the gates in global memory (the same scan as the producer, so the same values and
   // the same choice of form), and the bf16 outputs are staged in the chunk's P slot,
-  // which delta^T P^T no longer reads.  It also issues S Q^T, which must wait for the
-  // previous chunk's outputs to leave the accumulator.
+  // which delta^T P^T no longer reads.  It also issues S Q^T into the output
+  // accumulator of the chunk's parity, whose previous chunk it drained one iteration
+  // earlier.
   const int atid = tid - 256;
 #define AO_WAIT(bar, par) \
   if (group_wait_fails((bar), (par), abort_flag, false, 3, 128)) break;
-  // Iteration i drains the outputs of chunk i - 1 out of TMEM, issues S Q^T (i), then
-  // copies chunk i - 1 out: one issue site.
+  // Iteration i issues S Q^T (i), then drains the outputs of chunk i - 1 out of TMEM
+  // and copies them out: one issue site.
   GateLoad gnext = load_gates(log_alpha, beta, u, H, 0, lane);
   #pragma unroll 1
   for (int i = 0; i <= u.nc; ++i) {
     const int j = i - 1, b = j & 1;
-    __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(sm + ST_PS + b * PS_BYTES);
+    if (i < u.nc) {
+      // S Q^T (i) starts output accumulator i % 2: issued (from warp 11) once the chain
+      // has queued S W~^T (i), which reads the same bf16 S; in the strong-decay form
+      // also once aux P has scaled Q.  The chunk's form is read from its stage, which
+      // the chain waited for before signalling.  The accumulator's previous chunk,
+      // i - 2, left TMEM before the last iteration's final barrier.
+      AO_WAIT(&bars[SB_SWI], i & 1);
+      const int si = i % ST_NST;
+      if (flags[si] == 0) AO_WAIT(&bars[SB_PF + (i & 1)], (i >> 1) & 1);
+      if (atid == 96)
+        mma_k128_commit(tmem + TT_O + 64 * (i & 1), desc_k(sm + ST_SB, 0, 16384),
+                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),
+                        &bars[SB_SQ + (i & 1)]);
+    }
     if (i > 0) {
+      __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(sm + ST_PS + b * PS_BYTES);
       const GateLoad gcur = gnext;
       gnext = load_gates(log_alpha, beta, u, H, i, lane);  // in flight during the wait
       float g0, g1, tot;
@@ -1062,13 +1081,14 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       const bool factored = -tot < kMaxFactoredDecayLog2;
       const float e0 = factored ? ex2(g0) : 1.f, e1 = factored ? ex2(g1) : 1.f;
       // S Q^T and delta^T P^T of chunk j (the MMA warp commits delta^T P^T last)
-      AO_WAIT(&bars[SB_DP], j & 1);
+      AO_WAIT(&bars[SB_DP + b], (j >> 1) & 1);
       tc_fence_after();
       // ---- bf16 outputs staged in P slot b (row t at t * 256 bytes), 8 tokens a step ----
+      const uint32_t to = tq + TT_O + 64 * b;
 #pragma unroll 1
       for (int q = 0; q < 8; ++q) {
         uint32_t a[8];
-        tmem_ld8(tq + TT_O + 8 * q, a);
+        tmem_ld8(to + 8 * q, a);
         tmem_wait_ld();
         const float ev = q < 4 ? e0 : e1;  // e^{g_t} of tokens 8q .. 8q + 7 (lanes t % 32)
 #pragma unroll
@@ -1077,22 +1097,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
               __shfl_sync(0xffffffffu, ev, (8 * q + e) & 31) * __uint_as_float(a[e]));
       }
       tc_fence_before();
-      named_sync(3, 128);  // O of chunk j is out of TMEM: S Q^T (j + 1) may overwrite it
-    }
-    if (i < u.nc) {
-      // S Q^T (i) starts the output accumulator of chunk i: issued (from warp 11) once
-      // the chain has queued S W~^T (i), which reads the same bf16 S; in the
-      // strong-decay form also once aux P has scaled Q.  The chunk's form is read from
-      // its stage, which the chain waited for before signalling.
-      AO_WAIT(&bars[SB_SWI], i & 1);
-      const int si = i % ST_NST;
-      if (flags[si] == 0) AO_WAIT(&bars[SB_PF + (i & 1)], (i >> 1) & 1);
-      if (atid == 96)
-        mma_k128_commit(tmem + TT_O, desc_k(sm + ST_SB, 0, 16384),
-                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),
-                        &bars[SB_SQ]);
-    }
-    if (i > 0) {
+      named_sync(3, 128);  // outputs staged; accumulator b is free for S Q^T (j + 2)
       const long long c0 = (long long)j * kC;
       const int lc = (int)min((long long)kC, u.len - c0);
       const size_t obase = (size_t)(u.row0 + c0) * H + u.h;
