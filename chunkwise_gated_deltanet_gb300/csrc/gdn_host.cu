@@ -1,14 +1,18 @@
 // The forward on host buffers: copies in, the chunkwise forward, copies out, pipelined
 // over consecutive token ranges.
 //
-// A fixed-length batch [B, T, H, d] is cut into `pieces` ranges of whole chunks.  Range
-// r of every tensor is one strided block (B rows of L*H*d elements, pitch T*H*d), so it
-// moves with a single cudaMemcpy2DAsync.  Inputs go in on one copy stream, ranges are
+// A fixed-length batch [B, T, H, d] is cut into `pieces` ranges of whole chunks, each
+// about half as long as the one before.  Range r of every tensor is one strided block
+// (B rows of L*H*d elements, pitch T*H*d), so it moves with a single cudaMemcpy2DAsync.  Inputs go in on one copy stream, ranges are
 // computed in order on the caller's stream (range r starts from range r-1's fp32 final
 // state, so the result is the unsplit forward's), outputs come back on a second copy
 // stream; events order the three.  The copy of range r+1 and the write-back of range
 // r-1 then overlap the computation of range r, and the two copy directions overlap
-// each other.
+// each other.  Only the last range's computation and write-back follow the last input
+// copy, hence the decreasing lengths: the input copies take about four times as long per
+// chunk as the computation, so each range's computation still hides behind the next
+// range's copy while the tail shrinks.  (A write-back that overlaps the input copies
+// slows them by about half its own time, so the tail is the part worth shrinking.)
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -22,19 +26,35 @@ size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct HostLayout {
   int pieces;
-  long long per;      // tokens per range (a multiple of C)
+  long long bound[65];  // range r is tokens [bound[r], bound[r + 1]), whole chunks
   size_t q, k, v, la, be, out, s0, st, total;  // byte offsets of the device buffers
 };
+
+// Weight of range r is kRangeRatio^r; boundaries are rounded to whole chunks with at
+// least one chunk per range.
+constexpr double kRangeRatio = 0.5;
 
 HostLayout host_layout(int B, int H, int T, int dk, int dv, int C, int esz, int pieces,
                        bool has_beta) {
   HostLayout L;
-  const long long n_chunks = (T + C - 1) / C;
-  long long want = n_chunks < pieces ? n_chunks : pieces;
-  if (want < 1) want = 1;
-  const long long per_chunks = n_chunks > 0 ? (n_chunks + want - 1) / want : 1;
-  L.per = per_chunks * C;
-  L.pieces = n_chunks > 0 ? (int)((n_chunks + per_chunks - 1) / per_chunks) : 1;
+  const long long nc = (T + C - 1) / C;
+  int P = (int)(nc < pieces ? nc : pieces);
+  if (P < 1) P = 1;
+  double wsum = 0.0, w = 1.0;
+  for (int r = 0; r < P; ++r, w *= kRangeRatio) wsum += w;
+  L.bound[0] = 0;
+  double acc = 0.0;
+  long long prev = 0;
+  w = 1.0;
+  for (int r = 0; r < P; ++r, w *= kRangeRatio) {
+    acc += w / wsum;
+    long long c = (r == P - 1) ? nc : (long long)(acc * (double)nc + 0.5);
+    if (c < prev + 1) c = prev + 1;
+    if (c > nc - (P - 1 - r)) c = nc - (P - 1 - r);
+    L.bound[r + 1] = c * C < T ? c * C : T;
+    prev = c;
+  }
+  L.pieces = P;
   const size_t rows = (size_t)B * T * H;
   L.q = 0;
   L.k = L.q + al256(rows * dk * esz);
@@ -124,7 +144,7 @@ cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream) {
     e = cudaMemcpyAsync(s0_dev, a.S0, state_bytes, cudaMemcpyHostToDevice, cs.in);
   // every input range goes in first, in order, so the copy engine never waits
   for (int r = 0; r < n && e == cudaSuccess; ++r) {
-    const long long t0 = r * L.per, len = (t0 + L.per < a.T ? L.per : a.T - t0);
+    const long long t0 = L.bound[r], len = L.bound[r + 1] - t0;
     const size_t tok = (size_t)a.B * t0 * a.H;  // token-heads before this range
     e = copy_range(ws + L.q + tok * a.dk * esz, a.q, true, a.B, a.T, a.H, t0, len, a.dk, esz, cs.in);
     if (e == cudaSuccess)
@@ -140,7 +160,7 @@ cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream) {
   // ranges in order on the caller's stream, each from the previous final state
   const float* prev = s0_dev;
   for (int r = 0; r < n && e == cudaSuccess; ++r) {
-    const long long t0 = r * L.per, len = (t0 + L.per < a.T ? L.per : a.T - t0);
+    const long long t0 = L.bound[r], len = L.bound[r + 1] - t0;
     const size_t tok = (size_t)a.B * t0 * a.H;
     float* st = reinterpret_cast<float*>(ws + L.st + (size_t)(r & 1) * al256(state_bytes));
     e = cudaStreamWaitEvent(stream, loaded[r], 0);

@@ -137,8 +137,9 @@ size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int N_
  * HOST buffers, end to end: copies the inputs in, runs the forward, copies the outputs
  * back, and returns once they are in host memory.  Fixed-length batches only.
  *
- * The batch is cut into at most `pieces` consecutive ranges of whole chunks (1..64).
- * Inputs go in on one internal copy stream, range r is computed on `stream` from range
+ * The batch is cut into at most `pieces` consecutive ranges of whole chunks (1..64),
+ * each about half as long as the one before, so that little work follows the last input
+ * copy.  Inputs go in on one internal copy stream, range r is computed on `stream` from range
  * r-1's fp32 final state (so the results equal the unsplit forward's bit for bit), and
  * outputs come back on a second internal copy stream; the copies of one range overlap
  * the computation of the next, and the two copy directions overlap each other.  Each
