@@ -18,11 +18,12 @@
 //   chain (serial):  SW = U^T + S (-W~^T) = delta^T;  S <- e^{g_last} S + delta~^T K
 //                    (S accumulates in TMEM; delta feeds the MMAs from TMEM)
 //   MMA warp:        U^T = V^T (T diag(beta))^T into SW ahead of the chain;
-//                    O = S Q^T, then O += delta^T P^T (one accumulator per chunk
-//                    parity, so the outputs of chunk j drain while j+1 runs)
-//   aux P (ahead):   Q K^T -> P' = lower(q_t.k_j e^{-g_j}) (factored decay), or
-//                    P = lower(q_t.k_j e^{g_t-g_j}) and Q <- diag(e^g) Q in place
-//   aux O (behind):  o_t = e^{g_t} O_t (factored) or O_t -> out
+//                    O += delta^T P^T onto the output accumulator of the chunk's
+//                    parity (two, so the outputs of chunk j drain while j+1 runs)
+//   aux P (ahead):   Q K^T (M=64) -> P' = lower(q_t.k_j e^{-g_j}) (factored decay),
+//                    or P = lower(q_t.k_j e^{g_t-g_j}) and Q <- diag(e^g) Q in place
+//   aux O (behind):  O = S Q^T into that accumulator once the chain has queued its
+//                    S W~^T; then o_t = e^{g_t} O_t (factored) or O_t -> out
 // The factored form keeps the output accumulator in the frame of e^{-g_t}: the
 // state part S q_t and every in-chunk term e^{-g_j} (q_t.k_j) delta_j share that
 // factor, which aux O multiplies back.  It is used when the chunk's total decay
@@ -48,10 +49,12 @@
 //   WY:    kv_full[s]  (TMA bytes + producer arrive)   kv_empty[s] (WG after its MMAs)
 //          wg_mma[w]   (MMA commits of warpgroup w)
 //          hand_empty[b] (arrived by CTA 1 once chunk j's slot has been read)
-//   state: qk_full[s]; qk_empty[s] (chain after its state update + aux O after its
-//          copy-out); hand_full[b] (bulk-copy bytes); bar_u, bar_sq, bar_dp[b] (MMA warp
-//          commits); bar_c, bar_ds (chain commits); sw_issued, delta_ready (chain
-//          arrives); p_full[b] (aux P); o_empty[b] (aux O); bar_qk (aux P's commit)
+//   state: qk_full[s]; qk_empty[s] (chain after its state update + aux P after its
+//          Q K^T); hand_full[b] (bulk-copy bytes); bar_u[b], bar_dp[b] (MMA warp
+//          commits); bar_sq[b] (aux O's commit); bar_c, bar_ds (chain commits);
+//          sw_issued, delta_ready[b] (chain arrives); p_full[b] (aux P);
+//          o_empty[b] (aux O); bar_qk (aux P's commit).  Per-parity pairs [b] advance
+//          once per two chunks, so no waiter can find its barrier two phases ahead.
 // "Empty" barriers are waited with parity ^ 1 so that their first wait passes.
 // Every wait is bounded; a wait that gives up records a code in a device status
 // word, every role of both CTAs leaves its loop, and both CTAs still meet at the
@@ -770,8 +773,9 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   }
   if (warp == kMmaWarp) {
     // ------------- MMA warp: the tensor-core work that is not on the chain's path -------------
-    // U^T = V^T Tu^T (j + 1) goes in behind the chain's state update (j), into the other
-    // U/SW accumulator, ahead of delta^T P^T (j); S Q^T is issued by aux O and Q K^T by
+    // U^T = V^T Tu^T (j + 1) goes in behind the chain's state update (j), into the U/SW
+    // accumulator (which the chain's delta epilogue of j has read by then), ahead of
+    // delta^T P^T (j); S Q^T is issued by aux O and Q K^T by
     // aux P, so that the issue work is spread over three warp schedulers.  Each kind is
     // issued in chunk order; the warp polls (non-blocking tests), U first.
     int nu = 0, nd = 0;  // next U, delta^T P^T
@@ -799,7 +803,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       if (did) {
         if (kind == 0) {
           const int i = nu++;
-          if (lane == 0) {  // U^T(i) = V^T Tu^T (hi + lo) into U/SW accumulator i % 2
+          if (lane == 0) {  // U^T(i) = V^T Tu^T (hi + lo) into the U/SW accumulator
             tc_fence_after();
             uint8_t* stg = sm + ST_QK + (i % ST_NST) * ST_STAGE;
             uint8_t* hs = sm + ST_HS + (i & 1) * HS_BYTES;
