@@ -31,7 +31,13 @@
 //
 // Linear mode (beta == NULL; Nyysyyan, "Mamba2" and "Linear attention"): the
 // erase strength is 0 and the write strength 1, so A = 0, T = I, W~ = 0 and
-// U = V exactly; the same pipeline then computes S_t = alpha_t S_{t-1} + v_t k_t^T.
+// delta = U = V exactly, independent of the state: S_t = alpha_t S_{t-1} + v_t k_t^T.
+// gdn_tc_linear_kernel runs the state CTA alone (one CTA per (sequence, head)); its
+// chain is the state update and the S epilogue, and between them it makes the next
+// chunk's delta = V and delta~ = V diag(e^{g_last-g}) from the V tile into one of two
+// TMEM buffers while the state update runs; the MMA warp's delta^T P^T reads delta from
+// there.  The results are those of the delta-rule pipeline with these factors, bit for
+// bit (its extra products are exact zeros).
 //
 // W~ uses the decayed triangular factor (W~_i = gamma_i w_i with the WY
 // recursion of Nyysyyan's "Gated-DeltaNet" section); then
@@ -155,6 +161,12 @@ constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
 constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_QK = 320, TT_DH = 384, TT_DL = 416,
                    TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
+// Linear mode: delta (= V, exact bf16 pairs) and delta~ (hi / lo) of chunk j in buffer
+// j % 2.  Buffer 0 is the delta-rule columns; buffer 1 takes the U/SW accumulator (this
+// mode has no U and no S W~^T) and the delta lo columns (delta = V needs no lo term).
+__device__ __forceinline__ uint32_t tl_dh(int b) { return b ? TT_SW : TT_DH; }
+__device__ __forceinline__ uint32_t tl_dsh(int b) { return b ? TT_SW + 32 : TT_DSH; }
+__device__ __forceinline__ uint32_t tl_dsl(int b) { return b ? TT_DL : TT_DSL; }
 
 constexpr int ST_WAIT = 1;
 
@@ -718,7 +730,32 @@ __device__ __forceinline__ void delta_quarter(uint32_t tq, uint32_t t_sw, const 
   tmem_st8(tq + TT_DSL + 8 * qq, sl);
 }
 
+// Linear mode: row `row` (a dv index) of delta^T = V^T as exact bf16 pairs and of
+// delta~^T = V^T diag(e^{g_last - g}) as hi / lo pairs, for the chunk's tokens, read
+// from the V tile (two 64-column panels, 128-byte swizzle) into TMEM buffer b.  Tokens
+// from lc on belong to no sequence of this unit and write nothing (zeros).
+__device__ __forceinline__ void lin_delta(uint32_t tq, const uint8_t* vt, const float* ED,
+                                          int row, int b, int lc) {
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {  // tokens 32h .. 32h + 31, two per TMEM column
+    uint32_t dh[16], sh[16], sl[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int t = 32 * h + 2 * c;
+      const uint32_t v0 = t < lc ? *reinterpret_cast<const uint16_t*>(vt + sw128_offset(t, row, 64)) : 0u;
+      const uint32_t v1 =
+          t + 1 < lc ? *reinterpret_cast<const uint16_t*>(vt + sw128_offset(t + 1, row, 64)) : 0u;
+      dh[c] = v0 | (v1 << 16);
+      split2(__uint_as_float(v0 << 16) * ED[t], __uint_as_float(v1 << 16) * ED[t + 1], sh[c], sl[c]);
+    }
+    tmem_st16(tq + tl_dh(b) + 16 * h, dh);
+    tmem_st16(tq + tl_dsh(b) + 16 * h, sh);
+    tmem_st16(tq + tl_dsl(b) + 16 * h, sl);
+  }
+}
+
 // ========================================================= CTA 1: state ======
+template <bool LINEAR>
 __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUtensorMap* tm_q,
                           const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           const float* __restrict__ log_alpha,
@@ -769,6 +806,40 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
     #pragma unroll 1
     for (int j = issued - ST_NST; j < issued; ++j)
       if (j >= 0) (void)mbar_wait(&bars[SB_QK_FULL + j % ST_NST], (j / ST_NST) & 1, 100000000ull);
+    return;
+  }
+  if (LINEAR && warp == kMmaWarp) {
+    // ------------- MMA warp, linear mode: delta^T P^T (j) = V^T (P hi + P lo) -------------
+    // once the chain has made delta (j), aux P has published P (j) and S Q^T (j) has
+    // completed
+    int nd = 0;
+    uint64_t t_idle = globaltimer_ns();
+    #pragma unroll 1
+    while (nd < u.nc) {
+      const int j = nd;
+      if (mbar_test(&bars[SB_DR + (j & 1)], (j >> 1) & 1, false) &&
+          mbar_test(&bars[SB_PF + (j & 1)], (j >> 1) & 1, false) &&
+          mbar_test(&bars[SB_SQ + (j & 1)], (j >> 1) & 1, false)) {
+        ++nd;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint8_t* ps = sm + ST_PS + (j & 1) * PS_BYTES;
+          const uint32_t id = idesc_bf16(128, 64, 0, 0);
+          const uint64_t ph = desc_k(ps, 0, 8192), pl = desc_k(ps + 8192, 0, 8192);
+          const uint32_t d = tmem + TT_O + 64 * (j & 1), a = tmem + tl_dh(j & 1);
+          mma_k64<true, false, false>(d, 0, a, ph, id, 1);
+          mma_k64<true, false, false>(d, 0, a, pl, id, 1);
+          mma_commit(&bars[SB_DP + (j & 1)]);
+        }
+        __syncwarp();
+        t_idle = globaltimer_ns();
+      } else if (*abort_flag != 0) {
+        break;
+      } else if (globaltimer_ns() - t_idle > kWaitNs) {
+        atomicOr((int*)abort_flag, ST_WAIT);
+        break;
+      }
+    }
     return;
   }
   if (warp == kMmaWarp) {
@@ -891,10 +962,15 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(gam * v[e]);
         tmem_st32(tq + TT_S + 32 * p, sv);
       }
+      if constexpr (LINEAR) {
+        if (u.nc > 0)
+          lin_delta(tq, sm + ST_QK + ST_V, der_all + 128, row, 0, (int)min((long long)kC, u.len));
+      }
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       named_sync(1, 128);
+      if (LINEAR && tid == 0 && u.nc > 0) mbar_arrive(&bars[SB_DR + 0]);  // delta (0) made
     } while (0);
 
     #pragma unroll 1
@@ -906,41 +982,67 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       const uint32_t buse = (uint32_t)(j >> 1);
       uint8_t* hs = sm + ST_HS + b * HS_BYTES;
 
-      // ---- delta^T = U^T + S (-W~^T): U^T = V^T Tu^T is already in the accumulator
-      //      (issued by the MMA warp) ----
-      CH_WAIT3(&bars[SB_HF + b], buse & 1, true, &bars[SB_U + b], buse & 1, nullptr, 0);
-      if (tid == 0) {
+      if constexpr (LINEAR) {
+        // delta~ (j) was made in the previous iteration; the bf16 S of chunk j is final
+        if (tid == 0) {
+          mbar_arrive(&bars[SB_SWI]);  // S Q^T (j) may be queued
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 128, 0, 1);
+          const uint64_t dkb = desc_mn(stg + 8192, 0, 16384);
+          mma_k64<true, true, true>(tmem + TT_S, 0, tmem + tl_dsh(b), dkb, id, 1);
+          mma_k64<true, true, true>(tmem + TT_S, 0, tmem + tl_dsl(b), dkb, id, 1);
+          mma_commit(&bars[SB_DS]);
+        }
+        // delta (j + 1), delta~ (j + 1) into buffer b ^ 1 while the state update runs:
+        // chunk j + 1 is loaded, and delta^T P^T (j - 1) has read that buffer's delta
+        // (the state update of j - 1, its delta~, completed in the last iteration)
+        if (j + 1 < u.nc) {
+          CH_WAIT3(&bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1, false,
+                   j > 0 ? &bars[SB_DP + (b ^ 1)] : nullptr, ((j - 1) >> 1) & 1, nullptr, 0);
+          tc_fence_after();
+          const int s1 = (j + 1) % ST_NST;
+          lin_delta(tq, sm + ST_QK + s1 * ST_STAGE + ST_V, der_all + s1 * ST_DER_STAGE + 128, row,
+                    b ^ 1, (int)min((long long)kC, u.len - (long long)(j + 1) * kC));
+          tmem_wait_st();
+          tc_fence_before();
+        }
+      } else {
+        // ---- delta^T = U^T + S (-W~^T): U^T = V^T Tu^T is already in the accumulator
+        //      (issued by the MMA warp) ----
+        CH_WAIT3(&bars[SB_HF + b], buse & 1, true, &bars[SB_U + b], buse & 1, nullptr, 0);
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 64, 0, 1);
+          const uint64_t ds = desc_k(sm + ST_SB, 0, 16384), dw = desc_mn(hs, 0, 16384);
+          mma_k128<true>(tmem + TT_SW, ds, 16384 >> 4, dw, 0, id, 1);
+          mma_commit(&bars[SB_C]);
+          mbar_arrive(&bars[SB_SWI]);  // S Q^T may now be queued behind S W~^T
+        }
+        // S W~^T done; delta of chunk j - 1 read by its delta^T P^T
+        CH_WAIT3(&bars[SB_C], j & 1, false, j > 0 ? &bars[SB_DP + ((j - 1) & 1)] : nullptr,
+                 ((j - 1) >> 1) & 1, nullptr, 0);
         tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 1);
-        const uint64_t ds = desc_k(sm + ST_SB, 0, 16384), dw = desc_mn(hs, 0, 16384);
-        mma_k128<true>(tmem + TT_SW, ds, 16384 >> 4, dw, 0, id, 1);
-        mma_commit(&bars[SB_C]);
-        mbar_arrive(&bars[SB_SWI]);  // S Q^T may now be queued behind S W~^T
-      }
-      // S W~^T done; delta of chunk j - 1 read by its delta^T P^T
-      CH_WAIT3(&bars[SB_C], j & 1, false, j > 0 ? &bars[SB_DP + ((j - 1) & 1)] : nullptr,
-               ((j - 1) >> 1) & 1, nullptr, 0);
-      tc_fence_after();
-      // the slot's only readers were the MMAs whose completion was just observed
-      if (tid == 0) mbar_arrive_remote_relaxed(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + b)), 0));
+        // the slot's only readers were the MMAs whose completion was just observed
+        if (tid == 0) mbar_arrive_remote_relaxed(map_shared(smem_u32(sm + WY_BAR + 8 * (WB_HE + b)), 0));
 
-      // ---- delta and its decayed copy as hi/lo bf16 A operands in TMEM ----
+        // ---- delta and its decayed copy as hi/lo bf16 A operands in TMEM ----
 #pragma unroll 1
-      for (int qq = 0; qq < 4; ++qq) delta_quarter(tq, TT_SW, ED, qq);
-      tmem_wait_st();
-      tc_fence_before();
-      named_sync(1, 128);
+        for (int qq = 0; qq < 4; ++qq) delta_quarter(tq, TT_SW, ED, qq);
+        tmem_wait_st();
+        tc_fence_before();
+        named_sync(1, 128);
 
-      // ---- S <- e^{g_last} S + delta~^T K (accumulated onto the pre-scaled S) ----
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 128, 0, 1);
-        const uint64_t dkb = desc_mn(stg + 8192, 0, 16384);
-        mma_k64<true, true, true>(tmem + TT_S, 0, tmem + TT_DSH, dkb, id, 1);
-        mma_k64<true, true, true>(tmem + TT_S, 0, tmem + TT_DSL, dkb, id, 1);
-        mma_commit(&bars[SB_DS]);
-        // delta of chunk j is in TMEM and the accumulator of U^T + S(-W~^T) is free
-        mbar_arrive(&bars[SB_DR + b]);
+        // ---- S <- e^{g_last} S + delta~^T K (accumulated onto the pre-scaled S) ----
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 128, 0, 1);
+          const uint64_t dkb = desc_mn(stg + 8192, 0, 16384);
+          mma_k64<true, true, true>(tmem + TT_S, 0, tmem + TT_DSH, dkb, id, 1);
+          mma_k64<true, true, true>(tmem + TT_S, 0, tmem + TT_DSL, dkb, id, 1);
+          mma_commit(&bars[SB_DS]);
+          // delta of chunk j is in TMEM and the accumulator of U^T + S(-W~^T) is free
+          mbar_arrive(&bars[SB_DR + b]);
+        }
       }
       // the state update is done, S Q^T of chunk j has read S, chunk j + 1 is loaded
       const bool last = (j + 1 == u.nc);
@@ -948,6 +1050,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
                last ? nullptr : &bars[SB_QK_FULL + (j + 1) % ST_NST], ((j + 1) / ST_NST) & 1);
       tc_fence_after();
       if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // the chain's last read of stage s
+      if (LINEAR && tid == 0 && !last) mbar_arrive(&bars[SB_DR + (b ^ 1)]);  // delta (j + 1) made
       const float gam = last ? 1.f : der_all[((j + 1) % ST_NST) * ST_DER_STAGE + 64 + 63];
       // ---- new state: bf16 copy for the next chunk, pre-scaled fp32 back to TMEM ----
 #pragma unroll 1
@@ -1121,19 +1224,10 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
 #undef AO_WAIT
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ log_alpha,
-              const float* __restrict__ beta, const float* __restrict__ S0,
-              __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
-              const int32_t* __restrict__ cu_seqlens, int H, int T) {
-  extern __shared__ uint8_t smem_raw[];
-  // Align to 1024 bytes by pointer arithmetic on the shared array itself (accesses
-  // stay shared-memory accesses); the offset is the same in both CTAs.
-  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const uint32_t rank = cluster_ctarank();
-  const int unit = blockIdx.x >> 1;
+// (sequence, head) unit `unit` = n * H + h: its rows (cu_seqlens clamped to [0, T]),
+// chunk count and state offset.
+__device__ __forceinline__ Unit make_unit(int unit, const int32_t* __restrict__ cu_seqlens, int H,
+                                          int T) {
   Unit u;
   u.h = unit % H;
   const int n = unit / H;
@@ -1149,6 +1243,22 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   }
   u.nc = (int)((u.len + kC - 1) / kC);
   u.sidx = ((size_t)n * H + u.h) * kD * kD;
+  return u;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ log_alpha,
+              const float* __restrict__ beta, const float* __restrict__ S0,
+              __nv_bfloat16* __restrict__ out, float* __restrict__ S_final,
+              const int32_t* __restrict__ cu_seqlens, int H, int T) {
+  extern __shared__ uint8_t smem_raw[];
+  // Align to 1024 bytes by pointer arithmetic on the shared array itself (accesses
+  // stay shared-memory accesses); the offset is the same in both CTAs.
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const Unit u = make_unit(blockIdx.x >> 1, cu_seqlens, H, T);
 
   uint8_t* misc = sm + (rank == 0 ? WY_MISC : ST_MISC);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(misc);
@@ -1188,7 +1298,8 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (rank == 0)
     run_wy(sm, tmem, &tm_k, log_alpha, beta, u, H, abort_flag);
   else
-    run_state(sm, tmem, &tm_q, &tm_k, &tm_v, log_alpha, beta, S0, out, S_final, u, H, abort_flag);
+    run_state<false>(sm, tmem, &tm_q, &tm_k, &tm_v, log_alpha, beta, S0, out, S_final, u, H,
+                     abort_flag);
 
   tc_fence_before();
   __syncthreads();
@@ -1205,6 +1316,50 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     tmem_dealloc(tmem, TM_COLS);
   }
   cluster_sync();  // neither CTA leaves while the other may still touch its memory
+}
+
+// Linear mode (no erase, write strength 1): the WY factors are T = I, W~ = 0, U = V, so
+// the state CTA runs alone, one CTA per (sequence, head): its chain is the state update
+// and the S epilogue, with delta and delta~ made from the V tile by aux P.
+__global__ void __launch_bounds__(kThreads, 1)
+gdn_tc_linear_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ log_alpha,
+                     const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
+                     float* __restrict__ S_final, const int32_t* __restrict__ cu_seqlens, int H,
+                     int T) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const Unit u = make_unit(blockIdx.x, cu_seqlens, H, T);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + ST_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + ST_MISC + 4);
+  if (warp == 0) tmem_alloc(tslot, TM_COLS);
+  if (tid == 32) {
+    *abort_flag = 0;
+    uint64_t* b = reinterpret_cast<uint64_t*>(sm + ST_BAR);
+    for (int s = 0; s < ST_NST; ++s) {
+      mbar_init(&b[SB_QK_FULL + s], 2);
+      mbar_init(&b[SB_QK_EMPTY + s], 2);  // the chain (after its state update) and aux P
+    }
+    for (int k = SB_HF; k < SB_COUNT; ++k) mbar_init(&b[k], 1);
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    fence_mbarrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  run_state<true>(sm, tmem, &tm_q, &tm_k, &tm_v, log_alpha, nullptr, S0, out, S_final, u, H,
+                  abort_flag);
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) atomicOr(&g_tc_status, *abort_flag);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
@@ -1250,6 +1405,16 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
   if (!make_map(&mq, a.q, rows, a.H) || !make_map(&mk, a.k, rows, a.H) ||
       !make_map(&mv, a.v, rows, a.H))
     return cudaErrorInvalidValue;
+  if (a.beta == nullptr) {  // linear mode: the state CTA alone, one per unit
+    const long long units = (long long)a.N * a.H;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    static std::atomic<unsigned long long> smem_lin{0};
+    const cudaError_t e = ensure_smem_cap(gdn_tc_linear_kernel, SMEM_BYTES, smem_lin);
+    if (e != cudaSuccess) return e;
+    gdn_tc_linear_kernel<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(
+        mq, mk, mv, a.log_alpha, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.cu_seqlens, a.H, a.T);
+    return cudaGetLastError();
+  }
   const long long blocks = 2LL * a.N * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   static std::atomic<unsigned long long> smem_set{0};
