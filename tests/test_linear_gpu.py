@@ -137,3 +137,18 @@ def test_linear_empty_sequence_returns_S0():
     assert o.size == 0
     ref = np.zeros_like(s) if inp["S0"] is None else inp["S0"].numpy()
     assert np.array_equal(s, ref)
+
+
+@pytest.mark.parametrize("alpha_one", [False, True], ids=["mamba2", "linear_attention"])
+def test_linear_bf16_packed_empty_and_short_sequences(alpha_one):
+    """The tensor-core linear kernel on a packed batch with empty, one-token, one-chunk,
+    one-chunk-plus-one and ragged sequences, each from its own S0: the chunk loop's
+    first chunk, partial last chunks and sequences with no chunk at all."""
+    base = W["gdn_bf16_b4h16t4096d128c64"]
+    lens = [0, 1, 64, 65, 3, 0, 130, 17, 200]
+    inp = workloads.make_inputs(base, B=1, H=2, T=sum(lens), seed=6)
+    inp["cu_seqlens"] = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    inp["N"] = len(lens)
+    g = torch.Generator().manual_seed(7)
+    inp["S0"] = torch.randn(len(lens), 2, base.dv, base.dk, generator=g) * 0.1
+    _full(inp, 64, alpha_one)
