@@ -179,7 +179,10 @@ size_t gdn_chunk_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, i
  * which is gdn_chunk_fwd's recurrence with the erase strength set to 0 and the
  * write strength to 1.  Arguments, layouts, ownership, paths and errors are those of
  * gdn_chunk_fwd, without beta; log_alpha may be NULL, meaning alpha_t = 1 (plain
- * linear attention).
+ * linear attention).  On the tensor-core path (GDN_PATH_TCGEN05) this mode has a kernel
+ * of its own: with no erase the pseudo-values are V itself, so one CTA per (sequence,
+ * head) runs without the WY factors; the results equal gdn_chunk_fwd's pipeline run with
+ * these factors, bit for bit.
  */
 int gdn_linear_chunk_fwd(const void* q, const void* k, const void* v,
                          const float* log_alpha, const float* S0,
