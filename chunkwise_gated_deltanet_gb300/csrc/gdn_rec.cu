@@ -12,20 +12,31 @@
 // one CTA owns RB rows of one (sequence, head) and walks the sequence; each thread holds
 // 4 columns of 2 rows in registers, a row's dot products are warp-shuffle sums over the
 // dk / 4 lanes that hold it, and no CTA needs another's results.  Token inputs are
-// staged in shared memory by cp.async, one block of kRecSub tokens ahead.
+// staged in shared memory by cp.async, one block of kRecSub tokens ahead.  CTAs have 8
+// warps; when that leaves most SMs idle (few (sequence, head) pairs), CTAs of 8 rows
+// (16 at dk = 16) spread the same rows over more SMs, so that each per-token chain runs
+// with its scheduler nearly to itself.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "gdn_internal.h"
 
 namespace gdn {
 namespace {
 
-constexpr int kRecThreads = 256;  // 8 warps
-constexpr int kRecSub = 16;       // tokens per staged block
+constexpr int kRecSub = 16;  // tokens per staged block
 
+// rows one warp access covers, and the warps of the small-CTA shape (8 rows per CTA,
+// 16 at dk = 16): at least 16 bytes of each staged v row for either input type
 template <int DK>
-__host__ __device__ constexpr int rec_rows() { return 16 * (32 / (DK / 4)); }
+__host__ __device__ constexpr int rec_rpw() { return 32 / (DK / 4); }
+template <int DK>
+__host__ __device__ constexpr int rec_small_warps() { return rec_rpw<DK>() >= 4 ? 1 : 4 / rec_rpw<DK>(); }
+// rows per CTA of NW warps: each warp holds 2 accesses
+template <int DK, int NW>
+__host__ __device__ constexpr int rec_rows() { return 2 * NW * rec_rpw<DK>(); }
 
 template <typename T>
 __device__ __forceinline__ float rec_f(T x);
@@ -85,9 +96,9 @@ __device__ __forceinline__ float4 rec_update(float a, float4 s, float u, float4 
 }
 
 // one staging buffer: k, q [kRecSub][DK], v [kRecSub][RB] (TIn), log alpha, beta [kRecSub]
-template <int DK, typename TIn>
+template <int DK, typename TIn, int NW>
 struct RecSmem {
-  static constexpr int RB = rec_rows<DK>();
+  static constexpr int RB = rec_rows<DK, NW>();
   static constexpr size_t kOff = 0;
   static constexpr size_t qOff = kOff + (size_t)kRecSub * DK * sizeof(TIn);
   static constexpr size_t vOff = qOff + (size_t)kRecSub * DK * sizeof(TIn);
@@ -97,13 +108,14 @@ struct RecSmem {
   static constexpr size_t bytes = 2 * stage;
 };
 
-template <int DK, typename TIn>
-__global__ void __launch_bounds__(kRecThreads)
+template <int DK, typename TIn, int NW>
+__global__ void __launch_bounds__(32 * NW)
 gdn_rec_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
                const float* __restrict__ log_alpha, const float* __restrict__ beta,
                const float* __restrict__ S0, TIn* __restrict__ out, float* __restrict__ S_final,
                const int32_t* __restrict__ cu_seqlens, int H, int T, int dv) {
-  using SM = RecSmem<DK, TIn>;
+  using SM = RecSmem<DK, TIn, NW>;
+  constexpr int kRecThreads = 32 * NW;
   constexpr int LPR = DK / 4;    // lanes per row, 4 columns each
   constexpr int RPW = 32 / LPR;  // rows per warp access
   constexpr int RB = SM::RB;
@@ -113,10 +125,10 @@ gdn_rec_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* 
   const int rb0 = rb * RB;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c4 = lane % LPR, rsub = lane / LPR;
-  const int rl0 = warp * RPW + rsub, rl1 = rl0 + 8 * RPW;  // this thread's rows in the block
+  const int rl0 = warp * RPW + rsub, rl1 = rl0 + NW * RPW;  // this thread's rows in the block
   const int r0 = rb0 + rl0, r1 = rb0 + rl1;
   const bool ok0 = r0 < dv, ok1 = r1 < dv;
-  const int nrows = min(RB, dv - rb0);  // a multiple of 16
+  const int nrows = min(RB, dv - rb0);  // a multiple of 8
   const bool linear = beta == nullptr;  // erase 0, write 1
 
   long long row0, len;
@@ -211,17 +223,38 @@ gdn_rec_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* 
   }
 }
 
-template <int DK, typename TIn>
-cudaError_t launch_rec_t(const FwdArgs& a, cudaStream_t stream) {
-  using SM = RecSmem<DK, TIn>;
-  const long long units = (long long)a.N * a.H;
-  if (units == 0) return cudaSuccess;
-  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+template <int DK, typename TIn, int NW>
+cudaError_t launch_rec_nw(const FwdArgs& a, long long units, cudaStream_t stream) {
+  using SM = RecSmem<DK, TIn, NW>;
   const int nrb = (a.dv + SM::RB - 1) / SM::RB;
-  gdn_rec_kernel<DK, TIn><<<dim3((unsigned)units, nrb), kRecThreads, SM::bytes, stream>>>(
+  gdn_rec_kernel<DK, TIn, NW><<<dim3((unsigned)units, nrb), 32 * NW, SM::bytes, stream>>>(
       (const TIn*)a.q, (const TIn*)a.k, (const TIn*)a.v, a.log_alpha, a.beta, a.S0, (TIn*)a.out,
       a.S_final, a.cu_seqlens, a.H, a.T, a.dv);
   return cudaGetLastError();
+}
+
+int rec_sm_count() {
+  static std::atomic<int> sms{0};
+  int n = sms.load();
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    sms.store(n);
+  }
+  return n;
+}
+
+template <int DK, typename TIn>
+cudaError_t launch_rec_t(const FwdArgs& a, cudaStream_t stream) {
+  const long long units = (long long)a.N * a.H;
+  if (units == 0) return cudaSuccess;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // 8-warp CTAs unless they would leave more than half of the SMs idle
+  const long long big = units * ((a.dv + rec_rows<DK, 8>() - 1) / rec_rows<DK, 8>());
+  if (2 * big >= rec_sm_count()) return launch_rec_nw<DK, TIn, 8>(a, units, stream);
+  return launch_rec_nw<DK, TIn, rec_small_warps<DK>()>(a, units, stream);
 }
 
 }  // namespace
