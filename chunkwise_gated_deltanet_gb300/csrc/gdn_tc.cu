@@ -861,9 +861,10 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             mbar_test(&bars[SB_HF + (i & 1)], (i >> 1) & 1, true))
           kind = 0;
       }
-      if (kind < 0 && nd < nu) {
+      if (kind < 0 && nd < nu && (nu > nd + 1 || nu == u.nc)) {
         // delta of chunk j in TMEM, P(j) published, and S Q^T (j), which starts the
-        // output accumulator, completed (it comes from another thread)
+        // output accumulator, completed (it comes from another thread); U^T (j + 1) goes
+        // into the tensor pipe first
         const int j = nd;
         if (mbar_test(&bars[SB_DR + (j & 1)], (j >> 1) & 1, false) &&
             mbar_test(&bars[SB_PF + (j & 1)], (j >> 1) & 1, false) &&
