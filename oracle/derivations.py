@@ -6,7 +6,7 @@ read against the page's equations; ``chunked_wy_delta`` alone uses token rows,
 the layout of the library.  Library routines used as single steps: matrix
 products and ``np.linalg.solve`` (a triangular system solved densely).
 
-Readings taken where the page is garbled (each also listed in the design doc):
+Readings taken where the page is garbled:
 * the WY matrix form writes "U_i" where the strict upper mask M^u_i is meant and
   loses a parenthesis; read W = (K - W (M^u o K^T K)) D_beta;
 * "Gamma o K^T K" in the U matrix form is strictly upper (the page says so in
