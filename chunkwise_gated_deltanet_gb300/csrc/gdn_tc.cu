@@ -357,6 +357,11 @@ struct Unit {
 struct GateLoad {
   float la0, la1, b0, b1;
 };
+// A gate of alpha = 0 (log alpha = -inf, the whole state forgotten) enters as log alpha =
+// -80: alpha = e^-80 ~ 1.8e-35 leaves nothing measurable of the earlier state, and the
+// in-chunk gate sums and their differences stay finite (-inf - -inf would be NaN) and
+// accurate (|sum| <= 80 * 64).
+constexpr float kMinLogAlpha = -80.f;
 __device__ __forceinline__ GateLoad load_gates(const float* __restrict__ log_alpha,
                                                const float* __restrict__ beta, const Unit& u, int H,
                                                int chunk, int lane) {
@@ -375,10 +380,10 @@ __device__ __forceinline__ GateLoad load_gates(const float* __restrict__ log_alp
   return g;
 }
 // In-chunk cumulative gate sums in log2 units (g0 for token lane, g1 for token
-// lane + 32) and their total.
+// lane + 32) and their total, each log alpha taken at least kMinLogAlpha.
 __device__ __forceinline__ void scan_gates(const GateLoad& in, int lane, float& g0, float& g1,
                                            float& tot) {
-  float x0 = in.la0, x1 = in.la1;
+  float x0 = fmaxf(in.la0, kMinLogAlpha), x1 = fmaxf(in.la1, kMinLogAlpha);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
