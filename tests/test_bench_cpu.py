@@ -54,3 +54,24 @@ def test_recorded_traffic_is_dropped_once_the_kernel_changes(tmp_path, monkeypat
     src.write_bytes(src.read_bytes() + b"\n// changed\n")
     assert bench.measured_traffic(name) is None
     assert bench.measured_traffic("no_such_workload") is None
+
+
+def test_reference_arm_under_torchrun_two_gloo_ranks():
+    """The launch the driver uses for N > 1 (torchrun, one process per rank), on CPU with
+    gloo: rank 0 alone runs the oracle and prints the one line, rank 1 exits 0 without
+    work, and the process group comes up and goes down cleanly."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "0", "--workload", "deltanet_f32_b1h1t64d16c16"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT,
+                       env=dict(os.environ, OMP_NUM_THREADS="2", CUDA_VISIBLE_DEVICES=""))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert KEYS <= set(d) and d["impl"] == "reference" and d["n_gpus"] == 2
