@@ -477,7 +477,7 @@ def bwd_algorithmic(inp: dict) -> dict:
 
 
 def run_bwd(args, w, world, rank, local):
-    """One step = one gdn_chunk_bwd over the workload (its two launches)."""
+    """One step = one gdn_chunk_bwd over the workload, on the path --bwd-path names."""
     if args.impl == "reference":
         if rank != 0:
             return
@@ -516,10 +516,15 @@ def run_bwd(args, w, world, rank, local):
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    path = {"auto": gdn.GDN_BWD_AUTO, "tokens": gdn.GDN_BWD_TOKENS,
+            "chunked": gdn.GDN_BWD_CHUNKED}[args.bwd_path]
+    taken = gdn.gdn_bwd_select_path(dk, dv, inp["q"].dtype) if path == gdn.GDN_BWD_AUTO else path
+    launches = 29 if taken == gdn.GDN_BWD_CHUNKED and B * T > 0 else 2
 
     def step():
         gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],
-                          gd["d_out"], gd["dS_final"], *outs, ws, d["cu_seqlens"], stream=stream)
+                          gd["d_out"], gd["dS_final"], *outs, ws, d["cu_seqlens"], stream=stream,
+                          path=path)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -592,6 +597,7 @@ def run_bwd(args, w, world, rank, local):
             "data": "synthetic",
             "config": {"workload": w.name, "pass": "backward", "B": B, "H": H, "T": T,
                        "dk": dk, "dv": dv, "qkv_dtype": w.dtype, "workspace_bytes": nbytes,
+                       "path": "chunked" if taken == gdn.GDN_BWD_CHUNKED else "tokens",
                        "l2": "flushed between timed steps (512 MiB write)",
                        "parallelism": f"replicas{world}"},
             "roofline": {"bound": "alu", "achieved": achieved_tf, "peak": alu_peak,
@@ -603,7 +609,7 @@ def run_bwd(args, w, world, rank, local):
             "clocks": clk.summary(),
             "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": launches * args.steps,
             "cpu_baseline": cpu,
             "wall_s_timed_region": t_wall}), flush=True)
 
@@ -659,6 +665,8 @@ def main():
                          "(for small profiling captures; the default is the workload's)")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward (gdn_chunk_bwd) of the workload instead")
+    ap.add_argument("--bwd-path", choices=("auto", "tokens", "chunked"), default="auto",
+                    help="backward kernel family (auto: the library's choice for the sizes)")
     ap.add_argument("--seqpar", type=int, default=0,
                     help="time the sequence-parallel split over this many ranks on one GPU")
     args = ap.parse_args()

@@ -156,7 +156,15 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* lo
 
 size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int N_seqs) {
   if (B <= 0 || H <= 0 || T <= 0 || N_seqs <= 0 || !head_ok(dk) || !head_ok(dv)) return 0;
-  return gdn::bwd_workspace_bytes((long long)B * T, H, dk, dv, N_seqs);
+  const size_t a = gdn::bwd_workspace_bytes((long long)B * T, H, dk, dv, N_seqs);
+  const size_t b = gdn::bwd_chunked_workspace_bytes((long long)B * T, H, dk, dv, N_seqs);
+  return a > b ? a : b;
+}
+
+int gdn_bwd_select_path(int dk, int dv, int qkv_dtype) {
+  if (!head_ok(dk) || !head_ok(dv)) return 0;
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16) return 0;
+  return gdn::bwd_chunked_supported(dk, dv) ? GDN_BWD_CHUNKED : GDN_BWD_TOKENS;
 }
 
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* log_alpha,
@@ -165,7 +173,24 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
                   float* d_S0, void* workspace, size_t workspace_bytes, int B, int H, int T,
                   int dk, int dv, const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
                   void* stream) {
+  return gdn_chunk_bwd_ex(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v,
+                          d_log_alpha, d_beta, d_S0, workspace, workspace_bytes, B, H, T, dk,
+                          dv, cu_seqlens, N_seqs, qkv_dtype, GDN_BWD_AUTO, stream);
+}
+
+int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v, const float* log_alpha,
+                     const float* beta, const float* S0, const void* d_out,
+                     const float* dS_final, void* d_q, void* d_k, void* d_v,
+                     float* d_log_alpha, float* d_beta, float* d_S0, void* workspace,
+                     size_t workspace_bytes, int B, int H, int T, int dk, int dv,
+                     const int32_t* cu_seqlens, int N_seqs, int qkv_dtype, int bwd_path,
+                     void* stream) {
   const char* fn = "gdn_chunk_bwd";
+  if (bwd_path != GDN_BWD_AUTO && bwd_path != GDN_BWD_TOKENS && bwd_path != GDN_BWD_CHUNKED)
+    return fail(GDN_EINVAL, "%s: unknown backward path %d", fn, bwd_path);
+  if (bwd_path == GDN_BWD_CHUNKED && !gdn::bwd_chunked_supported(dk, dv))
+    return fail(GDN_EINVAL, "%s: the chunked path needs dk = dv = 64 or 128 (got %d, %d)", fn,
+                dk, dv);
   if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
     return fail(GDN_EDTYPE, "%s: qkv_dtype %d is neither GDN_F32 nor GDN_BF16", fn, qkv_dtype);
   if (T > 0 && (!q || !k || !v || !log_alpha || !beta || !d_out || !d_q || !d_k || !d_v ||
@@ -194,7 +219,10 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
   const long long rows = (long long)B * T;
   if (rows * H * (dk > dv ? dk : dv) > (1LL << 40))
     return fail(GDN_EINVAL, "%s: problem too large", fn);
-  const size_t need = gdn::bwd_workspace_bytes(rows, H, dk, dv, N);
+  if (bwd_path == GDN_BWD_AUTO) bwd_path = gdn_bwd_select_path(dk, dv, qkv_dtype);
+  const bool chunked = bwd_path == GDN_BWD_CHUNKED && rows > 0;
+  const size_t need = chunked ? gdn::bwd_chunked_workspace_bytes(rows, H, dk, dv, N)
+                              : gdn::bwd_workspace_bytes(rows, H, dk, dv, N);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(GDN_EINVAL, "%s: workspace of %zu bytes needed (got %zu%s)", fn, need,
                 workspace_bytes, workspace ? "" : ", NULL");
@@ -204,7 +232,8 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
   a.dq = d_q; a.dk_out = d_k; a.dv_out = d_v; a.dlog_alpha = d_log_alpha; a.dbeta = d_beta;
   a.dS0 = d_S0; a.workspace = workspace; a.cu_seqlens = cu_seqlens;
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.N = N; a.bf16 = qkv_dtype == GDN_BF16;
-  const cudaError_t e = gdn::launch_bwd(a, (cudaStream_t)stream);
+  const cudaError_t e = chunked ? gdn::launch_bwd_chunked(a, (cudaStream_t)stream)
+                                : gdn::launch_bwd(a, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return fail(GDN_ELAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
   return GDN_OK;

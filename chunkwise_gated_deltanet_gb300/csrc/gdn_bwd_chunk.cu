@@ -1,0 +1,863 @@
+// Chunked backward of the Gated DeltaNet recurrence (gradients of q, k, v, log alpha,
+// beta and S0), the reverse-mode derivative of the chunk form (Nyysyyan,
+// "Gated-DeltaNet", the WY representation and the chunkwise algorithm).  The pages derive
+// no backward; this follows the derivative written per chunk as matrix products.  In a
+// chunk of C tokens with chunk-start state S, gradient dS' of the chunk-end state,
+// g the in-chunk cumulative log gate, D_ij = e^{g_i - g_j} (j <= i), E = e^{g_last - g},
+// A = strictly-lower(beta_i K K^T o D), T = (I + A)^{-1}, W~ = T diag(beta e^g) K,
+// U = T diag(beta) V, delta = U - W~ S^T, P = lower(Q K^T o D):
+//
+//   d delta = P^T dO + E K dS'^T
+//   dS      = dO^T diag(e^g) Q + e^{g_last} dS' - d delta^T W~     (handed to chunk j-1)
+//   dP      = lower(dO delta^T)
+//   dQ      = e^g o (dO S) + (dP o D) K
+//   dW      = -d delta S,  dT = d delta (beta o V)^T + dW (beta e^g o K)^T
+//   dA      = strictly-lower(-T^T dT T^T),  X = dA o D o beta_i
+//   dK      = (dP o D)^T Q + E o (delta dS') + beta e^g o T^T dW + X K + X^T K
+//   dV      = beta o T^T d delta
+//   dbeta   = (T^T d delta . v) + e^g (T^T dW . k) + rowsum(dA o KK^T o D)
+//   dg      = rowsum(dD o D) - colsum(dD o D) + e^g (beta (T^T dW . k) + dO S . q)
+//             - E (delta dS' . k), plus sum(E (delta dS' . k)) + e^{g_last} <dS', S>
+//             at the last token;  dD = dA beta_i K K^T + dP o Q K^T
+//   d log alpha = the reverse cumulative sum of dg inside the chunk.
+//
+// Layout of the work.  Every (chunk, head) pair is one batch entry b of padded fp32
+// buffers in the workspace (a ragged last chunk is zero-filled with beta = 0 and
+// log alpha = 0, which adds nothing to any sum).  The two serial parts, the chunk-start
+// states S_j (forward) and the chunk-end state gradients dS'_j (reverse), run in one
+// chain kernel that splits the dv rows of the state over CTAs: rows are independent
+// given the chunk's operands.  Everything else is chunk-parallel: a batched fp32 GEMM
+// (64 x 64 output tiles, one per CTA and batch entry) and small per-chunk kernels for
+// the triangular solve, the gate terms and the final per-token sums.
+//
+// fp32 arithmetic throughout (CUDA cores).  Head sizes dk = dv = 64 or 128.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kCk = 64;             // chunk length
+constexpr int kRows = 32;           // state rows per chain CTA
+constexpr float kLogAlphaMin = -80.f;  // alpha = 0 (log alpha = -inf) is taken as e^-80
+
+// Per-batch-entry gate vectors, each kCk long.
+enum { G_BETA = 0, G_G = 1, G_EG = 2, G_E = 3, G_BEG = 4, kGates = 5 };
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T>
+__device__ __forceinline__ T from_f(float x);
+template <>
+__device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// ---------------------------------------------------------------------------------
+// Chunk table: for every chunk its first token row and length, for every sequence
+// the index of its first chunk, and the count of live batch entries (chunks x H).
+// One CTA; sequences in tiles of 1024 with a block scan.  Entries past nc_max (only
+// reachable with offsets that overrun the token count) are dropped.
+__global__ void __launch_bounds__(1024)
+ck_table_kernel(const int32_t* __restrict__ cu, int N, int T, int H, long long nc_max,
+                long long* __restrict__ crow0, int* __restrict__ clen, int* __restrict__ cbase,
+                long long* __restrict__ nlive) {
+  __shared__ int wsum[32];
+  __shared__ long long carry;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int n0 = 0; n0 < N; n0 += 1024) {
+    const int n = n0 + threadIdx.x;
+    long long start = 0;
+    int len = 0;
+    if (n < N) {
+      if (cu) {
+        start = cu[n];
+        len = cu[n + 1] - cu[n];
+      } else {
+        start = (long long)n * T;
+        len = T;
+      }
+    }
+    const int nc = len > 0 ? (len + kCk - 1) / kCk : 0;
+    int x = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int s = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += y;
+      }
+      wsum[lane] = s;
+    }
+    __syncthreads();
+    const long long incl = carry + x + (w > 0 ? wsum[w - 1] : 0);
+    const long long base = incl - nc;
+    if (n < N) {
+      cbase[n] = (int)(base < nc_max ? base : nc_max);
+      for (int j = 0; j < nc && base + j < nc_max; ++j) {
+        crow0[base + j] = start + (long long)j * kCk;
+        clen[base + j] = min(kCk, len - j * kCk);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const long long total = carry < nc_max ? carry : nc_max;
+    cbase[N] = (int)total;
+    nlive[0] = total * H;
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Gather one (chunk, head): q, k, v, dO as padded fp32 [kCk][D] tiles, and the gate
+// vectors: beta, g (in-chunk inclusive cumulative log alpha), e^g, E = e^{g_last - g},
+// beta e^g, and Gamma = e^{g_last}.
+struct GatherArgs {
+  const void *q, *k, *v, *dout;
+  const float *log_alpha, *beta;
+  const long long* crow0;
+  const int* clen;
+  const long long* nlive;
+  float *Qc, *Kc, *Vc, *dOc, *gates, *gam;
+  int H;
+};
+
+template <int D, typename TIn>
+__global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
+  const long long b = blockIdx.x;
+  if (b >= *p.nlive) return;
+  const long long cid = b / p.H;
+  const int h = (int)(b - cid * p.H);
+  const long long row0 = p.crow0[cid];
+  const int len = p.clen[cid];
+  const TIn* q = reinterpret_cast<const TIn*>(p.q);
+  const TIn* k = reinterpret_cast<const TIn*>(p.k);
+  const TIn* v = reinterpret_cast<const TIn*>(p.v);
+  const TIn* dO = reinterpret_cast<const TIn*>(p.dout);
+  const size_t ob = (size_t)b * kCk * D;
+  for (int i = threadIdx.x; i < kCk * D; i += 256) {
+    const int c = i / D, x = i % D;
+    float qv = 0.f, kv = 0.f, vv = 0.f, ov = 0.f;
+    if (c < len) {
+      const size_t o = ((size_t)(row0 + c) * p.H + h) * D + x;
+      qv = to_f(q[o]);
+      kv = to_f(k[o]);
+      vv = to_f(v[o]);
+      ov = to_f(dO[o]);
+    }
+    p.Qc[ob + i] = qv;
+    p.Kc[ob + i] = kv;
+    p.Vc[ob + i] = vv;
+    p.dOc[ob + i] = ov;
+  }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x, c0 = 2 * lane, c1 = c0 + 1;
+    float la0 = 0.f, la1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if (c0 < len) {
+      la0 = fmaxf(p.log_alpha[(size_t)(row0 + c0) * p.H + h], kLogAlphaMin);
+      b0 = p.beta[(size_t)(row0 + c0) * p.H + h];
+    }
+    if (c1 < len) {
+      la1 = fmaxf(p.log_alpha[(size_t)(row0 + c1) * p.H + h], kLogAlphaMin);
+      b1 = p.beta[(size_t)(row0 + c1) * p.H + h];
+    }
+    float s = la0 + la1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    const float g1 = s, g0 = s - la1;
+    const float glast = __shfl_sync(0xffffffffu, s, 31);
+    float* G = p.gates + (size_t)b * kGates * kCk;
+    const float e0 = expf(g0), e1 = expf(g1);
+    G[G_BETA * kCk + c0] = b0;
+    G[G_BETA * kCk + c1] = b1;
+    G[G_G * kCk + c0] = g0;
+    G[G_G * kCk + c1] = g1;
+    G[G_EG * kCk + c0] = e0;
+    G[G_EG * kCk + c1] = e1;
+    G[G_E * kCk + c0] = expf(glast - g0);
+    G[G_E * kCk + c1] = expf(glast - g1);
+    G[G_BEG * kCk + c0] = b0 * e0;
+    G[G_BEG * kCk + c1] = b1 * e1;
+    if (lane == 0) p.gam[b] = expf(glast);
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Batched fp32 GEMM: for every live batch entry b,
+//   C(m, n) = alpha * sum_k A(m, k) * ks[k] * B(k, n) * cs[n] * Dg(m, n)  (+ C(m, n))
+// A(m, k) = A[b*ab + m*am + k*ak] (likewise B and C), so either operand may be read
+// transposed.  ks, cs: optional per-entry vectors (stride vb); gv: optional g vector,
+// Dg(m, n) = e^{g_m - g_n} for n <= m and 0 above; mask 1 keeps n <= m, mask 2 n < m.
+// One CTA per 64 x 64 output tile and entry; M, N multiples of 64, K of 32.
+struct Mm {
+  const float* A;
+  long long ab;
+  int am, ak;
+  const float* B;
+  long long bb;
+  int bk, bn;
+  float* C;
+  long long cb;
+  int cm, cn;
+  const float *ks, *cs, *gv;
+  long long vb;
+  float alpha;
+  int accum, mask, M, N, K;
+  const long long* nlive;
+};
+
+__global__ void __launch_bounds__(256, 3) ck_mm_kernel(Mm p) {
+  const long long b = blockIdx.x;
+  if (b >= *p.nlive) return;
+  __shared__ float As[32][65], Bs[32][65];
+  const int tilesN = p.N / 64;
+  const int m0 = (blockIdx.y / tilesN) * 64, n0 = (blockIdx.y % tilesN) * 64;
+  const float* A = p.A + b * p.ab;
+  const float* B = p.B + b * p.bb;
+  const float* ks = p.ks ? p.ks + b * p.vb : nullptr;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < p.K; k0 += 32) {
+#pragma unroll 4
+    for (int r = 0; r < 8; ++r) {
+      const int idx = tid + 256 * r;
+      int mm, ka;
+      if (p.ak == 1) {
+        ka = idx & 31;
+        mm = idx >> 5;
+      } else {
+        mm = idx & 63;
+        ka = idx >> 6;
+      }
+      As[ka][mm] = A[(long long)(m0 + mm) * p.am + (long long)(k0 + ka) * p.ak];
+      int nn, kb;
+      if (p.bn == 1) {
+        nn = idx & 63;
+        kb = idx >> 6;
+      } else {
+        kb = idx & 31;
+        nn = idx >> 5;
+      }
+      float x = B[(long long)(k0 + kb) * p.bk + (long long)(n0 + nn) * p.bn];
+      if (ks) x *= ks[k0 + kb];
+      Bs[kb][nn] = x;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  const float* cs = p.cs ? p.cs + b * p.vb : nullptr;
+  const float* gv = p.gv ? p.gv + b * p.vb : nullptr;
+  float* C = p.C + b * p.cb;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 16 * i;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx + 16 * j;
+      float x = p.alpha * acc[i][j];
+      if (cs) x *= cs[n];
+      if (gv) x = n <= m ? x * expf(gv[m] - gv[n]) : 0.f;
+      if ((p.mask == 1 && n > m) || (p.mask == 2 && n >= m)) x = 0.f;
+      float* o = C + (long long)m * p.cm + (long long)n * p.cn;
+      *o = p.accum ? *o + x : x;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Per (chunk, head): A = strictly-lower(beta_i KK^T_ij D_ij), T = (I + A)^{-1} by
+// forward substitution (T_i = e_i - sum_{j<i} A_ij T_j), and P = lower(QK^T o D).
+// Thread c < 64 owns column c of T.
+struct TsolveArgs {
+  const float *KK, *QK, *gates;
+  float *T, *P;
+  const long long* nlive;
+};
+
+__global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
+  const long long b = blockIdx.x;
+  if (b >= *p.nlive) return;
+  __shared__ float As[kCk][kCk + 1], Ts[kCk][kCk + 1], g[kCk], be[kCk];
+  const int tid = threadIdx.x;
+  const float* G = p.gates + (size_t)b * kGates * kCk;
+  if (tid < kCk) {
+    g[tid] = G[G_G * kCk + tid];
+    be[tid] = G[G_BETA * kCk + tid];
+  }
+  __syncthreads();
+  const size_t ob = (size_t)b * kCk * kCk;
+  for (int idx = tid; idx < kCk * kCk; idx += 128) {
+    const int i = idx >> 6, j = idx & 63;
+    const float Dij = j <= i ? expf(g[i] - g[j]) : 0.f;
+    As[i][j] = j < i ? be[i] * p.KK[ob + idx] * Dij : 0.f;
+    p.P[ob + idx] = p.QK[ob + idx] * Dij;
+  }
+  __syncthreads();
+  if (tid < kCk) {
+    const int c = tid;
+    for (int i = 0; i < c; ++i) Ts[i][c] = 0.f;
+    Ts[c][c] = 1.f;
+    for (int i = c + 1; i < kCk; ++i) {
+      float s0 = 0.f, s1 = 0.f;
+      int j = c;
+      for (; j + 1 < i; j += 2) {
+        s0 = fmaf(As[i][j], Ts[j][c], s0);
+        s1 = fmaf(As[i][j + 1], Ts[j + 1][c], s1);
+      }
+      if (j < i) s0 = fmaf(As[i][j], Ts[j][c], s0);
+      Ts[i][c] = -(s0 + s1);
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < kCk * kCk; idx += 128) p.T[ob + idx] = Ts[idx >> 6][idx & 63];
+}
+
+// ---------------------------------------------------------------------------------
+// The state chain of one (sequence, head) over kRows rows of the state, chunk by chunk
+// (forward, or in reverse for the gradient).  Per chunk, with the rows St (kRows x D):
+//   X1(c, r) = Add1(c, r) + s1_c * sum_k A1(c, k) St(r, k)       -> out1
+//   St(r, k) = Add2(r, k) + Gamma St(r, k) + sum_c s2_c X1(c, r) A2(c, k)
+// forward:  Add1 = U, s1 = -1, A1 = W~, s2 = E, A2 = K, no Add2 (X1 = delta, St = S)
+// reverse:  Add1 = P^T dO, s1 = E, A1 = K, s2 = -1, A2 = W~, Add2 = dO^T diag(e^g) Q
+//           (X1 = d delta, St = dS')
+// St is stored for every chunk before its update; the last update goes to fin.
+struct ChainArgs {
+  const int* cbase;
+  const float* init;  // [N][H][D][D] or null (zeros)
+  float* fin;         // [N][H][D][D] or null
+  float* st;
+  const float *add1, *a1, *a2, *add2;
+  float* out1;
+  const float *gates, *gam;
+  int H;
+};
+
+template <int D>
+constexpr int chain_smem_bytes() {
+  return 4 * (kRows * (D + 1) + 2 * kCk * (D + 1) + kCk * (kRows + 1) + kCk);
+}
+
+template <int D, bool REV>
+__global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
+  extern __shared__ float sm[];
+  constexpr int LD = D + 1, LR = kRows + 1, NJ = D / 32;
+  float* St = sm;
+  float* A1 = St + kRows * LD;
+  float* A2 = A1 + kCk * LD;
+  float* X1 = A2 + kCk * LD;
+  float* Ev = X1 + kCk * LR;
+  const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H, r0 = blockIdx.y * kRows;
+  const int tid = threadIdx.x;
+  const int base = p.cbase[n], nc = p.cbase[n + 1] - base;
+  const size_t sidx = ((size_t)n * p.H + h) * D * D;
+  for (int i = tid; i < kRows * D; i += 256) {
+    const int r = i / D, k = i % D;
+    St[r * LD + k] = p.init ? p.init[sidx + (size_t)(r0 + r) * D + k] : 0.f;
+  }
+  for (int jj = 0; jj < nc; ++jj) {
+    const int j = REV ? nc - 1 - jj : jj;
+    const long long b = (long long)(base + j) * p.H + h;
+    __syncthreads();
+    float* stb = p.st + (size_t)b * D * D;
+    for (int i = tid; i < kRows * D / 4; i += 256) {
+      const int r = i / (D / 4), k = 4 * (i % (D / 4));
+      const float* s = St + r * LD + k;
+      *reinterpret_cast<float4*>(stb + (size_t)(r0 + r) * D + k) = make_float4(s[0], s[1], s[2], s[3]);
+    }
+    const float* a1 = p.a1 + (size_t)b * kCk * D;
+    const float* a2 = p.a2 + (size_t)b * kCk * D;
+    for (int i = tid; i < kCk * D / 4; i += 256) {
+      const int c = i / (D / 4), k = 4 * (i % (D / 4));
+      const float4 x = *reinterpret_cast<const float4*>(a1 + (size_t)c * D + k);
+      const float4 y = *reinterpret_cast<const float4*>(a2 + (size_t)c * D + k);
+      float* d1 = A1 + c * LD + k;
+      float* d2 = A2 + c * LD + k;
+      d1[0] = x.x; d1[1] = x.y; d1[2] = x.z; d1[3] = x.w;
+      d2[0] = y.x; d2[1] = y.y; d2[2] = y.z; d2[3] = y.w;
+    }
+    if (tid < kCk) Ev[tid] = p.gates[(size_t)b * kGates * kCk + G_E * kCk + tid];
+    __syncthreads();
+    const float gam = p.gam[b];
+    {  // X1: kCk x kRows, thread rows c = cy + 32 i, columns r = rx + 8 j
+      const int cy = tid >> 3, rx = tid & 7;
+      float acc[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) acc[i][jq] = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < D; ++k) {
+        const float a0 = A1[cy * LD + k], a1v = A1[(cy + 32) * LD + k];
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) {
+          const float s = St[(rx + 8 * jq) * LD + k];
+          acc[0][jq] = fmaf(a0, s, acc[0][jq]);
+          acc[1][jq] = fmaf(a1v, s, acc[1][jq]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = cy + 32 * i;
+        const float s1 = REV ? Ev[c] : -1.f, s2 = REV ? -1.f : Ev[c];
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) {
+          const int r = rx + 8 * jq;
+          const size_t o = (size_t)b * kCk * D + (size_t)c * D + r0 + r;
+          const float x = p.add1[o] + s1 * acc[i][jq];
+          p.out1[o] = x;
+          X1[c * LR + r] = s2 * x;
+        }
+      }
+    }
+    __syncthreads();
+    {  // St update: kRows x D, thread rows r = ry + 8 i, columns k = kx + 32 j
+      const int ry = tid >> 5, kx = tid & 31;
+      float acc[4][NJ];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int jq = 0; jq < NJ; ++jq) acc[i][jq] = 0.f;
+#pragma unroll 4
+      for (int c = 0; c < kCk; ++c) {
+        float x[4], a[NJ];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = X1[c * LR + ry + 8 * i];
+#pragma unroll
+        for (int jq = 0; jq < NJ; ++jq) a[jq] = A2[c * LD + kx + 32 * jq];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jq = 0; jq < NJ; ++jq) acc[i][jq] = fmaf(x[i], a[jq], acc[i][jq]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = ry + 8 * i;
+#pragma unroll
+        for (int jq = 0; jq < NJ; ++jq) {
+          const int k = kx + 32 * jq;
+          float v = fmaf(gam, St[r * LD + k], acc[i][jq]);
+          if (REV) v += p.add2[(size_t)b * D * D + (size_t)(r0 + r) * D + k];
+          St[r * LD + k] = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (p.fin)
+    for (int i = tid; i < kRows * D; i += 256) {
+      const int r = i / D, k = i % D;
+      p.fin[sidx + (size_t)(r0 + r) * D + k] = St[r * LD + k];
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Per (chunk, head), from dA = strictly-lower(-T^T dT T^T): X = dA o D o beta_i, the
+// row sums of dA o KK^T o D (the triangular solve's part of dbeta) and
+// dg1 = rowsum(dD o D) - colsum(dD o D) with dD = dA beta_i KK^T + dP o QK^T.
+struct DaArgs {
+  const float *dA, *KK, *QK, *dPm, *gates;
+  float *X, *db3, *dg1;
+  const long long* nlive;
+};
+
+__global__ void __launch_bounds__(256) ck_da_kernel(DaArgs p) {
+  const long long b = blockIdx.x;
+  if (b >= *p.nlive) return;
+  __shared__ float E1[kCk][kCk + 1], E2[kCk][kCk + 1], g[kCk], be[kCk];
+  const int tid = threadIdx.x;
+  const float* G = p.gates + (size_t)b * kGates * kCk;
+  if (tid < kCk) {
+    g[tid] = G[G_G * kCk + tid];
+    be[tid] = G[G_BETA * kCk + tid];
+  }
+  __syncthreads();
+  const size_t ob = (size_t)b * kCk * kCk;
+  for (int idx = tid; idx < kCk * kCk; idx += 256) {
+    const int i = idx >> 6, j = idx & 63;
+    const float Dij = j <= i ? expf(g[i] - g[j]) : 0.f;
+    const float da = p.dA[ob + idx], kk = p.KK[ob + idx];
+    p.X[ob + idx] = da * Dij * be[i];
+    E1[i][j] = da * kk * Dij;
+    E2[i][j] = (da * be[i] * kk + p.dPm[ob + idx] * p.QK[ob + idx]) * Dij;
+  }
+  __syncthreads();
+  if (tid < kCk) {
+    float r1 = 0.f, r2 = 0.f, c2 = 0.f;
+    for (int j = 0; j < kCk; ++j) {
+      r1 += E1[tid][j];
+      r2 += E2[tid][j];
+      c2 += E2[j][tid];
+    }
+    p.db3[(size_t)b * kCk + tid] = r1;
+    p.dg1[(size_t)b * kCk + tid] = r2 - c2;
+  }
+}
+
+// <dS', S> per (chunk, head).
+__global__ void __launch_bounds__(256)
+ck_sdot_kernel(const float* __restrict__ dSn, const float* __restrict__ S, float* __restrict__ sdot,
+               int DD, const long long* __restrict__ nlive) {
+  const long long b = blockIdx.x;
+  if (b >= *nlive) return;
+  __shared__ float red[8];
+  const float4* x = reinterpret_cast<const float4*>(dSn + (size_t)b * DD);
+  const float4* y = reinterpret_cast<const float4*>(S + (size_t)b * DD);
+  float s = 0.f;
+  for (int i = threadIdx.x; i < DD / 4; i += 256) {
+    const float4 a = x[i], c = y[i];
+    s += a.x * c.x + a.y * c.y + a.z * c.z + a.w * c.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    sdot[b] = t;
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Per (chunk, head): the per-token sums and the stores.  dq, dk, dv go to the token rows
+// of the chunk; dg is completed at the last token and summed in reverse into d log alpha.
+struct ScatterArgs {
+  const float *Qc, *Kc, *Vc, *dQa, *dKa, *dOS, *Rd, *TdW, *TdU, *gates, *gam, *db3, *dg1, *sdot;
+  const long long* crow0;
+  const int* clen;
+  const long long* nlive;
+  void *dq, *dk, *dv;
+  float *dlog_alpha, *dbeta;
+  int H;
+};
+
+template <int D, typename TIn>
+__global__ void __launch_bounds__(256) ck_scatter_kernel(ScatterArgs p) {
+  const long long b = blockIdx.x;
+  if (b >= *p.nlive) return;
+  constexpr int NQ = D / 32;
+  __shared__ float sdg[kCk], sdE[kCk];
+  const long long cid = b / p.H;
+  const int h = (int)(b - cid * p.H);
+  const long long row0 = p.crow0[cid];
+  const int len = p.clen[cid];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const float* G = p.gates + (size_t)b * kGates * kCk;
+  TIn* dq = reinterpret_cast<TIn*>(p.dq);
+  TIn* dk = reinterpret_cast<TIn*>(p.dk);
+  TIn* dv = reinterpret_cast<TIn*>(p.dv);
+  for (int c = w; c < kCk; c += 8) {
+    const float eg = G[G_EG * kCk + c], E = G[G_E * kCk + c];
+    const float be = G[G_BETA * kCk + c], beg = G[G_BEG * kCk + c];
+    const size_t o = ((size_t)b * kCk + c) * D;
+    const size_t ot = ((size_t)(row0 + c) * p.H + h) * D;
+    float d1 = 0.f, d2 = 0.f, d3 = 0.f, d4 = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < NQ; ++qq) {
+      const int x = lane + 32 * qq;
+      const float dos = p.dOS[o + x], qv = p.Qc[o + x], kv = p.Kc[o + x];
+      const float rd = p.Rd[o + x], tdw = p.TdW[o + x], tdu = p.TdU[o + x], vv = p.Vc[o + x];
+      d1 = fmaf(tdu, vv, d1);
+      d2 = fmaf(tdw, kv, d2);
+      d3 = fmaf(dos, qv, d3);
+      d4 = fmaf(rd, kv, d4);
+      if (c < len) {
+        dq[ot + x] = from_f<TIn>(fmaf(eg, dos, p.dQa[o + x]));
+        dk[ot + x] = from_f<TIn>(fmaf(beg, tdw, fmaf(E, rd, p.dKa[o + x])));
+        dv[ot + x] = from_f<TIn>(be * tdu);
+      }
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) {
+      d1 += __shfl_xor_sync(0xffffffffu, d1, s);
+      d2 += __shfl_xor_sync(0xffffffffu, d2, s);
+      d3 += __shfl_xor_sync(0xffffffffu, d3, s);
+      d4 += __shfl_xor_sync(0xffffffffu, d4, s);
+    }
+    if (lane == 0) {
+      if (c < len) p.dbeta[(size_t)(row0 + c) * p.H + h] = d1 + eg * d2 + p.db3[(size_t)b * kCk + c];
+      sdg[c] = p.dg1[(size_t)b * kCk + c] + (be * d2 + d3) * eg - d4 * E;
+      sdE[c] = d4 * E;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && len > 0) {
+    float tot = p.sdot[b] * p.gam[b];
+    for (int c = 0; c < len; ++c) tot += sdE[c];
+    sdg[len - 1] += tot;
+    float run = 0.f;
+    for (int c = len - 1; c >= 0; --c) {
+      run += sdg[c];
+      p.dlog_alpha[(size_t)(row0 + c) * p.H + h] = run;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Workspace: chunk tables, gate vectors, and the per-entry fp32 buffers.
+enum { QC, KC, WT, DOS, DW, RD, TDW, DQA, DKA, NCD };           // [kCk][D]
+enum { VC, DOC, UB, DL, YB, DDL, TDU, NCV };                     // [kCk][D]
+enum { KKB, QKB, TB, PB, DPM, DPD, DTB, M1B, DAB, XB, NCC };     // [kCk][kCk]
+enum { SB, ZB, DSN, NDD };                                        // [D][D]
+
+struct CkLayout {
+  long long nc, nb;
+  size_t crow0, clen, cbase, nlive, gates, gam, db3, dg1, sdot;
+  size_t cd[NCD], cv[NCV], cc[NCC], dd[NDD], total;
+};
+
+size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+CkLayout ck_layout(long long rows, int H, int D, int N) {
+  CkLayout L;
+  L.nc = rows / kCk + N;  // bounds the chunk count of any split of rows tokens into N
+  L.nb = L.nc * H;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += al256(bytes); return at; };
+  L.crow0 = take((size_t)L.nc * 8);
+  L.clen = take((size_t)L.nc * 4);
+  L.cbase = take((size_t)(N + 1) * 4);
+  L.nlive = take(8);
+  L.gates = take((size_t)L.nb * kGates * kCk * 4);
+  L.gam = take((size_t)L.nb * 4);
+  L.db3 = take((size_t)L.nb * kCk * 4);
+  L.dg1 = take((size_t)L.nb * kCk * 4);
+  L.sdot = take((size_t)L.nb * 4);
+  for (int i = 0; i < NCD; ++i) L.cd[i] = take((size_t)L.nb * kCk * D * 4);
+  for (int i = 0; i < NCV; ++i) L.cv[i] = take((size_t)L.nb * kCk * D * 4);
+  for (int i = 0; i < NCC; ++i) L.cc[i] = take((size_t)L.nb * kCk * kCk * 4);
+  for (int i = 0; i < NDD; ++i) L.dd[i] = take((size_t)L.nb * D * D * 4);
+  L.total = o;
+  return L;
+}
+
+struct MmLauncher {
+  long long nb;
+  const long long* nlive;
+  cudaStream_t s;
+  cudaError_t err = cudaSuccess;
+  // C = alpha * op(A) op(B), operands given by (pointer, batch stride, row stride,
+  // inner stride); see ck_mm_kernel.
+  Mm make(const float* A, long long ab, int am, int ak, const float* B, long long bb, int bk,
+          int bn, float* C, long long cb, int cm, int cn, int M, int N, int K) const {
+    Mm m;
+    m.A = A; m.ab = ab; m.am = am; m.ak = ak;
+    m.B = B; m.bb = bb; m.bk = bk; m.bn = bn;
+    m.C = C; m.cb = cb; m.cm = cm; m.cn = cn;
+    m.ks = m.cs = m.gv = nullptr;
+    m.vb = (long long)kGates * kCk;
+    m.alpha = 1.f; m.accum = 0; m.mask = 0;
+    m.M = M; m.N = N; m.K = K;
+    m.nlive = nlive;
+    return m;
+  }
+  void run(const Mm& m) {
+    if (err != cudaSuccess) return;
+    ck_mm_kernel<<<dim3((unsigned)nb, (unsigned)((m.M / 64) * (m.N / 64))), 256, 0, s>>>(m);
+    err = cudaGetLastError();
+  }
+};
+
+template <int D, typename TIn>
+cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
+  const long long rows = (long long)a.B * a.T;
+  const CkLayout L = ck_layout(rows, a.H, D, a.N);
+  unsigned char* ws = reinterpret_cast<unsigned char*>(a.workspace);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  long long* crow0 = reinterpret_cast<long long*>(ws + L.crow0);
+  int* clen = reinterpret_cast<int*>(ws + L.clen);
+  int* cbase = reinterpret_cast<int*>(ws + L.cbase);
+  long long* nlive = reinterpret_cast<long long*>(ws + L.nlive);
+  float* gates = F(L.gates);
+  float* gam = F(L.gam);
+  float *Qc = F(L.cd[QC]), *Kc = F(L.cd[KC]), *Wt = F(L.cd[WT]), *dOS = F(L.cd[DOS]);
+  float *dW = F(L.cd[DW]), *Rd = F(L.cd[RD]), *TdW = F(L.cd[TDW]), *dQa = F(L.cd[DQA]);
+  float* dKa = F(L.cd[DKA]);
+  float *Vc = F(L.cv[VC]), *dOc = F(L.cv[DOC]), *U = F(L.cv[UB]), *Dl = F(L.cv[DL]);
+  float *Y = F(L.cv[YB]), *dDl = F(L.cv[DDL]), *TdU = F(L.cv[TDU]);
+  float *KK = F(L.cc[KKB]), *QK = F(L.cc[QKB]), *Tm = F(L.cc[TB]), *P = F(L.cc[PB]);
+  float *dPm = F(L.cc[DPM]), *dPD = F(L.cc[DPD]), *dT = F(L.cc[DTB]), *M1 = F(L.cc[M1B]);
+  float *dA = F(L.cc[DAB]), *X = F(L.cc[XB]);
+  float *S = F(L.dd[SB]), *Z = F(L.dd[ZB]), *dSn = F(L.dd[DSN]);
+
+  ck_table_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.N, a.T, a.H, L.nc, crow0, clen, cbase, nlive);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned nb = (unsigned)L.nb;
+
+  GatherArgs ga;
+  ga.q = a.q; ga.k = a.k; ga.v = a.v; ga.dout = a.dout;
+  ga.log_alpha = a.log_alpha; ga.beta = a.beta;
+  ga.crow0 = crow0; ga.clen = clen; ga.nlive = nlive;
+  ga.Qc = Qc; ga.Kc = Kc; ga.Vc = Vc; ga.dOc = dOc; ga.gates = gates; ga.gam = gam; ga.H = a.H;
+  ck_gather_kernel<D, TIn><<<nb, 256, 0, s>>>(ga);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const long long CD = (long long)kCk * D, CC = (long long)kCk * kCk, DD = (long long)D * D;
+  MmLauncher mm{L.nb, nlive, s};
+  // KK^T = K K^T, QK^T = Q K^T
+  mm.run(mm.make(Kc, CD, D, 1, Kc, CD, 1, D, KK, CC, kCk, 1, kCk, kCk, D));
+  mm.run(mm.make(Qc, CD, D, 1, Kc, CD, 1, D, QK, CC, kCk, 1, kCk, kCk, D));
+  if (mm.err != cudaSuccess) return mm.err;
+  TsolveArgs ta{KK, QK, gates, Tm, P, nlive};
+  ck_tsolve_kernel<<<nb, 128, 0, s>>>(ta);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {  // W~ = T diag(beta e^g) K,  U = T diag(beta) V
+    Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
+    m.ks = gates + G_BEG * kCk;
+    mm.run(m);
+    m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
+    m.ks = gates + G_BETA * kCk;
+    mm.run(m);
+  }
+  if (mm.err != cudaSuccess) return mm.err;
+
+  constexpr int smem = chain_smem_bytes<D>();
+  static std::atomic<unsigned long long> set_f{0}, set_r{0};
+  if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, smem, set_f)) != cudaSuccess) return e;
+  if ((e = ensure_smem_cap(ck_chain_kernel<D, true>, smem, set_r)) != cudaSuccess) return e;
+  const dim3 cgrid((unsigned)((long long)a.N * a.H), D / kRows);
+  ChainArgs cf;
+  cf.cbase = cbase; cf.init = a.S0; cf.fin = nullptr; cf.st = S;
+  cf.add1 = U; cf.a1 = Wt; cf.a2 = Kc; cf.add2 = nullptr; cf.out1 = Dl;
+  cf.gates = gates; cf.gam = gam; cf.H = a.H;
+  ck_chain_kernel<D, false><<<cgrid, 256, smem, s>>>(cf);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  {  // Y = P^T dO,  Z = dO^T diag(e^g) Q
+    mm.run(mm.make(P, CC, 1, kCk, dOc, CD, D, 1, Y, CD, D, 1, kCk, D, kCk));
+    Mm m = mm.make(dOc, CD, 1, D, Qc, CD, D, 1, Z, DD, D, 1, D, D, kCk);
+    m.ks = gates + G_EG * kCk;
+    mm.run(m);
+  }
+  if (mm.err != cudaSuccess) return mm.err;
+  ChainArgs cr;
+  cr.cbase = cbase; cr.init = a.dS_final; cr.fin = a.dS0; cr.st = dSn;
+  cr.add1 = Y; cr.a1 = Kc; cr.a2 = Wt; cr.add2 = Z; cr.out1 = dDl;
+  cr.gates = gates; cr.gam = gam; cr.H = a.H;
+  ck_chain_kernel<D, true><<<cgrid, 256, smem, s>>>(cr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  {
+    // dP = lower(dO delta^T), and dP o D
+    Mm m = mm.make(dOc, CD, D, 1, Dl, CD, 1, D, dPm, CC, kCk, 1, kCk, kCk, D);
+    m.mask = 1;
+    mm.run(m);
+    m = mm.make(dOc, CD, D, 1, Dl, CD, 1, D, dPD, CC, kCk, 1, kCk, kCk, D);
+    m.gv = gates + G_G * kCk;
+    mm.run(m);
+    // (dP o D) K, (dP o D)^T Q
+    mm.run(mm.make(dPD, CC, kCk, 1, Kc, CD, D, 1, dQa, CD, D, 1, kCk, D, kCk));
+    mm.run(mm.make(dPD, CC, 1, kCk, Qc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk));
+    // dO S, dW = -d delta S, delta dS'
+    mm.run(mm.make(dOc, CD, D, 1, S, DD, D, 1, dOS, CD, D, 1, kCk, D, D));
+    m = mm.make(dDl, CD, D, 1, S, DD, D, 1, dW, CD, D, 1, kCk, D, D);
+    m.alpha = -1.f;
+    mm.run(m);
+    mm.run(mm.make(Dl, CD, D, 1, dSn, DD, D, 1, Rd, CD, D, 1, kCk, D, D));
+    // T^T d delta, T^T dW
+    mm.run(mm.make(Tm, CC, 1, kCk, dDl, CD, D, 1, TdU, CD, D, 1, kCk, D, kCk));
+    mm.run(mm.make(Tm, CC, 1, kCk, dW, CD, D, 1, TdW, CD, D, 1, kCk, D, kCk));
+    // dT = d delta (beta o V)^T + dW (beta e^g o K)^T
+    m = mm.make(dDl, CD, D, 1, Vc, CD, 1, D, dT, CC, kCk, 1, kCk, kCk, D);
+    m.cs = gates + G_BETA * kCk;
+    mm.run(m);
+    m = mm.make(dW, CD, D, 1, Kc, CD, 1, D, dT, CC, kCk, 1, kCk, kCk, D);
+    m.cs = gates + G_BEG * kCk;
+    m.accum = 1;
+    mm.run(m);
+    // dA = strictly-lower(-T^T dT T^T)
+    m = mm.make(Tm, CC, 1, kCk, dT, CC, kCk, 1, M1, CC, kCk, 1, kCk, kCk, kCk);
+    m.alpha = -1.f;
+    mm.run(m);
+    m = mm.make(M1, CC, kCk, 1, Tm, CC, 1, kCk, dA, CC, kCk, 1, kCk, kCk, kCk);
+    m.mask = 2;
+    mm.run(m);
+  }
+  if (mm.err != cudaSuccess) return mm.err;
+  float* db3 = F(L.db3);
+  float* dg1 = F(L.dg1);
+  float* sdot = F(L.sdot);
+  DaArgs da{dA, KK, QK, dPm, gates, X, db3, dg1, nlive};
+  ck_da_kernel<<<nb, 256, 0, s>>>(da);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {  // dK += X K + X^T K
+    Mm m = mm.make(X, CC, kCk, 1, Kc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk);
+    m.accum = 1;
+    mm.run(m);
+    m = mm.make(X, CC, 1, kCk, Kc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk);
+    m.accum = 1;
+    mm.run(m);
+  }
+  if (mm.err != cudaSuccess) return mm.err;
+  ck_sdot_kernel<<<nb, 256, 0, s>>>(dSn, S, sdot, (int)DD, nlive);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  ScatterArgs sa;
+  sa.Qc = Qc; sa.Kc = Kc; sa.Vc = Vc; sa.dQa = dQa; sa.dKa = dKa; sa.dOS = dOS; sa.Rd = Rd;
+  sa.TdW = TdW; sa.TdU = TdU; sa.gates = gates; sa.gam = gam; sa.db3 = db3; sa.dg1 = dg1;
+  sa.sdot = sdot; sa.crow0 = crow0; sa.clen = clen; sa.nlive = nlive;
+  sa.dq = a.dq; sa.dk = a.dk_out; sa.dv = a.dv_out; sa.dlog_alpha = a.dlog_alpha;
+  sa.dbeta = a.dbeta; sa.H = a.H;
+  ck_scatter_kernel<D, TIn><<<nb, 256, 0, s>>>(sa);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_chunked_supported(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
+
+size_t bwd_chunked_workspace_bytes(long long rows, int H, int dk, int dv, int N) {
+  if (rows == 0 || !bwd_chunked_supported(dk, dv)) return 0;
+  return ck_layout(rows, H, dk, N).total;
+}
+
+cudaError_t launch_bwd_chunked(const BwdArgs& a, cudaStream_t stream) {
+  if (!bwd_chunked_supported(a.dk, a.dv)) return cudaErrorInvalidValue;
+  if ((long long)a.N * a.H > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (a.dk == 64) return a.bf16 ? launch_ck_t<64, __nv_bfloat16>(a, stream) : launch_ck_t<64, float>(a, stream);
+  return a.bf16 ? launch_ck_t<128, __nv_bfloat16>(a, stream) : launch_ck_t<128, float>(a, stream);
+}
+
+}  // namespace gdn

@@ -121,6 +121,10 @@ struct BwdArgs {
 };
 size_t bwd_workspace_bytes(long long rows, int H, int dk, int dv, int N);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// The chunk-form backward (dk = dv = 64 or 128, rows > 0).
+bool bwd_chunked_supported(int dk, int dv);
+size_t bwd_chunked_workspace_bytes(long long rows, int H, int dk, int dv, int N);
+cudaError_t launch_bwd_chunked(const BwdArgs& a, cudaStream_t stream);
 // S <- S M_i + L_i for i < count per state (S_in NULL: zeros), already validated.
 cudaError_t launch_state_fold(const float* S_in, const float* M, const float* L, int count,
                               float* S_out, int units, int dv, int dk, cudaStream_t stream);

@@ -20,9 +20,10 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
 GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
+GDN_BWD_AUTO, GDN_BWD_TOKENS, GDN_BWD_CHUNKED = 0, 1, 2
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_host_workspace_bytes",
            "gdn_decode_step_host", "gdn_decode_step_host_workspace_bytes",
-           "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_bytes",
+           "gdn_chunk_bwd", "gdn_chunk_bwd_ex", "gdn_chunk_bwd_workspace_bytes", "gdn_bwd_select_path",
            "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
            "gdn_check_status", "gdn_selftest_wait_timeout", "gdn_last_error", "gdn_version")
 
@@ -56,6 +57,11 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
                                   I, I, I, I, I, P, I, I, P]
     lib.gdn_chunk_bwd.restype = I
+    lib.gdn_chunk_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
+                                     I, I, I, I, I, P, I, I, I, P]
+    lib.gdn_chunk_bwd_ex.restype = I
+    lib.gdn_bwd_select_path.argtypes = [I, I, I]
+    lib.gdn_bwd_select_path.restype = I
     lib.gdn_chunk_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.gdn_chunk_bwd_workspace_bytes.restype = Z
     lib.gdn_chunk_fwd_host.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, Z, P]
@@ -359,14 +365,20 @@ def gdn_chunk_bwd_workspace_bytes(B: int, H: int, T: int, dk: int, dv: int, n_se
     return int(load_library().gdn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, n_seqs))
 
 
+def gdn_bwd_select_path(dk: int, dv: int, dtype: torch.dtype) -> int:
+    """The backward path (GDN_BWD_TOKENS or GDN_BWD_CHUNKED) taken for these sizes."""
+    return load_library().gdn_bwd_select_path(dk, dv, _dtype_code(dtype))
+
+
 def gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_log_alpha,
                   d_beta, d_S0, workspace, cu_seqlens: Optional[torch.Tensor] = None,
-                  stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Tensor-level call of the C entry point of the same name.  Inputs as for
-    ``gdn_chunk_fwd``; d_out like out; dS_final like S_final (or None); the gradient
-    outputs d_q, d_k, d_v (input dtype), d_log_alpha, d_beta (fp32) and d_S0 (fp32 or
-    None); workspace a CUDA uint8 tensor of at least ``gdn_chunk_bwd_workspace_bytes``
-    bytes.  Launches on ``stream`` (default: current) without synchronising."""
+                  stream: Optional[torch.cuda.Stream] = None, path: int = GDN_BWD_AUTO) -> None:
+    """Tensor-level call of the C entry point gdn_chunk_bwd_ex (gdn_chunk_bwd for
+    path = GDN_BWD_AUTO).  Inputs as for ``gdn_chunk_fwd``; d_out like out; dS_final like
+    S_final (or None); the gradient outputs d_q, d_k, d_v (input dtype), d_log_alpha,
+    d_beta (fp32) and d_S0 (fp32 or None); workspace a CUDA uint8 tensor of at least
+    ``gdn_chunk_bwd_workspace_bytes`` bytes.  Launches on ``stream`` (default: current)
+    without synchronising."""
     lib = load_library()
     B, T, H, dk = k.shape
     dv = v.shape[-1]
@@ -386,18 +398,19 @@ def gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, 
     n_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     s = stream if stream is not None else torch.cuda.current_stream(v.device)
-    _check(lib.gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                             _ptr(d_out), _ptr(dS_final), _ptr(d_q), _ptr(d_k), _ptr(d_v),
-                             _ptr(d_log_alpha), _ptr(d_beta), _ptr(d_S0), _ptr(workspace),
-                             ws_bytes, B, H, T, dk, dv, _ptr(cu_seqlens),
-                             0 if cu_seqlens is None else n_seqs, code,
-                             ctypes.c_void_p(s.cuda_stream)))
+    _check(lib.gdn_chunk_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(S0), _ptr(d_out), _ptr(dS_final), _ptr(d_q), _ptr(d_k),
+                                _ptr(d_v), _ptr(d_log_alpha), _ptr(d_beta), _ptr(d_S0),
+                                _ptr(workspace), ws_bytes, B, H, T, dk, dv, _ptr(cu_seqlens),
+                                0 if cu_seqlens is None else n_seqs, code, int(path),
+                                ctypes.c_void_p(s.cuda_stream)))
 
 
 def chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final=None, cu_seqlens=None,
-              want_dS0: bool = True):
+              want_dS0: bool = True, path: int = GDN_BWD_AUTO):
     """Allocate the gradients and the workspace and run the backward on the current
-    stream (device tensors).  Returns (d_q, d_k, d_v, d_log_alpha, d_beta, d_S0 or None)."""
+    stream (device tensors), on ``path`` (GDN_BWD_AUTO, GDN_BWD_TOKENS or
+    GDN_BWD_CHUNKED).  Returns (d_q, d_k, d_v, d_log_alpha, d_beta, d_S0 or None)."""
     B, T, H, dk = k.shape
     dv = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
@@ -409,7 +422,7 @@ def chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final=None, cu_seqlens=Non
     nbytes = gdn_chunk_bwd_workspace_bytes(B, H, T, dk, dv, N)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_la, d_b, d_S0,
-                  ws, cu_seqlens)
+                  ws, cu_seqlens, path=path)
     return d_q, d_k, d_v, d_la, d_b, d_S0
 
 

@@ -115,7 +115,8 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v,
  *            (may be NULL when that is 0); its contents need no initialisation
  *
  * Device pointers, caller-owned, 16-byte aligned; outputs must not overlap inputs.
- * Asynchronous; 2 kernel launches.  Errors: GDN_EINVAL / GDN_EDTYPE before any launch
+ * Asynchronous; the path gdn_bwd_select_path names (2 kernel launches on the per-token
+ * path, 29 on the chunked one).  Errors: GDN_EINVAL / GDN_EDTYPE before any launch
  * (including a missing or short workspace, with the size needed in the message),
  * GDN_ELAUNCH.  With packed sequences, token rows outside every sequence get
  * unspecified gradients.
@@ -128,9 +129,45 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v,
                   int B, int H, int T, int dk, int dv,
                   const int32_t* cu_seqlens, int N_seqs, int qkv_dtype, void* stream);
 
-/* Workspace bytes gdn_chunk_bwd needs (N_seqs = number of sequences: B, or the packed
- * count); 0 for T == 0 or unsupported sizes. */
+/* Workspace bytes gdn_chunk_bwd and gdn_chunk_bwd_ex (either path) need (N_seqs = number
+ * of sequences: B, or the packed count); 0 for T == 0 or unsupported sizes. */
 size_t gdn_chunk_bwd_workspace_bytes(int B, int H, int T, int dk, int dv, int N_seqs);
+
+/* Backward kernel families. */
+typedef enum {
+  GDN_BWD_AUTO = 0,     /* the one gdn_bwd_select_path names */
+  GDN_BWD_TOKENS = 1,   /* per-token recurrence over row blocks of the state, from
+                           checkpoints every 8 tokens: every head size */
+  GDN_BWD_CHUNKED = 2   /* the chunk form: per chunk of 64 tokens the derivative as dense
+                           products, with the chunk-start states and the chunk-end state
+                           gradients from two chains over the chunks; dk = dv = 64 or 128 */
+} gdn_bwd_path;
+
+/* The backward path gdn_chunk_bwd takes for these sizes (GDN_BWD_TOKENS or
+ * GDN_BWD_CHUNKED), 0 if unsupported. */
+int gdn_bwd_select_path(int dk, int dv, int qkv_dtype);
+
+/*
+ * gdn_chunk_bwd_ex -- gdn_chunk_bwd on a chosen path (gdn_bwd_path).  Both paths compute
+ * the same derivative in fp32 arithmetic and are deterministic; they differ in summation
+ * order only.  The chunked path is the derivative of the chunk form (Nyysyyan,
+ * "Gated-DeltaNet", WY representation and chunkwise algorithm): per chunk, with T the
+ * inverse of the chunk's unit lower-triangular WY matrix, W~ = T diag(beta e^g) K and
+ * U = T diag(beta) V,
+ *   d delta = P^T dO + E K dS'^T,   dS = dO^T diag(e^g) Q + e^{g_last} dS' - d delta^T W~,
+ * and dQ, dK, dV, dbeta, dlog_alpha through P = lower(Q K^T o D), the state write and
+ * the WY factors (dA = -T^T dT T^T for the triangular solve); T == 0 and unsupported head
+ * sizes run the per-token path.  Errors as gdn_chunk_bwd, plus GDN_EINVAL for an unknown
+ * path or GDN_BWD_CHUNKED with head sizes it does not support.
+ */
+int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v,
+                     const float* log_alpha, const float* beta, const float* S0,
+                     const void* d_out, const float* dS_final,
+                     void* d_q, void* d_k, void* d_v, float* d_log_alpha, float* d_beta,
+                     float* d_S0, void* workspace, size_t workspace_bytes,
+                     int B, int H, int T, int dk, int dv,
+                     const int32_t* cu_seqlens, int N_seqs, int qkv_dtype, int bwd_path,
+                     void* stream);
 
 /*
  * gdn_chunk_fwd_host -- gdn_chunk_fwd (or, with beta == NULL, gdn_linear_chunk_fwd) on

@@ -278,3 +278,43 @@ def test_header_compiles_standalone(lang, std, tmp_path):
                         "-I", os.path.join(ROOT, "include"), str(src)],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def _call_bwd(lib, path, **over):
+    """Call gdn_chunk_bwd_ex with fake (never dereferenced) aligned pointers."""
+    a = dict(B=2, H=4, T=128, dk=64, dv=64, dt=gdn.GDN_F32)
+    a.update(over)
+    P = ctypes.c_void_p
+    ptrs = [P(4096 * (i + 1)) for i in range(14)]
+    ptrs[5] = ptrs[7] = ptrs[13] = None  # S0, dS_final, d_S0
+    return lib.gdn_chunk_bwd_ex(*ptrs, P(1 << 20), ctypes.c_size_t(1 << 40), a["B"], a["H"],
+                                a["T"], a["dk"], a["dv"], None, 0, a["dt"], path, None)
+
+
+def test_bwd_select_path(lib):
+    assert gdn.gdn_bwd_select_path(128, 128, torch.bfloat16) == gdn.GDN_BWD_CHUNKED
+    assert gdn.gdn_bwd_select_path(64, 64, torch.float32) == gdn.GDN_BWD_CHUNKED
+    for dk, dv in ((16, 16), (32, 32), (64, 128), (128, 64)):
+        assert gdn.gdn_bwd_select_path(dk, dv, torch.float32) == gdn.GDN_BWD_TOKENS
+    assert gdn.gdn_bwd_select_path(48, 48, torch.float32) == 0
+
+
+def test_bwd_workspace_covers_both_paths(lib):
+    for dk in (64, 128):
+        a = lib.gdn_chunk_bwd_workspace_bytes(4, 16, 4096, dk, dk, 4)
+        assert a > 0
+    # chunk buffers: at least 16 [64 x d] and 3 [d x d] fp32 tiles per (chunk, head)
+    assert lib.gdn_chunk_bwd_workspace_bytes(4, 16, 4096, 128, 128, 4) >= 64 * 16 * (
+        16 * 64 * 128 + 3 * 128 * 128) * 4
+
+
+@pytest.mark.parametrize("path,over,word", [
+    (7, {}, "unknown backward path"),
+    (-1, {}, "unknown backward path"),
+    (gdn.GDN_BWD_CHUNKED, dict(dk=32, dv=32), "chunked path needs"),
+    (gdn.GDN_BWD_CHUNKED, dict(dk=64, dv=128), "chunked path needs"),
+])
+def test_bwd_path_rejected_before_launch(lib, path, over, word):
+    assert _call_bwd(lib, path, **over) == binding.GDN_EINVAL
+    msg = lib.gdn_last_error().decode()
+    assert word in msg, msg
