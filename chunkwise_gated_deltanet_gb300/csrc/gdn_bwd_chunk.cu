@@ -210,11 +210,14 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
 
 // ---------------------------------------------------------------------------------
 // Batched fp32 GEMM: for every live batch entry b,
-//   C(m, n) = alpha * sum_k A(m, k) * ks[k] * B(k, n) * cs[n] * Dg(m, n)  (+ C(m, n))
+//   C(m, n) = alpha * sum_k A(m, k) * ks[k] * B(k, n) * cs[n]   (+ C(m, n) with accum)
 // A(m, k) = A[b*ab + m*am + k*ak] (likewise B and C), so either operand may be read
-// transposed.  ks, cs: optional per-entry vectors (stride vb); gv: optional g vector,
-// Dg(m, n) = e^{g_m - g_n} for n <= m and 0 above; mask 1 keeps n <= m, mask 2 n < m.
-// One CTA per 64 x 64 output tile and entry; M, N multiples of 64, K of 32.
+// transposed; one of each operand's two strides is 1.  ks, cs: optional per-entry
+// vectors (stride vb).  mask 1 keeps n <= m, mask 2 n < m.  With C2, the product is also
+// written there times Dg(m, n) = e^{g_m - g_n} for n <= m (0 above), g = gv.
+// One CTA of 128 threads per 64 x 64 output tile and entry, 8 x 4 outputs per thread
+// read as 128-bit shared-memory vectors; the next 32-deep K slice is fetched into
+// registers while the current one is multiplied.  M, N multiples of 64, K of 32.
 struct Mm {
   const float* A;
   long long ab;
@@ -225,6 +228,7 @@ struct Mm {
   float* C;
   long long cb;
   int cm, cn;
+  float* C2;
   const float *ks, *cs, *gv;
   long long vb;
   float alpha;
@@ -232,73 +236,107 @@ struct Mm {
   const long long* nlive;
 };
 
-__global__ void __launch_bounds__(256, 3) ck_mm_kernel(Mm p) {
+constexpr int kMmThreads = 128, kMmLd = 68;
+
+// Slice k0..k0+31 of a 64-row operand X(r, k) = X[r*rs + k*ks_] (one stride 1) as four
+// float4 per thread, scaled by sc[k] when given.
+__device__ __forceinline__ void mm_fetch(const float* X, int rs, int ks_, int r0, int k0,
+                                         const float* sc, float4 (&v)[4]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid + kMmThreads * i;  // 512 float4
+    if (ks_ == 1) {                        // contiguous in k: row idx / 8, k 4 (idx % 8)
+      const int r = idx >> 3, k = 4 * (idx & 7);
+      v[i] = *reinterpret_cast<const float4*>(X + (long long)(r0 + r) * rs + k0 + k);
+      if (sc) {
+        v[i].x *= sc[k0 + k]; v[i].y *= sc[k0 + k + 1];
+        v[i].z *= sc[k0 + k + 2]; v[i].w *= sc[k0 + k + 3];
+      }
+    } else {                               // contiguous in r: k idx / 16, rows 4 (idx % 16)
+      const int k = idx >> 4, r = 4 * (idx & 15);
+      v[i] = *reinterpret_cast<const float4*>(X + (long long)(k0 + k) * ks_ + r0 + r);
+      if (sc) {
+        const float f = sc[k0 + k];
+        v[i].x *= f; v[i].y *= f; v[i].z *= f; v[i].w *= f;
+      }
+    }
+  }
+}
+
+// Store a fetched slice as S[k][r] (row stride kMmLd).
+__device__ __forceinline__ void mm_stash(float* S, int ks_, const float4 (&v)[4]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid + kMmThreads * i;
+    if (ks_ == 1) {
+      const int r = idx >> 3, k = 4 * (idx & 7);
+      S[(k + 0) * kMmLd + r] = v[i].x;
+      S[(k + 1) * kMmLd + r] = v[i].y;
+      S[(k + 2) * kMmLd + r] = v[i].z;
+      S[(k + 3) * kMmLd + r] = v[i].w;
+    } else {
+      const int k = idx >> 4, r = 4 * (idx & 15);
+      *reinterpret_cast<float4*>(S + k * kMmLd + r) = v[i];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMmThreads) ck_mm_kernel(Mm p) {
   const long long b = blockIdx.x;
   if (b >= *p.nlive) return;
-  __shared__ float As[32][65], Bs[32][65];
+  __shared__ __align__(16) float As[32 * kMmLd], Bs[32 * kMmLd];
   const int tilesN = p.N / 64;
   const int m0 = (blockIdx.y / tilesN) * 64, n0 = (blockIdx.y % tilesN) * 64;
   const float* A = p.A + b * p.ab;
   const float* B = p.B + b * p.bb;
   const float* ks = p.ks ? p.ks + b * p.vb : nullptr;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  float acc[4][4];
+  // A(m, k) as rows m: stride am, inner ak.  B(k, n) as rows n: stride bn, inner bk.
+  float4 va[4], vb[4];
+  mm_fetch(A, p.am, p.ak, m0, 0, nullptr, va);
+  mm_fetch(B, p.bn, p.bk, n0, 0, ks, vb);
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int k0 = 0; k0 < p.K; k0 += 32) {
-#pragma unroll 4
-    for (int r = 0; r < 8; ++r) {
-      const int idx = tid + 256 * r;
-      int mm, ka;
-      if (p.ak == 1) {
-        ka = idx & 31;
-        mm = idx >> 5;
-      } else {
-        mm = idx & 63;
-        ka = idx >> 6;
-      }
-      As[ka][mm] = A[(long long)(m0 + mm) * p.am + (long long)(k0 + ka) * p.ak];
-      int nn, kb;
-      if (p.bn == 1) {
-        nn = idx & 63;
-        kb = idx >> 6;
-      } else {
-        kb = idx & 31;
-        nn = idx >> 5;
-      }
-      float x = B[(long long)(k0 + kb) * p.bk + (long long)(n0 + nn) * p.bn];
-      if (ks) x *= ks[k0 + kb];
-      Bs[kb][nn] = x;
-    }
+    mm_stash(As, p.ak, va);
+    mm_stash(Bs, p.bk, vb);
     __syncthreads();
+    if (k0 + 32 < p.K) {
+      mm_fetch(A, p.am, p.ak, m0, k0 + 32, nullptr, va);
+      mm_fetch(B, p.bn, p.bk, n0, k0 + 32, ks, vb);
+    }
 #pragma unroll 8
     for (int kk = 0; kk < 32; ++kk) {
-      float a[4], c[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(As + kk * kMmLd + 8 * ty);
+      const float4 a1 = *reinterpret_cast<const float4*>(As + kk * kMmLd + 8 * ty + 4);
+      const float4 c = *reinterpret_cast<const float4*>(Bs + kk * kMmLd + 4 * tx);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) c[j] = Bs[kk][tx + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], cv[j], acc[i][j]);
     }
     __syncthreads();
   }
   const float* cs = p.cs ? p.cs + b * p.vb : nullptr;
   const float* gv = p.gv ? p.gv + b * p.vb : nullptr;
   float* C = p.C + b * p.cb;
+  float* C2 = p.C2 ? p.C2 + b * p.cb : nullptr;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty + 16 * i;
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + 8 * ty + i;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx + 16 * j;
+      const int n = n0 + 4 * tx + j;
       float x = p.alpha * acc[i][j];
       if (cs) x *= cs[n];
-      if (gv) x = n <= m ? x * expf(gv[m] - gv[n]) : 0.f;
+      if (C2) C2[(long long)m * p.cm + (long long)n * p.cn] = n <= m ? x * expf(gv[m] - gv[n]) : 0.f;
       if ((p.mask == 1 && n > m) || (p.mask == 2 && n >= m)) x = 0.f;
       float* o = C + (long long)m * p.cm + (long long)n * p.cn;
       *o = p.accum ? *o + x : x;
@@ -340,14 +378,16 @@ __global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
     for (int i = 0; i < c; ++i) Ts[i][c] = 0.f;
     Ts[c][c] = 1.f;
     for (int i = c + 1; i < kCk; ++i) {
-      float s0 = 0.f, s1 = 0.f;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
       int j = c;
-      for (; j + 1 < i; j += 2) {
+      for (; j + 3 < i; j += 4) {
         s0 = fmaf(As[i][j], Ts[j][c], s0);
         s1 = fmaf(As[i][j + 1], Ts[j + 1][c], s1);
+        s2 = fmaf(As[i][j + 2], Ts[j + 2][c], s2);
+        s3 = fmaf(As[i][j + 3], Ts[j + 3][c], s3);
       }
-      if (j < i) s0 = fmaf(As[i][j], Ts[j][c], s0);
-      Ts[i][c] = -(s0 + s1);
+      for (; j < i; ++j) s0 = fmaf(As[i][j], Ts[j][c], s0);
+      Ts[i][c] = -((s0 + s1) + (s2 + s3));
     }
   }
   __syncthreads();
@@ -376,112 +416,166 @@ struct ChainArgs {
 
 template <int D>
 constexpr int chain_smem_bytes() {
-  return 4 * (kRows * (D + 1) + 2 * kCk * (D + 1) + kCk * (kRows + 1) + kCk);
+  return 4 * (kRows * (D + 4) + 2 * kCk * (D + 4) + 2 * kCk + kRows * (kCk + 4));
+}
+
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A [kCk][D] operand tile into shared memory rows of LD floats, as one async group;
+// with vec, also the entry's E and e^g gate vectors (threads 0..31).
+template <int D>
+__device__ __forceinline__ void chain_issue(float* dst, const float* src, float* vec,
+                                            const float* gates) {
+  constexpr int LD = D + 4;
+  for (int i = threadIdx.x; i < kCk * D / 4; i += 256) {
+    const int c = i / (D / 4), k = 4 * (i % (D / 4));
+    cp_async16(dst + c * LD + k, src + (size_t)c * D + k);
+  }
+  if (vec && threadIdx.x < 32) {
+    const int t = threadIdx.x;
+    const float* g = gates + (t < 16 ? G_E * kCk + 4 * t : G_EG * kCk + 4 * (t - 16));
+    cp_async16(vec + 4 * t, g);
+  }
+  cp_async_commit();
 }
 
 template <int D, bool REV>
 __global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
-  extern __shared__ float sm[];
-  constexpr int LD = D + 1, LR = kRows + 1, NJ = D / 32;
-  float* St = sm;
-  float* A1 = St + kRows * LD;
-  float* A2 = A1 + kCk * LD;
-  float* X1 = A2 + kCk * LD;
-  float* Ev = X1 + kCk * LR;
+  extern __shared__ __align__(16) float sm[];
+  constexpr int LD = D + 4, LX = kCk + 4, NK = D / 64;
+  float* St = sm;                  // [kRows][LD]
+  float* A1 = St + kRows * LD;     // [kCk][LD]
+  float* A2 = A1 + kCk * LD;       // [kCk][LD]
+  float* Vv = A2 + kCk * LD;       // E [kCk], e^g [kCk]
+  float* X1 = Vv + 2 * kCk;        // s2_c X1(c, r) stored as [kRows][LX]
   const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H, r0 = blockIdx.y * kRows;
   const int tid = threadIdx.x;
   const int base = p.cbase[n], nc = p.cbase[n + 1] - base;
   const size_t sidx = ((size_t)n * p.H + h) * D * D;
+  auto entry = [&](int jj) { return (long long)(base + (REV ? nc - 1 - jj : jj)) * p.H + h; };
+  if (nc > 0) {
+    const long long b = entry(0);
+    chain_issue<D>(A1, p.a1 + (size_t)b * kCk * D, Vv, p.gates + (size_t)b * kGates * kCk);
+    chain_issue<D>(A2, p.a2 + (size_t)b * kCk * D, nullptr, nullptr);
+  }
   for (int i = tid; i < kRows * D; i += 256) {
     const int r = i / D, k = i % D;
     St[r * LD + k] = p.init ? p.init[sidx + (size_t)(r0 + r) * D + k] : 0.f;
   }
+  const int cy = tid >> 3, rx = tid & 7;   // X1 roles: c = cy + 32 i, r = rx + 8 j
+  // St roles: rows 8 rg .. 8 rg + 7, columns kh D/2 + lane + 32 j (j < NK)
+  const int rg = (tid >> 5) & 3, kc = (tid >> 7) * (D / 2) + (tid & 31);
   for (int jj = 0; jj < nc; ++jj) {
-    const int j = REV ? nc - 1 - jj : jj;
-    const long long b = (long long)(base + j) * p.H + h;
-    __syncthreads();
+    const long long b = entry(jj);
+    __syncthreads();  // St complete (init or the previous update)
     float* stb = p.st + (size_t)b * D * D;
     for (int i = tid; i < kRows * D / 4; i += 256) {
       const int r = i / (D / 4), k = 4 * (i % (D / 4));
-      const float* s = St + r * LD + k;
-      *reinterpret_cast<float4*>(stb + (size_t)(r0 + r) * D + k) = make_float4(s[0], s[1], s[2], s[3]);
+      *reinterpret_cast<float4*>(stb + (size_t)(r0 + r) * D + k) =
+          *reinterpret_cast<const float4*>(St + r * LD + k);
     }
-    const float* a1 = p.a1 + (size_t)b * kCk * D;
-    const float* a2 = p.a2 + (size_t)b * kCk * D;
-    for (int i = tid; i < kCk * D / 4; i += 256) {
-      const int c = i / (D / 4), k = 4 * (i % (D / 4));
-      const float4 x = *reinterpret_cast<const float4*>(a1 + (size_t)c * D + k);
-      const float4 y = *reinterpret_cast<const float4*>(a2 + (size_t)c * D + k);
-      float* d1 = A1 + c * LD + k;
-      float* d2 = A2 + c * LD + k;
-      d1[0] = x.x; d1[1] = x.y; d1[2] = x.z; d1[3] = x.w;
-      d2[0] = y.x; d2[1] = y.y; d2[2] = y.z; d2[3] = y.w;
-    }
-    if (tid < kCk) Ev[tid] = p.gates[(size_t)b * kGates * kCk + G_E * kCk + tid];
+    float add1[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int jq = 0; jq < 4; ++jq)
+        add1[i][jq] = p.add1[(size_t)b * kCk * D + (size_t)(cy + 32 * i) * D + r0 + rx + 8 * jq];
+    cp_async_wait<1>();  // A1 and the gate vectors
     __syncthreads();
-    const float gam = p.gam[b];
-    {  // X1: kCk x kRows, thread rows c = cy + 32 i, columns r = rx + 8 j
-      const int cy = tid >> 3, rx = tid & 7;
+    {  // X1(c, r) = Add1 + s1_c sum_k A1(c, k) St(r, k)
       float acc[2][4];
 #pragma unroll
       for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int jq = 0; jq < 4; ++jq) acc[i][jq] = 0.f;
-#pragma unroll 4
-      for (int k = 0; k < D; ++k) {
-        const float a0 = A1[cy * LD + k], a1v = A1[(cy + 32) * LD + k];
+#pragma unroll 2
+      for (int k = 0; k < D; k += 4) {
+        const float4 a0 = *reinterpret_cast<const float4*>(A1 + cy * LD + k);
+        const float4 a1v = *reinterpret_cast<const float4*>(A1 + (cy + 32) * LD + k);
 #pragma unroll
         for (int jq = 0; jq < 4; ++jq) {
-          const float s = St[(rx + 8 * jq) * LD + k];
-          acc[0][jq] = fmaf(a0, s, acc[0][jq]);
-          acc[1][jq] = fmaf(a1v, s, acc[1][jq]);
+          const float4 sv = *reinterpret_cast<const float4*>(St + (rx + 8 * jq) * LD + k);
+          acc[0][jq] = fmaf(a0.w, sv.w, fmaf(a0.z, sv.z, fmaf(a0.y, sv.y, fmaf(a0.x, sv.x, acc[0][jq]))));
+          acc[1][jq] = fmaf(a1v.w, sv.w, fmaf(a1v.z, sv.z, fmaf(a1v.y, sv.y, fmaf(a1v.x, sv.x, acc[1][jq]))));
         }
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int c = cy + 32 * i;
-        const float s1 = REV ? Ev[c] : -1.f, s2 = REV ? -1.f : Ev[c];
+        const float e = Vv[c];
+        const float s1 = REV ? e : -1.f, s2 = REV ? -1.f : e;
 #pragma unroll
         for (int jq = 0; jq < 4; ++jq) {
           const int r = rx + 8 * jq;
-          const size_t o = (size_t)b * kCk * D + (size_t)c * D + r0 + r;
-          const float x = p.add1[o] + s1 * acc[i][jq];
-          p.out1[o] = x;
-          X1[c * LR + r] = s2 * x;
+          const float x = add1[i][jq] + s1 * acc[i][jq];
+          p.out1[(size_t)b * kCk * D + (size_t)c * D + r0 + r] = x;
+          X1[r * LX + c] = s2 * x;
         }
       }
     }
+    const float gam = Vv[kCk + kCk - 1];  // e^{g_last}
+    float add2[8][NK];
+    if (REV) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int jq = 0; jq < NK; ++jq)
+          add2[i][jq] = p.add2[(size_t)b * D * D + (size_t)(r0 + 8 * rg + i) * D + kc + 32 * jq];
+    }
+    __syncthreads();  // X1 complete; A1 and the gate vectors free
+    if (jj + 1 < nc) {
+      const long long bn = entry(jj + 1);
+      chain_issue<D>(A1, p.a1 + (size_t)bn * kCk * D, Vv, p.gates + (size_t)bn * kGates * kCk);
+      cp_async_wait<1>();  // A2 of this chunk
+    } else {
+      cp_async_wait<0>();
+    }
     __syncthreads();
-    {  // St update: kRows x D, thread rows r = ry + 8 i, columns k = kx + 32 j
-      const int ry = tid >> 5, kx = tid & 31;
-      float acc[4][NJ];
+    {  // St(r, k) = Add2 + Gamma St(r, k) + sum_c s2_c X1(c, r) A2(c, k)
+      float acc[8][NK];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int jq = 0; jq < NJ; ++jq) acc[i][jq] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < kCk; ++c) {
-        float x[4], a[NJ];
+        for (int jq = 0; jq < NK; ++jq) acc[i][jq] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < kCk; c += 4) {
+        float a[4][NK];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = X1[c * LR + ry + 8 * i];
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int jq = 0; jq < NJ; ++jq) a[jq] = A2[c * LD + kx + 32 * jq];
+          for (int jq = 0; jq < NK; ++jq) a[u][jq] = A2[(c + u) * LD + kc + 32 * jq];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = *reinterpret_cast<const float4*>(X1 + (8 * rg + i) * LX + c);
 #pragma unroll
-          for (int jq = 0; jq < NJ; ++jq) acc[i][jq] = fmaf(x[i], a[jq], acc[i][jq]);
+          for (int jq = 0; jq < NK; ++jq)
+            acc[i][jq] = fmaf(x.w, a[3][jq], fmaf(x.z, a[2][jq], fmaf(x.y, a[1][jq], fmaf(x.x, a[0][jq], acc[i][jq]))));
+        }
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = ry + 8 * i;
+      for (int i = 0; i < 8; ++i) {
+        const int r = 8 * rg + i;
 #pragma unroll
-        for (int jq = 0; jq < NJ; ++jq) {
-          const int k = kx + 32 * jq;
+        for (int jq = 0; jq < NK; ++jq) {
+          const int k = kc + 32 * jq;
           float v = fmaf(gam, St[r * LD + k], acc[i][jq]);
-          if (REV) v += p.add2[(size_t)b * D * D + (size_t)(r0 + r) * D + k];
+          if (REV) v += add2[i][jq];
           St[r * LD + k] = v;
         }
       }
+    }
+    __syncthreads();  // A2 free
+    if (jj + 1 < nc) {
+      const long long bn = entry(jj + 1);
+      chain_issue<D>(A2, p.a2 + (size_t)bn * kCk * D, nullptr, nullptr);
     }
   }
   __syncthreads();
@@ -686,6 +780,7 @@ struct MmLauncher {
     m.A = A; m.ab = ab; m.am = am; m.ak = ak;
     m.B = B; m.bb = bb; m.bk = bk; m.bn = bn;
     m.C = C; m.cb = cb; m.cm = cm; m.cn = cn;
+    m.C2 = nullptr;
     m.ks = m.cs = m.gv = nullptr;
     m.vb = (long long)kGates * kCk;
     m.alpha = 1.f; m.accum = 0; m.mask = 0;
@@ -695,7 +790,12 @@ struct MmLauncher {
   }
   void run(const Mm& m) {
     if (err != cudaSuccess) return;
-    ck_mm_kernel<<<dim3((unsigned)nb, (unsigned)((m.M / 64) * (m.N / 64))), 256, 0, s>>>(m);
+    if (m.M % 64 || m.N % 64 || m.K % 32 || (m.am != 1 && m.ak != 1) ||
+        (m.bk != 1 && m.bn != 1)) {
+      err = cudaErrorInvalidValue;
+      return;
+    }
+    ck_mm_kernel<<<dim3((unsigned)nb, (unsigned)((m.M / 64) * (m.N / 64))), kMmThreads, 0, s>>>(m);
     err = cudaGetLastError();
   }
 };
@@ -784,8 +884,7 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
     // dP = lower(dO delta^T), and dP o D
     Mm m = mm.make(dOc, CD, D, 1, Dl, CD, 1, D, dPm, CC, kCk, 1, kCk, kCk, D);
     m.mask = 1;
-    mm.run(m);
-    m = mm.make(dOc, CD, D, 1, Dl, CD, 1, D, dPD, CC, kCk, 1, kCk, kCk, D);
+    m.C2 = dPD;
     m.gv = gates + G_G * kCk;
     mm.run(m);
     // (dP o D) K, (dP o D)^T Q
