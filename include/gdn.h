@@ -116,7 +116,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v,
  *
  * Device pointers, caller-owned, 16-byte aligned; outputs must not overlap inputs.
  * Asynchronous; the path gdn_bwd_select_path names (2 kernel launches on the per-token
- * path, 29 on the chunked one).  Errors: GDN_EINVAL / GDN_EDTYPE before any launch
+ * path, 28 on the chunked one).  Errors: GDN_EINVAL / GDN_EDTYPE before any launch
  * (including a missing or short workspace, with the size needed in the message),
  * GDN_ELAUNCH.  With packed sequences, token rows outside every sequence get
  * unspecified gradients.
