@@ -209,15 +209,20 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
 }
 
 // ---------------------------------------------------------------------------------
-// Batched fp32 GEMM: for every live batch entry b,
+// Batched GEMM with fp32 accuracy: for every live batch entry b,
 //   C(m, n) = alpha * sum_k A(m, k) * ks[k] * B(k, n) * cs[n]   (+ C(m, n) with accum)
 // A(m, k) = A[b*ab + m*am + k*ak] (likewise B and C), so either operand may be read
 // transposed; one of each operand's two strides is 1.  ks, cs: optional per-entry
 // vectors (stride vb).  mask 1 keeps n <= m, mask 2 n < m.  With C2, the product is also
 // written there times Dg(m, n) = e^{g_m - g_n} for n <= m (0 above), g = gv.
-// One CTA of 128 threads per 64 x 64 output tile and entry, 8 x 4 outputs per thread
-// read as 128-bit shared-memory vectors; the next 32-deep K slice is fetched into
-// registers while the current one is multiplied.  M, N multiples of 64, K of 32.
+//
+// On the tensor cores in three TF32 passes: each fp32 operand is split into two TF32
+// parts and hi*hi + hi*lo + lo*hi is accumulated in fp32 (~2^-22 relative error per
+// product, the fp32 level).  One CTA of 4 warps per 64 x 64 output tile and entry; warp w
+// owns a 32 x 32 quarter as 2 x 4 m16n8k8 tiles.  32-deep K slices of both operands come
+// into a two-stage shared-memory ring by cp.async, each in its own orientation (rows of
+// 36 floats when contiguous in k, of 72 when contiguous in m or n), which keeps every
+// fragment read free of bank conflicts.  M, N multiples of 64, K of 32 and at most 128.
 struct Mm {
   const float* A;
   long long ab;
@@ -236,93 +241,118 @@ struct Mm {
   const long long* nlive;
 };
 
-constexpr int kMmThreads = 128, kMmLd = 68;
+constexpr int kMmThreads = 128, kMmStage = 2304, kMmKMax = 128;
 
-// Slice k0..k0+31 of a 64-row operand X(r, k) = X[r*rs + k*ks_] (one stride 1) as four
-// float4 per thread, scaled by sc[k] when given.
-__device__ __forceinline__ void mm_fetch(const float* X, int rs, int ks_, int r0, int k0,
-                                         const float* sc, float4 (&v)[4]) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Slice k0..k0+31 of a 64-row operand X(r, k) = X[r*rs + k*ks_] into S: [r][36] when
+// ks_ == 1, else [k][72] (then rs == 1).
+__device__ __forceinline__ void mm_issue(float* S, const float* X, int rs, int ks_, int r0, int k0) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int idx = tid + kMmThreads * i;  // 512 float4
-    if (ks_ == 1) {                        // contiguous in k: row idx / 8, k 4 (idx % 8)
+    const int idx = threadIdx.x + kMmThreads * i;  // 512 chunks of 16 bytes
+    if (ks_ == 1) {
       const int r = idx >> 3, k = 4 * (idx & 7);
-      v[i] = *reinterpret_cast<const float4*>(X + (long long)(r0 + r) * rs + k0 + k);
-      if (sc) {
-        v[i].x *= sc[k0 + k]; v[i].y *= sc[k0 + k + 1];
-        v[i].z *= sc[k0 + k + 2]; v[i].w *= sc[k0 + k + 3];
-      }
-    } else {                               // contiguous in r: k idx / 16, rows 4 (idx % 16)
+      cp_async16(S + r * 36 + k, X + (long long)(r0 + r) * rs + k0 + k);
+    } else {
       const int k = idx >> 4, r = 4 * (idx & 15);
-      v[i] = *reinterpret_cast<const float4*>(X + (long long)(k0 + k) * ks_ + r0 + r);
-      if (sc) {
-        const float f = sc[k0 + k];
-        v[i].x *= f; v[i].y *= f; v[i].z *= f; v[i].w *= f;
-      }
+      cp_async16(S + k * 72 + r, X + (long long)(k0 + k) * ks_ + r0 + r);
     }
   }
 }
 
-// Store a fetched slice as S[k][r] (row stride kMmLd).
-__device__ __forceinline__ void mm_stash(float* S, int ks_, const float4 (&v)[4]) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = tid + kMmThreads * i;
-    if (ks_ == 1) {
-      const int r = idx >> 3, k = 4 * (idx & 7);
-      S[(k + 0) * kMmLd + r] = v[i].x;
-      S[(k + 1) * kMmLd + r] = v[i].y;
-      S[(k + 2) * kMmLd + r] = v[i].z;
-      S[(k + 3) * kMmLd + r] = v[i].w;
-    } else {
-      const int k = idx >> 4, r = 4 * (idx & 15);
-      *reinterpret_cast<float4*>(S + k * kMmLd + r) = v[i];
-    }
-  }
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+// D (16 x 8, fp32) += A (16 x 8, row) B (8 x 8, col), TF32 inputs.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
 __global__ void __launch_bounds__(kMmThreads) ck_mm_kernel(Mm p) {
   const long long b = blockIdx.x;
   if (b >= *p.nlive) return;
-  __shared__ __align__(16) float As[32 * kMmLd], Bs[32 * kMmLd];
+  __shared__ __align__(16) float sA[2][kMmStage], sB[2][kMmStage];
+  __shared__ float sK[kMmKMax];
   const int tilesN = p.N / 64;
   const int m0 = (blockIdx.y / tilesN) * 64, n0 = (blockIdx.y % tilesN) * 64;
   const float* A = p.A + b * p.ab;
   const float* B = p.B + b * p.bb;
-  const float* ks = p.ks ? p.ks + b * p.vb : nullptr;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  // A(m, k) as rows m: stride am, inner ak.  B(k, n) as rows n: stride bn, inner bk.
-  float4 va[4], vb[4];
-  mm_fetch(A, p.am, p.ak, m0, 0, nullptr, va);
-  mm_fetch(B, p.bn, p.bk, n0, 0, ks, vb);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+  const int wm = (warp >> 1) * 32, wn = (warp & 1) * 32;
+  // B(k, n) as rows n of X: stride bn, inner bk.
+  mm_issue(sA[0], A, p.am, p.ak, m0, 0);
+  mm_issue(sB[0], B, p.bn, p.bk, n0, 0);
+  cp_async_commit();
+  if (tid < p.K) sK[tid] = p.ks ? p.ks[b * p.vb + tid] : 1.f;
+  const bool akc = p.ak == 1, bkc = p.bk == 1;
   float acc[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < p.K; k0 += 32) {
-    mm_stash(As, p.ak, va);
-    mm_stash(Bs, p.bk, vb);
-    __syncthreads();
-    if (k0 + 32 < p.K) {
-      mm_fetch(A, p.am, p.ak, m0, k0 + 32, nullptr, va);
-      mm_fetch(B, p.bn, p.bk, n0, k0 + 32, ks, vb);
-    }
-#pragma unroll 8
-    for (int kk = 0; kk < 32; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(As + kk * kMmLd + 8 * ty);
-      const float4 a1 = *reinterpret_cast<const float4*>(As + kk * kMmLd + 8 * ty + 4);
-      const float4 c = *reinterpret_cast<const float4*>(Bs + kk * kMmLd + 4 * tx);
-      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float cv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], cv[j], acc[i][j]);
+  const int ns = p.K / 32;
+  for (int sl = 0; sl < ns; ++sl) {
+    if (sl + 1 < ns) {
+      mm_issue(sA[(sl + 1) & 1], A, p.am, p.ak, m0, 32 * (sl + 1));
+      mm_issue(sB[(sl + 1) & 1], B, p.bn, p.bk, n0, 32 * (sl + 1));
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
+    const float* SA = sA[sl & 1];
+    const float* SB = sB[sl & 1];
+#pragma unroll
+    for (int kb = 0; kb < 32; kb += 8) {
+      uint32_t ah[2][4], al[2][4], bh[4][2], bl[4][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int m = wm + 16 * mt + g, k = kb + t;
+        const float x0 = akc ? SA[m * 36 + k] : SA[k * 72 + m];
+        const float x1 = akc ? SA[(m + 8) * 36 + k] : SA[k * 72 + m + 8];
+        const float x2 = akc ? SA[m * 36 + k + 4] : SA[(k + 4) * 72 + m];
+        const float x3 = akc ? SA[(m + 8) * 36 + k + 4] : SA[(k + 4) * 72 + m + 8];
+        tf32_split(x0, ah[mt][0], al[mt][0]);
+        tf32_split(x1, ah[mt][1], al[mt][1]);
+        tf32_split(x2, ah[mt][2], al[mt][2]);
+        tf32_split(x3, ah[mt][3], al[mt][3]);
+      }
+      const float f0 = sK[32 * sl + kb + t], f1 = sK[32 * sl + kb + t + 4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int n = wn + 8 * nt + g, k = kb + t;
+        const float y0 = bkc ? SB[n * 36 + k] : SB[k * 72 + n];
+        const float y1 = bkc ? SB[n * 36 + k + 4] : SB[(k + 4) * 72 + n];
+        tf32_split(y0 * f0, bh[nt][0], bl[nt][0]);
+        tf32_split(y1 * f1, bh[nt][1], bl[nt][1]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          mma_tf32(acc[4 * mt + nt], al[mt], bh[nt]);
+          mma_tf32(acc[4 * mt + nt], ah[mt], bl[nt]);
+          mma_tf32(acc[4 * mt + nt], ah[mt], bh[nt]);
+        }
+    }
+    __syncthreads();  // this stage is free for slice sl + 2
   }
   const float* cs = p.cs ? p.cs + b * p.vb : nullptr;
   const float* gv = p.gv ? p.gv + b * p.vb : nullptr;
@@ -330,10 +360,11 @@ __global__ void __launch_bounds__(kMmThreads) ck_mm_kernel(Mm p) {
   float* C2 = p.C2 ? p.C2 + b * p.cb : nullptr;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int m = m0 + 8 * ty + i;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int n = n0 + 4 * tx + j;
+      // fragment element j of tile (i / 4, i % 4): rows g and g + 8, columns 2t and 2t + 1
+      const int m = m0 + wm + 16 * (i >> 2) + g + 8 * (j >> 1);
+      const int n = n0 + wn + 8 * (i & 3) + 2 * t + (j & 1);
       float x = p.alpha * acc[i][j];
       if (cs) x *= cs[n];
       if (C2) C2[(long long)m * p.cm + (long long)n * p.cn] = n <= m ? x * expf(gv[m] - gv[n]) : 0.f;
@@ -417,16 +448,6 @@ struct ChainArgs {
 template <int D>
 constexpr int chain_smem_bytes() {
   return 4 * (kRows * (D + 4) + 2 * kCk * (D + 4) + 2 * kCk + kRows * (kCk + 4));
-}
-
-__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // A [kCk][D] operand tile into shared memory rows of LD floats, as one async group;
@@ -790,7 +811,7 @@ struct MmLauncher {
   }
   void run(const Mm& m) {
     if (err != cudaSuccess) return;
-    if (m.M % 64 || m.N % 64 || m.K % 32 || (m.am != 1 && m.ak != 1) ||
+    if (m.M % 64 || m.N % 64 || m.K % 32 || m.K > kMmKMax || (m.am != 1 && m.ak != 1) ||
         (m.bk != 1 && m.bn != 1)) {
       err = cudaErrorInvalidValue;
       return;
