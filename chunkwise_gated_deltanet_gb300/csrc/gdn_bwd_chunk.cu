@@ -447,15 +447,14 @@ struct ChainArgs {
 
 template <int D>
 constexpr int chain_smem_bytes() {
-  return 4 * (kRows * (D + 4) + 2 * kCk * (D + 4) + 2 * kCk + kRows * (kCk + 4));
+  return 4 * (kRows * (D + 4) + kCk * (D + 4) + kCk * (D + 8) + 2 * kCk + kRows * (kCk + 4));
 }
 
 // A [kCk][D] operand tile into shared memory rows of LD floats, as one async group;
 // with vec, also the entry's E and e^g gate vectors (threads 0..31).
-template <int D>
+template <int D, int LD>
 __device__ __forceinline__ void chain_issue(float* dst, const float* src, float* vec,
                                             const float* gates) {
-  constexpr int LD = D + 4;
   for (int i = threadIdx.x; i < kCk * D / 4; i += 256) {
     const int c = i / (D / 4), k = 4 * (i % (D / 4));
     cp_async16(dst + c * LD + k, src + (size_t)c * D + k);
@@ -468,32 +467,38 @@ __device__ __forceinline__ void chain_issue(float* dst, const float* src, float*
   cp_async_commit();
 }
 
+// The two products on the tensor cores in three TF32 passes, like ck_mm_kernel.
+//   X1 (kCk x kRows): warp w takes rows 16 (w % 4) .. +15 and the two 8-column tiles
+//     2 (w / 4) and 2 (w / 4) + 1; A = A1 [c][k] (row stride D + 4), B(k, r) = St[r][k].
+//   St (kRows x D):  warp w takes rows 16 (w % 2) .. +15 and D / 32 8-column tiles from
+//     D / 32 * (w / 2); A(r, c) = X1t[r][c] (row stride kCk + 4), B(c, k) = A2 [c][k]
+//     (row stride D + 8).
+// The strides put the 32 lanes' fragment reads in 32 different banks.
 template <int D, bool REV>
 __global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
   extern __shared__ __align__(16) float sm[];
-  constexpr int LD = D + 4, LX = kCk + 4, NK = D / 64;
-  float* St = sm;                  // [kRows][LD]
-  float* A1 = St + kRows * LD;     // [kCk][LD]
-  float* A2 = A1 + kCk * LD;       // [kCk][LD]
-  float* Vv = A2 + kCk * LD;       // E [kCk], e^g [kCk]
-  float* X1 = Vv + 2 * kCk;        // s2_c X1(c, r) stored as [kRows][LX]
+  constexpr int LD1 = D + 4, LD2 = D + 8, LX = kCk + 4, NT = D / 32;
+  float* St = sm;                  // [kRows][LD1]
+  float* A1 = St + kRows * LD1;    // [kCk][LD1]
+  float* A2 = A1 + kCk * LD1;      // [kCk][LD2]
+  float* Vv = A2 + kCk * LD2;      // E [kCk], e^g [kCk]
+  float* X1 = Vv + 2 * kCk;        // s2_c X1(c, r) as [kRows][LX]
   const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H, r0 = blockIdx.y * kRows;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int base = p.cbase[n], nc = p.cbase[n + 1] - base;
   const size_t sidx = ((size_t)n * p.H + h) * D * D;
   auto entry = [&](int jj) { return (long long)(base + (REV ? nc - 1 - jj : jj)) * p.H + h; };
   if (nc > 0) {
     const long long b = entry(0);
-    chain_issue<D>(A1, p.a1 + (size_t)b * kCk * D, Vv, p.gates + (size_t)b * kGates * kCk);
-    chain_issue<D>(A2, p.a2 + (size_t)b * kCk * D, nullptr, nullptr);
+    chain_issue<D, LD1>(A1, p.a1 + (size_t)b * kCk * D, Vv, p.gates + (size_t)b * kGates * kCk);
+    chain_issue<D, LD2>(A2, p.a2 + (size_t)b * kCk * D, nullptr, nullptr);
   }
   for (int i = tid; i < kRows * D; i += 256) {
     const int r = i / D, k = i % D;
-    St[r * LD + k] = p.init ? p.init[sidx + (size_t)(r0 + r) * D + k] : 0.f;
+    St[r * LD1 + k] = p.init ? p.init[sidx + (size_t)(r0 + r) * D + k] : 0.f;
   }
-  const int cy = tid >> 3, rx = tid & 7;   // X1 roles: c = cy + 32 i, r = rx + 8 j
-  // St roles: rows 8 rg .. 8 rg + 7, columns kh D/2 + lane + 32 j (j < NK)
-  const int rg = (tid >> 5) & 3, kc = (tid >> 7) * (D / 2) + (tid & 31);
+  const int xm = 16 * (warp & 3), xn = 16 * (warp >> 2);      // X1 tile origin
+  const int sm0 = 16 * (warp & 1), sn = 8 * NT * (warp >> 1);  // St tile origin
   for (int jj = 0; jj < nc; ++jj) {
     const long long b = entry(jj);
     __syncthreads();  // St complete (init or the previous update)
@@ -501,109 +506,125 @@ __global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
     for (int i = tid; i < kRows * D / 4; i += 256) {
       const int r = i / (D / 4), k = 4 * (i % (D / 4));
       *reinterpret_cast<float4*>(stb + (size_t)(r0 + r) * D + k) =
-          *reinterpret_cast<const float4*>(St + r * LD + k);
+          *reinterpret_cast<const float4*>(St + r * LD1 + k);
     }
     float add1[2][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int jq = 0; jq < 4; ++jq)
-        add1[i][jq] = p.add1[(size_t)b * kCk * D + (size_t)(cy + 32 * i) * D + r0 + rx + 8 * jq];
+      for (int j = 0; j < 4; ++j) {
+        const int c = xm + g + 8 * (j >> 1), r = xn + 8 * q + 2 * t + (j & 1);
+        add1[q][j] = p.add1[(size_t)b * kCk * D + (size_t)c * D + r0 + r];
+      }
     cp_async_wait<1>();  // A1 and the gate vectors
     __syncthreads();
     {  // X1(c, r) = Add1 + s1_c sum_k A1(c, k) St(r, k)
       float acc[2][4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int jq = 0; jq < 4; ++jq) acc[i][jq] = 0.f;
-#pragma unroll 2
-      for (int k = 0; k < D; k += 4) {
-        const float4 a0 = *reinterpret_cast<const float4*>(A1 + cy * LD + k);
-        const float4 a1v = *reinterpret_cast<const float4*>(A1 + (cy + 32) * LD + k);
+        for (int j = 0; j < 4; ++j) acc[q][j] = 0.f;
+#pragma unroll 4
+      for (int kb = 0; kb < D; kb += 8) {
+        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+        const float* a = A1 + (xm + g) * LD1 + kb + t;
+        tf32_split(a[0], ah[0], al[0]);
+        tf32_split(a[8 * LD1], ah[1], al[1]);
+        tf32_split(a[4], ah[2], al[2]);
+        tf32_split(a[8 * LD1 + 4], ah[3], al[3]);
 #pragma unroll
-        for (int jq = 0; jq < 4; ++jq) {
-          const float4 sv = *reinterpret_cast<const float4*>(St + (rx + 8 * jq) * LD + k);
-          acc[0][jq] = fmaf(a0.w, sv.w, fmaf(a0.z, sv.z, fmaf(a0.y, sv.y, fmaf(a0.x, sv.x, acc[0][jq]))));
-          acc[1][jq] = fmaf(a1v.w, sv.w, fmaf(a1v.z, sv.z, fmaf(a1v.y, sv.y, fmaf(a1v.x, sv.x, acc[1][jq]))));
+        for (int q = 0; q < 2; ++q) {
+          const float* bp = St + (xn + 8 * q + g) * LD1 + kb + t;
+          tf32_split(bp[0], bh[q][0], bl[q][0]);
+          tf32_split(bp[4], bh[q][1], bl[q][1]);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          mma_tf32(acc[q], al, bh[q]);
+          mma_tf32(acc[q], ah, bl[q]);
+          mma_tf32(acc[q], ah, bh[q]);
         }
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int c = cy + 32 * i;
-        const float e = Vv[c];
-        const float s1 = REV ? e : -1.f, s2 = REV ? -1.f : e;
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int jq = 0; jq < 4; ++jq) {
-          const int r = rx + 8 * jq;
-          const float x = add1[i][jq] + s1 * acc[i][jq];
+        for (int j = 0; j < 4; ++j) {
+          const int c = xm + g + 8 * (j >> 1), r = xn + 8 * q + 2 * t + (j & 1);
+          const float e = Vv[c];
+          const float s1 = REV ? e : -1.f, s2 = REV ? -1.f : e;
+          const float x = add1[q][j] + s1 * acc[q][j];
           p.out1[(size_t)b * kCk * D + (size_t)c * D + r0 + r] = x;
           X1[r * LX + c] = s2 * x;
         }
-      }
     }
     const float gam = Vv[kCk + kCk - 1];  // e^{g_last}
-    float add2[8][NK];
+    float add2[NT][4];
     if (REV) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int q = 0; q < NT; ++q)
 #pragma unroll
-        for (int jq = 0; jq < NK; ++jq)
-          add2[i][jq] = p.add2[(size_t)b * D * D + (size_t)(r0 + 8 * rg + i) * D + kc + 32 * jq];
+        for (int j = 0; j < 4; ++j) {
+          const int r = sm0 + g + 8 * (j >> 1), k = sn + 8 * q + 2 * t + (j & 1);
+          add2[q][j] = p.add2[(size_t)b * D * D + (size_t)(r0 + r) * D + k];
+        }
     }
     __syncthreads();  // X1 complete; A1 and the gate vectors free
     if (jj + 1 < nc) {
       const long long bn = entry(jj + 1);
-      chain_issue<D>(A1, p.a1 + (size_t)bn * kCk * D, Vv, p.gates + (size_t)bn * kGates * kCk);
+      chain_issue<D, LD1>(A1, p.a1 + (size_t)bn * kCk * D, Vv, p.gates + (size_t)bn * kGates * kCk);
       cp_async_wait<1>();  // A2 of this chunk
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
     {  // St(r, k) = Add2 + Gamma St(r, k) + sum_c s2_c X1(c, r) A2(c, k)
-      float acc[8][NK];
+      float acc[NT][4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int q = 0; q < NT; ++q)
 #pragma unroll
-        for (int jq = 0; jq < NK; ++jq) acc[i][jq] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[q][j] = 0.f;
 #pragma unroll 2
-      for (int c = 0; c < kCk; c += 4) {
-        float a[4][NK];
+      for (int kb = 0; kb < kCk; kb += 8) {
+        uint32_t ah[4], al[4], bh[NT][2], bl[NT][2];
+        const float* a = X1 + (sm0 + g) * LX + kb + t;
+        tf32_split(a[0], ah[0], al[0]);
+        tf32_split(a[8 * LX], ah[1], al[1]);
+        tf32_split(a[4], ah[2], al[2]);
+        tf32_split(a[8 * LX + 4], ah[3], al[3]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int q = 0; q < NT; ++q) {
+          const float* bp = A2 + (kb + t) * LD2 + sn + 8 * q + g;
+          tf32_split(bp[0], bh[q][0], bl[q][0]);
+          tf32_split(bp[4 * LD2], bh[q][1], bl[q][1]);
+        }
 #pragma unroll
-          for (int jq = 0; jq < NK; ++jq) a[u][jq] = A2[(c + u) * LD + kc + 32 * jq];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 x = *reinterpret_cast<const float4*>(X1 + (8 * rg + i) * LX + c);
-#pragma unroll
-          for (int jq = 0; jq < NK; ++jq)
-            acc[i][jq] = fmaf(x.w, a[3][jq], fmaf(x.z, a[2][jq], fmaf(x.y, a[1][jq], fmaf(x.x, a[0][jq], acc[i][jq]))));
+        for (int q = 0; q < NT; ++q) {
+          mma_tf32(acc[q], al, bh[q]);
+          mma_tf32(acc[q], ah, bl[q]);
+          mma_tf32(acc[q], ah, bh[q]);
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 8 * rg + i;
+      for (int q = 0; q < NT; ++q)
 #pragma unroll
-        for (int jq = 0; jq < NK; ++jq) {
-          const int k = kc + 32 * jq;
-          float v = fmaf(gam, St[r * LD + k], acc[i][jq]);
-          if (REV) v += add2[i][jq];
-          St[r * LD + k] = v;
+        for (int j = 0; j < 4; ++j) {
+          const int r = sm0 + g + 8 * (j >> 1), k = sn + 8 * q + 2 * t + (j & 1);
+          float v = fmaf(gam, St[r * LD1 + k], acc[q][j]);
+          if (REV) v += add2[q][j];
+          St[r * LD1 + k] = v;
         }
-      }
     }
     __syncthreads();  // A2 free
     if (jj + 1 < nc) {
       const long long bn = entry(jj + 1);
-      chain_issue<D>(A2, p.a2 + (size_t)bn * kCk * D, nullptr, nullptr);
+      chain_issue<D, LD2>(A2, p.a2 + (size_t)bn * kCk * D, nullptr, nullptr);
     }
   }
   __syncthreads();
   if (p.fin)
     for (int i = tid; i < kRows * D; i += 256) {
       const int r = i / D, k = i % D;
-      p.fin[sidx + (size_t)(r0 + r) * D + k] = St[r * LD + k];
+      p.fin[sidx + (size_t)(r0 + r) * D + k] = St[r * LD1 + k];
     }
 }
 
