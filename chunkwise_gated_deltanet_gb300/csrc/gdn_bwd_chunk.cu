@@ -26,11 +26,14 @@
 // log alpha = 0, which adds nothing to any sum).  The two serial parts, the chunk-start
 // states S_j (forward) and the chunk-end state gradients dS'_j (reverse), run in one
 // chain kernel that splits the dv rows of the state over CTAs: rows are independent
-// given the chunk's operands.  Everything else is chunk-parallel: a batched fp32 GEMM
+// given the chunk's operands.  Everything else is chunk-parallel: a batched GEMM
 // (64 x 64 output tiles, one per CTA and batch entry) and small per-chunk kernels for
 // the triangular solve, the gate terms and the final per-token sums.
 //
-// fp32 arithmetic throughout (CUDA cores).  Head sizes dk = dv = 64 or 128.
+// Accuracy is fp32's: the products (batched GEMM and both chain products) run on the
+// tensor cores in three TF32 passes (hi*hi + hi*lo + lo*hi of a two-part TF32 split of
+// each fp32 operand, accumulated in fp32: ~2^-22 relative error per product); the rest is
+// fp32 on the CUDA cores.  Head sizes dk = dv = 64 or 128.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

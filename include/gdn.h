@@ -149,8 +149,10 @@ int gdn_bwd_select_path(int dk, int dv, int qkv_dtype);
 
 /*
  * gdn_chunk_bwd_ex -- gdn_chunk_bwd on a chosen path (gdn_bwd_path).  Both paths compute
- * the same derivative in fp32 arithmetic and are deterministic; they differ in summation
- * order only.  The chunked path is the derivative of the chunk form (Nyysyyan,
+ * the same derivative to fp32 accuracy and are deterministic: the per-token path in fp32
+ * on the CUDA cores, the chunked path with its products on the tensor cores in three TF32
+ * passes (a two-part TF32 split of each fp32 operand, hi*hi + hi*lo + lo*hi accumulated in
+ * fp32, ~2^-22 relative error per product).  The chunked path is the derivative of the chunk form (Nyysyyan,
  * "Gated-DeltaNet", WY representation and chunkwise algorithm): per chunk, with T the
  * inverse of the chunk's unit lower-triangular WY matrix, W~ = T diag(beta e^g) K and
  * U = T diag(beta) V,
