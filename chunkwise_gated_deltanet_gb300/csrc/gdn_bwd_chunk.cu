@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "gdn_internal.h"
 
@@ -845,6 +846,32 @@ struct MmLauncher {
   }
 };
 
+// A second stream per device for the products that do not depend on a chain, with the
+// events of the fork and the joins.  Created on first use; the launch sequence that uses
+// them runs under g_side_mu.
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, yz = nullptr, fwd = nullptr, side = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream(SideStream*& out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStream& x = g_side[dev];
+  if (!x.st) {
+    if ((e = cudaStreamCreateWithFlags(&x.st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    for (cudaEvent_t* ev : {&x.fork, &x.yz, &x.fwd, &x.side})
+      if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  out = &x;
+  return cudaSuccess;
+}
+
 template <int D, typename TIn>
 cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.B * a.T;
@@ -889,6 +916,23 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   TsolveArgs ta{KK, QK, gates, Tm, P, nlive};
   ck_tsolve_kernel<<<nb, 128, 0, s>>>(ta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // Fork: the side stream takes P^T dO and dO^T diag(e^g) Q (they need the solve's P and
+  // the gathered tiles only) while this stream makes W~, U and the forward chain.
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* side = nullptr;
+  if ((e = side_stream(side)) != cudaSuccess) return e;
+  cudaStream_t s2 = side->st;
+  if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(s2, side->fork, 0)) != cudaSuccess) return e;
+  MmLauncher mm2{L.nb, nlive, s2};
+  {  // Y = P^T dO,  Z = dO^T diag(e^g) Q
+    mm2.run(mm2.make(P, CC, 1, kCk, dOc, CD, D, 1, Y, CD, D, 1, kCk, D, kCk));
+    Mm m = mm2.make(dOc, CD, 1, D, Qc, CD, D, 1, Z, DD, D, 1, D, D, kCk);
+    m.ks = gates + G_EG * kCk;
+    mm2.run(m);
+  }
+  if (mm2.err != cudaSuccess) return mm2.err;
+  if ((e = cudaEventRecord(side->yz, s2)) != cudaSuccess) return e;
   {  // W~ = T diag(beta e^g) K,  U = T diag(beta) V
     Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
     m.ks = gates + G_BEG * kCk;
@@ -911,13 +955,25 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   ck_chain_kernel<D, false><<<cgrid, 256, smem, s>>>(cf);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  {  // Y = P^T dO,  Z = dO^T diag(e^g) Q
-    mm.run(mm.make(P, CC, 1, kCk, dOc, CD, D, 1, Y, CD, D, 1, kCk, D, kCk));
-    Mm m = mm.make(dOc, CD, 1, D, Qc, CD, D, 1, Z, DD, D, 1, D, D, kCk);
-    m.ks = gates + G_EG * kCk;
-    mm.run(m);
+  // The side stream continues with the products of delta and S (dO delta^T, (dP o D) K,
+  // (dP o D)^T Q, dO S) while this stream runs the reverse chain.
+  if ((e = cudaEventRecord(side->fwd, s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(s2, side->fwd, 0)) != cudaSuccess) return e;
+  {
+    // dP = lower(dO delta^T), and dP o D
+    Mm m = mm2.make(dOc, CD, D, 1, Dl, CD, 1, D, dPm, CC, kCk, 1, kCk, kCk, D);
+    m.mask = 1;
+    m.C2 = dPD;
+    m.gv = gates + G_G * kCk;
+    mm2.run(m);
+    // (dP o D) K, (dP o D)^T Q, dO S
+    mm2.run(mm2.make(dPD, CC, kCk, 1, Kc, CD, D, 1, dQa, CD, D, 1, kCk, D, kCk));
+    mm2.run(mm2.make(dPD, CC, 1, kCk, Qc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk));
+    mm2.run(mm2.make(dOc, CD, D, 1, S, DD, D, 1, dOS, CD, D, 1, kCk, D, D));
   }
-  if (mm.err != cudaSuccess) return mm.err;
+  if (mm2.err != cudaSuccess) return mm2.err;
+  if ((e = cudaEventRecord(side->side, s2)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(s, side->yz, 0)) != cudaSuccess) return e;
   ChainArgs cr;
   cr.cbase = cbase; cr.init = a.dS_final; cr.fin = a.dS0; cr.st = dSn;
   cr.add1 = Y; cr.a1 = Kc; cr.a2 = Wt; cr.add2 = Z; cr.out1 = dDl;
@@ -926,18 +982,8 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   {
-    // dP = lower(dO delta^T), and dP o D
-    Mm m = mm.make(dOc, CD, D, 1, Dl, CD, 1, D, dPm, CC, kCk, 1, kCk, kCk, D);
-    m.mask = 1;
-    m.C2 = dPD;
-    m.gv = gates + G_G * kCk;
-    mm.run(m);
-    // (dP o D) K, (dP o D)^T Q
-    mm.run(mm.make(dPD, CC, kCk, 1, Kc, CD, D, 1, dQa, CD, D, 1, kCk, D, kCk));
-    mm.run(mm.make(dPD, CC, 1, kCk, Qc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk));
-    // dO S, dW = -d delta S, delta dS'
-    mm.run(mm.make(dOc, CD, D, 1, S, DD, D, 1, dOS, CD, D, 1, kCk, D, D));
-    m = mm.make(dDl, CD, D, 1, S, DD, D, 1, dW, CD, D, 1, kCk, D, D);
+    // dW = -d delta S, delta dS'
+    Mm m = mm.make(dDl, CD, D, 1, S, DD, D, 1, dW, CD, D, 1, kCk, D, D);
     m.alpha = -1.f;
     mm.run(m);
     mm.run(mm.make(Dl, CD, D, 1, dSn, DD, D, 1, Rd, CD, D, 1, kCk, D, D));
@@ -964,6 +1010,8 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   float* db3 = F(L.db3);
   float* dg1 = F(L.dg1);
   float* sdot = F(L.sdot);
+  // Join: the dA terms need dP, and dK accumulates onto (dP o D)^T Q.
+  if ((e = cudaStreamWaitEvent(s, side->side, 0)) != cudaSuccess) return e;
   DaArgs da{dA, KK, QK, dPm, gates, X, db3, dg1, nlive};
   ck_da_kernel<<<nb, 256, 0, s>>>(da);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
