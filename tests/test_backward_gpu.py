@@ -31,12 +31,12 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def _gpu(inp, grads, with_S0_grad=True, with_dSf=True):
+def _gpu(inp, grads, with_S0_grad=True, with_dSf=True, path=gdn.GDN_BWD_AUTO):
     d = to_device(inp)
     g = to_device(grads)
     res = gdn.chunk_bwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], g["d_out"],
                         g["dS_final"] if with_dSf else None, d["cu_seqlens"],
-                        want_dS0=with_S0_grad)
+                        want_dS0=with_S0_grad, path=path)
     gdn.gdn_check_status()
     torch.cuda.synchronize()
     return [None if x is None else x.float().cpu().numpy().astype(np.float64) for x in res]
@@ -172,3 +172,22 @@ def test_autograd_function_matches_oracle(dtype):
     ref = _oracle(inp, grads)
     # the autograd loss multiplies by the bf16 d_out widened to fp32: the same values
     _compare(got, ref, dtype == "bf16")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_backward_tokens_path_at_chunked_head_sizes(d, dtype):
+    """d = 64 and 128 take the chunked path by default; the per-token path stays
+    selectable there (GDN_BWD_TOKENS) and must meet the same bound, packed batches
+    included."""
+    w = dataclasses.replace(W["gdn_f32_b2h4t1024d64c64"], dk=d, dv=d, dtype=dtype)
+    inp = workloads.make_inputs(w, B=2, H=2, T=77, seed=d + 5)
+    grads = workloads.make_grad_inputs(inp, seed=d + 6)
+    _compare(_gpu(inp, grads, path=gdn.GDN_BWD_TOKENS), _oracle(inp, grads), dtype == "bf16")
+    lens = [40, 0, 75]
+    inp = workloads.make_inputs(w, B=1, H=2, T=sum(lens), seed=d + 7)
+    inp["cu_seqlens"] = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    inp["N"] = len(lens)
+    inp["S0"] = None
+    grads = workloads.make_grad_inputs(inp, seed=d + 8)
+    _compare(_gpu(inp, grads, path=gdn.GDN_BWD_TOKENS), _oracle(inp, grads), dtype == "bf16")
