@@ -100,8 +100,11 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v,
  *   dlog_alpha_t = a_t (<G, S_{t-1}> - beta_t du . S_{t-1} k_t);
  *   dk_t = G^T u_t - beta_t a_t S_{t-1}^T du   (u_t = beta_t (v_t - a_t S_{t-1} k_t));
  *   G <- a_t G (I - beta_t k_t k_t^T);   dS0 = G at the start
- * (a_t = exp(log_alpha_t)).  States are recomputed from checkpoints every 8 tokens
- * kept in `workspace`; fp32 arithmetic on CUDA cores; deterministic.
+ * (a_t = exp(log_alpha_t)).  The kernels are those gdn_bwd_select_path names: for
+ * dk = dv = 64 or 128 the chunked path (the same derivative in the chunk form, see
+ * gdn_chunk_bwd_ex), otherwise the per-token path, which walks this recurrence with the
+ * states recomputed from checkpoints every 8 tokens kept in `workspace`, in fp32 on the
+ * CUDA cores.  Both are deterministic.
  *
  * q, k, v, log_alpha, beta, S0, B, H, T, dk, dv, cu_seqlens, N_seqs, qkv_dtype: as
  *            passed to gdn_chunk_fwd (S0 NULL = zeros)
