@@ -186,3 +186,28 @@ def test_chunk_form_pin_catches_planted_mistake(kind):
     ref = BW.gdn_sequence_bwd(*args, dO, dSf)
     got = ns["chunked_wy_delta_bwd"](*args, dO, dSf, 16)
     assert not all(np.allclose(g, r, rtol=1e-9, atol=1e-11) for g, r in zip(got, ref))
+
+
+@pytest.mark.parametrize("L,C", [(37, 16), (65, 64), (1, 64)])
+def test_zero_padded_tail_changes_no_gradient(L, C):
+    """A ragged last chunk can be filled out to C tokens with q = k = v = dO = 0, beta = 0
+    and log alpha = 0 (alpha = 1): such tokens leave the state unchanged (the erase and
+    the write vanish with beta = 0, the gate with alpha = 1) and add nothing to any output,
+    so the real tokens' gradients and dS0 are those of the unpadded sequence; the chunk
+    form then works on whole chunks only (the chunked backward kernels rely on this).
+    Checked on the chunk-form derivative itself."""
+    from oracle import derivations as D
+    args, dO, dSf = _rand(L, 6, 5, 300 + L)
+    pad = (-L) % C
+    padded = [np.concatenate([x, np.zeros((pad,) + x.shape[1:])]) for x in args[:5]] + [args[5]]
+    dOp = np.concatenate([dO, np.zeros((pad, dO.shape[1]))])
+    ref = D.chunked_wy_delta_bwd(*args, dO, dSf, C)
+    got = D.chunked_wy_delta_bwd(*padded, dOp, dSf, C)
+    for name, g, r in zip(("dq", "dk", "dv", "dla", "dbeta"), got[:5], ref[:5]):
+        assert np.allclose(g[:L], r, rtol=1e-10, atol=1e-12), (name, np.abs(g[:L] - r).max())
+    assert np.allclose(got[5], ref[5], rtol=1e-10, atol=1e-12)
+    # the padding tokens' own dq, dk, dv, dbeta are 0 (their d log alpha is <G, S>, which
+    # the padding does not use: those rows are never returned)
+    per_token = BW.gdn_sequence_bwd(*padded, dOp, dSf)
+    for j in (0, 1, 2, 4):
+        assert np.abs(per_token[j][L:]).max() <= 1e-12, j
