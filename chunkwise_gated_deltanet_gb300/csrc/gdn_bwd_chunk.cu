@@ -380,9 +380,10 @@ __global__ void __launch_bounds__(kMmThreads) ck_mm_kernel(Mm p) {
 }
 
 // ---------------------------------------------------------------------------------
-// Per (chunk, head): A = strictly-lower(beta_i KK^T_ij D_ij), T = (I + A)^{-1} by
-// forward substitution (T_i = e_i - sum_{j<i} A_ij T_j), and P = lower(QK^T o D).
-// Thread c < 64 owns column c of T.
+// Per (chunk, head): A = strictly-lower(beta_i KK^T_ij D_ij), T = (I + A)^{-1}, and
+// P = lower(QK^T o D).  T in 16 x 16 blocks: the diagonal blocks by forward substitution
+// (one thread per column), then block rows in order from (I + A) T = I:
+// T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
 struct TsolveArgs {
   const float *KK, *QK, *gates;
   float *T, *P;
@@ -392,7 +393,7 @@ struct TsolveArgs {
 __global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
   const long long b = blockIdx.x;
   if (b >= *p.nlive) return;
-  __shared__ float As[kCk][kCk + 1], Ts[kCk][kCk + 1], g[kCk], be[kCk];
+  __shared__ float As[kCk][kCk + 1], Ts[kCk][kCk + 1], Wb[3 * 256], g[kCk], be[kCk];
   const int tid = threadIdx.x;
   const float* G = p.gates + (size_t)b * kGates * kCk;
   if (tid < kCk) {
@@ -407,25 +408,41 @@ __global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
     As[i][j] = j < i ? be[i] * p.KK[ob + idx] * Dij : 0.f;
     p.P[ob + idx] = p.QK[ob + idx] * Dij;
   }
+  for (int idx = tid; idx < kCk * kCk; idx += 128) Ts[idx >> 6][idx & 63] = 0.f;
   __syncthreads();
+  // Diagonal 16 x 16 blocks: T_ii = (I + A_ii)^{-1}, one thread per column of a block.
   if (tid < kCk) {
-    const int c = tid;
-    for (int i = 0; i < c; ++i) Ts[i][c] = 0.f;
-    Ts[c][c] = 1.f;
-    for (int i = c + 1; i < kCk; ++i) {
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    const int o = tid & ~15, c = tid & 15;
+    Ts[o + c][o + c] = 1.f;
+    for (int r = c + 1; r < 16; ++r) {
+      float s0 = 0.f, s1 = 0.f;
       int j = c;
-      for (; j + 3 < i; j += 4) {
-        s0 = fmaf(As[i][j], Ts[j][c], s0);
-        s1 = fmaf(As[i][j + 1], Ts[j + 1][c], s1);
-        s2 = fmaf(As[i][j + 2], Ts[j + 2][c], s2);
-        s3 = fmaf(As[i][j + 3], Ts[j + 3][c], s3);
+      for (; j + 1 < r; j += 2) {
+        s0 = fmaf(As[o + r][o + j], Ts[o + j][o + c], s0);
+        s1 = fmaf(As[o + r][o + j + 1], Ts[o + j + 1][o + c], s1);
       }
-      for (; j < i; ++j) s0 = fmaf(As[i][j], Ts[j][c], s0);
-      Ts[i][c] = -((s0 + s1) + (s2 + s3));
+      if (j < r) s0 = fmaf(As[o + r][o + j], Ts[o + j][o + c], s0);
+      Ts[o + r][o + c] = -(s0 + s1);
     }
   }
   __syncthreads();
+  // Block rows below, in order: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj  (j < i).
+  for (int bi = 1; bi < kCk / 16; ++bi) {
+    for (int e = tid; e < bi * 256; e += 128) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      float acc = 0.f;
+      for (int k = 16 * j; k < 16 * bi; ++k) acc = fmaf(As[16 * bi + r][k], Ts[k][16 * j + c], acc);
+      Wb[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < bi * 256; e += 128) {
+      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      float acc = 0.f;
+      for (int m = 0; m <= r; ++m) acc = fmaf(Ts[16 * bi + r][16 * bi + m], Wb[(j << 8) + (m << 4) + c], acc);
+      Ts[16 * bi + r][16 * j + c] = -acc;
+    }
+    __syncthreads();
+  }
   for (int idx = tid; idx < kCk * kCk; idx += 128) p.T[ob + idx] = Ts[idx >> 6][idx & 63];
 }
 
