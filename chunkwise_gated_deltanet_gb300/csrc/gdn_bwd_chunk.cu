@@ -52,21 +52,32 @@ constexpr float kLogAlphaMin = -80.f;  // alpha = 0 (log alpha = -inf) is taken 
 // Per-batch-entry gate vectors, each kCk long.
 enum { G_BETA = 0, G_G = 1, G_EG = 2, G_E = 3, G_BEG = 4, kGates = 5 };
 
+// Four consecutive elements (8- or 16-byte aligned) as fp32, and back.
 template <typename T>
-__device__ __forceinline__ float to_f(T x);
+__device__ __forceinline__ float4 load4(const T* p);
 template <>
-__device__ __forceinline__ float to_f<float>(float x) { return x; }
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
 template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
 }
 template <typename T>
-__device__ __forceinline__ T from_f(float x);
+__device__ __forceinline__ void store4(T* p, float4 v);
 template <>
-__device__ __forceinline__ float from_f<float>(float x) { return x; }
+__device__ __forceinline__ void store4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
 template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
-  return __float2bfloat16_rn(x);
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 w;
+  w.x = *reinterpret_cast<const unsigned*>(&a);
+  w.y = *reinterpret_cast<const unsigned*>(&b);
+  *reinterpret_cast<uint2*>(p) = w;
 }
 
 // ---------------------------------------------------------------------------------
@@ -162,20 +173,21 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
   const TIn* v = reinterpret_cast<const TIn*>(p.v);
   const TIn* dO = reinterpret_cast<const TIn*>(p.dout);
   const size_t ob = (size_t)b * kCk * D;
-  for (int i = threadIdx.x; i < kCk * D; i += 256) {
-    const int c = i / D, x = i % D;
-    float qv = 0.f, kv = 0.f, vv = 0.f, ov = 0.f;
+  for (int i = threadIdx.x; i < kCk * D / 4; i += 256) {
+    const int c = i / (D / 4), x = 4 * (i % (D / 4));
+    float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv, vv = qv, ov = qv;
     if (c < len) {
       const size_t o = ((size_t)(row0 + c) * p.H + h) * D + x;
-      qv = to_f(q[o]);
-      kv = to_f(k[o]);
-      vv = to_f(v[o]);
-      ov = to_f(dO[o]);
+      qv = load4(q + o);
+      kv = load4(k + o);
+      vv = load4(v + o);
+      ov = load4(dO + o);
     }
-    p.Qc[ob + i] = qv;
-    p.Kc[ob + i] = kv;
-    p.Vc[ob + i] = vv;
-    p.dOc[ob + i] = ov;
+    const size_t d = ob + (size_t)c * D + x;
+    store4(p.Qc + d, qv);
+    store4(p.Kc + d, kv);
+    store4(p.Vc + d, vv);
+    store4(p.dOc + d, ov);
   }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x, c0 = 2 * lane, c1 = c0 + 1;
@@ -734,7 +746,6 @@ template <int D, typename TIn>
 __global__ void __launch_bounds__(256) ck_scatter_kernel(ScatterArgs p) {
   const long long b = blockIdx.x;
   if (b >= *p.nlive) return;
-  constexpr int NQ = D / 32;
   __shared__ float sdg[kCk], sdE[kCk];
   const long long cid = b / p.H;
   const int h = (int)(b - cid * p.H);
@@ -748,22 +759,26 @@ __global__ void __launch_bounds__(256) ck_scatter_kernel(ScatterArgs p) {
   for (int c = w; c < kCk; c += 8) {
     const float eg = G[G_EG * kCk + c], E = G[G_E * kCk + c];
     const float be = G[G_BETA * kCk + c], beg = G[G_BEG * kCk + c];
-    const size_t o = ((size_t)b * kCk + c) * D;
-    const size_t ot = ((size_t)(row0 + c) * p.H + h) * D;
+    const size_t o = ((size_t)b * kCk + c) * D + 4 * lane;  // lane: columns 4 lane .. + 3
+    const size_t ot = ((size_t)(row0 + c) * p.H + h) * D + 4 * lane;
     float d1 = 0.f, d2 = 0.f, d3 = 0.f, d4 = 0.f;
-#pragma unroll
-    for (int qq = 0; qq < NQ; ++qq) {
-      const int x = lane + 32 * qq;
-      const float dos = p.dOS[o + x], qv = p.Qc[o + x], kv = p.Kc[o + x];
-      const float rd = p.Rd[o + x], tdw = p.TdW[o + x], tdu = p.TdU[o + x], vv = p.Vc[o + x];
-      d1 = fmaf(tdu, vv, d1);
-      d2 = fmaf(tdw, kv, d2);
-      d3 = fmaf(dos, qv, d3);
-      d4 = fmaf(rd, kv, d4);
+    if (4 * lane < D) {
+      const float4 dos = load4(p.dOS + o), qv = load4(p.Qc + o), kv = load4(p.Kc + o);
+      const float4 rd = load4(p.Rd + o), tdw = load4(p.TdW + o), tdu = load4(p.TdU + o);
+      const float4 vv = load4(p.Vc + o);
+      d1 = tdu.x * vv.x + tdu.y * vv.y + tdu.z * vv.z + tdu.w * vv.w;
+      d2 = tdw.x * kv.x + tdw.y * kv.y + tdw.z * kv.z + tdw.w * kv.w;
+      d3 = dos.x * qv.x + dos.y * qv.y + dos.z * qv.z + dos.w * qv.w;
+      d4 = rd.x * kv.x + rd.y * kv.y + rd.z * kv.z + rd.w * kv.w;
       if (c < len) {
-        dq[ot + x] = from_f<TIn>(fmaf(eg, dos, p.dQa[o + x]));
-        dk[ot + x] = from_f<TIn>(fmaf(beg, tdw, fmaf(E, rd, p.dKa[o + x])));
-        dv[ot + x] = from_f<TIn>(be * tdu);
+        const float4 qa = load4(p.dQa + o), ka = load4(p.dKa + o);
+        store4(dq + ot, make_float4(fmaf(eg, dos.x, qa.x), fmaf(eg, dos.y, qa.y),
+                                    fmaf(eg, dos.z, qa.z), fmaf(eg, dos.w, qa.w)));
+        store4(dk + ot, make_float4(fmaf(beg, tdw.x, fmaf(E, rd.x, ka.x)),
+                                    fmaf(beg, tdw.y, fmaf(E, rd.y, ka.y)),
+                                    fmaf(beg, tdw.z, fmaf(E, rd.z, ka.z)),
+                                    fmaf(beg, tdw.w, fmaf(E, rd.w, ka.w))));
+        store4(dv + ot, make_float4(be * tdu.x, be * tdu.y, be * tdu.z, be * tdu.w));
       }
     }
 #pragma unroll
