@@ -18,7 +18,8 @@ KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
     ["--workload", "linear_bf16_b4h16t4096d128c64", "--ref-budget", "1"],
     ["--workload", "decode_f32_n64h8d64"],
     ["--bwd", "--workload", "gdn_f32_b2h4t1024d64c64", "--ref-budget", "1"],
-], ids=["forward", "linear", "decode", "backward"])
+    ["--bwd", "--bwd-path", "tokens", "--workload", "gdn_f32_b2h4t1024d64c64", "--ref-budget", "1"],
+], ids=["forward", "linear", "decode", "backward", "backward-tokens-path"])
 def test_reference_arm_prints_one_contract_line(args):
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
            "--steps", "1", "--warmup", "0"] + args
