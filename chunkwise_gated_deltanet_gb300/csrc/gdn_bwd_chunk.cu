@@ -100,8 +100,12 @@ ck_table_kernel(const int32_t* __restrict__ cu, int N, int T, int H, long long n
     int len = 0;
     if (n < N) {
       if (cu) {
-        start = cu[n];
-        len = cu[n + 1] - cu[n];
+        // offsets clamped to [0, T] (T is the packed token count), as the forward does,
+        // so that no chunk of a malformed offset table reaches outside the tensors
+        const long long a = min(max((long long)cu[n], 0LL), (long long)T);
+        const long long b = min(max((long long)cu[n + 1], a), (long long)T);
+        start = a;
+        len = (int)(b - a);
       } else {
         start = (long long)n * T;
         len = T;
@@ -904,6 +908,19 @@ cudaError_t side_stream(SideStream*& out) {
   return cudaSuccess;
 }
 
+// Orders the caller's stream after everything queued on the side stream when a launch
+// sequence leaves early (an error after the fork); the normal path joins explicitly and
+// sets `done`.
+struct SideJoin {
+  SideStream* side;
+  cudaStream_t s2, s;
+  bool done = false;
+  ~SideJoin() {
+    if (done) return;
+    if (cudaEventRecord(side->side, s2) == cudaSuccess) (void)cudaStreamWaitEvent(s, side->side, 0);
+  }
+};
+
 template <int D, typename TIn>
 cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.B * a.T;
@@ -948,6 +965,12 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   TsolveArgs ta{KK, QK, gates, Tm, P, nlive};
   ck_tsolve_kernel<<<nb, 128, 0, s>>>(ta);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // The chain kernels' shared-memory caps are raised before the fork, so that this
+  // per-device first-call step cannot fail while side-stream work is in flight.
+  constexpr int smem = chain_smem_bytes<D>();
+  static std::atomic<unsigned long long> set_f{0}, set_r{0};
+  if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, smem, set_f)) != cudaSuccess) return e;
+  if ((e = ensure_smem_cap(ck_chain_kernel<D, true>, smem, set_r)) != cudaSuccess) return e;
   // Fork: the side stream takes P^T dO and dO^T diag(e^g) Q (they need the solve's P and
   // the gathered tiles only) while this stream makes W~, U and the forward chain.
   std::lock_guard<std::mutex> lock(g_side_mu);
@@ -956,6 +979,10 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   cudaStream_t s2 = side->st;
   if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return e;
   if ((e = cudaStreamWaitEvent(s2, side->fork, 0)) != cudaSuccess) return e;
+  // Every exit from here on, the error returns included, leaves the caller's stream
+  // ordered after all side-stream work: the caller may free the workspace as soon as
+  // its own stream has passed this call.
+  SideJoin join{side, s2, s};
   MmLauncher mm2{L.nb, nlive, s2};
   {  // Y = P^T dO,  Z = dO^T diag(e^g) Q
     mm2.run(mm2.make(P, CC, 1, kCk, dOc, CD, D, 1, Y, CD, D, 1, kCk, D, kCk));
@@ -975,10 +1002,6 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   }
   if (mm.err != cudaSuccess) return mm.err;
 
-  constexpr int smem = chain_smem_bytes<D>();
-  static std::atomic<unsigned long long> set_f{0}, set_r{0};
-  if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, smem, set_f)) != cudaSuccess) return e;
-  if ((e = ensure_smem_cap(ck_chain_kernel<D, true>, smem, set_r)) != cudaSuccess) return e;
   const dim3 cgrid((unsigned)((long long)a.N * a.H), D / kRows);
   ChainArgs cf;
   cf.cbase = cbase; cf.init = a.S0; cf.fin = nullptr; cf.st = S;
@@ -1044,6 +1067,7 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   float* sdot = F(L.sdot);
   // Join: the dA terms need dP, and dK accumulates onto (dP o D)^T Q.
   if ((e = cudaStreamWaitEvent(s, side->side, 0)) != cudaSuccess) return e;
+  join.done = true;
   DaArgs da{dA, KK, QK, dPm, gates, X, db3, dg1, nlive};
   ck_da_kernel<<<nb, 256, 0, s>>>(da);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

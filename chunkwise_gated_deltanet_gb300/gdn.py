@@ -142,14 +142,17 @@ def _chunk_call(entry: str, q, k, v, log_alpha, beta, S0, out, S_final, C: int,
     n_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
     s = ctypes.c_void_p((stream if stream is not None
                          else torch.cuda.current_stream(v.device)).cuda_stream)
-    if entry == "gdn_chunk_fwd":
-        st = lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-                               _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
-                               _ptr(cu_seqlens), n_seqs, code, s)
-    else:
-        st = lib.gdn_linear_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(S0),
-                                      _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
-                                      _ptr(cu_seqlens), n_seqs, code, s)
+    # the library resolves tensor maps, per-device state and streams on the current
+    # device, which must be the tensors' device
+    with torch.cuda.device(v.device):
+        if entry == "gdn_chunk_fwd":
+            st = lib.gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                   _ptr(S0), _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
+                                   _ptr(cu_seqlens), n_seqs, code, s)
+        else:
+            st = lib.gdn_linear_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(S0),
+                                          _ptr(out), _ptr(S_final), B, H, T, dk, dv, C,
+                                          _ptr(cu_seqlens), n_seqs, code, s)
     _check(st)
 
 
@@ -306,8 +309,10 @@ def gdn_decode_step(q, k, v, log_alpha, beta, S, out,
         if t.dtype != torch.float32:
             raise TypeError(f"{name} must be float32")
     s = stream if stream is not None else torch.cuda.current_stream(v.device)
-    _check(lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
-                               _ptr(out), N, H, dk, dv, code, ctypes.c_void_p(s.cuda_stream)))
+    with torch.cuda.device(v.device):
+        st = lib.gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S),
+                                 _ptr(out), N, H, dk, dv, code, ctypes.c_void_p(s.cuda_stream))
+    _check(st)
 
 
 def decode_step(q, k, v, log_alpha, beta, S, pieces: int = 4) -> torch.Tensor:
@@ -356,8 +361,10 @@ def gdn_state_fold(S_in, M, L, S_out, stream: Optional[torch.cuda.Stream] = None
         if t is not None and t.numel() != units * dv * dk:
             raise ValueError(f"gdn_state_fold: {name} does not hold one state per unit")
     s = stream if stream is not None else torch.cuda.current_stream(L.device)
-    _check(lib.gdn_state_fold(_ptr(S_in), _ptr(M), _ptr(L), count, _ptr(S_out), units, dv, dk,
-                              ctypes.c_void_p(s.cuda_stream)))
+    with torch.cuda.device(L.device):
+        st = lib.gdn_state_fold(_ptr(S_in), _ptr(M), _ptr(L), count, _ptr(S_out), units, dv, dk,
+                                ctypes.c_void_p(s.cuda_stream))
+    _check(st)
 
 
 def gdn_chunk_bwd_workspace_bytes(B: int, H: int, T: int, dk: int, dv: int, n_seqs: int) -> int:
@@ -398,12 +405,14 @@ def gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, 
     n_seqs = B if cu_seqlens is None else cu_seqlens.numel() - 1
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     s = stream if stream is not None else torch.cuda.current_stream(v.device)
-    _check(lib.gdn_chunk_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
-                                _ptr(S0), _ptr(d_out), _ptr(dS_final), _ptr(d_q), _ptr(d_k),
-                                _ptr(d_v), _ptr(d_log_alpha), _ptr(d_beta), _ptr(d_S0),
-                                _ptr(workspace), ws_bytes, B, H, T, dk, dv, _ptr(cu_seqlens),
-                                0 if cu_seqlens is None else n_seqs, code, int(path),
-                                ctypes.c_void_p(s.cuda_stream)))
+    with torch.cuda.device(v.device):
+        st = lib.gdn_chunk_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                  _ptr(S0), _ptr(d_out), _ptr(dS_final), _ptr(d_q), _ptr(d_k),
+                                  _ptr(d_v), _ptr(d_log_alpha), _ptr(d_beta), _ptr(d_S0),
+                                  _ptr(workspace), ws_bytes, B, H, T, dk, dv, _ptr(cu_seqlens),
+                                  0 if cu_seqlens is None else n_seqs, code, int(path),
+                                  ctypes.c_void_p(s.cuda_stream))
+    _check(st)
 
 
 def chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final=None, cu_seqlens=None,

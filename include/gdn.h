@@ -18,6 +18,11 @@
  * caller, contiguous, 16-byte aligned.  No call allocates, frees or
  * synchronises unless stated.  Every function returns a gdn_status; on a non-OK
  * status `gdn_last_error()` gives a message for the calling host thread.
+ *
+ * Current device: every call works on the calling thread's current CUDA device
+ * (cudaSetDevice).  The device pointers and the stream passed to a call must belong
+ * to that device: tensor maps, kernel attributes and the library's internal streams
+ * are resolved on it, so a mismatch fails with a CUDA error (GDN_ELAUNCH or GDN_ECUDA).
  */
 #ifndef GDN_H_
 #define GDN_H_

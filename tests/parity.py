@@ -28,14 +28,17 @@ def to_device(inp: dict, dev="cuda") -> dict:
     return {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-def run_gpu(inp: dict, C: int, S_final: bool = True):
+def run_gpu(inp: dict, C: int, S_final: bool = True, f64: bool = True):
     d = to_device(inp)
     out, Sf = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],
                             d["cu_seqlens"], C=C, output_final_state=S_final)
     gdn.gdn_check_status()
     torch.cuda.synchronize()
-    o = out.float().cpu().numpy().astype(np.float64)
-    s = None if Sf is None else Sf.cpu().numpy().astype(np.float64)
+    o = out.float().cpu().numpy()
+    s = None if Sf is None else Sf.cpu().numpy()
+    if f64:
+        o = o.astype(np.float64)
+        s = None if s is None else s.astype(np.float64)
     return o, s
 
 
@@ -101,3 +104,32 @@ def compare_sampled(inp: dict, out: np.ndarray, Sf: np.ndarray, units, fp32: boo
                       stored_bf16=not fp32)
     es = assert_close(np.stack(got_s), np.stack(ref_s), fp32, "S_final (sampled)")
     return eo, es
+
+
+def compare_all_units(inp: dict, out: np.ndarray, Sf: np.ndarray, block_rows: int = 1 << 14):
+    """Every (sequence, head) unit of a full-size bf16 run against the oracle run on
+    every unit, with the bf16 bounds of ``assert_close``; the comparison walks the
+    token rows in blocks so that a multi-GB output needs no multi-GB temporaries.
+    ``out`` may be fp32 (the bf16 outputs are exact in it)."""
+    ref_o, ref_s = run_oracle(inp)
+    assert out.shape == ref_o.shape and Sf.shape == ref_s.shape
+    ro = ref_o.reshape(-1, ref_o.shape[-1])
+    go = out.reshape(-1, out.shape[-1])
+    ss = 0.0
+    for r in range(0, ro.shape[0], block_rows):
+        ss += float((ro[r:r + block_rows] ** 2).sum())
+    rms = np.sqrt(ss / ro.size)
+    worst, dss = -np.inf, 0.0
+    for r in range(0, ro.shape[0], block_rows):
+        g = go[r:r + block_rows].astype(np.float64)
+        x = ro[r:r + block_rows]
+        assert np.isfinite(g).all(), "out: non-finite values"
+        d = np.abs(g - x)
+        dss += float((d ** 2).sum())
+        worst = max(worst, float((d - TOL_BF16_MAX_OVER_RMS * rms - BF16_STORAGE_REL * np.abs(x)).max()))
+    e = dict(worst_excess_over_rms=worst / rms, rms_ratio=np.sqrt(dss / ro.size) / rms,
+             units=int(ref_s.shape[0] * ref_s.shape[1]))
+    assert worst <= 0, f"out (every unit): {e}"
+    assert e["rms_ratio"] <= TOL_BF16_MAX_OVER_RMS, f"out (every unit): {e}"
+    es = assert_close(Sf.astype(np.float64), ref_s, False, "S_final (every unit)")
+    return e, es

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA library against the fp64 oracle, element by element.
 
-Small cases are compared in full; the full-size workloads run in the same call
-the benchmark times and are compared on a sample of (sequence, head) pairs that
-the oracle computes one by one.  Tolerances are in tests/parity.py.
+Every case is compared in full, the full-size workloads included (they run in the
+same call the benchmark times, and the oracle runs every (sequence, head) unit).
+Tolerances are in tests/parity.py.
 """
 import numpy as np
 import pytest
@@ -10,8 +10,7 @@ import torch
 
 import chunkwise_gated_deltanet_gb300 as gdn
 import workloads
-from tests.parity import (assert_close, compare_sampled, run_gpu, run_oracle, sample_units,
-                          to_device)
+from tests.parity import (assert_close, compare_all_units, run_gpu, run_oracle, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,18 +43,19 @@ def test_gdn_f32_b2h4t1024d64c64_full():
     _full_check(workloads.make_inputs(W["gdn_f32_b2h4t1024d64c64"]), 64)
 
 
-@pytest.mark.parametrize("name,count", [
-    ("gdn_bf16_b4h16t4096d128c64", 10),
-    ("gdn_bf16_b1h32t32768d128c64", 4),
-    ("gdn_bf16_varlen256_h16d128c64", 24),
+@pytest.mark.parametrize("name", [
+    "gdn_bf16_b4h16t4096d128c64",
+    "gdn_bf16_b1h32t32768d128c64",
+    "gdn_bf16_varlen256_h16d128c64",
 ])
-def test_full_size_workload_sampled(name, count):
+def test_full_size_workload_every_unit(name):
+    """The three full-size bf16 workloads, in the launch configuration the benchmark
+    times, compared on every (sequence, head) unit against the oracle."""
     w = W[name]
     inp = workloads.make_inputs(w)
-    o, s = run_gpu(inp, w.C)
+    o, s = run_gpu(inp, w.C, f64=False)
     assert np.isfinite(o).all() and np.isfinite(s).all()
-    units = sample_units(inp["N"], inp["H"], count)
-    compare_sampled(inp, o, s, units, fp32=False)
+    compare_all_units(inp, o, s)
 
 
 def test_bf16_headline_shape_small_full():
