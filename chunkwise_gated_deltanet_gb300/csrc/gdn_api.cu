@@ -239,6 +239,37 @@ int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v, const float* l
   return GDN_OK;
 }
 
+size_t gdn_chunk_bwd_noalloc_max_scratch_bytes(void) { return gdn::kBwdNoAllocScratchBytes; }
+
+int gdn_chunk_bwd_noalloc(const void* q, const void* k, const void* v, const float* log_alpha,
+                          const float* beta, const float* S0, const void* d_out,
+                          const float* dS_final, void* d_q, void* d_k, void* d_v,
+                          float* d_log_alpha, float* d_beta, float* d_S0, int B, int H, int T,
+                          int dk, int dv, const int32_t* cu_seqlens, int N_seqs, int qkv_dtype,
+                          void* stream) {
+  const char* fn = "gdn_chunk_bwd_noalloc";
+  // The per-token path with the library's fixed scratch array as its workspace: the
+  // size it needs is checked against the array first, then gdn_chunk_bwd_ex validates
+  // everything else and launches exactly as for a caller-supplied workspace.
+  void* scratch = nullptr;
+  if (B > 0 && H > 0 && T > 0 && head_ok(dk) && head_ok(dv) && (!cu_seqlens || N_seqs > 0)) {
+    const int N = cu_seqlens ? N_seqs : B;
+    const size_t need = gdn::bwd_workspace_bytes((long long)B * T, H, dk, dv, N);
+    if (need > gdn::kBwdNoAllocScratchBytes)
+      return fail(GDN_EINVAL, "%s: these sizes need %zu bytes of scratch, more than the "
+                  "library's fixed %zu-byte array; use gdn_chunk_bwd with a workspace", fn,
+                  need, (size_t)gdn::kBwdNoAllocScratchBytes);
+    const cudaError_t e = gdn::bwd_noalloc_scratch(&scratch);
+    if (e != cudaSuccess)
+      return fail(GDN_ECUDA, "%s: looking up the scratch array failed: %s", fn,
+                  cudaGetErrorString(e));
+  }
+  return gdn_chunk_bwd_ex(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v,
+                          d_log_alpha, d_beta, d_S0, scratch,
+                          scratch ? gdn::kBwdNoAllocScratchBytes : 0, B, H, T, dk, dv,
+                          cu_seqlens, N_seqs, qkv_dtype, GDN_BWD_TOKENS, stream);
+}
+
 int gdn_state_fold(const float* S_in, const float* M, const float* L, int count, float* S_out,
                    int units, int dv, int dk, void* stream) {
   if (units < 0 || count < 1)

@@ -31,7 +31,17 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "gdn_internal.h"
+
+// Scratch of the allocation-free backward (gdn_chunk_bwd_noalloc): a fixed array in
+// the library's own device memory, so that a caller that cannot allocate device memory
+// still gets the per-token backward's checkpoints and per-row partial sums.  Every
+// device that loads the library holds it until the process exits.  In host code this
+// name is only a stand-in for the device array: kernels get its device address from
+// bwd_noalloc_scratch() below, never the name itself.
+static __device__ __align__(256) unsigned char g_bwd_noalloc_scratch[gdn::kBwdNoAllocScratchBytes];
 
 namespace gdn {
 namespace {
@@ -489,6 +499,28 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
 size_t bwd_workspace_bytes(long long rows, int H, int dk, int dv, int N) {
   if (rows == 0) return 0;
   return bwd_layout(rows, H, dk, dv, N).total;
+}
+
+// Device address of the fixed scratch array on the current device, looked up once per
+// device (with that device current) and kept.  The first lookup may load the library's
+// device code on that device, so a first call should not happen during stream capture.
+cudaError_t bwd_noalloc_scratch(void** ptr) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_bwd_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {

@@ -121,6 +121,10 @@ struct BwdArgs {
 };
 size_t bwd_workspace_bytes(long long rows, int H, int dk, int dv, int N);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// Size of the per-token backward's fixed scratch array (gdn_chunk_bwd_noalloc), and its
+// device address on the current device (looked up once per device).
+constexpr size_t kBwdNoAllocScratchBytes = size_t(64) << 20;
+cudaError_t bwd_noalloc_scratch(void** ptr);
 // The chunk-form backward (dk = dv = 64 or 128, rows > 0).
 bool bwd_chunked_supported(int dk, int dv);
 size_t bwd_chunked_workspace_bytes(long long rows, int H, int dk, int dv, int N);

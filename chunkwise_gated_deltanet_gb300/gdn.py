@@ -25,7 +25,8 @@ EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_host_workspace_
            "gdn_decode_step_host", "gdn_decode_step_host_workspace_bytes",
            "gdn_chunk_bwd", "gdn_chunk_bwd_ex", "gdn_chunk_bwd_workspace_bytes", "gdn_bwd_select_path",
            "gdn_linear_chunk_fwd", "gdn_decode_step", "gdn_state_fold", "gdn_select_path", "gdn_launches_per_call",
-           "gdn_check_status", "gdn_selftest_wait_timeout", "gdn_last_error", "gdn_version")
+           "gdn_check_status", "gdn_selftest_wait_timeout", "gdn_last_error", "gdn_version",
+           "gdn_chunk_bwd_noalloc", "gdn_chunk_bwd_noalloc_max_scratch_bytes")
 
 
 class GdnError(RuntimeError):
@@ -60,6 +61,11 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_chunk_bwd_ex.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
                                      I, I, I, I, I, P, I, I, I, P]
     lib.gdn_chunk_bwd_ex.restype = I
+    lib.gdn_chunk_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                          I, I, I, I, I, P, I, I, P]
+    lib.gdn_chunk_bwd_noalloc.restype = I
+    lib.gdn_chunk_bwd_noalloc_max_scratch_bytes.argtypes = []
+    lib.gdn_chunk_bwd_noalloc_max_scratch_bytes.restype = ctypes.c_size_t
     lib.gdn_bwd_select_path.argtypes = [I, I, I]
     lib.gdn_bwd_select_path.restype = I
     lib.gdn_chunk_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
@@ -412,6 +418,32 @@ def gdn_chunk_bwd(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, 
                                   _ptr(workspace), ws_bytes, B, H, T, dk, dv, _ptr(cu_seqlens),
                                   0 if cu_seqlens is None else n_seqs, code, int(path),
                                   ctypes.c_void_p(s.cuda_stream))
+    _check(st)
+
+
+def gdn_chunk_bwd_noalloc(q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v,
+                          d_log_alpha, d_beta, d_S0, cu_seqlens: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name: the per-token backward
+    with the library's fixed scratch array instead of a workspace, for callers that
+    cannot allocate device memory.  Arguments as for ``gdn_chunk_bwd`` without the
+    workspace; sizes whose scratch exceeds the array raise GdnError(GDN_EINVAL)."""
+    lib = load_library()
+    B, T, H, dk = k.shape
+    dv = v.shape[-1]
+    for t in (q, k, v, log_alpha, beta, S0, d_out, dS_final, d_q, d_k, d_v, d_log_alpha,
+              d_beta, d_S0, cu_seqlens):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("gdn_chunk_bwd_noalloc: every tensor must be a contiguous CUDA tensor")
+    code = _dtype_code(v.dtype)
+    n_seqs = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    s = stream if stream is not None else torch.cuda.current_stream(v.device)
+    with torch.cuda.device(v.device):
+        st = lib.gdn_chunk_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                       _ptr(S0), _ptr(d_out), _ptr(dS_final), _ptr(d_q),
+                                       _ptr(d_k), _ptr(d_v), _ptr(d_log_alpha), _ptr(d_beta),
+                                       _ptr(d_S0), B, H, T, dk, dv, _ptr(cu_seqlens), n_seqs,
+                                       code, ctypes.c_void_p(s.cuda_stream))
     _check(st)
 
 

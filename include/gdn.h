@@ -180,6 +180,39 @@ int gdn_chunk_bwd_ex(const void* q, const void* k, const void* v,
                      void* stream);
 
 /*
+ * gdn_chunk_bwd_noalloc -- gdn_chunk_bwd on the per-token path (GDN_BWD_TOKENS) for
+ * callers that cannot allocate device memory: code running where cudaMalloc is not
+ * allowed or not wanted (inside a caller's own memory pool, a plugin that receives only
+ * its input and output buffers, a path that must not synchronise the device the way an
+ * allocation can), or with no allocator at hand at all.  It takes no workspace; the
+ * per-token backward's scratch (checkpoints and per-row partial sums) lives in one
+ * fixed array of gdn_chunk_bwd_noalloc_max_scratch_bytes() bytes (64 MiB) inside the
+ * library's device memory, which every device that loads the library holds until the
+ * process exits.  The pages have no counterpart of this entry point: it is a packaging
+ * of the same backward, with the same results as gdn_chunk_bwd_ex(..., GDN_BWD_TOKENS).
+ *
+ * Arguments as for gdn_chunk_bwd without `workspace` / `workspace_bytes`; the caller
+ * still owns and passes every input and output.
+ *
+ * Sizes whose scratch (gdn_chunk_bwd_workspace_bytes for the per-token path) exceeds the
+ * fixed array are rejected with GDN_EINVAL before any launch; at dk = dv = 128 that is
+ * about 16 KB per token and head.  Nothing is allocated or freed: no cudaMalloc, cudaFree
+ * or allocating library routine.  The first call on a device looks up the array's device
+ * address with that device current (this may load the library's device code there), so
+ * make that first call before any stream capture.  Every call shares the one array and
+ * it keeps the last call's contents; the kernels write every scratch word they read, so
+ * nothing needs clearing, but calls that overlap on the GPU (on different streams, or
+ * from different host threads without ordering) race on it and must not run at once.
+ */
+size_t gdn_chunk_bwd_noalloc_max_scratch_bytes(void);
+int gdn_chunk_bwd_noalloc(const void* q, const void* k, const void* v,
+                          const float* log_alpha, const float* beta, const float* S0,
+                          const void* d_out, const float* dS_final,
+                          void* d_q, void* d_k, void* d_v, float* d_log_alpha, float* d_beta,
+                          float* d_S0, int B, int H, int T, int dk, int dv,
+                          const int32_t* cu_seqlens, int N_seqs, int qkv_dtype, void* stream);
+
+/*
  * gdn_chunk_fwd_host -- gdn_chunk_fwd (or, with beta == NULL, gdn_linear_chunk_fwd) on
  * HOST buffers, end to end: copies the inputs in, runs the forward, copies the outputs
  * back, and returns once they are in host memory.  Fixed-length batches only.
