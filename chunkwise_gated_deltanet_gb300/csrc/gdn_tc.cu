@@ -18,12 +18,12 @@
 //   chain (serial):  SW = U^T + S (-W~^T) = delta^T;  S <- e^{g_last} S + delta~^T K
 //                    (S accumulates in TMEM; delta feeds the MMAs from TMEM)
 //   MMA warp:        U^T = V^T (T diag(beta))^T into SW ahead of the chain;
-//                    O += delta^T P^T onto the output accumulator of the chunk's
-//                    parity (two, so the outputs of chunk j drain while j+1 runs)
+//                    O += delta^T P^T onto the output accumulator
 //   aux P (ahead):   Q K^T (M=64) -> P' = lower(q_t.k_j e^{-g_j}) (factored decay),
 //                    or P = lower(q_t.k_j e^{g_t-g_j}) and Q <- diag(e^g) Q in place
-//   aux O (behind):  O = S Q^T into that accumulator once the chain has queued its
-//                    S W~^T; then o_t = e^{g_t} O_t (factored) or O_t -> out
+//   aux O (behind):  o_t = e^{g_t} O_t (factored) or O_t -> out for chunk j - 1, then
+//                    O = S Q^T (j) (S as hi + lo) into the emptied accumulator once the
+//                    chain has queued its S W~^T
 // The factored form keeps the output accumulator in the frame of e^{-g_t}: the
 // state part S q_t and every in-chunk term e^{-g_j} (q_t.k_j) delta_j share that
 // factor, which aux O multiplies back.  It is used when the chunk's total decay
@@ -47,9 +47,11 @@
 // Precision: operands are bf16, accumulators fp32.  T, delta, the decayed delta
 // (delta~ = delta diag(e^{g_last-g})) and P are carried as two bf16 terms
 // (hi = bf16(x), lo = bf16(x - hi)) and multiplied as hi*hi + hi*lo + lo*hi, or
-// hi + lo against an exact bf16 operand (K, V).  S and W~ are single bf16
-// operands (and Q scaled by e^{g} in the strong-decay form); the running state
-// itself stays fp32 (in TMEM).
+// hi + lo against an exact bf16 operand (K, V, Q).  The state enters S Q^T (the
+// outputs' read of the carried state) as hi + lo as well, so that outputs dominated by
+// a decaying carried state keep the rounding of a 16-bit mantissa; it enters S W~^T,
+// and W~ enters, as single bf16 terms (and Q scaled by e^{g} in the strong-decay form).
+// The running state itself stays fp32 (in TMEM).
 //
 // Synchronisation (mbarriers; "phase j" completes once per chunk j):
 //   WY:    kv_full[s]  (TMA bytes + producer arrive)   kv_empty[s] (WG after its MMAs)
@@ -76,7 +78,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_internal.h"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace gdn {
 
@@ -86,12 +88,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kC = 64;
-constexpr int kD = 128;
 constexpr int kThreads = 448;  // 3 warpgroups, a TMA producer warp and (state CTA) an MMA warp
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarp = 13;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 
 // ---- CTA 0 ("WY") shared memory ----
 constexpr int WY_KV = 0;                 // 3 stages x 16 KB: K p0 | K p1 (8 KB each)
@@ -137,11 +136,6 @@ static_assert(SC_TUL + 8192 <= WY_SCR_BYTES, "WY scratch");
 static_assert(WY_NWG == WY_NST, "one K stage per WY warpgroup");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// The factored decay e^{g_i} e^{-g_j} replaces e^{g_i - g_j} when the chunk's
-// total decay (in log2 units) is below this bound, so that neither factor
-// overflows or underflows fp32.
-constexpr float kMaxFactoredDecayLog2 = 80.f;
-
 // barrier slots (8 bytes each)
 enum WyBar { WB_KV_FULL = 0, WB_KV_EMPTY = 3, WB_MMA = 6, WB_HE = 9, WB_COUNT = 11 };
 static_assert(WB_COUNT * 8 <= WY_MISC - WY_BAR, "WY barriers");
@@ -155,11 +149,12 @@ static_assert(SB_COUNT * 8 <= ST_MISC - ST_BAR, "state barriers");
 // TMEM columns.  WY: per warpgroup w at 128*w: K K^T 0, W~^T 64.
 constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
 // state: S 0..127, U^T + S(-W~^T) 128 (one accumulator: U^T(j + 1) is issued only after
-// the delta epilogue of chunk j has read it), outputs of chunk j at 192 + 64 (j % 2),
-// QK 320, delta hi 384, delta lo 416, delta~ hi 448, delta~ lo 480 (packed bf16 pairs,
-// A operands).
-constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_QK = 320, TT_DH = 384, TT_DL = 416,
-                   TT_DSH = 448, TT_DSL = 480;
+// the delta epilogue of chunk j has read it), the output accumulator 192 and the lo term
+// of the state operand of S Q^T at 256 (packed bf16 pairs, an A operand; the linear mode
+// has outputs of chunk j at 192 + 64 (j % 2) instead), QK 320, delta hi 384, delta lo 416,
+// delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
+constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_SLO = 256, TT_QK = 320, TT_DH = 384,
+                   TT_DL = 416, TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
 // Linear mode: delta (= V, exact bf16 pairs) and delta~ (hi / lo) of chunk j in buffer
 // j % 2.  Buffer 0 is the delta-rule columns; buffer 1 takes the U/SW accumulator (this
@@ -168,289 +163,32 @@ __device__ __forceinline__ uint32_t tl_dh(int b) { return b ? TT_SW : TT_DH; }
 __device__ __forceinline__ uint32_t tl_dsh(int b) { return b ? TT_SW + 32 : TT_DSH; }
 __device__ __forceinline__ uint32_t tl_dsl(int b) { return b ? TT_DL : TT_DSL; }
 
-constexpr int ST_WAIT = 1;
 
-constexpr float kLog2e = 1.4426950408889634f;
-__device__ __forceinline__ float ex2(float x) {  // 2^x by the PTX ex2.approx instruction
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-// 8 consecutive columns (col % 8 == 0) of `row` into a 128B-swizzled bf16 tile.
-__device__ __forceinline__ void st_sw128_8(uint8_t* tile, int row, int col, int rows,
-                                           const float* v) {
-  st_shared_v4(smem_u32(tile + sw128_offset(row, col, rows)), pack_bf16(v[0], v[1]),
-               pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
-}
-// Two floats as a pair of packed bf16 terms: hi = bf16(x), lo = bf16(x - hi).
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(x0, x1);
-  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
-  lo = pack_bf16(x0 - h0, x1 - h1);
-}
-__device__ __forceinline__ void st_sw128_8_split(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                                 int col, int rows, const float* v) {
-  uint32_t h[4], l[4];
+// The lo term of 32 state columns (32p .. 32p + 31 of row `row`), bf16(x - bf16(x)), as
+// packed pairs into the state-lo columns of TMEM: the K = 128 A operand of S lo Q^T.
+__device__ __forceinline__ void state_lo_to_tmem(uint32_t tq, int p, const float* v) {
+  uint32_t lo[16];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) split2(v[2 * u], v[2 * u + 1], h[u], l[u]);
-  const uint32_t off = sw128_offset(row, col, rows);
-  st_shared_v4(smem_u32(hi_tile + off), h[0], h[1], h[2], h[3]);
-  st_shared_v4(smem_u32(lo_tile + off), l[0], l[1], l[2], l[3]);
-}
-// K-major operand, 128B swizzle, K advanced by 16 elements per step.
-__device__ __forceinline__ uint64_t desc_k(const uint8_t* tile, int kstep, int panel_bytes) {
-  return smem_desc(smem_u32(tile) + (kstep >> 2) * panel_bytes + (kstep & 3) * 32, 16, 1024);
-}
-// MN-major operand stored as [K rows][MN cols] in 64-column panels, K advanced by 16 rows.
-__device__ __forceinline__ uint64_t desc_mn(const uint8_t* tile, int kstep, int panel_bytes) {
-  return smem_desc(smem_u32(tile) + kstep * 2048, panel_bytes, 1024);
-}
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ void st4(float* p, float a, float b, float c, float d) {
-  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
-}
-
-// Bounded parity wait that also gives up when another role of this CTA already
-// gave up.  Returns false on timeout (recording `code`) or on abort.  The polling
-// loop is one shared out-of-line function; only the first test is inlined at
-// each call site, which keeps the hot code of every role small.
-__device__ __noinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
-                                           volatile int* abort_flag, bool cluster_scope) {
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-    if (ok) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) {
-      atomicOr((int*)abort_flag, ST_WAIT);
-      return false;
-    }
+  for (int e = 0; e < 16; ++e) {
+    uint32_t hi;
+    split2(v[2 * e], v[2 * e + 1], hi, lo[e]);
   }
+  tmem_st16(tq + TT_SLO + 16 * p, lo);
 }
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         bool cluster_scope) {
-  const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-  return ok || wait_bar_poll(bar, parity, abort_flag, cluster_scope);
-}
-
-// A bounded wait taken by every thread of a named-barrier group (`nb`, `nthreads`),
-// followed by one vote: true when the group must leave its loop because its own wait
-// gave up or another role already did.  Out of line, shared by all call sites.
-__device__ __noinline__ bool group_wait_fails(uint64_t* bar, uint32_t parity,
-                                              volatile int* abort_flag, bool cluster_scope,
-                                              uint32_t nb, uint32_t nthreads) {
-  const bool ok = wait_bar(bar, parity, abort_flag, cluster_scope);
-  return named_sync_or(nb, nthreads, !ok || *abort_flag != 0);
-}
-// Inline form for the latency-critical roles, over up to three barriers (a null
-// barrier is skipped) with a single vote: every wait point that is not already
-// satisfied costs a full round of the named barrier, so the chain merges the
-// barriers it needs at the same point.
-__device__ __forceinline__ bool group_waits_fail(volatile int* abort_flag, uint32_t nb,
-                                                 uint32_t nthreads, uint64_t* b1, uint32_t p1,
-                                                 bool c1, uint64_t* b2 = nullptr, uint32_t p2 = 0,
-                                                 uint64_t* b3 = nullptr, uint32_t p3 = 0) {
-  bool ok = wait_bar(b1, p1, abort_flag, c1);
-  if (ok && b2) ok = wait_bar(b2, p2, abort_flag, false);
-  if (ok && b3) ok = wait_bar(b3, p3, abort_flag, false);
-  return named_sync_or(nb, nthreads, !ok || *abort_flag != 0);
-}
-// The same for a single warp.
-__device__ __noinline__ bool warp_wait_fails(uint64_t* bar, uint32_t parity,
-                                             volatile int* abort_flag, bool cluster_scope) {
-  return !__all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, cluster_scope));
-}
-
-// MMA issue from one thread.  Descriptors are built once per operand and advanced
-// by constants (16-byte units: 2 per k-step for a K-major operand, 128 for an
-// MN-major one, whose k-step is 16 rows of 128 bytes); a tcgen05.mma then costs the
-// issuing thread little beyond the tensor core's own rate.
-constexpr uint32_t kStepK = 2;
-constexpr uint32_t kStepMN = 128;
-// K = 128 (8 k-steps): A K-major in two 64-column panels pa16 apart; B K-major in
-// panels pb16 apart, or MN-major.  Rolled over the panels, 4 constant steps inside.
-template <bool B_MN>
-__device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a, uint32_t pa16, uint64_t b,
-                                         uint32_t pb16, uint32_t id, uint32_t acc_first) {
+// S Q^T with the state as two bf16 terms: S hi (shared memory, K-major, two 64-column
+// panels) and S lo (TMEM, packed pairs), against Q (K-major, two panels), then commit.
+__device__ __noinline__ void sq_hilo_commit(uint32_t d, uint64_t a_hi, uint32_t a_lo_tmem,
+                                            uint64_t b, uint32_t id, uint64_t* bar) {
+  tc_fence_after();
+  mma_k128<false>(d, a_hi, 16384 >> 4, b, 16384 >> 4, id, 0);
 #pragma unroll 1
   for (int p = 0; p < 2; ++p) {
-    const uint64_t ap = a + (uint64_t)(p * pa16);
-    const uint64_t bp = b + (uint64_t)(B_MN ? p * 4 * kStepMN : p * pb16);
+    const uint64_t bp = b + (uint64_t)(p * (16384 >> 4));
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      mma_bf16(d, ap + kStepK * k, bp + (B_MN ? kStepMN : kStepK) * k, id, (p | k) ? 1u : acc_first);
+      mma_bf16_ta(d, a_lo_tmem + 32 * p + 8 * k, bp + kStepK * k, id, 1u);
   }
-}
-// Out-of-line form of mma_k128<false> followed by a commit, shared by the roles that
-// are not on the serial path (one copy of the issue code in the instruction cache).
-__device__ __noinline__ void mma_k128_commit(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                             uint64_t* bar) {
-  tc_fence_after();
-  mma_k128<false>(d, a, 16384 >> 4, b, 16384 >> 4, id, 0);
   mma_commit(bar);
-}
-// K = 64 (4 k-steps): A from TMEM (8 columns per step) or MN-major smem; B K-major
-// or MN-major.  UNROLL for the chain's own MMAs, rolled elsewhere.
-template <bool A_TMEM, bool B_MN, bool UNROLL>
-__device__ __forceinline__ void mma_k64(uint32_t d, uint64_t a, uint32_t a_tmem, uint64_t b,
-                                        uint32_t id, uint32_t acc_first) {
-  if (UNROLL) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint64_t bk = b + (B_MN ? kStepMN : kStepK) * k;
-      if (A_TMEM)
-        mma_bf16_ta(d, a_tmem + 8 * k, bk, id, k ? 1u : acc_first);
-      else
-        mma_bf16(d, a + kStepMN * k, bk, id, k ? 1u : acc_first);
-    }
-  } else {
-#pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-      if (A_TMEM)
-        mma_bf16_ta(d, a_tmem, b, id, k ? 1u : acc_first);
-      else
-        mma_bf16(d, a, b, id, k ? 1u : acc_first);
-      a += kStepMN;
-      a_tmem += 8;
-      b += B_MN ? kStepMN : kStepK;
-    }
-  }
-}
-
-// Bounded wait until the hand-off ticket reaches `want`; false on timeout or abort.
-__device__ __forceinline__ bool wait_ticket(volatile int* ticket, int want,
-                                            volatile int* abort_flag) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (*ticket == want) return true;
-    if (*abort_flag) return false;
-    if (it == 0) {
-      t0 = globaltimer_ns();
-    } else if (globaltimer_ns() - t0 > kWaitNs) {
-      atomicOr((int*)abort_flag, ST_WAIT);
-      return false;
-    }
-  }
-}
-
-struct Unit {
-  long long row0, len;
-  int nc, h;
-  size_t sidx;  // offset of S[n][h] in S0 / S_final
-};
-
-// Gate inputs of one chunk for a whole warp: thread `lane` owns tokens lane and
-// lane + 32 (zeros past the sequence end).  Split from the scan so the loads of
-// the next chunk can be in flight while the current one is processed.  A NULL
-// log_alpha reads as alpha = 1; a NULL beta (the linear mode, erase 0) as a write
-// strength of 1.
-struct GateLoad {
-  float la0, la1, b0, b1;
-};
-// A gate of alpha = 0 (log alpha = -inf, the whole state forgotten) enters as log alpha =
-// -80: alpha = e^-80 ~ 1.8e-35 leaves nothing measurable of the earlier state, and the
-// in-chunk gate sums and their differences stay finite (-inf - -inf would be NaN) and
-// accurate (|sum| <= 80 * 64).
-constexpr float kMinLogAlpha = -80.f;
-__device__ __forceinline__ GateLoad load_gates(const float* __restrict__ log_alpha,
-                                               const float* __restrict__ beta, const Unit& u, int H,
-                                               int chunk, int lane) {
-  GateLoad g{0.f, 0.f, 0.f, 0.f};
-  const long long c0 = (long long)chunk * kC;
-  if (chunk < u.nc && c0 + lane < u.len) {
-    const size_t gi = (size_t)(u.row0 + c0 + lane) * H + u.h;
-    g.la0 = log_alpha ? __ldg(log_alpha + gi) : 0.f;
-    g.b0 = beta ? __ldg(beta + gi) : 1.f;
-  }
-  if (chunk < u.nc && c0 + lane + 32 < u.len) {
-    const size_t gi = (size_t)(u.row0 + c0 + lane + 32) * H + u.h;
-    g.la1 = log_alpha ? __ldg(log_alpha + gi) : 0.f;
-    g.b1 = beta ? __ldg(beta + gi) : 1.f;
-  }
-  return g;
-}
-// In-chunk cumulative gate sums in log2 units (g0 for token lane, g1 for token
-// lane + 32) and their total, each log alpha taken at least kMinLogAlpha.
-__device__ __forceinline__ void scan_gates(const GateLoad& in, int lane, float& g0, float& g1,
-                                           float& tot) {
-  float x0 = fmaxf(in.la0, kMinLogAlpha), x1 = fmaxf(in.la1, kMinLogAlpha);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-    const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-    if (lane >= o) {
-      x0 += y0;
-      x1 += y1;
-    }
-  }
-  const float t0 = __shfl_sync(0xffffffffu, x0, 31);
-  const float t1 = __shfl_sync(0xffffffffu, x1, 31);
-  g0 = x0 * kLog2e;
-  g1 = (x1 + t0) * kLog2e;
-  tot = (t0 + t1) * kLog2e;
-}
-
-// Row i of A = strictly-lower(beta_i e^{g_i - g_j} k_i.k_j) from the K K^T
-// accumulator (two halves of 32 columns) into fp32 scratch.  FACTORED: ci =
-// beta_i e^{g_i} and colv = e^{-g_j}; otherwise ci = beta_i, gi = g_i, colv = g_j.
-// One instantiation per form keeps the hot form's code contiguous.
-template <bool FACTORED>
-__device__ __forceinline__ void wy_epi_a(uint32_t t_kk, float* arow, int i, float ci, float gi,
-                                         const float* colv) {
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    uint32_t r[32];
-    tmem_ld32(t_kk + 32 * hh, r);
-    tmem_wait_ld();
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int jc0 = 32 * hh + 4 * q;
-      const float4 c4 = ld4(colv + jc0);
-      const float c[4] = {c4.x, c4.y, c4.z, c4.w};
-      float v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = __uint_as_float(r[4 * q + e]);
-        const float f = FACTORED ? ci * c[e] : ci * ex2(gi - c[e]);
-        v[e] = (jc0 + e < i) ? f * x : 0.f;
-      }
-      st4(arow + jc0, v[0], v[1], v[2], v[3]);
-    }
-  }
-}
-
-// Row t of P (or P') from the Q K^T accumulator as hi/lo bf16 into a P slot.
-// FACTORED: P'_{t,j} = q_t.k_j e^{-g_j} with colv = e^{-g_j}; otherwise
-// P_{t,j} = q_t.k_j e^{g_t - g_j} with gt = g_t and colv = g_j.
-template <bool FACTORED>
-__device__ __forceinline__ void aux_epi_p(uint32_t t_qk, uint8_t* ps, int t, float gt,
-                                          const float* colv, bool store) {
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {  // columns 8c .. 8c + 7
-    uint32_t r[8];
-    tmem_ld8(t_qk + 8 * c, r);
-    tmem_wait_ld();
-    const int jc0 = 8 * c;
-    const float4 ca = ld4(colv + jc0), cb = ld4(colv + jc0 + 4);
-    const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-    float v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float x = __uint_as_float(r[e]);
-      v[e] = (jc0 + e <= t) ? (FACTORED ? x * cv[e] : ex2(gt - cv[e]) * x) : 0.f;
-    }
-    if (store) st_sw128_8_split(ps, ps + 8192, t, jc0, 64, v);
-  }
 }
 
 // ============================================================ CTA 0: WY ======
@@ -898,7 +636,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             const uint8_t* ps = sm + ST_PS + (j & 1) * PS_BYTES;
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
             const uint64_t ph = desc_k(ps, 0, 8192), pl = desc_k(ps + 8192, 0, 8192);
-            const uint32_t d = tmem + TT_O + 64 * (j & 1);
+            const uint32_t d = tmem + TT_O;  // the one output accumulator of the delta rule
             mma_k64<true, false, false>(d, 0, tmem + TT_DH, ph, id, 1);
             mma_k64<true, false, false>(d, 0, tmem + TT_DH, pl, id, 1);
             mma_k64<true, false, false>(d, 0, tmem + TT_DL, ph, id, 1);
@@ -963,6 +701,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) st_sw128_8(sm + ST_SB, row, 32 * p + 8 * q, 128, v + 8 * q);
+        if constexpr (!LINEAR) state_lo_to_tmem(tq, p, v);
         uint32_t sv[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) sv[e] = __float_as_uint(gam * v[e]);
@@ -1058,6 +797,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       if (tid == 0) mbar_arrive(&bars[SB_QK_EMPTY + s]);  // the chain's last read of stage s
       if (LINEAR && tid == 0 && !last) mbar_arrive(&bars[SB_DR + (b ^ 1)]);  // delta (j + 1) made
       const float gam = last ? 1.f : der_all[((j + 1) % ST_NST) * ST_DER_STAGE + 64 + 63];
+
       // ---- new state: bf16 copy for the next chunk, pre-scaled fp32 back to TMEM ----
 #pragma unroll 1
       for (int p = 0; p < 4; ++p) {
@@ -1076,6 +816,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         } else {
 #pragma unroll
           for (int q = 0; q < 4; ++q) st_sw128_8(sm + ST_SB, row, 32 * p + 8 * q, 128, v + 8 * q);
+          if constexpr (!LINEAR) state_lo_to_tmem(tq, p, v);  // S Q^T (j + 1) has read the last
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(gam * v[e]);
           tmem_st32(tq + TT_S + 32 * p, r);
@@ -1159,32 +900,37 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   // aux O holds no stage: each of its warps recomputes the chunk's gate factors from
   // the gates in global memory (the same scan as the producer, so the same values and
   // the same choice of form), and the bf16 outputs are staged in the chunk's P slot,
-  // which delta^T P^T no longer reads.  It also issues S Q^T into the output
-  // accumulator of the chunk's parity, whose previous chunk it drained one iteration
-  // earlier.
+  // which delta^T P^T no longer reads.  It also issues S Q^T, one issue site: the delta
+  // rule has one output accumulator, drained (outputs of chunk i - 1) before S Q^T (i)
+  // starts it again, with S as hi + lo terms; the linear mode has two, so S Q^T (i)
+  // goes into accumulator i % 2 before the outputs of chunk i - 1 are drained.
   const int atid = tid - 256;
 #define AO_WAIT(bar, par) \
   if (group_wait_fails((bar), (par), abort_flag, false, 3, 128)) break;
-  // Iteration i issues S Q^T (i), then drains the outputs of chunk i - 1 out of TMEM
-  // and copies them out: one issue site.
+  // S Q^T (i): issued (from warp 11) once the chain has queued S W~^T (i), which reads
+  // the same bf16 S, and, in the strong-decay form, once aux P has scaled Q.  The
+  // chunk's form is read from its stage, which the chain waited for before signalling.
+#define AO_ISSUE_SQ(i)                                                                          \
+  {                                                                                           \
+    AO_WAIT(&bars[SB_SWI], (i) & 1);                                                          \
+    const int si = (i) % ST_NST;                                                              \
+    if (flags[si] == 0) AO_WAIT(&bars[SB_PF + ((i) & 1)], ((i) >> 1) & 1);                    \
+    if (atid == 96) {                                                                         \
+      if constexpr (LINEAR)                                                                   \
+        mma_k128_commit(tmem + TT_O + 64 * ((i) & 1), desc_k(sm + ST_SB, 0, 16384),            \
+                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0), \
+                        &bars[SB_SQ + ((i) & 1)]);                                            \
+      else                                                                                    \
+        sq_hilo_commit(tmem + TT_O, desc_k(sm + ST_SB, 0, 16384), tmem + TT_SLO,              \
+                       desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),  \
+                       &bars[SB_SQ + ((i) & 1)]);                                             \
+    }                                                                                         \
+  }
   GateLoad gnext = load_gates(log_alpha, beta, u, H, 0, lane);
   #pragma unroll 1
   for (int i = 0; i <= u.nc; ++i) {
     const int j = i - 1, b = j & 1;
-    if (i < u.nc) {
-      // S Q^T (i) starts output accumulator i % 2: issued (from warp 11) once the chain
-      // has queued S W~^T (i), which reads the same bf16 S; in the strong-decay form
-      // also once aux P has scaled Q.  The chunk's form is read from its stage, which
-      // the chain waited for before signalling.  The accumulator's previous chunk,
-      // i - 2, left TMEM before the last iteration's final barrier.
-      AO_WAIT(&bars[SB_SWI], i & 1);
-      const int si = i % ST_NST;
-      if (flags[si] == 0) AO_WAIT(&bars[SB_PF + (i & 1)], (i >> 1) & 1);
-      if (atid == 96)
-        mma_k128_commit(tmem + TT_O + 64 * (i & 1), desc_k(sm + ST_SB, 0, 16384),
-                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),
-                        &bars[SB_SQ + (i & 1)]);
-    }
+    if (LINEAR && i < u.nc) AO_ISSUE_SQ(i)
     if (i > 0) {
       __nv_bfloat16* ost0 = reinterpret_cast<__nv_bfloat16*>(sm + ST_PS + b * PS_BYTES);
       const GateLoad gcur = gnext;
@@ -1197,7 +943,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       AO_WAIT(&bars[SB_DP + b], (j >> 1) & 1);
       tc_fence_after();
       // ---- bf16 outputs staged in P slot b (row t at t * 256 bytes), 8 tokens a step ----
-      const uint32_t to = tq + TT_O + 64 * b;
+      const uint32_t to = tq + TT_O + (LINEAR ? 64 * b : 0);
 #pragma unroll 1
       for (int q = 0; q < 8; ++q) {
         uint32_t a[8];
@@ -1210,7 +956,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
               __shfl_sync(0xffffffffu, ev, (8 * q + e) & 31) * __uint_as_float(a[e]));
       }
       tc_fence_before();
-      named_sync(3, 128);  // outputs staged; accumulator b is free for S Q^T (j + 2)
+      named_sync(3, 128);  // outputs staged; the accumulator is free for its next S Q^T
       const long long c0 = (long long)j * kC;
       const int lc = (int)min((long long)kC, u.len - c0);
       const size_t obase = (size_t)(u.row0 + c0) * H + u.h;
@@ -1226,31 +972,12 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       named_sync(3, 128);
       if (atid == 0) mbar_arrive(&bars[SB_PE + b]);  // P slot b may be refilled
     }
+    if (!LINEAR && i < u.nc) AO_ISSUE_SQ(i)
   }
+#undef AO_ISSUE_SQ
 #undef AO_WAIT
 }
 
-// (sequence, head) unit `unit` = n * H + h: its rows (cu_seqlens clamped to [0, T]),
-// chunk count and state offset.
-__device__ __forceinline__ Unit make_unit(int unit, const int32_t* __restrict__ cu_seqlens, int H,
-                                          int T) {
-  Unit u;
-  u.h = unit % H;
-  const int n = unit / H;
-  if (cu_seqlens) {
-    int a = cu_seqlens[n], b = cu_seqlens[n + 1];
-    a = min(max(a, 0), T);
-    b = min(max(b, a), T);
-    u.row0 = a;
-    u.len = b - a;
-  } else {
-    u.row0 = (long long)n * T;
-    u.len = T;
-  }
-  u.nc = (int)((u.len + kC - 1) / kC);
-  u.sidx = ((size_t)n * H + u.h) * kD * kD;
-  return u;
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1366,33 +1093,6 @@ gdn_tc_linear_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// [rows][H][128] bf16, box of 64 columns x 1 head x 64 rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, int H) {
-  auto enc = get_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-  cuuint32_t box[3] = {64, 1, 64};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
 }
 
 }  // namespace

@@ -372,3 +372,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint32_t a, ui
 }
 }  // namespace ptx
 }  // namespace gdn
+
+namespace gdn {
+namespace ptx {
+// TMA tile store from this CTA's shared memory to global memory (bulk-group
+// completion: cp.async.bulk.commit_group, then wait_group(.read) before the source is
+// reused).  Rows beyond the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+}  // namespace ptx
+}  // namespace gdn

@@ -124,10 +124,10 @@ def test_tcgen05_strong_decay_forms(alpha_mu):
 
 @pytest.mark.parametrize("beta_mode", ["zero", "one", "alternating"])
 def test_tcgen05_beta_extremes(beta_mode):
-    """beta = 0 writes nothing (the state only decays from S0), beta = 1 with unit keys
-    overwrites the stored value along k exactly (the write invariant of Nyysyyan's
-    "Gated-DeltaNet" section), and the two alternate token by token; all through the
-    tcgen05 kernel."""
+    """beta = 0 writes nothing (the state only decays from S0, so every output is the
+    carried state read out), beta = 1 with unit keys overwrites the stored value along k
+    exactly (the write invariant of Nyysyyan's "Gated-DeltaNet" section), and the two
+    alternate token by token; all through the tcgen05 kernel, to the plain bounds."""
     w = W["gdn_bf16_b4h16t4096d128c64"]
     inp = workloads.make_inputs(w, B=2, H=2, T=200, seed=21)
     if beta_mode == "zero":
@@ -138,23 +138,21 @@ def test_tcgen05_beta_extremes(beta_mode):
         inp["beta"] = (torch.arange(200)[None, :, None] % 2).float().expand_as(inp["beta"]).contiguous()
     g = torch.Generator().manual_seed(22)
     inp["S0"] = torch.randn(2, 2, 128, 128, generator=g) * 0.1
-    if beta_mode != "zero":
-        _full_check(inp, 64)
-        return
-    # beta = 0: every output is the pure decay e^{g_t} S0 q_t, and its scale falls by
-    # ~20x along the sequence, so the whole-output RMS bound asks for 0.1% of the
-    # largest outputs, below what the single-bf16 state operand of S Q^T gives (a known
-    # limit of the kernel's precision design).  What holds: the state to the usual bound,
-    # the whole-output RMS error ratio, and every token's outputs within 2e-2 of that
-    # token's own output RMS.
-    o, s_ = run_gpu(inp, 64)
-    ro, rs = run_oracle(inp)
-    assert_close(s_, rs, False, "S_final")
-    assert np.isfinite(o).all()
-    d = np.abs(o - ro) - 2.0 ** -8 * np.abs(ro)
-    assert np.sqrt(((o - ro) ** 2).mean()) <= 2e-2 * np.sqrt((ro ** 2).mean())
-    tok_rms = np.sqrt((ro ** 2).mean(axis=(2, 3), keepdims=True))
-    assert (d <= 2e-2 * tok_rms).all(), float((d / tok_rms).max())
+    _full_check(inp, 64)
+
+
+@pytest.mark.parametrize("beta_const", [0.0, 0.02, 0.1, 0.2, 0.3, 0.5])
+@pytest.mark.parametrize("s0_std", [0.1, 1.0])
+def test_tcgen05_weak_and_moderate_writes(beta_const, s0_std):
+    """Constant write strengths on both sides of the bound below which a chunk takes the
+    state operand of S Q^T as two bf16 terms, with a decaying carried state of two
+    scales: the outputs meet the plain bounds whichever form a chunk takes."""
+    w = W["gdn_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(w, B=1, H=3, T=400, seed=31)
+    inp["beta"] = torch.full_like(inp["beta"], beta_const)
+    g = torch.Generator().manual_seed(32)
+    inp["S0"] = torch.randn(1, 3, 128, 128, generator=g) * s0_std
+    _full_check(inp, 64)
 
 
 def test_without_S0_and_without_S_final():
