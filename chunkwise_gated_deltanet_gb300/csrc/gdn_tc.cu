@@ -149,11 +149,12 @@ static_assert(SB_COUNT * 8 <= ST_MISC - ST_BAR, "state barriers");
 // TMEM columns.  WY: per warpgroup w at 128*w: K K^T 0, W~^T 64.
 constexpr uint32_t WT_KK = 0, WT_W = 64, WT_WG = 128;
 // state: S 0..127, U^T + S(-W~^T) 128 (one accumulator: U^T(j + 1) is issued only after
-// the delta epilogue of chunk j has read it), the output accumulator 192 and the lo term
-// of the state operand of S Q^T at 256 (packed bf16 pairs, an A operand; the linear mode
-// has outputs of chunk j at 192 + 64 (j % 2) instead), QK 320, delta hi 384, delta lo 416,
-// delta~ hi 448, delta~ lo 480 (packed bf16 pairs, A operands).
-constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_SLO = 256, TT_QK = 320, TT_DH = 384,
+// the delta epilogue of chunk j has read it), outputs of chunk j at 192 + 64 (j % 2),
+// QK 320, delta hi 384, delta lo 416, delta~ hi 448, delta~ lo 480 (packed bf16 pairs,
+// A operands).  The delta rule puts the lo term of the state operand of S Q^T (packed
+// bf16 pairs, an A operand) at 320 and accumulates Q K^T (j) in output accumulator j % 2
+// instead, which is free from the drain of chunk j - 2 until S Q^T (j).
+constexpr uint32_t TT_S = 0, TT_SW = 128, TT_O = 192, TT_QK = 320, TT_SLO = 320, TT_DH = 384,
                    TT_DL = 416, TT_DSH = 448, TT_DSL = 480;
 constexpr uint32_t TM_COLS = 512;
 // Linear mode: delta (= V, exact bf16 pairs) and delta~ (hi / lo) of chunk j in buffer
@@ -592,7 +593,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
     // delta^T P^T (j); S Q^T is issued by aux O and Q K^T by
     // aux P, so that the issue work is spread over three warp schedulers.  Each kind is
     // issued in chunk order; the warp polls (non-blocking tests), U first.
-    int nu = 0, nd = 0;  // next U, delta^T P^T
+    int nu = 0, ns = 0, nd = 0;  // next U, S Q^T, delta^T P^T
     uint64_t t_idle = globaltimer_ns();
     #pragma unroll 1
     while (nd < u.nc) {
@@ -604,15 +605,21 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             mbar_test(&bars[SB_HF + (i & 1)], (i >> 1) & 1, true))
           kind = 0;
       }
-      if (kind < 0 && nd < nu && (nu > nd + 1 || nu == u.nc)) {
-        // delta of chunk j in TMEM, P(j) published, and S Q^T (j), which starts the
-        // output accumulator, completed (it comes from another thread); U^T (j + 1) goes
-        // into the tensor pipe first
+      if (kind < 0 && ns < u.nc) {
+        // S Q^T (i) starts output accumulator i % 2 once the chain has queued S W~^T (i),
+        // which reads the same bf16 S (and waited for the chunk's stage), and aux P has
+        // published P (i): it read its Q K^T out of that accumulator (and, in the
+        // strong-decay form, scaled Q)
+        const int i = ns;
+        if (mbar_test(&bars[SB_SWI], i & 1, false) &&
+            mbar_test(&bars[SB_PF + (i & 1)], (i >> 1) & 1, false))
+          kind = 1;
+      }
+      if (kind < 0 && nd < ns && (nu > nd + 1 || nu == u.nc)) {
+        // delta of chunk j in TMEM; S Q^T (j), issued before by this thread into the same
+        // accumulator, runs first; U^T (j + 1) goes into the tensor pipe first
         const int j = nd;
-        if (mbar_test(&bars[SB_DR + (j & 1)], (j >> 1) & 1, false) &&
-            mbar_test(&bars[SB_PF + (j & 1)], (j >> 1) & 1, false) &&
-            mbar_test(&bars[SB_SQ + (j & 1)], (j >> 1) & 1, false))
-          kind = 2;
+        if (mbar_test(&bars[SB_DR + (j & 1)], (j >> 1) & 1, false)) kind = 2;
       }
       const bool did = kind >= 0;
       if (did) {
@@ -629,6 +636,12 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             mma_k64<false, false, false>(d, dv, 0, desc_k(hs + HS_TUL, 0, 8192), id_u, 1);
             mma_commit(&bars[SB_U + (i & 1)]);
           }
+        } else if (kind == 1) {
+          const int i = ns++;
+          if (lane == 0)  // O = S Q^T (i), S as hi (shared memory) + lo (TMEM)
+            sq_hilo_commit(tmem + TT_O + 64 * (i & 1), desc_k(sm + ST_SB, 0, 16384),
+                           tmem + TT_SLO, desc_k(sm + ST_QK + (i % ST_NST) * ST_STAGE, 0, 16384),
+                           idesc_bf16(128, 64, 0, 0), &bars[SB_SQ + (i & 1)]);
         } else {
           const int j = nd++;
           if (lane == 0) {  // += delta^T P^T (j): hi*hi + hi*lo + lo*hi
@@ -636,7 +649,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
             const uint8_t* ps = sm + ST_PS + (j & 1) * PS_BYTES;
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
             const uint64_t ph = desc_k(ps, 0, 8192), pl = desc_k(ps + 8192, 0, 8192);
-            const uint32_t d = tmem + TT_O;  // the one output accumulator of the delta rule
+            const uint32_t d = tmem + TT_O + 64 * (j & 1);
             mma_k64<true, false, false>(d, 0, tmem + TT_DH, ph, id, 1);
             mma_k64<true, false, false>(d, 0, tmem + TT_DH, pl, id, 1);
             mma_k64<true, false, false>(d, 0, tmem + TT_DL, ph, id, 1);
@@ -846,14 +859,20 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       const float* EG = GN + 64;
       AP_WAIT(&bars[SB_QK_FULL + s], (j / ST_NST) & 1);
       const bool factored = flags[s] != 0;
+      // the delta rule accumulates Q K^T in output accumulator b, free once the outputs of
+      // chunk j - 2 (which also leave P slot b) were drained
+      const uint32_t t_qk = LINEAR ? TT_QK : TT_O + 64 * b;
+      if constexpr (!LINEAR) AP_WAIT(&bars[SB_PE + b], ((j >> 1) & 1) ^ 1);
 
       // ---- Q K^T as an M=64 accumulator (row m in TMEM lane 32 (m / 16) + m % 16, so
       //      every warp of this group holds 16 rows), issued from warp 6 ----
-      if (atid == 64)
-        mma_k128_commit(tmem + TT_QK, desc_k(stg, 0, 16384), desc_k(stg + 8192, 0, 16384),
+      if (atid == 64) {
+        tc_fence_after();
+        mma_k128_commit(tmem + t_qk, desc_k(stg, 0, 16384), desc_k(stg + 8192, 0, 16384),
                         idesc_bf16(64, 64, 0, 0), &bars[SB_QKM]);
+      }
       AP_WAIT(&bars[SB_QKM], j & 1);
-      AP_WAIT(&bars[SB_PE + b], ((j >> 1) & 1) ^ 1);  // outputs of chunk j - 2 left slot b
+      if constexpr (LINEAR) AP_WAIT(&bars[SB_PE + b], ((j >> 1) & 1) ^ 1);  // slot b is free
       tc_fence_after();
       // factored:  P'_{t,j} = q_t.k_j e^{-g_j}      (the e^{g_t} is applied to the outputs)
       // otherwise: P_{t,j}  = q_t.k_j e^{g_t - g_j} (and Q is scaled by e^{g_t} below)
@@ -861,9 +880,9 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
         // the TMEM loads are warp-wide; lanes 16..31 of each warp hold no row
         const int prow = 16 * q4 + (lane & 15);
         if (factored)
-          aux_epi_p<true>(tq + TT_QK, ps, prow, 0.f, GN, lane < 16);
+          aux_epi_p<true>(tq + t_qk, ps, prow, 0.f, GN, lane < 16);
         else
-          aux_epi_p<false>(tq + TT_QK, ps, prow, GN[prow], GN, lane < 16);
+          aux_epi_p<false>(tq + t_qk, ps, prow, GN[prow], GN, lane < 16);
       }
       if (!factored) {
         // Q <- diag(e^{g}) Q in place (bf16), after Q K^T has read it: 16-byte pieces,
@@ -900,31 +919,24 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
   // aux O holds no stage: each of its warps recomputes the chunk's gate factors from
   // the gates in global memory (the same scan as the producer, so the same values and
   // the same choice of form), and the bf16 outputs are staged in the chunk's P slot,
-  // which delta^T P^T no longer reads.  It also issues S Q^T, one issue site: the delta
-  // rule has one output accumulator, drained (outputs of chunk i - 1) before S Q^T (i)
-  // starts it again, with S as hi + lo terms; the linear mode has two, so S Q^T (i)
-  // goes into accumulator i % 2 before the outputs of chunk i - 1 are drained.
+  // which delta^T P^T no longer reads.  In the linear mode it also issues S Q^T (i) into
+  // output accumulator i % 2 before it drains the outputs of chunk i - 1 out of the other
+  // one (one issue site); in the delta rule the MMA warp issues S Q^T.
   const int atid = tid - 256;
 #define AO_WAIT(bar, par) \
   if (group_wait_fails((bar), (par), abort_flag, false, 3, 128)) break;
-  // S Q^T (i): issued (from warp 11) once the chain has queued S W~^T (i), which reads
-  // the same bf16 S, and, in the strong-decay form, once aux P has scaled Q.  The
-  // chunk's form is read from its stage, which the chain waited for before signalling.
+  // Linear mode, S Q^T (i): issued (from warp 11) once the chain has queued S W~^T (i),
+  // which reads the same bf16 S, and, in the strong-decay form, once aux P has scaled Q.
+  // The chunk's form is read from its stage, which the chain waited for before signalling.
 #define AO_ISSUE_SQ(i)                                                                          \
   {                                                                                           \
     AO_WAIT(&bars[SB_SWI], (i) & 1);                                                          \
     const int si = (i) % ST_NST;                                                              \
     if (flags[si] == 0) AO_WAIT(&bars[SB_PF + ((i) & 1)], ((i) >> 1) & 1);                    \
-    if (atid == 96) {                                                                         \
-      if constexpr (LINEAR)                                                                   \
-        mma_k128_commit(tmem + TT_O + 64 * ((i) & 1), desc_k(sm + ST_SB, 0, 16384),            \
-                        desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0), \
-                        &bars[SB_SQ + ((i) & 1)]);                                            \
-      else                                                                                    \
-        sq_hilo_commit(tmem + TT_O, desc_k(sm + ST_SB, 0, 16384), tmem + TT_SLO,              \
-                       desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),  \
-                       &bars[SB_SQ + ((i) & 1)]);                                             \
-    }                                                                                         \
+    if (atid == 96)                                                                           \
+      mma_k128_commit(tmem + TT_O + 64 * ((i) & 1), desc_k(sm + ST_SB, 0, 16384),              \
+                      desc_k(sm + ST_QK + si * ST_STAGE, 0, 16384), idesc_bf16(128, 64, 0, 0),   \
+                      &bars[SB_SQ + ((i) & 1)]);                                              \
   }
   GateLoad gnext = load_gates(log_alpha, beta, u, H, 0, lane);
   #pragma unroll 1
@@ -943,7 +955,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       AO_WAIT(&bars[SB_DP + b], (j >> 1) & 1);
       tc_fence_after();
       // ---- bf16 outputs staged in P slot b (row t at t * 256 bytes), 8 tokens a step ----
-      const uint32_t to = tq + TT_O + (LINEAR ? 64 * b : 0);
+      const uint32_t to = tq + TT_O + 64 * b;
 #pragma unroll 1
       for (int q = 0; q < 8; ++q) {
         uint32_t a[8];
@@ -972,7 +984,6 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
       named_sync(3, 128);
       if (atid == 0) mbar_arrive(&bars[SB_PE + b]);  // P slot b may be refilled
     }
-    if (!LINEAR && i < u.nc) AO_ISSUE_SQ(i)
   }
 #undef AO_ISSUE_SQ
 #undef AO_WAIT
