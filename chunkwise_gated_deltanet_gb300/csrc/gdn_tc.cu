@@ -827,9 +827,21 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
               st4(S_final + u.sidx + (size_t)row * kD + 32 * p + 4 * q, v[4 * q], v[4 * q + 1],
                   v[4 * q + 2], v[4 * q + 3]);
         } else {
+          // bf16 S (the hi term) into shared memory and, in the delta rule, the lo term
+          // bf16(S - hi) into TMEM (S Q^T (j), the last reader of both, completed)
+          uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) st_sw128_8(sm + ST_SB, row, 32 * p + 8 * q, 128, v + 8 * q);
-          if constexpr (!LINEAR) state_lo_to_tmem(tq, p, v);  // S Q^T (j + 1) has read the last
+          for (int e = 0; e < 16; ++e) {
+            hi[e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+            if constexpr (!LINEAR)
+              lo[e] = pack_bf16(v[2 * e] - __uint_as_float(hi[e] << 16),
+                                v[2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u));
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st_shared_v4(smem_u32(sm + ST_SB + sw128_offset(row, 32 * p + 8 * q, 128)), hi[4 * q],
+                         hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+          if constexpr (!LINEAR) tmem_st16(tq + TT_SLO + 16 * p, lo);
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(gam * v[e]);
           tmem_st32(tq + TT_S + 32 * p, r);
