@@ -519,7 +519,7 @@ def run_bwd(args, w, world, rank, local):
     path = {"auto": gdn.GDN_BWD_AUTO, "tokens": gdn.GDN_BWD_TOKENS,
             "chunked": gdn.GDN_BWD_CHUNKED}[args.bwd_path]
     taken = gdn.gdn_bwd_select_path(dk, dv, inp["q"].dtype) if path == gdn.GDN_BWD_AUTO else path
-    launches = 28 if taken == gdn.GDN_BWD_CHUNKED and B * T > 0 else 2
+    launches = 25 if taken == gdn.GDN_BWD_CHUNKED and B * T > 0 else 2
 
     def step():
         gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"],

@@ -37,10 +37,12 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
 #include "gdn_internal.h"
+#include "tc_common.cuh"
 
 namespace gdn {
 namespace {
@@ -229,39 +231,72 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
 }
 
 // ---------------------------------------------------------------------------------
-// Batched GEMM with fp32 accuracy: for every live batch entry b,
-//   C(m, n) = alpha * sum_k A(m, k) * ks[k] * B(k, n) * cs[n]   (+ C(m, n) with accum)
-// A(m, k) = A[b*ab + m*am + k*ak] (likewise B and C), so either operand may be read
-// transposed; one of each operand's two strides is 1.  ks, cs: optional per-entry
-// vectors (stride vb).  mask 1 keeps n <= m, mask 2 n < m.  With C2, the product is also
-// written there times Dg(m, n) = e^{g_m - g_n} for n <= m (0 above), g = gv.
+// Batched GEMM with fp32 accuracy: for every live batch entry b, the sum of one or two
+// products (terms t)
+//   C(m, n) = alpha * sum_t sum_k A_t(m, k) * ks_t[k] * B_t(k, n) * bs_t[n]
+// A_t(m, k) = A_t[b*ab + m*am + k*ak] (likewise B_t and C), so either operand may be read
+// transposed; one of each operand's two strides is 1, and C's column stride is 1.  ks_t,
+// bs_t: optional per-entry vectors (stride vb).  mask 1 keeps n <= m, mask 2 n < m.  With
+// C2, the product is also written there times Dg(m, n) = e^{g_m - g_n} for n <= m (0
+// above), g = gv.  M and N are 64 or 128, each term's K 64 or 128: every entry's whole
+// product is one tile.
 //
-// On the tensor cores in three TF32 passes: each fp32 operand is split into two TF32
-// parts and hi*hi + hi*lo + lo*hi is accumulated in fp32 (~2^-22 relative error per
-// product, the fp32 level).  One CTA of 4 warps per 64 x 64 output tile and entry; warp w
-// owns a 32 x 32 quarter as 2 x 4 m16n8k8 tiles.  32-deep K slices of both operands come
-// into a two-stage shared-memory ring by cp.async, each in its own orientation (rows of
-// 36 floats when contiguous in k, of 72 when contiguous in m or n), which keeps every
-// fragment read free of bank conflicts.  M, N multiples of 64, K of 32 and at most 128.
-struct Mm {
+// On the tcgen05 tensor cores in three TF32 passes: each fp32 operand is split into two
+// TF32 parts and lo*hi + hi*lo + hi*hi is accumulated in fp32 in tensor memory (~2^-22
+// relative error per product, the fp32 level).  A persistent CTA walks the live entries
+// (b = blockIdx.x, + gridDim.x, ...) with four roles joined by mbarriers:
+//   warp 0     TMA: 32-deep k panels of both operands, as stored, into a raw ring of 3 to 8
+//              slots (as many as fit: the loads in flight are what the CTA's bandwidth
+//              rests on); a panel contiguous in k lands in the MMA's K-major
+//              128-byte-swizzled layout already, one contiguous in m or n as [32 k][rows];
+//   warps 2-9  split: each raw panel into TF32 hi and lo panels, K-major and swizzled,
+//              scaled on the way (a ring of 2 to 4 slots); the transposing reads of a plain
+//              panel go down its columns, one row per lane, free of bank conflicts;
+//   warp 1     MMA: 12 tcgen05.mma (kind::tf32) per panel into one of two accumulators,
+//              as C^T = B^T A^T: the columns n of C are the TMEM lanes;
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator (a thread per column n, 32 rows m
+//              per load), alpha, mask, C2, and the stores (a warp writes 32
+//              consecutive n of a row m per instruction).
+// Every wait is bounded; one that gives up stops the CTA and records a code in the
+// library's status word (read by gdn_check_status).
+struct MmTerm {
   const float* A;
   long long ab;
   int am, ak;
   const float* B;
   long long bb;
   int bk, bn;
+  const float *ks, *bs;
+  int K;
+};
+
+struct Mm {
+  MmTerm t[2];
+  int nt;  // 1 or 2 terms
   float* C;
   long long cb;
   int cm, cn;
   float* C2;
-  const float *ks, *cs, *gv;
+  const float* gv;
   long long vb;
   float alpha;
-  int accum, mask, M, N, K;
+  int mask, M, N;
   const long long* nlive;
 };
 
-constexpr int kMmThreads = 128, kMmStage = 2304, kMmKMax = 128;
+struct MmArgs {
+  Mm m;
+  int akc[2], bkc[2];  // 1: the operand is contiguous in k
+  int np0, np;         // k panels of the first term, of both
+  int* status;
+};
+
+constexpr int kMmSplitThreads = 256;  // 8 split warps
+constexpr int kMmThreads = 64 + kMmSplitThreads + 128;
+constexpr int kMmRing = 229376;       // both rings: 2 to 4 split slots, 3 to 8 raw slots
+constexpr int kMmMaxRaw = 8, kMmMaxSplit = 4;
+constexpr int kMmSmem = kMmRing + 1024;
+constexpr int kMmTmemCols = 256;      // two accumulators of up to 128 columns
 
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
   const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
@@ -271,22 +306,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Slice k0..k0+31 of a 64-row operand X(r, k) = X[r*rs + k*ks_] into S: [r][36] when
-// ks_ == 1, else [k][72] (then rs == 1).
-__device__ __forceinline__ void mm_issue(float* S, const float* X, int rs, int ks_, int r0, int k0) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + kMmThreads * i;  // 512 chunks of 16 bytes
-    if (ks_ == 1) {
-      const int r = idx >> 3, k = 4 * (idx & 7);
-      cp_async16(S + r * 36 + k, X + (long long)(r0 + r) * rs + k0 + k);
-    } else {
-      const int k = idx >> 4, r = 4 * (idx & 15);
-      cp_async16(S + k * 72 + r, X + (long long)(k0 + k) * ks_ + r0 + r);
-    }
-  }
 }
 
 __device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
@@ -304,95 +323,286 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__global__ void __launch_bounds__(kMmThreads) ck_mm_kernel(Mm p) {
-  const long long b = blockIdx.x;
-  if (b >= *p.nlive) return;
-  __shared__ __align__(16) float sA[2][kMmStage], sB[2][kMmStage];
-  __shared__ float sK[kMmKMax];
-  const int tilesN = p.N / 64;
-  const int m0 = (blockIdx.y / tilesN) * 64, n0 = (blockIdx.y % tilesN) * 64;
-  const float* A = p.A + b * p.ab;
-  const float* B = p.B + b * p.bb;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
-  const int wm = (warp >> 1) * 32, wn = (warp & 1) * 32;
-  // B(k, n) as rows n of X: stride bn, inner bk.
-  mm_issue(sA[0], A, p.am, p.ak, m0, 0);
-  mm_issue(sB[0], B, p.bn, p.bk, n0, 0);
-  cp_async_commit();
-  if (tid < p.K) sK[tid] = p.ks ? p.ks[b * p.vb + tid] : 1.f;
-  const bool akc = p.ak == 1, bkc = p.bk == 1;
-  float acc[8][4];
+// Instruction descriptor, kind::tf32: fp32 accumulator, TF32 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+// One thread: D(tmem) (+)= A(smem) B(smem)^T, kind::tf32.
+__device__ __forceinline__ void umma_tf32(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+// One raw k panel of an operand (R rows, k0 = its first k) into TF32 hi and lo panels,
+// K-major with the 128-byte swizzle (row r at r * 128 bytes, 16-byte chunk c of it at
+// (c ^ r % 8) * 16).  KC: the raw panel has that layout already (TMA with the swizzle);
+// else it is [32 k][R] plain fp32, read down its columns (one row per lane).  ks, rs:
+// optional scales per k and per row.  kMmSplitThreads threads, ts = 0 .. kMmSplitThreads - 1; each takes
+// R * 8 / kMmSplitThreads 16-byte chunks, loaded together before any is converted.
+template <int R, bool KC>
+__device__ __forceinline__ void mm_split(const uint8_t* raw, uint8_t* hi, uint8_t* lo,
+                                         const float* __restrict__ ks,
+                                         const float* __restrict__ rs, int k0, int ts) {
+  constexpr int kPer = R * 8 / kMmSplitThreads;
+  float4 x[kPer];
+  int off[kPer];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  const int ns = p.K / 32;
-  for (int sl = 0; sl < ns; ++sl) {
-    if (sl + 1 < ns) {
-      mm_issue(sA[(sl + 1) & 1], A, p.am, p.ak, m0, 32 * (sl + 1));
-      mm_issue(sB[(sl + 1) & 1], B, p.bn, p.bk, n0, 32 * (sl + 1));
-      cp_async_commit();
-      cp_async_wait<1>();
+  for (int i = 0; i < kPer; ++i) {
+    const int t = ts + kMmSplitThreads * i;
+    int c, r;  // logical 16-byte chunk (4 consecutive k) of row r
+    if (KC) {
+      off[i] = 16 * t;
+      r = t >> 3;
+      c = (t & 7) ^ (r & 7);
+      x[i] = *reinterpret_cast<const float4*>(raw + off[i]);
     } else {
-      cp_async_wait<0>();
+      r = t & (R - 1);
+      c = t / R;
+      off[i] = r * 128 + ((c ^ (r & 7)) << 4);
+      const float* rf = reinterpret_cast<const float*>(raw) + 4 * c * R + r;
+      x[i] = make_float4(rf[0], rf[R], rf[2 * R], rf[3 * R]);
     }
-    __syncthreads();
-    const float* SA = sA[sl & 1];
-    const float* SB = sB[sl & 1];
+    if (ks) {
+      const float4 f = *reinterpret_cast<const float4*>(ks + k0 + 4 * c);
+      x[i].x *= f.x; x[i].y *= f.y; x[i].z *= f.z; x[i].w *= f.w;
+    }
+    if (rs) {
+      const float f = rs[r];
+      x[i].x *= f; x[i].y *= f; x[i].z *= f; x[i].w *= f;
+    }
+  }
 #pragma unroll
-    for (int kb = 0; kb < 32; kb += 8) {
-      uint32_t ah[2][4], al[2][4], bh[4][2], bl[4][2];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int m = wm + 16 * mt + g, k = kb + t;
-        const float x0 = akc ? SA[m * 36 + k] : SA[k * 72 + m];
-        const float x1 = akc ? SA[(m + 8) * 36 + k] : SA[k * 72 + m + 8];
-        const float x2 = akc ? SA[m * 36 + k + 4] : SA[(k + 4) * 72 + m];
-        const float x3 = akc ? SA[(m + 8) * 36 + k + 4] : SA[(k + 4) * 72 + m + 8];
-        tf32_split(x0, ah[mt][0], al[mt][0]);
-        tf32_split(x1, ah[mt][1], al[mt][1]);
-        tf32_split(x2, ah[mt][2], al[mt][2]);
-        tf32_split(x3, ah[mt][3], al[mt][3]);
+  for (int i = 0; i < kPer; ++i) {
+    uint4 h, l;
+    tf32_split(x[i].x, h.x, l.x);
+    tf32_split(x[i].y, h.y, l.y);
+    tf32_split(x[i].z, h.z, l.z);
+    tf32_split(x[i].w, h.w, l.w);
+    *reinterpret_cast<uint4*>(hi + off[i]) = h;
+    *reinterpret_cast<uint4*>(lo + off[i]) = l;
+  }
+}
+
+__device__ __forceinline__ void mm_split_any(const uint8_t* raw, uint8_t* hi, uint8_t* lo, int R,
+                                             bool kc, const float* ks, const float* rs, int k0,
+                                             int ts) {
+  if (R == 128) {
+    if (kc) mm_split<128, true>(raw, hi, lo, ks, rs, k0, ts);
+    else mm_split<128, false>(raw, hi, lo, ks, rs, k0, ts);
+  } else {
+    if (kc) mm_split<64, true>(raw, hi, lo, ks, rs, k0, ts);
+    else mm_split<64, false>(raw, hi, lo, ks, rs, k0, ts);
+  }
+}
+
+__global__ void __launch_bounds__(kMmThreads, 1)
+    ck_mm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapB0,
+                 const __grid_constant__ CUtensorMap mapA1, const __grid_constant__ CUtensorMap mapB1,
+                 const MmArgs p) {
+  extern __shared__ uint8_t mm_smem_raw[];
+  uint8_t* sm = mm_smem_raw + ((1024u - (smem_u32(mm_smem_raw) & 1023u)) & 1023u);
+  enum { RF = 0, RE = 8, SF = 16, SE = 20, AF = 24, AE = 26, DONE = 28, NBAR = 29 };
+  __shared__ __align__(8) uint64_t bars[NBAR];
+  __shared__ uint32_t tslot;
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  const Mm& m = p.m;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int M = m.M, N = m.N, np = p.np, np0 = p.np0;
+  const long long nlive = *m.nlive;
+  // one raw slot: a k panel of A and B, (M + N) x 128 bytes; one split slot: its hi and lo
+  // ring depths: as many split slots as leave room for 3 raw slots (2 to 4), then up to
+  // 8 raw slots
+  const int raw_bytes = (M + N) * 128, split_bytes = 2 * raw_bytes;
+  const int ns = max(2, min(kMmMaxSplit, (kMmRing - 3 * raw_bytes) / split_bytes));
+  const int nr = min(kMmMaxRaw, (kMmRing - ns * split_bytes) / raw_bytes);
+  constexpr int kSplitWarps = kMmSplitThreads / 32;
+  if (tid == 0) {
+    for (int i = 0; i < kMmMaxRaw; ++i) {
+      mbar_init(&bars[RF + i], 1);
+      mbar_init(&bars[RE + i], kSplitWarps);
+    }
+    for (int i = 0; i < kMmMaxSplit; ++i) {
+      mbar_init(&bars[SF + i], kSplitWarps);
+      mbar_init(&bars[SE + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[AF + i], 1);
+      mbar_init(&bars[AE + i], 4);
+    }
+    mbar_init(&bars[DONE], 1);
+    abort_s = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tslot, kMmTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  uint8_t* const spl0 = sm;
+  uint8_t* const raw0 = sm + ns * split_bytes;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      prefetch_tensormap(&mapA0);
+      prefetch_tensormap(&mapB0);
+      if (m.nt > 1) {
+        prefetch_tensormap(&mapA1);
+        prefetch_tensormap(&mapB1);
       }
-      const float f0 = sK[32 * sl + kb + t], f1 = sK[32 * sl + kb + t + 4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int n = wn + 8 * nt + g, k = kb + t;
-        const float y0 = bkc ? SB[n * 36 + k] : SB[k * 72 + n];
-        const float y1 = bkc ? SB[n * 36 + k + 4] : SB[(k + 4) * 72 + n];
-        tf32_split(y0 * f0, bh[nt][0], bl[nt][0]);
-        tf32_split(y1 * f1, bh[nt][1], bl[nt][1]);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          mma_tf32(acc[4 * mt + nt], al[mt], bh[nt]);
-          mma_tf32(acc[4 * mt + nt], ah[mt], bl[nt]);
-          mma_tf32(acc[4 * mt + nt], ah[mt], bh[nt]);
+      const uint32_t bytes = (uint32_t)raw_bytes;
+      int q = 0, s = 0, ph = 0;  // panel count, its raw slot and that slot's phase
+      for (long long b = blockIdx.x; b < nlive; b += gridDim.x) {
+        bool ok = true;
+        for (int pn = 0; pn < np; ++pn, ++q) {
+          if (!(ok = wait_bar(&bars[RE + s], ph ^ 1, abort_flag, false))) break;
+          uint8_t* raw = raw0 + s * raw_bytes;
+          mbar_arrive_expect_tx(&bars[RF + s], bytes);
+          const int t = pn >= np0, k0 = 32 * (pn - (t ? np0 : 0));
+          const CUtensorMap* ma = t ? &mapA1 : &mapA0;
+          const CUtensorMap* mb = t ? &mapB1 : &mapB0;
+          if (p.akc[t]) tma_load_3d(raw, ma, &bars[RF + s], k0, 0, (int)b);
+          else tma_load_3d(raw, ma, &bars[RF + s], 0, k0, (int)b);
+          if (p.bkc[t]) tma_load_3d(raw + M * 128, mb, &bars[RF + s], k0, 0, (int)b);
+          else tma_load_3d(raw + M * 128, mb, &bars[RF + s], 0, k0, (int)b);
+          if (++s == nr) { s = 0; ph ^= 1; }
         }
+        if (!ok) break;
+      }
+      // Copies still in flight land before the CTA's shared memory is released: the last
+      // min(q, nr) panels, each in its own slot.
+      for (int u = 0; u < min(q, nr); ++u) {
+        if (--s < 0) { s = nr - 1; ph ^= 1; }
+        (void)mbar_wait(&bars[RF + s], ph, kWaitNs);
+      }
     }
-    __syncthreads();  // this stage is free for slice sl + 2
-  }
-  const float* cs = p.cs ? p.cs + b * p.vb : nullptr;
-  const float* gv = p.gv ? p.gv + b * p.vb : nullptr;
-  float* C = p.C + b * p.cb;
-  float* C2 = p.C2 ? p.C2 + b * p.cb : nullptr;
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer: C^T = B^T A^T, so that C's columns are TMEM lanes
+      const uint32_t id = idesc_tf32(N, M);
+      int i = 0, s = 0, sph = 0;  // item count; split slot and its phase
+      for (long long b = blockIdx.x; b < nlive; b += gridDim.x, ++i) {
+        const int a = i & 1;
+        if (!wait_bar(&bars[AE + a], ((i >> 1) & 1) ^ 1, abort_flag, false)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + 128u * a;
+        bool ok = true;
+        for (int pn = 0; pn < np; ++pn) {
+          if (!(ok = wait_bar(&bars[SF + s], sph, abort_flag, false))) break;
+          tc_fence_after();
+          // descriptors once per panel, advanced 32 bytes (2 units) per 8-deep k step
+          const uint32_t ahi = smem_u32(spl0 + s * split_bytes), alo = ahi + M * 128;
+          const uint32_t bhi = alo + M * 128, blo = bhi + N * 128;
+          const uint64_t dah = smem_desc(ahi, 16, 1024), dal = smem_desc(alo, 16, 1024);
+          const uint64_t dbh = smem_desc(bhi, 16, 1024), dbl = smem_desc(blo, 16, 1024);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t o = 2u * kk;
+            umma_tf32(d, dbl + o, dah + o, id, (pn | kk) != 0);
+            umma_tf32(d, dbh + o, dal + o, id, 1u);
+            umma_tf32(d, dbh + o, dah + o, id, 1u);
+          }
+          mma_commit(&bars[SE + s]);
+          if (++s == ns) { s = 0; sph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(&bars[AF + a]);
+      }
+      // Every MMA issued is complete before tensor memory is freed.
+      mma_commit(&bars[DONE]);
+      (void)mbar_wait(&bars[DONE], 0, kWaitNs);
+    }
+  } else if (warp < 2 + kSplitWarps) {  // split
+    const int ts = tid - 64;
+    int r = 0, rph = 0, s = 0, sph = 0;  // raw and split slots and their phases
+    for (long long b = blockIdx.x; b < nlive; b += gridDim.x) {
+      bool ok = true;
+      for (int pn = 0; pn < np; ++pn) {
+        ok = wait_bar(&bars[RF + r], rph, abort_flag, false) &&
+             wait_bar(&bars[SE + s], sph ^ 1, abort_flag, false);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t* raw = raw0 + r * raw_bytes;
+        uint8_t* spl = spl0 + s * split_bytes;
+        const int t = pn >= np0;
+        const MmTerm& tm = m.t[t];
+        const float* ks = tm.ks ? tm.ks + b * m.vb : nullptr;
+        const float* bs = tm.bs ? tm.bs + b * m.vb : nullptr;
+        mm_split_any(raw, spl, spl + M * 128, M, p.akc[t], nullptr, nullptr, 0, ts);
+        mm_split_any(raw + M * 128, spl + 2 * M * 128, spl + 2 * M * 128 + N * 128, N, p.bkc[t],
+                     ks, bs, 32 * (pn - (t ? np0 : 0)), ts);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[SF + s]);
+          mbar_arrive(&bars[RE + r]);
+        }
+        if (++r == nr) { r = 0; rph ^= 1; }
+        if (++s == ns) { s = 0; sph ^= 1; }
+      }
+      if (!ok) break;
+    }
+  } else {  // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, one column n of C each
+    const int qd = warp & 3;
+    const bool valid = N == 128 || lane < 16;
+    // an accumulator of 64 lanes keeps column n in lane 32 (n / 16) + n % 16
+    const int n = (N == 128 ? 32 : 16) * qd + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+    int i = 0;
+    for (long long b = blockIdx.x; b < nlive; b += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (warp_wait_fails(&bars[AF + a], (i >> 1) & 1, abort_flag, false)) break;
+      tc_fence_after();
+      const float* gv = m.gv ? m.gv + b * m.vb : nullptr;
+      const float scale = m.alpha;
+      // Dg(m, n) = 2^{(g_m - g_n) log2 e} by ex2.approx (relative error ~2^-22)
+      const float gn = (gv && valid) ? gv[n] * kLog2e : 0.f;
+      float* C = m.C + b * m.cb + n;
+      float* C2 = m.C2 ? m.C2 + b * m.cb + n : nullptr;
+      for (int mb = 0; mb < M / 32; ++mb) {
+        uint32_t r[32];
+        tmem_ld32(tl + 128u * a + 32u * mb, r);
+        const float gml = gv ? gv[32 * mb + lane] * kLog2e : 0.f;
+        tmem_wait_ld();
+        if (mb == M / 32 - 1) {  // the accumulator is free for the MMA warp
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[AE + a]);
+        }
+        float x[32];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // fragment element j of tile (i / 4, i % 4): rows g and g + 8, columns 2t and 2t + 1
-      const int m = m0 + wm + 16 * (i >> 2) + g + 8 * (j >> 1);
-      const int n = n0 + wn + 8 * (i & 3) + 2 * t + (j & 1);
-      float x = p.alpha * acc[i][j];
-      if (cs) x *= cs[n];
-      if (C2) C2[(long long)m * p.cm + (long long)n * p.cn] = n <= m ? x * expf(gv[m] - gv[n]) : 0.f;
-      if ((p.mask == 1 && n > m) || (p.mask == 2 && n >= m)) x = 0.f;
-      float* o = C + (long long)m * p.cm + (long long)n * p.cn;
-      *o = p.accum ? *o + x : x;
+        for (int j = 0; j < 32; ++j) x[j] = scale * __uint_as_float(r[j]);
+        if (C2) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int mm = 32 * mb + j;
+            const float gm = __shfl_sync(0xffffffffu, gml, j);
+            if (valid) C2[(long long)mm * m.cm] = n <= mm ? x[j] * ex2(gm - gn) : 0.f;
+          }
+        }
+        if (!valid) continue;
+        if (m.mask) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int mm = 32 * mb + j;
+            if ((m.mask == 1 && n > mm) || (m.mask == 2 && n >= mm)) x[j] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) C[(long long)(32 * mb + j) * m.cm] = x[j];
+      }
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kMmTmemCols);
+  }
+  if (tid == 0 && *abort_flag) atomicOr(p.status, *abort_flag);
 }
 
 // ---------------------------------------------------------------------------------
@@ -666,8 +876,8 @@ __global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
 }
 
 // ---------------------------------------------------------------------------------
-// Per (chunk, head), from dA = strictly-lower(-T^T dT T^T): X = dA o D o beta_i, the
-// row sums of dA o KK^T o D (the triangular solve's part of dbeta) and
+// Per (chunk, head), from dA = strictly-lower(-T^T dT T^T): X + X^T with X = dA o D o beta_i
+// (the operand of dK's X K + X^T K), the row sums of dA o KK^T o D (the triangular solve's part of dbeta) and
 // dg1 = rowsum(dD o D) - colsum(dD o D) with dD = dA beta_i KK^T + dP o QK^T.
 struct DaArgs {
   const float *dA, *KK, *QK, *dPm, *gates;
@@ -691,7 +901,10 @@ __global__ void __launch_bounds__(256) ck_da_kernel(DaArgs p) {
     const int i = idx >> 6, j = idx & 63;
     const float Dij = j <= i ? expf(g[i] - g[j]) : 0.f;
     const float da = p.dA[ob + idx], kk = p.KK[ob + idx];
-    p.X[ob + idx] = da * Dij * be[i];
+    // X + X^T: dA is strictly lower, so each element takes the one of X(i, j), X(j, i)
+    // that can be nonzero
+    const int hi = i > j ? i : j, lo = i > j ? j : i;
+    p.X[ob + idx] = i == j ? 0.f : p.dA[ob + hi * kCk + lo] * expf(g[hi] - g[lo]) * be[hi];
     E1[i][j] = da * kk * Dij;
     E2[i][j] = (da * be[i] * kk + p.dPm[ob + idx] * p.QK[ob + idx]) * Dij;
   }
@@ -849,35 +1062,85 @@ CkLayout ck_layout(long long rows, int H, int D, int N) {
   return L;
 }
 
+// Tensor map of one operand over all entries: a [32 k] x [rows] box per k panel, with the
+// 128-byte swizzle when the operand is contiguous in k (the MMA's K-major layout), plain
+// when it is contiguous in its rows (then split and transposed on chip).
+bool mm_map(CUtensorMap* map, const float* base, long long nb, long long bstride, int rows,
+            int K, int row_stride, int k_stride) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  const bool kc = k_stride == 1;
+  cuuint64_t dims[3] = {(cuuint64_t)(kc ? K : rows), (cuuint64_t)(kc ? rows : K), (cuuint64_t)nb};
+  cuuint64_t strides[2] = {(cuuint64_t)(kc ? row_stride : k_stride) * 4, (cuuint64_t)bstride * 4};
+  cuuint32_t box[3] = {(cuuint32_t)(kc ? 32 : rows), (cuuint32_t)(kc ? rows : 32), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             kc ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct MmLauncher {
   long long nb;
   const long long* nlive;
   cudaStream_t s;
+  int* status;
+  int grid;
   cudaError_t err = cudaSuccess;
   // C = alpha * op(A) op(B), operands given by (pointer, batch stride, row stride,
   // inner stride); see ck_mm_kernel.
   Mm make(const float* A, long long ab, int am, int ak, const float* B, long long bb, int bk,
           int bn, float* C, long long cb, int cm, int cn, int M, int N, int K) const {
     Mm m;
-    m.A = A; m.ab = ab; m.am = am; m.ak = ak;
-    m.B = B; m.bb = bb; m.bk = bk; m.bn = bn;
+    m.nt = 1;
+    m.t[0] = MmTerm{A, ab, am, ak, B, bb, bk, bn, nullptr, nullptr, K};
+    m.t[1] = m.t[0];
     m.C = C; m.cb = cb; m.cm = cm; m.cn = cn;
     m.C2 = nullptr;
-    m.ks = m.cs = m.gv = nullptr;
+    m.gv = nullptr;
     m.vb = (long long)kGates * kCk;
-    m.alpha = 1.f; m.accum = 0; m.mask = 0;
-    m.M = M; m.N = N; m.K = K;
+    m.alpha = 1.f; m.mask = 0;
+    m.M = M; m.N = N;
     m.nlive = nlive;
     return m;
   }
+  // A second term, + op(A) op(B) (same M and N), summed on the tensor cores.
+  static void add(Mm& m, const float* A, long long ab, int am, int ak, const float* B, long long bb,
+                  int bk, int bn, int K) {
+    m.t[1] = MmTerm{A, ab, am, ak, B, bb, bk, bn, nullptr, nullptr, K};
+    m.nt = 2;
+  }
   void run(const Mm& m) {
     if (err != cudaSuccess) return;
-    if (m.M % 64 || m.N % 64 || m.K % 32 || m.K > kMmKMax || (m.am != 1 && m.ak != 1) ||
-        (m.bk != 1 && m.bn != 1)) {
+    auto dim_ok = [](int x) { return x == 64 || x == 128; };
+    bool ok = dim_ok(m.M) && dim_ok(m.N) && m.cn == 1 && (m.nt == 1 || m.nt == 2) && nb > 0 &&
+              nb <= 0x7fffffffLL;
+    for (int t = 0; ok && t < m.nt; ++t) {
+      const MmTerm& x = m.t[t];
+      ok = dim_ok(x.K) && (x.am == 1 || x.ak == 1) && (x.bk == 1 || x.bn == 1);
+    }
+    if (!ok) {
       err = cudaErrorInvalidValue;
       return;
     }
-    ck_mm_kernel<<<dim3((unsigned)nb, (unsigned)((m.M / 64) * (m.N / 64))), kMmThreads, 0, s>>>(m);
+    MmArgs a;
+    a.m = m;
+    CUtensorMap map[2][2];
+    for (int t = 0; t < 2; ++t) {
+      const MmTerm& x = m.t[t < m.nt ? t : 0];
+      a.akc[t] = x.ak == 1;
+      a.bkc[t] = x.bk == 1;
+      if (!mm_map(&map[t][0], x.A, nb, x.ab, m.M, x.K, x.am, x.ak) ||
+          !mm_map(&map[t][1], x.B, nb, x.bb, m.N, x.K, x.bn, x.bk)) {
+        err = cudaErrorInvalidValue;
+        return;
+      }
+    }
+    a.np0 = m.t[0].K / 32;
+    a.np = a.np0 + (m.nt > 1 ? m.t[1].K / 32 : 0);
+    a.status = status;
+    ck_mm_kernel<<<(unsigned)grid, kMmThreads, kMmSmem, s>>>(map[0][0], map[0][1], map[1][0],
+                                                             map[1][1], a);
     err = cudaGetLastError();
   }
 };
@@ -956,8 +1219,19 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   ck_gather_kernel<D, TIn><<<nb, 256, 0, s>>>(ga);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
+  // The product kernel: persistent, one CTA per SM at most; its shared-memory cap is
+  // raised here, before any side-stream work exists.
+  static std::atomic<unsigned long long> set_mm{0};
+  if ((e = ensure_smem_cap(ck_mm_kernel, kMmSmem, set_mm)) != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  int* status = nullptr;
+  if ((e = tc_status_address(&status)) != cudaSuccess) return e;
+  const int mm_grid = (int)std::min<long long>(L.nb, std::max(sms, 1));
   const long long CD = (long long)kCk * D, CC = (long long)kCk * kCk, DD = (long long)D * D;
-  MmLauncher mm{L.nb, nlive, s};
+  MmLauncher mm{L.nb, nlive, s, status, mm_grid};
   // KK^T = K K^T, QK^T = Q K^T
   mm.run(mm.make(Kc, CD, D, 1, Kc, CD, 1, D, KK, CC, kCk, 1, kCk, kCk, D));
   mm.run(mm.make(Qc, CD, D, 1, Kc, CD, 1, D, QK, CC, kCk, 1, kCk, kCk, D));
@@ -983,21 +1257,21 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   // ordered after all side-stream work: the caller may free the workspace as soon as
   // its own stream has passed this call.
   SideJoin join{side, s2, s};
-  MmLauncher mm2{L.nb, nlive, s2};
+  MmLauncher mm2{L.nb, nlive, s2, status, mm_grid};
   {  // Y = P^T dO,  Z = dO^T diag(e^g) Q
     mm2.run(mm2.make(P, CC, 1, kCk, dOc, CD, D, 1, Y, CD, D, 1, kCk, D, kCk));
     Mm m = mm2.make(dOc, CD, 1, D, Qc, CD, D, 1, Z, DD, D, 1, D, D, kCk);
-    m.ks = gates + G_EG * kCk;
+    m.t[0].ks = gates + G_EG * kCk;
     mm2.run(m);
   }
   if (mm2.err != cudaSuccess) return mm2.err;
   if ((e = cudaEventRecord(side->yz, s2)) != cudaSuccess) return e;
   {  // W~ = T diag(beta e^g) K,  U = T diag(beta) V
     Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
-    m.ks = gates + G_BEG * kCk;
+    m.t[0].ks = gates + G_BEG * kCk;
     mm.run(m);
     m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
-    m.ks = gates + G_BETA * kCk;
+    m.t[0].ks = gates + G_BETA * kCk;
     mm.run(m);
   }
   if (mm.err != cudaSuccess) return mm.err;
@@ -1011,7 +1285,7 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // The side stream continues with the products of delta and S (dO delta^T, (dP o D) K,
-  // (dP o D)^T Q, dO S) while this stream runs the reverse chain.
+  // dO S) while this stream runs the reverse chain.
   if ((e = cudaEventRecord(side->fwd, s)) != cudaSuccess) return e;
   if ((e = cudaStreamWaitEvent(s2, side->fwd, 0)) != cudaSuccess) return e;
   {
@@ -1021,9 +1295,8 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
     m.C2 = dPD;
     m.gv = gates + G_G * kCk;
     mm2.run(m);
-    // (dP o D) K, (dP o D)^T Q, dO S
+    // (dP o D) K, dO S
     mm2.run(mm2.make(dPD, CC, kCk, 1, Kc, CD, D, 1, dQa, CD, D, 1, kCk, D, kCk));
-    mm2.run(mm2.make(dPD, CC, 1, kCk, Qc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk));
     mm2.run(mm2.make(dOc, CD, D, 1, S, DD, D, 1, dOS, CD, D, 1, kCk, D, D));
   }
   if (mm2.err != cudaSuccess) return mm2.err;
@@ -1047,11 +1320,9 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
     mm.run(mm.make(Tm, CC, 1, kCk, dW, CD, D, 1, TdW, CD, D, 1, kCk, D, kCk));
     // dT = d delta (beta o V)^T + dW (beta e^g o K)^T
     m = mm.make(dDl, CD, D, 1, Vc, CD, 1, D, dT, CC, kCk, 1, kCk, kCk, D);
-    m.cs = gates + G_BETA * kCk;
-    mm.run(m);
-    m = mm.make(dW, CD, D, 1, Kc, CD, 1, D, dT, CC, kCk, 1, kCk, kCk, D);
-    m.cs = gates + G_BEG * kCk;
-    m.accum = 1;
+    m.t[0].bs = gates + G_BETA * kCk;
+    MmLauncher::add(m, dW, CD, D, 1, Kc, CD, 1, D, D);
+    m.t[1].bs = gates + G_BEG * kCk;
     mm.run(m);
     // dA = strictly-lower(-T^T dT T^T)
     m = mm.make(Tm, CC, 1, kCk, dT, CC, kCk, 1, M1, CC, kCk, 1, kCk, kCk, kCk);
@@ -1065,18 +1336,15 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   float* db3 = F(L.db3);
   float* dg1 = F(L.dg1);
   float* sdot = F(L.sdot);
-  // Join: the dA terms need dP, and dK accumulates onto (dP o D)^T Q.
+  // Join: the dA terms need dP, and dK needs dP o D.
   if ((e = cudaStreamWaitEvent(s, side->side, 0)) != cudaSuccess) return e;
   join.done = true;
   DaArgs da{dA, KK, QK, dPm, gates, X, db3, dg1, nlive};
   ck_da_kernel<<<nb, 256, 0, s>>>(da);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  {  // dK += X K + X^T K
-    Mm m = mm.make(X, CC, kCk, 1, Kc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk);
-    m.accum = 1;
-    mm.run(m);
-    m = mm.make(X, CC, 1, kCk, Kc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk);
-    m.accum = 1;
+  {  // dK's products: (dP o D)^T Q + X K + X^T K, with X + X^T made by the dA kernel
+    Mm m = mm.make(dPD, CC, 1, kCk, Qc, CD, D, 1, dKa, CD, D, 1, kCk, D, kCk);
+    MmLauncher::add(m, X, CC, kCk, 1, Kc, CD, D, 1, kCk);
     mm.run(m);
   }
   if (mm.err != cudaSuccess) return mm.err;

@@ -139,5 +139,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Reads and clears the tcgen05 kernel's device status word (synchronous copy).
 // Returns 0 if clear, else the code a bounded wait recorded.
 int tc_read_and_clear_status(cudaStream_t stream, cudaError_t* err);
+// Device address of that status word on the current device (looked up once per device),
+// for other kernels' bounded waits to record their codes in.
+cudaError_t tc_status_address(int** ptr);
 
 }  // namespace gdn

@@ -77,6 +77,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "gdn_internal.h"
 #include "tc_common.cuh"
 
@@ -1175,6 +1177,24 @@ __global__ void gdn_wait_selftest_kernel() {
 cudaError_t launch_wait_selftest(cudaStream_t stream) {
   gdn_wait_selftest_kernel<<<1, 32, 0, stream>>>();
   return cudaGetLastError();
+}
+
+cudaError_t tc_status_address(int** ptr) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static int* addr[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_tc_status)) != cudaSuccess) return e;
+    addr[dev] = static_cast<int*>(p);
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 int tc_read_and_clear_status(cudaStream_t stream, cudaError_t* err) {
