@@ -247,13 +247,14 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
 // (b = blockIdx.x, + gridDim.x, ...) with four roles joined by mbarriers:
 //   warp 0     TMA: 32-deep k panels of both operands, as stored, into a raw ring of 3 to 8
 //              slots (as many as fit: the loads in flight are what the CTA's bandwidth
-//              rests on); a panel contiguous in k lands in the MMA's K-major
+//              rests on), with the panel's scale vectors by bulk copy; a panel contiguous in
+//              k lands in the MMA's K-major
 //              128-byte-swizzled layout already, one contiguous in m or n as [32 k][rows];
 //   warps 2-9  split: each raw panel into TF32 hi and lo panels, K-major and swizzled,
-//              scaled on the way (a ring of 2 to 4 slots); the transposing reads of a plain
+//              scaled on the way (a ring of 2 slots); the transposing reads of a plain
 //              panel go down its columns, one row per lane, free of bank conflicts;
-//   warp 1     MMA: 12 tcgen05.mma (kind::tf32) per panel into one of two accumulators,
-//              as C^T = B^T A^T: the columns n of C are the TMEM lanes;
+//   warps 1,14 MMA: 12 tcgen05.mma (kind::tf32) per panel, as C^T = B^T A^T (the columns n
+//              of C are the TMEM lanes); one warp per accumulator, even and odd entries;
 //   warps 10-13 epilogue: tcgen05.ld of the accumulator (a thread per column n, 32 rows m
 //              per load), alpha, mask, C2, and the stores (a warp writes 32
 //              consecutive n of a row m per instruction).
@@ -293,10 +294,12 @@ struct MmArgs {
 
 constexpr int kMmSplitThreads = 256;  // 8 split warps
 constexpr int kMmThreads = 64 + kMmSplitThreads + 128;
-constexpr int kMmRing = 229376;       // both rings: 2 to 4 split slots, 3 to 8 raw slots
-constexpr int kMmMaxRaw = 8, kMmMaxSplit = 4;
-constexpr int kMmSmem = kMmRing + 1024;
-constexpr int kMmTmemCols = 256;      // two accumulators of up to 128 columns
+constexpr int kMmRing = 214784;       // both rings: 2 split slots, 2 to 8 raw slots
+constexpr int kMmXch = 16384;         // epilogue exchange buffer: 2 x [32][64] fp32
+constexpr int kMmMaxRaw = 8, kMmMaxSplit = 2;
+constexpr int kMmAux = 384;           // per raw slot: 32 ks + kCk bs values
+constexpr int kMmSmem = kMmRing + kMmXch + 1024;
+constexpr int kMmTmemCols = 512;      // two accumulators of up to 256 columns
 
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
   const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
@@ -338,16 +341,23 @@ __device__ __forceinline__ void umma_tf32(uint32_t d, uint64_t a, uint64_t b, ui
       : "memory");
 }
 
-// One raw k panel of an operand (R rows, k0 = its first k) into TF32 hi and lo panels,
-// K-major with the 128-byte swizzle (row r at r * 128 bytes, 16-byte chunk c of it at
-// (c ^ r % 8) * 16).  KC: the raw panel has that layout already (TMA with the swizzle);
-// else it is [32 k][R] plain fp32, read down its columns (one row per lane).  ks, rs:
-// optional scales per k and per row.  kMmSplitThreads threads, ts = 0 .. kMmSplitThreads - 1; each takes
-// R * 8 / kMmSplitThreads 16-byte chunks, loaded together before any is converted.
+// fp32 -> TF32 hi + lo, each rounded to nearest with ties away from zero (the format's
+// conversion) by adding half a TF32 unit to the magnitude bits and clearing the 13 low
+// bits; x - hi is exact in fp32.  Integer and one fp32 operation only.
+__device__ __forceinline__ void tf32_split_rn(float x, uint32_t& hi, uint32_t& lo) {
+  hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+  lo = (__float_as_uint(x - __uint_as_float(hi)) + 0x1000u) & 0xffffe000u;
+}
+
+// One raw k panel of an operand (R rows) into TF32 hi and lo panels, K-major with the
+// 128-byte swizzle (row r at r * 128 bytes, 16-byte chunk c of it at (c ^ r % 8) * 16).
+// KC: the raw panel has that layout already (TMA with the swizzle); else it is [32 k][R]
+// plain fp32, read down its columns (one row per lane).  ks, rs: optional scales per k of
+// the panel and per row, in shared memory.  kMmSplitThreads threads, ts = 0 .. -1; each
+// takes R * 8 / kMmSplitThreads 16-byte chunks, loaded together before any is converted.
 template <int R, bool KC>
 __device__ __forceinline__ void mm_split(const uint8_t* raw, uint8_t* hi, uint8_t* lo,
-                                         const float* __restrict__ ks,
-                                         const float* __restrict__ rs, int k0, int ts) {
+                                         const float* ks, const float* rs, int ts) {
   constexpr int kPer = R * 8 / kMmSplitThreads;
   float4 x[kPer];
   int off[kPer];
@@ -368,7 +378,7 @@ __device__ __forceinline__ void mm_split(const uint8_t* raw, uint8_t* hi, uint8_
       x[i] = make_float4(rf[0], rf[R], rf[2 * R], rf[3 * R]);
     }
     if (ks) {
-      const float4 f = *reinterpret_cast<const float4*>(ks + k0 + 4 * c);
+      const float4 f = *reinterpret_cast<const float4*>(ks + 4 * c);
       x[i].x *= f.x; x[i].y *= f.y; x[i].z *= f.z; x[i].w *= f.w;
     }
     if (rs) {
@@ -379,24 +389,23 @@ __device__ __forceinline__ void mm_split(const uint8_t* raw, uint8_t* hi, uint8_
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     uint4 h, l;
-    tf32_split(x[i].x, h.x, l.x);
-    tf32_split(x[i].y, h.y, l.y);
-    tf32_split(x[i].z, h.z, l.z);
-    tf32_split(x[i].w, h.w, l.w);
+    tf32_split_rn(x[i].x, h.x, l.x);
+    tf32_split_rn(x[i].y, h.y, l.y);
+    tf32_split_rn(x[i].z, h.z, l.z);
+    tf32_split_rn(x[i].w, h.w, l.w);
     *reinterpret_cast<uint4*>(hi + off[i]) = h;
     *reinterpret_cast<uint4*>(lo + off[i]) = l;
   }
 }
 
 __device__ __forceinline__ void mm_split_any(const uint8_t* raw, uint8_t* hi, uint8_t* lo, int R,
-                                             bool kc, const float* ks, const float* rs, int k0,
-                                             int ts) {
+                                             bool kc, const float* ks, const float* rs, int ts) {
   if (R == 128) {
-    if (kc) mm_split<128, true>(raw, hi, lo, ks, rs, k0, ts);
-    else mm_split<128, false>(raw, hi, lo, ks, rs, k0, ts);
+    if (kc) mm_split<128, true>(raw, hi, lo, ks, rs, ts);
+    else mm_split<128, false>(raw, hi, lo, ks, rs, ts);
   } else {
-    if (kc) mm_split<64, true>(raw, hi, lo, ks, rs, k0, ts);
-    else mm_split<64, false>(raw, hi, lo, ks, rs, k0, ts);
+    if (kc) mm_split<64, true>(raw, hi, lo, ks, rs, ts);
+    else mm_split<64, false>(raw, hi, lo, ks, rs, ts);
   }
 }
 
@@ -415,12 +424,15 @@ __global__ void __launch_bounds__(kMmThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int M = m.M, N = m.N, np = p.np, np0 = p.np0;
   const long long nlive = *m.nlive;
-  // one raw slot: a k panel of A and B, (M + N) x 128 bytes; one split slot: its hi and lo
-  // ring depths: as many split slots as leave room for 3 raw slots (2 to 4), then up to
-  // 8 raw slots
-  const int raw_bytes = (M + N) * 128, split_bytes = 2 * raw_bytes;
-  const int ns = max(2, min(kMmMaxSplit, (kMmRing - 3 * raw_bytes) / split_bytes));
-  const int nr = min(kMmMaxRaw, (kMmRing - ns * split_bytes) / raw_bytes);
+  // one raw slot: a k panel of A and B, (M + N) x 128 bytes, with an aux slot for the
+  // panel's 32 ks values and the kCk bs values (the scale vectors ride with the panel's
+  // copies); one split slot: the hi and lo panels.  Ring depths: two split slots (the split
+  // keeps ahead of the MMAs), and as many raw slots as fit, up to 8: the copies in flight
+  // carry the CTA's share of the memory bandwidth.
+  const int pan_bytes = (M + N) * 128, split_bytes = 2 * pan_bytes;
+  const int ns = 2;
+  const int ring = kMmRing + (N == 64 ? 0 : kMmXch);  // the exchange buffer only for N = 64
+  const int nr = min(kMmMaxRaw, (ring - ns * split_bytes) / (pan_bytes + kMmAux));
   constexpr int kSplitWarps = kMmSplitThreads / 32;
   if (tid == 0) {
     for (int i = 0; i < kMmMaxRaw; ++i) {
@@ -446,6 +458,8 @@ __global__ void __launch_bounds__(kMmThreads, 1)
   const uint32_t tmem = tslot;
   uint8_t* const spl0 = sm;
   uint8_t* const raw0 = sm + ns * split_bytes;
+  uint8_t* const aux0 = raw0 + nr * pan_bytes;
+  uint8_t* const xch0 = sm + kMmRing;  // the epilogue's exchange buffer (N = 64)
 
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
@@ -455,15 +469,20 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         prefetch_tensormap(&mapA1);
         prefetch_tensormap(&mapB1);
       }
-      const uint32_t bytes = (uint32_t)raw_bytes;
+      uint32_t bytes[2];
+      for (int t = 0; t < 2; ++t)
+        bytes[t] = pan_bytes + (m.t[t].ks ? 128 : 0) + (m.t[t].bs ? 4 * kCk : 0);
       int q = 0, s = 0, ph = 0;  // panel count, its raw slot and that slot's phase
       for (long long b = blockIdx.x; b < nlive; b += gridDim.x) {
         bool ok = true;
         for (int pn = 0; pn < np; ++pn, ++q) {
           if (!(ok = wait_bar(&bars[RE + s], ph ^ 1, abort_flag, false))) break;
-          uint8_t* raw = raw0 + s * raw_bytes;
-          mbar_arrive_expect_tx(&bars[RF + s], bytes);
+          uint8_t* raw = raw0 + s * pan_bytes;
+          uint8_t* aux = aux0 + s * kMmAux;
           const int t = pn >= np0, k0 = 32 * (pn - (t ? np0 : 0));
+          mbar_arrive_expect_tx(&bars[RF + s], bytes[t]);
+          if (m.t[t].ks) bulk_load(aux, m.t[t].ks + b * m.vb + k0, 128, &bars[RF + s]);
+          if (m.t[t].bs) bulk_load(aux + 128, m.t[t].bs + b * m.vb, 4 * kCk, &bars[RF + s]);
           const CUtensorMap* ma = t ? &mapA1 : &mapA0;
           const CUtensorMap* mb = t ? &mapB1 : &mapB0;
           if (p.akc[t]) tma_load_3d(raw, ma, &bars[RF + s], k0, 0, (int)b);
@@ -482,29 +501,34 @@ __global__ void __launch_bounds__(kMmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer: C^T = B^T A^T, so that C's columns are TMEM lanes
-      const uint32_t id = idesc_tf32(N, M);
+    // MMA issuer: C^T = B^T A^T, so that C's columns are TMEM lanes.  The hi and lo panels
+    // of an operand lie back to back, so that one descriptor spans both: with N = 64, one
+    // MMA per 8-deep k step multiplies [B_hi; B_lo] (128 rows) by [A_hi; A_lo] (2M rows)
+    // and the four quadrants of the accumulator sum to C; with N = 128, B_hi times
+    // [A_hi; A_lo] and B_lo times A_hi (two MMAs) leave C as the sum of two column halves.
+    if (lane == 0) {
+      const bool stacked = N == 64;
+      const uint32_t id2 = idesc_tf32(128, 2 * M), id1 = idesc_tf32(128, M);
       int i = 0, s = 0, sph = 0;  // item count; split slot and its phase
       for (long long b = blockIdx.x; b < nlive; b += gridDim.x, ++i) {
         const int a = i & 1;
         if (!wait_bar(&bars[AE + a], ((i >> 1) & 1) ^ 1, abort_flag, false)) break;
         tc_fence_after();
-        const uint32_t d = tmem + 128u * a;
+        const uint32_t d = tmem + 256u * a;
         bool ok = true;
         for (int pn = 0; pn < np; ++pn) {
           if (!(ok = wait_bar(&bars[SF + s], sph, abort_flag, false))) break;
           tc_fence_after();
           // descriptors once per panel, advanced 32 bytes (2 units) per 8-deep k step
-          const uint32_t ahi = smem_u32(spl0 + s * split_bytes), alo = ahi + M * 128;
-          const uint32_t bhi = alo + M * 128, blo = bhi + N * 128;
-          const uint64_t dah = smem_desc(ahi, 16, 1024), dal = smem_desc(alo, 16, 1024);
+          const uint32_t ahi = smem_u32(spl0 + s * split_bytes);
+          const uint32_t bhi = ahi + 2 * M * 128, blo = bhi + N * 128;
+          const uint64_t dah = smem_desc(ahi, 16, 1024);
           const uint64_t dbh = smem_desc(bhi, 16, 1024), dbl = smem_desc(blo, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t o = 2u * kk;
-            umma_tf32(d, dbl + o, dah + o, id, (pn | kk) != 0);
-            umma_tf32(d, dbh + o, dal + o, id, 1u);
-            umma_tf32(d, dbh + o, dah + o, id, 1u);
+            umma_tf32(d, dbh + o, dah + o, id2, (pn | kk) != 0);
+            if (!stacked) umma_tf32(d, dbl + o, dah + o, id1, 1u);
           }
           mma_commit(&bars[SE + s]);
           if (++s == ns) { s = 0; sph ^= 1; }
@@ -525,15 +549,15 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         ok = wait_bar(&bars[RF + r], rph, abort_flag, false) &&
              wait_bar(&bars[SE + s], sph ^ 1, abort_flag, false);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const uint8_t* raw = raw0 + r * raw_bytes;
+        const uint8_t* raw = raw0 + r * pan_bytes;
+        const uint8_t* aux = aux0 + r * kMmAux;
         uint8_t* spl = spl0 + s * split_bytes;
         const int t = pn >= np0;
-        const MmTerm& tm = m.t[t];
-        const float* ks = tm.ks ? tm.ks + b * m.vb : nullptr;
-        const float* bs = tm.bs ? tm.bs + b * m.vb : nullptr;
-        mm_split_any(raw, spl, spl + M * 128, M, p.akc[t], nullptr, nullptr, 0, ts);
+        const float* ks = m.t[t].ks ? reinterpret_cast<const float*>(aux) : nullptr;
+        const float* bs = m.t[t].bs ? reinterpret_cast<const float*>(aux + 128) : nullptr;
+        mm_split_any(raw, spl, spl + M * 128, M, p.akc[t], nullptr, nullptr, ts);
         mm_split_any(raw + M * 128, spl + 2 * M * 128, spl + 2 * M * 128 + N * 128, N, p.bkc[t],
-                     ks, bs, 32 * (pn - (t ? np0 : 0)), ts);
+                     ks, bs, ts);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -545,26 +569,30 @@ __global__ void __launch_bounds__(kMmThreads, 1)
       }
       if (!ok) break;
     }
-  } else {  // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, one column n of C each
-    const int qd = warp & 3;
-    const bool valid = N == 128 || lane < 16;
-    // an accumulator of 64 lanes keeps column n in lane 32 (n / 16) + n % 16
-    const int n = (N == 128 ? 32 : 16) * qd + lane;
+  } else {
+    // Epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. one column n of C (or, with
+    // N = 64, the hi half of column n in lanes 0..63 and its lo half in lanes 64..127;
+    // the lo warps hand their sums to the hi warps through shared memory).
+    const int qd = warp & 3, tl_row = 32 * qd + lane;
+    const bool stacked = N == 64;
+    const int n = stacked ? (tl_row & 63) : tl_row;
+    const bool top = !stacked || tl_row < 64;
+    float* xch = reinterpret_cast<float*>(xch0);
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
     int i = 0;
     for (long long b = blockIdx.x; b < nlive; b += gridDim.x, ++i) {
       const int a = i & 1;
-      if (warp_wait_fails(&bars[AF + a], (i >> 1) & 1, abort_flag, false)) break;
+      if (group_wait_fails(&bars[AF + a], (i >> 1) & 1, abort_flag, false, 2, 128)) break;
       tc_fence_after();
       const float* gv = m.gv ? m.gv + b * m.vb : nullptr;
-      const float scale = m.alpha;
       // Dg(m, n) = 2^{(g_m - g_n) log2 e} by ex2.approx (relative error ~2^-22)
-      const float gn = (gv && valid) ? gv[n] * kLog2e : 0.f;
+      const float gn = gv ? gv[n] * kLog2e : 0.f;
       float* C = m.C + b * m.cb + n;
       float* C2 = m.C2 ? m.C2 + b * m.cb + n : nullptr;
       for (int mb = 0; mb < M / 32; ++mb) {
-        uint32_t r[32];
-        tmem_ld32(tl + 128u * a + 32u * mb, r);
+        uint32_t r[32], r2[32];
+        tmem_ld32(tl + 256u * a + 32u * mb, r);
+        tmem_ld32(tl + 256u * a + M + 32u * mb, r2);
         const float gml = gv ? gv[32 * mb + lane] * kLog2e : 0.f;
         tmem_wait_ld();
         if (mb == M / 32 - 1) {  // the accumulator is free for the MMA warp
@@ -574,16 +602,28 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         }
         float x[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = scale * __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) + __uint_as_float(r2[j]);
+        if (stacked) {  // [32 m][64 n], two halves used in turn
+          float* xs = xch + (mb & 1) * 32 * 64;
+          if (!top) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xs[j * 64 + n] = x[j];
+          }
+          named_sync(3, 128);
+          if (!top) continue;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] += xs[j * 64 + n];
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] *= m.alpha;
         if (C2) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int mm = 32 * mb + j;
             const float gm = __shfl_sync(0xffffffffu, gml, j);
-            if (valid) C2[(long long)mm * m.cm] = n <= mm ? x[j] * ex2(gm - gn) : 0.f;
+            C2[(long long)mm * m.cm] = n <= mm ? x[j] * ex2(gm - gn) : 0.f;
           }
         }
-        if (!valid) continue;
         if (m.mask) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -1117,8 +1157,11 @@ struct MmLauncher {
               nb <= 0x7fffffffLL;
     for (int t = 0; ok && t < m.nt; ++t) {
       const MmTerm& x = m.t[t];
-      ok = dim_ok(x.K) && (x.am == 1 || x.ak == 1) && (x.bk == 1 || x.bn == 1);
+      // the scale vectors are kCk long: ks needs K <= kCk, bs N <= kCk
+      ok = dim_ok(x.K) && (x.am == 1 || x.ak == 1) && (x.bk == 1 || x.bn == 1) &&
+           (!x.ks || x.K <= kCk) && (!x.bs || m.N <= kCk);
     }
+    if (m.nt == 1) ok = ok && !m.t[1].ks && !m.t[1].bs;
     if (!ok) {
       err = cudaErrorInvalidValue;
       return;
