@@ -353,17 +353,17 @@ __device__ __forceinline__ void tf32_split_rn(float x, uint32_t& hi, uint32_t& l
 // 128-byte swizzle (row r at r * 128 bytes, 16-byte chunk c of it at (c ^ r % 8) * 16).
 // KC: the raw panel has that layout already (TMA with the swizzle); else it is [32 k][R]
 // plain fp32, read down its columns (one row per lane).  ks, rs: optional scales per k of
-// the panel and per row, in shared memory.  kMmSplitThreads threads, ts = 0 .. -1; each
-// takes R * 8 / kMmSplitThreads 16-byte chunks, loaded together before any is converted.
-template <int R, bool KC>
+// the panel and per row, in shared memory.  Thread ts = 0 .. NT - 1 of NT; each
+// takes R * 8 / NT 16-byte chunks (NT threads), loaded together before any is converted.
+template <int R, bool KC, int NT = kMmSplitThreads>
 __device__ __forceinline__ void mm_split(const uint8_t* raw, uint8_t* hi, uint8_t* lo,
                                          const float* ks, const float* rs, int ts) {
-  constexpr int kPer = R * 8 / kMmSplitThreads;
+  constexpr int kPer = R * 8 / NT;
   float4 x[kPer];
   int off[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
-    const int t = ts + kMmSplitThreads * i;
+    const int t = ts + NT * i;
     int c, r;  // logical 16-byte chunk (4 consecutive k) of row r
     if (KC) {
       off[i] = 16 * t;
@@ -916,6 +916,330 @@ __global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
 }
 
 // ---------------------------------------------------------------------------------
+// The same chain on the tcgen05 tensor cores, for dk = dv = 128: one CTA per (sequence,
+// head) holds the whole state St (128 x 128 fp32) in tensor memory, as the accumulator of
+// its update, and runs both products of a chunk in three TF32 passes:
+//   X1^T(r, c) = sum_k St(r, k) A1(c, k):  A = the hi and lo parts of St, copied to tensor
+//                memory; B = [A1_hi; A1_lo] (128 rows) for St_hi and A1_hi for St_lo;
+//   St(r, k)  += sum_c (s2 o X1)(c, r) A2(c, k):  A = the hi and lo parts of s2 o X1 in
+//                tensor memory; B = A2^T, hi and lo (A2 transposed on chip).
+// Roles: warp 0 TMA (A1 as four [64 c][32 k] swizzled panels, A2 as two [32 c][128 d]
+// plain panels, one raw slot each); warps 2-5 split them into TF32 hi and lo K-major
+// panels; warp 1 issues the MMAs; warps 6-13 (two per TMEM lane quarter, one state row per
+// thread, each warp one half of the columns) run the two passes of a chunk:
+//   state pass: St -> st (the chunk-start state), St's hi and lo parts -> tensor memory,
+//               Gamma St + Add2 -> the accumulator;
+//   X pass:     the product -> X1 = Add1 + s1 o (St A1^T)^T -> out1, and the hi and lo parts
+//               of s2 o X1 -> tensor memory.
+// Every wait is bounded and reports through the status word.
+struct ChainTcArgs {
+  ChainArgs c;
+  int* status;
+};
+
+constexpr int kCtThreads = 448;  // 14 warps
+// shared memory: A1 raw 32 KB, A2 raw 32 KB, A1 hi/lo 64 KB, A2 hi/lo 64 KB, and a 32 x 33
+// transpose tile per pass warp (rows of the state <-> coalesced global rows)
+constexpr int kCtRaw1 = 0, kCtRaw2 = 32768, kCtS1 = 65536, kCtS2 = 131072, kCtTile = 196608;
+constexpr int kCtSmem = kCtTile + 8 * 32 * 33 * 4 + 1024;
+// tensor memory columns: St, St_hi, St_lo, the X1 product (its lo part at +64), whose
+// columns then take s2 o X1's hi and lo parts
+constexpr uint32_t kTcSt = 0, kTcShi = 128, kTcSlo = 256, kTcX = 384, kTcXhi = 384,
+                   kTcXlo = 448;
+
+// One thread: D(tmem) (+)= A(tmem) B(smem)^T, kind::tf32.
+__device__ __forceinline__ void umma_tf32_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void split32_to_tmem(uint32_t t_hi, uint32_t t_lo, const float* v) {
+  uint32_t h[32], l[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) tf32_split_rn(v[e], h[e], l[e]);
+  tmem_st32(t_hi, h);
+  tmem_st32(t_lo, l);
+}
+
+template <bool REV>
+__global__ void __launch_bounds__(kCtThreads, 1)
+    ck_chain_tc_kernel(const __grid_constant__ CUtensorMap mapA1,
+                       const __grid_constant__ CUtensorMap mapA2, const ChainTcArgs args) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t ct_smem_raw[];
+  uint8_t* sm = ct_smem_raw + ((1024u - (smem_u32(ct_smem_raw) & 1023u)) & 1023u);
+  enum { R1F, R1E, R2F, R2E, S1F, S1E, S2F, S2E, SPD, G1D, XED, G2D, DONE, NBAR };
+  __shared__ __align__(8) uint64_t bars[NBAR];
+  __shared__ uint32_t tslot;
+  __shared__ int abort_s;
+  volatile int* abort_flag = &abort_s;
+  const ChainArgs& p = args.c;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H;
+  const int base = p.cbase[n], nc = p.cbase[n + 1] - base;
+  const size_t sidx = ((size_t)n * p.H + h) * D * D;
+  auto entry = [&](int jj) { return (long long)(base + (REV ? nc - 1 - jj : jj)) * p.H + h; };
+  if (tid == 0) {
+    mbar_init(&bars[R1F], 1);
+    mbar_init(&bars[R1E], 4);
+    mbar_init(&bars[R2F], 1);
+    mbar_init(&bars[R2E], 4);
+    mbar_init(&bars[S1F], 4);
+    mbar_init(&bars[S1E], 1);
+    mbar_init(&bars[S2F], 4);
+    mbar_init(&bars[S2E], 1);
+    mbar_init(&bars[SPD], 8);
+    mbar_init(&bars[G1D], 1);
+    mbar_init(&bars[XED], 8);
+    mbar_init(&bars[G2D], 1);
+    mbar_init(&bars[DONE], 1);
+    abort_s = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tslot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      prefetch_tensormap(&mapA1);
+      prefetch_tensormap(&mapA2);
+      int issued1 = 0, issued2 = 0;
+      for (int jj = 0; jj < nc; ++jj) {
+        const int b = (int)entry(jj);
+        const uint32_t ph = (jj & 1) ^ 1;
+        if (!wait_bar(&bars[R1E], ph, abort_flag, false)) break;
+        // the chunk's Add1 (and Add2) blocks, read by the passes with plain loads, into L2
+        bulk_prefetch_l2(p.add1 + (size_t)b * kCk * D, kCk * D * 4);
+        if (REV) bulk_prefetch_l2(p.add2 + (size_t)b * D * D, D * D * 4);
+        mbar_arrive_expect_tx(&bars[R1F], 32768);
+        for (int q = 0; q < 4; ++q)
+          tma_load_3d(sm + kCtRaw1 + q * 8192, &mapA1, &bars[R1F], 32 * q, 0, b);
+        issued1 = jj + 1;
+        if (!wait_bar(&bars[R2E], ph, abort_flag, false)) break;
+        mbar_arrive_expect_tx(&bars[R2F], 32768);
+        for (int q = 0; q < 2; ++q)
+          tma_load_3d(sm + kCtRaw2 + q * 16384, &mapA2, &bars[R2F], 0, 32 * q, b);
+        issued2 = jj + 1;
+      }
+      // copies still in flight land before shared memory is released
+      if (issued1) (void)mbar_wait(&bars[R1F], (issued1 - 1) & 1, kWaitNs);
+      if (issued2) (void)mbar_wait(&bars[R2F], (issued2 - 1) & 1, kWaitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t id128 = idesc_tf32(128, 128), id64 = idesc_tf32(128, 64);
+      const uint64_t d1 = smem_desc(smem_u32(sm + kCtS1), 16, 1024);
+      const uint64_t d2h = smem_desc(smem_u32(sm + kCtS2), 16, 1024);
+      const uint64_t d2l = smem_desc(smem_u32(sm + kCtS2 + 32768), 16, 1024);
+      for (int jj = 0; jj < nc; ++jj) {
+        const uint32_t ph = jj & 1;
+        if (!wait_bar(&bars[SPD], ph, abort_flag, false) ||
+            !wait_bar(&bars[S1F], ph, abort_flag, false))
+          break;
+        tc_fence_after();
+        // X1^T = St_hi [A1_hi; A1_lo]^T + St_lo A1_hi^T: 4 panels of 16 KB (hi | lo)
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          const uint64_t o = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);  // 16-byte units
+          umma_tf32_ta(tmem + kTcX, tmem + kTcShi + 8 * ks, d1 + o, id128, ks != 0);
+          umma_tf32_ta(tmem + kTcX, tmem + kTcSlo + 8 * ks, d1 + o, id64, 1u);
+        }
+        mma_commit(&bars[G1D]);
+        mma_commit(&bars[S1E]);
+        if (!wait_bar(&bars[XED], ph, abort_flag, false) ||
+            !wait_bar(&bars[S2F], ph, abort_flag, false))
+          break;
+        tc_fence_after();
+        // St += Xs_hi A2T_hi^T + Xs_hi A2T_lo^T + Xs_lo A2T_hi^T: 2 panels of 16 KB each
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t o = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
+          umma_tf32_ta(tmem + kTcSt, tmem + kTcXhi + 8 * ks, d2h + o, id128, 1u);
+          umma_tf32_ta(tmem + kTcSt, tmem + kTcXhi + 8 * ks, d2l + o, id128, 1u);
+          umma_tf32_ta(tmem + kTcSt, tmem + kTcXlo + 8 * ks, d2h + o, id128, 1u);
+        }
+        mma_commit(&bars[G2D]);
+        mma_commit(&bars[S2E]);
+      }
+      mma_commit(&bars[DONE]);
+      (void)mbar_wait(&bars[DONE], 0, kWaitNs);
+    }
+  } else if (warp < 6) {  // split: A1 (K-major already) and A2 (transposed)
+    const int ts = tid - 64;
+    for (int jj = 0; jj < nc; ++jj) {
+      const uint32_t ph = jj & 1;
+      bool ok = wait_bar(&bars[R1F], ph, abort_flag, false) &&
+                wait_bar(&bars[S1E], ph ^ 1, abort_flag, false);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q)
+        mm_split<64, true, 128>(sm + kCtRaw1 + q * 8192, sm + kCtS1 + q * 16384,
+                                sm + kCtS1 + q * 16384 + 8192, nullptr, nullptr, ts);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[S1F]);
+        mbar_arrive(&bars[R1E]);
+      }
+      ok = wait_bar(&bars[R2F], ph, abort_flag, false) &&
+           wait_bar(&bars[S2E], ph ^ 1, abort_flag, false);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q)
+        mm_split<128, false, 128>(sm + kCtRaw2 + q * 16384, sm + kCtS2 + q * 16384,
+                                  sm + kCtS2 + 32768 + q * 16384, nullptr, nullptr, ts);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[S2F]);
+        mbar_arrive(&bars[R2E]);
+      }
+    }
+  } else {  // the state and X passes: row r of the state, column half hf
+    const int qd = warp & 3, hf = (warp - 6) >> 2, r = 32 * qd + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+    const float* G = p.gates;
+    for (int jj = 0; jj < nc; ++jj) {
+      const long long b = entry(jj);
+      const float* gb = G + (size_t)b * kGates * kCk;
+      const float gam = p.gam[b];
+      // ---- state pass (the state after chunk jj - 1, or the initial state)
+      if (jj > 0) {
+        if (group_wait_fails(&bars[G2D], (jj - 1) & 1, abort_flag, false, 2, 256)) break;
+        tc_fence_after();
+      }
+      // the state's rows go out (and Add2's come in) through the warp's transpose tile, so
+      // that every global access of a warp covers 32 consecutive columns of one row
+      float* const tile = reinterpret_cast<float*>(sm + kCtTile) + (warp - 6) * 32 * 33;
+      float* const stb = p.st + (size_t)b * D * D + (size_t)(32 * qd) * D + lane;
+#pragma unroll 1
+      for (int hq = 0; hq < 2; ++hq) {
+        const int c0 = 64 * hf + 32 * hq;  // 32 state columns
+        float a2c[32];  // Add2(32 qd + e, c0 + lane)
+        if (REV) {
+          const float* a2p = p.add2 + (size_t)b * D * D + (size_t)(32 * qd) * D + c0 + lane;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) a2c[e] = a2p[(size_t)e * D];
+        }
+        float v[32];
+        if (jj > 0) {
+          uint32_t u[32];
+          tmem_ld32(tl + kTcSt + c0, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(u[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 x = p.init ? ld4(p.init + sidx + (size_t)r * D + c0 + e)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) tile[lane * 33 + e] = v[e];
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) stb[(size_t)e * D + c0] = tile[e * 33 + lane];
+        __syncwarp();
+        split32_to_tmem(tl + kTcShi + c0, tl + kTcSlo + c0, v);
+        uint32_t w[32];
+        if (REV) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) tile[e * 33 + lane] = a2c[e];
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(fmaf(gam, v[e], tile[lane * 33 + e]));
+          __syncwarp();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(gam * v[e]);
+        }
+        tmem_st32(tl + kTcSt + c0, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[SPD]);
+      // ---- X pass; Add1(c, r) for the 32 c of this half is loaded while the product runs
+      float add1[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) add1[e] = p.add1[(size_t)b * kCk * D + (size_t)(32 * hf + e) * D + r];
+      if (group_wait_fails(&bars[G1D], jj & 1, abort_flag, false, 2, 256)) break;
+      tc_fence_after();
+      {
+        const int c0 = 32 * hf;  // 32 chunk positions c
+        uint32_t u[32], u2[32];
+        tmem_ld32(tl + kTcX + c0, u);
+        tmem_ld32(tl + kTcX + 64 + c0, u2);
+        tmem_wait_ld();
+        float xs[32];
+        float* o1 = p.out1 + (size_t)b * kCk * D + r;
+        const float ecl = gb[G_E * kCk + c0 + lane];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float pr = __uint_as_float(u[e]) + __uint_as_float(u2[e]);
+          const float ec = __shfl_sync(0xffffffffu, ecl, e);
+          const float x = REV ? fmaf(ec, pr, add1[e]) : add1[e] - pr;
+          o1[(size_t)(c0 + e) * D] = x;
+          xs[e] = REV ? -x : ec * x;
+        }
+        split32_to_tmem(tl + kTcXhi + c0, tl + kTcXlo + c0, xs);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[XED]);
+    }
+    // the final state (the vote keeps the eight warps together after a failed wait)
+    if (p.fin) {
+      bool ok = true;
+      if (nc > 0) {
+        ok = !group_wait_fails(&bars[G2D], (nc - 1) & 1, abort_flag, false, 2, 256);
+        tc_fence_after();
+      }
+      if (ok) {
+#pragma unroll 1
+        for (int hq = 0; hq < 2; ++hq) {
+          const int c0 = 64 * hf + 32 * hq;
+          float* f = p.fin + sidx + (size_t)r * D + c0;
+          if (nc > 0) {
+            uint32_t u[32];
+            tmem_ld32(tl + kTcSt + c0, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              st4(f + e, __uint_as_float(u[e]), __uint_as_float(u[e + 1]),
+                  __uint_as_float(u[e + 2]), __uint_as_float(u[e + 3]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 x = p.init ? ld4(p.init + sidx + (size_t)r * D + c0 + e)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+              st4(f + e, x.x, x.y, x.z, x.w);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (tid == 0 && *abort_flag) atomicOr(args.status, *abort_flag);
+}
+
+// ---------------------------------------------------------------------------------
 // Per (chunk, head), from dA = strictly-lower(-T^T dT T^T): X + X^T with X = dA o D o beta_i
 // (the operand of dK's X K + X^T K), the row sums of dA o KK^T o D (the triangular solve's part of dbeta) and
 // dg1 = rowsum(dD o D) - colsum(dD o D) with dD = dA beta_i KK^T + dP o QK^T.
@@ -1120,6 +1444,19 @@ bool mm_map(CUtensorMap* map, const float* base, long long nb, long long bstride
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [nb][rows][D] fp32 as boxes of 32 rows x D columns, plain (the chain's A2 panels).
+bool tile_map_plain(CUtensorMap* map, const float* base, long long nb, int rows, int D) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)nb};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)rows * D * 4};
+  cuuint32_t box[3] = {(cuuint32_t)D, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct MmLauncher {
   long long nb;
   const long long* nlive;
@@ -1227,6 +1564,25 @@ struct SideJoin {
   }
 };
 
+// One chain: the tcgen05 kernel for D = 128 (one CTA per (sequence, head)), the
+// CUDA-core-fed one for D = 64 (D / kRows CTAs per (sequence, head)).
+template <int D, bool REV>
+cudaError_t launch_chain(const ChainArgs& c, long long nb, int N, int H, int* status,
+                         cudaStream_t s) {
+  const unsigned units = (unsigned)((long long)N * H);
+  if (D == 128) {
+    CUtensorMap m1, m2;
+    if (!mm_map(&m1, c.a1, nb, (long long)kCk * D, kCk, D, D, 1) ||
+        !tile_map_plain(&m2, c.a2, nb, kCk, D))
+      return cudaErrorInvalidValue;
+    ChainTcArgs t{c, status};
+    ck_chain_tc_kernel<REV><<<units, kCtThreads, kCtSmem, s>>>(m1, m2, t);
+  } else {
+    ck_chain_kernel<D, REV><<<dim3(units, D / kRows), 256, chain_smem_bytes<D>(), s>>>(c);
+  }
+  return cudaGetLastError();
+}
+
 template <int D, typename TIn>
 cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.B * a.T;
@@ -1286,8 +1642,13 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   // per-device first-call step cannot fail while side-stream work is in flight.
   constexpr int smem = chain_smem_bytes<D>();
   static std::atomic<unsigned long long> set_f{0}, set_r{0};
-  if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, smem, set_f)) != cudaSuccess) return e;
-  if ((e = ensure_smem_cap(ck_chain_kernel<D, true>, smem, set_r)) != cudaSuccess) return e;
+  if (D == 128) {
+    if ((e = ensure_smem_cap(ck_chain_tc_kernel<false>, kCtSmem, set_f)) != cudaSuccess) return e;
+    if ((e = ensure_smem_cap(ck_chain_tc_kernel<true>, kCtSmem, set_r)) != cudaSuccess) return e;
+  } else {
+    if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, smem, set_f)) != cudaSuccess) return e;
+    if ((e = ensure_smem_cap(ck_chain_kernel<D, true>, smem, set_r)) != cudaSuccess) return e;
+  }
   // Fork: the side stream takes P^T dO and dO^T diag(e^g) Q (they need the solve's P and
   // the gathered tiles only) while this stream makes W~, U and the forward chain.
   std::lock_guard<std::mutex> lock(g_side_mu);
@@ -1319,13 +1680,11 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   }
   if (mm.err != cudaSuccess) return mm.err;
 
-  const dim3 cgrid((unsigned)((long long)a.N * a.H), D / kRows);
   ChainArgs cf;
   cf.cbase = cbase; cf.init = a.S0; cf.fin = nullptr; cf.st = S;
   cf.add1 = U; cf.a1 = Wt; cf.a2 = Kc; cf.add2 = nullptr; cf.out1 = Dl;
   cf.gates = gates; cf.gam = gam; cf.H = a.H;
-  ck_chain_kernel<D, false><<<cgrid, 256, smem, s>>>(cf);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_chain<D, false>(cf, L.nb, a.N, a.H, status, s)) != cudaSuccess) return e;
 
   // The side stream continues with the products of delta and S (dO delta^T, (dP o D) K,
   // dO S) while this stream runs the reverse chain.
@@ -1349,8 +1708,7 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   cr.cbase = cbase; cr.init = a.dS_final; cr.fin = a.dS0; cr.st = dSn;
   cr.add1 = Y; cr.a1 = Kc; cr.a2 = Wt; cr.add2 = Z; cr.out1 = dDl;
   cr.gates = gates; cr.gam = gam; cr.H = a.H;
-  ck_chain_kernel<D, true><<<cgrid, 256, smem, s>>>(cr);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_chain<D, true>(cr, L.nb, a.N, a.H, status, s)) != cudaSuccess) return e;
 
   {
     // dW = -d delta S, delta dS'
