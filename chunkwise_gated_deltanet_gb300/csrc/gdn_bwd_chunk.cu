@@ -923,12 +923,15 @@ __global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
 //                memory; B = [A1_hi; A1_lo] (128 rows) for St_hi and A1_hi for St_lo;
 //   St(r, k)  += sum_c (s2 o X1)(c, r) A2(c, k):  A = the hi and lo parts of s2 o X1 in
 //                tensor memory; B = A2^T, hi and lo (A2 transposed on chip).
-// Roles: warp 0 TMA (A1 as four [64 c][32 k] swizzled panels, A2 as two [32 c][128 d]
-// plain panels, one raw slot each); warps 2-5 split them into TF32 hi and lo K-major
-// panels; warp 1 issues the MMAs; warps 6-13 (two per TMEM lane quarter, one state row per
-// thread, each warp one half of the columns) run the two passes of a chunk:
-//   state pass: St -> st (the chunk-start state), St's hi and lo parts -> tensor memory,
-//               Gamma St + Add2 -> the accumulator;
+// Roles: warp 0 TMA (A1 as four [64 c][32 k] swizzled panels straight into the lo halves
+// of its split panels, split there in place; A2 as two [32 c][128 d] plain panels into a
+// raw slot); warps 2-5 split them into TF32 hi and lo K-major panels; warp 1 issues the
+// MMAs; warps 6-13 (two per TMEM lane quarter, one state row per thread, each warp one
+// half of the columns) run the two passes of a chunk:
+//   state pass: St's hi and lo parts -> tensor memory, Gamma St + Add2 -> the accumulator,
+//               and St -> st (the chunk-start state) by TMA store from a swizzled 32 x 32
+//               tile per warp and column quarter; Add2 comes in by TMA into the same tiles
+//               one chunk ahead;
 //   X pass:     the product -> X1 = Add1 + s1 o (St A1^T)^T -> out1, and the hi and lo parts
 //               of s2 o X1 -> tensor memory.
 // Every wait is bounded and reports through the status word.
@@ -938,10 +941,10 @@ struct ChainTcArgs {
 };
 
 constexpr int kCtThreads = 448;  // 14 warps
-// shared memory: A1 raw 32 KB, A2 raw 32 KB, A1 hi/lo 64 KB, A2 hi/lo 64 KB, and a 32 x 33
-// transpose tile per pass warp (rows of the state <-> coalesced global rows)
-constexpr int kCtRaw1 = 0, kCtRaw2 = 32768, kCtS1 = 65536, kCtS2 = 131072, kCtTile = 196608;
-constexpr int kCtSmem = kCtTile + 8 * 32 * 33 * 4 + 1024;
+// shared memory: A1 hi/lo 64 KB (4 panels of [hi 8 KB | lo 8 KB]), A2 raw 32 KB, A2 hi/lo
+// 64 KB, and two 4 KB tiles ([32 rows][32 fp32], 128-byte swizzle) per pass warp
+constexpr int kCtS1 = 0, kCtRaw2 = 65536, kCtS2 = 98304, kCtTile = 163840;
+constexpr int kCtSmem = kCtTile + 8 * 2 * 4096 + 1024;
 // tensor memory columns: St, St_hi, St_lo, the X1 product (its lo part at +64), whose
 // columns then take s2 o X1's hi and lo parts
 constexpr uint32_t kTcSt = 0, kTcShi = 128, kTcSlo = 256, kTcX = 384, kTcXhi = 384,
@@ -968,11 +971,13 @@ __device__ __forceinline__ void split32_to_tmem(uint32_t t_hi, uint32_t t_lo, co
 template <bool REV>
 __global__ void __launch_bounds__(kCtThreads, 1)
     ck_chain_tc_kernel(const __grid_constant__ CUtensorMap mapA1,
-                       const __grid_constant__ CUtensorMap mapA2, const ChainTcArgs args) {
+                       const __grid_constant__ CUtensorMap mapA2,
+                       const __grid_constant__ CUtensorMap mapSt,
+                       const __grid_constant__ CUtensorMap mapAdd2, const ChainTcArgs args) {
   constexpr int D = 128;
   extern __shared__ uint8_t ct_smem_raw[];
   uint8_t* sm = ct_smem_raw + ((1024u - (smem_u32(ct_smem_raw) & 1023u)) & 1023u);
-  enum { R1F, R1E, R2F, R2E, S1F, S1E, S2F, S2E, SPD, G1D, XED, G2D, DONE, NBAR };
+  enum { R1F, R2F, R2E, S1F, S1E, S2F, S2E, SPD, G1D, XED, G2D, DONE, AD0, NBAR = AD0 + 8 };
   __shared__ __align__(8) uint64_t bars[NBAR];
   __shared__ uint32_t tslot;
   __shared__ int abort_s;
@@ -985,7 +990,6 @@ __global__ void __launch_bounds__(kCtThreads, 1)
   auto entry = [&](int jj) { return (long long)(base + (REV ? nc - 1 - jj : jj)) * p.H + h; };
   if (tid == 0) {
     mbar_init(&bars[R1F], 1);
-    mbar_init(&bars[R1E], 4);
     mbar_init(&bars[R2F], 1);
     mbar_init(&bars[R2E], 4);
     mbar_init(&bars[S1F], 4);
@@ -997,6 +1001,7 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     mbar_init(&bars[XED], 8);
     mbar_init(&bars[G2D], 1);
     mbar_init(&bars[DONE], 1);
+    for (int w = 0; w < 8; ++w) mbar_init(&bars[AD0 + w], 1);
     abort_s = 0;
     fence_mbarrier_init();
   }
@@ -1014,13 +1019,14 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       for (int jj = 0; jj < nc; ++jj) {
         const int b = (int)entry(jj);
         const uint32_t ph = (jj & 1) ^ 1;
-        if (!wait_bar(&bars[R1E], ph, abort_flag, false)) break;
-        // the chunk's Add1 (and Add2) blocks, read by the passes with plain loads, into L2
+        // A1 lands in the lo halves of the split panels, free once the previous X1 product
+        // is complete
+        if (!wait_bar(&bars[S1E], ph, abort_flag, false)) break;
+        // the chunk's Add1 block, read by the X pass with plain loads, into L2
         bulk_prefetch_l2(p.add1 + (size_t)b * kCk * D, kCk * D * 4);
-        if (REV) bulk_prefetch_l2(p.add2 + (size_t)b * D * D, D * D * 4);
         mbar_arrive_expect_tx(&bars[R1F], 32768);
         for (int q = 0; q < 4; ++q)
-          tma_load_3d(sm + kCtRaw1 + q * 8192, &mapA1, &bars[R1F], 32 * q, 0, b);
+          tma_load_3d(sm + kCtS1 + q * 16384 + 8192, &mapA1, &bars[R1F], 32 * q, 0, b);
         issued1 = jj + 1;
         if (!wait_bar(&bars[R2E], ph, abort_flag, false)) break;
         mbar_arrive_expect_tx(&bars[R2F], 32768);
@@ -1071,23 +1077,19 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       mma_commit(&bars[DONE]);
       (void)mbar_wait(&bars[DONE], 0, kWaitNs);
     }
-  } else if (warp < 6) {  // split: A1 (K-major already) and A2 (transposed)
+  } else if (warp < 6) {  // split: A1 in place (K-major already), A2 transposed
     const int ts = tid - 64;
     for (int jj = 0; jj < nc; ++jj) {
       const uint32_t ph = jj & 1;
-      bool ok = wait_bar(&bars[R1F], ph, abort_flag, false) &&
-                wait_bar(&bars[S1E], ph ^ 1, abort_flag, false);
+      bool ok = wait_bar(&bars[R1F], ph, abort_flag, false);
       if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll 1
       for (int q = 0; q < 4; ++q)
-        mm_split<64, true, 128>(sm + kCtRaw1 + q * 8192, sm + kCtS1 + q * 16384,
+        mm_split<64, true, 128>(sm + kCtS1 + q * 16384 + 8192, sm + kCtS1 + q * 16384,
                                 sm + kCtS1 + q * 16384 + 8192, nullptr, nullptr, ts);
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[S1F]);
-        mbar_arrive(&bars[R1E]);
-      }
+      if (lane == 0) mbar_arrive(&bars[S1F]);
       ok = wait_bar(&bars[R2F], ph, abort_flag, false) &&
            wait_bar(&bars[S2E], ph ^ 1, abort_flag, false);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -1103,31 +1105,41 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       }
     }
   } else {  // the state and X passes: row r of the state, column half hf
-    const int qd = warp & 3, hf = (warp - 6) >> 2, r = 32 * qd + lane;
+    const int pw = warp - 6, qd = warp & 3, hf = pw >> 2, r = 32 * qd + lane;
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+    uint8_t* const tiles = sm + kCtTile + pw * 8192;  // two [32][32] fp32 tiles, swizzled
+    uint64_t* const abar = &bars[AD0 + pw];
+    // Add2 of a chunk into this warp's tiles: rows 32 qd.., columns 64 hf + 32 hq..
+    int add2_loads = 0;  // issued by lane 0
+    auto load_add2 = [&](int jj) {
+      const int b = (int)entry(jj);
+      ++add2_loads;
+      mbar_arrive_expect_tx(abar, 8192);
+      for (int hq = 0; hq < 2; ++hq)
+        tma_load_3d(tiles + hq * 4096, &mapAdd2, abar, 64 * hf + 32 * hq, 32 * qd, b);
+    };
+    if (REV && lane == 0 && nc > 0) load_add2(0);
     const float* G = p.gates;
     for (int jj = 0; jj < nc; ++jj) {
       const long long b = entry(jj);
       const float* gb = G + (size_t)b * kGates * kCk;
       const float gam = p.gam[b];
       // ---- state pass (the state after chunk jj - 1, or the initial state)
-      if (jj > 0) {
-        if (group_wait_fails(&bars[G2D], (jj - 1) & 1, abort_flag, false, 2, 256)) break;
+      {
+        uint64_t* b1 = REV ? abar : nullptr;
+        bool fail;
+        if (jj > 0)
+          fail = group_waits_fail(abort_flag, 2, 256, &bars[G2D], (jj - 1) & 1, false, b1, jj & 1);
+        else
+          fail = b1 ? group_waits_fail(abort_flag, 2, 256, b1, 0, false) : false;
+        if (fail) break;
         tc_fence_after();
       }
-      // the state's rows go out (and Add2's come in) through the warp's transpose tile, so
-      // that every global access of a warp covers 32 consecutive columns of one row
-      float* const tile = reinterpret_cast<float*>(sm + kCtTile) + (warp - 6) * 32 * 33;
-      float* const stb = p.st + (size_t)b * D * D + (size_t)(32 * qd) * D + lane;
 #pragma unroll 1
       for (int hq = 0; hq < 2; ++hq) {
         const int c0 = 64 * hf + 32 * hq;  // 32 state columns
-        float a2c[32];  // Add2(32 qd + e, c0 + lane)
-        if (REV) {
-          const float* a2p = p.add2 + (size_t)b * D * D + (size_t)(32 * qd) * D + c0 + lane;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) a2c[e] = a2p[(size_t)e * D];
-        }
+        uint8_t* const tile = tiles + hq * 4096;
+        const uint32_t trow = smem_u32(tile) + lane * 128;  // this thread's row of the tile
         float v[32];
         if (jj > 0) {
           uint32_t u[32];
@@ -1143,31 +1155,48 @@ __global__ void __launch_bounds__(kCtThreads, 1)
             v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
           }
         }
-#pragma unroll
-        for (int e = 0; e < 32; ++e) tile[lane * 33 + e] = v[e];
-        __syncwarp();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) stb[(size_t)e * D + c0] = tile[e * 33 + lane];
-        __syncwarp();
-        split32_to_tmem(tl + kTcShi + c0, tl + kTcSlo + c0, v);
         uint32_t w[32];
-        if (REV) {
+        if (REV) {  // Add2(r, c0 + 4c ..) from the tile's 16-byte chunk c ^ (r % 8)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) tile[e * 33 + lane] = a2c[e];
-          __syncwarp();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(fmaf(gam, v[e], tile[lane * 33 + e]));
-          __syncwarp();
+          for (int c = 0; c < 8; ++c) {
+            float4 x;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                         : "r"(trow + ((c ^ (lane & 7)) << 4)));
+            w[4 * c] = __float_as_uint(fmaf(gam, v[4 * c], x.x));
+            w[4 * c + 1] = __float_as_uint(fmaf(gam, v[4 * c + 1], x.y));
+            w[4 * c + 2] = __float_as_uint(fmaf(gam, v[4 * c + 2], x.z));
+            w[4 * c + 3] = __float_as_uint(fmaf(gam, v[4 * c + 3], x.w));
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(gam * v[e]);
         }
         tmem_st32(tl + kTcSt + c0, w);
+        split32_to_tmem(tl + kTcShi + c0, tl + kTcSlo + c0, v);
+        // the chunk-start state: the tile, then one TMA store per warp and quarter
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(trow + ((c ^ (lane & 7)) << 4), __float_as_uint(v[4 * c]),
+                       __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                       __float_as_uint(v[4 * c + 3]));
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&mapSt, tile, c0, 32 * qd, (int)b);
+          bulk_commit();
+        }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[SPD]);
+      // the tiles take the next chunk's Add2 once the stores have read them
+      if (lane == 0) {
+        bulk_wait_read_all();
+        if (REV && jj + 1 < nc) load_add2(jj + 1);
+      }
+      __syncwarp();
       // ---- X pass; Add1(c, r) for the 32 c of this half is loaded while the product runs
       float add1[32];
 #pragma unroll
@@ -1228,6 +1257,12 @@ __global__ void __launch_bounds__(kCtThreads, 1)
           }
         }
       }
+    }
+    // the TMA stores are complete before the CTA ends; an Add2 load still in flight (after a
+    // failed wait) lands first
+    if (lane == 0) {
+      bulk_wait_all();
+      if (REV && add2_loads > 0) (void)mbar_wait(abar, (add2_loads - 1) & 1, kWaitNs);
     }
   }
   tc_fence_before();
@@ -1457,6 +1492,19 @@ bool tile_map_plain(CUtensorMap* map, const float* base, long long nb, int rows,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [nb][D][D] fp32 as 32 x 32 boxes with the 128-byte swizzle (the chain's state tiles).
+bool state_tile_map(CUtensorMap* map, const float* base, long long nb, int D) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)nb};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct MmLauncher {
   long long nb;
   const long long* nlive;
@@ -1571,12 +1619,16 @@ cudaError_t launch_chain(const ChainArgs& c, long long nb, int N, int H, int* st
                          cudaStream_t s) {
   const unsigned units = (unsigned)((long long)N * H);
   if (D == 128) {
-    CUtensorMap m1, m2;
+    CUtensorMap m1, m2, mst, madd2;
     if (!mm_map(&m1, c.a1, nb, (long long)kCk * D, kCk, D, D, 1) ||
-        !tile_map_plain(&m2, c.a2, nb, kCk, D))
+        !tile_map_plain(&m2, c.a2, nb, kCk, D) ||
+        !state_tile_map(&mst, c.st, nb, D))
       return cudaErrorInvalidValue;
+    // Add2 is read only by the reverse chain; the forward one gets a copy of the st map
+    madd2 = mst;
+    if (REV && !state_tile_map(&madd2, c.add2, nb, D)) return cudaErrorInvalidValue;
     ChainTcArgs t{c, status};
-    ck_chain_tc_kernel<REV><<<units, kCtThreads, kCtSmem, s>>>(m1, m2, t);
+    ck_chain_tc_kernel<REV><<<units, kCtThreads, kCtSmem, s>>>(m1, m2, mst, madd2, t);
   } else {
     ck_chain_kernel<D, REV><<<dim3(units, D / kRows), 256, chain_smem_bytes<D>(), s>>>(c);
   }
