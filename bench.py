@@ -799,7 +799,8 @@ def main():
             "data": "synthetic",
             "config": {"workload": w.name, "B": B, "H": H, "T": T, "dk": dk, "dv": dv, "C": C,
                        "seqs": N, "qkv_dtype": w.dtype,
-                       "path": {1: "recurrence (CUDA cores)", 2: "tcgen05"}.get(path, "none"),
+                       "path": {1: "recurrence (CUDA cores)", 2: "tcgen05",
+                                3: "chunk form, tcgen05 three-pass TF32"}.get(path, "none"),
                        "l2": "flushed between timed steps (512 MiB write)",
                        "parallelism": f"replicas{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],

@@ -36,6 +36,7 @@ int gdn_select_path(int dk, int dv, int C, int qkv_dtype) {
   if (!head_ok(dk) || !head_ok(dv) || !chunk_ok(C)) return GDN_PATH_NONE;
   if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16) return GDN_PATH_NONE;
   if (gdn::tc_supported(dk, dv, C, qkv_dtype == GDN_BF16)) return GDN_PATH_TCGEN05;
+  if (gdn::fwd_chunked_supported(dk, dv, C)) return GDN_PATH_TF32;
   return GDN_PATH_SIMT;
 }
 
@@ -44,6 +45,7 @@ int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype) {
   a.dk = dk; a.dv = dv; a.C = C; a.bf16 = qkv_dtype == GDN_BF16;
   switch (gdn_select_path(dk, dv, C, qkv_dtype)) {
     case GDN_PATH_TCGEN05: return gdn::tc_launches(a);
+    case GDN_PATH_TF32: return gdn::fwd_chunked_launches();
     case GDN_PATH_SIMT: return 1;  // the recurrence kernel
     default: return 0;
   }
@@ -97,6 +99,8 @@ int chunk_fwd_impl(const char* fn, bool linear, const void* q, const void* k, co
   const int path = gdn_select_path(dk, dv, C, qkv_dtype);
   if (path == GDN_PATH_TCGEN05)
     e = gdn::launch_tc(a, s);
+  else if (path == GDN_PATH_TF32 && !linear)
+    e = gdn::launch_fwd_chunked(a, s);
   else
     e = gdn::launch_rec(a, s);
   if (e != cudaSuccess)
@@ -346,7 +350,8 @@ int gdn_chunk_fwd_host(const void* q, const void* k, const void* v, const float*
   a.out = out; a.S_final = S_final; a.workspace = workspace;
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.C = C; a.pieces = pieces;
   a.bf16 = qkv_dtype == GDN_BF16;
-  a.tc = gdn_select_path(dk, dv, C, qkv_dtype) == GDN_PATH_TCGEN05;
+  const int path = gdn_select_path(dk, dv, C, qkv_dtype);
+  a.tc = path == GDN_PATH_TCGEN05 ? 1 : (path == GDN_PATH_TF32 && !linear ? 2 : 0);
   const cudaError_t e = gdn::launch_host_fwd(a, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return fail(GDN_ECUDA, "%s: %s", fn, cudaGetErrorString(e));

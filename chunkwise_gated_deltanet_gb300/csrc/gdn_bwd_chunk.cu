@@ -187,13 +187,13 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
       qv = load4(q + o);
       kv = load4(k + o);
       vv = load4(v + o);
-      ov = load4(dO + o);
+      if (dO) ov = load4(dO + o);
     }
     const size_t d = ob + (size_t)c * D + x;
     store4(p.Qc + d, qv);
     store4(p.Kc + d, kv);
     store4(p.Vc + d, vv);
-    store4(p.dOc + d, ov);
+    if (dO) store4(p.dOc + d, ov);  // the forward gathers no dO
   }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x, c0 = 2 * lane, c1 = c0 + 1;
@@ -233,10 +233,10 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
 // ---------------------------------------------------------------------------------
 // Batched GEMM with fp32 accuracy: for every live batch entry b, the sum of one or two
 // products (terms t)
-//   C(m, n) = alpha * sum_t sum_k A_t(m, k) * ks_t[k] * B_t(k, n) * bs_t[n]
+//   C(m, n) = alpha * sum_t sum_k as_t[m] * A_t(m, k) * ks_t[k] * B_t(k, n) * bs_t[n]
 // A_t(m, k) = A_t[b*ab + m*am + k*ak] (likewise B_t and C), so either operand may be read
 // transposed; one of each operand's two strides is 1, and C's column stride is 1.  ks_t,
-// bs_t: optional per-entry vectors (stride vb).  mask 1 keeps n <= m, mask 2 n < m.  With
+// bs_t, as_t: optional per-entry vectors (stride vb).  mask 1 keeps n <= m, mask 2 n < m.  With
 // C2, the product is also written there times Dg(m, n) = e^{g_m - g_n} for n <= m (0
 // above), g = gv.  M and N are 64 or 128, each term's K 64 or 128: every entry's whole
 // product is one tile.
@@ -267,7 +267,7 @@ struct MmTerm {
   const float* B;
   long long bb;
   int bk, bn;
-  const float *ks, *bs;
+  const float *ks, *bs, *as;  // scales per k, per column n of B, per row m of A
   int K;
 };
 
@@ -297,7 +297,7 @@ constexpr int kMmThreads = 64 + kMmSplitThreads + 128;
 constexpr int kMmRing = 214784;       // both rings: 2 split slots, 2 to 8 raw slots
 constexpr int kMmXch = 16384;         // epilogue exchange buffer: 2 x [32][64] fp32
 constexpr int kMmMaxRaw = 8, kMmMaxSplit = 2;
-constexpr int kMmAux = 384;           // per raw slot: 32 ks + kCk bs values
+constexpr int kMmAux = 640;           // per raw slot: 32 ks + kCk bs + kCk as values
 constexpr int kMmSmem = kMmRing + kMmXch + 1024;
 constexpr int kMmTmemCols = 512;      // two accumulators of up to 256 columns
 
@@ -471,7 +471,8 @@ __global__ void __launch_bounds__(kMmThreads, 1)
       }
       uint32_t bytes[2];
       for (int t = 0; t < 2; ++t)
-        bytes[t] = pan_bytes + (m.t[t].ks ? 128 : 0) + (m.t[t].bs ? 4 * kCk : 0);
+        bytes[t] = pan_bytes + (m.t[t].ks ? 128 : 0) + (m.t[t].bs ? 4 * kCk : 0) +
+                   (m.t[t].as ? 4 * kCk : 0);
       int q = 0, s = 0, ph = 0;  // panel count, its raw slot and that slot's phase
       for (long long b = blockIdx.x; b < nlive; b += gridDim.x) {
         bool ok = true;
@@ -483,6 +484,7 @@ __global__ void __launch_bounds__(kMmThreads, 1)
           mbar_arrive_expect_tx(&bars[RF + s], bytes[t]);
           if (m.t[t].ks) bulk_load(aux, m.t[t].ks + b * m.vb + k0, 128, &bars[RF + s]);
           if (m.t[t].bs) bulk_load(aux + 128, m.t[t].bs + b * m.vb, 4 * kCk, &bars[RF + s]);
+          if (m.t[t].as) bulk_load(aux + 384, m.t[t].as + b * m.vb, 4 * kCk, &bars[RF + s]);
           const CUtensorMap* ma = t ? &mapA1 : &mapA0;
           const CUtensorMap* mb = t ? &mapB1 : &mapB0;
           if (p.akc[t]) tma_load_3d(raw, ma, &bars[RF + s], k0, 0, (int)b);
@@ -555,7 +557,8 @@ __global__ void __launch_bounds__(kMmThreads, 1)
         const int t = pn >= np0;
         const float* ks = m.t[t].ks ? reinterpret_cast<const float*>(aux) : nullptr;
         const float* bs = m.t[t].bs ? reinterpret_cast<const float*>(aux + 128) : nullptr;
-        mm_split_any(raw, spl, spl + M * 128, M, p.akc[t], nullptr, nullptr, ts);
+        const float* as = m.t[t].as ? reinterpret_cast<const float*>(aux + 384) : nullptr;
+        mm_split_any(raw, spl, spl + M * 128, M, p.akc[t], nullptr, as, ts);
         mm_split_any(raw + M * 128, spl + 2 * M * 128, spl + 2 * M * 128 + N * 128, N, p.bkc[t],
                      ks, bs, ts);
         fence_async_smem();
@@ -1518,7 +1521,7 @@ struct MmLauncher {
           int bn, float* C, long long cb, int cm, int cn, int M, int N, int K) const {
     Mm m;
     m.nt = 1;
-    m.t[0] = MmTerm{A, ab, am, ak, B, bb, bk, bn, nullptr, nullptr, K};
+    m.t[0] = MmTerm{A, ab, am, ak, B, bb, bk, bn, nullptr, nullptr, nullptr, K};
     m.t[1] = m.t[0];
     m.C = C; m.cb = cb; m.cm = cm; m.cn = cn;
     m.C2 = nullptr;
@@ -1532,7 +1535,7 @@ struct MmLauncher {
   // A second term, + op(A) op(B) (same M and N), summed on the tensor cores.
   static void add(Mm& m, const float* A, long long ab, int am, int ak, const float* B, long long bb,
                   int bk, int bn, int K) {
-    m.t[1] = MmTerm{A, ab, am, ak, B, bb, bk, bn, nullptr, nullptr, K};
+    m.t[1] = MmTerm{A, ab, am, ak, B, bb, bk, bn, nullptr, nullptr, nullptr, K};
     m.nt = 2;
   }
   void run(const Mm& m) {
@@ -1542,11 +1545,10 @@ struct MmLauncher {
               nb <= 0x7fffffffLL;
     for (int t = 0; ok && t < m.nt; ++t) {
       const MmTerm& x = m.t[t];
-      // the scale vectors are kCk long: ks needs K <= kCk, bs N <= kCk
+      // the scale vectors are kCk long: ks needs K <= kCk, bs N <= kCk, as M <= kCk
       ok = dim_ok(x.K) && (x.am == 1 || x.ak == 1) && (x.bk == 1 || x.bn == 1) &&
-           (!x.ks || x.K <= kCk) && (!x.bs || m.N <= kCk);
+           (!x.ks || x.K <= kCk) && (!x.bs || m.N <= kCk) && (!x.as || m.M <= kCk);
     }
-    if (m.nt == 1) ok = ok && !m.t[1].ks && !m.t[1].bs;
     if (!ok) {
       err = cudaErrorInvalidValue;
       return;
@@ -1813,6 +1815,173 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------
+// The chunk-form forward on the same kernels, for q/k/v in fp32 (or bf16 at dk = dv = 64),
+// dk = dv = 64 or 128, C = 64 (Nyysyyan, "Chunk Computation"; myhz0606 section 4.5): per
+// (chunk, head) entry, A = strictly-lower(beta_i K K^T o D), T = (I + A)^{-1}, W~ =
+// T diag(beta e^g) K, U = T diag(beta) V, P = lower(Q K^T o D); the forward chain gives the
+// chunk-start states S_j, delta = U - W~ S_j^T and the final state; then
+//   O = diag(e^g) Q S_j^T + P delta
+// is one two-term product, and a last kernel writes O's real rows to out.  All products
+// and the chain run in three TF32 passes (fp32 accuracy).
+enum { FQ, FK, FV, FW, FU, FDL, FO, NFCD };  // [kCk][D]
+enum { FKK, FQK, FT, FP, NFCC };             // [kCk][kCk]
+
+struct FwdLayout {
+  long long nc, nb;
+  size_t crow0, clen, cbase, nlive, gates, gam, s, cd[NFCD], cc[NFCC], total;
+};
+
+FwdLayout fwd_layout(long long rows, int H, int D, int N) {
+  FwdLayout L;
+  L.nc = rows / kCk + N;
+  L.nb = L.nc * H;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += al256(bytes); return at; };
+  L.crow0 = take((size_t)L.nc * 8);
+  L.clen = take((size_t)L.nc * 4);
+  L.cbase = take((size_t)(N + 1) * 4);
+  L.nlive = take(8);
+  L.gates = take((size_t)L.nb * kGates * kCk * 4);
+  L.gam = take((size_t)L.nb * 4);
+  L.s = take((size_t)L.nb * D * D * 4);
+  for (int i = 0; i < NFCD; ++i) L.cd[i] = take((size_t)L.nb * kCk * D * 4);
+  for (int i = 0; i < NFCC; ++i) L.cc[i] = take((size_t)L.nb * kCk * kCk * 4);
+  L.total = o;
+  return L;
+}
+
+// O's real rows of every entry to out [rows][H][D] (the input dtype).
+template <int D, typename TOut>
+__global__ void __launch_bounds__(256)
+ck_out_kernel(const float* __restrict__ O, const long long* __restrict__ crow0,
+              const int* __restrict__ clen, const long long* __restrict__ nlive, void* out, int H) {
+  const long long b = blockIdx.x;
+  if (b >= *nlive) return;
+  const long long cid = b / H;
+  const int h = (int)(b - cid * H);
+  const long long row0 = crow0[cid];
+  const int len = clen[cid];
+  TOut* o = reinterpret_cast<TOut*>(out);
+  for (int i = threadIdx.x; i < len * (D / 4); i += 256) {
+    const int c = i / (D / 4), x = 4 * (i % (D / 4));
+    store4(o + ((size_t)(row0 + c) * H + h) * D + x, load4(O + ((size_t)b * kCk + c) * D + x));
+  }
+}
+
+// The forward's scratch comes from a stream-ordered pool of the library's own per device
+// (memory kept for reuse, so that repeated calls do not return to the driver).
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+
+cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pool[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if ((e = cudaMemPoolCreate(&g_pool[dev], &props)) != cudaSuccess) return e;
+      uint64_t keep = ~0ull;
+      if ((e = cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep)) !=
+          cudaSuccess)
+        return e;
+    }
+    pool = g_pool[dev];
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, s);
+}
+
+template <int D, typename TIn>
+cudaError_t launch_fwd_ck_t(const FwdArgs& a, cudaStream_t s) {
+  const long long rows = (long long)a.B * a.T;
+  const FwdLayout L = fwd_layout(rows, a.H, D, a.N);
+  cudaError_t e;
+  static std::atomic<unsigned long long> set_mm{0}, set_c{0};
+  if ((e = ensure_smem_cap(ck_mm_kernel, kMmSmem, set_mm)) != cudaSuccess) return e;
+  if (D == 128) {
+    if ((e = ensure_smem_cap(ck_chain_tc_kernel<false>, kCtSmem, set_c)) != cudaSuccess) return e;
+  } else {
+    if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, chain_smem_bytes<D>(), set_c)) !=
+        cudaSuccess)
+      return e;
+  }
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  int* status = nullptr;
+  if ((e = tc_status_address(&status)) != cudaSuccess) return e;
+  void* wsv = nullptr;
+  if ((e = pool_alloc(&wsv, L.total, s)) != cudaSuccess) return e;
+  unsigned char* ws = reinterpret_cast<unsigned char*>(wsv);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  long long* crow0 = reinterpret_cast<long long*>(ws + L.crow0);
+  int* clen = reinterpret_cast<int*>(ws + L.clen);
+  int* cbase = reinterpret_cast<int*>(ws + L.cbase);
+  long long* nlive = reinterpret_cast<long long*>(ws + L.nlive);
+  float *gates = F(L.gates), *gam = F(L.gam), *S = F(L.s);
+  float *Qc = F(L.cd[FQ]), *Kc = F(L.cd[FK]), *Vc = F(L.cd[FV]), *Wt = F(L.cd[FW]);
+  float *U = F(L.cd[FU]), *Dl = F(L.cd[FDL]), *O = F(L.cd[FO]);
+  float *KK = F(L.cc[FKK]), *QK = F(L.cc[FQK]), *Tm = F(L.cc[FT]), *P = F(L.cc[FP]);
+  const unsigned nb = (unsigned)L.nb;
+  const long long CD = (long long)kCk * D, CC = (long long)kCk * kCk, DD = (long long)D * D;
+  auto run = [&]() -> cudaError_t {
+    cudaError_t e2;
+    ck_table_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.N, a.T, a.H, L.nc, crow0, clen, cbase,
+                                       nlive);
+    if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+    GatherArgs ga;
+    ga.q = a.q; ga.k = a.k; ga.v = a.v; ga.dout = nullptr;
+    ga.log_alpha = a.log_alpha; ga.beta = a.beta;
+    ga.crow0 = crow0; ga.clen = clen; ga.nlive = nlive;
+    ga.Qc = Qc; ga.Kc = Kc; ga.Vc = Vc; ga.dOc = nullptr; ga.gates = gates; ga.gam = gam;
+    ga.H = a.H;
+    ck_gather_kernel<D, TIn><<<nb, 256, 0, s>>>(ga);
+    if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+    MmLauncher mm{L.nb, nlive, s, status, (int)std::min<long long>(L.nb, std::max(sms, 1))};
+    mm.run(mm.make(Kc, CD, D, 1, Kc, CD, 1, D, KK, CC, kCk, 1, kCk, kCk, D));
+    mm.run(mm.make(Qc, CD, D, 1, Kc, CD, 1, D, QK, CC, kCk, 1, kCk, kCk, D));
+    if (mm.err != cudaSuccess) return mm.err;
+    TsolveArgs ta{KK, QK, gates, Tm, P, nlive};
+    ck_tsolve_kernel<<<nb, 128, 0, s>>>(ta);
+    if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+    {  // W~ = T diag(beta e^g) K,  U = T diag(beta) V
+      Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
+      m.t[0].ks = gates + G_BEG * kCk;
+      mm.run(m);
+      m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
+      m.t[0].ks = gates + G_BETA * kCk;
+      mm.run(m);
+    }
+    if (mm.err != cudaSuccess) return mm.err;
+    ChainArgs cf;
+    cf.cbase = cbase; cf.init = a.S0; cf.fin = a.S_final; cf.st = S;
+    cf.add1 = U; cf.a1 = Wt; cf.a2 = Kc; cf.add2 = nullptr; cf.out1 = Dl;
+    cf.gates = gates; cf.gam = gam; cf.H = a.H;
+    if ((e2 = launch_chain<D, false>(cf, L.nb, a.N, a.H, status, s)) != cudaSuccess) return e2;
+    {  // O = diag(e^g) Q S_j^T + P delta
+      Mm m = mm.make(Qc, CD, D, 1, S, DD, 1, D, O, CD, D, 1, kCk, D, D);
+      m.t[0].as = gates + G_EG * kCk;
+      MmLauncher::add(m, P, CC, kCk, 1, Dl, CD, D, 1, kCk);
+      mm.run(m);
+    }
+    if (mm.err != cudaSuccess) return mm.err;
+    ck_out_kernel<D, TIn><<<nb, 256, 0, s>>>(O, crow0, clen, nlive, a.out, a.H);
+    return cudaGetLastError();
+  };
+  e = run();
+  // the scratch returns to the pool behind the launches (also after a failed launch)
+  const cudaError_t ef = cudaFreeAsync(wsv, s);
+  return e != cudaSuccess ? e : ef;
+}
+
 }  // namespace
 
 bool bwd_chunked_supported(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
@@ -1827,6 +1996,19 @@ cudaError_t launch_bwd_chunked(const BwdArgs& a, cudaStream_t stream) {
   if ((long long)a.N * a.H > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (a.dk == 64) return a.bf16 ? launch_ck_t<64, __nv_bfloat16>(a, stream) : launch_ck_t<64, float>(a, stream);
   return a.bf16 ? launch_ck_t<128, __nv_bfloat16>(a, stream) : launch_ck_t<128, float>(a, stream);
+}
+
+bool fwd_chunked_supported(int dk, int dv, int C) {
+  return dk == dv && (dk == 64 || dk == 128) && C == kCk;
+}
+
+int fwd_chunked_launches() { return 10; }
+
+cudaError_t launch_fwd_chunked(const FwdArgs& a, cudaStream_t stream) {
+  if (!fwd_chunked_supported(a.dk, a.dv, a.C)) return cudaErrorInvalidValue;
+  if ((long long)a.N * a.H > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (a.dk == 64) return a.bf16 ? launch_fwd_ck_t<64, __nv_bfloat16>(a, stream) : launch_fwd_ck_t<64, float>(a, stream);
+  return a.bf16 ? launch_fwd_ck_t<128, __nv_bfloat16>(a, stream) : launch_fwd_ck_t<128, float>(a, stream);
 }
 
 }  // namespace gdn

@@ -177,7 +177,8 @@ cudaError_t launch_host_fwd(const HostFwdArgs& a, cudaStream_t stream) {
     f.cu_seqlens = nullptr;
     f.B = a.B; f.H = a.H; f.T = (int)len; f.dk = a.dk; f.dv = a.dv; f.C = a.C; f.N = a.B;
     f.bf16 = a.bf16;
-    e = a.tc ? launch_tc(f, stream) : launch_rec(f, stream);
+    e = a.tc == 1 ? launch_tc(f, stream)
+                  : (a.tc == 2 ? launch_fwd_chunked(f, stream) : launch_rec(f, stream));
     if (e == cudaSuccess) e = cudaEventRecord(computed[r], stream);
     prev = st;
     if (e != cudaSuccess) break;

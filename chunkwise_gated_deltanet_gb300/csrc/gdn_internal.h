@@ -44,6 +44,12 @@ struct FwdArgs {
 // Per-token recurrence on CUDA cores, fp32 arithmetic, any supported shape (C unused).
 cudaError_t launch_rec(const FwdArgs& a, cudaStream_t stream);
 
+// The chunk form on the backward's tcgen05 kernels (three TF32 passes): dk = dv = 64 or
+// 128, C = 64, fp32 or bf16 q/k/v; scratch from a stream-ordered pool of the library's.
+bool fwd_chunked_supported(int dk, int dv, int C);
+int fwd_chunked_launches();
+cudaError_t launch_fwd_chunked(const FwdArgs& a, cudaStream_t stream);
+
 // tcgen05 kernel: bf16, dk = dv = 128, C = 64.
 bool tc_supported(int dk, int dv, int C, int bf16);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream);
@@ -73,7 +79,8 @@ struct HostFwdArgs {
   void* workspace;        // device, host_fwd_workspace_bytes(...)
   int B, H, T, dk, dv, C, pieces;
   int bf16;
-  int tc;                 // 1: the tcgen05 kernel, 0: the SIMT kernel
+  int tc;                 // 1: the tcgen05 kernel, 2: the chunk form on the TF32 kernels,
+                          // 0: the SIMT kernel
 };
 size_t host_fwd_workspace_bytes(int B, int H, int T, int dk, int dv, int C, int esz, int pieces,
                                 bool has_beta);

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 GDN_OK, GDN_EINVAL, GDN_EDTYPE, GDN_ELAUNCH, GDN_ETIMEOUT, GDN_ECUDA = range(6)
 GDN_F32, GDN_BF16 = 0, 1
-GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05 = 0, 1, 2
+GDN_PATH_NONE, GDN_PATH_SIMT, GDN_PATH_TCGEN05, GDN_PATH_TF32 = 0, 1, 2, 3
 GDN_BWD_AUTO, GDN_BWD_TOKENS, GDN_BWD_CHUNKED = 0, 1, 2
 EXPORTS = ("gdn_chunk_fwd", "gdn_chunk_fwd_host", "gdn_chunk_fwd_host_workspace_bytes",
            "gdn_decode_step_host", "gdn_decode_step_host_workspace_bytes",

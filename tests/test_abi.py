@@ -52,9 +52,11 @@ def test_version(lib):
 
 @pytest.mark.parametrize("dk,dv,C,dt,path", [
     (128, 128, 64, torch.bfloat16, None),     # tensor-core path once available
-    (128, 128, 64, torch.float32, gdn.GDN_PATH_SIMT),
+    (128, 128, 64, torch.float32, gdn.GDN_PATH_TF32),
     (16, 16, 16, torch.float32, gdn.GDN_PATH_SIMT),
-    (64, 64, 64, torch.float32, gdn.GDN_PATH_SIMT),
+    (64, 64, 64, torch.float32, gdn.GDN_PATH_TF32),
+    (64, 64, 64, torch.bfloat16, gdn.GDN_PATH_TF32),
+    (64, 64, 32, torch.float32, gdn.GDN_PATH_SIMT),
     (64, 128, 32, torch.bfloat16, gdn.GDN_PATH_SIMT),
     (48, 64, 64, torch.float32, gdn.GDN_PATH_NONE),
     (64, 64, 128, torch.float32, gdn.GDN_PATH_NONE),

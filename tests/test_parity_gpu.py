@@ -227,4 +227,5 @@ def test_host_tensors_round_trip():
 def test_selected_path_reported():
     p = gdn.gdn_select_path(128, 128, 64, torch.bfloat16)
     assert p in (gdn.GDN_PATH_SIMT, gdn.GDN_PATH_TCGEN05)
-    assert gdn.gdn_select_path(64, 64, 64, torch.float32) == gdn.GDN_PATH_SIMT
+    assert gdn.gdn_select_path(64, 64, 64, torch.float32) == gdn.GDN_PATH_TF32
+    assert gdn.gdn_select_path(16, 16, 16, torch.float32) == gdn.GDN_PATH_SIMT
