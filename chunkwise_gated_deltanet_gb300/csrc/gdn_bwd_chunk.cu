@@ -665,19 +665,35 @@ __global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
   __shared__ float As[kCk][kCk + 1], Ts[kCk][kCk + 1], Wb[3 * 256], g[kCk], be[kCk];
   const int tid = threadIdx.x;
   const float* G = p.gates + (size_t)b * kGates * kCk;
+  const size_t ob = (size_t)b * kCk * kCk;
+  // both 64 x 64 inputs as 8 float4 per thread, all loads in flight together
+  float4 kk[8], qk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    kk[i] = ld4(p.KK + ob + 4 * tid + 512 * i);
+    qk[i] = ld4(p.QK + ob + 4 * tid + 512 * i);
+  }
   if (tid < kCk) {
     g[tid] = G[G_G * kCk + tid];
     be[tid] = G[G_BETA * kCk + tid];
   }
   __syncthreads();
-  const size_t ob = (size_t)b * kCk * kCk;
-  for (int idx = tid; idx < kCk * kCk; idx += 128) {
-    const int i = idx >> 6, j = idx & 63;
-    const float Dij = j <= i ? expf(g[i] - g[j]) : 0.f;
-    As[i][j] = j < i ? be[i] * p.KK[ob + idx] * Dij : 0.f;
-    p.P[ob + idx] = p.QK[ob + idx] * Dij;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = 4 * tid + 512 * i, r = idx >> 6, j0 = idx & 63;
+    const float x[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
+    const float y[4] = {qk[i].x, qk[i].y, qk[i].z, qk[i].w};
+    float pd[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + e;
+      const float Dij = j <= r ? expf(g[r] - g[j]) : 0.f;
+      As[r][j] = j < r ? be[r] * x[e] * Dij : 0.f;
+      pd[e] = y[e] * Dij;
+      Ts[r][j] = 0.f;
+    }
+    st4(p.P + ob + idx, pd[0], pd[1], pd[2], pd[3]);
   }
-  for (int idx = tid; idx < kCk * kCk; idx += 128) Ts[idx >> 6][idx & 63] = 0.f;
   __syncthreads();
   // Diagonal 16 x 16 blocks: T_ii = (I + A_ii)^{-1}, one thread per column of a block.
   if (tid < kCk) {
@@ -1290,35 +1306,63 @@ struct DaArgs {
 __global__ void __launch_bounds__(256) ck_da_kernel(DaArgs p) {
   const long long b = blockIdx.x;
   if (b >= *p.nlive) return;
-  __shared__ float E1[kCk][kCk + 1], E2[kCk][kCk + 1], g[kCk], be[kCk];
+  __shared__ float Ad[kCk][kCk + 1], E2[kCk][kCk + 1], g[kCk], be[kCk];
   const int tid = threadIdx.x;
   const float* G = p.gates + (size_t)b * kGates * kCk;
+  const size_t ob = (size_t)b * kCk * kCk;
+  // the four 64 x 64 inputs as 4 float4 each per thread, all loads in flight together;
+  // a thread's float4 i covers row tid / 16 + 16 i, columns 4 (tid % 16) ..
+  float4 da[4], kk[4], dp[4], qk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const size_t o = ob + 4 * tid + 1024 * i;
+    da[i] = ld4(p.dA + o);
+    kk[i] = ld4(p.KK + o);
+    dp[i] = ld4(p.dPm + o);
+    qk[i] = ld4(p.QK + o);
+  }
   if (tid < kCk) {
     g[tid] = G[G_G * kCk + tid];
     be[tid] = G[G_BETA * kCk + tid];
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = tid / 16 + 16 * i, j0 = 4 * (tid % 16);
+    Ad[r][j0] = da[i].x; Ad[r][j0 + 1] = da[i].y; Ad[r][j0 + 2] = da[i].z; Ad[r][j0 + 3] = da[i].w;
+  }
   __syncthreads();
-  const size_t ob = (size_t)b * kCk * kCk;
-  for (int idx = tid; idx < kCk * kCk; idx += 256) {
-    const int i = idx >> 6, j = idx & 63;
-    const float Dij = j <= i ? expf(g[i] - g[j]) : 0.f;
-    const float da = p.dA[ob + idx], kk = p.KK[ob + idx];
-    // X + X^T: dA is strictly lower, so each element takes the one of X(i, j), X(j, i)
-    // that can be nonzero
-    const int hi = i > j ? i : j, lo = i > j ? j : i;
-    p.X[ob + idx] = i == j ? 0.f : p.dA[ob + hi * kCk + lo] * expf(g[hi] - g[lo]) * be[hi];
-    E1[i][j] = da * kk * Dij;
-    E2[i][j] = (da * be[i] * kk + p.dPm[ob + idx] * p.QK[ob + idx]) * Dij;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = tid / 16 + 16 * i, j0 = 4 * (tid % 16);
+    const float a4[4] = {da[i].x, da[i].y, da[i].z, da[i].w};
+    const float k4[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
+    const float d4[4] = {dp[i].x, dp[i].y, dp[i].z, dp[i].w};
+    const float q4[4] = {qk[i].x, qk[i].y, qk[i].z, qk[i].w};
+    float xs[4], e1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + e;
+      const float Dij = j <= r ? expf(g[r] - g[j]) : 0.f;
+      // X + X^T: dA is strictly lower, so each element takes the one of X(r, j), X(j, r)
+      // that can be nonzero
+      const int hi = r > j ? r : j, lo = r > j ? j : r;
+      xs[e] = r == j ? 0.f : Ad[hi][lo] * expf(g[hi] - g[lo]) * be[hi];
+      e1 += a4[e] * k4[e] * Dij;
+      E2[r][j] = (a4[e] * be[r] * k4[e] + d4[e] * q4[e]) * Dij;
+    }
+    st4(p.X + ob + 4 * tid + 1024 * i, xs[0], xs[1], xs[2], xs[3]);
+    // row sum of dA o KK^T o D over the row's 16 threads (a half warp)
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+    if ((tid & 15) == 0) p.db3[(size_t)b * kCk + r] = e1;
   }
   __syncthreads();
   if (tid < kCk) {
-    float r1 = 0.f, r2 = 0.f, c2 = 0.f;
+    float r2 = 0.f, c2 = 0.f;
     for (int j = 0; j < kCk; ++j) {
-      r1 += E1[tid][j];
       r2 += E2[tid][j];
       c2 += E2[j][tid];
     }
-    p.db3[(size_t)b * kCk + tid] = r1;
     p.dg1[(size_t)b * kCk + tid] = r2 - c2;
   }
 }
