@@ -33,23 +33,29 @@ def _inputs(B=2, T=150, H=2, dk=16, dv=16, seed=0):
     return q, k, v, la, beta, S0
 
 
-def _oracle_forward(q, k, v, la, beta, S0, C, linear):
+def _oracle_forward(q, k, v, la, beta, S0, C, linear, cu_seqlens=None):
     """Each (sequence, head) through the fp64 per-token recurrence (C is irrelevant
-    to the definition).  Linear mode: erase 0, write 1."""
+    to the definition).  Linear mode: erase 0, write 1.  With cu_seqlens, the members
+    of a packed [1, T, ...] batch."""
     B, T, H, dk = k.shape
     dv = v.shape[-1]
+    if cu_seqlens is None:
+        spans = [(b, 0, T) for b in range(B)]
+    else:
+        cu = [int(x) for x in cu_seqlens.tolist()]
+        spans = [(0, cu[n], cu[n + 1]) for n in range(len(cu) - 1)]
     out = np.zeros((B, T, H, dv))
-    Sf = np.zeros((B, H, dv, dk))
-    for b in range(B):
+    Sf = np.zeros((len(spans), H, dv, dk))
+    for n, (b, t0, t1) in enumerate(spans):
         for h in range(H):
-            s0 = None if S0 is None else S0[b, h].double().numpy()
+            s0 = None if S0 is None else S0[n, h].double().numpy()
             kw = {}
             if linear:
-                kw = dict(erase=np.zeros(T), write=np.ones(T))
-            o, S = R.gdn_sequence(q[b, :, h].double().numpy(), k[b, :, h].double().numpy(),
-                                  v[b, :, h].double().numpy(), la[b, :, h].double().numpy(),
-                                  beta[b, :, h].double().numpy(), s0, **kw)
-            out[b, :, h], Sf[b, h] = o, S
+                kw = dict(erase=np.zeros(t1 - t0), write=np.ones(t1 - t0))
+            o, S = R.gdn_sequence(q[b, t0:t1, h].double().numpy(), k[b, t0:t1, h].double().numpy(),
+                                  v[b, t0:t1, h].double().numpy(), la[b, t0:t1, h].double().numpy(),
+                                  beta[b, t0:t1, h].double().numpy(), s0, **kw)
+            out[b, t0:t1, h], Sf[n, h] = o, S
     return torch.from_numpy(out), torch.from_numpy(Sf)
 
 
@@ -115,6 +121,40 @@ def test_emulated_split_matches_unsplit(world, linear):
     assert torch.allclose(Sf, ref_S, rtol=1e-10, atol=1e-12)
 
 
+PACKED_LENS = [5, 0, 70, 130, 1, 33]
+
+
+def _packed_inputs(seed=0):
+    q, k, v, la, beta, _ = _inputs(B=1, T=sum(PACKED_LENS), seed=seed)
+    g = torch.Generator().manual_seed(seed + 100)
+    S0 = 0.1 * torch.randn(len(PACKED_LENS), 2, 16, 16, generator=g)
+    cu = torch.tensor([0] + list(np.cumsum(PACKED_LENS)), dtype=torch.int32)
+    return q, k, v, la, beta, S0, cu
+
+
+def test_packed_segments_cover_each_member_in_order():
+    cu = torch.tensor([0] + list(np.cumsum(PACKED_LENS)), dtype=torch.int32)
+    for world in (1, 2, 3, 4):
+        parts = seqpar.packed_segments(cu, world, 16)
+        seen = torch.cat([idx for idx, _ in parts])
+        assert sorted(seen.tolist()) == list(range(int(cu[-1])))
+        for n, L in enumerate(PACKED_LENS):
+            pieces = [(int(c[n + 1] - c[n])) for _, c in parts]
+            assert sum(pieces) == L
+            b = seqpar.segment_bounds(L, world, 16)
+            assert pieces == [e - a for a, e in b]
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5])
+@pytest.mark.parametrize("linear", [False, True])
+def test_emulated_packed_split_matches_unsplit(world, linear):
+    q, k, v, la, beta, S0, cu = _packed_inputs(seed=world)
+    out, Sf = seqpar.emulate(q, k, v, la, beta, S0, 16, world, linear, ORACLE_OPS, cu)
+    ref_o, ref_S = _oracle_forward(q, k, v, la, beta, S0, 16, linear, cu)
+    assert torch.allclose(out, ref_o, rtol=1e-10, atol=1e-12)
+    assert torch.allclose(Sf, ref_S, rtol=1e-10, atol=1e-12)
+
+
 # -------------------------------------------------------- gloo, real ranks --
 
 def _free_port():
@@ -138,6 +178,45 @@ def _rank_main(rank, world, port, linear, queue):
     queue.put((rank, bnd, out.numpy(), Sf.numpy()))
     dist.barrier()
     dist.destroy_process_group()
+
+
+def _packed_rank_main(rank, world, port, queue):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from chunkwise_gated_deltanet_gb300 import seqpar as sp
+    from tests import test_seqpar_cpu as me
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q, k, v, la, beta, S0, cu = me._packed_inputs(seed=9)
+    idx, cu_r = sp.packed_segments(cu, world, 16)[rank]
+    seg = [sp.packed_segment(t, idx) for t in (q, k, v, la, beta)]
+    out, Sf = sp.seqpar_chunk_fwd(*seg, S0 if rank == 0 else None, 16, ops=me.ORACLE_OPS,
+                                  cu_seqlens=cu_r)
+    queue.put((rank, idx.numpy(), out.numpy(), Sf.numpy()))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_gloo_ranks_packed_match_unsplit(world):
+    ctx = mp.get_context("spawn")
+    queue = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_packed_rank_main, args=(r, world, port, queue))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted((queue.get(timeout=300) for _ in range(world)), key=lambda x: x[0])
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    q, k, v, la, beta, S0, cu = _packed_inputs(seed=9)
+    ref_o, ref_S = _oracle_forward(q, k, v, la, beta, S0, 16, False, cu)
+    got = np.zeros(ref_o.shape)
+    for _, idx, o, _ in res:
+        got[:, idx] = o
+    assert np.allclose(got, ref_o.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(res[-1][3], ref_S.numpy(), rtol=1e-10, atol=1e-12)
 
 
 @pytest.mark.parametrize("world,linear", [(2, False), (3, False), (3, True)])

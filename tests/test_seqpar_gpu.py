@@ -102,3 +102,34 @@ def test_split_bf16_tcgen05(world, linear):
     ro, rs = _oracle(inp, linear)
     assert_close(o, ro, False, "out", stored_bf16=True)
     assert_close(s, rs, False, "S_final")
+
+
+@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("name", ["gdn_f32_b2h4t1024d64c64", "gdn_bf16_varlen256_h16d128c64"],
+                         ids=["f32_d64", "bf16_d128"])
+def test_split_packed(name, world):
+    """A packed batch (members of uneven lengths, one shorter than a chunk, one empty):
+    each member cut at its own chunk-aligned bounds, the ranks' packed segments run
+    through the library and folded, against the unsplit oracle."""
+    w = W[name]
+    lens = [5, 0, 70, 130, 1, 200]
+    # the fixed-length generator of the same dtype and head size, packed by hand
+    base = w if not w.varlen else W["gdn_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(base, B=1, H=2, T=sum(lens), seed=world)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    inp["cu_seqlens"] = cu
+    inp["N"] = len(lens)
+    inp["S0"] = 0.1 * torch.randn(len(lens), 2, w.dv, w.dk,
+                                  generator=torch.Generator().manual_seed(world))
+    d = to_device(inp)
+    out, Sf = seqpar.emulate(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], 64,
+                             world, False, cu_seqlens=d["cu_seqlens"])
+    gdn.gdn_check_status()
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy().astype(np.float64)
+    s = Sf.cpu().numpy().astype(np.float64)
+    ro, rs = native.gdn_forward_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"],
+                                  inp["S0"], inp["cu_seqlens"])
+    fp32 = inp["dtype"] == "f32"
+    assert_close(o, ro, fp32, "out", stored_bf16=not fp32)
+    assert_close(s, rs, fp32, "S_final")
