@@ -25,15 +25,15 @@
 // buffers in the workspace (a ragged last chunk is zero-filled with beta = 0 and
 // log alpha = 0, which adds nothing to any sum).  The two serial parts, the chunk-start
 // states S_j (forward) and the chunk-end state gradients dS'_j (reverse), run in one
-// chain kernel that splits the dv rows of the state over CTAs: rows are independent
-// given the chunk's operands.  Everything else is chunk-parallel: a batched GEMM
-// (64 x 64 output tiles, one per CTA and batch entry) and small per-chunk kernels for
-// the triangular solve, the gate terms and the final per-token sums.
+// chain kernel with the state of a (sequence, head) in tensor memory.  Everything else is
+// chunk-parallel: a persistent batched product kernel (a whole entry's product per work
+// item) and small per-chunk kernels for the triangular solve, the gate terms and the final
+// per-token sums.
 //
-// Accuracy is fp32's: the products (batched GEMM and both chain products) run on the
-// tensor cores in three TF32 passes (hi*hi + hi*lo + lo*hi of a two-part TF32 split of
-// each fp32 operand, accumulated in fp32: ~2^-22 relative error per product); the rest is
-// fp32 on the CUDA cores.  Head sizes dk = dv = 64 or 128.
+// Accuracy is fp32's: the products (batched and in both chains) run on the tcgen05 tensor
+// cores in three TF32 passes (hi*hi + hi*lo + lo*hi of a two-part TF32 split of each fp32
+// operand, accumulated in fp32: ~2^-22 relative error per product); the rest is fp32 on
+// the CUDA cores.  Head sizes dk = dv = 64 or 128.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -48,7 +48,6 @@ namespace gdn {
 namespace {
 
 constexpr int kCk = 64;             // chunk length
-constexpr int kRows = 32;           // state rows per chain CTA
 constexpr float kLogAlphaMin = -80.f;  // alpha = 0 (log alpha = -inf) is taken as e^-80
 
 // Per-batch-entry gate vectors, each kCk long.
@@ -300,31 +299,6 @@ constexpr int kMmMaxRaw = 8, kMmMaxSplit = 2;
 constexpr int kMmAux = 640;           // per raw slot: 32 ks + kCk bs + kCk as values
 constexpr int kMmSmem = kMmRing + kMmXch + 1024;
 constexpr int kMmTmemCols = 512;      // two accumulators of up to 256 columns
-
-__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-  const float r = x - __uint_as_float(hi);
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
-}
-
-// D (16 x 8, fp32) += A (16 x 8, row) B (8 x 8, col), TF32 inputs.
-__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
-}
 
 // Instruction descriptor, kind::tf32: fp32 accumulator, TF32 A and B, both K-major.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -732,8 +706,8 @@ __global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
 }
 
 // ---------------------------------------------------------------------------------
-// The state chain of one (sequence, head) over kRows rows of the state, chunk by chunk
-// (forward, or in reverse for the gradient).  Per chunk, with the rows St (kRows x D):
+// The state chain of one (sequence, head), chunk by chunk (forward, or in reverse for the
+// gradient).  Per chunk, with the state St (D x D):
 //   X1(c, r) = Add1(c, r) + s1_c * sum_k A1(c, k) St(r, k)       -> out1
 //   St(r, k) = Add2(r, k) + Gamma St(r, k) + sum_c s2_c X1(c, r) A2(c, k)
 // forward:  Add1 = U, s1 = -1, A1 = W~, s2 = E, A2 = K, no Add2 (X1 = delta, St = S)
@@ -751,193 +725,10 @@ struct ChainArgs {
   int H;
 };
 
-template <int D>
-constexpr int chain_smem_bytes() {
-  return 4 * (kRows * (D + 4) + kCk * (D + 4) + kCk * (D + 8) + 2 * kCk + kRows * (kCk + 4));
-}
-
-// A [kCk][D] operand tile into shared memory rows of LD floats, as one async group;
-// with vec, also the entry's E and e^g gate vectors (threads 0..31).
-template <int D, int LD>
-__device__ __forceinline__ void chain_issue(float* dst, const float* src, float* vec,
-                                            const float* gates) {
-  for (int i = threadIdx.x; i < kCk * D / 4; i += 256) {
-    const int c = i / (D / 4), k = 4 * (i % (D / 4));
-    cp_async16(dst + c * LD + k, src + (size_t)c * D + k);
-  }
-  if (vec && threadIdx.x < 32) {
-    const int t = threadIdx.x;
-    const float* g = gates + (t < 16 ? G_E * kCk + 4 * t : G_EG * kCk + 4 * (t - 16));
-    cp_async16(vec + 4 * t, g);
-  }
-  cp_async_commit();
-}
-
-// The two products on the tensor cores in three TF32 passes, like ck_mm_kernel.
-//   X1 (kCk x kRows): warp w takes rows 16 (w % 4) .. +15 and the two 8-column tiles
-//     2 (w / 4) and 2 (w / 4) + 1; A = A1 [c][k] (row stride D + 4), B(k, r) = St[r][k].
-//   St (kRows x D):  warp w takes rows 16 (w % 2) .. +15 and D / 32 8-column tiles from
-//     D / 32 * (w / 2); A(r, c) = X1t[r][c] (row stride kCk + 4), B(c, k) = A2 [c][k]
-//     (row stride D + 8).
-// The strides put the 32 lanes' fragment reads in 32 different banks.
-template <int D, bool REV>
-__global__ void __launch_bounds__(256) ck_chain_kernel(ChainArgs p) {
-  extern __shared__ __align__(16) float sm[];
-  constexpr int LD1 = D + 4, LD2 = D + 8, LX = kCk + 4, NT = D / 32;
-  float* St = sm;                  // [kRows][LD1]
-  float* A1 = St + kRows * LD1;    // [kCk][LD1]
-  float* A2 = A1 + kCk * LD1;      // [kCk][LD2]
-  float* Vv = A2 + kCk * LD2;      // E [kCk], e^g [kCk]
-  float* X1 = Vv + 2 * kCk;        // s2_c X1(c, r) as [kRows][LX]
-  const int unit = blockIdx.x, n = unit / p.H, h = unit % p.H, r0 = blockIdx.y * kRows;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
-  const int base = p.cbase[n], nc = p.cbase[n + 1] - base;
-  const size_t sidx = ((size_t)n * p.H + h) * D * D;
-  auto entry = [&](int jj) { return (long long)(base + (REV ? nc - 1 - jj : jj)) * p.H + h; };
-  if (nc > 0) {
-    const long long b = entry(0);
-    chain_issue<D, LD1>(A1, p.a1 + (size_t)b * kCk * D, Vv, p.gates + (size_t)b * kGates * kCk);
-    chain_issue<D, LD2>(A2, p.a2 + (size_t)b * kCk * D, nullptr, nullptr);
-  }
-  for (int i = tid; i < kRows * D; i += 256) {
-    const int r = i / D, k = i % D;
-    St[r * LD1 + k] = p.init ? p.init[sidx + (size_t)(r0 + r) * D + k] : 0.f;
-  }
-  const int xm = 16 * (warp & 3), xn = 16 * (warp >> 2);      // X1 tile origin
-  const int sm0 = 16 * (warp & 1), sn = 8 * NT * (warp >> 1);  // St tile origin
-  for (int jj = 0; jj < nc; ++jj) {
-    const long long b = entry(jj);
-    __syncthreads();  // St complete (init or the previous update)
-    float* stb = p.st + (size_t)b * D * D;
-    for (int i = tid; i < kRows * D / 4; i += 256) {
-      const int r = i / (D / 4), k = 4 * (i % (D / 4));
-      *reinterpret_cast<float4*>(stb + (size_t)(r0 + r) * D + k) =
-          *reinterpret_cast<const float4*>(St + r * LD1 + k);
-    }
-    float add1[2][4];
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = xm + g + 8 * (j >> 1), r = xn + 8 * q + 2 * t + (j & 1);
-        add1[q][j] = p.add1[(size_t)b * kCk * D + (size_t)c * D + r0 + r];
-      }
-    cp_async_wait<1>();  // A1 and the gate vectors
-    __syncthreads();
-    {  // X1(c, r) = Add1 + s1_c sum_k A1(c, k) St(r, k)
-      float acc[2][4];
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[q][j] = 0.f;
-#pragma unroll 4
-      for (int kb = 0; kb < D; kb += 8) {
-        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
-        const float* a = A1 + (xm + g) * LD1 + kb + t;
-        tf32_split(a[0], ah[0], al[0]);
-        tf32_split(a[8 * LD1], ah[1], al[1]);
-        tf32_split(a[4], ah[2], al[2]);
-        tf32_split(a[8 * LD1 + 4], ah[3], al[3]);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float* bp = St + (xn + 8 * q + g) * LD1 + kb + t;
-          tf32_split(bp[0], bh[q][0], bl[q][0]);
-          tf32_split(bp[4], bh[q][1], bl[q][1]);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          mma_tf32(acc[q], al, bh[q]);
-          mma_tf32(acc[q], ah, bl[q]);
-          mma_tf32(acc[q], ah, bh[q]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = xm + g + 8 * (j >> 1), r = xn + 8 * q + 2 * t + (j & 1);
-          const float e = Vv[c];
-          const float s1 = REV ? e : -1.f, s2 = REV ? -1.f : e;
-          const float x = add1[q][j] + s1 * acc[q][j];
-          p.out1[(size_t)b * kCk * D + (size_t)c * D + r0 + r] = x;
-          X1[r * LX + c] = s2 * x;
-        }
-    }
-    const float gam = Vv[kCk + kCk - 1];  // e^{g_last}
-    float add2[NT][4];
-    if (REV) {
-#pragma unroll
-      for (int q = 0; q < NT; ++q)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = sm0 + g + 8 * (j >> 1), k = sn + 8 * q + 2 * t + (j & 1);
-          add2[q][j] = p.add2[(size_t)b * D * D + (size_t)(r0 + r) * D + k];
-        }
-    }
-    __syncthreads();  // X1 complete; A1 and the gate vectors free
-    if (jj + 1 < nc) {
-      const long long bn = entry(jj + 1);
-      chain_issue<D, LD1>(A1, p.a1 + (size_t)bn * kCk * D, Vv, p.gates + (size_t)bn * kGates * kCk);
-      cp_async_wait<1>();  // A2 of this chunk
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    {  // St(r, k) = Add2 + Gamma St(r, k) + sum_c s2_c X1(c, r) A2(c, k)
-      float acc[NT][4];
-#pragma unroll
-      for (int q = 0; q < NT; ++q)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[q][j] = 0.f;
-#pragma unroll 2
-      for (int kb = 0; kb < kCk; kb += 8) {
-        uint32_t ah[4], al[4], bh[NT][2], bl[NT][2];
-        const float* a = X1 + (sm0 + g) * LX + kb + t;
-        tf32_split(a[0], ah[0], al[0]);
-        tf32_split(a[8 * LX], ah[1], al[1]);
-        tf32_split(a[4], ah[2], al[2]);
-        tf32_split(a[8 * LX + 4], ah[3], al[3]);
-#pragma unroll
-        for (int q = 0; q < NT; ++q) {
-          const float* bp = A2 + (kb + t) * LD2 + sn + 8 * q + g;
-          tf32_split(bp[0], bh[q][0], bl[q][0]);
-          tf32_split(bp[4 * LD2], bh[q][1], bl[q][1]);
-        }
-#pragma unroll
-        for (int q = 0; q < NT; ++q) {
-          mma_tf32(acc[q], al, bh[q]);
-          mma_tf32(acc[q], ah, bl[q]);
-          mma_tf32(acc[q], ah, bh[q]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < NT; ++q)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = sm0 + g + 8 * (j >> 1), k = sn + 8 * q + 2 * t + (j & 1);
-          float v = fmaf(gam, St[r * LD1 + k], acc[q][j]);
-          if (REV) v += add2[q][j];
-          St[r * LD1 + k] = v;
-        }
-    }
-    __syncthreads();  // A2 free
-    if (jj + 1 < nc) {
-      const long long bn = entry(jj + 1);
-      chain_issue<D, LD2>(A2, p.a2 + (size_t)bn * kCk * D, nullptr, nullptr);
-    }
-  }
-  __syncthreads();
-  if (p.fin)
-    for (int i = tid; i < kRows * D; i += 256) {
-      const int r = i / D, k = i % D;
-      p.fin[sidx + (size_t)(r0 + r) * D + k] = St[r * LD1 + k];
-    }
-}
-
 // ---------------------------------------------------------------------------------
-// The same chain on the tcgen05 tensor cores, for dk = dv = 128: one CTA per (sequence,
-// head) holds the whole state St (128 x 128 fp32) in tensor memory, as the accumulator of
-// its update, and runs both products of a chunk in three TF32 passes:
+// The chain on the tcgen05 tensor cores (dk = dv = 128 or 64): one CTA per (sequence,
+// head) holds the whole state St (D x D fp32) in tensor memory, as the accumulator of its
+// update, and runs both products of a chunk in three TF32 passes:
 //   X1^T(r, c) = sum_k St(r, k) A1(c, k):  A = the hi and lo parts of St, copied to tensor
 //                memory; B = [A1_hi; A1_lo] (128 rows) for St_hi and A1_hi for St_lo;
 //   St(r, k)  += sum_c (s2 o X1)(c, r) A2(c, k):  A = the hi and lo parts of s2 o X1 in
@@ -987,13 +778,16 @@ __device__ __forceinline__ void split32_to_tmem(uint32_t t_hi, uint32_t t_lo, co
   tmem_st32(t_lo, l);
 }
 
-template <bool REV>
+template <bool REV, int D>
 __global__ void __launch_bounds__(kCtThreads, 1)
     ck_chain_tc_kernel(const __grid_constant__ CUtensorMap mapA1,
                        const __grid_constant__ CUtensorMap mapA2,
                        const __grid_constant__ CUtensorMap mapSt,
                        const __grid_constant__ CUtensorMap mapAdd2, const ChainTcArgs args) {
-  constexpr int D = 128;
+  // D = 128 or 64: the state's rows are TMEM lanes 0 .. D-1 (with D = 64 the upper lanes
+  // hold zeros in the A operands, so they add nothing); the A1 panels number D / 32, an A2
+  // panel is [32 c][D] (A2P bytes), its transposed hi or lo panel [D rows][32 c] (S2P bytes)
+  constexpr int NP1 = D / 32, A2P = 32 * D * 4, S2P = D * 128, NQ = D / 64;
   extern __shared__ uint8_t ct_smem_raw[];
   uint8_t* sm = ct_smem_raw + ((1024u - (smem_u32(ct_smem_raw) & 1023u)) & 1023u);
   enum { R1F, R2F, R2E, S1F, S1E, S2F, S2E, SPD, G1D, XED, G2D, DONE, AD0, NBAR = AD0 + 8 };
@@ -1043,14 +837,14 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         if (!wait_bar(&bars[S1E], ph, abort_flag, false)) break;
         // the chunk's Add1 block, read by the X pass with plain loads, into L2
         bulk_prefetch_l2(p.add1 + (size_t)b * kCk * D, kCk * D * 4);
-        mbar_arrive_expect_tx(&bars[R1F], 32768);
-        for (int q = 0; q < 4; ++q)
+        mbar_arrive_expect_tx(&bars[R1F], NP1 * 8192);
+        for (int q = 0; q < NP1; ++q)
           tma_load_3d(sm + kCtS1 + q * 16384 + 8192, &mapA1, &bars[R1F], 32 * q, 0, b);
         issued1 = jj + 1;
         if (!wait_bar(&bars[R2E], ph, abort_flag, false)) break;
-        mbar_arrive_expect_tx(&bars[R2F], 32768);
+        mbar_arrive_expect_tx(&bars[R2F], 2 * A2P);
         for (int q = 0; q < 2; ++q)
-          tma_load_3d(sm + kCtRaw2 + q * 16384, &mapA2, &bars[R2F], 0, 32 * q, b);
+          tma_load_3d(sm + kCtRaw2 + q * A2P, &mapA2, &bars[R2F], 0, 32 * q, b);
         issued2 = jj + 1;
       }
       // copies still in flight land before shared memory is released
@@ -1060,9 +854,10 @@ __global__ void __launch_bounds__(kCtThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       const uint32_t id128 = idesc_tf32(128, 128), id64 = idesc_tf32(128, 64);
+      const uint32_t idD = idesc_tf32(128, D);
       const uint64_t d1 = smem_desc(smem_u32(sm + kCtS1), 16, 1024);
       const uint64_t d2h = smem_desc(smem_u32(sm + kCtS2), 16, 1024);
-      const uint64_t d2l = smem_desc(smem_u32(sm + kCtS2 + 32768), 16, 1024);
+      const uint64_t d2l = smem_desc(smem_u32(sm + kCtS2 + 2 * S2P), 16, 1024);
       for (int jj = 0; jj < nc; ++jj) {
         const uint32_t ph = jj & 1;
         if (!wait_bar(&bars[SPD], ph, abort_flag, false) ||
@@ -1071,7 +866,7 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         tc_fence_after();
         // X1^T = St_hi [A1_hi; A1_lo]^T + St_lo A1_hi^T: 4 panels of 16 KB (hi | lo)
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
+        for (int ks = 0; ks < D / 8; ++ks) {
           const uint64_t o = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);  // 16-byte units
           umma_tf32_ta(tmem + kTcX, tmem + kTcShi + 8 * ks, d1 + o, id128, ks != 0);
           umma_tf32_ta(tmem + kTcX, tmem + kTcSlo + 8 * ks, d1 + o, id64, 1u);
@@ -1085,10 +880,10 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         // St += Xs_hi A2T_hi^T + Xs_hi A2T_lo^T + Xs_lo A2T_hi^T: 2 panels of 16 KB each
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t o = (uint64_t)((ks >> 2) * 1024 + (ks & 3) * 2);
-          umma_tf32_ta(tmem + kTcSt, tmem + kTcXhi + 8 * ks, d2h + o, id128, 1u);
-          umma_tf32_ta(tmem + kTcSt, tmem + kTcXhi + 8 * ks, d2l + o, id128, 1u);
-          umma_tf32_ta(tmem + kTcSt, tmem + kTcXlo + 8 * ks, d2h + o, id128, 1u);
+          const uint64_t o = (uint64_t)((ks >> 2) * (S2P / 16) + (ks & 3) * 2);
+          umma_tf32_ta(tmem + kTcSt, tmem + kTcXhi + 8 * ks, d2h + o, idD, 1u);
+          umma_tf32_ta(tmem + kTcSt, tmem + kTcXhi + 8 * ks, d2l + o, idD, 1u);
+          umma_tf32_ta(tmem + kTcSt, tmem + kTcXlo + 8 * ks, d2h + o, idD, 1u);
         }
         mma_commit(&bars[G2D]);
         mma_commit(&bars[S2E]);
@@ -1103,7 +898,7 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       bool ok = wait_bar(&bars[R1F], ph, abort_flag, false);
       if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < NP1; ++q)
         mm_split<64, true, 128>(sm + kCtS1 + q * 16384 + 8192, sm + kCtS1 + q * 16384,
                                 sm + kCtS1 + q * 16384 + 8192, nullptr, nullptr, ts);
       fence_async_smem();
@@ -1114,8 +909,8 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll 1
       for (int q = 0; q < 2; ++q)
-        mm_split<128, false, 128>(sm + kCtRaw2 + q * 16384, sm + kCtS2 + q * 16384,
-                                  sm + kCtS2 + 32768 + q * 16384, nullptr, nullptr, ts);
+        mm_split<D, false, 128>(sm + kCtRaw2 + q * A2P, sm + kCtS2 + q * S2P,
+                                sm + kCtS2 + 2 * S2P + q * S2P, nullptr, nullptr, ts);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -1125,19 +920,21 @@ __global__ void __launch_bounds__(kCtThreads, 1)
     }
   } else {  // the state and X passes: row r of the state, column half hf
     const int pw = warp - 6, qd = warp & 3, hf = pw >> 2, r = 32 * qd + lane;
+    // a warp's rows are all state rows (r < D) or none (D = 64, lanes 64..127)
+    const bool rows = 32 * qd < D;
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
     uint8_t* const tiles = sm + kCtTile + pw * 8192;  // two [32][32] fp32 tiles, swizzled
     uint64_t* const abar = &bars[AD0 + pw];
-    // Add2 of a chunk into this warp's tiles: rows 32 qd.., columns 64 hf + 32 hq..
+    // Add2 of a chunk into this warp's tiles: rows 32 qd.., columns D/2 hf + 32 hq..
     int add2_loads = 0;  // issued by lane 0
     auto load_add2 = [&](int jj) {
       const int b = (int)entry(jj);
       ++add2_loads;
-      mbar_arrive_expect_tx(abar, 8192);
-      for (int hq = 0; hq < 2; ++hq)
-        tma_load_3d(tiles + hq * 4096, &mapAdd2, abar, 64 * hf + 32 * hq, 32 * qd, b);
+      mbar_arrive_expect_tx(abar, 4096 * NQ);
+      for (int hq = 0; hq < NQ; ++hq)
+        tma_load_3d(tiles + hq * 4096, &mapAdd2, abar, (D / 2) * hf + 32 * hq, 32 * qd, b);
     };
-    if (REV && lane == 0 && nc > 0) load_add2(0);
+    if (REV && rows && lane == 0 && nc > 0) load_add2(0);
     const float* G = p.gates;
     for (int jj = 0; jj < nc; ++jj) {
       const long long b = entry(jj);
@@ -1145,18 +942,32 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       const float gam = p.gam[b];
       // ---- state pass (the state after chunk jj - 1, or the initial state)
       {
-        uint64_t* b1 = REV ? abar : nullptr;
+        uint64_t* b1 = REV && rows ? abar : nullptr;
         bool fail;
-        if (jj > 0)
+        if (jj > 0) {
           fail = group_waits_fail(abort_flag, 2, 256, &bars[G2D], (jj - 1) & 1, false, b1, jj & 1);
-        else
-          fail = b1 ? group_waits_fail(abort_flag, 2, 256, b1, 0, false) : false;
+        } else if (REV) {  // every pass warp takes part in the vote
+          const bool ok = !b1 || wait_bar(b1, 0, abort_flag, false);
+          fail = named_sync_or(2, 256, !ok || *abort_flag != 0);
+        } else {
+          fail = false;
+        }
         if (fail) break;
         tc_fence_after();
       }
+      if (!rows) {  // lanes beyond the state: zero A operands, nothing else
+        uint32_t z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0u;
+#pragma unroll
+        for (int hq = 0; hq < NQ; ++hq) {
+          tmem_st32(tl + kTcShi + (D / 2) * hf + 32 * hq, z);
+          tmem_st32(tl + kTcSlo + (D / 2) * hf + 32 * hq, z);
+        }
+      }
 #pragma unroll 1
-      for (int hq = 0; hq < 2; ++hq) {
-        const int c0 = 64 * hf + 32 * hq;  // 32 state columns
+      for (int hq = 0; hq < (rows ? NQ : 0); ++hq) {
+        const int c0 = (D / 2) * hf + 32 * hq;  // 32 state columns
         uint8_t* const tile = tiles + hq * 4096;
         const uint32_t trow = smem_u32(tile) + lane * 128;  // this thread's row of the tile
         float v[32];
@@ -1211,18 +1022,23 @@ __global__ void __launch_bounds__(kCtThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[SPD]);
       // the tiles take the next chunk's Add2 once the stores have read them
-      if (lane == 0) {
+      if (lane == 0 && rows) {
         bulk_wait_read_all();
         if (REV && jj + 1 < nc) load_add2(jj + 1);
       }
       __syncwarp();
       // ---- X pass; Add1(c, r) for the 32 c of this half is loaded while the product runs
       float add1[32];
+      if (rows) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) add1[e] = p.add1[(size_t)b * kCk * D + (size_t)(32 * hf + e) * D + r];
+        for (int e = 0; e < 32; ++e)
+          add1[e] = p.add1[(size_t)b * kCk * D + (size_t)(32 * hf + e) * D + r];
+      }
       if (group_wait_fails(&bars[G1D], jj & 1, abort_flag, false, 2, 256)) break;
       tc_fence_after();
-      {
+      // lanes beyond the state: their product rows are zero, and so stay the hi and lo
+      // parts written over them
+      if (rows) {
         const int c0 = 32 * hf;  // 32 chunk positions c
         uint32_t u[32], u2[32];
         tmem_ld32(tl + kTcX + c0, u);
@@ -1253,10 +1069,10 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         ok = !group_wait_fails(&bars[G2D], (nc - 1) & 1, abort_flag, false, 2, 256);
         tc_fence_after();
       }
-      if (ok) {
+      if (ok && rows) {
 #pragma unroll 1
-        for (int hq = 0; hq < 2; ++hq) {
-          const int c0 = 64 * hf + 32 * hq;
+        for (int hq = 0; hq < NQ; ++hq) {
+          const int c0 = (D / 2) * hf + 32 * hq;
           float* f = p.fin + sidx + (size_t)r * D + c0;
           if (nc > 0) {
             uint32_t u[32];
@@ -1658,26 +1474,20 @@ struct SideJoin {
   }
 };
 
-// One chain: the tcgen05 kernel for D = 128 (one CTA per (sequence, head)), the
-// CUDA-core-fed one for D = 64 (D / kRows CTAs per (sequence, head)).
+// One chain on the tcgen05 kernel: one CTA per (sequence, head).
 template <int D, bool REV>
 cudaError_t launch_chain(const ChainArgs& c, long long nb, int N, int H, int* status,
                          cudaStream_t s) {
   const unsigned units = (unsigned)((long long)N * H);
-  if (D == 128) {
-    CUtensorMap m1, m2, mst, madd2;
-    if (!mm_map(&m1, c.a1, nb, (long long)kCk * D, kCk, D, D, 1) ||
-        !tile_map_plain(&m2, c.a2, nb, kCk, D) ||
-        !state_tile_map(&mst, c.st, nb, D))
-      return cudaErrorInvalidValue;
-    // Add2 is read only by the reverse chain; the forward one gets a copy of the st map
-    madd2 = mst;
-    if (REV && !state_tile_map(&madd2, c.add2, nb, D)) return cudaErrorInvalidValue;
-    ChainTcArgs t{c, status};
-    ck_chain_tc_kernel<REV><<<units, kCtThreads, kCtSmem, s>>>(m1, m2, mst, madd2, t);
-  } else {
-    ck_chain_kernel<D, REV><<<dim3(units, D / kRows), 256, chain_smem_bytes<D>(), s>>>(c);
-  }
+  CUtensorMap m1, m2, mst, madd2;
+  if (!mm_map(&m1, c.a1, nb, (long long)kCk * D, kCk, D, D, 1) ||
+      !tile_map_plain(&m2, c.a2, nb, kCk, D) || !state_tile_map(&mst, c.st, nb, D))
+    return cudaErrorInvalidValue;
+  // Add2 is read only by the reverse chain; the forward one gets a copy of the st map
+  madd2 = mst;
+  if (REV && !state_tile_map(&madd2, c.add2, nb, D)) return cudaErrorInvalidValue;
+  ChainTcArgs t{c, status};
+  ck_chain_tc_kernel<REV, D><<<units, kCtThreads, kCtSmem, s>>>(m1, m2, mst, madd2, t);
   return cudaGetLastError();
 }
 
@@ -1738,15 +1548,9 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // The chain kernels' shared-memory caps are raised before the fork, so that this
   // per-device first-call step cannot fail while side-stream work is in flight.
-  constexpr int smem = chain_smem_bytes<D>();
   static std::atomic<unsigned long long> set_f{0}, set_r{0};
-  if (D == 128) {
-    if ((e = ensure_smem_cap(ck_chain_tc_kernel<false>, kCtSmem, set_f)) != cudaSuccess) return e;
-    if ((e = ensure_smem_cap(ck_chain_tc_kernel<true>, kCtSmem, set_r)) != cudaSuccess) return e;
-  } else {
-    if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, smem, set_f)) != cudaSuccess) return e;
-    if ((e = ensure_smem_cap(ck_chain_kernel<D, true>, smem, set_r)) != cudaSuccess) return e;
-  }
+  if ((e = ensure_smem_cap(ck_chain_tc_kernel<false, D>, kCtSmem, set_f)) != cudaSuccess) return e;
+  if ((e = ensure_smem_cap(ck_chain_tc_kernel<true, D>, kCtSmem, set_r)) != cudaSuccess) return e;
   // Fork: the side stream takes P^T dO and dO^T diag(e^g) Q (they need the solve's P and
   // the gathered tiles only) while this stream makes W~, U and the forward chain.
   std::lock_guard<std::mutex> lock(g_side_mu);
@@ -1949,13 +1753,7 @@ cudaError_t launch_fwd_ck_t(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e;
   static std::atomic<unsigned long long> set_mm{0}, set_c{0};
   if ((e = ensure_smem_cap(ck_mm_kernel, kMmSmem, set_mm)) != cudaSuccess) return e;
-  if (D == 128) {
-    if ((e = ensure_smem_cap(ck_chain_tc_kernel<false>, kCtSmem, set_c)) != cudaSuccess) return e;
-  } else {
-    if ((e = ensure_smem_cap(ck_chain_kernel<D, false>, chain_smem_bytes<D>(), set_c)) !=
-        cudaSuccess)
-      return e;
-  }
+  if ((e = ensure_smem_cap(ck_chain_tc_kernel<false, D>, kCtSmem, set_c)) != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
