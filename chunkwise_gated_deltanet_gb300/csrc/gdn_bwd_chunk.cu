@@ -1537,6 +1537,12 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   int* status = nullptr;
   if ((e = tc_status_address(&status)) != cudaSuccess) return e;
   const int mm_grid = (int)std::min<long long>(L.nb, std::max(sms, 1));
+  // The side stream's products run beside a chain, which holds one SM per (sequence,
+  // head) for its whole length: they take the SMs it leaves (a CTA of either kernel fills
+  // an SM's shared memory), so that none of their CTAs waits for the chain to end.
+  const long long units = (long long)a.N * a.H;
+  const int side_grid =
+      units < sms ? (int)std::min<long long>(L.nb, std::max<long long>(sms - units, 1)) : mm_grid;
   const long long CD = (long long)kCk * D, CC = (long long)kCk * kCk, DD = (long long)D * D;
   MmLauncher mm{L.nb, nlive, s, status, mm_grid};
   // KK^T = K K^T, QK^T = Q K^T
@@ -1551,8 +1557,18 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   static std::atomic<unsigned long long> set_f{0}, set_r{0};
   if ((e = ensure_smem_cap(ck_chain_tc_kernel<false, D>, kCtSmem, set_f)) != cudaSuccess) return e;
   if ((e = ensure_smem_cap(ck_chain_tc_kernel<true, D>, kCtSmem, set_r)) != cudaSuccess) return e;
+  {  // W~ = T diag(beta e^g) K,  U = T diag(beta) V
+    Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
+    m.t[0].ks = gates + G_BEG * kCk;
+    mm.run(m);
+    m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
+    m.t[0].ks = gates + G_BETA * kCk;
+    mm.run(m);
+  }
+  if (mm.err != cudaSuccess) return mm.err;
   // Fork: the side stream takes P^T dO and dO^T diag(e^g) Q (they need the solve's P and
-  // the gathered tiles only) while this stream makes W~, U and the forward chain.
+  // the gathered tiles only) on the SMs the forward chain leaves, while this stream runs
+  // the chain.
   std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* side = nullptr;
   if ((e = side_stream(side)) != cudaSuccess) return e;
@@ -1563,7 +1579,7 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   // ordered after all side-stream work: the caller may free the workspace as soon as
   // its own stream has passed this call.
   SideJoin join{side, s2, s};
-  MmLauncher mm2{L.nb, nlive, s2, status, mm_grid};
+  MmLauncher mm2{L.nb, nlive, s2, status, side_grid};
   {  // Y = P^T dO,  Z = dO^T diag(e^g) Q
     mm2.run(mm2.make(P, CC, 1, kCk, dOc, CD, D, 1, Y, CD, D, 1, kCk, D, kCk));
     Mm m = mm2.make(dOc, CD, 1, D, Qc, CD, D, 1, Z, DD, D, 1, D, D, kCk);
@@ -1572,15 +1588,6 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   }
   if (mm2.err != cudaSuccess) return mm2.err;
   if ((e = cudaEventRecord(side->yz, s2)) != cudaSuccess) return e;
-  {  // W~ = T diag(beta e^g) K,  U = T diag(beta) V
-    Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
-    m.t[0].ks = gates + G_BEG * kCk;
-    mm.run(m);
-    m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
-    m.t[0].ks = gates + G_BETA * kCk;
-    mm.run(m);
-  }
-  if (mm.err != cudaSuccess) return mm.err;
 
   ChainArgs cf;
   cf.cbase = cbase; cf.init = a.S0; cf.fin = nullptr; cf.st = S;
