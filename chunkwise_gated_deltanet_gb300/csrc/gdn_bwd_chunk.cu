@@ -82,12 +82,13 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v
 }
 
 // ---------------------------------------------------------------------------------
-// Chunk table: for every chunk its first token row and length, for every sequence
+// Chunk table: for every chunk of cl tokens (cl <= kCk; the batch entry of a shorter
+// chunk is zero-padded to kCk rows) its first token row and length, for every sequence
 // the index of its first chunk, and the count of live batch entries (chunks x H).
 // One CTA; sequences in tiles of 1024 with a block scan.  Entries past nc_max (only
 // reachable with offsets that overrun the token count) are dropped.
 __global__ void __launch_bounds__(1024)
-ck_table_kernel(const int32_t* __restrict__ cu, int N, int T, int H, long long nc_max,
+ck_table_kernel(const int32_t* __restrict__ cu, int N, int T, int H, int cl, long long nc_max,
                 long long* __restrict__ crow0, int* __restrict__ clen, int* __restrict__ cbase,
                 long long* __restrict__ nlive) {
   __shared__ int wsum[32];
@@ -112,7 +113,7 @@ ck_table_kernel(const int32_t* __restrict__ cu, int N, int T, int H, long long n
         len = T;
       }
     }
-    const int nc = len > 0 ? (len + kCk - 1) / kCk : 0;
+    const int nc = len > 0 ? (len + cl - 1) / cl : 0;
     int x = nc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -136,8 +137,8 @@ ck_table_kernel(const int32_t* __restrict__ cu, int N, int T, int H, long long n
     if (n < N) {
       cbase[n] = (int)(base < nc_max ? base : nc_max);
       for (int j = 0; j < nc && base + j < nc_max; ++j) {
-        crow0[base + j] = start + (long long)j * kCk;
-        clen[base + j] = min(kCk, len - j * kCk);
+        crow0[base + j] = start + (long long)j * cl;
+        clen[base + j] = min(cl, len - j * cl);
       }
     }
     __syncthreads();
@@ -1513,7 +1514,8 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
   float *dA = F(L.cc[DAB]), *X = F(L.cc[XB]);
   float *S = F(L.dd[SB]), *Z = F(L.dd[ZB]), *dSn = F(L.dd[DSN]);
 
-  ck_table_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.N, a.T, a.H, L.nc, crow0, clen, cbase, nlive);
+  ck_table_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.N, a.T, a.H, kCk, L.nc, crow0, clen, cbase,
+                                     nlive);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned nb = (unsigned)L.nb;
@@ -1671,8 +1673,10 @@ cudaError_t launch_ck_t(const BwdArgs& a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------
-// The chunk-form forward on the same kernels, for q/k/v in fp32 (or bf16 at dk = dv = 64),
-// dk = dv = 64 or 128, C = 64 (Nyysyyan, "Chunk Computation"; myhz0606 section 4.5): per
+// The chunk-form forward on the same kernels, for q/k/v in fp32 (or bf16 off the bf16
+// headline kernel's shape), dk = dv = 64 or 128, chunks of C = 16, 32 or 64 tokens (a
+// shorter chunk's entry is zero-padded to 64 rows, where beta = 0 and log alpha = 0 make
+// the padding add nothing) (Nyysyyan, "Chunk Computation"; myhz0606 section 4.5): per
 // (chunk, head) entry, A = strictly-lower(beta_i K K^T o D), T = (I + A)^{-1}, W~ =
 // T diag(beta e^g) K, U = T diag(beta) V, P = lower(Q K^T o D); the forward chain gives the
 // chunk-start states S_j, delta = U - W~ S_j^T and the final state; then
@@ -1687,9 +1691,9 @@ struct FwdLayout {
   size_t crow0, clen, cbase, nlive, gates, gam, s, cd[NFCD], cc[NFCC], total;
 };
 
-FwdLayout fwd_layout(long long rows, int H, int D, int N) {
+FwdLayout fwd_layout(long long rows, int H, int D, int N, int C) {
   FwdLayout L;
-  L.nc = rows / kCk + N;
+  L.nc = rows / C + N;  // bounds the chunk count of any split of rows tokens into N
   L.nb = L.nc * H;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o += al256(bytes); return at; };
@@ -1756,7 +1760,7 @@ cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t s) {
 template <int D, typename TIn>
 cudaError_t launch_fwd_ck_t(const FwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.B * a.T;
-  const FwdLayout L = fwd_layout(rows, a.H, D, a.N);
+  const FwdLayout L = fwd_layout(rows, a.H, D, a.N, a.C);
   cudaError_t e;
   static std::atomic<unsigned long long> set_mm{0}, set_c{0};
   if ((e = ensure_smem_cap(ck_mm_kernel, kMmSmem, set_mm)) != cudaSuccess) return e;
@@ -1783,8 +1787,8 @@ cudaError_t launch_fwd_ck_t(const FwdArgs& a, cudaStream_t s) {
   const long long CD = (long long)kCk * D, CC = (long long)kCk * kCk, DD = (long long)D * D;
   auto run = [&]() -> cudaError_t {
     cudaError_t e2;
-    ck_table_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.N, a.T, a.H, L.nc, crow0, clen, cbase,
-                                       nlive);
+    ck_table_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.N, a.T, a.H, a.C, L.nc, crow0, clen,
+                                       cbase, nlive);
     if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
     GatherArgs ga;
     ga.q = a.q; ga.k = a.k; ga.v = a.v; ga.dout = nullptr;
@@ -1848,7 +1852,7 @@ cudaError_t launch_bwd_chunked(const BwdArgs& a, cudaStream_t stream) {
 }
 
 bool fwd_chunked_supported(int dk, int dv, int C) {
-  return dk == dv && (dk == 64 || dk == 128) && C == kCk;
+  return dk == dv && (dk == 64 || dk == 128) && (C == 16 || C == 32 || C == kCk);
 }
 
 int fwd_chunked_launches() { return 10; }

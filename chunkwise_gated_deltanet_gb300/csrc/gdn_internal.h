@@ -45,7 +45,8 @@ struct FwdArgs {
 cudaError_t launch_rec(const FwdArgs& a, cudaStream_t stream);
 
 // The chunk form on the backward's tcgen05 kernels (three TF32 passes): dk = dv = 64 or
-// 128, C = 64, fp32 or bf16 q/k/v; scratch from a stream-ordered pool of the library's.
+// 128, C = 16, 32 or 64, fp32 or bf16 q/k/v; scratch from a stream-ordered pool of the
+// library's.
 bool fwd_chunked_supported(int dk, int dv, int C);
 int fwd_chunked_launches();
 cudaError_t launch_fwd_chunked(const FwdArgs& a, cudaStream_t stream);

@@ -49,13 +49,14 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 typedef enum {
   GDN_PATH_NONE = 0,      /* sizes not supported */
   GDN_PATH_SIMT = 1,      /* CUDA-core kernel, fp32 arithmetic, the per-token recurrence
-                             (exact; C is not used): head sizes 16 and 32, C = 16 or 32 */
+                             (exact; C is not used): head sizes 16 and 32, dk != dv */
   GDN_PATH_TCGEN05 = 2,   /* bf16 tcgen05 tensor-core kernel: dk = dv = 128, C = 64 */
   GDN_PATH_TF32 = 3       /* the chunk form on tcgen05 tensor cores in three TF32 passes
                              (fp32 accuracy), as a sequence of batched per-chunk kernels:
-                             dk = dv = 64 or 128, C = 64, fp32 q/k/v (or bf16 at 64);
-                             scratch from a stream-ordered memory pool the library keeps
-                             per device.  The linear mode takes the recurrence here. */
+                             dk = dv = 64 or 128, C = 16, 32 or 64, every shape and dtype
+                             the bf16 kernel does not take; scratch from a stream-ordered
+                             memory pool the library keeps per device.  The linear mode
+                             takes the recurrence here. */
 } gdn_path;
 
 /*

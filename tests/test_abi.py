@@ -56,7 +56,9 @@ def test_version(lib):
     (16, 16, 16, torch.float32, gdn.GDN_PATH_SIMT),
     (64, 64, 64, torch.float32, gdn.GDN_PATH_TF32),
     (64, 64, 64, torch.bfloat16, gdn.GDN_PATH_TF32),
-    (64, 64, 32, torch.float32, gdn.GDN_PATH_SIMT),
+    (64, 64, 32, torch.float32, gdn.GDN_PATH_TF32),
+    (128, 128, 16, torch.bfloat16, gdn.GDN_PATH_TF32),
+    (32, 32, 32, torch.float32, gdn.GDN_PATH_SIMT),
     (64, 128, 32, torch.bfloat16, gdn.GDN_PATH_SIMT),
     (48, 64, 64, torch.float32, gdn.GDN_PATH_NONE),
     (64, 64, 128, torch.float32, gdn.GDN_PATH_NONE),

@@ -1,6 +1,7 @@
 """The chunk form on the tensor cores for the shapes the bf16 headline kernel does not take
-(GDN_PATH_TF32: dk = dv = 64 or 128, C = 64, fp32 q/k/v, or bf16 at 64), against the fp64
-oracle element by element.  Its products and state chain run in three TF32 passes, so the
+(GDN_PATH_TF32: dk = dv = 64 or 128, C = 16, 32 or 64, fp32 q/k/v, or bf16 off the bf16
+kernel's shape), against the fp64 oracle element by element.  Its products and state
+chain run in three TF32 passes, so the
 fp32 bound (relative max error 1e-4) applies to every fp32 result, S_final of bf16 inputs
 included; a bf16 output is also held to one bf16 rounding unit per element."""
 import numpy as np
@@ -21,13 +22,13 @@ def _built():
     assert torch.cuda.is_available()
 
 
-def _wl(dtype, d, T, B=2, H=2, alpha_mu=2.0):
-    return workloads.Workload("tf32", dtype, B=B, H=H, T=T, dk=d, dv=d, C=64,
+def _wl(dtype, d, T, B=2, H=2, alpha_mu=2.0, C=64):
+    return workloads.Workload("tf32", dtype, B=B, H=H, T=T, dk=d, dv=d, C=C,
                               alpha_mu=alpha_mu, s0_std=0.1)
 
 
-def _check(inp):
-    o, s = run_gpu(inp, 64)
+def _check(inp, C=64):
+    o, s = run_gpu(inp, C)
     ro, rs = run_oracle(inp)
     if inp["dtype"] == "f32":
         assert_close(o, ro, True, "out")
@@ -39,11 +40,33 @@ def _check(inp):
     assert_close(s, rs, True, "S_final")
 
 
-@pytest.mark.parametrize("d,dtype", [(64, "f32"), (128, "f32"), (64, "bf16")])
-def test_path_is_the_chunk_form(d, dtype):
+@pytest.mark.parametrize("d,dtype,C", [(64, "f32", 64), (128, "f32", 64), (64, "bf16", 64),
+                                       (64, "f32", 16), (128, "bf16", 32)])
+def test_path_is_the_chunk_form(d, dtype, C):
     dt = torch.float32 if dtype == "f32" else torch.bfloat16
-    assert gdn.gdn_select_path(d, d, 64, dt) == gdn.GDN_PATH_TF32
-    assert gdn.gdn_launches_per_call(d, d, 64, dt) == 10
+    assert gdn.gdn_select_path(d, d, C, dt) == gdn.GDN_PATH_TF32
+    assert gdn.gdn_launches_per_call(d, d, C, dt) == 10
+
+
+@pytest.mark.parametrize("C", [16, 32])
+@pytest.mark.parametrize("d,dtype", [(64, "f32"), (128, "f32"), (128, "bf16")])
+def test_shorter_chunks(d, dtype, C):
+    """Chunks of 16 or 32 tokens: each padded to a 64-row entry, which must add nothing;
+    lengths that leave a ragged last chunk."""
+    _check(workloads.make_inputs(_wl(dtype, d, 150, C=C), seed=16), C)
+
+
+def test_shorter_chunks_packed_and_reset():
+    lens = [0, 17, 33, 100, 1]
+    inp = workloads.make_inputs(_wl("f32", 128, sum(lens), B=1, C=16), seed=17)
+    inp["cu_seqlens"] = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    inp["N"] = len(lens)
+    g = torch.Generator().manual_seed(18)
+    inp["S0"] = torch.randn(len(lens), 2, 128, 128, generator=g) * 0.1
+    la = inp["log_alpha"].clone()
+    la[:, 40] = -float("inf")
+    inp["log_alpha"] = la
+    _check(inp, 16)
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
