@@ -686,20 +686,37 @@ __global__ void __launch_bounds__(128) ck_tsolve_kernel(TsolveArgs p) {
     }
   }
   __syncthreads();
-  // Block rows below, in order: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj  (j < i).
+  // Block rows below, in order: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj  (j < i).  Thread
+  // tid takes elements e = tid + 128 i of the block row (block j = i / 2, row r, column c);
+  // with the block row unrolled every trip count is a constant, so the thread's dot
+  // products are independent chains the compiler interleaves.
+  const int r0 = tid >> 4, c = tid & 15;
+#pragma unroll
   for (int bi = 1; bi < kCk / 16; ++bi) {
-    for (int e = tid; e < bi * 256; e += 128) {
-      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      float acc = 0.f;
-      for (int k = 16 * j; k < 16 * bi; ++k) acc = fmaf(As[16 * bi + r][k], Ts[k][16 * j + c], acc);
-      Wb[e] = acc;
+    float acc[6];
+#pragma unroll
+    for (int i = 0; i < 2 * bi; ++i) {
+      const int j = i >> 1, r = r0 + 8 * (i & 1);
+      float x = 0.f;
+#pragma unroll
+      for (int k = 16 * j; k < 16 * bi; ++k) x = fmaf(As[16 * bi + r][k], Ts[k][16 * j + c], x);
+      acc[i] = x;
     }
+#pragma unroll
+    for (int i = 0; i < 2 * bi; ++i) Wb[tid + 128 * i] = acc[i];
     __syncthreads();
-    for (int e = tid; e < bi * 256; e += 128) {
-      const int j = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      float acc = 0.f;
-      for (int m = 0; m <= r; ++m) acc = fmaf(Ts[16 * bi + r][16 * bi + m], Wb[(j << 8) + (m << 4) + c], acc);
-      Ts[16 * bi + r][16 * j + c] = -acc;
+#pragma unroll
+    for (int i = 0; i < 2 * bi; ++i) {
+      const int j = i >> 1, r = r0 + 8 * (i & 1);
+      float x = 0.f;
+      for (int m = 0; m <= r; ++m)
+        x = fmaf(Ts[16 * bi + r][16 * bi + m], Wb[(j << 8) + (m << 4) + c], x);
+      acc[i] = x;
+    }
+#pragma unroll
+    for (int i = 0; i < 2 * bi; ++i) {
+      const int j = i >> 1, r = r0 + 8 * (i & 1);
+      Ts[16 * bi + r][16 * j + c] = -acc[i];
     }
     __syncthreads();
   }
