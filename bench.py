@@ -754,6 +754,9 @@ def main():
     achieved_tf = alg["flops"] / sec / 1e12
     path = gdn.gdn_select_path(dk, dv, C, d["v"].dtype)
     launches = gdn.gdn_launches_per_call(dk, dv, C, d["v"].dtype)
+    if w.linear and inp["cu_seqlens"] is None and \
+            gdn.gdn_linear_split_segments(B, H, T, dk, dv, C, d["v"].dtype) > 1:
+        launches = 2  # the segments, then the fold and correction
 
     # ---- end to end through the public call with pinned host buffers ----
     host_in = {k: (inp[k].pin_memory() if inp[k] is not None else None)

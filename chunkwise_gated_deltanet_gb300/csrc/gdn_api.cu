@@ -40,6 +40,12 @@ int gdn_select_path(int dk, int dv, int C, int qkv_dtype) {
   return GDN_PATH_SIMT;
 }
 
+int gdn_linear_split_segments(int N, int H, int T, int dk, int dv, int C, int qkv_dtype) {
+  if (N <= 0 || H <= 0 || T < 0) return 0;
+  if (gdn_select_path(dk, dv, C, qkv_dtype) != GDN_PATH_TCGEN05) return 1;
+  return gdn::linear_split_segments(N, H, T);
+}
+
 int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype) {
   gdn::FwdArgs a{};
   a.dk = dk; a.dv = dv; a.C = C; a.bf16 = qkv_dtype == GDN_BF16;

@@ -1868,6 +1868,10 @@ cudaError_t launch_bwd_chunked(const BwdArgs& a, cudaStream_t stream) {
   return a.bf16 ? launch_ck_t<128, __nv_bfloat16>(a, stream) : launch_ck_t<128, float>(a, stream);
 }
 
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+  return pool_alloc(ptr, bytes, stream);
+}
+
 bool fwd_chunked_supported(int dk, int dv, int C) {
   return dk == dv && (dk == 64 || dk == 128) && (C == 16 || C == 32 || C == kCk);
 }

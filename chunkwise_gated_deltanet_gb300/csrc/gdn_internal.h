@@ -12,15 +12,21 @@ namespace gdn {
 // Raise a kernel's dynamic shared-memory cap to `bytes`, once per device.  The
 // attribute belongs to the function in the current context; it is not set per
 // launch, because changing a kernel's attributes while launches of it are in
-// flight on other streams can serialise them.  `done` holds one bit per device.
+// flight on other streams can serialise them.  `done` holds one bit per device.  With
+// `max_carveout` the kernel also asks for the largest shared-memory carveout, so that
+// as many CTAs as its shared memory allows fit an SM.
 template <typename Kernel>
-cudaError_t ensure_smem_cap(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+cudaError_t ensure_smem_cap(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done,
+                            bool max_carveout = false) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && max_carveout)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
   return e;
 }
@@ -55,6 +61,10 @@ cudaError_t launch_fwd_chunked(const FwdArgs& a, cudaStream_t stream);
 bool tc_supported(int dk, int dv, int C, int bf16);
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream);
 int tc_launches(const FwdArgs& a);
+// Segments per sequence the linear mode's split runs with for these sizes (1: no split).
+int linear_split_segments(long long N, int H, int T);
+// Stream-ordered scratch from the library's per-device memory pool (cudaFreeAsync frees).
+cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream);
 // Single-token decode step (recurrent form), already validated by the API layer.
 struct DecodeArgs {
   const void* q;

@@ -77,6 +77,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -703,7 +704,7 @@ __device__ __forceinline__ void run_state(uint8_t* sm, uint32_t tmem, const CUte
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (S0) t4 = *reinterpret_cast<const float4*>(S0 + u.sidx + (size_t)row * kD + 32 * p + 4 * q);
+          if (S0) t4 = *reinterpret_cast<const float4*>(S0 + u.s0idx + (size_t)row * kD + 32 * p + 4 * q);
           v[4 * q] = t4.x; v[4 * q + 1] = t4.y; v[4 * q + 2] = t4.z; v[4 * q + 3] = t4.w;
         }
         if (u.nc == 0) {
@@ -1076,19 +1077,60 @@ gdn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   cluster_sync();  // neither CTA leaves while the other may still touch its memory
 }
 
+// ---------------------------------------------------------------------------------
+// The linear mode over more SMs.  In the linear mode a segment of tokens maps the state
+// affinely with a scalar gain: S_end = Gamma S_start + L, Gamma = e^{sum of log alpha}
+// over the segment ([N] "Mamba2": the state is a decayed sum of the writes).  When the
+// (sequence, head) units fill at most half of the SMs, every sequence of a fixed-length
+// batch is cut into R chunk-aligned, non-empty segments that run as units of their own:
+//   1. the linear kernel on the N R segments, the first of each sequence from S0, the
+//      others from zero: outputs o(0) and end states L_r;
+//   2. the correction of segments r >= 1, o_t += e^{G_t} S_start q_t (G_t the sum of log
+//      alpha from the segment's first token through t: what the start state adds to the
+//      output, which is linear in it), each CTA folding the start state it needs,
+//      S_start_1 = L_0 and S_start_r = Gamma_{r-1} S_start_{r-1} + L_{r-1}, and one CTA
+//      per (sequence, head) writing S_final = Gamma_{R-1} S_start_{R-1} + L_{R-1}.
+constexpr int kLsMaxSeg = 4;
+
+// Token bounds [a, b) of segment r of a length-T sequence: whole chunks, as even as the
+// chunk count allows (R from linear_split_segments leaves none empty).
+__host__ __device__ __forceinline__ void seg_bounds(int T, int R, int r, int& a, int& b) {
+  const int nch = (T + kC - 1) / kC, per = (nch + R - 1) / R;
+  a = min(r * per * kC, T);
+  b = min((r + 1) * per * kC, T);
+}
+__host__ __device__ __forceinline__ int seg_tiles(int T, int R, int r) {
+  int a, b;
+  seg_bounds(T, R, r, a, b);
+  return a < b ? (b - a + 63) / 64 : 0;
+}
+
 // Linear mode (no erase, write strength 1): the WY factors are T = I, W~ = 0, U = V, so
 // the state CTA runs alone, one CTA per (sequence, head): its chain is the state update
-// and the S epilogue, with delta and delta~ made from the V tile by aux P.
+// and the S epilogue, with delta and delta~ made from the V tile by aux P.  With R > 1
+// (fixed-length batch, no cu_seqlens) CTA (n R + r) H + h runs segment r of sequence n,
+// from S0[n][h] when r = 0 and from zero otherwise, and writes its end state to
+// S_final[(n R + r) H + h].
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_tc_linear_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ log_alpha,
                      const float* __restrict__ S0, __nv_bfloat16* __restrict__ out,
                      float* __restrict__ S_final, const int32_t* __restrict__ cu_seqlens, int H,
-                     int T) {
+                     int T, int R) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const Unit u = make_unit(blockIdx.x, cu_seqlens, H, T);
+  Unit u = make_unit(blockIdx.x, cu_seqlens, H, T);
+  if (R > 1) {
+    const int nr = blockIdx.x / H, n = nr / R, r = nr % R;
+    int a, b;
+    seg_bounds(T, R, r, a, b);
+    u.row0 = (long long)n * T + a;
+    u.len = b - a;
+    u.nc = (int)((u.len + kC - 1) / kC);
+    u.s0idx = ((size_t)n * H + u.h) * kD * kD;
+    if (r > 0) S0 = nullptr;
+  }
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + ST_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + ST_MISC + 4);
   if (warp == 0) tmem_alloc(tslot, TM_COLS);
@@ -1120,6 +1162,337 @@ gdn_tc_linear_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   }
 }
 
+
+// The correction's epilogue warps (0-3) synchronise among themselves on named barrier 1.
+constexpr uint32_t kLsEpiBar = 1;
+// Sum over the 128 epilogue threads (all of them call it).
+__device__ __forceinline__ float ls_block_sum(float x, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  named_sync(kLsEpiBar, 128);  // red free from its last use
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  named_sync(kLsEpiBar, 128);
+  return (red[0] + red[1]) + (red[2] + red[3]);
+}
+// Sum of log alpha over tokens [t0, t1) of sequence n, head h (0 without a gate): the 128
+// epilogue threads, sixteen strided loads each in flight per round of 2048 tokens.
+__device__ __forceinline__ float ls_la_sum(const float* __restrict__ log_alpha, int n, int T,
+                                           int H, int h, int t0, int t1, float* red) {
+  float s = 0.f;
+  if (log_alpha) {
+    const float* la = log_alpha + (size_t)n * T * H + h;
+    for (int base = t0; base < t1; base += 2048) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int t = base + (int)threadIdx.x + 128 * e;
+        v[e] = t < t1 ? la[(size_t)t * H] : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] += v[e + 8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] += v[e + 4];
+      s += (v[0] + v[1]) + (v[2] + v[3]);
+    }
+  }
+  return ls_block_sum(s, red);
+}
+
+// The correction, persistent: the (sequence, head, segment r >= 1, 64-token tile) list
+// in that order, an even contiguous share per CTA, so a CTA meets at most a few segments.
+// Warp 4 (one thread) loads q and out tiles by TMA into a three-stage ring, issues
+// D^T (dv x 64 tokens) = S_hi Q^T + S_lo Q^T into one of two TMEM accumulators a tile
+// ahead of the epilogue, and stores each corrected out tile back by TMA.  Warps 0-3, a
+// thread per state row / output column d: on reaching a segment they fold its start
+// state from the segments' end states L (fp32) into tensor memory as bf16 hi and lo
+// pairs (the A operand); per tile they scan the gates and add e^{G_t} times their TMEM
+// lane into the out tile in shared memory.  Two CTAs fit an SM.
+constexpr int kLsStages = 3, kLsStageBytes = 32768;  // per stage: q 16 KB, out 16 KB
+constexpr int kLsSmem = kLsStages * kLsStageBytes + 1024;
+constexpr int kLsThreads = 160;
+constexpr uint32_t kLsTmHi = 0, kLsTmLo = 64, kLsTmAcc = 128;  // TMEM columns
+
+__global__ void __launch_bounds__(kLsThreads, 2)
+ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+               int N, int H, int T, int R, const float* __restrict__ log_alpha,
+               const float* __restrict__ L, float* __restrict__ S_final) {
+  extern __shared__ uint8_t ls_smem_raw[];
+  uint8_t* sm = ls_smem_raw + ((1024u - (smem_u32(ls_smem_raw) & 1023u)) & 1023u);
+  // full[s], out_ready[s] (the epilogue has written stage s's out tile), acc_full[a],
+  // acc_empty[a], s_ready (a segment's start state is in TMEM)
+  __shared__ __align__(8) uint64_t bars[2 * kLsStages + 5];
+  uint64_t* full = bars;
+  uint64_t* out_ready = bars + kLsStages;
+  uint64_t* acc_full = bars + 2 * kLsStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* s_ready = acc_full + 4;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_s;
+  __shared__ __align__(16) float sc[64], eg[64], red[4];
+  volatile int* abort_flag = &abort_s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int tpu = 0;  // tiles per (sequence, head)
+  for (int r = 1; r < R; ++r) tpu += seg_tiles(T, R, r);
+  const long long tot = (long long)N * H * tpu;
+  const long long i0 = tot * blockIdx.x / gridDim.x, i1 = tot * (blockIdx.x + 1) / gridDim.x;
+  if (i0 >= i1) return;
+  const int n_t = (int)(i1 - i0);
+  // tile i of the list: (sequence, head) unit, segment r, tile k of the segment
+  auto decode = [&](long long i, int& unit, int& r, int& k) {
+    unit = (int)(i / tpu);
+    k = (int)(i % tpu);
+    r = 1;
+    while (r + 1 < R && k >= seg_tiles(T, R, r)) k -= seg_tiles(T, R, r++);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kLsStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&out_ready[s], 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(s_ready, 4);
+    abort_s = 0;
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_o);
+    fence_mbarrier_init();
+  }
+  if (warp == 0) tmem_alloc(&tslot, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+
+  if (warp == 4) {
+    if (lane == 0) {  // loads, products and stores
+      auto load = [&](int it) {
+        int unit, r, k, a, b;
+        decode(i0 + it, unit, r, k);
+        seg_bounds(T, R, r, a, b);
+        const int s = it % kLsStages, h = unit % H, row = (unit / H) * T + a + 64 * k;
+        uint8_t* qb = sm + s * kLsStageBytes;
+        mbar_arrive_expect_tx(&full[s], 32768);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(qb + c * 8192, &tm_q, &full[s], 64 * c, h, row);
+          tma_load_3d(qb + 16384 + c * 8192, &tm_o, &full[s], 64 * c, h, row);
+        }
+      };
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+      long long seg = -1;
+      int nseg = 0;
+      auto product = [&](int it) {  // false: a wait gave up
+        int unit, r, k;
+        decode(i0 + it, unit, r, k);
+        const int s = it % kLsStages, a = it & 1;
+        if ((long long)unit * R + r != seg) {  // its start state is in TMEM once s_ready flips
+          seg = (long long)unit * R + r;
+          if (!wait_bar(s_ready, nseg++ & 1, abort_flag, false)) return false;
+        }
+        if (!wait_bar(&full[s], (it / kLsStages) & 1, abort_flag, false)) return false;
+        if (it >= 2 && !wait_bar(&acc_empty[a], ((it >> 1) - 1) & 1, abort_flag, false))
+          return false;
+        tc_fence_after();
+        const uint8_t* qb = sm + s * kLsStageBytes;
+        const uint32_t d = tmem + kLsTmAcc + 64u * a;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t dq = desc_k(qb, ks, 8192);
+          mma_bf16_ta(d, tmem + kLsTmHi + 8 * ks, dq, id, ks != 0);
+          mma_bf16_ta(d, tmem + kLsTmLo + 8 * ks, dq, id, 1u);
+        }
+        mma_commit(&acc_full[a]);
+        return true;
+      };
+      for (int it = 0; it < min(kLsStages, n_t); ++it) load(it);
+      bool ok = product(0);
+      for (int it = 0; ok && it < n_t; ++it) {
+        if (it + 1 < n_t && !(ok = product(it + 1))) break;  // one tile ahead
+        // tile it back to HBM once the epilogue has written it
+        const int s = it % kLsStages;
+        if (!(ok = wait_bar(&out_ready[s], (it / kLsStages) & 1, abort_flag, false))) break;
+        int unit, r, k, a, b;
+        decode(i0 + it, unit, r, k);
+        seg_bounds(T, R, r, a, b);
+        // the store writes the tile's 64 rows: past a sequence's end the rows loaded from
+        // the next sequence's first segment, which nothing else writes meanwhile, go back
+        // unchanged
+        const uint8_t* ob = sm + s * kLsStageBytes + 16384;
+        for (int c = 0; c < 2; ++c)
+          tma_store_3d(&tm_o, ob + c * 8192, 64 * c, unit % H, (unit / H) * T + a + 64 * k);
+        bulk_commit();
+        // the stage of tile it - 1 takes tile it + 2 once that tile's store has read it
+        if (it >= 1 && it + 2 < n_t) {
+          bulk_wait_read_1();
+          load(it + 2);
+        }
+      }
+      bulk_wait_all();
+    }
+  } else {  // warps 0-3
+    const uint32_t tl_row = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
+    long long seg = -1;  // the segment whose start state is in TMEM
+    float pcur = 0.f;    // sum of log alpha from the segment's first token to the tile's
+    // warps 0-1: log alpha of token 32 warp + lane of a tile, loaded a tile ahead
+    auto gate_of = [&](int it) {
+      int unit, r, k, a, b;
+      decode(i0 + it, unit, r, k);
+      seg_bounds(T, R, r, a, b);
+      const int t = 32 * warp + lane, t0 = a + 64 * k;
+      return (log_alpha && t0 + t < b)
+                 ? log_alpha[((size_t)(unit / H) * T + t0 + t) * H + unit % H]
+                 : 0.f;
+    };
+    float la_next = warp < 2 ? gate_of(0) : 0.f;
+    // this thread's output column d = tid in the out tile: panel, 16-byte chunk, byte
+    const uint32_t col_off = (uint32_t)((tid >> 6) * 8192 + (tid & 7) * 2);
+    const int col_chunk = (tid & 63) >> 3;
+    for (int it = 0; it < n_t; ++it) {
+      const int s = it % kLsStages, a_ = it & 1;
+      int unit, r, k, a, b;
+      decode(i0 + it, unit, r, k);
+      seg_bounds(T, R, r, a, b);
+      const int n = unit / H, h = unit % H, t0 = a + 64 * k, len = min(64, b - t0);
+      if ((long long)unit * R + r != seg) {  // the same for all four warps
+        // the previous segment's products are complete: its last tile's were waited for
+        seg = (long long)unit * R + r;
+        const size_t DD = (size_t)kD * kD, row = (size_t)tid * kD;
+        const float* Lu = L + ((size_t)n * R * H + h) * DD + row;  // L_j row: Lu + j H DD
+        float4 x[16];  // L_0 row, columns 0 .. 63: in flight while the gate sums run
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = ld4(Lu + 4 * e);
+        // the CTA holding the last segment's first tile writes the sequence's end state;
+        // a CTA that starts at its segment's first tile has no prefix to sum
+        const bool fin = S_final != nullptr && r == R - 1 && k == 0;
+        pcur = k > 0 ? ls_la_sum(log_alpha, n, T, H, h, a, t0, red) : 0.f;
+        const float gfin = fin ? expf(ls_la_sum(log_alpha, n, T, H, h, a, b, red)) : 0.f;
+        float gam[kLsMaxSeg - 1] = {1.f, 1.f, 1.f};  // Gamma_j of segments 1 .. r - 1
+        for (int j = 1; j < r; ++j) {
+          int ja, jb;
+          seg_bounds(T, R, j, ja, jb);
+          const float g = expf(ls_la_sum(log_alpha, n, T, H, h, ja, jb, red));
+          gam[0] = j == 1 ? g : gam[0];
+          gam[1] = j == 2 ? g : gam[1];
+          gam[2] = j == 3 ? g : gam[2];
+        }
+#pragma unroll 1
+        for (int hv = 0; hv < 2; ++hv) {  // columns 64 hv .. 64 hv + 63
+          if (hv == 1)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = ld4(Lu + 64 + 4 * e);
+#pragma unroll 1
+          for (int j = 1; j < r; ++j) {  // S_start_{j+1} = Gamma_j S_start_j + L_j
+            const float gj = j == 1 ? gam[0] : (j == 2 ? gam[1] : gam[2]);
+            const float* Lj = Lu + (size_t)j * H * DD + 64 * hv;
+            float4 y[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) y[e] = ld4(Lj + 4 * e);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              x[e].x = fmaf(gj, x[e].x, y[e].x);
+              x[e].y = fmaf(gj, x[e].y, y[e].y);
+              x[e].z = fmaf(gj, x[e].z, y[e].z);
+              x[e].w = fmaf(gj, x[e].w, y[e].w);
+            }
+          }
+          if (fin) {
+            const float* Lr = Lu + (size_t)r * H * DD + 64 * hv;
+            float* Sf = S_final + ((size_t)n * H + h) * DD + row + 64 * hv;
+            float4 y[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) y[e] = ld4(Lr + 4 * e);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              st4(Sf + 4 * e, fmaf(gfin, x[e].x, y[e].x), fmaf(gfin, x[e].y, y[e].y),
+                  fmaf(gfin, x[e].z, y[e].z), fmaf(gfin, x[e].w, y[e].w));
+          }
+          uint32_t hi[32], lo[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            split2(x[e].x, x[e].y, hi[2 * e], lo[2 * e]);
+            split2(x[e].z, x[e].w, hi[2 * e + 1], lo[2 * e + 1]);
+          }
+          tmem_st32(tl_row + kLsTmHi + 32 * hv, hi);
+          tmem_st32(tl_row + kLsTmLo + 32 * hv, lo);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_ready);
+      }
+      if (warp < 2) {  // inclusive scan of the tile's 64 log alpha, 32 per warp
+        const int t = 32 * warp + lane;
+        float x = la_next;
+        if (it + 1 < n_t) la_next = gate_of(it + 1);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        sc[t] = x;
+      }
+      named_sync(kLsEpiBar, 128);
+      if (tid < 64) eg[tid] = expf(pcur + sc[tid] + (tid >= 32 ? sc[31] : 0.f));
+      pcur += sc[31] + sc[63];
+      // the out tile has landed and the product is done
+      if (group_waits_fail(abort_flag, kLsEpiBar, 128, &full[s], (it / kLsStages) & 1, false,
+                           &acc_full[a_], (it >> 1) & 1))
+        break;
+      tc_fence_after();
+      uint8_t* ob = sm + s * kLsStageBytes + 16384 + col_off;
+      const uint32_t tl = tl_row + kLsTmAcc + 64u * a_;
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {  // tokens 32 cb .. 32 cb + 31 of column d
+        uint32_t u[32];
+        tmem_ld32(tl + 32 * cb, u);
+        // all 32 out values and gate factors first, so that the loads overlap
+        unsigned short ov[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          ov[j] = *reinterpret_cast<const unsigned short*>(
+              ob + (32 * cb + j) * 128 + ((col_chunk ^ (j & 7)) << 4));
+        float e[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(eg + 32 * cb + 4 * q);
+          e[4 * q] = v.x;
+          e[4 * q + 1] = v.y;
+          e[4 * q + 2] = v.z;
+          e[4 * q + 3] = v.w;
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (32 * cb + j < len) {
+            const float o = __uint_as_float((uint32_t)ov[j] << 16) + e[j] * __uint_as_float(u[j]);
+            *reinterpret_cast<__nv_bfloat16*>(ob + (32 * cb + j) * 128 +
+                                              ((col_chunk ^ (j & 7)) << 4)) = __float2bfloat16_rn(o);
+          }
+      }
+      tc_fence_before();
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&acc_empty[a_]);
+        mbar_arrive(&out_ready[s]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {  // let copies and products still in flight land before TMEM goes
+    const uint64_t tw = globaltimer_ns();
+    while (globaltimer_ns() - tw < 50000ull) {
+    }
+    if (tid == 0) atomicOr(&g_tc_status, *abort_flag);
+  }
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 }  // namespace
 
 bool tc_supported(int dk, int dv, int C, int bf16) {
@@ -1127,6 +1500,22 @@ bool tc_supported(int dk, int dv, int C, int bf16) {
 }
 
 int tc_launches(const FwdArgs&) { return 1; }
+
+// Segments per sequence of the linear mode's split (1: no split): as many as the SMs
+// hold beside the N H units (at most kLsMaxSeg), each with at least two chunks.
+int linear_split_segments(long long N, int H, int T) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 1;
+  const long long units = N * H;
+  if (units <= 0 || 2 * units > sms) return 1;
+  int R = (int)std::min<long long>(kLsMaxSeg, sms / units);
+  const int nch = (T + kC - 1) / kC;
+  while (R > 1 && nch < 2 * R) --R;
+  if (R > 1) R = (nch + (nch + R - 1) / R - 1) / ((nch + R - 1) / R);  // none left empty
+  return R;
+}
 
 cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
   const long long rows = (long long)a.B * a.T;
@@ -1139,12 +1528,45 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
   if (a.beta == nullptr) {  // linear mode: the state CTA alone, one per unit
     const long long units = (long long)a.N * a.H;
     if (units > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    static std::atomic<unsigned long long> smem_lin{0};
-    const cudaError_t e = ensure_smem_cap(gdn_tc_linear_kernel, SMEM_BYTES, smem_lin);
+    static std::atomic<unsigned long long> smem_lin{0}, smem_corr{0};
+    cudaError_t e = ensure_smem_cap(gdn_tc_linear_kernel, SMEM_BYTES, smem_lin);
     if (e != cudaSuccess) return e;
-    gdn_tc_linear_kernel<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(
-        mq, mk, mv, a.log_alpha, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.cu_seqlens, a.H, a.T);
-    return cudaGetLastError();
+    const int R = a.cu_seqlens ? 1 : linear_split_segments(a.N, a.H, a.T);
+    if (R <= 1) {
+      gdn_tc_linear_kernel<<<(unsigned)units, kThreads, SMEM_BYTES, stream>>>(
+          mq, mk, mv, a.log_alpha, a.S0, (__nv_bfloat16*)a.out, a.S_final, a.cu_seqlens, a.H,
+          a.T, 1);
+      return cudaGetLastError();
+    }
+    // R whole-chunk segments per sequence on more SMs, then the correction (which folds
+    // the start states and writes S_final); the segments' end states L in pool scratch
+    if ((e = ensure_smem_cap(ls_corr_kernel, kLsSmem, smem_corr, true)) != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    void* Lv = nullptr;
+    if ((e = scratch_alloc(&Lv, (size_t)units * R * kD * kD * sizeof(float), stream)) != cudaSuccess)
+      return e;
+    float* L = static_cast<float*>(Lv);
+    long long tiles = 0;
+    for (int r = 1; r < R; ++r) tiles += seg_tiles(a.T, R, r);
+    tiles *= units;
+    const unsigned grid = (unsigned)std::min<long long>(tiles, 2LL * sms);  // two CTAs an SM
+    CUtensorMap mo;
+    e = make_map(&mo, a.out, rows, a.H) ? cudaSuccess : cudaErrorInvalidValue;
+    if (e == cudaSuccess) {
+      gdn_tc_linear_kernel<<<(unsigned)(units * R), kThreads, SMEM_BYTES, stream>>>(
+          mq, mk, mv, a.log_alpha, a.S0, (__nv_bfloat16*)a.out, L, nullptr, a.H, a.T, R);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+      ls_corr_kernel<<<grid, kLsThreads, kLsSmem, stream>>>(mq, mo, a.N, a.H, a.T, R, a.log_alpha, L,
+                                                     a.S_final);
+      e = cudaGetLastError();
+    }
+    const cudaError_t ef = cudaFreeAsync(Lv, stream);
+    return e != cudaSuccess ? e : ef;
   }
   const long long blocks = 2LL * a.N * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

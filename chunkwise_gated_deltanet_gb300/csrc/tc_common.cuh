@@ -205,7 +205,8 @@ __device__ __forceinline__ bool wait_ticket(volatile int* ticket, int want,
 struct Unit {
   long long row0, len;
   int nc, h;
-  size_t sidx;  // offset of S[n][h] in S0 / S_final
+  size_t sidx;   // offset of S[n][h] in S_final
+  size_t s0idx;  // and in S0
 };
 
 // Gate inputs of one chunk for a whole warp: thread `lane` owns tokens lane and
@@ -331,6 +332,7 @@ __device__ __forceinline__ Unit make_unit(int unit, const int32_t* __restrict__ 
   }
   u.nc = (int)((u.len + kC - 1) / kC);
   u.sidx = ((size_t)n * H + u.h) * kD * kD;
+  u.s0idx = u.sidx;
   return u;
 }
 

@@ -123,6 +123,12 @@ def gdn_launches_per_call(dk: int, dv: int, C: int, dtype: torch.dtype) -> int:
     return load_library().gdn_launches_per_call(dk, dv, C, _dtype_code(dtype))
 
 
+def gdn_linear_split_segments(N: int, H: int, T: int, dk: int, dv: int, C: int,
+                              dtype: torch.dtype) -> int:
+    """Segments per sequence of the linear mode's split on the current device (1: none)."""
+    return load_library().gdn_linear_split_segments(N, H, T, dk, dv, C, _dtype_code(dtype))
+
+
 def gdn_check_status(stream: Optional[torch.cuda.Stream] = None) -> None:
     s = stream if stream is not None else torch.cuda.current_stream()
     _check(load_library().gdn_check_status(ctypes.c_void_p(s.cuda_stream)))

@@ -361,6 +361,19 @@ int gdn_select_path(int dk, int dv, int C, int qkv_dtype);
 int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype);
 
 /*
+ * Segments per sequence that gdn_linear_chunk_fwd cuts a fixed-length batch of N
+ * sequences into on the tensor-core path (1: none; 0: invalid sizes).  When the N x H
+ * (sequence, head) units fill at most half of the device's SMs, each sequence runs as R
+ * whole-chunk segments on separate SMs (R <= 4, at least two chunks each, none empty),
+ * and one more kernel folds the segments' end states into the start states and S_final
+ * (the linear mode's segment map is S_end = Gamma S_start + L with a scalar Gamma) and
+ * adds e^{G_t} S_start q_t to the later segments' outputs: 2 launches in place of 1.
+ * Packed batches are not split.
+ * Scratch comes from the library's stream-ordered memory pool.  Uses the current device.
+ */
+int gdn_linear_split_segments(int N, int H, int T, int dk, int dv, int C, int qkv_dtype);
+
+/*
  * Synchronise `stream`, then read and clear the device status word that kernels
  * set when a bounded wait (mbarrier, async copy) gives up.  Returns GDN_OK or
  * GDN_ETIMEOUT (message names the wait), or GDN_ECUDA if the stream failed.

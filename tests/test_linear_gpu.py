@@ -152,3 +152,18 @@ def test_linear_bf16_packed_empty_and_short_sequences(alpha_one):
     g = torch.Generator().manual_seed(7)
     inp["S0"] = torch.randn(len(lens), 2, base.dv, base.dk, generator=g) * 0.1
     _full(inp, 64, alpha_one)
+
+
+@pytest.mark.parametrize("B,H,T,R", [(1, 1, 600, 4), (1, 1, 520, 3), (2, 3, 333, 3),
+                                     (4, 16, 300, 2), (2, 16, 1000, 4)])
+@pytest.mark.parametrize("alpha_one", [False, True], ids=["mamba2", "linear_attention"])
+def test_linear_split_over_more_sms(B, H, T, R, alpha_one):
+    """Few (sequence, head) units: the tcgen05 path cuts each sequence into whole-chunk
+    segments on more SMs, folds their end states and corrects the later segments' outputs;
+    every unit against the oracle, S0 given, ragged tails.  T = 520 (9 chunks) would leave
+    a fourth segment of 3-chunk segments empty, so it takes three."""
+    w = W["gdn_bf16_b4h16t4096d128c64"]
+    assert gdn.gdn_linear_split_segments(B, H, T, 128, 128, 64, torch.bfloat16) == R
+    inp = workloads.make_inputs(w, B=B, H=H, T=T, seed=B + H)
+    inp["S0"] = torch.randn((B, H, 128, 128), generator=torch.Generator().manual_seed(T)) * 0.1
+    _full(inp, 64, alpha_one)
