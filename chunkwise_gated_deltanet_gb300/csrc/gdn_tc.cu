@@ -1197,9 +1197,34 @@ __device__ __forceinline__ float ls_la_sum(const float* __restrict__ log_alpha, 
   }
   return ls_block_sum(s, red);
 }
+// Sums of log alpha over [t0, tm) and [tm, t1) of sequence n, head h in one pass.
+__device__ __forceinline__ float2 ls_la_sum2(const float* __restrict__ log_alpha, int n, int T,
+                                             int H, int h, int t0, int tm, int t1, float* red) {
+  float s0 = 0.f, s1 = 0.f;
+  if (log_alpha) {
+    const float* la = log_alpha + (size_t)n * T * H + h;
+    for (int base = t0; base < t1; base += 2048) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int t = base + (int)threadIdx.x + 128 * e;
+        v[e] = t < t1 ? la[(size_t)t * H] : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int t = base + (int)threadIdx.x + 128 * e;
+        if (t < tm) s0 += v[e]; else s1 += v[e];
+      }
+    }
+  }
+  const float a = ls_block_sum(s0, red);
+  return make_float2(a, ls_block_sum(s1, red));
+}
 
-// The correction, persistent: the (sequence, head, segment r >= 1, 64-token tile) list
-// in that order, an even contiguous share per CTA, so a CTA meets at most a few segments.
+// The correction.  Its work is the (sequence, head, segment r >= 1, 64-token tile) list in
+// that order; with cps > 0 each segment is split into cps contiguous shares, one per CTA
+// (grid = segments x cps), else each CTA takes a contiguous run of whole segments.  The
+// CTA that finishes the last segment of a (sequence, head) also writes its S_final.
 // Warp 4 (one thread) loads q and out tiles by TMA into a three-stage ring, issues
 // D^T (dv x 64 tokens) = S_hi Q^T + S_lo Q^T into one of two TMEM accumulators a tile
 // ahead of the epilogue, and stores each corrected out tile back by TMA.  Warps 0-3, a
@@ -1214,7 +1239,7 @@ constexpr uint32_t kLsTmHi = 0, kLsTmLo = 64, kLsTmAcc = 128;  // TMEM columns
 
 __global__ void __launch_bounds__(kLsThreads, 2)
 ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-               int N, int H, int T, int R, const float* __restrict__ log_alpha,
+               int N, int H, int T, int R, int cps, const float* __restrict__ log_alpha,
                const float* __restrict__ L, float* __restrict__ S_final) {
   extern __shared__ uint8_t ls_smem_raw[];
   uint8_t* sm = ls_smem_raw + ((1024u - (smem_u32(ls_smem_raw) & 1023u)) & 1023u);
@@ -1233,8 +1258,23 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int tpu = 0;  // tiles per (sequence, head)
   for (int r = 1; r < R; ++r) tpu += seg_tiles(T, R, r);
-  const long long tot = (long long)N * H * tpu;
-  const long long i0 = tot * blockIdx.x / gridDim.x, i1 = tot * (blockIdx.x + 1) / gridDim.x;
+  const long long tot = (long long)N * H * tpu, nseg = (long long)N * H * (R - 1);
+  auto seg_first = [&](long long sg) {  // list index of segment sg's first tile
+    if (sg >= nseg) return tot;
+    long long i = sg / (R - 1) * tpu;
+    for (int q = 1; q < 1 + (int)(sg % (R - 1)); ++q) i += seg_tiles(T, R, q);
+    return i;
+  };
+  long long i0, i1;
+  if (cps > 0) {
+    const long long sg = blockIdx.x / cps, base = seg_first(sg);
+    const int j = blockIdx.x % cps, nt = seg_tiles(T, R, 1 + (int)(sg % (R - 1)));
+    i0 = base + (long long)nt * j / cps;
+    i1 = base + (long long)nt * (j + 1) / cps;
+  } else {
+    i0 = seg_first(nseg * blockIdx.x / gridDim.x);
+    i1 = seg_first(nseg * (blockIdx.x + 1) / gridDim.x);
+  }
   if (i0 >= i1) return;
   const int n_t = (int)(i1 - i0);
   // tile i of the list: (sequence, head) unit, segment r, tile k of the segment
@@ -1334,6 +1374,27 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t tl_row = tmem + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
     long long seg = -1;  // the segment whose start state is in TMEM
     float pcur = 0.f;    // sum of log alpha from the segment's first token to the tile's
+    float gam[kLsMaxSeg - 1] = {1.f, 1.f, 1.f};  // Gamma_j of the segment's earlier ones
+    const size_t DD = (size_t)kD * kD, row = (size_t)tid * kD;
+    // Columns 64 hv .. 64 hv + 63 of row `tid` of S_start_r from the end states, given in
+    // x the same columns of L_0: S_start_{j+1} = Gamma_j S_start_j + L_j.
+    auto fold_start = [&](const float* Lu, int r, int hv, float4 (&x)[16]) {
+#pragma unroll 1
+      for (int j = 1; j < r; ++j) {
+        const float gj = j == 1 ? gam[0] : (j == 2 ? gam[1] : gam[2]);
+        const float* Lj = Lu + (size_t)j * H * DD + 64 * hv;
+        float4 y[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) y[e] = ld4(Lj + 4 * e);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          x[e].x = fmaf(gj, x[e].x, y[e].x);
+          x[e].y = fmaf(gj, x[e].y, y[e].y);
+          x[e].z = fmaf(gj, x[e].z, y[e].z);
+          x[e].w = fmaf(gj, x[e].w, y[e].w);
+        }
+      }
+    };
     // warps 0-1: log alpha of token 32 warp + lane of a tile, loaded a tile ahead
     auto gate_of = [&](int it) {
       int unit, r, k, a, b;
@@ -1354,20 +1415,24 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       decode(i0 + it, unit, r, k);
       seg_bounds(T, R, r, a, b);
       const int n = unit / H, h = unit % H, t0 = a + 64 * k, len = min(64, b - t0);
+      const float* Lu = L + ((size_t)n * R * H + h) * DD + row;  // L_j row: Lu + j H DD
       if ((long long)unit * R + r != seg) {  // the same for all four warps
         // the previous segment's products are complete: its last tile's were waited for
         seg = (long long)unit * R + r;
-        const size_t DD = (size_t)kD * kD, row = (size_t)tid * kD;
-        const float* Lu = L + ((size_t)n * R * H + h) * DD + row;  // L_j row: Lu + j H DD
         float4 x[16];  // L_0 row, columns 0 .. 63: in flight while the gate sums run
 #pragma unroll
         for (int e = 0; e < 16; ++e) x[e] = ld4(Lu + 4 * e);
-        // the CTA holding the last segment's first tile writes the sequence's end state;
-        // a CTA that starts at its segment's first tile has no prefix to sum
-        const bool fin = S_final != nullptr && r == R - 1 && k == 0;
-        pcur = k > 0 ? ls_la_sum(log_alpha, n, T, H, h, a, t0, red) : 0.f;
-        const float gfin = fin ? expf(ls_la_sum(log_alpha, n, T, H, h, a, b, red)) : 0.f;
-        float gam[kLsMaxSeg - 1] = {1.f, 1.f, 1.f};  // Gamma_j of segments 1 .. r - 1
+        // the CTAs of a sequence's last segment also write S_final, each a share of its
+        // elements: they need the segment's whole gate sum besides their prefix
+        const bool fin = S_final != nullptr && r == R - 1;
+        float gfin = 0.f;
+        if (fin) {
+          const float2 ps = ls_la_sum2(log_alpha, n, T, H, h, a, t0, b, red);
+          pcur = ps.x;
+          gfin = expf(ps.x + ps.y);
+        } else {  // a CTA that starts at its segment's first tile has no prefix to sum
+          pcur = k > 0 ? ls_la_sum(log_alpha, n, T, H, h, a, t0, red) : 0.f;
+        }
         for (int j = 1; j < r; ++j) {
           int ja, jb;
           seg_bounds(T, R, j, ja, jb);
@@ -1381,32 +1446,7 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           if (hv == 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) x[e] = ld4(Lu + 64 + 4 * e);
-#pragma unroll 1
-          for (int j = 1; j < r; ++j) {  // S_start_{j+1} = Gamma_j S_start_j + L_j
-            const float gj = j == 1 ? gam[0] : (j == 2 ? gam[1] : gam[2]);
-            const float* Lj = Lu + (size_t)j * H * DD + 64 * hv;
-            float4 y[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) y[e] = ld4(Lj + 4 * e);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              x[e].x = fmaf(gj, x[e].x, y[e].x);
-              x[e].y = fmaf(gj, x[e].y, y[e].y);
-              x[e].z = fmaf(gj, x[e].z, y[e].z);
-              x[e].w = fmaf(gj, x[e].w, y[e].w);
-            }
-          }
-          if (fin) {
-            const float* Lr = Lu + (size_t)r * H * DD + 64 * hv;
-            float* Sf = S_final + ((size_t)n * H + h) * DD + row + 64 * hv;
-            float4 y[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) y[e] = ld4(Lr + 4 * e);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              st4(Sf + 4 * e, fmaf(gfin, x[e].x, y[e].x), fmaf(gfin, x[e].y, y[e].y),
-                  fmaf(gfin, x[e].z, y[e].z), fmaf(gfin, x[e].w, y[e].w));
-          }
+          fold_start(Lu, r, hv, x);
           uint32_t hi[32], lo[32];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -1420,6 +1460,29 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_ready);
+        if (fin) {  // S_final = Gamma_r S_start_r + L_r over this CTA's share, coalesced
+          // the shares of this CTA's tiles k .. kend - 1 of the segment's nt, so the CTAs of
+          // the segment cover the whole state between them
+          const int nt = seg_tiles(T, R, r);
+          const long long sf = i0 + it - k;  // list index of the segment's first tile
+          const int kend = (int)(min(i1, sf + nt) - sf);
+          const int f0 = (int)(DD / 4) * k / nt, f1 = (int)(DD / 4) * kend / nt;
+          const float4* L4 = reinterpret_cast<const float4*>(L + ((size_t)n * R * H + h) * DD);
+          float4* S4 = reinterpret_cast<float4*>(S_final + ((size_t)n * H + h) * DD);
+          const size_t js = (size_t)H * DD / 4;  // L_j to L_{j+1}, in float4
+          for (int f = f0 + tid; f < f1; f += 128) {
+            float4 v = L4[f];
+            for (int j = 1; j < r; ++j) {
+              const float gj = j == 1 ? gam[0] : (j == 2 ? gam[1] : gam[2]);
+              const float4 y = L4[f + j * js];
+              v = make_float4(fmaf(gj, v.x, y.x), fmaf(gj, v.y, y.y), fmaf(gj, v.z, y.z),
+                              fmaf(gj, v.w, y.w));
+            }
+            const float4 y = L4[f + r * js];
+            S4[f] = make_float4(fmaf(gfin, v.x, y.x), fmaf(gfin, v.y, y.y), fmaf(gfin, v.z, y.z),
+                                fmaf(gfin, v.w, y.w));
+          }
+        }
       }
       if (warp < 2) {  // inclusive scan of the tile's 64 log alpha, 32 per warp
         const int t = 32 * warp + lane;
@@ -1549,10 +1612,11 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
     if ((e = scratch_alloc(&Lv, (size_t)units * R * kD * kD * sizeof(float), stream)) != cudaSuccess)
       return e;
     float* L = static_cast<float*>(Lv);
-    long long tiles = 0;
-    for (int r = 1; r < R; ++r) tiles += seg_tiles(a.T, R, r);
-    tiles *= units;
-    const unsigned grid = (unsigned)std::min<long long>(tiles, 2LL * sms);  // two CTAs an SM
+    // two correction CTAs an SM: a share of one segment each when there are enough, else
+    // runs of whole segments
+    const long long nseg = units * (R - 1), slots = 2LL * sms;
+    const int cps = nseg <= slots ? (int)std::min<long long>(slots / nseg, seg_tiles(a.T, R, 1)) : 0;
+    const unsigned grid = (unsigned)(cps > 0 ? nseg * cps : slots);
     CUtensorMap mo;
     e = make_map(&mo, a.out, rows, a.H) ? cudaSuccess : cudaErrorInvalidValue;
     if (e == cudaSuccess) {
@@ -1561,8 +1625,8 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
       e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
-      ls_corr_kernel<<<grid, kLsThreads, kLsSmem, stream>>>(mq, mo, a.N, a.H, a.T, R, a.log_alpha, L,
-                                                     a.S_final);
+      ls_corr_kernel<<<grid, kLsThreads, kLsSmem, stream>>>(mq, mo, a.N, a.H, a.T, R, cps,
+                                                            a.log_alpha, L, a.S_final);
       e = cudaGetLastError();
     }
     const cudaError_t ef = cudaFreeAsync(Lv, stream);
