@@ -754,9 +754,13 @@ def main():
     achieved_tf = alg["flops"] / sec / 1e12
     path = gdn.gdn_select_path(dk, dv, C, d["v"].dtype)
     launches = gdn.gdn_launches_per_call(dk, dv, C, d["v"].dtype)
+    scope = "one launch"
     if w.linear and inp["cu_seqlens"] is None and \
             gdn.gdn_linear_split_segments(B, H, T, dk, dv, C, d["v"].dtype) > 1:
         launches = 2  # the segments, then the fold and correction
+        scope = "the step's two launches (segments, then fold and correction) against the path's algorithmic bytes"
+    elif launches > 1:
+        scope = f"the step's {launches} launches against the path's algorithmic bytes"
 
     # ---- end to end through the public call with pinned host buffers ----
     host_in = {k: (inp[k].pin_memory() if inp[k] is not None else None)
@@ -810,7 +814,7 @@ def main():
                          "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
                          "traffic": measured_traffic(w.name) if args.T == 0 else None,
                          "peak_source": peaks["source"],
-                         "algorithmic_bytes": alg["bytes"],
+                         "algorithmic_bytes": alg["bytes"], "scope": scope,
                          "tensor_tflops": achieved_tf,
                          "tensor_frac": achieved_tf / peaks["bf16_tflops"]},
             "clocks": clk.summary(),
