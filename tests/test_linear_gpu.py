@@ -167,3 +167,20 @@ def test_linear_split_over_more_sms(B, H, T, R, alpha_one):
     inp = workloads.make_inputs(w, B=B, H=H, T=T, seed=B + H)
     inp["S0"] = torch.randn((B, H, 128, 128), generator=torch.Generator().manual_seed(T)) * 0.1
     _full(inp, 64, alpha_one)
+
+
+@pytest.mark.parametrize("alpha_mu", [2.0, -2.0], ids=["mild", "strong_decay"])
+def test_linear_split_with_resets_at_segment_edges(alpha_mu):
+    """Four segments of 256 tokens (B=1, H=2, T=1000): alpha = 0 (a full reset) on the last
+    token of a segment, on the first token of the next, inside a later segment and on the
+    sequence's last token, so the folded start states and the correction's gate sums meet
+    exp(-inf) = 0 at the edges; mild and strong decay."""
+    w = workloads.Workload("split_resets", "bf16", B=1, H=2, T=1000, dk=128, dv=128, C=64,
+                           alpha_mu=alpha_mu, s0_std=0.1)
+    assert gdn.gdn_linear_split_segments(1, 2, 1000, 128, 128, 64, torch.bfloat16) == 4
+    inp = workloads.make_inputs(w, seed=21)
+    la = inp["log_alpha"].clone()
+    for t in (255, 256, 511, 600, 999):
+        la[:, t, :] = -float("inf")
+    inp["log_alpha"] = la
+    _full(inp, 64)
