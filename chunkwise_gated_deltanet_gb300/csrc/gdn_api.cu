@@ -105,7 +105,7 @@ int chunk_fwd_impl(const char* fn, bool linear, const void* q, const void* k, co
   const int path = gdn_select_path(dk, dv, C, qkv_dtype);
   if (path == GDN_PATH_TCGEN05)
     e = gdn::launch_tc(a, s);
-  else if (path == GDN_PATH_TF32 && !linear)
+  else if (path == GDN_PATH_TF32)
     e = gdn::launch_fwd_chunked(a, s);
   else
     e = gdn::launch_rec(a, s);
@@ -357,7 +357,7 @@ int gdn_chunk_fwd_host(const void* q, const void* k, const void* v, const float*
   a.B = B; a.H = H; a.T = T; a.dk = dk; a.dv = dv; a.C = C; a.pieces = pieces;
   a.bf16 = qkv_dtype == GDN_BF16;
   const int path = gdn_select_path(dk, dv, C, qkv_dtype);
-  a.tc = path == GDN_PATH_TCGEN05 ? 1 : (path == GDN_PATH_TF32 && !linear ? 2 : 0);
+  a.tc = path == GDN_PATH_TCGEN05 ? 1 : (path == GDN_PATH_TF32 ? 2 : 0);
   const cudaError_t e = gdn::launch_host_fwd(a, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return fail(GDN_ECUDA, "%s: %s", fn, cudaGetErrorString(e));

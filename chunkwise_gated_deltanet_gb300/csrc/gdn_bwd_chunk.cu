@@ -198,13 +198,15 @@ __global__ void __launch_bounds__(256) ck_gather_kernel(GatherArgs p) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x, c0 = 2 * lane, c1 = c0 + 1;
     float la0 = 0.f, la1 = 0.f, b0 = 0.f, b1 = 0.f;
+    // a NULL log_alpha is alpha = 1; a NULL beta (the forward's linear mode) an erase
+    // strength of 0, so A = 0, T = I and W~ = 0
     if (c0 < len) {
-      la0 = fmaxf(p.log_alpha[(size_t)(row0 + c0) * p.H + h], kLogAlphaMin);
-      b0 = p.beta[(size_t)(row0 + c0) * p.H + h];
+      if (p.log_alpha) la0 = fmaxf(p.log_alpha[(size_t)(row0 + c0) * p.H + h], kLogAlphaMin);
+      if (p.beta) b0 = p.beta[(size_t)(row0 + c0) * p.H + h];
     }
     if (c1 < len) {
-      la1 = fmaxf(p.log_alpha[(size_t)(row0 + c1) * p.H + h], kLogAlphaMin);
-      b1 = p.beta[(size_t)(row0 + c1) * p.H + h];
+      if (p.log_alpha) la1 = fmaxf(p.log_alpha[(size_t)(row0 + c1) * p.H + h], kLogAlphaMin);
+      if (p.beta) b1 = p.beta[(size_t)(row0 + c1) * p.H + h];
     }
     float s = la0 + la1;
 #pragma unroll
@@ -1777,6 +1779,8 @@ cudaError_t pool_alloc(void** ptr, size_t bytes, cudaStream_t s) {
 template <int D, typename TIn>
 cudaError_t launch_fwd_ck_t(const FwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.B * a.T;
+  // the linear mode (beta NULL): erase 0 (the gather's gates), write 1 (delta = V)
+  const bool linear = a.beta == nullptr;
   const FwdLayout L = fwd_layout(rows, a.H, D, a.N, a.C);
   cudaError_t e;
   static std::atomic<unsigned long long> set_mm{0}, set_c{0};
@@ -1826,14 +1830,16 @@ cudaError_t launch_fwd_ck_t(const FwdArgs& a, cudaStream_t s) {
       Mm m = mm.make(Tm, CC, kCk, 1, Kc, CD, D, 1, Wt, CD, D, 1, kCk, D, kCk);
       m.t[0].ks = gates + G_BEG * kCk;
       mm.run(m);
-      m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
-      m.t[0].ks = gates + G_BETA * kCk;
-      mm.run(m);
+      if (!linear) {  // the linear mode writes with strength 1: U = V
+        m = mm.make(Tm, CC, kCk, 1, Vc, CD, D, 1, U, CD, D, 1, kCk, D, kCk);
+        m.t[0].ks = gates + G_BETA * kCk;
+        mm.run(m);
+      }
     }
     if (mm.err != cudaSuccess) return mm.err;
     ChainArgs cf;
     cf.cbase = cbase; cf.init = a.S0; cf.fin = a.S_final; cf.st = S;
-    cf.add1 = U; cf.a1 = Wt; cf.a2 = Kc; cf.add2 = nullptr; cf.out1 = Dl;
+    cf.add1 = linear ? Vc : U; cf.a1 = Wt; cf.a2 = Kc; cf.add2 = nullptr; cf.out1 = Dl;
     cf.gates = gates; cf.gam = gam; cf.H = a.H;
     if ((e2 = launch_chain<D, false>(cf, L.nb, a.N, a.H, status, s)) != cudaSuccess) return e2;
     {  // O = diag(e^g) Q S_j^T + P delta

@@ -56,7 +56,7 @@ typedef enum {
                              dk = dv = 64 or 128, C = 16, 32 or 64, every shape and dtype
                              the bf16 kernel does not take; scratch from a stream-ordered
                              memory pool the library keeps per device.  The linear mode
-                             takes the recurrence here. */
+                             runs here too, with erase 0 (T = I, W~ = 0) and U = V. */
 } gdn_path;
 
 /*
@@ -268,7 +268,10 @@ size_t gdn_chunk_fwd_host_workspace_bytes(int B, int H, int T, int dk, int dv, i
  * linear attention).  On the tensor-core path (GDN_PATH_TCGEN05) this mode has a kernel
  * of its own: with no erase the pseudo-values are V itself, so one CTA per (sequence,
  * head) runs without the WY factors; the results equal gdn_chunk_fwd's pipeline run with
- * these factors, bit for bit.
+ * these factors, bit for bit, except where gdn_linear_split_segments splits the sequences
+ * (few (sequence, head) units; see there), which changes the order of the sums.  On
+ * GDN_PATH_TF32 it runs the same batched chunk-form kernels as gdn_chunk_fwd with the
+ * erase gates 0 (so T = I and W~ = 0) and U = V.
  */
 int gdn_linear_chunk_fwd(const void* q, const void* k, const void* v,
                          const float* log_alpha, const float* S0,

@@ -184,3 +184,35 @@ def test_linear_split_with_resets_at_segment_edges(alpha_mu):
         la[:, t, :] = -float("inf")
     inp["log_alpha"] = la
     _full(inp, 64)
+
+
+@pytest.mark.parametrize("d,dtype,C", [(64, "f32", 64), (128, "f32", 64), (64, "bf16", 32),
+                                       (128, "bf16", 16)])
+@pytest.mark.parametrize("alpha_one", [False, True], ids=["mamba2", "linear_attention"])
+def test_linear_on_the_tf32_chunk_path(d, dtype, C, alpha_one):
+    """The shapes off the bf16 kernel run the linear mode on the TF32 chunk path (the
+    gather's erase gates 0, so T = I and W~ = 0, and U = V): every unit against the
+    oracle, S0 given, a ragged last chunk, with and without gates."""
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    assert gdn.gdn_select_path(d, d, C, dt) == gdn.GDN_PATH_TF32
+    w = workloads.Workload("lin_tf32", dtype, B=2, H=2, T=333, dk=d, dv=d, C=C, alpha_mu=2.0,
+                           s0_std=0.1)
+    _full(workloads.make_inputs(w, seed=31 + d + C), C, alpha_one)
+
+
+def test_linear_tf32_chunk_path_packed_with_resets():
+    """A packed fp32 batch on the TF32 chunk path: empty, one-token, one-chunk, ragged
+    members, each from its own S0, with alpha = 0 resets inside and at the first token."""
+    lens = [0, 1, 64, 65, 130, 17]
+    w = workloads.Workload("lin_tf32_packed", "f32", B=1, H=2, T=sum(lens), dk=128, dv=128,
+                           C=64, alpha_mu=2.0, s0_std=0.0)
+    inp = workloads.make_inputs(w, seed=41)
+    inp["cu_seqlens"] = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    inp["N"] = len(lens)
+    inp["S0"] = torch.randn(len(lens), 2, 128, 128,
+                            generator=torch.Generator().manual_seed(42)) * 0.1
+    la = inp["log_alpha"].clone()
+    for t in (1, 2, 100, 200):
+        la[:, t, :] = -float("inf")
+    inp["log_alpha"] = la
+    _full(inp, 64)
