@@ -216,3 +216,22 @@ def test_linear_tf32_chunk_path_packed_with_resets():
         la[:, t, :] = -float("inf")
     inp["log_alpha"] = la
     _full(inp, 64)
+
+
+def test_linear_split_without_S0_or_final_state():
+    """The split path with S0 = NULL (every segment from zero) and S_final not requested
+    (the correction then writes no end state); the outputs against the oracle."""
+    w = workloads.Workload("split_plain", "bf16", B=1, H=3, T=700, dk=128, dv=128, C=64,
+                           alpha_mu=4.0, s0_std=0.0)
+    assert gdn.gdn_linear_split_segments(1, 3, 700, 128, 128, 64, torch.bfloat16) > 1
+    inp = workloads.make_inputs(w, seed=51)
+    assert inp["S0"] is None
+    d = to_device(inp)
+    out, Sf = gdn.linear_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], None, None, C=64,
+                                   output_final_state=False)
+    gdn.gdn_check_status()
+    torch.cuda.synchronize()
+    assert Sf is None
+    ro, _ = _oracle(inp, False)
+    assert_close(out.float().cpu().numpy().astype(np.float64), ro, False, "out",
+                 stored_bf16=True)
