@@ -1470,17 +1470,28 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           const float4* L4 = reinterpret_cast<const float4*>(L + ((size_t)n * R * H + h) * DD);
           float4* S4 = reinterpret_cast<float4*>(S_final + ((size_t)n * H + h) * DD);
           const size_t js = (size_t)H * DD / 4;  // L_j to L_{j+1}, in float4
-          for (int f = f0 + tid; f < f1; f += 128) {
-            float4 v = L4[f];
+          for (int f = f0 + tid; f < f1; f += 8 * 128) {  // eight float4 a thread in flight
+            float4 v[8], y[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int ff = min(f + 128 * u, f1 - 1);  // past the share: a repeat, not stored
+              v[u] = L4[ff];
+              y[u] = L4[ff + r * js];
+            }
             for (int j = 1; j < r; ++j) {
               const float gj = j == 1 ? gam[0] : (j == 2 ? gam[1] : gam[2]);
-              const float4 y = L4[f + j * js];
-              v = make_float4(fmaf(gj, v.x, y.x), fmaf(gj, v.y, y.y), fmaf(gj, v.z, y.z),
-                              fmaf(gj, v.w, y.w));
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const float4 z = L4[min(f + 128 * u, f1 - 1) + j * js];
+                v[u] = make_float4(fmaf(gj, v[u].x, z.x), fmaf(gj, v[u].y, z.y),
+                                   fmaf(gj, v[u].z, z.z), fmaf(gj, v[u].w, z.w));
+              }
             }
-            const float4 y = L4[f + r * js];
-            S4[f] = make_float4(fmaf(gfin, v.x, y.x), fmaf(gfin, v.y, y.y), fmaf(gfin, v.z, y.z),
-                                fmaf(gfin, v.w, y.w));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (f + 128 * u < f1)
+                S4[f + 128 * u] = make_float4(fmaf(gfin, v[u].x, y[u].x), fmaf(gfin, v[u].y, y[u].y),
+                                              fmaf(gfin, v[u].z, y[u].z), fmaf(gfin, v[u].w, y[u].w));
           }
         }
       }
