@@ -389,7 +389,8 @@ def run_seqpar(args, w, world, rank, local):
     """The sequence-parallel split of one workload over R = --seqpar ranks, with every
     rank's work timed alone on this one GPU: phase 1 (rank 0's segment from S0; a
     middle rank's (M, L) passes on two streams), then phase 2 (the fold and the
-    segment from the folded start state).  The critical path max(phase 1) +
+    segment from the folded start state; in the linear mode at bf16 d = 128 the ranks
+    r > 0 run their segment from zero in phase 1 and only correct it in phase 2).  The critical path max(phase 1) +
     max(phase 2) is what R GPUs would take, less the exchange of two state-sized
     tensors per rank, which is not timed here."""
     import chunkwise_gated_deltanet_gb300 as gdn
@@ -445,7 +446,8 @@ def run_seqpar(args, w, world, rank, local):
     crit = max(ph1) + max(ph2)
     tokens = inp["B"] * T
     print(json.dumps({
-        "metric": f"gated-DeltaNet sequence-parallel fwd tokens/s over {Rk} ranks "
+        "metric": ("linear-attention (Mamba2 gate)" if w.linear else "gated-DeltaNet") +
+                  f" sequence-parallel fwd tokens/s over {Rk} ranks "
                   "(per-rank work timed on one GPU)",
         "value": tokens / (crit * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": crit, "higher_is_better": True,

@@ -122,7 +122,48 @@ cudaError_t launch_fold_dk(const float* S_in, const float* M, const float* L, in
   return cudaSuccess;
 }
 
+// The linear mode's map over each sequence (Nyysyyan, "Mamba2": the state is the decayed
+// sum of the writes, so M = (product of alpha_t) I): one block per (sequence, head) sums
+// its log alpha (fp32, strided loads eight in flight), then writes the dk x dk M.
+__global__ void __launch_bounds__(256)
+gain_map_kernel(const float* __restrict__ log_alpha, float* __restrict__ M, int H, int T, int dk,
+                const int32_t* __restrict__ cu_seqlens) {
+  const int unit = blockIdx.x, n = unit / H, h = unit % H;
+  long long a = (long long)n * T, b = a + T;
+  if (cu_seqlens) {  // a packed member, clamped to the token range like the forward
+    const long long lo = min(max((long long)cu_seqlens[n], 0LL), (long long)T);
+    a = lo;
+    b = min(max((long long)cu_seqlens[n + 1], lo), (long long)T);
+  }
+  __shared__ float red[8];
+  float s = 0.f;
+  if (log_alpha)
+    for (long long t0 = a + threadIdx.x; t0 < b; t0 += 8 * 256) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const long long t = t0 + 256LL * e;
+        v[e] = t < b ? log_alpha[t * H + h] : 0.f;
+      }
+      s += ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  const float g = expf(((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7])));
+  float* m = M + (size_t)unit * dk * dk;
+  for (int i = threadIdx.x; i < dk * dk; i += 256) m[i] = (i / dk == i % dk) ? g : 0.f;
+}
+
 }  // namespace
+
+cudaError_t launch_gain_map(const float* log_alpha, float* M, int units, int H, int T, int dk,
+                            const int32_t* cu_seqlens, cudaStream_t stream) {
+  if (units == 0) return cudaSuccess;
+  gain_map_kernel<<<units, 256, 0, stream>>>(log_alpha, M, H, T, dk, cu_seqlens);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_state_fold(const float* S_in, const float* M, const float* L, int count,
                               float* S_out, int units, int dv, int dk, cudaStream_t stream) {

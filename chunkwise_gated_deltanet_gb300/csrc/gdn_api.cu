@@ -134,6 +134,36 @@ int gdn_linear_chunk_fwd(const void* q, const void* k, const void* v, const floa
                         S_final, B, H, T, dk, dv, C, cu_seqlens, N_seqs, qkv_dtype, stream);
 }
 
+int gdn_linear_state_correct_supported(int dk, int dv, int qkv_dtype) {
+  return gdn::linear_correct_supported(dk, dv, qkv_dtype == GDN_BF16) ? 1 : 0;
+}
+
+int gdn_linear_state_correct(const void* q, const float* log_alpha, const float* S_start,
+                             void* out, float* S_end, int B, int H, int T, int dk, int dv,
+                             int qkv_dtype, void* stream) {
+  const char* fn = "gdn_linear_state_correct";
+  if (qkv_dtype != GDN_F32 && qkv_dtype != GDN_BF16)
+    return fail(GDN_EDTYPE, "%s: qkv_dtype must be GDN_F32 or GDN_BF16", fn);
+  if (!gdn::linear_correct_supported(dk, dv, qkv_dtype == GDN_BF16))
+    return fail(GDN_EINVAL, "%s: needs bf16 with dk = dv = 128 (got dk %d, dv %d)", fn, dk, dv);
+  if (B <= 0 || H <= 0 || T < 0)
+    return fail(GDN_EINVAL, "%s: need B, H > 0 and T >= 0", fn);
+  if (!S_start || (T > 0 && (!q || !out)))
+    return fail(GDN_EINVAL, "%s: S_start (and q, out when T > 0) must be non-NULL", fn);
+  if ((long long)B * T > 0x7fffffffLL)
+    return fail(GDN_EINVAL, "%s: problem too large", fn);
+  const void* ptrs[] = {q, log_alpha, S_start, out, S_end};
+  const char* names[] = {"q", "log_alpha", "S_start", "out", "S_end"};
+  for (int i = 0; i < 5; ++i)
+    if (ptrs[i] && !aligned16(ptrs[i]))
+      return fail(GDN_EINVAL, "%s: %s is not 16-byte aligned", fn, names[i]);
+  const cudaError_t e = gdn::launch_linear_correct(q, log_alpha, S_start, out, S_end, B, H, T,
+                                                   (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(GDN_ELAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return GDN_OK;
+}
+
 int gdn_decode_step(const void* q, const void* k, const void* v, const float* log_alpha,
                     const float* beta, float* S, void* out, int N, int H, int dk, int dv,
                     int qkv_dtype, void* stream) {
@@ -278,6 +308,25 @@ int gdn_chunk_bwd_noalloc(const void* q, const void* k, const void* v, const flo
                           d_log_alpha, d_beta, d_S0, scratch,
                           scratch ? gdn::kBwdNoAllocScratchBytes : 0, B, H, T, dk, dv,
                           cu_seqlens, N_seqs, qkv_dtype, GDN_BWD_TOKENS, stream);
+}
+
+int gdn_linear_segment_map(const float* log_alpha, float* M, int B, int H, int T, int dk,
+                           const int32_t* cu_seqlens, int N_seqs, void* stream) {
+  const char* fn = "gdn_linear_segment_map";
+  if (B <= 0 || H <= 0 || T < 0 || !head_ok(dk))
+    return fail(GDN_EINVAL, "%s: need B, H > 0, T >= 0 and dk in {16, 32, 64, 128}", fn);
+  if (cu_seqlens && (B != 1 || N_seqs <= 0))
+    return fail(GDN_EINVAL, "%s: a packed batch needs B = 1 and N_seqs > 0", fn);
+  if (!M) return fail(GDN_EINVAL, "%s: M must be non-NULL", fn);
+  if ((log_alpha && !aligned16(log_alpha)) || !aligned16(M))
+    return fail(GDN_EINVAL, "%s: log_alpha and M must be 16-byte aligned", fn);
+  const long long units = (long long)(cu_seqlens ? N_seqs : B) * H;
+  if (units > 0x7fffffffLL || (long long)B * T > 0x7fffffffLL)
+    return fail(GDN_EINVAL, "%s: problem too large", fn);
+  const cudaError_t e = gdn::launch_gain_map(log_alpha, M, (int)units, H, T, dk,
+                                             cu_seqlens, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(GDN_ELAUNCH, "%s: launch failed: %s", fn, cudaGetErrorString(e));
+  return GDN_OK;
 }
 
 int gdn_state_fold(const float* S_in, const float* M, const float* L, int count, float* S_out,

@@ -63,6 +63,12 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream);
 int tc_launches(const FwdArgs& a);
 // Segments per sequence the linear mode's split runs with for these sizes (1: no split).
 int linear_split_segments(long long N, int H, int T);
+// The linear mode's start-state correction of whole fixed-length sequences (bf16,
+// dk = dv = 128): out += e^{G_t} S_start q_t, S_end <- Gamma S_start + S_end.
+bool linear_correct_supported(int dk, int dv, int bf16);
+cudaError_t launch_linear_correct(const void* q, const float* log_alpha, const float* S_start,
+                                  void* out, float* S_end, int B, int H, int T,
+                                  cudaStream_t stream);
 // Stream-ordered scratch from the library's per-device memory pool (cudaFreeAsync frees).
 cudaError_t scratch_alloc(void** ptr, size_t bytes, cudaStream_t stream);
 // Single-token decode step (recurrent form), already validated by the API layer.
@@ -147,6 +153,10 @@ cudaError_t bwd_noalloc_scratch(void** ptr);
 bool bwd_chunked_supported(int dk, int dv);
 size_t bwd_chunked_workspace_bytes(long long rows, int H, int dk, int dv, int N);
 cudaError_t launch_bwd_chunked(const BwdArgs& a, cudaStream_t stream);
+// M[n][h] = e^{sum of log alpha over sequence n} I (dk x dk), already validated; packed
+// members from cu_seqlens (T is then the packed token count).
+cudaError_t launch_gain_map(const float* log_alpha, float* M, int units, int H, int T, int dk,
+                            const int32_t* cu_seqlens, cudaStream_t stream);
 // S <- S M_i + L_i for i < count per state (S_in NULL: zeros), already validated.
 cudaError_t launch_state_fold(const float* S_in, const float* M, const float* L, int count,
                               float* S_out, int units, int dv, int dk, cudaStream_t stream);

@@ -1104,6 +1104,22 @@ __host__ __device__ __forceinline__ int seg_tiles(int T, int R, int r) {
   seg_bounds(T, R, r, a, b);
   return a < b ? (b - a + 63) / 64 : 0;
 }
+// The correction's segment r >= 1: segment r of the split, or, when the start states are
+// given (`whole`), the whole sequence as its one segment.
+__host__ __device__ __forceinline__ void corr_bounds(int T, int R, int r, bool whole, int& a,
+                                                     int& b) {
+  if (whole) {
+    a = 0;
+    b = T;
+  } else {
+    seg_bounds(T, R, r, a, b);
+  }
+}
+__host__ __device__ __forceinline__ int corr_tiles(int T, int R, int r, bool whole) {
+  int a, b;
+  corr_bounds(T, R, r, whole, a, b);
+  return a < b ? (b - a + 63) / 64 : 0;
+}
 
 // Linear mode (no erase, write strength 1): the WY factors are T = I, W~ = 0, U = V, so
 // the state CTA runs alone, one CTA per (sequence, head): its chain is the state update
@@ -1224,7 +1240,9 @@ __device__ __forceinline__ float2 ls_la_sum2(const float* __restrict__ log_alpha
 // The correction.  Its work is the (sequence, head, segment r >= 1, 64-token tile) list in
 // that order; with cps > 0 each segment is split into cps contiguous shares, one per CTA
 // (grid = segments x cps), else each CTA takes a contiguous run of whole segments.  The
-// CTA that finishes the last segment of a (sequence, head) also writes its S_final.
+// CTAs of the last segment of a (sequence, head) also write its S_final.  With Sst given
+// (R = 2), each whole sequence is the one corrected segment: its start state is
+// Sst[n][h], and S_final holds its end state from zero on entry (updated in place).
 // Warp 4 (one thread) loads q and out tiles by TMA into a three-stage ring, issues
 // D^T (dv x 64 tokens) = S_hi Q^T + S_lo Q^T into one of two TMEM accumulators a tile
 // ahead of the epilogue, and stores each corrected out tile back by TMA.  Warps 0-3, a
@@ -1240,7 +1258,9 @@ constexpr uint32_t kLsTmHi = 0, kLsTmLo = 64, kLsTmAcc = 128;  // TMEM columns
 __global__ void __launch_bounds__(kLsThreads, 2)
 ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
                int N, int H, int T, int R, int cps, const float* __restrict__ log_alpha,
-               const float* __restrict__ L, float* __restrict__ S_final) {
+               const float* __restrict__ L, float* __restrict__ S_final,
+               const float* __restrict__ Sst, __nv_bfloat16* __restrict__ out) {
+  const bool whole = Sst != nullptr;
   extern __shared__ uint8_t ls_smem_raw[];
   uint8_t* sm = ls_smem_raw + ((1024u - (smem_u32(ls_smem_raw) & 1023u)) & 1023u);
   // full[s], out_ready[s] (the epilogue has written stage s's out tile), acc_full[a],
@@ -1257,18 +1277,18 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   volatile int* abort_flag = &abort_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int tpu = 0;  // tiles per (sequence, head)
-  for (int r = 1; r < R; ++r) tpu += seg_tiles(T, R, r);
+  for (int r = 1; r < R; ++r) tpu += corr_tiles(T, R, r, whole);
   const long long tot = (long long)N * H * tpu, nseg = (long long)N * H * (R - 1);
   auto seg_first = [&](long long sg) {  // list index of segment sg's first tile
     if (sg >= nseg) return tot;
     long long i = sg / (R - 1) * tpu;
-    for (int q = 1; q < 1 + (int)(sg % (R - 1)); ++q) i += seg_tiles(T, R, q);
+    for (int q = 1; q < 1 + (int)(sg % (R - 1)); ++q) i += corr_tiles(T, R, q, whole);
     return i;
   };
   long long i0, i1;
   if (cps > 0) {
     const long long sg = blockIdx.x / cps, base = seg_first(sg);
-    const int j = blockIdx.x % cps, nt = seg_tiles(T, R, 1 + (int)(sg % (R - 1)));
+    const int j = blockIdx.x % cps, nt = corr_tiles(T, R, 1 + (int)(sg % (R - 1)), whole);
     i0 = base + (long long)nt * j / cps;
     i1 = base + (long long)nt * (j + 1) / cps;
   } else {
@@ -1282,7 +1302,7 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     unit = (int)(i / tpu);
     k = (int)(i % tpu);
     r = 1;
-    while (r + 1 < R && k >= seg_tiles(T, R, r)) k -= seg_tiles(T, R, r++);
+    while (r + 1 < R && k >= corr_tiles(T, R, r, whole)) k -= corr_tiles(T, R, r++, whole);
   };
   if (tid == 0) {
     for (int s = 0; s < kLsStages; ++s) {
@@ -1310,7 +1330,7 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       auto load = [&](int it) {
         int unit, r, k, a, b;
         decode(i0 + it, unit, r, k);
-        seg_bounds(T, R, r, a, b);
+        corr_bounds(T, R, r, whole, a, b);
         const int s = it % kLsStages, h = unit % H, row = (unit / H) * T + a + 64 * k;
         uint8_t* qb = sm + s * kLsStageBytes;
         mbar_arrive_expect_tx(&full[s], 32768);
@@ -1354,13 +1374,14 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!(ok = wait_bar(&out_ready[s], (it / kLsStages) & 1, abort_flag, false))) break;
         int unit, r, k, a, b;
         decode(i0 + it, unit, r, k);
-        seg_bounds(T, R, r, a, b);
-        // the store writes the tile's 64 rows: past a sequence's end the rows loaded from
-        // the next sequence's first segment, which nothing else writes meanwhile, go back
-        // unchanged
+        corr_bounds(T, R, r, whole, a, b);
+        // a whole tile goes back by TMA store; a sequence's ragged last tile was written
+        // to its rows by the epilogue (past them are another sequence's), so its group is
+        // empty
         const uint8_t* ob = sm + s * kLsStageBytes + 16384;
-        for (int c = 0; c < 2; ++c)
-          tma_store_3d(&tm_o, ob + c * 8192, 64 * c, unit % H, (unit / H) * T + a + 64 * k);
+        if (a + 64 * k + 64 <= b)
+          for (int c = 0; c < 2; ++c)
+            tma_store_3d(&tm_o, ob + c * 8192, 64 * c, unit % H, (unit / H) * T + a + 64 * k);
         bulk_commit();
         // the stage of tile it - 1 takes tile it + 2 once that tile's store has read it
         if (it >= 1 && it + 2 < n_t) {
@@ -1399,7 +1420,7 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto gate_of = [&](int it) {
       int unit, r, k, a, b;
       decode(i0 + it, unit, r, k);
-      seg_bounds(T, R, r, a, b);
+      corr_bounds(T, R, r, whole, a, b);
       const int t = 32 * warp + lane, t0 = a + 64 * k;
       return (log_alpha && t0 + t < b)
                  ? log_alpha[((size_t)(unit / H) * T + t0 + t) * H + unit % H]
@@ -1413,9 +1434,11 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const int s = it % kLsStages, a_ = it & 1;
       int unit, r, k, a, b;
       decode(i0 + it, unit, r, k);
-      seg_bounds(T, R, r, a, b);
+      corr_bounds(T, R, r, whole, a, b);
       const int n = unit / H, h = unit % H, t0 = a + 64 * k, len = min(64, b - t0);
-      const float* Lu = L + ((size_t)n * R * H + h) * DD + row;  // L_j row: Lu + j H DD
+      // this thread's row of L_j (Lu + j H DD), or of the given start state
+      const float* Lu = whole ? Sst + ((size_t)n * H + h) * DD + row
+                              : L + ((size_t)n * R * H + h) * DD + row;
       if ((long long)unit * R + r != seg) {  // the same for all four warps
         // the previous segment's products are complete: its last tile's were waited for
         seg = (long long)unit * R + r;
@@ -1463,20 +1486,24 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (fin) {  // S_final = Gamma_r S_start_r + L_r over this CTA's share, coalesced
           // the shares of this CTA's tiles k .. kend - 1 of the segment's nt, so the CTAs of
           // the segment cover the whole state between them
-          const int nt = seg_tiles(T, R, r);
+          const int nt = corr_tiles(T, R, r, whole);
           const long long sf = i0 + it - k;  // list index of the segment's first tile
           const int kend = (int)(min(i1, sf + nt) - sf);
           const int f0 = (int)(DD / 4) * k / nt, f1 = (int)(DD / 4) * kend / nt;
-          const float4* L4 = reinterpret_cast<const float4*>(L + ((size_t)n * R * H + h) * DD);
+          // L_0 (or the given start state), L_j for the fold, L_r (or, given start states,
+          // the end state from zero, updated in place)
           float4* S4 = reinterpret_cast<float4*>(S_final + ((size_t)n * H + h) * DD);
+          const float4* L4 = reinterpret_cast<const float4*>(
+              whole ? Sst + ((size_t)n * H + h) * DD : L + ((size_t)n * R * H + h) * DD);
           const size_t js = (size_t)H * DD / 4;  // L_j to L_{j+1}, in float4
+          const float4* E4 = whole ? S4 : L4 + r * js;
           for (int f = f0 + tid; f < f1; f += 8 * 128) {  // eight float4 a thread in flight
             float4 v[8], y[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const int ff = min(f + 128 * u, f1 - 1);  // past the share: a repeat, not stored
               v[u] = L4[ff];
-              y[u] = L4[ff + r * js];
+              y[u] = E4[ff];
             }
             for (int j = 1; j < r; ++j) {
               const float gj = j == 1 ? gam[0] : (j == 2 ? gam[1] : gam[2]);
@@ -1536,13 +1563,23 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           e[4 * q + 3] = v.w;
         }
         tmem_wait_ld();
+        if (len == 64) {  // back into the tile, for the TMA store
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (32 * cb + j < len) {
+          for (int j = 0; j < 32; ++j) {
             const float o = __uint_as_float((uint32_t)ov[j] << 16) + e[j] * __uint_as_float(u[j]);
             *reinterpret_cast<__nv_bfloat16*>(ob + (32 * cb + j) * 128 +
                                               ((col_chunk ^ (j & 7)) << 4)) = __float2bfloat16_rn(o);
           }
+        } else {  // a ragged last tile: straight to its own rows
+          __nv_bfloat16* og = out + ((size_t)n * T + t0) * H * kD + (size_t)h * kD + tid;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (32 * cb + j < len) {
+              const float o =
+                  __uint_as_float((uint32_t)ov[j] << 16) + e[j] * __uint_as_float(u[j]);
+              og[(size_t)(32 * cb + j) * H * kD] = __float2bfloat16_rn(o);
+            }
+        }
       }
       tc_fence_before();
       fence_async_smem();
@@ -1567,6 +1604,13 @@ ls_corr_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   }
 }
 
+// S_end += S_start, element by element (the correction of an empty segment: Gamma = 1).
+__global__ void __launch_bounds__(256)
+ls_add_kernel(float* __restrict__ S_end, const float* __restrict__ S_start, long long n) {
+  for (long long i = (long long)blockIdx.x * 256 + threadIdx.x; i < n; i += (long long)gridDim.x * 256)
+    S_end[i] += S_start[i];
+}
+
 }  // namespace
 
 bool tc_supported(int dk, int dv, int C, int bf16) {
@@ -1574,6 +1618,41 @@ bool tc_supported(int dk, int dv, int C, int bf16) {
 }
 
 int tc_launches(const FwdArgs&) { return 1; }
+
+bool linear_correct_supported(int dk, int dv, int bf16) { return tc_supported(dk, dv, kC, bf16); }
+
+cudaError_t launch_linear_correct(const void* q, const float* log_alpha, const float* S_start,
+                                  void* out, float* S_end, int B, int H, int T,
+                                  cudaStream_t stream) {
+  const long long units = (long long)B * H, rows = (long long)B * T;
+  if (units <= 0) return cudaSuccess;
+  if (rows > 0x7fffffffLL || units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (T == 0) {  // an empty segment: Gamma = 1 and no outputs
+    if (!S_end) return cudaSuccess;
+    const long long n = units * kD * kD;
+    ls_add_kernel<<<(unsigned)std::min<long long>((n + 255) / 256, 4096), 256, 0, stream>>>(
+        S_end, S_start, n);
+    return cudaGetLastError();
+  }
+  static std::atomic<unsigned long long> smem_corr{0};
+  cudaError_t e = ensure_smem_cap(ls_corr_kernel, kLsSmem, smem_corr, true);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  CUtensorMap mq, mo;
+  if (!make_map(&mq, q, rows, H) || !make_map(&mo, out, rows, H)) return cudaErrorInvalidValue;
+  // the split's grid rule with each whole sequence as the one corrected segment
+  const long long slots = 2LL * sms;
+  const int cps = units <= slots ? (int)std::min<long long>(slots / units, (T + 63) / 64) : 0;
+  const unsigned grid = (unsigned)(cps > 0 ? units * cps : slots);
+  ls_corr_kernel<<<grid, kLsThreads, kLsSmem, stream>>>(mq, mo, B, H, T, 2, cps, log_alpha,
+                                                        nullptr, S_end, S_start,
+                                                        (__nv_bfloat16*)out);
+  return cudaGetLastError();
+}
+
 
 // Segments per sequence of the linear mode's split (1: no split): as many as the SMs
 // hold beside the N H units (at most kLsMaxSeg), each with at least two chunks.
@@ -1636,8 +1715,9 @@ cudaError_t launch_tc(const FwdArgs& a, cudaStream_t stream) {
       e = cudaGetLastError();
     }
     if (e == cudaSuccess) {
-      ls_corr_kernel<<<grid, kLsThreads, kLsSmem, stream>>>(mq, mo, a.N, a.H, a.T, R, cps,
-                                                            a.log_alpha, L, a.S_final);
+      ls_corr_kernel<<<grid, kLsThreads, kLsSmem, stream>>>(
+          mq, mo, a.N, a.H, a.T, R, cps, a.log_alpha, L, a.S_final, nullptr,
+          (__nv_bfloat16*)a.out);
       e = cudaGetLastError();
     }
     const cudaError_t ef = cudaFreeAsync(Lv, stream);

@@ -80,6 +80,12 @@ def load_library(path: str = LIB_PATH):
     lib.gdn_decode_step_host_workspace_bytes.restype = Z
     lib.gdn_state_fold.argtypes = [P, P, P, I, P, I, I, I, P]
     lib.gdn_state_fold.restype = I
+    lib.gdn_linear_state_correct.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
+    lib.gdn_linear_state_correct.restype = I
+    lib.gdn_linear_state_correct_supported.argtypes = [I, I, I]
+    lib.gdn_linear_state_correct_supported.restype = I
+    lib.gdn_linear_segment_map.argtypes = [P, P, I, I, I, I, P, I, P]
+    lib.gdn_linear_segment_map.restype = I
     for name in ("gdn_select_path", "gdn_launches_per_call"):
         getattr(lib, name).argtypes = [I, I, I, I]
         getattr(lib, name).restype = I
@@ -376,6 +382,49 @@ def gdn_state_fold(S_in, M, L, S_out, stream: Optional[torch.cuda.Stream] = None
     with torch.cuda.device(L.device):
         st = lib.gdn_state_fold(_ptr(S_in), _ptr(M), _ptr(L), count, _ptr(S_out), units, dv, dk,
                                 ctypes.c_void_p(s.cuda_stream))
+    _check(st)
+
+
+def gdn_linear_state_correct_supported(dk: int, dv: int, dtype: torch.dtype) -> bool:
+    return bool(load_library().gdn_linear_state_correct_supported(dk, dv, _dtype_code(dtype)))
+
+
+def gdn_linear_state_correct(q, log_alpha, S_start, out, S_end,
+                             stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name: out and S_end of a
+    linear-mode run from a zero start state become the run's results from S_start
+    (in place).  q [B, T, H, dk] bf16; log_alpha [B, T, H] fp32 or None; S_start,
+    S_end (or None) [B, H, dv, dk] fp32; out [B, T, H, dv] bf16.  Contiguous CUDA
+    tensors; returns without synchronising."""
+    lib = load_library()
+    B, T, H, dk = q.shape
+    dv = out.shape[-1]
+    for name, t in (("q", q), ("log_alpha", log_alpha), ("S_start", S_start), ("out", out),
+                    ("S_end", S_end)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"gdn_linear_state_correct: {name} must be a contiguous CUDA tensor")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = lib.gdn_linear_state_correct(_ptr(q), _ptr(log_alpha), _ptr(S_start), _ptr(out),
+                                          _ptr(S_end), B, H, T, dk, dv, _dtype_code(q.dtype),
+                                          ctypes.c_void_p(s.cuda_stream))
+    _check(st)
+
+
+def gdn_linear_segment_map(log_alpha, M, B: int, T: int, cu_seqlens=None,
+                           stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Tensor-level call of the C entry point of the same name: M [N, H, dk, dk] fp32
+    gets (product of alpha_t over each sequence) I.  log_alpha [B, T, H] fp32 or None
+    (alpha = 1); cu_seqlens int32 or None.  Returns without synchronising."""
+    lib = load_library()
+    N, H, dk = M.shape[0], M.shape[1], M.shape[-1]
+    for name, t in (("log_alpha", log_alpha), ("M", M), ("cu_seqlens", cu_seqlens)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"gdn_linear_segment_map: {name} must be a contiguous CUDA tensor")
+    s = stream if stream is not None else torch.cuda.current_stream(M.device)
+    with torch.cuda.device(M.device):
+        st = lib.gdn_linear_segment_map(_ptr(log_alpha), _ptr(M), B, H, T, dk, _ptr(cu_seqlens),
+                                        N, ctypes.c_void_p(s.cuda_stream))
     _check(st)
 
 

@@ -22,7 +22,13 @@ two phases around one exchange:
 
 Rank 0 runs one segment pass, a middle rank three (two of them independent), the
 last rank one after the exchange.  The linear mode works the same way (there
-M = (product of alpha_t) I).  Fixed-length batches split every sequence at the same
+M = (product of alpha_t) I, which the CUDA compute writes with one small kernel in place
+of the M pass), except where the compute can correct a run's results for
+its start state (``SegmentOps.correct``; in the linear mode the outputs are affine in
+the start state with a scalar gain, o_t = o_t(0) + e^{G_t} S_start q_t): there every rank
+r > 0 keeps the outputs and end state of its pass from zero and, after the exchange,
+corrects them in place instead of running its segment again, so that every rank runs
+one segment pass before the exchange and a cheap correction after it.  Fixed-length batches split every sequence at the same
 chunk-aligned bounds; packed batches (cu_seqlens) split each member at its own bounds,
 so that rank r holds a packed batch of the members' r-th segments (some of them empty:
 an empty segment's map is M = I, L = 0, which the same passes give).
@@ -85,13 +91,18 @@ class SegmentOps:
     [, cu_seqlens]) -> (out, S_final); fold(Ms, Ls) -> S after S = L_0,
     S <- S M_i + L_i for i >= 1 (Ms [count, N, H, dk, dk] and Ls [count, N, H, dv, dk]
     stacked; M_0 not read); states are state_dtype tensors.  summary(q, k, v,
-    log_alpha, beta, C, linear[, cu_seqlens]) -> (M, L), if given, replaces the two
-    forward calls of ``segment_summary``.  cu_seqlens is passed only for packed
-    batches."""
+    log_alpha, beta, C, linear[, cu_seqlens]) -> (M, L, out of the L pass), if given,
+    replaces the two forward calls of ``segment_summary``.  cu_seqlens is passed only
+    for packed batches.  correctable(q, v, cu_seqlens) -> bool and correct(q, log_alpha,
+    S_start, out, S_end), if given, are the linear mode's start-state correction: it
+    turns out and S_end of a run from a zero start state into those of the run from
+    S_start, in place, for the tensors correctable accepts."""
     forward: Callable
     fold: Callable
     state_dtype: torch.dtype = torch.float32
     summary: Optional[Callable] = None
+    correctable: Optional[Callable] = None
+    correct: Optional[Callable] = None
 
 
 _side_streams = {}
@@ -130,6 +141,14 @@ def cuda_ops() -> SegmentOps:
         N = B if cu_seqlens is None else cu_seqlens.numel() - 1
         dev = k.device
         main = torch.cuda.current_stream(dev)
+        if linear:  # M = (product of alpha_t) I: one small kernel instead of the M pass
+            out_l = torch.empty((B, T, H, dv), dtype=v.dtype, device=dev)
+            L = torch.empty((N, H, dv, dk), dtype=torch.float32, device=dev)
+            M = torch.empty((N, H, dk, dk), dtype=torch.float32, device=dev)
+            gdn.gdn_linear_chunk_fwd(q, k, v, log_alpha, None, out_l, L, C, cu_seqlens,
+                                     stream=main)
+            gdn.gdn_linear_segment_map(log_alpha, M, B, T, cu_seqlens, stream=main)
+            return M, L, out_l
         I = torch.eye(dk, dtype=torch.float32, device=dev).expand(N, H, dk, dk).contiguous()
         vz = torch.zeros((B, T, H, dk), dtype=v.dtype, device=dev)
         out_m = torch.empty((B, T, H, dk), dtype=v.dtype, device=dev)
@@ -148,9 +167,22 @@ def cuda_ops() -> SegmentOps:
                                   stream=st)
         main.wait_stream(sm)
         main.wait_stream(sl)
-        return M, L
+        return M, L, out_l
 
-    return SegmentOps(forward, fold, torch.float32, summary)
+    def correctable(q, v, cu_seqlens=None):
+        return cu_seqlens is None and gdn.gdn_linear_state_correct_supported(
+            q.shape[-1], v.shape[-1], q.dtype)
+
+    def correct(q, log_alpha, S_start, out, S_end):
+        gdn.gdn_linear_state_correct(q, log_alpha, S_start, out, S_end)
+
+    return SegmentOps(forward, fold, torch.float32, summary, correctable, correct)
+
+
+def _corrects(ops: SegmentOps, linear: bool, q, v, cu_seqlens) -> bool:
+    """Whether the ranks r > 0 correct their runs from zero instead of running again."""
+    return bool(linear and ops.correct is not None and ops.correctable is not None
+                and ops.correctable(q, v, cu_seqlens))
 
 
 def _fwd(ops: SegmentOps, q, k, v, log_alpha, beta, S0, C, linear, cu_seqlens):
@@ -160,21 +192,23 @@ def _fwd(ops: SegmentOps, q, k, v, log_alpha, beta, S0, C, linear, cu_seqlens):
 
 
 def segment_summary(q, k, v, log_alpha, beta, C: int, linear: bool, ops: SegmentOps,
-                    cu_seqlens: Optional[torch.Tensor] = None
-                    ) -> Tuple[torch.Tensor, torch.Tensor]:
+                    cu_seqlens: Optional[torch.Tensor] = None, with_out: bool = False):
     """(M, L) of one segment: L = final state from zero, M = final state of the same
-    recurrence with v = 0 and S0 = I (dv taken as dk); one pair per sequence."""
+    recurrence with v = 0 and S0 = I (dv taken as dk); one pair per sequence.  With
+    with_out, (M, L, the segment's outputs from zero)."""
     if ops.summary is not None:
         if cu_seqlens is None:
-            return ops.summary(q, k, v, log_alpha, beta, C, linear)
-        return ops.summary(q, k, v, log_alpha, beta, C, linear, cu_seqlens)
+            M, L, out = ops.summary(q, k, v, log_alpha, beta, C, linear)
+        else:
+            M, L, out = ops.summary(q, k, v, log_alpha, beta, C, linear, cu_seqlens)
+        return (M, L, out) if with_out else (M, L)
     B, T, H, dk = k.shape
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     I = torch.eye(dk, dtype=ops.state_dtype, device=k.device).expand(N, H, dk, dk).contiguous()
     vz = torch.zeros((B, T, H, dk), dtype=v.dtype, device=v.device)
-    _, L = _fwd(ops, q, k, v, log_alpha, beta, None, C, linear, cu_seqlens)
+    out, L = _fwd(ops, q, k, v, log_alpha, beta, None, C, linear, cu_seqlens)
     _, M = _fwd(ops, q, k, vz, log_alpha, beta, I, C, linear, cu_seqlens)
-    return M, L
+    return (M, L, out) if with_out else (M, L)
 
 
 def fold(Ms: torch.Tensor, Ls: torch.Tensor, r: int, ops: SegmentOps):
@@ -187,7 +221,9 @@ def fold(Ms: torch.Tensor, Ls: torch.Tensor, r: int, ops: SegmentOps):
 def phase1(rank: int, world: int, q, k, v, log_alpha, beta, S0, C: int, linear: bool,
            ops: SegmentOps, cu_seqlens: Optional[torch.Tensor] = None):
     """What a rank computes before the exchange.  Returns (M, L, result) where
-    (M, L) is its contribution and result = (out, S_final) for rank 0, else None."""
+    (M, L) is its contribution and result = (out, S_final) for rank 0; for a rank r > 0
+    that corrects its run afterwards (see ``SegmentOps.correct``), its outputs and end
+    state from a zero start; else None."""
     B, T, H, dk = k.shape
     dv = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
@@ -196,10 +232,17 @@ def phase1(rank: int, world: int, q, k, v, log_alpha, beta, S0, C: int, linear: 
         out, Sf = _fwd(ops, q, k, v, log_alpha, beta, S0, C, linear, cu_seqlens)
         M = torch.zeros((N, H, dk, dk), dtype=ops.state_dtype, device=dev)  # not read
         return M, Sf, (out, Sf)
+    corrects = _corrects(ops, linear, q, v, cu_seqlens)
     if rank == world - 1:  # nobody needs the last segment's map
         zM = torch.zeros((N, H, dk, dk), dtype=ops.state_dtype, device=dev)
         zL = torch.zeros((N, H, dv, dk), dtype=ops.state_dtype, device=dev)
+        if corrects:  # its run from zero, corrected after the exchange
+            return zM, zL, _fwd(ops, q, k, v, log_alpha, beta, None, C, linear, cu_seqlens)
         return zM, zL, None
+    if corrects:
+        M, L, out = segment_summary(q, k, v, log_alpha, beta, C, linear, ops, cu_seqlens,
+                                    with_out=True)
+        return M, L, (out, L.clone())  # L goes out in the exchange; the copy is corrected
     M, L = segment_summary(q, k, v, log_alpha, beta, C, linear, ops, cu_seqlens)
     return M, L, None
 
@@ -208,10 +251,15 @@ def phase2(rank: int, q, k, v, log_alpha, beta, C: int, linear: bool, ops: Segme
            Ms: torch.Tensor, Ls: torch.Tensor, result,
            cu_seqlens: Optional[torch.Tensor] = None):
     """What a rank computes after the exchange: its segment from the folded start
-    state (rank 0 already has its result).  Ms, Ls stack every rank's summary."""
+    state (rank 0 already has its result), or, where phase 1 kept the run from zero,
+    that run corrected for the start state.  Ms, Ls stack every rank's summary."""
     if rank == 0:
         return result
     S_start = fold(Ms, Ls, rank, ops)
+    if result is not None and _corrects(ops, linear, q, v, cu_seqlens):
+        out, S_end = result
+        ops.correct(q, log_alpha, S_start, out, S_end)
+        return out, S_end
     return _fwd(ops, q, k, v, log_alpha, beta, S_start, C, linear, cu_seqlens)
 
 

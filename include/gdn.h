@@ -377,6 +377,47 @@ int gdn_launches_per_call(int dk, int dv, int C, int qkv_dtype);
 int gdn_linear_split_segments(int N, int H, int T, int dk, int dv, int C, int qkv_dtype);
 
 /*
+ * gdn_linear_state_correct -- the linear mode's start-state correction.  In the linear
+ * mode (gdn_linear_chunk_fwd) the outputs and the end state of a run are affine in its
+ * start state with a scalar gain (Nyysyyan, "Mamba2": the state is the decayed sum of the
+ * writes):
+ *
+ *     o_t   = o_t(from zero) + e^{G_t} S_start q_t,   G_t = sum of log alpha over 0..t
+ *     S_end = Gamma S_start + S_end(from zero),       Gamma = e^{G_{T-1}}
+ *
+ * Given out and S_end of a gdn_linear_chunk_fwd run of B fixed-length sequences from a
+ * zero start state (S0 NULL), this call adds the contribution of S_start in place, so
+ * that they become the run's results from S_start.  A sequence-parallel rank uses it to
+ * finish its segment once the exchange has given it the start state.
+ *   q [B, T, H, dk] bf16, log_alpha [B, T, H] fp32 or NULL (alpha = 1): as passed to the
+ *   run; S_start [B, H, dv, dk] fp32; out [B, T, H, dv] bf16, read and written;
+ *   S_end [B, H, dv, dk] fp32, read and written, or NULL (not updated).  T = 0 gives
+ *   S_end += S_start.  Device pointers, 16-byte aligned, asynchronous on `stream`.
+ * Only bf16 with dk = dv = 128 (gdn_linear_state_correct_supported), fixed-length
+ * batches; anything else returns GDN_EINVAL before any launch.  The product with
+ * S_start runs on the tensor cores with S_start as two bf16 terms; the sums are fp32; out
+ * is rounded to bf16 once more.
+ */
+int gdn_linear_state_correct(const void* q, const float* log_alpha, const float* S_start,
+                             void* out, float* S_end, int B, int H, int T, int dk, int dv,
+                             int qkv_dtype, void* stream);
+/* 1 when gdn_linear_state_correct takes these sizes and dtype, else 0. */
+int gdn_linear_state_correct_supported(int dk, int dv, int qkv_dtype);
+
+/*
+ * gdn_linear_segment_map -- the linear mode's state map over each sequence: with no erase
+ * the state is the decayed sum of the writes (Nyysyyan, "Mamba2"), so the M of
+ * S_end = S_start M + L is (product of alpha_t) I.  Writes M[n][h] = e^{sum of log alpha
+ * over sequence n} I for every sequence and head, the M that gdn_state_fold takes.
+ *   log_alpha [B, T, H] fp32 or NULL (alpha = 1: M = I); M [N, H, dk, dk] fp32, written;
+ *   cu_seqlens as for gdn_chunk_fwd (B = 1, N = N_seqs members, clamped to [0, T]) or
+ *   NULL (N = B).  Device pointers, 16-byte aligned, asynchronous on `stream`; one
+ *   launch.  Errors: GDN_EINVAL for bad sizes or pointers, before any launch.
+ */
+int gdn_linear_segment_map(const float* log_alpha, float* M, int B, int H, int T, int dk,
+                           const int32_t* cu_seqlens, int N_seqs, void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the device status word that kernels
  * set when a bounded wait (mbarrier, async copy) gives up.  Returns GDN_OK or
  * GDN_ETIMEOUT (message names the wait), or GDN_ECUDA if the stream failed.

@@ -69,6 +69,27 @@ def _oracle_fold(Ms, Ls):
 ORACLE_OPS = seqpar.SegmentOps(_oracle_forward, _oracle_fold, torch.float64)
 
 
+def _oracle_correct(q, la, S_start, out, S_end):
+    """The linear mode's start-state correction from its formula, fp64, in place:
+    o_t += e^{G_t} S_start q_t (G_t = sum of log alpha through t), S_end += e^{G_last}
+    S_start ([N] Mamba2: the state is the decayed sum of the writes)."""
+    B, T, H, _ = q.shape
+    for b in range(B):
+        for h in range(H):
+            G = np.cumsum(la[b, :, h].double().numpy()) if la is not None else np.zeros(T)
+            Ss = S_start[b, h].double().numpy()
+            out[b, :, h] += torch.from_numpy(np.exp(G)[:, None] * (q[b, :, h].double().numpy()
+                                                                  @ Ss.T))
+            if S_end is not None:
+                S_end[b, h] += torch.from_numpy(np.exp(G[-1] if T else 0.0) * Ss)
+
+
+# the same compute with the linear mode's correction (fixed-length batches)
+CORRECTING_OPS = seqpar.SegmentOps(_oracle_forward, _oracle_fold, torch.float64,
+                                   correctable=lambda q, v, cu=None: cu is None,
+                                   correct=_oracle_correct)
+
+
 # ------------------------------------------------------ the affine property --
 
 @pytest.mark.parametrize("linear", [False, True])
@@ -113,9 +134,13 @@ def test_segment_bounds(T, world, C):
 
 @pytest.mark.parametrize("world", [1, 2, 3, 5])
 @pytest.mark.parametrize("linear", [False, True])
-def test_emulated_split_matches_unsplit(world, linear):
+@pytest.mark.parametrize("ops", ["plain", "correcting"])
+def test_emulated_split_matches_unsplit(world, linear, ops):
+    """Every rank in turn; in the linear mode with a correcting compute the ranks r > 0
+    keep their runs from zero and correct them after the exchange."""
     q, k, v, la, beta, S0 = _inputs(seed=world)
-    out, Sf = seqpar.emulate(q, k, v, la, beta, S0, 16, world, linear, ORACLE_OPS)
+    o = ORACLE_OPS if ops == "plain" else CORRECTING_OPS
+    out, Sf = seqpar.emulate(q, k, v, la, beta, S0, 16, world, linear, o)
     ref_o, ref_S = _oracle_forward(q, k, v, la, beta, S0, 16, linear)
     assert torch.allclose(out, ref_o, rtol=1e-10, atol=1e-12)
     assert torch.allclose(Sf, ref_S, rtol=1e-10, atol=1e-12)
@@ -163,7 +188,7 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, linear, queue):
+def _rank_main(rank, world, port, linear, queue, correcting=False):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
@@ -174,7 +199,7 @@ def _rank_main(rank, world, port, linear, queue):
     bnd = sp.segment_bounds(q.shape[1], world, 16)[rank]
     seg = [sp.segment(t, bnd) for t in (q, k, v, la, beta)]
     out, Sf = sp.seqpar_chunk_fwd(*seg, S0 if rank == 0 else None, 16, linear=linear,
-                                  ops=me.ORACLE_OPS)
+                                  ops=me.CORRECTING_OPS if correcting else me.ORACLE_OPS)
     queue.put((rank, bnd, out.numpy(), Sf.numpy()))
     dist.barrier()
     dist.destroy_process_group()
@@ -219,12 +244,14 @@ def test_gloo_ranks_packed_match_unsplit(world):
     assert np.allclose(res[-1][3], ref_S.numpy(), rtol=1e-10, atol=1e-12)
 
 
-@pytest.mark.parametrize("world,linear", [(2, False), (3, False), (3, True)])
-def test_gloo_ranks_match_unsplit(world, linear):
+@pytest.mark.parametrize("world,linear,correcting", [(2, False, False), (3, False, False),
+                                                    (3, True, False), (2, True, True),
+                                                    (3, True, True)])
+def test_gloo_ranks_match_unsplit(world, linear, correcting):
     ctx = mp.get_context("spawn")
     queue = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, world, port, linear, queue))
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, linear, queue, correcting))
              for r in range(world)]
     for p in procs:
         p.start()
@@ -238,3 +265,33 @@ def test_gloo_ranks_match_unsplit(world, linear):
     assert np.allclose(got_o, ref_o.numpy(), rtol=1e-10, atol=1e-12)
     assert np.allclose(res[-1][3], ref_S.numpy(), rtol=1e-10, atol=1e-12)
     assert [r[1] for r in res] == seqpar.segment_bounds(q.shape[1], world, 16)
+
+
+def test_correcting_ranks_run_their_segment_once():
+    """With the linear mode's correction, a rank r > 0 runs its segment once from zero
+    (a middle rank's M pass beside it) before the exchange and no pass after it."""
+    q, k, v, la, beta, S0 = _inputs(seed=3)
+    calls = []
+
+    def counting_forward(*a, **kw):
+        calls.append(a[5] is None)  # S0 argument: None = from zero
+        return _oracle_forward(*a, **kw)
+
+    ops = seqpar.SegmentOps(counting_forward, _oracle_fold, torch.float64,
+                            correctable=lambda q, v, cu=None: cu is None,
+                            correct=_oracle_correct)
+    world = 4
+    bounds = seqpar.segment_bounds(q.shape[1], world, 16)
+    segs = [[seqpar.segment(t, b) for t in (q, k, v, la, beta)] for b in bounds]
+    first = [seqpar.phase1(r, world, *segs[r], S0, 16, True, ops) for r in range(world)]
+    n1 = len(calls)
+    assert n1 == 1 + 2 * (world - 2) + 1  # rank 0; (L, M) per middle rank; the last rank
+    Ms = torch.stack([m for m, _, _ in first])
+    Ls = torch.stack([l for _, l, _ in first])
+    outs = [seqpar.phase2(r, *segs[r], 16, True, ops, Ms, Ls, first[r][2])
+            for r in range(world)]
+    assert len(calls) == n1  # no pass after the exchange
+    ref_o, ref_S = _oracle_forward(q, k, v, la, beta, S0, 16, True)
+    assert torch.allclose(torch.cat([o for o, _ in outs], dim=1), ref_o, rtol=1e-10,
+                          atol=1e-12)
+    assert torch.allclose(outs[-1][1], ref_S, rtol=1e-10, atol=1e-12)

@@ -133,3 +133,102 @@ def test_split_packed(name, world):
     fp32 = inp["dtype"] == "f32"
     assert_close(o, ro, fp32, "out", stored_bf16=not fp32)
     assert_close(s, rs, fp32, "S_final")
+
+
+@pytest.mark.parametrize("alpha_one", [False, True], ids=["mamba2", "linear_attention"])
+@pytest.mark.parametrize("B,H,T", [(2, 3, 333), (1, 1, 64), (4, 16, 200)])
+def test_linear_state_correct_equals_the_run_from_S_start(B, H, T, alpha_one):
+    """A linear-mode run from zero, then gdn_linear_state_correct with S_start, against
+    the oracle's run from S_start (outputs and end state)."""
+    w = W["linear_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(w, B=B, H=H, T=T, seed=B * T + H)
+    if alpha_one:
+        inp["log_alpha"] = torch.zeros_like(inp["log_alpha"])
+    S_start = torch.randn(B, H, 128, 128, generator=torch.Generator().manual_seed(T)) * 0.1
+    d = to_device(inp)
+    la = None if alpha_one else d["log_alpha"]
+    out, S_end = gdn.linear_chunk_fwd(d["q"], d["k"], d["v"], la, None, None, C=64)
+    gdn.gdn_linear_state_correct(d["q"], la, S_start.cuda(), out, S_end)
+    gdn.gdn_check_status()
+    torch.cuda.synchronize()
+    ref = dict(inp, S0=S_start)
+    ro, rs = _oracle(ref, True)
+    assert_close(out.float().cpu().numpy().astype(np.float64), ro, False, "out",
+                 stored_bf16=True)
+    assert_close(S_end.cpu().numpy().astype(np.float64), rs, False, "S_final")
+
+
+def test_linear_state_correct_edge_cases():
+    """T = 0 adds S_start to S_end (no outputs); S_end = None corrects the outputs only;
+    unsupported sizes are refused before any launch."""
+    S_start = torch.randn(2, 2, 128, 128, device="cuda")
+    S_end = torch.randn(2, 2, 128, 128, device="cuda")
+    q0 = torch.empty(2, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    o0 = torch.empty(2, 0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    expect = S_end + S_start
+    gdn.gdn_linear_state_correct(q0, None, S_start, o0, S_end)
+    torch.cuda.synchronize()
+    assert torch.equal(S_end, expect)
+    w = W["linear_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(w, B=1, H=2, T=130, seed=5)
+    d = to_device(inp)
+    out, _ = gdn.linear_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], None, None, C=64,
+                                  output_final_state=False)
+    gdn.gdn_linear_state_correct(d["q"], d["log_alpha"], S_start[:1].contiguous(), out, None)
+    torch.cuda.synchronize()
+    ro, _ = _oracle(dict(inp, S0=S_start[:1].cpu()), True)
+    assert_close(out.float().cpu().numpy().astype(np.float64), ro, False, "out",
+                 stored_bf16=True)
+    assert not gdn.gdn_linear_state_correct_supported(64, 64, torch.bfloat16)
+    assert not gdn.gdn_linear_state_correct_supported(128, 128, torch.float32)
+    qf = torch.zeros(1, 4, 2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_linear_state_correct(qf, None, torch.zeros(1, 2, 64, 64, device="cuda"),
+                                     torch.zeros_like(qf), None)
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_linear_split_corrects_instead_of_rerunning(world):
+    """The bf16 d = 128 linear mode: ranks r > 0 correct their runs from zero (checked
+    against the oracle; the correcting path is the one the CUDA ops choose here)."""
+    inp = workloads.make_inputs(W["linear_bf16_b4h16t4096d128c64"], B=2, H=2, T=900,
+                                seed=world + 40)
+    inp["S0"] = torch.randn(2, 2, 128, 128, generator=torch.Generator().manual_seed(world)) * 0.1
+    d = to_device(inp)
+    assert seqpar.cuda_ops().correctable(d["q"], d["v"], None)
+    o, s = _split(inp, 64, world, True)
+    ro, rs = _oracle(inp, True)
+    assert_close(o, ro, False, "out", stored_bf16=True)
+    assert_close(s, rs, False, "S_final")
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_linear_segment_map_is_the_gain_times_identity(packed):
+    """M[n][h] = e^{sum of log alpha over the sequence} I, fixed-length and packed (an
+    empty member gives I, a reset anywhere gives 0), against fp64 sums."""
+    g = torch.Generator().manual_seed(3)
+    if packed:
+        lens = [0, 5, 64, 130, 1]
+        T, B, N = sum(lens), 1, len(lens)
+        cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    else:
+        T, B, N, cu = 300, 2, 2, None
+    H, dk = 3, 64
+    la = -torch.nn.functional.softplus(-(torch.randn(B, T, H, generator=g) + 4.0)) * 0.05
+    la[0, 7, 1] = -float("inf")
+    M = torch.empty(N, H, dk, dk, device="cuda")
+    gdn.gdn_linear_segment_map(la.cuda(), M, B, T, None if cu is None else cu.cuda())
+    torch.cuda.synchronize()
+    spans = [(n, 0, n * T, (n + 1) * T) for n in range(B)] if cu is None else \
+        [(n, 0, int(cu[n]), int(cu[n + 1])) for n in range(N)]
+    for n, _, a, b in spans:
+        for h in range(H):
+            flat = la.reshape(-1, H)[a:b, h].double()
+            gam = float(torch.exp(flat.sum())) if b > a else 1.0
+            ref = gam * np.eye(dk)
+            got = M[n, h].double().cpu().numpy()
+            assert np.abs(got - ref).max() <= 1e-5 * max(gam, 1e-30) + 1e-30, (n, h, gam)
+    M1 = torch.empty(N, H, dk, dk, device="cuda")
+    gdn.gdn_linear_segment_map(None, M1, B, T, None if cu is None else cu.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(M1, torch.eye(dk, device="cuda").expand(N, H, dk, dk))

@@ -74,6 +74,10 @@ WORKLOADS = {
     "linear_bf16_b4h16t4096d128c64": Workload(
         "linear_bf16_b4h16t4096d128c64", "bf16", B=4, H=16, T=4096, dk=128, dv=128, C=64,
         alpha_mu=2.0, s0_std=0.0, linear=True),
+    # the long-sequence sizes in the linear mode (32 units: each sequence split over SMs)
+    "linear_bf16_b1h32t32768d128c64": Workload(
+        "linear_bf16_b1h32t32768d128c64", "bf16", B=1, H=32, T=32768, dk=128, dv=128, C=64,
+        alpha_mu=3.0, s0_std=0.1, linear=True),
 }
 
 # The headline workload that bench.py times by default.
