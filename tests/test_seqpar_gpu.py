@@ -232,3 +232,32 @@ def test_linear_segment_map_is_the_gain_times_identity(packed):
     gdn.gdn_linear_segment_map(None, M1, B, T, None if cu is None else cu.cuda())
     torch.cuda.synchronize()
     assert torch.equal(M1, torch.eye(dk, device="cuda").expand(N, H, dk, dk))
+
+
+@pytest.mark.parametrize("name", ["gdn_f32_b2h4t1024d64c64", "linear_bf16_b4h16t4096d128c64"])
+@pytest.mark.parametrize("world", [2, 3])
+def test_split_packed_linear_mode(name, world):
+    """The linear mode on a packed batch: each member cut at its own bounds; the middle
+    ranks' maps M = (prod alpha) I come from gdn_linear_segment_map with the ranks'
+    cu_seqlens, the ranks run their segments again from the folded start states."""
+    w = W[name]
+    lens = [5, 0, 70, 130, 1, 200]
+    inp = workloads.make_inputs(w, B=1, H=2, T=sum(lens), seed=world + 7)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    inp["cu_seqlens"] = cu
+    inp["N"] = len(lens)
+    inp["S0"] = 0.1 * torch.randn(len(lens), 2, w.dv, w.dk,
+                                  generator=torch.Generator().manual_seed(world + 7))
+    d = to_device(inp)
+    out, Sf = seqpar.emulate(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], 64,
+                             world, True, cu_seqlens=d["cu_seqlens"])
+    gdn.gdn_check_status()
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy().astype(np.float64)
+    s = Sf.cpu().numpy().astype(np.float64)
+    z = torch.zeros_like(inp["log_alpha"])
+    ro, rs = native.gdn_forward_c(inp["q"], inp["k"], inp["v"], inp["log_alpha"], z, inp["S0"],
+                                  inp["cu_seqlens"], erase=z, write=torch.ones_like(z))
+    fp32 = inp["dtype"] == "f32"
+    assert_close(o, ro, fp32, "out", stored_bf16=not fp32)
+    assert_close(s, rs, fp32, "S_final")
