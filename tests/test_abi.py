@@ -322,3 +322,53 @@ def test_bwd_path_rejected_before_launch(lib, path, over, word):
     assert _call_bwd(lib, path, **over) == binding.GDN_EINVAL
     msg = lib.gdn_last_error().decode()
     assert word in msg, msg
+
+
+def _call_correct(lib, **over):
+    """Call gdn_linear_state_correct with fake (never dereferenced) aligned pointers."""
+    a = dict(q=4096, la=8192, Ss=12288, out=16384, Se=20480, B=2, H=4, T=128, dk=128, dv=128,
+             dt=gdn.GDN_BF16, stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_linear_state_correct(P(a["q"]), P(a["la"]), P(a["Ss"]), P(a["out"]),
+                                        P(a["Se"]), a["B"], a["H"], a["T"], a["dk"], a["dv"],
+                                        a["dt"], P(a["stream"]))
+
+
+@pytest.mark.parametrize("over,code,word", [
+    (dict(dk=64, dv=64), binding.GDN_EINVAL, "dk = dv = 128"),
+    (dict(dt=gdn.GDN_F32), binding.GDN_EINVAL, "bf16"),
+    (dict(dt=7), binding.GDN_EDTYPE, "qkv_dtype"),
+    (dict(B=0), binding.GDN_EINVAL, "B, H > 0"),
+    (dict(T=-1), binding.GDN_EINVAL, "T >= 0"),
+    (dict(Ss=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(q=None), binding.GDN_EINVAL, "non-NULL"),
+    (dict(out=16388), binding.GDN_EINVAL, "out is not 16-byte aligned"),
+])
+def test_linear_state_correct_rejects_before_launch(lib, over, code, word):
+    assert _call_correct(lib, **over) == code
+    assert word in lib.gdn_last_error().decode()
+
+
+def test_linear_state_correct_support_query(lib):
+    assert lib.gdn_linear_state_correct_supported(128, 128, gdn.GDN_BF16) == 1
+    assert lib.gdn_linear_state_correct_supported(64, 64, gdn.GDN_BF16) == 0
+    assert lib.gdn_linear_state_correct_supported(128, 128, gdn.GDN_F32) == 0
+
+
+@pytest.mark.parametrize("over,word", [
+    (dict(B=0), "B, H > 0"),
+    (dict(dk=48), "dk in"),
+    (dict(M=None), "M must be non-NULL"),
+    (dict(M=4100), "16-byte aligned"),
+    (dict(cu=28672, N=0, B=1), "N_seqs > 0"),
+    (dict(cu=28672, N=3, B=2), "B = 1"),
+])
+def test_linear_segment_map_rejects_before_launch(lib, over, word):
+    a = dict(la=8192, M=4096, B=2, H=4, T=128, dk=128, cu=None, N=2, stream=None)
+    a.update(over)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    st = lib.gdn_linear_segment_map(P(a["la"]), P(a["M"]), a["B"], a["H"], a["T"], a["dk"],
+                                    P(a["cu"]), a["N"], P(a["stream"]))
+    assert st == binding.GDN_EINVAL
+    assert word in lib.gdn_last_error().decode()
