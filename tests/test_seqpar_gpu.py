@@ -261,3 +261,21 @@ def test_split_packed_linear_mode(name, world):
     fp32 = inp["dtype"] == "f32"
     assert_close(o, ro, fp32, "out", stored_bf16=not fp32)
     assert_close(s, rs, fp32, "S_final")
+
+
+def test_linear_state_correct_many_units():
+    """More (sequence, head) units than two CTAs an SM hold (B = 20, H = 16: 320): each
+    correction CTA takes a run of whole sequences, folds a start state per sequence and
+    writes each one's S_final; ragged last tiles (T = 100)."""
+    w = W["linear_bf16_b4h16t4096d128c64"]
+    inp = workloads.make_inputs(w, B=20, H=16, T=100, seed=61)
+    S_start = torch.randn(20, 16, 128, 128, generator=torch.Generator().manual_seed(62)) * 0.1
+    d = to_device(inp)
+    out, S_end = gdn.linear_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], None, None, C=64)
+    gdn.gdn_linear_state_correct(d["q"], d["log_alpha"], S_start.cuda(), out, S_end)
+    gdn.gdn_check_status()
+    torch.cuda.synchronize()
+    ro, rs = _oracle(dict(inp, S0=S_start), True)
+    assert_close(out.float().cpu().numpy().astype(np.float64), ro, False, "out",
+                 stored_bf16=True)
+    assert_close(S_end.cpu().numpy().astype(np.float64), rs, False, "S_final")
