@@ -389,6 +389,38 @@ def gdn_linear_state_correct_supported(dk: int, dv: int, dtype: torch.dtype) -> 
     return bool(load_library().gdn_linear_state_correct_supported(dk, dv, _dtype_code(dtype)))
 
 
+def _correct_shapes(q, log_alpha, S_start, out, S_end) -> None:
+    """gdn_linear_state_correct's shapes and dtypes (the C entry point sees only
+    pointers): out like q's dtype [B, T, H, dv]; S_start, S_end fp32 [B, H, dv, dk];
+    log_alpha fp32 [B, T, H]."""
+    B, T, H, dk = q.shape
+    dv = out.shape[-1]
+    want = {"out": (out, (B, T, H, dv), q.dtype),
+            "S_start": (S_start, (B, H, dv, dk), torch.float32),
+            "log_alpha": (log_alpha, (B, T, H), torch.float32),
+            "S_end": (S_end, (B, H, dv, dk), torch.float32)}
+    for name, (t, shape, dt) in want.items():
+        if t is not None and (tuple(t.shape) != shape or t.dtype != dt):
+            raise ValueError(f"gdn_linear_state_correct: {name} must be {dt} of shape {shape}, "
+                             f"got {t.dtype} {tuple(t.shape)}")
+
+
+def _segment_map_shapes(log_alpha, M, B: int, T: int, cu_seqlens) -> None:
+    """gdn_linear_segment_map's shapes and dtypes (the C entry point sees only pointers)."""
+    if M.dim() != 4 or M.shape[2] != M.shape[3] or M.dtype != torch.float32:
+        raise ValueError("gdn_linear_segment_map: M must be fp32 [N, H, dk, dk]")
+    N, H = M.shape[0], M.shape[1]
+    if log_alpha is not None and (tuple(log_alpha.shape) != (B, T, H) or
+                                  log_alpha.dtype != torch.float32):
+        raise ValueError(f"gdn_linear_segment_map: log_alpha must be fp32 of shape {(B, T, H)}")
+    if cu_seqlens is None and N != B:
+        raise ValueError("gdn_linear_segment_map: M must hold one map per sequence (N = B)")
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or
+                                   cu_seqlens.numel() != N + 1 or B != 1):
+        raise ValueError("gdn_linear_segment_map: cu_seqlens must be int32 with N + 1 "
+                         "entries (B = 1)")
+
+
 def gdn_linear_state_correct(q, log_alpha, S_start, out, S_end,
                              stream: Optional[torch.cuda.Stream] = None) -> None:
     """Tensor-level call of the C entry point of the same name: out and S_end of a
@@ -403,6 +435,7 @@ def gdn_linear_state_correct(q, log_alpha, S_start, out, S_end,
                     ("S_end", S_end)):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"gdn_linear_state_correct: {name} must be a contiguous CUDA tensor")
+    _correct_shapes(q, log_alpha, S_start, out, S_end)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
         st = lib.gdn_linear_state_correct(_ptr(q), _ptr(log_alpha), _ptr(S_start), _ptr(out),
@@ -421,6 +454,7 @@ def gdn_linear_segment_map(log_alpha, M, B: int, T: int, cu_seqlens=None,
     for name, t in (("log_alpha", log_alpha), ("M", M), ("cu_seqlens", cu_seqlens)):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"gdn_linear_segment_map: {name} must be a contiguous CUDA tensor")
+    _segment_map_shapes(log_alpha, M, B, T, cu_seqlens)
     s = stream if stream is not None else torch.cuda.current_stream(M.device)
     with torch.cuda.device(M.device):
         st = lib.gdn_linear_segment_map(_ptr(log_alpha), _ptr(M), B, H, T, dk, _ptr(cu_seqlens),

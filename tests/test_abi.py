@@ -372,3 +372,35 @@ def test_linear_segment_map_rejects_before_launch(lib, over, word):
                                     P(a["cu"]), a["N"], P(a["stream"]))
     assert st == binding.GDN_EINVAL
     assert word in lib.gdn_last_error().decode()
+
+
+def test_linear_correct_binding_checks_shapes_and_dtypes():
+    """The bindings of the two linear-mode entry points refuse tensors whose shape or dtype
+    the pointers cannot carry (checked on CPU tensors, before any device is touched)."""
+    bf, f = torch.bfloat16, torch.float32
+    q = torch.zeros(2, 8, 3, 128, dtype=bf)
+    ok = dict(q=q, log_alpha=torch.zeros(2, 8, 3), S_start=torch.zeros(2, 3, 128, 128),
+              out=torch.zeros(2, 8, 3, 128, dtype=bf), S_end=torch.zeros(2, 3, 128, 128))
+    binding._correct_shapes(**ok)
+    binding._correct_shapes(**dict(ok, log_alpha=None, S_end=None))
+    for bad in (dict(S_start=torch.zeros(2, 3, 128, 128, dtype=bf)),
+                dict(S_start=torch.zeros(1, 3, 128, 128)),
+                dict(S_end=torch.zeros(2, 3, 128, 64)),
+                dict(out=torch.zeros(2, 8, 3, 128, dtype=f)),
+                dict(log_alpha=torch.zeros(2, 8, 4))):
+        with pytest.raises(ValueError):
+            binding._correct_shapes(**dict(ok, **bad))
+    M = torch.zeros(2, 3, 64, 64)
+    binding._segment_map_shapes(torch.zeros(2, 8, 3), M, 2, 8, None)
+    binding._segment_map_shapes(None, M, 2, 8, None)
+    binding._segment_map_shapes(torch.zeros(1, 8, 3), M, 1, 8, torch.tensor([0, 3, 8],
+                                                                              dtype=torch.int32))
+    for args in ((torch.zeros(2, 8, 3), torch.zeros(2, 3, 64, 32), 2, 8, None),
+                 (torch.zeros(2, 8, 3), M.double(), 2, 8, None),
+                 (torch.zeros(2, 9, 3), M, 2, 8, None),
+                 (torch.zeros(2, 8, 3), torch.zeros(2, 4, 64, 64), 2, 8, None),
+                 (None, M, 3, 8, None),
+                 (None, M, 1, 8, torch.tensor([0, 8], dtype=torch.int32)),
+                 (None, M, 1, 8, torch.tensor([0, 3, 8], dtype=torch.int64))):
+        with pytest.raises(ValueError):
+            binding._segment_map_shapes(*args)
